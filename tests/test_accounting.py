@@ -1,0 +1,62 @@
+"""Host accounting of algorithmic bytes/FLOPs pinned to the figures the pages print."""
+
+import os
+
+import pytest
+
+from indexer_driven_sparse_gb300 import accounting as A
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_figures.txt")
+MiB = 1 << 20
+GiB = 1 << 30
+KiB = 1 << 10
+
+
+def figs():
+    vals = {}
+    with open(GOLDEN, encoding="utf-8") as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = line.split()
+                vals[k] = float(v)
+    return vals
+
+
+def test_page_byte_figures():
+    f = figs()
+    assert A.kv_read_bytes(2048) == f["kv_bytes_per_layer"] == 4 * MiB
+    assert 12 * A.kv_read_bytes(2048) == f["kv_bytes_per_step_12_layers"] == 48 * MiB
+    assert A.pooled_scan_bytes(250_000) == f["pooled_bytes_per_layer_250000"]
+    assert round(12 * A.pooled_scan_bytes(250_000) / MiB) == f["pooled_mib_per_step_12_layers"]
+    vram, ram = A.per_token_memory(12)
+    assert vram / KiB == f["vram_kib_per_token"]
+    assert ram / KiB == f["ram_kib_per_token"]
+    assert (vram + ram) / KiB == f["all_vram_kib_per_token"]
+    # 204 GiB per naive 4096-token chunk: the padded selection is 2176 = 17 x 128 tokens
+    assert round(A.naive_prefill_kv_bytes(4096, 2176, 12) / GiB) == f["naive_prefill_gib_per_chunk"]
+    assert round(A.naive_prefill_kv_bytes(4096, 2048, 12) / GiB) != f["naive_prefill_gib_per_chunk"]
+
+
+def test_attended_and_threshold():
+    f = figs()
+    assert max(p for p in range(5000) if A.visible_blocks(p) <= 512) == f["dense_limit_tokens"]
+    for p in [2052, 2053, 2054, 2055, 1048320, 262144 + 17]:
+        assert A.attended(p) == f["selected_tokens"] + p % 4 + 1
+    for p in [0, 1, 3, 4, 2051]:
+        assert A.attended(p) == p + 1
+
+
+def test_workload_totals():
+    # tiny decode: p = 4096, 8 query heads
+    assert A.decode_layer_step_bytes([4096], 8) == 4_466_944
+    # long decode: p = 131072, 16 query heads
+    assert A.decode_layer_step_bytes([131072], 16) == 12_601_600
+    # million-token decode
+    assert A.decode_layer_step_bytes([1048320], 16) == 71_305_472
+    assert A.pooled_scan_bytes(A.visible_blocks(1048320)) == 67_092_480
+    # prefill chunk: 4096 queries at 262144 + i
+    assert A.prefill_attention_flops(262144, 4096) == 8_398_848 * 16 * 1024
+    assert A.prefill_score_flops(262144, 4096) == 256 * 270_530_560
+    assert A.prefill_attention_flops(262144, 4096) / 1e9 == pytest.approx(137.6, abs=0.05)
+    assert A.prefill_score_flops(262144, 4096) / 1e9 == pytest.approx(69.26, abs=0.01)

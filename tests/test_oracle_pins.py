@@ -1,0 +1,346 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test fixes part of the oracle by a closed form, a hand-solved example,
+brute force on tiny inputs, a library routine (torch's fp32->bf16 rounding,
+torch's scaled_dot_product_attention, scipy's logsumexp, Python's sorted) or a
+figure the pages print. A dropped term, a wrong sign or index, or a transposed
+operand in the oracle fails at least one of them.
+"""
+
+import ast
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits_of(x_f32):
+    return torch.tensor(np.asarray(x_f32, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def to_bits(a):
+    """Exact bf16 values -> bits (asserting exactness)."""
+    a = np.asarray(a, dtype=np.float64)
+    bits = O.f64_to_bf16_bits(a)
+    assert np.array_equal(O.bf16_bits_to_f64(bits), a), "value not exactly representable in bf16"
+    return bits
+
+
+# ----------------------------------------------------------------------------- bf16 rounding
+
+def test_rne_matches_torch_on_fp32_values():
+    # torch rounds fp32 -> bf16 to nearest-even; on fp32-exact inputs the oracle must agree.
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.standard_normal(200000).astype(np.float32),
+        (rng.standard_normal(20000) * 1e-38).astype(np.float32),   # fp32 subnormal range
+        (rng.standard_normal(20000) * 1e30).astype(np.float32),
+        # exact ties: bf16 value + half a bf16 ulp
+        (np.float32(1.0) + np.float32(2.0 ** -8) * np.arange(1, 64, 2, dtype=np.float32)),
+    ])
+    assert np.array_equal(O.f64_to_bf16_bits(x.astype(np.float64)), bf16_bits_of(x))
+
+
+def test_rne_hand_cases():
+    cases = {
+        1.0 + 2.0 ** -8: 0x3F80,                 # tie, even neighbour 1.0
+        1.0 + 3 * 2.0 ** -8: 0x3F82,             # tie, even neighbour 1 + 2^-6
+        1.0 + 2.0 ** -8 + 2.0 ** -40: 0x3F81,    # just above the tie: a detour via fp32 would give 0x3F80
+        -(1.0 + 2.0 ** -8 + 2.0 ** -40): 0xBF81,
+        2.0 ** -133: 0x0001,                     # smallest bf16 subnormal
+        1.5 * 2.0 ** -133: 0x0002,               # subnormal tie -> even
+        0.5 * 2.0 ** -133: 0x0000,               # tie between 0 and 2^-133 -> 0
+        3.3895313892515355e38: 0x7F7F,           # largest finite bf16
+        3.40e38: 0x7F80,                          # rounds past the top -> +inf
+        -0.0: 0x8000,
+        2.5: 0x4020,
+    }
+    for x, want in cases.items():
+        assert int(O.f64_to_bf16_bits(x)) == want, (x, hex(int(O.f64_to_bf16_bits(x))), hex(want))
+    assert int(O.f64_to_bf16_bits(float("nan"))) == 0x7FC0
+    assert int(O.f64_to_bf16_bits(float("-inf"))) == 0xFF80
+
+
+# ----------------------------------------------------------------------------- pooling
+
+def test_pool_hand_cases():
+    raw = np.array([[1.0, 2.0], [2.0, 2.0], [3.0, 2.0], [4.0, 2.0],          # mean (2.5, 2)
+                    [1.0, 1.0], [1.0, 1.0 + 2 ** -7], [1.0, 1.0], [1.0, 1.0 + 2 ** -7],  # (1, 1+2^-8 -> tie -> 1)
+                    [7.0, 7.0], [7.0, 7.0], [7.0, 7.0]])                     # partial block: not pooled
+    pooled = O.bf16_bits_to_f64(O.pool_keys(to_bits(raw)))
+    assert pooled.shape == (2, 2)
+    assert np.array_equal(pooled, [[2.5, 2.0], [1.0, 1.0]])
+
+
+def test_pool_matches_torch_mean_when_exact():
+    # For 4 bf16 values within a 2^15 magnitude ratio the fp32 sum is exact, so
+    # torch's (sum/4 in fp32).to(bf16) is the exactly rounded mean.
+    g = torch.Generator().manual_seed(3)
+    raw = (torch.randn(4096, 128, generator=g) / math.sqrt(128)).to(torch.bfloat16)
+    r32 = raw.float().view(-1, 4, 128)
+    s32 = ((r32[:, 0] + r32[:, 1]) + r32[:, 2]) + r32[:, 3]
+    s64 = r32.double().sum(1)
+    exact = (s32.double() == s64).all(dim=1).numpy()
+    assert exact.mean() > 0.99
+    want = (s32 / 4).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = O.pool_keys(raw.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(got[exact], want[exact])
+
+
+def test_pool_constant_block_is_itself():
+    rng = np.random.default_rng(5)
+    row = to_bits(O.bf16_bits_to_f64(O.f64_to_bf16_bits(rng.standard_normal(128))))
+    raw = np.tile(row, (8, 1))
+    assert np.array_equal(O.pool_keys(raw), np.tile(row, (2, 1)))
+
+
+# ----------------------------------------------------------------------------- visibility and budget
+
+def test_dense_limit_is_2051():
+    figs = read_page_figures()
+    limit = int(figs["dense_limit_tokens"])
+    for p in range(0, 4000):
+        nb = O.visible_blocks(p)
+        sel = O.select_blocks(np.zeros(nb))
+        dense = len(sel) == nb
+        assert dense == (p <= limit), p
+    assert O.DENSE_LIMIT == limit
+    # just past the limit: 513 blocks scored, 512 kept
+    assert O.visible_blocks(2052) == 513 and len(O.select_blocks(np.zeros(513))) == 512
+
+
+def test_budget_exact_beyond_limit():
+    figs = read_page_figures()
+    rng = np.random.default_rng(7)
+    for p in list(range(2052, 2200)) + rng.integers(2052, 3_000_000, 200).tolist():
+        nb = O.visible_blocks(p)
+        sel = O.select_blocks(rng.standard_normal(nb))
+        assert len(sel) * O.COMPRESS_RATIO == int(figs["selected_tokens"])
+        toks = O.attended_tokens(p, sel)
+        assert len(toks) == 2048 + (p % 4) + 1
+        assert toks[-1] == p and len(np.unique(toks)) == len(toks)
+
+
+def test_attended_tokens_membership_definition():
+    # t in J  <=>  t <= p and (block(t) selected or t in the query's own block)
+    rng = np.random.default_rng(11)
+    for p in [0, 1, 3, 4, 5, 37, 2051, 2052, 5000]:
+        nb = O.visible_blocks(p)
+        sel = np.sort(rng.choice(nb, size=min(nb, 7), replace=False)) if nb else np.zeros(0, np.int64)
+        want = [t for t in range(p + 1) if (t // 4) in set(sel.tolist()) or t // 4 >= nb]
+        assert O.attended_tokens(p, sel).tolist() == want
+
+
+# ----------------------------------------------------------------------------- scoring
+
+def test_scores_exact_on_integers():
+    rng = np.random.default_rng(13)
+    q = rng.integers(-8, 9, 128)
+    pk = rng.integers(-8, 9, (50, 128))
+    got = O.score_blocks(to_bits(q), to_bits(pk))
+    want = [sum(int(a) * int(b) for a, b in zip(q, row)) for row in pk]   # exact integer arithmetic
+    assert got.tolist() == want
+
+
+def test_scores_basis_vectors():
+    eye = to_bits(np.eye(128))
+    q = to_bits(np.arange(128) - 64.0)
+    assert np.array_equal(O.score_blocks(q, eye), np.arange(128) - 64.0)
+
+
+# ----------------------------------------------------------------------------- top-k
+
+def _brute_force_topk(s, k):
+    """The unique k-subset in which every member beats every non-member, where
+    a beats b iff s[a] > s[b] or (s[a] == s[b] and a < b)."""
+    n = len(s)
+    beats = lambda a, b: s[a] > s[b] or (s[a] == s[b] and a < b)
+    found = [c for c in itertools.combinations(range(n), k)
+             if all(beats(a, b) for a in c for b in range(n) if b not in c)]
+    assert len(found) == 1
+    return list(found[0])
+
+
+def test_topk_brute_force_tiny():
+    rng = np.random.default_rng(17)
+    for n in range(0, 10):
+        for trial in range(6):
+            s = rng.integers(-2, 3, n).astype(np.float64)          # many duplicates
+            if trial == 0:
+                s[:] = 1.0                                         # all equal
+            for k in range(0, n + 2):
+                got = O.select_blocks(s, k).tolist()
+                assert got == _brute_force_topk(s, min(k, n)), (s, k)
+                srt = sorted(range(n), key=lambda i: (-s[i], i))[: min(k, n)]
+                assert got == sorted(srt)
+
+
+def test_topk_nan_ranks_last_and_kth_score():
+    s = np.array([0.5, np.nan, 2.0, 2.0, -1.0])
+    assert O.select_blocks(s, 4).tolist() == [0, 2, 3, 4]
+    assert O.kth_score(s, 3) == 0.5
+    assert O.select_blocks(s, 9).tolist() == [0, 1, 2, 3, 4]
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _sdpa(q, k, v, mask, n_kv_heads, scale):
+    """torch SDPA in fp64 for one query: q [Hq, D], k/v [T, Hkv, D], mask [T] bool."""
+    hq = q.shape[0]
+    kk = torch.tensor(k).permute(1, 0, 2).repeat_interleave(hq // n_kv_heads, dim=0)   # [Hq, T, D]
+    vv = torch.tensor(v).permute(1, 0, 2).repeat_interleave(hq // n_kv_heads, dim=0)
+    qq = torch.tensor(q)[:, None, :]                                                  # [Hq, 1, D]
+    m = torch.tensor(mask)[None, None, :].expand(hq, 1, -1)
+    out = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=m, scale=scale)
+    return out[:, 0, :].numpy()
+
+
+def _rand_case(rng, p, hq, hkv, d, sharp=True):
+    s = 1.0 if sharp else 1.0 / math.sqrt(d)
+    q = rng.standard_normal((hq, d)) * s
+    k = rng.standard_normal((p + 1, hkv, d)) * s
+    v = rng.standard_normal((p + 1, hkv, d))
+    return q, k, v
+
+
+def test_dense_regime_equals_causal_sdpa():
+    rng = np.random.default_rng(19)
+    for p in [0, 1, 2, 3, 4, 9, 100, 2047, 2051]:
+        q, k, v = _rand_case(rng, p, 4, 2, 16)
+        scores = rng.standard_normal(O.visible_blocks(p))
+        sel = O.select_blocks(scores)
+        toks = O.attended_tokens(p, sel)
+        assert toks.tolist() == list(range(p + 1))
+        out, lse = O.attend(q, k, v, toks, 2, 1 / math.sqrt(16))
+        ref = _sdpa(q, k, v, np.ones(p + 1, bool), 2, 1 / math.sqrt(16))
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_sparse_regime_equals_masked_sdpa_and_logsumexp():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(23)
+    for p in [2052, 2055, 3001, 9000]:
+        hq, hkv, d = 8, 2, 32
+        q, k, v = _rand_case(rng, p, hq, hkv, d)
+        sel = O.select_blocks(rng.standard_normal(O.visible_blocks(p)))
+        toks = O.attended_tokens(p, sel)
+        mask = np.zeros(p + 1, bool)
+        mask[toks] = True
+        out, lse = O.attend(q, k, v, toks, hkv, 0.125)
+        np.testing.assert_allclose(out, _sdpa(q, k, v, mask, hkv, 0.125), rtol=1e-11, atol=1e-12)
+        for h in range(hq):
+            logits = (k[toks, h // (hq // hkv)] @ q[h]) * 0.125
+            assert abs(lse[h] - logsumexp(logits)) < 1e-11
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(29)
+    hq, hkv, d = 4, 2, 8
+    # p = 0: only the query's own token -> out = V[0] exactly, lse = its logit
+    q, k, v = _rand_case(rng, 0, hq, hkv, d)
+    out, lse = O.attend(q, k, v, O.attended_tokens(0, []), hkv, 0.5)
+    for h in range(hq):
+        assert np.array_equal(out[h], v[0, h // 2])
+        assert lse[h] == pytest.approx(0.5 * float(k[0, h // 2] @ q[h]), abs=1e-14)
+    # constant V rows -> that row; equal keys -> mean of V over J
+    p = 5000
+    q, k, v = _rand_case(rng, p, hq, hkv, d)
+    sel = O.select_blocks(rng.standard_normal(O.visible_blocks(p)))
+    toks = O.attended_tokens(p, sel)
+    vc = np.broadcast_to(v[0:1], v.shape).copy()
+    out, _ = O.attend(q, k, vc, toks, hkv, 0.5)
+    np.testing.assert_allclose(out, np.stack([v[0, h // 2] for h in range(hq)]), rtol=1e-13)
+    ke = np.broadcast_to(k[0:1], k.shape).copy()
+    out, lse = O.attend(q, ke, v, toks, hkv, 0.5)
+    np.testing.assert_allclose(out, np.stack([v[toks, h // 2].mean(0) for h in range(hq)]), rtol=1e-12)
+    for h in range(hq):
+        assert lse[h] == pytest.approx(0.5 * float(k[0, h // 2] @ q[h]) + math.log(len(toks)), rel=1e-12)
+    # one dominant key -> its V row
+    kd = k.copy()
+    t_star = toks[len(toks) // 3]
+    kd[t_star] = 200.0 * q[[0, 2]]
+    out, _ = O.attend(q[[0, 2]], kd, v, toks, hkv, 1.0)
+    np.testing.assert_allclose(out, v[t_star], rtol=1e-9, atol=1e-9)
+
+
+def test_lse_merge_of_any_partition_equals_unsplit():
+    rng = np.random.default_rng(31)
+    p = 4099
+    hq, hkv, d = 8, 2, 16
+    q, k, v = _rand_case(rng, p, hq, hkv, d)
+    toks = O.attended_tokens(p, O.select_blocks(rng.standard_normal(O.visible_blocks(p))))
+    want_out, want_lse = O.attend(q, k, v, toks, hkv, 0.25)
+    for n_parts in [1, 2, 3, 7, 64]:
+        perm = rng.permutation(toks)
+        cuts = np.sort(rng.choice(np.arange(1, len(toks)), n_parts - 1, replace=False)) if n_parts > 1 else []
+        parts = [O.attend_partial(q, k, v, piece, hkv, 0.25) for piece in np.split(perm, cuts)]
+        parts.append(O.attend_partial(q, k, v, np.zeros(0, np.int64), hkv, 0.25))   # an empty split
+        out, lse = O.lse_merge(parts)
+        np.testing.assert_allclose(out, want_out, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, want_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_interval_walk_equals_per_query_attention():
+    rng = np.random.default_rng(37)
+    p = 9000
+    hq, hkv, d = 4, 2, 16
+    q, k, v = _rand_case(rng, p, hq, hkv, d)
+    sel = O.select_blocks(rng.standard_normal(O.visible_blocks(p)))
+    want_out, want_lse = O.attend(q, k, v, O.attended_tokens(p, sel), hkv, 0.25)
+    for interval in [1000, 4096, 8192, 16384]:
+        out, lse = O.interval_walk_query(p, sel, q, k, v, hkv, interval, scale=0.25)
+        np.testing.assert_allclose(out, want_out, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, want_lse, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- golden files
+
+def read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, val = line.split("=", 1)
+                vals[key.strip()] = ast.literal_eval(val.strip())
+    return vals
+
+
+def read_page_figures():
+    vals = {}
+    with open(os.path.join(GOLDEN, "page_figures.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, val = line.split()
+                vals[key] = float(val)
+    return vals
+
+
+def _closed_form(expr):
+    return eval(expr, {"__builtins__": {}}, {"e": math.e, "ln": math.log})
+
+
+def test_tiny_worked_example():
+    g = read_golden("tiny_worked_example.txt")
+    raw = to_bits(g["raw_idx_k"])
+    pooled = O.pool_keys(raw)
+    assert O.bf16_bits_to_f64(pooled).tolist() == g["expect_pooled"]
+    k = np.stack([g["k_kv0"], g["k_kv1"]], axis=1).astype(np.float64)   # [T, Hkv, D]
+    v = np.stack([g["v_kv0"], g["v_kv1"]], axis=1).astype(np.float64)
+    r = O.decode_query(g["p"], to_bits(g["q_idx"]), pooled, to_bits(g["q"]), to_bits(k), to_bits(v),
+                       g["n_kv_heads"], scale=g["scale"], k_blocks=g["k_blocks"])
+    assert r["scores"].tolist() == g["expect_scores"]
+    assert r["sel"].tolist() == g["expect_sel"]
+    assert r["tokens"].tolist() == g["expect_tokens"]
+    want_out = np.array([[_closed_form(x) for x in row] for row in g["expect_out"]])
+    want_lse = np.array([_closed_form(x) for x in g["expect_lse"]])
+    np.testing.assert_allclose(r["out"], want_out, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(r["lse"], want_lse, rtol=1e-14)
