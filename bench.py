@@ -1,0 +1,578 @@
+#!/usr/bin/env python
+"""Benchmark of indexer-driven sparse attention on one GB300 (or N independent replicas).
+
+Headline: million-token decode (batch 1, context 1,048,320 = 262,080 pooled blocks,
+12 layers, 16 query / 2 KV heads, budget 2048). One step = one decode token through
+all 12 layers; each layer-step pools the newest complete block, scores every pooled
+block, selects the top 512, and runs the split-K gathered attention with its LSE merge.
+The 12 layer-steps are replayed as one CUDA graph, layers in stream order.
+Metric: layer-steps/s (plus the algorithmic HBM GB/s it implies). The same JSON line
+carries the prefill chunk (4096 queries over a 262,144-token history) in chunk tok/s.
+
+Inputs are synthetic (seeded), already resident in HBM for `value`; `e2e` adds the
+per-step host->device copy of the new token's inputs and the device->host read of the
+step's result through the same C-ABI path. The working set (12 x 64 MiB pooled keys
++ 12 x 2 GiB K/V) is far larger than L2, so no explicit flush is needed between steps.
+
+`--impl reference` times the fp64 CPU oracle on the host cores on a bounded sample of
+the same workload (one layer-step per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn decode layer-steps/s at 1M ctx (+ HBM GB/s; prefill chunk tok/s)"
+UNIT = "layer-steps/s"
+N_LAYERS = 12
+CTX_1M = 1048320
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-instrument", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sust=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qsa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax = float(f[2])
+                    power.append(float(f[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        finally:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+class DeviceEvents:
+    """Timing events recorded as graph nodes (cudaEventRecordExternal) on a capturing
+    stream, so per-kernel durations can be read after each graph replay."""
+
+    def __init__(self):
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.events = []
+
+    def new(self):
+        ev = ctypes.c_void_p()
+        if self.rt.cudaEventCreate(ctypes.byref(ev)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+        self.events.append(ev)
+        return ev
+
+    def record(self, ev, stream_handle: int):
+        if self.rt.cudaEventRecordWithFlags(ev, ctypes.c_void_p(stream_handle), 1) != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed")
+
+    def elapsed_ms(self, a, b) -> float:
+        ms = ctypes.c_float()
+        if self.rt.cudaEventElapsedTime(ctypes.byref(ms), a, b) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return ms.value
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- decode
+
+class DecodeLayers:
+    """12 layers of the million-token decode workload resident in HBM."""
+
+    def __init__(self, n_layers, device):
+        import torch
+        from indexer_driven_sparse_gb300 import inputs as I
+        from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+        self.w = I.million_decode(seed=0, device=device, n_layers=n_layers)
+        self.b = DecodeBatch(16, 2, self.w.ctx_len, device=device)
+        self.pooled = []
+        for L in self.w.layers:
+            pk = self.b.new_pooled()
+            self.b.pool(L.raw_idx_k, pk)
+            self.pooled.append(pk)
+        p = self.w.ctx_len[0]
+        nblk = (p + 1) // 4
+        i32 = dict(dtype=torch.int32, device=device)
+        self.inc_begin = torch.tensor([nblk - 1], **i32)   # newest complete block
+        self.inc_end = torch.tensor([nblk], **i32)
+        torch.cuda.synchronize()
+        st = self.b.device_status()
+        if st[0] != 0:
+            raise RuntimeError(f"device status after pooling: {st}")
+
+    def layer_step(self, l, events=None, stream_handle=None):
+        """Pool the newest block, then score -> top-k -> attend for layer l."""
+        from indexer_driven_sparse_gb300 import binding as qb
+        b, L = self.b, self.w.layers[l]
+        rec = (lambda name: events(l, name)) if events else (lambda name: None)
+        rec("pool0")
+        qb.qsa_pool_keys(b.cfg, L.raw_idx_k, b.tok_off, b.blk_off, self.inc_begin, self.inc_end, 1, self.pooled[l],
+                         b.ws)
+        rec("pool1")
+        b.score(L.q_idx, self.pooled[l])
+        rec("score1")
+        b.topk()
+        rec("topk1")
+        b.attend(L.q, L.k_cache, L.v_cache)
+        rec("attend1")
+
+    def step(self, events=None):
+        for l in range(len(self.w.layers)):
+            self.layer_step(l, events)
+
+
+def capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_graph(g, stream, steps, warmup, world):
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return t0.elapsed_time(t1) / 1000.0
+
+
+def instrumented_kernel_times(dl, stream, steps):
+    """Per-kernel mean durations (us) from event nodes inside a replayed step graph."""
+    import torch
+    ev = DeviceEvents()
+    marks = {}
+    h = stream.cuda_stream
+
+    def events(l, name):
+        e = ev.new()
+        ev.record(e, h)
+        marks[(l, name)] = e
+
+    def body():
+        ev_first = ev.new()
+        ev.record(ev_first, h)
+        marks[("start",)] = ev_first
+        dl.step(events)
+
+    g = capture(body, stream)
+    sums = {"pool": 0.0, "score": 0.0, "topk": 0.0, "attend": 0.0}
+    n_layers = len(dl.w.layers)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(n_layers):
+            sums["pool"] += ev.elapsed_ms(marks[(l, "pool0")], marks[(l, "pool1")])
+            sums["score"] += ev.elapsed_ms(marks[(l, "pool1")], marks[(l, "score1")])
+            sums["topk"] += ev.elapsed_ms(marks[(l, "score1")], marks[(l, "topk1")])
+            sums["attend"] += ev.elapsed_ms(marks[(l, "topk1")], marks[(l, "attend1")])
+    return {k: 1000.0 * v / (steps * n_layers) for k, v in sums.items()}
+
+
+def e2e_decode(dl, stream, steps, warmup):
+    """Same step with the new token's inputs copied host->device from pinned memory
+    and the last layer's output read back, every step."""
+    import torch
+    b, layers = dl.b, dl.w.layers
+    p = dl.w.ctx_len[0]
+    # per layer: q [16,256] + q_idx [128] + new token k,v [2,256] each + raw idx key [128] (bf16)
+    per_layer = 16 * 256 + 128 + 2 * 2 * 256 + 128
+    host_in = torch.empty(len(layers) * per_layer, dtype=torch.bfloat16).pin_memory()
+    host_in.copy_(torch.randn(host_in.shape, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16) / 16)
+    dev_in = torch.empty_like(host_in, device="cuda")
+    host_out = torch.empty(16 * 256 + 32, dtype=torch.bfloat16).pin_memory()
+    out_view = b.out.view(-1)
+    lse_view = b.lse.view(torch.bfloat16).view(-1)
+
+    def body():
+        for l, L in enumerate(layers):
+            o = l * per_layer
+            L.q.view(-1).copy_(dev_in[o:o + 4096])
+            L.q_idx.view(-1).copy_(dev_in[o + 4096:o + 4224])
+            L.k_cache[p].view(-1).copy_(dev_in[o + 4224:o + 4736])
+            L.v_cache[p].view(-1).copy_(dev_in[o + 4736:o + 5248])
+            L.raw_idx_k[p].copy_(dev_in[o + 5248:o + 5376])
+            dl.layer_step(l)
+
+    g = capture(body, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            dev_in.copy_(host_in, non_blocking=True)
+            g.replay()
+            host_out[:4096].copy_(out_view, non_blocking=True)
+            host_out[4096:].copy_(lse_view, non_blocking=True)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            dev_in.copy_(host_in, non_blocking=True)
+            g.replay()
+            host_out[:4096].copy_(out_view, non_blocking=True)
+            host_out[4096:].copy_(lse_view, non_blocking=True)
+            stream.synchronize()
+        dt = time.perf_counter() - t0
+    h2d = host_in.numel() * 2
+    d2h = host_out.numel() * 2
+    return dt, h2d, d2h
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def prefill_bench(steps, warmup, pk):
+    import torch
+    from indexer_driven_sparse_gb300 import accounting as A
+    from indexer_driven_sparse_gb300 import binding as qb
+    from indexer_driven_sparse_gb300 import inputs as I
+    from indexer_driven_sparse_gb300.pipeline import PrefillChunk
+    w = I.prefill_chunk(device="cuda")
+    L = w.layers[0]
+    p0, nc = w.ctx_len[0], w.n_chunk
+    c = PrefillChunk(16, 2, p0, nc, 8192, device="cuda")
+    pooled = c.new_pooled()
+    c.pool(L.raw_idx_k, pooled)            # history blocks (setup)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    chunk_begin = torch.tensor([p0 // 4], **i32)
+    chunk_end = torch.tensor([(p0 + nc) // 4], **i32)
+    stream = torch.cuda.Stream()
+
+    def chunk():
+        qb.qsa_pool_keys(c.cfg, L.raw_idx_k, c.tok_off, c.blk_off, chunk_begin, chunk_end, nc // 4, pooled, c.ws)
+        c.run(L.q_idx, L.q, L.k_cache, L.v_cache, pooled)
+
+    def attend_only():
+        c.attend(L.q, L.k_cache, L.v_cache)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        chunk()
+    torch.cuda.synchronize()
+    st = c.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"prefill device status {st}")
+    n = max(2, steps // 20)
+    g_chunk = capture(chunk, stream)
+    t_chunk = time_graph(g_chunk, stream, n, max(1, warmup), 1) / n
+    g_att = capture(attend_only, stream)
+    t_att = time_graph(g_att, stream, n, max(1, warmup), 1) / n
+    att_flops = A.prefill_attention_flops(p0, nc)
+    score_flops = A.prefill_score_flops(p0, nc)
+    ach = att_flops / t_att / 1e12
+    return {
+        "workload": f"prefill chunk: {nc} queries at p0={p0}, 16 q / 2 kv heads, intervals 8192",
+        "chunk_tok_s": nc / t_chunk, "ms_per_chunk": t_chunk * 1e3,
+        "attention_only_tok_s": nc / t_att, "ms_attention": t_att * 1e3,
+        "attention_gflop_algorithmic": att_flops / 1e9, "scoring_gflop_algorithmic": score_flops / 1e9,
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": ach / pk["bf16"], "traffic": None,
+                     "kernel": "sparse_prefill_chunk (algorithmic FLOPs)"},
+    }
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def cpu_baseline_child(seconds: float):
+    """Time the fp64 oracle on one layer of the million-token decode workload (CPU draw
+    of the same recipe), single-threaded BLAS; prints one JSON object."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from indexer_driven_sparse_gb300 import inputs as I
+    torch.set_num_threads(1)
+    t_setup = time.perf_counter()
+    w = I.million_decode(seed=0, device="cpu", n_layers=1)
+    L = w.layers[0]
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    raw, qi, q, k, v = bits(L.raw_idx_k), bits(L.q_idx), bits(L.q), bits(L.k_cache), bits(L.v_cache)
+    p = w.ctx_len[0]
+    pooled = O.pool_keys(raw)                 # setup (steady state pools one block per 4 steps)
+    setup = time.perf_counter() - t_setup
+    n, t0 = 0, time.perf_counter()
+    while True:
+        O.pool_keys(raw[4 * (p // 4 - 1):4 * (p // 4)])
+        O.decode_query(p, qi[0], pooled, q[0], k, v, 2)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    print(json.dumps({"value": n / dt, "n": n, "seconds": dt, "setup_s": setup}))
+
+
+def run_cpu_baseline(seconds: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
+                        "--cpu-seconds", str(seconds)], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{d['n']} layer-steps of one million-token layer (CPU draw of the same recipe), "
+                      f"fp64 numpy, single-threaded BLAS, {d['seconds']:.1f} s"}
+
+
+def reference_main(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"                  # before numpy loads its BLAS: one host core
+    import numpy as np
+    import torch
+    import oracle as O
+    from indexer_driven_sparse_gb300 import inputs as I
+    w = I.million_decode(seed=0, device="cpu", n_layers=1)
+    L = w.layers[0]
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    raw, qi, q, k, v = bits(L.raw_idx_k), bits(L.q_idx), bits(L.q), bits(L.k_cache), bits(L.v_cache)
+    p = w.ctx_len[0]
+    pooled = O.pool_keys(raw)
+
+    def step():
+        O.pool_keys(raw[4 * (p // 4 - 1):4 * (p // 4)])
+        O.decode_query(p, qi[0], pooled, q[0], k, v, 2)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    val = args.steps / dt
+    cores = 1
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "million_decode_ctx1048320 (one layer-step per step)", "batch": 1,
+                       "ctx": CTX_1M, "n_q_heads": 16, "n_kv_heads": 2, "head_dim": 256, "budget": 2048},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one million-token layer (CPU draw of the same recipe), fp64 numpy"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_baseline_child:
+        cpu_baseline_child(args.cpu_seconds)
+        return 0
+    if args.impl == "reference":
+        return reference_main(args)
+
+    cpu_base = None
+    rank, local, world = dist_setup()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = run_cpu_baseline(args.cpu_seconds)   # before any CUDA work in this process
+
+    import torch
+    from indexer_driven_sparse_gb300 import accounting as A
+    from indexer_driven_sparse_gb300 import binding as qb
+    from indexer_driven_sparse_gb300 import build as qbuild
+    qbuild.build()
+    qb.load()
+    torch.cuda.set_device(local)
+    pk = peaks()
+
+    dl = DecodeLayers(args.layers, "cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        dl.step()                               # eager warm-up, checks status below
+    torch.cuda.synchronize()
+    st = dl.b.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status {st}")
+    g = capture(dl.step, stream)
+
+    with ClockSampler(local) as clk:
+        t = time_graph(g, stream, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    t = max_over_ranks(t, world)
+    n_layers = len(dl.w.layers)
+    layer_steps = world * args.steps * n_layers
+    value = layer_steps / t
+    bytes_ls = A.decode_layer_step_bytes(dl.w.ctx_len, 16)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"million_decode_ctx{CTX_1M}", "batch": 1, "ctx": CTX_1M, "layers": n_layers,
+                   "n_q_heads": 16, "n_kv_heads": 2, "head_dim": 256, "idx_dim": 128, "ratio": 4,
+                   "budget": 2048, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (12 x 64 MiB pooled keys + 12 x 2 GiB K/V), no flush"},
+        "hbm_gbs_algorithmic": bytes_ls * value / world / 1e9,
+        "us_per_layer_step": 1e6 * t / (args.steps * n_layers),
+        "clocks": clocks,
+        "gpu_launches": None,
+    }
+    launches_per_layer = 5                       # pool, score, topk, attention, merge
+    line["gpu_launches"] = launches_per_layer * n_layers * args.steps
+
+    if not args.no_instrument:
+        kt = instrumented_kernel_times(dl, stream, max(5, min(50, args.steps)))
+        line["kernel_us"] = kt
+        algo = {"score": A.score_scan_bytes(dl.w.ctx_len),
+                "attend": A.kv_read_bytes(A.attended(CTX_1M)) + 2 * 16 * 256 * 2}
+        dom = max(kt, key=kt.get)
+        if dom in algo:
+            ach = algo[dom] / (kt[dom] * 1e-6) / 1e9
+            line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
+                                "frac": ach / pk["hbm"], "traffic": None, "kernel": dom,
+                                "peak_src": pk["src"]}
+        else:
+            sc = kt["score"]
+            ach = algo["score"] / (sc * 1e-6) / 1e9
+            line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
+                                "frac": ach / pk["hbm"], "traffic": None, "kernel": "score",
+                                "note": f"dominant kernel is {dom} (latency-bound); score scan reported",
+                                "peak_src": pk["src"]}
+
+    if not args.no_e2e:
+        dt, h2d, d2h = e2e_decode(dl, stream, max(10, args.steps // 4), max(3, args.warmup))
+        n = max(10, args.steps // 4)
+        line["e2e"] = {"value": n * n_layers / dt * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h}
+
+    if not args.no_prefill:
+        del g
+        line["prefill"] = prefill_bench(args.steps, args.warmup, pk)
+
+    if cpu_base is not None:
+        line["cpu_baseline"] = cpu_base
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

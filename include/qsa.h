@@ -1,0 +1,189 @@
+/*
+ * qsa.h — C ABI of the GB300 (sm_103a) indexer-driven sparse attention library (libqsa.so).
+ *
+ * The method (Qwen Sparse Attention style), as stated on
+ * "3090x3で 314 万コンテキスト; KVキャッシュをホストRAMに置けるアーキテクチャの偉大さ":
+ *   section "なぜ": an indexer scores every pooled 4-token block of the history
+ *     (indexer_compress_ratio = 4) and keeps a fixed budget of 2048 tokens
+ *     (indexer_budget = 2048, i.e. the top 512 blocks); up to 4*512+3 = 2051
+ *     tokens of context everything is read;
+ *   section "VRAM に残す必要があるもの": the pooled key of a block is 128 x bf16 and
+ *     the indexer scans all of them every step;
+ *   section "カーネルを書き換えずに済む": the gather kernel addresses
+ *     K/V as (tok * n_kv_heads + kv_head) * head_dim + d;
+ *   section "ちなみにこの欠点": prefill walks the history in fixed intervals
+ *     (outer loop) with all chunk tokens inside (inner loop), merging softmax
+ *     partials across intervals.
+ * Partial results over disjoint token sets are merged by log-sum-exp
+ * ("GLM-5.3 最適化 第2部：16基のH200上でのPCP、DCP、およびHybrid HiSparse", section "DCP").
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    never allocates, never frees, never keeps a pointer after returning and never
+ *    synchronises, except qsa_read_device_status, which synchronises the stream it is given.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream). Nothing else is launched, so the calls can be captured in a CUDA graph.
+ *  - Row-major layouts; bf16 values are passed as raw 16-bit patterns (qsa_bf16).
+ *  - Ragged batches are flat token arrays with int32 offsets (tok_off[s] .. tok_off[s+1]).
+ *  - Host-side validation failures return immediately with nothing enqueued.
+ *    A failed launch returns QSA_ERR_CUDA. Errors found on the device (an index out
+ *    of range, a bounded wait that gave up) never trap: the kernel skips the access,
+ *    records the first error in the workspace's status word and returns; read it
+ *    with qsa_read_device_status. The status word is sticky until qsa_workspace_init.
+ *  - Supported geometry: head_dim 256, idx_dim 128, indexer_compress_ratio 4,
+ *    indexer_budget 2048, n_q_heads % n_kv_heads == 0, n_q_heads / n_kv_heads <= 16.
+ *    Anything else returns QSA_ERR_UNSUPPORTED.
+ *  - Per-thread detail of the last host-side error: qsa_last_error().
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QSA_API __attribute__((visibility("default")))
+#else
+#define QSA_API
+#endif
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, negative size, bad stride */
+    QSA_ERR_UNSUPPORTED = 2,        /* geometry outside the supported set */
+    QSA_ERR_WORKSPACE_TOO_SMALL = 3,
+    QSA_ERR_CUDA = 4,               /* a CUDA launch or runtime call failed */
+    QSA_ERR_DEVICE_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+    QSA_ERR_DEVICE_BOUNDS = 6       /* a device-side index/offset check failed */
+} qsa_status;
+
+typedef enum {
+    QSA_OP_POOL_KEYS = 0,
+    QSA_OP_INDEX_SCORE = 1,
+    QSA_OP_TOPK_BLOCKS = 2,
+    QSA_OP_SPARSE_DECODE = 3,
+    QSA_OP_SPARSE_PREFILL_CHUNK = 4
+} qsa_op;
+
+/* Geometry. Field names follow the model config the page quotes
+ * (indexer_budget, indexer_compress_ratio, section "なぜ"). */
+typedef struct {
+    int32_t n_q_heads;              /* query heads (8 or 16 in the workloads) */
+    int32_t n_kv_heads;             /* KV heads (2); query head h reads KV head h / (n_q_heads/n_kv_heads) */
+    int32_t head_dim;               /* 256 */
+    int32_t idx_dim;                /* 128: width of raw/pooled indexer keys and indexer queries */
+    int32_t indexer_compress_ratio; /* 4 tokens per pooled block */
+    int32_t indexer_budget;         /* 2048 tokens = 512 blocks kept per query */
+    float softmax_scale;            /* <= 0 selects 1/sqrt(head_dim) */
+} qsa_config;
+
+typedef uint16_t qsa_bf16;          /* raw bf16 bits */
+typedef void *qsa_stream;           /* cudaStream_t */
+
+/* Workspace bytes an op needs for the given sizes (0 on unsupported geometry).
+ * n_rows: queries (index_score/topk), sequences (decode), chunk queries (prefill).
+ * max_blocks: the largest number of visible blocks of any row (topk: the scores' ld).
+ * Every workspace starts with a 256-byte status block; it must be zeroed once with
+ * qsa_workspace_init before first use (and after a device error). One workspace
+ * may be reused by consecutive calls on the same stream; calls that run
+ * concurrently need separate workspaces. */
+QSA_API size_t qsa_workspace_size(int32_t op, const qsa_config *cfg, int32_t n_rows, int64_t max_blocks);
+
+/* Zero `ws_bytes` bytes of the workspace on `stream` (clears the status word). */
+QSA_API qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream);
+
+/* Synchronise `stream`, then copy the workspace's status word to *out and the
+ * kernel-specific detail (e.g. the offending row) to *detail (may be NULL). */
+QSA_API qsa_status qsa_read_device_status(const void *ws, qsa_stream stream, qsa_status *out, int32_t *detail);
+
+/* a1 — Pool indexer keys ("VRAM に残す必要があるもの": one pooled 128 x bf16 key per
+ * 4-token block). For each sequence s < B and each block b in [blk_begin[s], blk_end[s]):
+ *   pooled[blk_off[s] + b][d] = bf16_rne( (raw[t0][d] + raw[t0+1][d] + raw[t0+2][d] + raw[t0+3][d]) / 4 ),
+ *   t0 = tok_off[s] + 4 b,
+ * with the sum exact (accumulated in fp64) and a single round-to-nearest-even.
+ *   raw_idx_k  [n_tokens_total, idx_dim] bf16, 16-byte aligned
+ *   tok_off    [B+1] int32 (device), blk_off [B+1] int32, blk_begin [B], blk_end [B] int32
+ *   pooled     [n_pooled_total, idx_dim] bf16 (written), 16-byte aligned
+ *   max_blocks_per_seq: host upper bound of blk_end[s] - blk_begin[s] (sizes the grid)
+ * Device checks: 0 <= blk_begin <= blk_end, blk_end - blk_begin <= max_blocks_per_seq,
+ * 4*blk_end <= tokens of s, blk_off[s] + blk_end <= n_pooled_total; a failing sequence
+ * is skipped and QSA_ERR_DEVICE_BOUNDS recorded. Only complete blocks are pooled. */
+QSA_API qsa_status qsa_pool_keys(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, int64_t n_tokens_total,
+                                 const int32_t *tok_off, const int32_t *blk_off, const int32_t *blk_begin,
+                                 const int32_t *blk_end, int32_t B, int64_t max_blocks_per_seq,
+                                 qsa_bf16 *pooled, int64_t n_pooled_total,
+                                 void *ws, size_t ws_bytes, qsa_stream stream);
+
+/* a2 — Indexer scores ("なぜ", "VRAM に残す必要があるもの": every pooled block is scored
+ * every step). For query r < Nq with p = q_pos[r] history tokens and nb = p / 4:
+ *   scores[r * ld + b] = sum_d q_idx[r][d] * pooled[blk_off[q_seq[r]] + b][d],  b < nb,
+ * fp32 accumulation of exact bf16 products. Entries b >= nb are not written.
+ *   q_idx [Nq, idx_dim] bf16; q_seq [Nq], q_pos [Nq] int32; pooled as above;
+ *   blk_off [B+1] int32 (per-sequence pooled offsets); scores [Nq, ld] fp32.
+ * Device checks: nb <= ld, blk_off[s] + nb <= n_pooled_total. */
+QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_seq,
+                                   const int32_t *q_pos, int32_t Nq, const qsa_bf16 *pooled,
+                                   int64_t n_pooled_total, const int32_t *blk_off, float *scores, int64_t ld,
+                                   void *ws, size_t ws_bytes, qsa_stream stream);
+
+/* a3 — Fixed-budget block selection ("なぜ": exactly 2048 tokens = 512 blocks beyond 2051
+ * tokens of context; all blocks below). For row r with nb = q_pos[r] / 4, k = budget/ratio:
+ * the min(k, nb) blocks with the largest scores, ties to the lower block id
+ * ("125B MoE を 3090 3 枚で運用する vLLM 最適化編" section 3.3 uses the same rule), written
+ * to blocks[r * k ...] in ASCENDING id order; the rest of the row is set to -1;
+ * count[r] = min(k, nb). NaN scores rank below every number; -0 equals +0.
+ *   scores [Nq, ld] fp32 (only b < nb read); q_pos [Nq]; blocks [Nq, k] int32; count [Nq] int32. */
+QSA_API qsa_status qsa_topk_blocks(const qsa_config *cfg, const float *scores, int64_t ld, const int32_t *q_pos,
+                                   int32_t Nq, int32_t *blocks, int32_t *count,
+                                   void *ws, size_t ws_bytes, qsa_stream stream);
+
+/* a4 + a5 — Sparse GQA decode over the selected blocks with split partials merged by
+ * log-sum-exp ("なぜ": 4 MiB of K/V per layer whatever the context; "カーネルを
+ * 書き換えずに済む": K/V addressing; "GLM-5.3 最適化 第2部" section DCP: LSE merge).
+ * Sequence s has its query at position p = ctx_len[s]; its tokens live at
+ * tok_off[s] .. tok_off[s+1]-1 and the current token's K/V is already at index p.
+ * Attended tokens J = {4b .. 4b+3 : b in blocks[s][0 .. count[s])} U {4*(p/4) .. p}.
+ * For query head h (KV head h / (Hq/Hkv)):
+ *   out[s][h] = sum_{j in J} softmax_j(scale * q[s][h] . K[j]) V[j],   lse[s][h] = ln sum_j e^(scale q.K[j])
+ *   q [B, Hq, D] bf16; k_cache, v_cache [n_tokens_total, Hkv, D] bf16 (token-major);
+ *   blocks [B, k] int32 (as written by qsa_topk_blocks; any order, no duplicates), count [B];
+ *   out [B, Hq, D] bf16; lse [B, Hq] fp32 or NULL.
+ * Device checks: p + 1 <= tokens of s, count <= min(k, p/4), 0 <= block < p/4. */
+QSA_API qsa_status qsa_sparse_decode(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                     const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
+                                     const int32_t *ctx_len, int32_t B, const int32_t *blocks,
+                                     const int32_t *count, qsa_bf16 *out, float *lse,
+                                     void *ws, size_t ws_bytes, qsa_stream stream);
+
+/* a6 — Prefill chunk ("ちなみにこの欠点": each chunk token selects its own 2048 tokens;
+ * the history is walked interval by interval with a softmax merge). Chunk query i
+ * (0 <= i < Nc) sits at p_i = p0 + i of one sequence whose K/V (history and chunk)
+ * occupy tokens 0 .. p0+Nc-1; it attends exactly what qsa_sparse_decode would for
+ * p = p_i with its own blocks[i] / count[i]. interval_tokens (a positive multiple of
+ * 128) sets the evaluation order only, not the result.
+ *   q [Nc, Hq, D] bf16; k_cache, v_cache [p0+Nc, Hkv, D] bf16; blocks [Nc, k]; count [Nc];
+ *   out [Nc, Hq, D] bf16; lse [Nc, Hq] fp32 or NULL. */
+QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
+                                            const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                            const int32_t *blocks, const int32_t *count, int32_t interval_tokens,
+                                            qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                            qsa_stream stream);
+
+/* Static description of a status code. */
+QSA_API const char *qsa_status_string(qsa_status s);
+
+/* Detail of the last host-side error on the calling thread ("" if none). */
+QSA_API const char *qsa_last_error(void);
+
+/* Library version, e.g. "qsa-gb300 0.1.0 sm_103a". */
+QSA_API const char *qsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

@@ -1,0 +1,186 @@
+"""ctypes binding of libqsa.so: argument marshalling only.
+
+Every function named ``qsa_*`` here calls the C entry point of the same name with
+the device pointers of the torch tensors it is given; all work runs in the
+library's CUDA kernels. PyTorch only supplies device memory and streams. If the
+library is missing, :func:`load` raises: there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+QSA_OK = 0
+QSA_ERR_INVALID_ARGUMENT = 1
+QSA_ERR_UNSUPPORTED = 2
+QSA_ERR_WORKSPACE_TOO_SMALL = 3
+QSA_ERR_CUDA = 4
+QSA_ERR_DEVICE_TIMEOUT = 5
+QSA_ERR_DEVICE_BOUNDS = 6
+
+OP_POOL_KEYS, OP_INDEX_SCORE, OP_TOPK_BLOCKS, OP_SPARSE_DECODE, OP_SPARSE_PREFILL_CHUNK = range(5)
+BLOCK_TOPK = 512
+
+
+class QsaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class qsa_config(C.Structure):
+    _fields_ = [("n_q_heads", C.c_int32), ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("idx_dim", C.c_int32), ("indexer_compress_ratio", C.c_int32), ("indexer_budget", C.c_int32),
+                ("softmax_scale", C.c_float)]
+
+
+def make_config(n_q_heads: int, n_kv_heads: int = 2, head_dim: int = 256, idx_dim: int = 128,
+                ratio: int = 4, budget: int = 2048, softmax_scale: float = 0.0) -> qsa_config:
+    return qsa_config(n_q_heads, n_kv_heads, head_dim, idx_dim, ratio, budget, softmax_scale)
+
+
+_P = C.c_void_p
+_I32 = C.c_int32
+_I64 = C.c_int64
+_SZ = C.c_size_t
+_CFG = C.POINTER(qsa_config)
+
+_SIGNATURES = {
+    "qsa_workspace_size": (_SZ, [_I32, _CFG, _I32, _I64]),
+    "qsa_workspace_init": (_I32, [_P, _SZ, _P]),
+    "qsa_read_device_status": (_I32, [_P, _P, C.POINTER(_I32), C.POINTER(_I32)]),
+    "qsa_pool_keys": (_I32, [_CFG, _P, _I64, _P, _P, _P, _P, _I32, _I64, _P, _I64, _P, _SZ, _P]),
+    "qsa_index_score": (_I32, [_CFG, _P, _P, _P, _I32, _P, _I64, _P, _P, _I64, _P, _SZ, _P]),
+    "qsa_topk_blocks": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "qsa_sparse_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qsa_sparse_prefill_chunk": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "qsa_status_string": (C.c_char_p, [_I32]),
+    "qsa_last_error": (C.c_char_p, []),
+    "qsa_version": (C.c_char_p, []),
+}
+
+_LIB = None
+
+
+def load(path: str | None = None):
+    """Load libqsa.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() (no CPU fallback exists)")
+    lib = C.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, dtype=None, name="tensor") -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _check(status: int, what: str):
+    if status != QSA_OK:
+        lib = load()
+        raise QsaError(status, f"{what}: {lib.qsa_status_string(status).decode()}: {lib.qsa_last_error().decode()}")
+
+
+def workspace_size(op: int, cfg: qsa_config, n_rows: int, max_blocks: int = 0) -> int:
+    return int(load().qsa_workspace_size(op, C.byref(cfg), n_rows, max_blocks))
+
+
+def make_workspace(op: int, cfg: qsa_config, n_rows: int, max_blocks: int = 0, device="cuda", stream=None):
+    """A zero-initialised workspace tensor for ``op`` (allocated by torch)."""
+    n = workspace_size(op, cfg, n_rows, max_blocks)
+    if n == 0:
+        raise QsaError(QSA_ERR_UNSUPPORTED, "unsupported geometry for workspace")
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    qsa_workspace_init(ws, stream)
+    return ws
+
+
+def qsa_workspace_init(ws, stream=None):
+    _check(load().qsa_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "qsa_workspace_init")
+
+
+def qsa_read_device_status(ws, stream=None):
+    st, det = _I32(0), _I32(0)
+    _check(load().qsa_read_device_status(_ptr(ws), _stream(stream), C.byref(st), C.byref(det)),
+           "qsa_read_device_status")
+    return st.value, det.value
+
+
+def _ws_args(ws):
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def qsa_pool_keys(cfg, raw_idx_k, tok_off, blk_off, blk_begin, blk_end, max_blocks_per_seq, pooled, ws, stream=None):
+    B = tok_off.numel() - 1
+    _check(load().qsa_pool_keys(C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"), raw_idx_k.shape[0],
+                                _ptr(tok_off, torch.int32), _ptr(blk_off, torch.int32), _ptr(blk_begin, torch.int32),
+                                _ptr(blk_end, torch.int32), B, int(max_blocks_per_seq),
+                                _ptr(pooled, torch.bfloat16, "pooled"), pooled.shape[0], *_ws_args(ws),
+                                _stream(stream)), "qsa_pool_keys")
+
+
+def qsa_index_score(cfg, q_idx, q_seq, q_pos, pooled, blk_off, scores, ws, stream=None):
+    _check(load().qsa_index_score(C.byref(cfg), _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(q_seq, torch.int32),
+                                  _ptr(q_pos, torch.int32), q_idx.shape[0], _ptr(pooled, torch.bfloat16, "pooled"),
+                                  pooled.shape[0], _ptr(blk_off, torch.int32), _ptr(scores, torch.float32, "scores"),
+                                  scores.shape[1], *_ws_args(ws), _stream(stream)), "qsa_index_score")
+
+
+def qsa_topk_blocks(cfg, scores, q_pos, blocks, count, ws, stream=None):
+    _check(load().qsa_topk_blocks(C.byref(cfg), _ptr(scores, torch.float32, "scores"), scores.shape[1],
+                                  _ptr(q_pos, torch.int32), q_pos.numel(), _ptr(blocks, torch.int32, "blocks"),
+                                  _ptr(count, torch.int32, "count"), *_ws_args(ws), _stream(stream)),
+           "qsa_topk_blocks")
+
+
+def qsa_sparse_decode(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out, lse, ws, stream=None):
+    _check(load().qsa_sparse_decode(C.byref(cfg), _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k"),
+                                    _ptr(v_cache, torch.bfloat16, "v"), k_cache.shape[0], _ptr(tok_off, torch.int32),
+                                    _ptr(ctx_len, torch.int32), ctx_len.numel(), _ptr(blocks, torch.int32),
+                                    _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
+                                    _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _stream(stream)),
+           "qsa_sparse_decode")
+
+
+def qsa_sparse_prefill_chunk(cfg, q, p0, k_cache, v_cache, blocks, count, interval_tokens, out, lse, ws,
+                             stream=None):
+    _check(load().qsa_sparse_prefill_chunk(C.byref(cfg), _ptr(q, torch.bfloat16, "q"), int(p0), q.shape[0],
+                                           _ptr(k_cache, torch.bfloat16, "k"), _ptr(v_cache, torch.bfloat16, "v"),
+                                           _ptr(blocks, torch.int32), _ptr(count, torch.int32), int(interval_tokens),
+                                           _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                                           *_ws_args(ws), _stream(stream)), "qsa_sparse_prefill_chunk")
+
+
+def version() -> str:
+    return load().qsa_version().decode()

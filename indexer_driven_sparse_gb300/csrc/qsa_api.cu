@@ -1,0 +1,272 @@
+// extern "C" entry points of libqsa.so: host-side validation, workspace layout and
+// launch on the caller's stream. No allocation and no synchronisation happen here
+// (except qsa_read_device_status, which synchronises by design).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "qsa_internal.cuh"
+
+using namespace qsa;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+qsa_status fail(qsa_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+qsa_status ok() {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+}
+
+qsa_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(QSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qsa_status check_config(const qsa_config *c) {
+    if (c == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "config is NULL");
+    if (c->head_dim != kHeadDim) return fail(QSA_ERR_UNSUPPORTED, "head_dim %d (only 256)", c->head_dim);
+    if (c->idx_dim != kIdxDim) return fail(QSA_ERR_UNSUPPORTED, "idx_dim %d (only 128)", c->idx_dim);
+    if (c->indexer_compress_ratio != kRatio)
+        return fail(QSA_ERR_UNSUPPORTED, "indexer_compress_ratio %d (only 4)", c->indexer_compress_ratio);
+    if (c->indexer_budget != kRatio * kBlockTopK)
+        return fail(QSA_ERR_UNSUPPORTED, "indexer_budget %d (only 2048)", c->indexer_budget);
+    if (c->n_kv_heads < 1 || c->n_q_heads < 1)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "head counts must be positive (%d, %d)", c->n_q_heads, c->n_kv_heads);
+    if (c->n_q_heads % c->n_kv_heads != 0)
+        return fail(QSA_ERR_UNSUPPORTED, "n_q_heads %d not a multiple of n_kv_heads %d", c->n_q_heads, c->n_kv_heads);
+    const int g = c->n_q_heads / c->n_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16)
+        return fail(QSA_ERR_UNSUPPORTED, "query heads per KV head %d (1, 2, 4, 8 or 16)", g);
+    if (c->n_q_heads * (int64_t)kHeadDim > (1 << 20)) return fail(QSA_ERR_UNSUPPORTED, "too many heads");
+    if (!(c->softmax_scale <= 0.f) && !isfinite(c->softmax_scale))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "softmax_scale must be finite");
+    return QSA_OK;
+}
+
+float scale_of(const qsa_config *c) {
+    return c->softmax_scale > 0.f ? c->softmax_scale : 1.0f / sqrtf((float)c->head_dim);
+}
+
+size_t ws_size(int32_t op, const qsa_config *c, int32_t n_rows, int64_t max_blocks) {
+    if (n_rows < 0 || max_blocks < 0) return 0;
+    switch (op) {
+        case QSA_OP_POOL_KEYS:
+        case QSA_OP_INDEX_SCORE: return kWsHeaderBytes;
+        case QSA_OP_TOPK_BLOCKS: return kWsHeaderBytes + topk_scratch_bytes(n_rows, max_blocks);
+        case QSA_OP_SPARSE_DECODE: return kWsHeaderBytes + decode_scratch_bytes(n_rows, c->n_q_heads, c->n_kv_heads);
+        case QSA_OP_SPARSE_PREFILL_CHUNK:
+            return kWsHeaderBytes + prefill_scratch_bytes(n_rows, c->n_q_heads, c->n_kv_heads);
+        default: return 0;
+    }
+}
+
+qsa_status check_ws(int32_t op, const qsa_config *c, int32_t n_rows, int64_t max_blocks, void *ws, size_t bytes) {
+    if (ws == nullptr) return fail(QSA_ERR_INVALID_ARGUMENT, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(QSA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+    const size_t need = ws_size(op, c, n_rows, max_blocks);
+    if (bytes < need) return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", bytes, need);
+    return QSA_OK;
+}
+
+#define QSA_TRY(expr)                         \
+    do {                                      \
+        const qsa_status _s = (expr);         \
+        if (_s != QSA_OK) return _s;          \
+    } while (0)
+
+#define QSA_NEED(cond, ...)                                           \
+    do {                                                              \
+        if (!(cond)) return fail(QSA_ERR_INVALID_ARGUMENT, __VA_ARGS__); \
+    } while (0)
+
+constexpr int kMaxGridYZ = 65535;
+
+}  // namespace
+
+extern "C" {
+
+QSA_API size_t qsa_workspace_size(int32_t op, const qsa_config *cfg, int32_t n_rows, int64_t max_blocks) {
+    if (check_config(cfg) != QSA_OK) return 0;
+    return ws_size(op, cfg, n_rows, max_blocks);
+}
+
+QSA_API qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_NEED(ws != nullptr, "workspace is NULL");
+    QSA_NEED(ws_bytes >= kWsHeaderBytes, "workspace smaller than its 256-byte status block");
+    const cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    return ok();
+}
+
+QSA_API qsa_status qsa_read_device_status(const void *ws, qsa_stream stream, qsa_status *out, int32_t *detail) {
+    QSA_NEED(ws != nullptr && out != nullptr, "workspace and out must be non-NULL");
+    int32_t h[3] = {0, 0, 0};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy status");
+    *out = static_cast<qsa_status>(h[0]);
+    if (detail != nullptr) *detail = h[1];
+    return ok();
+}
+
+QSA_API qsa_status qsa_pool_keys(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, int64_t n_tokens_total,
+                                 const int32_t *tok_off, const int32_t *blk_off, const int32_t *blk_begin,
+                                 const int32_t *blk_end, int32_t B, int64_t max_blocks_per_seq, qsa_bf16 *pooled,
+                                 int64_t n_pooled_total, void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(B >= 0 && B <= kMaxGridYZ, "B = %d out of range [0, 65535]", B);
+    QSA_NEED(n_tokens_total >= 0 && n_pooled_total >= 0 && max_blocks_per_seq >= 0, "negative size");
+    QSA_NEED(max_blocks_per_seq <= (int64_t)1 << 28, "max_blocks_per_seq too large");
+    QSA_TRY(check_ws(QSA_OP_POOL_KEYS, cfg, B, max_blocks_per_seq, ws, ws_bytes));
+    if (B == 0 || max_blocks_per_seq == 0) return ok();
+    QSA_NEED(raw_idx_k && pooled && tok_off && blk_off && blk_begin && blk_end, "NULL tensor pointer");
+    QSA_NEED(aligned(raw_idx_k, 16) && aligned(pooled, 16), "raw_idx_k and pooled must be 16-byte aligned");
+    const cudaError_t e = launch_pool_keys(raw_idx_k, n_tokens_total, tok_off, blk_off, blk_begin, blk_end, B,
+                                           max_blocks_per_seq, pooled, n_pooled_total,
+                                           static_cast<WsHeader *>(ws), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pool_keys launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_seq,
+                                   const int32_t *q_pos, int32_t Nq, const qsa_bf16 *pooled, int64_t n_pooled_total,
+                                   const int32_t *blk_off, float *scores, int64_t ld, void *ws, size_t ws_bytes,
+                                   qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(Nq >= 0 && Nq <= kMaxGridYZ, "Nq = %d out of range [0, 65535]", Nq);
+    QSA_NEED(ld >= 0 && n_pooled_total >= 0, "negative size");
+    QSA_NEED(ld <= (int64_t)1 << 28, "ld too large");
+    QSA_TRY(check_ws(QSA_OP_INDEX_SCORE, cfg, Nq, ld, ws, ws_bytes));
+    if (Nq == 0 || ld == 0) return ok();
+    QSA_NEED(q_idx && q_seq && q_pos && pooled && blk_off && scores, "NULL tensor pointer");
+    QSA_NEED(aligned(q_idx, 16) && aligned(pooled, 16), "q_idx and pooled must be 16-byte aligned");
+    QSA_NEED(aligned(scores, 4), "scores must be 4-byte aligned");
+    const cudaError_t e = launch_index_score(q_idx, q_seq, q_pos, Nq, pooled, n_pooled_total, blk_off, scores, ld,
+                                             static_cast<WsHeader *>(ws), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "index_score launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_topk_blocks(const qsa_config *cfg, const float *scores, int64_t ld, const int32_t *q_pos,
+                                   int32_t Nq, int32_t *blocks, int32_t *count, void *ws, size_t ws_bytes,
+                                   qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(Nq >= 0 && Nq <= (1 << 30), "Nq = %d out of range", Nq);
+    QSA_NEED(ld >= 0 && ld <= (int64_t)1 << 28, "ld out of range");
+    QSA_TRY(check_ws(QSA_OP_TOPK_BLOCKS, cfg, Nq, ld, ws, ws_bytes));
+    if (Nq == 0) return ok();
+    QSA_NEED(scores && q_pos && blocks && count, "NULL tensor pointer");
+    char *w = static_cast<char *>(ws);
+    const cudaError_t e = launch_topk_blocks(scores, ld, q_pos, Nq, blocks, count, reinterpret_cast<WsHeader *>(w),
+                                             w + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "topk_blocks launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_sparse_decode(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                     const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
+                                     const int32_t *ctx_len, int32_t B, const int32_t *blocks, const int32_t *count,
+                                     qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(B >= 0 && B <= kMaxGridYZ, "B = %d out of range [0, 65535]", B);
+    QSA_NEED(n_tokens_total >= 0, "negative size");
+    QSA_TRY(check_ws(QSA_OP_SPARSE_DECODE, cfg, B, 0, ws, ws_bytes));
+    if (B == 0) return ok();
+    QSA_NEED(q && k_cache && v_cache && tok_off && ctx_len && blocks && count && out, "NULL tensor pointer");
+    QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16),
+             "q, k_cache, v_cache and out must be 16-byte aligned");
+    char *w = static_cast<char *>(ws);
+    AttnArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.n_tok = n_tokens_total;
+    a.tok_off = tok_off;
+    a.ctx_len = ctx_len;
+    a.p0 = 0;
+    a.rows = B;
+    a.blocks = blocks;
+    a.count = count;
+    a.out = out;
+    a.lse = lse;
+    a.n_q_heads = cfg->n_q_heads;
+    a.n_kv_heads = cfg->n_kv_heads;
+    a.scale_log2 = scale_of(cfg) * kLog2e;
+    a.where = kWhereDecode;
+    const cudaError_t e = launch_sparse_decode(a, reinterpret_cast<WsHeader *>(w), w + kWsHeaderBytes,
+                                               ws_bytes - kWsHeaderBytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_decode launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
+                                            const qsa_bf16 *k_cache, const qsa_bf16 *v_cache, const int32_t *blocks,
+                                            const int32_t *count, int32_t interval_tokens, qsa_bf16 *out, float *lse,
+                                            void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(p0 >= 0 && Nc >= 0 && Nc <= kMaxGridYZ, "p0 = %d / Nc = %d out of range", p0, Nc);
+    QSA_NEED((int64_t)p0 + Nc <= INT32_MAX, "p0 + Nc overflows int32");
+    QSA_NEED(interval_tokens > 0 && interval_tokens % 128 == 0,
+             "interval_tokens = %d must be a positive multiple of 128", interval_tokens);
+    QSA_TRY(check_ws(QSA_OP_SPARSE_PREFILL_CHUNK, cfg, Nc, 0, ws, ws_bytes));
+    if (Nc == 0) return ok();
+    QSA_NEED(q && k_cache && v_cache && blocks && count && out, "NULL tensor pointer");
+    QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16),
+             "q, k_cache, v_cache and out must be 16-byte aligned");
+    char *w = static_cast<char *>(ws);
+    AttnArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.n_tok = (int64_t)p0 + Nc;
+    a.tok_off = nullptr;
+    a.ctx_len = nullptr;
+    a.p0 = p0;
+    a.rows = Nc;
+    a.blocks = blocks;
+    a.count = count;
+    a.out = out;
+    a.lse = lse;
+    a.n_q_heads = cfg->n_q_heads;
+    a.n_kv_heads = cfg->n_kv_heads;
+    a.scale_log2 = scale_of(cfg) * kLog2e;
+    a.where = kWherePrefill;
+    const cudaError_t e = launch_sparse_prefill(a, interval_tokens, reinterpret_cast<WsHeader *>(w),
+                                                w + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
+                                                static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_prefill_chunk launch");
+    return ok();
+}
+
+QSA_API const char *qsa_status_string(qsa_status s) {
+    switch (s) {
+        case QSA_OK: return "ok";
+        case QSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case QSA_ERR_UNSUPPORTED: return "unsupported geometry";
+        case QSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case QSA_ERR_CUDA: return "CUDA error";
+        case QSA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case QSA_ERR_DEVICE_BOUNDS: return "device-side bounds check failed";
+        default: return "unknown status";
+    }
+}
+
+QSA_API const char *qsa_last_error(void) { return g_last_error; }
+
+QSA_API const char *qsa_version(void) { return "qsa-gb300 0.1.0 sm_103a"; }
+
+}  // extern "C"

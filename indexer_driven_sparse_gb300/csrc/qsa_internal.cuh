@@ -1,0 +1,119 @@
+// Internal declarations shared by the CUDA translation units of libqsa.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "qsa.h"
+
+namespace qsa {
+
+constexpr int kHeadDim = 256;
+constexpr int kIdxDim = 128;
+constexpr int kRatio = 4;
+constexpr int kBlockTopK = 512;              // indexer_budget / ratio
+constexpr int kMaxGroup = 16;                // max query heads per KV head
+constexpr int kMaxAttended = kRatio * kBlockTopK + kRatio;   // 2052 = 2048 selected + own block
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// First 256 bytes of every workspace.
+struct WsHeader {
+    int32_t status;      // first device-side error (qsa_status), 0 = none
+    int32_t detail;      // kernel-specific detail (row, index)
+    int32_t where;       // which kernel recorded it
+    int32_t pad0;
+    uint32_t sem[60];    // self-resetting counters (last-CTA-done, grid barriers)
+};
+static_assert(sizeof(WsHeader) == 256, "status block must be 256 bytes");
+constexpr size_t kWsHeaderBytes = 256;
+
+enum Where : int32_t {
+    kWherePool = 1, kWhereScore = 2, kWhereTopk = 3, kWhereDecode = 4, kWhereMerge = 5, kWherePrefill = 6,
+};
+
+__device__ __forceinline__ void record_error(WsHeader *h, int32_t code, int32_t where, int32_t detail) {
+    if (h == nullptr) return;
+    if (atomicCAS(&h->status, 0, code) == 0) {
+        h->detail = detail;
+        h->where = where;
+    }
+}
+
+// bf16 bits -> float (exact).
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// Unpack 8 bf16 values from a 16-byte vector.
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+    f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// Read-only 16-byte global load that does not allocate in L1.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// fp32 -> bf16 bits, round to nearest even (CUDA intrinsic).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Order-preserving map of an fp32 score to uint32: larger score -> larger key.
+// -0 is folded onto +0 and NaN onto the smallest key.
+__device__ __forceinline__ uint32_t score_key(float s) {
+    uint32_t u = __float_as_uint(s);
+    if (u == 0x80000000u) u = 0u;
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------- launchers
+// Each returns cudaGetLastError() of its launches.
+cudaError_t launch_pool_keys(const uint16_t *raw, int64_t n_tok, const int32_t *tok_off, const int32_t *blk_off,
+                             const int32_t *blk_begin, const int32_t *blk_end, int B, int64_t max_blocks,
+                             uint16_t *pooled, int64_t n_pooled, WsHeader *hdr, cudaStream_t st);
+
+cudaError_t launch_index_score(const uint16_t *q_idx, const int32_t *q_seq, const int32_t *q_pos, int Nq,
+                               const uint16_t *pooled, int64_t n_pooled, const int32_t *blk_off, float *scores,
+                               int64_t ld, WsHeader *hdr, cudaStream_t st);
+
+size_t topk_scratch_bytes(int Nq, int64_t ld);
+cudaError_t launch_topk_blocks(const float *scores, int64_t ld, const int32_t *q_pos, int Nq, int32_t *blocks,
+                               int32_t *count, WsHeader *hdr, void *scratch, size_t scratch_bytes, cudaStream_t st);
+
+struct AttnArgs {
+    const uint16_t *q;        // [rows, Hq, D]
+    const uint16_t *k_cache;  // [T, Hkv, D]
+    const uint16_t *v_cache;
+    int64_t n_tok;
+    const int32_t *tok_off;   // decode: [B+1]; prefill: nullptr (one sequence from token 0)
+    const int32_t *ctx_len;   // decode: [B]; prefill: nullptr (p = p0 + row)
+    int32_t p0;
+    int32_t rows;
+    const int32_t *blocks;    // [rows, kBlockTopK]
+    const int32_t *count;     // [rows]
+    uint16_t *out;            // [rows, Hq, D]
+    float *lse;               // [rows, Hq] or nullptr
+    int32_t n_q_heads, n_kv_heads;
+    float scale_log2;         // softmax scale * log2(e)
+    int32_t where;
+};
+size_t decode_scratch_bytes(int B, int Hq, int Hkv);
+cudaError_t launch_sparse_decode(const AttnArgs &a, WsHeader *hdr, void *scratch, size_t scratch_bytes,
+                                 cudaStream_t st);
+
+// One CTA per (row, KV head) over the row's whole token set (no split partials).
+cudaError_t launch_attn_rows(const AttnArgs &a, WsHeader *hdr, cudaStream_t st);
+
+size_t prefill_scratch_bytes(int Nc, int Hq, int Hkv);
+cudaError_t launch_sparse_prefill(const AttnArgs &a, int interval_tokens, WsHeader *hdr, void *scratch,
+                                  size_t scratch_bytes, cudaStream_t st);
+
+}  // namespace qsa

@@ -1,0 +1,147 @@
+"""Device buffers and call sequences for one decode layer-step or one prefill chunk.
+
+Only marshalling: torch allocates the buffers and the metadata tensors, and every
+step of the path runs in libqsa.so through the ``qsa_*`` calls of :mod:`.binding`.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding as qb
+
+RATIO = 4
+
+
+class DecodeBatch:
+    """A ragged decode batch: sequence s has its query at p = ctx_len[s] and p + 1
+    cached tokens at tok_off[s] .. tok_off[s+1]-1 of the flat K/V arrays."""
+
+    def __init__(self, n_q_heads: int, n_kv_heads: int, ctx_len, device="cuda", softmax_scale: float = 0.0):
+        self.cfg = qb.make_config(n_q_heads, n_kv_heads, softmax_scale=softmax_scale)
+        self.ctx = [int(p) for p in ctx_len]
+        self.B = len(self.ctx)
+        self.device = device
+        i32 = dict(dtype=torch.int32, device=device)
+        tok_off, blk_off, nblk = [0], [0], []
+        for p in self.ctx:
+            tok_off.append(tok_off[-1] + p + 1)
+            nblk.append((p + 1) // RATIO)          # complete blocks among the p+1 cached tokens
+            blk_off.append(blk_off[-1] + nblk[-1])
+        self.n_tokens = tok_off[-1]
+        self.n_pooled = blk_off[-1]
+        self.max_blocks = max(nblk) if nblk else 0
+        self.ld = max(1, max((p // RATIO for p in self.ctx), default=1))
+        self.tok_off = torch.tensor(tok_off, **i32)
+        self.blk_off = torch.tensor(blk_off, **i32)
+        self.ctx_len = torch.tensor(self.ctx, **i32)
+        self.q_seq = torch.arange(self.B, **i32)
+        self.blk_begin = torch.zeros(self.B, **i32)
+        self.blk_end = torch.tensor(nblk, **i32)
+        self.scores = torch.empty(self.B, self.ld, dtype=torch.float32, device=device)
+        self.blocks = torch.empty(self.B, qb.BLOCK_TOPK, **i32)
+        self.count = torch.empty(self.B, **i32)
+        self.out = torch.empty(self.B, n_q_heads, 256, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(self.B, n_q_heads, dtype=torch.float32, device=device)
+        sizes = [qb.workspace_size(qb.OP_POOL_KEYS, self.cfg, self.B, self.max_blocks),
+                 qb.workspace_size(qb.OP_INDEX_SCORE, self.cfg, self.B, self.ld),
+                 qb.workspace_size(qb.OP_TOPK_BLOCKS, self.cfg, self.B, self.ld),
+                 qb.workspace_size(qb.OP_SPARSE_DECODE, self.cfg, self.B, self.ld)]
+        self.ws = _workspace(max(sizes), device)
+
+    def new_pooled(self):
+        return torch.empty(max(self.n_pooled, 1), 128, dtype=torch.bfloat16, device=self.device)
+
+    def pool(self, raw_idx_k, pooled, stream=None):
+        qb.qsa_pool_keys(self.cfg, raw_idx_k, self.tok_off, self.blk_off, self.blk_begin, self.blk_end,
+                         self.max_blocks, pooled, self.ws, stream)
+
+    def score(self, q_idx, pooled, stream=None):
+        qb.qsa_index_score(self.cfg, q_idx, self.q_seq, self.ctx_len, pooled, self.blk_off, self.scores, self.ws,
+                           stream)
+
+    def topk(self, stream=None):
+        qb.qsa_topk_blocks(self.cfg, self.scores, self.ctx_len, self.blocks, self.count, self.ws, stream)
+
+    def attend(self, q, k_cache, v_cache, blocks=None, count=None, stream=None):
+        qb.qsa_sparse_decode(self.cfg, q, k_cache, v_cache, self.tok_off, self.ctx_len,
+                             self.blocks if blocks is None else blocks, self.count if count is None else count,
+                             self.out, self.lse, self.ws, stream)
+
+    def step(self, q_idx, q, k_cache, v_cache, pooled, stream=None):
+        """One decode layer-step: score -> top-k -> sparse attention + LSE merge."""
+        self.score(q_idx, pooled, stream)
+        self.topk(stream)
+        self.attend(q, k_cache, v_cache, stream=stream)
+
+    def device_status(self, stream=None):
+        return qb.qsa_read_device_status(self.ws, stream)
+
+
+class PrefillChunk:
+    """A chunk of Nc queries at positions p0 .. p0+Nc-1 of one sequence whose cache
+    holds p0 + Nc tokens (the chunk's K/V already appended)."""
+
+    def __init__(self, n_q_heads: int, n_kv_heads: int, p0: int, n_chunk: int, interval_tokens: int = 8192,
+                 device="cuda", softmax_scale: float = 0.0):
+        self.cfg = qb.make_config(n_q_heads, n_kv_heads, softmax_scale=softmax_scale)
+        self.p0, self.Nc, self.interval = int(p0), int(n_chunk), int(interval_tokens)
+        self.device = device
+        i32 = dict(dtype=torch.int32, device=device)
+        self.n_tokens = self.p0 + self.Nc
+        self.n_pooled = self.n_tokens // RATIO
+        self.ld = max(1, (self.p0 + self.Nc - 1) // RATIO)
+        self.tok_off = torch.tensor([0, self.n_tokens], **i32)
+        self.blk_off = torch.zeros(2, **i32)
+        self.q_seq = torch.zeros(self.Nc, **i32)
+        self.q_pos = torch.arange(self.p0, self.p0 + self.Nc, **i32)
+        self.scores = torch.empty(self.Nc, self.ld, dtype=torch.float32, device=device)
+        self.blocks = torch.empty(self.Nc, qb.BLOCK_TOPK, **i32)
+        self.count = torch.empty(self.Nc, **i32)
+        self.out = torch.empty(self.Nc, n_q_heads, 256, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(self.Nc, n_q_heads, dtype=torch.float32, device=device)
+        sizes = [qb.workspace_size(qb.OP_POOL_KEYS, self.cfg, 1, self.n_pooled),
+                 qb.workspace_size(qb.OP_INDEX_SCORE, self.cfg, self.Nc, self.ld),
+                 qb.workspace_size(qb.OP_TOPK_BLOCKS, self.cfg, self.Nc, self.ld),
+                 qb.workspace_size(qb.OP_SPARSE_PREFILL_CHUNK, self.cfg, self.Nc, self.ld)]
+        self.ws = _workspace(max(sizes), device)
+
+    def new_pooled(self):
+        return torch.empty(max(self.n_pooled, 1), 128, dtype=torch.bfloat16, device=self.device)
+
+    def pool(self, raw_idx_k, pooled, first_block: int = 0, stream=None):
+        """Pool blocks [first_block, (p0+Nc)//4) (the whole history, or just the chunk's)."""
+        i32 = dict(dtype=torch.int32, device=self.device)
+        qb.qsa_pool_keys(self.cfg, raw_idx_k, self.tok_off, self.blk_off, torch.tensor([first_block], **i32),
+                         torch.tensor([self.n_pooled], **i32), max(0, self.n_pooled - first_block), pooled, self.ws,
+                         stream)
+
+    def score(self, q_idx, pooled, stream=None):
+        qb.qsa_index_score(self.cfg, q_idx, self.q_seq, self.q_pos, pooled, self.blk_off, self.scores, self.ws,
+                           stream)
+
+    def topk(self, stream=None):
+        qb.qsa_topk_blocks(self.cfg, self.scores, self.q_pos, self.blocks, self.count, self.ws, stream)
+
+    def attend(self, q, k_cache, v_cache, blocks=None, count=None, stream=None):
+        qb.qsa_sparse_prefill_chunk(self.cfg, q, self.p0, k_cache, v_cache,
+                                    self.blocks if blocks is None else blocks,
+                                    self.count if count is None else count, self.interval, self.out, self.lse,
+                                    self.ws, stream)
+
+    def run(self, q_idx, q, k_cache, v_cache, pooled, stream=None):
+        """The chunk's path after pooling: score -> top-k -> interval-walk attention."""
+        self.score(q_idx, pooled, stream)
+        self.topk(stream)
+        self.attend(q, k_cache, v_cache, stream=stream)
+
+    def device_status(self, stream=None):
+        return qb.qsa_read_device_status(self.ws, stream)
+
+
+def _workspace(nbytes: int, device):
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + nbytes]
+    qb.qsa_workspace_init(ws)
+    return ws

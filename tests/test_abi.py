@@ -1,0 +1,125 @@
+"""The C-ABI library loads, exports every declared symbol and validates arguments on
+the host (no kernel is launched and no GPU is needed)."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from indexer_driven_sparse_gb300 import binding as qb
+from indexer_driven_sparse_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qb.load()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+            names |= set(re.findall(r"QSA_API\s+[\w\s\*]+?\b(qsa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 11
+    for n in ["qsa_pool_keys", "qsa_index_score", "qsa_topk_blocks", "qsa_sparse_decode",
+              "qsa_sparse_prefill_chunk"]:
+        assert n in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_only_declared_symbols_are_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", qbuild.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("qsa_")}
+    assert exported == set(declared_symbols())
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in qb.version()
+    for s in range(7):
+        assert lib.qsa_status_string(s)
+    assert lib.qsa_status_string(99) == b"unknown status"
+
+
+def cfg(**kw):
+    base = dict(n_q_heads=16, n_kv_heads=2)
+    base.update(kw)
+    return qb.make_config(**base)
+
+
+def test_workspace_size(lib):
+    c = cfg()
+    assert lib.qsa_workspace_size(qb.OP_POOL_KEYS, C.byref(c), 1, 10) == 256
+    dec = lib.qsa_workspace_size(qb.OP_SPARSE_DECODE, C.byref(c), 32, 0)
+    assert dec >= 256 + 32 * 2 * 8 * 4
+    assert lib.qsa_workspace_size(qb.OP_SPARSE_DECODE, C.byref(cfg(head_dim=128)), 32, 0) == 0
+    assert lib.qsa_workspace_size(99, C.byref(c), 1, 1) == 0
+    assert lib.qsa_workspace_size(qb.OP_TOPK_BLOCKS, C.byref(c), -1, 1) == 0
+
+
+FAKE = 0x10000000  # never dereferenced: validation fails or returns before any launch
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(head_dim=128), qb.QSA_ERR_UNSUPPORTED),
+    (dict(idx_dim=64), qb.QSA_ERR_UNSUPPORTED),
+    (dict(ratio=8), qb.QSA_ERR_UNSUPPORTED),
+    (dict(budget=1024), qb.QSA_ERR_UNSUPPORTED),
+    (dict(n_q_heads=12, n_kv_heads=8), qb.QSA_ERR_UNSUPPORTED),
+    (dict(n_q_heads=96, n_kv_heads=2), qb.QSA_ERR_UNSUPPORTED),
+    (dict(n_kv_heads=0), qb.QSA_ERR_INVALID_ARGUMENT),
+])
+def test_bad_config_rejected(lib, bad, code):
+    c = cfg(**bad)
+    st = lib.qsa_sparse_decode(C.byref(c), FAKE, FAKE, FAKE, 100, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 0, FAKE, 1 << 20, 0)
+    assert st == code
+    assert lib.qsa_last_error()
+
+
+def test_argument_validation(lib):
+    c = cfg()
+    # NULL config
+    assert lib.qsa_topk_blocks(None, FAKE, 10, FAKE, 1, FAKE, FAKE, FAKE, 1 << 20, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    # NULL / misaligned / too-small workspace
+    assert lib.qsa_topk_blocks(C.byref(c), FAKE, 10, FAKE, 1, FAKE, FAKE, 0, 1 << 20, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_topk_blocks(C.byref(c), FAKE, 10, FAKE, 1, FAKE, FAKE, FAKE + 8, 1 << 20, 0) == \
+        qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_sparse_decode(C.byref(c), FAKE, FAKE, FAKE, 100, FAKE, FAKE, 4, FAKE, FAKE, FAKE, 0, FAKE, 256,
+                                 0) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    # NULL tensors
+    assert lib.qsa_sparse_decode(C.byref(c), 0, FAKE, FAKE, 100, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 0, FAKE, 1 << 20,
+                                 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    # misaligned K
+    assert lib.qsa_sparse_decode(C.byref(c), FAKE, FAKE + 2, FAKE, 100, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 0, FAKE,
+                                 1 << 20, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    # negative / out-of-range sizes
+    assert lib.qsa_index_score(C.byref(c), FAKE, FAKE, FAKE, -1, FAKE, 10, FAKE, FAKE, 10, FAKE, 256, 0) == \
+        qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_pool_keys(C.byref(c), FAKE, 100, FAKE, FAKE, FAKE, FAKE, 70000, 4, FAKE, 25, FAKE, 256, 0) == \
+        qb.QSA_ERR_INVALID_ARGUMENT
+    # prefill interval must be a positive multiple of 128
+    for iv in (0, -128, 100):
+        assert lib.qsa_sparse_prefill_chunk(C.byref(c), FAKE, 0, 16, FAKE, FAKE, FAKE, FAKE, iv, FAKE, 0, FAKE,
+                                            1 << 20, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"interval" in lib.qsa_last_error()
+
+
+def test_empty_batches_are_no_ops(lib):
+    c = cfg()
+    ws = FAKE
+    assert lib.qsa_pool_keys(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
+    assert lib.qsa_index_score(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
+    assert lib.qsa_topk_blocks(C.byref(c), 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
+    assert lib.qsa_sparse_decode(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
+    assert lib.qsa_sparse_prefill_chunk(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 8192, 0, 0, ws, 256, 0) == qb.QSA_OK

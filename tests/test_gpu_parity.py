@@ -1,0 +1,299 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Small cases cover several tiles and ragged tails; the full-size workloads (long and
+million-token decode, the prefill chunk) are checked on sampled rows that the oracle
+computes one by one.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from indexer_driven_sparse_gb300 import binding as qb
+from indexer_driven_sparse_gb300 import inputs as I
+from indexer_driven_sparse_gb300.pipeline import DecodeBatch, PrefillChunk
+from parity import bits, check_attention, check_selection
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _to(layer, device=DEV):
+    return I.Layer(*(getattr(layer, f).to(device) for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))
+
+
+def _assert_status_ok(obj):
+    st, det = obj.device_status()
+    assert st == 0, f"device status {st} detail {det}"
+
+
+# ----------------------------------------------------------------------------- pooling
+
+def test_pool_keys_bit_exact(cuda_lib):
+    g = torch.Generator().manual_seed(0)
+    lens = [0, 1, 3, 4, 7, 8, 1023, 4097, 64]
+    T = sum(lens)
+    raw = (torch.randn(T, 128, generator=g) / math.sqrt(128)).to(torch.bfloat16)
+    t0 = sum(lens[:8])
+    # last sequence: planted rounding cases (ties, spread exponents, subnormals)
+    one, up = 1.0, 1.0 + 2 ** -7
+    raw[t0:t0 + 4, :] = torch.tensor([one, up, one, up]).repeat_interleave(1).view(4, 1).to(torch.bfloat16)
+    raw[t0 + 4:t0 + 8, :] = torch.tensor([1e-3, 1e3, -1e3, 7.0]).view(4, 1).to(torch.bfloat16)
+    raw[t0 + 8:t0 + 12, :] = torch.tensor([2 ** -130, 2 ** -131, 0.0, -2 ** -133]).view(4, 1).to(torch.bfloat16)
+    raw[t0 + 12:t0 + 16, :] = torch.tensor([3e38, 3e38, 3e38, 3.3e38]).view(4, 1).to(torch.bfloat16)
+    nblk = [n // 4 for n in lens]
+    tok_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    blk_off = np.concatenate([[0], np.cumsum(nblk)]).astype(np.int32)
+    cfg = qb.make_config(8, 2)
+    ws = qb.make_workspace(qb.OP_POOL_KEYS, cfg, len(lens), max(nblk))
+    pooled = torch.full((blk_off[-1], 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dev = lambda a: torch.tensor(a, dtype=torch.int32, device=DEV)
+    qb.qsa_pool_keys(cfg, raw.to(DEV), dev(tok_off), dev(blk_off), dev([0] * len(lens)), dev(nblk), max(nblk),
+                     pooled, ws)
+    assert qb.qsa_read_device_status(ws)[0] == 0
+    got = bits(pooled)
+    rb = bits(raw)
+    for s in range(len(lens)):
+        want = O.pool_keys(rb[tok_off[s]:tok_off[s + 1]])
+        assert np.array_equal(got[blk_off[s]:blk_off[s + 1]], want), s
+    # incremental: only the last block of each sequence, into a fresh buffer
+    pooled2 = torch.zeros_like(pooled)
+    begin = [max(0, n - 1) for n in nblk]
+    qb.qsa_pool_keys(cfg, raw.to(DEV), dev(tok_off), dev(blk_off), dev(begin), dev(nblk), 1, pooled2, ws)
+    got2 = bits(pooled2)
+    for s in range(len(lens)):
+        if nblk[s]:
+            r = blk_off[s] + nblk[s] - 1
+            assert np.array_equal(got2[r], got[r])
+            assert not np.any(got2[blk_off[s]:r])
+
+
+# ----------------------------------------------------------------------------- scoring
+
+def test_index_score_within_fp32_bound(cuda_lib):
+    ctx = [0, 3, 4, 5, 2051, 2052, 4096, 10001]
+    w = I.decode_workload("t", ctx, 1, 8, 2, "gaussian", seed=1)
+    L = _to(w.layers[0])
+    b = DecodeBatch(8, 2, ctx)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    b.score(L.q_idx, pooled)
+    _assert_status_ok(b)
+    sc = b.scores.cpu().numpy().astype(np.float64)
+    rb, qb_ = bits(w.layers[0].raw_idx_k), bits(w.layers[0].q_idx)
+    off = w.tok_off
+    for s, p in enumerate(ctx):
+        pk = O.pool_keys(rb[off[s]:off[s + 1]])
+        nb = p // 4
+        want = O.score_blocks(qb_[s], pk[:nb])
+        bound = O.score_error_bound(qb_[s], pk[:nb])
+        assert np.all(np.abs(sc[s, :nb] - want) <= bound + 1e-30), s
+
+
+# ----------------------------------------------------------------------------- top-k
+
+def _topk_case_rows():
+    rng = np.random.default_rng(5)
+    rows = []
+    for nb in [0, 1, 511, 512, 513, 1024]:
+        rows.append(rng.standard_normal(nb).astype(np.float32))
+    rows.append(rng.integers(-3, 4, 5000).astype(np.float32))                   # heavy ties
+    rows.append(np.full(5000, 0.25, np.float32))                                # all equal
+    x = rng.standard_normal(4096).astype(np.float32)
+    x[rng.choice(4096, 40, replace=False)] = np.nan
+    x[rng.choice(4096, 40, replace=False)] = -0.0
+    x[rng.choice(4096, 40, replace=False)] = 0.0
+    x[rng.choice(4096, 7, replace=False)] = np.inf
+    x[rng.choice(4096, 7, replace=False)] = -np.inf
+    rows.append(x)
+    y = (rng.standard_normal(3000) * 1e-30).astype(np.float32)                  # tiny and subnormal scores
+    y[:600] = -y[:600]
+    rows.append(y)
+    rows.append(rng.standard_normal(262080).astype(np.float32))                 # million-token row
+    return rows
+
+
+def test_topk_exact_on_given_scores(cuda_lib):
+    rows = _topk_case_rows()
+    ld = max(len(r) for r in rows)
+    sc = np.zeros((len(rows), ld), np.float32)
+    for i, r in enumerate(rows):
+        sc[i, :len(r)] = r
+    q_pos = [4 * len(r) + (i % 4) for i, r in enumerate(rows)]
+    cfg = qb.make_config(16, 2)
+    ws = qb.make_workspace(qb.OP_TOPK_BLOCKS, cfg, len(rows), ld)
+    blocks = torch.empty(len(rows), 512, dtype=torch.int32, device=DEV)
+    count = torch.empty(len(rows), dtype=torch.int32, device=DEV)
+    qb.qsa_topk_blocks(cfg, torch.tensor(sc, device=DEV), torch.tensor(q_pos, dtype=torch.int32, device=DEV),
+                       blocks, count, ws)
+    assert qb.qsa_read_device_status(ws)[0] == 0
+    bl, ct = blocks.cpu().numpy(), count.cpu().numpy()
+    for i, r in enumerate(rows):
+        want = O.select_blocks(r.astype(np.float64))       # same fp32 values, decided exactly
+        assert ct[i] == len(want), i
+        assert np.array_equal(bl[i, :ct[i]], want), i
+        assert np.all(bl[i, ct[i]:] == -1)
+
+
+# ----------------------------------------------------------------------------- decode
+
+def _run_decode(w, layer=0):
+    L = _to(w.layers[layer])
+    b = DecodeBatch(w.n_q_heads, w.n_kv_heads, w.ctx_len)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    b.step(L.q_idx, L.q, L.k_cache, L.v_cache, pooled)
+    _assert_status_ok(b)
+    return b, pooled
+
+
+def _check_decode(w, b, pooled, layer=0, rows=None):
+    Lh = w.layers[layer]
+    rb, qib, qbits = bits(Lh.raw_idx_k), bits(Lh.q_idx), bits(Lh.q)
+    kb, vb = bits(Lh.k_cache), bits(Lh.v_cache)
+    pooled_gpu = bits(pooled)
+    blocks, count = b.blocks.cpu().numpy(), b.count.cpu().numpy()
+    out, lse = b.out.cpu(), b.lse.cpu().numpy()
+    off = w.tok_off
+    stats = dict(band=0, fp32=0, max_abs=0.0, rel=0.0)
+    for s in (range(w.batch) if rows is None else rows):
+        p = w.ctx_len[s]
+        pk = O.pool_keys(rb[off[s]:off[s + 1]])
+        assert np.array_equal(pooled_gpu[b.blk_off[s].item():b.blk_off[s + 1].item()], pk)
+        nb = p // 4
+        n_band, n_fp32 = check_selection(blocks[s], count[s], qib[s], pk, nb)
+        stats["band"] += n_band
+        stats["fp32"] += n_fp32
+        ref = O.decode_query(p, qib[s], pk, qbits[s], kb[off[s]:off[s + 1]], vb[off[s]:off[s + 1]], w.n_kv_heads,
+                             sel=blocks[s, :count[s]])
+        mx, _, rel = check_attention(out[s], ref["out"])
+        assert np.max(np.abs(lse[s] - ref["lse"])) < 1e-3
+        stats["max_abs"] = max(stats["max_abs"], mx)
+        stats["rel"] = max(stats["rel"], rel)
+    return stats
+
+
+def test_decode_tiny(cuda_lib):
+    w = I.tiny_decode()
+    b, pooled = _run_decode(w)
+    _check_decode(w, b, pooled)
+
+
+def test_decode_tiny_sharp(cuda_lib):
+    w = I.tiny_decode(kind="sharp", seed=3)
+    b, pooled = _run_decode(w)
+    st = _check_decode(w, b, pooled)
+    assert st["rel"] < 1e-2
+
+
+def test_decode_planted_ragged(cuda_lib):
+    ctx = [5000, 2052, 70001, 4, 12345]
+    w = I.decode_workload("planted_ragged", ctx, 1, 16, 2, "planted", seed=4)
+    b, pooled = _run_decode(w)
+    _check_decode(w, b, pooled)
+
+
+def test_decode_batched_short_contexts(cuda_lib):
+    lens = I.batched_ctx_lens(short_draw=True)
+    assert {0, 1, 3, 4, 2050, 2051, 2052, 2055} <= set(lens)
+    w = I.decode_workload("batched_short", lens, 1, 8, 2, "gaussian", seed=0)
+    b, pooled = _run_decode(w)
+    _check_decode(w, b, pooled)
+
+
+def test_decode_given_selection_any_order(cuda_lib):
+    # The attention must not depend on the order of the block list.
+    w = I.decode_workload("perm", [9001], 1, 16, 2, "sharp", seed=9)
+    b, pooled = _run_decode(w)
+    ref_out = b.out.clone()
+    blocks = b.blocks.clone()
+    blocks[0] = blocks[0][torch.randperm(512, device=DEV)]
+    L = _to(w.layers[0])
+    b.attend(L.q, L.k_cache, L.v_cache, blocks=blocks)
+    torch.cuda.synchronize()
+    d = (b.out.float() - ref_out.float()).abs().max().item()
+    assert d <= 2 ** -7
+
+
+def test_device_bounds_error_is_recorded(cuda_lib):
+    # Block id == nb is invalid; the kernel must flag it and skip the access. The id is
+    # chosen so that even an unchecked read would stay inside the K/V buffers.
+    w = I.decode_workload("bad", [9000, 9000], 1, 8, 2, "gaussian", seed=2)
+    b, pooled = _run_decode(w)
+    blocks = b.blocks.clone()
+    blocks[0, 5] = 9000 // 4
+    L = _to(w.layers[0])
+    b.attend(L.q, L.k_cache, L.v_cache, blocks=blocks)
+    st, det = b.device_status()
+    assert st == qb.QSA_ERR_DEVICE_BOUNDS and det == 0
+    qb.qsa_workspace_init(b.ws)
+    assert b.device_status()[0] == 0
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def _run_prefill(w, interval=8192):
+    L = _to(w.layers[0])
+    c = PrefillChunk(w.n_q_heads, w.n_kv_heads, w.ctx_len[0], w.n_chunk, interval)
+    pooled = c.new_pooled()
+    c.pool(L.raw_idx_k, pooled)
+    c.run(L.q_idx, L.q, L.k_cache, L.v_cache, pooled)
+    _assert_status_ok(c)
+    return c, pooled
+
+
+def _check_prefill(w, c, rows):
+    Lh = w.layers[0]
+    rb, qib, qbits = bits(Lh.raw_idx_k), bits(Lh.q_idx), bits(Lh.q)
+    kb, vb = bits(Lh.k_cache), bits(Lh.v_cache)
+    pk = O.pool_keys(rb)
+    blocks, count = c.blocks.cpu().numpy(), c.count.cpu().numpy()
+    out, lse = c.out.cpu(), c.lse.cpu().numpy()
+    for i in rows:
+        p = c.p0 + i
+        check_selection(blocks[i], count[i], qib[i], pk, p // 4)
+        ref = O.decode_query(p, qib[i], pk, qbits[i], kb, vb, w.n_kv_heads, sel=blocks[i, :count[i]])
+        check_attention(out[i], ref["out"])
+        assert np.max(np.abs(lse[i] - ref["lse"])) < 1e-3
+
+
+def test_prefill_small_ragged(cuda_lib):
+    w = I.prefill_workload("prefill_small", 8197, 300, 16, 2, "planted", seed=6)
+    c, _ = _run_prefill(w)
+    _check_prefill(w, c, range(300))
+
+
+def test_prefill_interval_invariance(cuda_lib):
+    w = I.prefill_workload("prefill_iv", 20000, 64, 16, 2, "sharp", seed=8)
+    outs = []
+    for iv in (1024, 8192, 16384):
+        c, _ = _run_prefill(w, iv)
+        outs.append(c.out.float().clone())
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 2 ** -7
+
+
+# ----------------------------------------------------------------------------- full-size workloads, sampled
+
+def test_long_decode_full_size_one_layer(cuda_lib):
+    w = I.long_decode(n_layers=1)
+    b, pooled = _run_decode(w)
+    w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
+    _check_decode(w, b, pooled)
+
+
+def test_million_decode_full_size_one_layer(cuda_lib):
+    w = I.million_decode(n_layers=1)
+    b, pooled = _run_decode(w)
+    w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
+    _check_decode(w, b, pooled)
+
+
+def test_prefill_chunk_full_size_sampled(cuda_lib):
+    w = I.prefill_chunk()
+    c, _ = _run_prefill(w)
+    w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
+    _check_prefill(w, c, [0, 1, 2, 3, 15, 16, 17, 1000, 2047, 4094, 4095])
