@@ -99,7 +99,7 @@ def pool_keys(raw_bits: np.ndarray) -> np.ndarray:
     """
     raw = bf16_bits_to_f64(raw_bits)
     nb = raw.shape[0] // COMPRESS_RATIO
-    r = raw[: nb * COMPRESS_RATIO].reshape(nb, COMPRESS_RATIO, -1)
+    r = raw[: nb * COMPRESS_RATIO].reshape(nb, COMPRESS_RATIO, raw.shape[1])
     s = ((r[:, 0] + r[:, 1]) + r[:, 2]) + r[:, 3]
     return f64_to_bf16_bits(s * 0.25)
 

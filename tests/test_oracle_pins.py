@@ -94,6 +94,11 @@ def test_pool_matches_torch_mean_when_exact():
     assert np.array_equal(got[exact], want[exact])
 
 
+def test_pool_empty_and_short_inputs():
+    for t in range(4):
+        assert O.pool_keys(np.zeros((t, 128), np.uint16)).shape == (0, 128)
+
+
 def test_pool_constant_block_is_itself():
     rng = np.random.default_rng(5)
     row = to_bits(O.bf16_bits_to_f64(O.f64_to_bf16_bits(rng.standard_normal(128))))
