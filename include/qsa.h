@@ -173,6 +173,27 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
                                             qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
                                             qsa_stream stream);
 
+/* Allocation-free variant of qsa_sparse_decode (the pages have no counterpart; this
+ * is a library convenience). Same arguments and result, but no workspace: the split
+ * partials live in a 16 MiB static device array inside the library, for callers that
+ * cannot allocate device memory at all (code running under global-mode stream
+ * capture, plug-in hosts that own all device memory, loops that must not risk an
+ * allocation's implicit synchronisation).
+ *  - Limit: qsa_workspace_size(QSA_OP_SPARSE_DECODE, cfg, B, 0) must not exceed 16 MiB
+ *    (B <= 30 at 16 query / 2 KV heads, B <= 61 at 8 / 2); larger batches return
+ *    QSA_ERR_WORKSPACE_TOO_SMALL with nothing enqueued.
+ *  - The first call on a device resolves the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make it before any stream capture.
+ *  - The array stays resident on every GPU that loads the library until exit.
+ *  - Every call reuses the same array: calls that overlap on the GPU race. Each call
+ *    clears the array's status block on `stream`; device-side bounds errors are not
+ *    reported (the bad access is still skipped). It never calls cudaMalloc/cudaFree. */
+QSA_API qsa_status qsa_sparse_decode_noalloc(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                             const qsa_bf16 *v_cache, int64_t n_tokens_total,
+                                             const int32_t *tok_off, const int32_t *ctx_len, int32_t B,
+                                             const int32_t *blocks, const int32_t *count, qsa_bf16 *out,
+                                             float *lse, qsa_stream stream);
+
 /* Static description of a status code. */
 QSA_API const char *qsa_status_string(qsa_status s);
 

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "qsa_topk_blocks": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "qsa_sparse_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "qsa_sparse_prefill_chunk": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "qsa_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
     "qsa_last_error": (C.c_char_p, []),
     "qsa_version": (C.c_char_p, []),
@@ -171,6 +172,15 @@ def qsa_sparse_decode(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count,
                                     _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
                                     _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _stream(stream)),
            "qsa_sparse_decode")
+
+
+def qsa_sparse_decode_noalloc(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out, lse, stream=None):
+    _check(load().qsa_sparse_decode_noalloc(C.byref(cfg), _ptr(q, torch.bfloat16, "q"),
+                                            _ptr(k_cache, torch.bfloat16, "k"), _ptr(v_cache, torch.bfloat16, "v"),
+                                            k_cache.shape[0], _ptr(tok_off, torch.int32), _ptr(ctx_len, torch.int32),
+                                            ctx_len.numel(), _ptr(blocks, torch.int32), _ptr(count, torch.int32),
+                                            _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                                            _stream(stream)), "qsa_sparse_decode_noalloc")
 
 
 def qsa_sparse_prefill_chunk(cfg, q, p0, k_cache, v_cache, blocks, count, interval_tokens, out, lse, ws,

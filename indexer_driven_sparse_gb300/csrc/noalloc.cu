@@ -1,0 +1,76 @@
+// qsa_sparse_decode_noalloc: the sparse decode of qsa_sparse_decode for callers
+// that cannot allocate device memory. Its split partials live in a fixed
+// file-scope device array instead of a caller workspace.
+//
+// Who needs it: code that runs while a stream is being captured in global mode
+// (where cudaMalloc is illegal), plug-in hosts that own every byte of device memory
+// and hand out none, and latency-critical loops that must not take the implicit
+// device synchronisation an allocation can cause.
+//
+// The array is kNoAllocScratchBytes (16 MiB) and stays resident on every GPU that
+// loads the library until the process exits. The first call on a device looks up
+// the array's device address with cudaGetSymbolAddress (with that device current)
+// and caches it; make that first call before any stream capture. Calls share the
+// array and each call overwrites it, so calls that overlap on the GPU (different
+// streams, or concurrent graphs) race; serialise them.
+#include <atomic>
+#include <mutex>
+
+#include "qsa_internal.cuh"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+std::mutex g_setup_mu;
+std::atomic<void *> g_scratch_addr[kMaxDevices];
+
+// Device address of g_decode_scratch on the current device (set-up on first use).
+qsa_status scratch_address(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return qsa::host_fail(QSA_ERR_CUDA, "cudaGetDevice failed", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return qsa::host_fail(QSA_ERR_UNSUPPORTED, "device ordinal >= 64", "");
+    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        p = g_scratch_addr[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            e = cudaGetSymbolAddress(&p, g_decode_scratch);
+            if (e != cudaSuccess || p == nullptr)
+                return qsa::host_fail(QSA_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed",
+                                      cudaGetErrorString(e));
+            g_scratch_addr[dev].store(p, std::memory_order_release);
+        }
+    }
+    *out = p;
+    return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" QSA_API qsa_status qsa_sparse_decode_noalloc(const qsa_config *cfg, const qsa_bf16 *q,
+                                                        const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                                        int64_t n_tokens_total, const int32_t *tok_off,
+                                                        const int32_t *ctx_len, int32_t B, const int32_t *blocks,
+                                                        const int32_t *count, qsa_bf16 *out, float *lse,
+                                                        qsa_stream stream) {
+    // Geometry errors are reported by qsa_sparse_decode itself (size 0 here).
+    const size_t need = qsa_workspace_size(QSA_OP_SPARSE_DECODE, cfg, B, 0);
+    if (need > kNoAllocScratchBytes)
+        return qsa::host_fail(QSA_ERR_WORKSPACE_TOO_SMALL,
+                              "qsa_sparse_decode_noalloc: this batch needs more scratch than the 16 MiB static array",
+                              "use qsa_sparse_decode with a caller workspace or split the batch");
+    void *scratch = nullptr;
+    const qsa_status s = scratch_address(&scratch);
+    if (s != QSA_OK) return s;
+    // The status block is the only part that must start at zero.
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, qsa::kWsHeaderBytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return qsa::host_fail(QSA_ERR_CUDA, "cudaMemsetAsync of the status block failed",
+                                                cudaGetErrorString(e));
+    return qsa_sparse_decode(cfg, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, blocks, count, out, lse,
+                             scratch, kNoAllocScratchBytes, stream);
+}

@@ -94,6 +94,10 @@ constexpr int kMaxGridYZ = 65535;
 
 }  // namespace
 
+qsa_status qsa::host_fail(qsa_status s, const char *what, const char *detail) {
+    return fail(s, "%s: %s", what, detail);
+}
+
 extern "C" {
 
 QSA_API size_t qsa_workspace_size(int32_t op, const qsa_config *cfg, int32_t n_rows, int64_t max_blocks) {

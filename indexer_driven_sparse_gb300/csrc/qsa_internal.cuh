@@ -113,6 +113,9 @@ cudaError_t launch_sparse_decode(const AttnArgs &a, WsHeader *hdr, void *scratch
 cudaError_t launch_attn_rows(const AttnArgs &a, WsHeader *hdr, cudaStream_t st);
 
 size_t prefill_scratch_bytes(int Nc, int Hq, int Hkv);
+
+// Set the calling thread's qsa_last_error() text to "<what>: <detail>" and return s.
+qsa_status host_fail(qsa_status s, const char *what, const char *detail);
 cudaError_t launch_sparse_prefill(const AttnArgs &a, int interval_tokens, WsHeader *hdr, void *scratch,
                                   size_t scratch_bytes, cudaStream_t st);
 
