@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="fused: qsa_decode_step (one launch per layer-step); separate: the five calls")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -190,10 +192,11 @@ def max_over_ranks(x: float, world: int) -> float:
 class DecodeLayers:
     """12 layers of the million-token decode workload resident in HBM."""
 
-    def __init__(self, n_layers, device):
+    def __init__(self, n_layers, device, fused=True):
         import torch
         from indexer_driven_sparse_gb300 import inputs as I
         from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+        self.fused = fused
         self.w = I.million_decode(seed=0, device=device, n_layers=n_layers)
         self.b = DecodeBatch(16, 2, self.w.ctx_len, device=device)
         self.pooled = []
@@ -216,6 +219,11 @@ class DecodeLayers:
         from indexer_driven_sparse_gb300 import binding as qb
         b, L = self.b, self.w.layers[l]
         rec = (lambda name: events(l, name)) if events else (lambda name: None)
+        if self.fused:
+            rec("step0")
+            b.fused_step(L.raw_idx_k, self.pooled[l], L.q_idx, L.q, L.k_cache, L.v_cache)
+            rec("step1")
+            return
         rec("pool0")
         qb.qsa_pool_keys(b.cfg, L.raw_idx_k, b.tok_off, b.blk_off, self.inc_begin, self.inc_end, 1, self.pooled[l],
                          b.ws)
@@ -278,7 +286,12 @@ def instrumented_kernel_times(dl, stream, steps):
         dl.step(events)
 
     g = capture(body, stream)
-    sums = {"pool": 0.0, "score": 0.0, "topk": 0.0, "attend": 0.0}
+    if dl.fused:
+        spans = {"decode_step": ("step0", "step1")}
+    else:
+        spans = {"pool": ("pool0", "pool1"), "score": ("pool1", "score1"), "topk": ("score1", "topk1"),
+                 "attend": ("topk1", "attend1")}
+    sums = {k: 0.0 for k in spans}
     n_layers = len(dl.w.layers)
     for _ in range(3):
         g.replay()
@@ -287,10 +300,8 @@ def instrumented_kernel_times(dl, stream, steps):
         g.replay()
         torch.cuda.synchronize()
         for l in range(n_layers):
-            sums["pool"] += ev.elapsed_ms(marks[(l, "pool0")], marks[(l, "pool1")])
-            sums["score"] += ev.elapsed_ms(marks[(l, "pool1")], marks[(l, "score1")])
-            sums["topk"] += ev.elapsed_ms(marks[(l, "score1")], marks[(l, "topk1")])
-            sums["attend"] += ev.elapsed_ms(marks[(l, "topk1")], marks[(l, "attend1")])
+            for k, (a, b) in spans.items():
+                sums[k] += ev.elapsed_ms(marks[(l, a)], marks[(l, b)])
     return {k: 1000.0 * v / (steps * n_layers) for k, v in sums.items()}
 
 
@@ -501,12 +512,12 @@ def main(argv=None):
     torch.cuda.set_device(local)
     pk = peaks()
 
-    dl = DecodeLayers(args.layers, "cuda")
+    dl = DecodeLayers(args.layers, "cuda", fused=args.path == "fused")
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         dl.step()                               # eager warm-up, checks status below
     torch.cuda.synchronize()
-    st = dl.b.device_status()
+    st = dl.b.fused_status() if dl.fused else dl.b.device_status()
     if st[0] != 0:
         raise RuntimeError(f"device status {st}")
     g = capture(dl.step, stream)
@@ -523,7 +534,8 @@ def main(argv=None):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"million_decode_ctx{CTX_1M}", "batch": 1, "ctx": CTX_1M, "layers": n_layers,
+        "config": {"workload": f"million_decode_ctx{CTX_1M}", "path": args.path, "batch": 1, "ctx": CTX_1M,
+                   "layers": n_layers,
                    "n_q_heads": 16, "n_kv_heads": 2, "head_dim": 256, "idx_dim": 128, "ratio": 4,
                    "budget": 2048, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (12 x 64 MiB pooled keys + 12 x 2 GiB K/V), no flush"},
@@ -532,14 +544,15 @@ def main(argv=None):
         "clocks": clocks,
         "gpu_launches": None,
     }
-    launches_per_layer = 5                       # pool, score, topk, attention, merge
+    launches_per_layer = 1 if dl.fused else 5    # fused step | pool, score, topk, attention, merge
     line["gpu_launches"] = launches_per_layer * n_layers * args.steps
 
     if not args.no_instrument:
         kt = instrumented_kernel_times(dl, stream, max(5, min(50, args.steps)))
         line["kernel_us"] = kt
         algo = {"score": A.score_scan_bytes(dl.w.ctx_len),
-                "attend": A.kv_read_bytes(A.attended(CTX_1M)) + 2 * 16 * 256 * 2}
+                "attend": A.kv_read_bytes(A.attended(CTX_1M)) + 2 * 16 * 256 * 2,
+                "decode_step": bytes_ls}
         dom = max(kt, key=kt.get)
         if dom in algo:
             ach = algo[dom] / (kt[dom] * 1e-6) / 1e9

@@ -66,7 +66,8 @@ typedef enum {
     QSA_OP_INDEX_SCORE = 1,
     QSA_OP_TOPK_BLOCKS = 2,
     QSA_OP_SPARSE_DECODE = 3,
-    QSA_OP_SPARSE_PREFILL_CHUNK = 4
+    QSA_OP_SPARSE_PREFILL_CHUNK = 4,
+    QSA_OP_DECODE_STEP = 5
 } qsa_op;
 
 /* Geometry. Field names follow the model config the page quotes
@@ -172,6 +173,30 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
                                             const int32_t *blocks, const int32_t *count, int32_t interval_tokens,
                                             qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
                                             qsa_stream stream);
+
+/* a1-a5 fused — one decode layer-step for a batch of B <= 64 sequences in a single
+ * cooperative launch ("なぜ", "VRAM に残す必要があるもの", "カーネルを書き換えずに済む";
+ * LSE merge from "GLM-5.3 最適化 第2部" section DCP). For sequence s with p = ctx_len[s],
+ * nb = p / 4:
+ *   1. pooled[blk_off[s] + nb - 1] is (re)computed from raw_idx_k as in qsa_pool_keys (the
+ *      newest block the query scores; blocks below it must already be pooled);
+ *   2. every block b < nb is scored as in qsa_index_score (fp32 accumulation);
+ *   3. the selection of qsa_topk_blocks is written to blocks[s] (ascending, -1 padded) and
+ *      count[s];
+ *   4. out[s] and lse[s] are computed as in qsa_sparse_decode over that selection.
+ * Arguments have the meaning, layout and alignment they have in those calls.
+ * max_blocks: host upper bound of nb over the batch (sizes the workspace:
+ * qsa_workspace_size(QSA_OP_DECODE_STEP, cfg, B, max_blocks)). Requires n_kv_heads <= 2 and
+ * a batch whose blocks fit the kernel's on-chip limit per CTA (else QSA_ERR_UNSUPPORTED;
+ * use the separate calls then). Device errors (bounds, a bounded wait that gave up) go to
+ * the workspace status word. The launch is cooperative; the first call on a device sizes
+ * the grid and should precede stream capture. */
+QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                   int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
+                                   const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                   int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len, int32_t B,
+                                   int64_t max_blocks, int32_t *blocks, int32_t *count, qsa_bf16 *out, float *lse,
+                                   void *ws, size_t ws_bytes, qsa_stream stream);
 
 /* Allocation-free variant of qsa_sparse_decode (the pages have no counterpart; this
  * is a library convenience). Same arguments and result, but no workspace: the split

@@ -23,7 +23,7 @@ QSA_ERR_CUDA = 4
 QSA_ERR_DEVICE_TIMEOUT = 5
 QSA_ERR_DEVICE_BOUNDS = 6
 
-OP_POOL_KEYS, OP_INDEX_SCORE, OP_TOPK_BLOCKS, OP_SPARSE_DECODE, OP_SPARSE_PREFILL_CHUNK = range(5)
+OP_POOL_KEYS, OP_INDEX_SCORE, OP_TOPK_BLOCKS, OP_SPARSE_DECODE, OP_SPARSE_PREFILL_CHUNK, OP_DECODE_STEP = range(6)
 BLOCK_TOPK = 512
 
 
@@ -59,6 +59,8 @@ _SIGNATURES = {
     "qsa_topk_blocks": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "qsa_sparse_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "qsa_sparse_prefill_chunk": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "qsa_decode_step": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _P,
+                                _P, _SZ, _P]),
     "qsa_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
     "qsa_last_error": (C.c_char_p, []),
@@ -172,6 +174,18 @@ def qsa_sparse_decode(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count,
                                     _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
                                     _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _stream(stream)),
            "qsa_sparse_decode")
+
+
+def qsa_decode_step(cfg, raw_idx_k, pooled, blk_off, q_idx, q, k_cache, v_cache, tok_off, ctx_len, max_blocks,
+                    blocks, count, out, lse, ws, stream=None):
+    _check(load().qsa_decode_step(C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"),
+                                  _ptr(pooled, torch.bfloat16, "pooled"), pooled.shape[0], _ptr(blk_off, torch.int32),
+                                  _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(q, torch.bfloat16, "q"),
+                                  _ptr(k_cache, torch.bfloat16, "k"), _ptr(v_cache, torch.bfloat16, "v"),
+                                  k_cache.shape[0], _ptr(tok_off, torch.int32), _ptr(ctx_len, torch.int32),
+                                  ctx_len.numel(), int(max_blocks), _ptr(blocks, torch.int32),
+                                  _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
+                                  _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _stream(stream)), "qsa_decode_step")
 
 
 def qsa_sparse_decode_noalloc(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out, lse, stream=None):

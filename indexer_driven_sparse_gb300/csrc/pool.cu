@@ -5,22 +5,6 @@
 
 namespace qsa {
 
-// Round a double to the nearest bf16 (ties to even) in one step. bf16 keeps 8
-// significant bits with fp32's exponent range: near |x| in [2^e, 2^(e+1)) the
-// spacing is 2^(e-7), and 2^-133 below 2^-126. Scaling by a power of two is exact,
-// rint() rounds half to even, and the result converts to fp32 exactly.
-__device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
-    if (isnan(x)) return 0x7FC0;
-    const uint16_t sign = signbit(x) ? 0x8000 : 0;
-    const double ax = fabs(x);
-    if (isinf(ax)) return sign | 0x7F80;
-    int e = (ax == 0.0) ? -126 : ilogb(ax);
-    if (e < -126) e = -126;
-    const double r = ldexp(rint(ldexp(ax, 7 - e)), e - 7);
-    if (r >= 0x1p128) return sign | 0x7F80;
-    return sign | (uint16_t)(__float_as_uint((float)r) >> 16);
-}
-
 // 16 threads per block, each owning 8 of the 128 dims (16-byte loads and stores).
 __global__ void __launch_bounds__(256) pool_keys_kernel(const uint16_t *__restrict__ raw, int64_t n_tok,
                                                         const int32_t *tok_off, const int32_t *blk_off,

@@ -6,6 +6,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "qsa_internal.cuh"
 
 using namespace qsa;
@@ -67,6 +69,7 @@ size_t ws_size(int32_t op, const qsa_config *c, int32_t n_rows, int64_t max_bloc
         case QSA_OP_SPARSE_DECODE: return kWsHeaderBytes + decode_scratch_bytes(n_rows, c->n_q_heads, c->n_kv_heads);
         case QSA_OP_SPARSE_PREFILL_CHUNK:
             return kWsHeaderBytes + prefill_scratch_bytes(n_rows, c->n_q_heads, c->n_kv_heads);
+        case QSA_OP_DECODE_STEP: return decode_step_ws_bytes(n_rows, max_blocks, c->n_q_heads);
         default: return 0;
     }
 }
@@ -253,6 +256,61 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
                                                 w + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
                                                 static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse_prefill_chunk launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                   int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
+                                   const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                   int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len, int32_t B,
+                                   int64_t max_blocks, int32_t *blocks, int32_t *count, qsa_bf16 *out, float *lse,
+                                   void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(B >= 0 && B <= kMaxStepRows, "B = %d out of range [0, 64]", B);
+    QSA_NEED(max_blocks >= 0 && max_blocks <= (int64_t)1 << 28, "max_blocks out of range");
+    QSA_NEED(n_tokens_total >= 0 && n_pooled_total >= 0, "negative size");
+    if (cfg->n_kv_heads > 2) return fail(QSA_ERR_UNSUPPORTED, "qsa_decode_step supports n_kv_heads <= 2");
+    QSA_TRY(check_ws(QSA_OP_DECODE_STEP, cfg, B, max_blocks, ws, ws_bytes));
+    if (B == 0) return ok();
+    QSA_NEED(raw_idx_k && pooled && blk_off && q_idx && q && k_cache && v_cache && tok_off && ctx_len && blocks &&
+                 count && out,
+             "NULL tensor pointer");
+    QSA_NEED(aligned(raw_idx_k, 16) && aligned(pooled, 16) && aligned(q_idx, 16) && aligned(k_cache, 16) &&
+                 aligned(v_cache, 16) && aligned(q, 16),
+             "bf16 tensors must be 16-byte aligned");
+    const int G = cfg->n_q_heads / cfg->n_kv_heads;
+    const int ctas = decode_step_grid(G);
+    if (ctas == 0) return fail(QSA_ERR_CUDA, "decode step: cannot size the cooperative grid on this device");
+    if (B > ctas) return fail(QSA_ERR_UNSUPPORTED, "decode step: B = %d exceeds %d co-resident CTAs", B, ctas);
+    // every CTA keeps at most decode_step_max_keys() scores on chip; bound the worst row
+    const int64_t K = 16384;
+    const int64_t worst = ctas > B ? (int64_t)B * (max_blocks + K) / (ctas - B) + 1 : max_blocks;
+    if (std::min<int64_t>(worst, max_blocks) > decode_step_max_keys())
+        return fail(QSA_ERR_UNSUPPORTED, "decode step: %lld blocks per CTA exceed the on-chip limit %d",
+                    (long long)std::min<int64_t>(worst, max_blocks), decode_step_max_keys());
+    StepArgs a{};
+    a.raw_idx_k = raw_idx_k;
+    a.pooled = pooled;
+    a.n_pooled = n_pooled_total;
+    a.blk_off = blk_off;
+    a.q_idx = q_idx;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.n_tok = n_tokens_total;
+    a.tok_off = tok_off;
+    a.ctx_len = ctx_len;
+    a.B = B;
+    a.max_blocks = max_blocks;
+    a.blocks = blocks;
+    a.count = count;
+    a.out = out;
+    a.lse = lse;
+    a.n_q_heads = cfg->n_q_heads;
+    a.n_kv_heads = cfg->n_kv_heads;
+    a.scale_log2 = scale_of(cfg) * kLog2e;
+    const cudaError_t e = launch_decode_step(a, ws, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
     return ok();
 }
 

@@ -23,14 +23,17 @@ struct WsHeader {
     int32_t status;      // first device-side error (qsa_status), 0 = none
     int32_t detail;      // kernel-specific detail (row, index)
     int32_t where;       // which kernel recorded it
-    int32_t pad0;
+    int32_t debug;       // test knob: kDebugStallBarrier makes the first row barrier never complete
     uint32_t sem[60];    // self-resetting counters (last-CTA-done, grid barriers)
 };
 static_assert(sizeof(WsHeader) == 256, "status block must be 256 bytes");
 constexpr size_t kWsHeaderBytes = 256;
+constexpr int32_t kDebugStallBarrier = 0x5741171;   // written only by the device-timeout test
+constexpr uint64_t kWaitLimitNs = 250ull * 1000 * 1000;   // every device-side wait gives up after 250 ms
 
 enum Where : int32_t {
     kWherePool = 1, kWhereScore = 2, kWhereTopk = 3, kWhereDecode = 4, kWhereMerge = 5, kWherePrefill = 6,
+    kWhereStep = 7,
 };
 
 __device__ __forceinline__ void record_error(WsHeader *h, int32_t code, int32_t where, int32_t detail) {
@@ -63,6 +66,22 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
 // fp32 -> bf16 bits, round to nearest even (CUDA intrinsic).
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Round a double to the nearest bf16 (ties to even) in one step. bf16 keeps 8
+// significant bits with fp32's exponent range: near |x| in [2^e, 2^(e+1)) the
+// spacing is 2^(e-7), and 2^-133 below 2^-126. Scaling by a power of two is exact,
+// rint() rounds half to even, and the result converts to fp32 exactly.
+__device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
+    if (isnan(x)) return 0x7FC0;
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    const double ax = fabs(x);
+    if (isinf(ax)) return sign | 0x7F80;
+    int e = (ax == 0.0) ? -126 : ilogb(ax);
+    if (e < -126) e = -126;
+    const double r = ldexp(rint(ldexp(ax, 7 - e)), e - 7);
+    if (r >= 0x1p128) return sign | 0x7F80;
+    return sign | (uint16_t)(__float_as_uint((float)r) >> 16);
 }
 
 // Order-preserving map of an fp32 score to uint32: larger score -> larger key.
@@ -113,6 +132,46 @@ cudaError_t launch_sparse_decode(const AttnArgs &a, WsHeader *hdr, void *scratch
 cudaError_t launch_attn_rows(const AttnArgs &a, WsHeader *hdr, cudaStream_t st);
 
 size_t prefill_scratch_bytes(int Nc, int Hq, int Hkv);
+
+// Fused decode layer-step (decode_step.cu).
+constexpr int kMaxStepCtas = 256;
+constexpr int kMaxStepRows = 64;
+struct StepArgs {
+    const uint16_t *raw_idx_k;
+    uint16_t *pooled;
+    int64_t n_pooled;
+    const int32_t *blk_off;
+    const uint16_t *q_idx;
+    const uint16_t *q;
+    const uint16_t *k_cache;
+    const uint16_t *v_cache;
+    int64_t n_tok;
+    const int32_t *tok_off;
+    const int32_t *ctx_len;
+    int32_t B;
+    int64_t max_blocks;
+    int32_t *blocks;
+    int32_t *count;
+    uint16_t *out;
+    float *lse;
+    int32_t n_q_heads, n_kv_heads;
+    float scale_log2;
+    // workspace views (set by launch_decode_step)
+    WsHeader *hdr;
+    void *rows;
+    uint32_t *hist;
+    unsigned long long *cands;
+    float *part;
+};
+struct StepLayout {
+    size_t rows, hist, cands, part, total;
+};
+StepLayout step_layout(int B, int64_t max_blocks, int Hq);
+size_t decode_step_ws_bytes(int B, int64_t max_blocks, int Hq);
+int decode_step_max_keys();
+// Number of CTAs the cooperative step kernel runs with on the current device (0 on error).
+int decode_step_grid(int G);
+cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st);
 
 // Set the calling thread's qsa_last_error() text to "<what>: <detail>" and return s.
 qsa_status host_fail(qsa_status s, const char *what, const char *detail);

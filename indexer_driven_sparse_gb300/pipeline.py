@@ -48,9 +48,23 @@ class DecodeBatch:
                  qb.workspace_size(qb.OP_TOPK_BLOCKS, self.cfg, self.B, self.ld),
                  qb.workspace_size(qb.OP_SPARSE_DECODE, self.cfg, self.B, self.ld)]
         self.ws = _workspace(max(sizes), device)
+        self.step_ws = None
+        if self.B <= 64:
+            n = qb.workspace_size(qb.OP_DECODE_STEP, self.cfg, self.B, self.ld)
+            if n:
+                self.step_ws = _workspace(n, device)
 
     def new_pooled(self):
         return torch.empty(max(self.n_pooled, 1), 128, dtype=torch.bfloat16, device=self.device)
+
+    def fused_step(self, raw_idx_k, pooled, q_idx, q, k_cache, v_cache, stream=None):
+        """One decode layer-step in one launch (qsa_decode_step): re-pool the newest
+        block, score, select, attend, merge."""
+        qb.qsa_decode_step(self.cfg, raw_idx_k, pooled, self.blk_off, q_idx, q, k_cache, v_cache, self.tok_off,
+                           self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse, self.step_ws, stream)
+
+    def fused_status(self, stream=None):
+        return qb.qsa_read_device_status(self.step_ws, stream)
 
     def pool(self, raw_idx_k, pooled, stream=None):
         qb.qsa_pool_keys(self.cfg, raw_idx_k, self.tok_off, self.blk_off, self.blk_begin, self.blk_end,

@@ -1,0 +1,150 @@
+"""The fused decode layer-step (qsa_decode_step) against the separate calls and the oracle.
+
+The fused kernel scores with the same fp32 arithmetic as qsa_index_score, so its
+selection must equal the separate path's exactly; its attention is graded against the
+oracle on that selection.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from indexer_driven_sparse_gb300 import binding as qb
+from indexer_driven_sparse_gb300 import inputs as I
+from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+from parity import bits, check_attention, check_selection
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _to(layer):
+    return I.Layer(*(getattr(layer, f).to(DEV) for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))
+
+
+def _host(layer):
+    return I.Layer(*(getattr(layer, f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))
+
+
+def _run_both(w, corrupt_newest=False):
+    L = _to(w.layers[0])
+    b = DecodeBatch(w.n_q_heads, w.n_kv_heads, w.ctx_len)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    b.step(L.q_idx, L.q, L.k_cache, L.v_cache, pooled)
+    assert b.device_status()[0] == 0
+    sep = (b.blocks.clone(), b.count.clone(), b.out.clone(), b.lse.clone())
+    want_pooled = pooled.clone()
+    if corrupt_newest:
+        for s, p in enumerate(w.ctx_len):
+            if p >= 4:
+                pooled[b.blk_off[s].item() + p // 4 - 1] = 7.0
+    b.blocks.fill_(-7)
+    b.out.zero_()
+    b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+    st = b.fused_status()
+    assert st[0] == 0, st
+    assert torch.equal(pooled, want_pooled)
+    return b, sep, pooled
+
+
+def _check(w, b, sep, pooled, rows=None):
+    blocks_sep, count_sep, out_sep, lse_sep = sep
+    assert torch.equal(b.count, count_sep)
+    assert torch.equal(b.blocks, blocks_sep), "fused selection differs from the separate path"
+    assert (b.out.float() - out_sep.float()).abs().max().item() <= 2 ** -6
+    Lh = w.layers[0]
+    rb, qib, qbits = bits(Lh.raw_idx_k), bits(Lh.q_idx), bits(Lh.q)
+    kb, vb = bits(Lh.k_cache), bits(Lh.v_cache)
+    blocks, count, out, lse = b.blocks.cpu().numpy(), b.count.cpu().numpy(), b.out.cpu(), b.lse.cpu().numpy()
+    off = w.tok_off
+    for s in (range(w.batch) if rows is None else rows):
+        p = w.ctx_len[s]
+        pk = O.pool_keys(rb[off[s]:off[s + 1]])
+        check_selection(blocks[s], count[s], qib[s], pk, p // 4)
+        ref = O.decode_query(p, qib[s], pk, qbits[s], kb[off[s]:off[s + 1]], vb[off[s]:off[s + 1]], w.n_kv_heads,
+                             sel=blocks[s, :count[s]])
+        check_attention(out[s], ref["out"])
+        assert np.max(np.abs(lse[s] - ref["lse"])) < 1e-3
+
+
+@pytest.mark.parametrize("case", ["tiny", "tiny_sharp", "planted_ragged", "batched_short", "dense_only"])
+def test_fused_step_small(cuda_lib, case):
+    if case == "tiny":
+        w = I.tiny_decode()
+    elif case == "tiny_sharp":
+        w = I.tiny_decode(kind="sharp", seed=3)
+    elif case == "planted_ragged":
+        w = I.decode_workload("planted_ragged", [5000, 2052, 70001, 4, 12345, 0, 3], 1, 16, 2, "planted", seed=4)
+    elif case == "batched_short":
+        w = I.decode_workload("batched_short", I.batched_ctx_lens(short_draw=True), 1, 8, 2, "gaussian", seed=0)
+    else:
+        w = I.decode_workload("dense_only", [0, 1, 7, 2047, 2051], 1, 16, 2, "sharp", seed=5)
+    b, sep, pooled = _run_both(w, corrupt_newest=True)
+    _check(w, b, sep, pooled)
+
+
+def test_fused_step_repeatable(cuda_lib):
+    w = I.decode_workload("rep", [40000, 9000], 1, 16, 2, "planted", seed=7)
+    b, sep, pooled = _run_both(w)
+    L = _to(w.layers[0])
+    outs = []
+    for _ in range(3):
+        b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+        outs.append((b.blocks.clone(), b.out.clone(), b.lse.clone()))
+    assert b.fused_status()[0] == 0
+    for o in outs[1:]:
+        assert all(torch.equal(x, y) for x, y in zip(o, outs[0]))
+
+
+def test_fused_step_all_equal_scores(cuda_lib):
+    # every score ties (zero indexer query): the lowest 512 block ids win; 50,000 candidates
+    w = I.decode_workload("ties", [200003], 1, 16, 2, "gaussian", seed=8)
+    w.layers[0].q_idx.zero_()
+    b, sep, pooled = _run_both(w)
+    assert torch.equal(b.blocks[0].cpu(), torch.arange(512, dtype=torch.int32))
+    _check(w, b, sep, pooled)
+
+
+def test_fused_step_long_and_million_one_layer(cuda_lib):
+    for w in (I.long_decode(n_layers=1), I.million_decode(n_layers=1)):
+        b, sep, pooled = _run_both(w)
+        w.layers = [_host(w.layers[0])]
+        _check(w, b, sep, pooled)
+        del b, sep, pooled
+        torch.cuda.empty_cache()
+
+
+def test_fused_step_batched_full_size_one_layer(cuda_lib):
+    w = I.batched_decode(n_layers=1)
+    b, sep, pooled = _run_both(w)
+    w.layers = [_host(w.layers[0])]
+    _check(w, b, sep, pooled, rows=[0, 7, 31])
+
+
+def test_fused_step_device_timeout_is_reported(cuda_lib):
+    # The header's test knob makes the first row barrier wait for an arrival that never
+    # comes; every CTA gives up after its bounded wait and the status says so.
+    w = I.decode_workload("stall", [9000], 1, 16, 2, "gaussian", seed=9)
+    L = _to(w.layers[0])
+    b = DecodeBatch(16, 2, w.ctx_len)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    b.step_ws.view(torch.int32)[3] = 0x5741171
+    b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+    st, det = b.fused_status()
+    assert st == qb.QSA_ERR_DEVICE_TIMEOUT and det == 0
+    qb.qsa_workspace_init(b.step_ws)
+    b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+    assert b.fused_status()[0] == 0
+
+
+def test_fused_step_rejects_unsupported(cuda_lib):
+    cfg = qb.make_config(16, 4)
+    lib = qb.load()
+    import ctypes as C
+    fake = 0x10000000
+    st = lib.qsa_decode_step(C.byref(cfg), fake, fake, 10, fake, fake, fake, fake, fake, 100, fake, fake, 1, 10,
+                             fake, fake, fake, None, fake, 1 << 30, None)
+    assert st == qb.QSA_ERR_UNSUPPORTED
