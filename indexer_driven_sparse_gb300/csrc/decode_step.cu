@@ -9,23 +9,26 @@
 //   "125B MoE を 3090 3 枚で運用する vLLM 最適化編", section 3.3: ordered-integer top-k keys
 //   with the id in the low bits, and a last-CTA-done finaliser.
 //
-// Layout of the work: each sequence (row) owns a contiguous group of CTAs (sized by its
-// context); CTA j of a row owns the contiguous block range [nb*j/c, nb*(j+1)/c).
+// Each sequence (row) owns a contiguous group of c CTAs (sized by its context); CTA j owns
+// the block range [nb*j/c, nb*(j+1)/c). The design keeps the number of dependent global
+// round trips after the bandwidth-bound scan small:
 //   1. The CTA owning block nb-1 re-pools it from the raw keys (exact fp64 mean).
-//   2. Each CTA streams its pooled rows through a 4-stage shared-memory ring filled by
-//      bulk async copies (TMA engine), keeps the 32-bit order-preserving score keys of its
-//      range in shared memory and histograms their top 12 bits.
-//   3. Row barrier; the last CTA to arrive finds the threshold bin and how many of its
-//      members are still needed.
-//   4. Each CTA counts its blocks above the bin and appends the bin's members (64-bit
-//      key = score key << 32 | ~block) to a candidate list.
-//   5. Row barrier; the last arriver radix-selects the exact 64-bit threshold among the
-//      candidates and publishes every CTA's output offset.
-//   6. Each CTA writes its selected ids (ascending) and attends its own selected tokens
+//   2. Each CTA streams its pooled rows through a 4-stage shared-memory ring filled by bulk
+//      async copies (TMA engine), keeping the 32-bit order-preserving score keys of its
+//      range on chip and histogramming their top 12 bits.
+//   3. Each CTA publishes its exact local top-K keys (64-bit: score key << 32 | ~block),
+//      K = 2 x 512 / c rounded up to a power of two in [32, 512].
+//   4. One row barrier. Every CTA then reads all published keys and computes the same
+//      exact 512th key T and every CTA's output offset. If some CTA might hold more than K
+//      selected blocks (its K-th key >= T), all CTAs take the exact fallback instead: a
+//      global histogram, a threshold bin and the bin's members resolved at two barriers.
+//   5. Each CTA writes its selected ids (ascending) and attends its own selected tokens
 //      (plus the query's own block, in the row's last CTA), producing an (m, l, acc) partial.
-//   7. Row barrier; the CTAs of the row merge all partials by LSE, each a slice of outputs.
-// Rows with nb <= 512 (dense) skip steps 2-5. Every wait is bounded: a barrier or mbarrier
-// that gives up records QSA_ERR_DEVICE_TIMEOUT and the CTA returns.
+//   6. Row barrier; the CTAs of the row merge all partials by LSE, each a slice of the
+//      outputs, loading everything they need in one round trip.
+// Dense rows (nb <= 512) select everything and skip 2-4. Every wait is bounded (250 ms on
+// the GPU clock): a barrier or mbarrier that gives up records QSA_ERR_DEVICE_TIMEOUT and
+// the CTA returns.
 #include "qsa_internal.cuh"
 #include "qsa_ptx.cuh"
 
@@ -38,25 +41,30 @@ constexpr int kHistShift = 20;
 constexpr int kRingStages = 4;
 constexpr int kChunkRows = 128;                       // 128 pooled rows = 32 KiB per stage
 constexpr int kChunkBytes = kChunkRows * kIdxDim * 2;
+constexpr int kRingBytes = kRingStages * kChunkBytes;
 constexpr int kMaxKeys = 12288;                       // score keys per CTA kept on chip
 constexpr int kAttnTok = 32;                          // tokens per attention step
 constexpr int kAttnWeightBlocks = 16384;              // attention cost of a row, in scanned blocks
+constexpr int kMaxPub = 512;                          // published keys per CTA (+1 flag slot)
+constexpr int kMergeRegs = 32;                        // partial values one thread merges
 
 constexpr size_t kRingOff = 0;
-constexpr size_t kKeysOff = kRingOff + (size_t)kRingStages * kChunkBytes;
+constexpr size_t kKeysOff = kRingOff + (size_t)kRingBytes;
 constexpr size_t kHistOff = kKeysOff + (size_t)kMaxKeys * 4;
-constexpr size_t kNewRowOff = kHistOff + (size_t)kHistBins * 4;
+constexpr size_t kQOff = kHistOff + (size_t)kHistBins * 4;          // query, bf16 [Hq][256]
+constexpr size_t kNewRowOff = kQOff + (size_t)2 * kMaxGroup * kHeadDim * 2;
 constexpr size_t kMbarOff = kNewRowOff + 256;
 constexpr size_t kStepSmem = kMbarOff + 64;
 
 struct StepRowState {
-    uint32_t bar_count;
-    uint32_t bar_gen;
-    int32_t t1;                 // threshold bin (top 12 key bits)
-    int32_t need;               // members of the threshold bin still to take
-    unsigned long long t64;     // exact 64-bit threshold key
+    uint32_t gen;               // barrier generation, advanced once per completed barrier
+    uint32_t pad0;
+    uint32_t counts[4];         // arrival counters, indexed by (generation - 1) & 3
+    int32_t t1;                 // fallback: threshold bin (top 12 key bits)
+    int32_t need;               // fallback: members of the threshold bin still to take
+    unsigned long long t64;     // fallback: exact 64-bit threshold key
     uint32_t cand_count;
-    int32_t pad;
+    int32_t pad1;
     int32_t definite[kMaxStepCtas];
     int32_t offset[kMaxStepCtas];
 };
@@ -70,7 +78,9 @@ StepLayout step_layout(int B, int64_t max_blocks, int Hq) {
     L.hist = L.rows + (size_t)B * step_row_state_bytes();
     L.cands = L.hist + (size_t)B * kHistBins * 4;
     L.part = L.cands + ((size_t)B * (size_t)max_blocks * 8 + 255) / 256 * 256;
-    L.total = L.part + (size_t)kMaxStepCtas * Hq * (kHeadDim + 2) * 4;
+    L.pub = L.part + (size_t)kMaxStepCtas * Hq * (kHeadDim + 2) * 4;
+    L.trace = L.pub + (size_t)kMaxStepCtas * (kMaxPub + 1) * 8;
+    L.total = L.trace + (size_t)kMaxStepCtas * kTraceSlots * 8;
     return L;
 }
 
@@ -120,77 +130,90 @@ __device__ void partition_rows(const int32_t *ctx_len, int B, RowPart *out) {
     if (in1) *out = RowPart{lane + 32, bid - (s1 - c1), c1, s1 - c1};
 }
 
-// Arrive at the row barrier. Returns 1 for the last CTA to arrive (which must call
-// row_release after its exclusive work), 0 for the others once released, -1 on timeout.
-__device__ int row_arrive(StepRowState *rs, int n, WsHeader *hdr, int row, int *s_flag) {
+// Row barrier over `n` CTAs. Barrier number k of a launch completes generation g0 + k + 1
+// (g0: the generation when the launch started). Arrival is one acq_rel atomic; the last
+// CTA to arrive gets 1 back, may do exclusive work, and must call bar_release, which
+// re-arms the next barrier's counter and publishes the generation with one release store.
+// Others poll the generation (bounded). Returns 1 (last), 0 (released) or -1 (timeout).
+__device__ int bar_arrive(StepRowState *rs, uint32_t g0, int k, int n, WsHeader *hdr, int row, int *s_flag) {
+    // A GPU-scope fence orders only the calling thread's writes: every thread that wrote
+    // data for other CTAs fences before the CTA barrier that precedes the arrival.
+    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        const uint32_t gen = ld_acquire_u32(&rs->bar_gen);
-        __threadfence();
-        const uint32_t arrived = atomicAdd(&rs->bar_count, 1u) + 1u;
+        const uint32_t g = g0 + (uint32_t)k + 1u;
+        const uint32_t old = atom_add_acq_rel_u32(&rs->counts[(g - 1u) & 3u], 1u);
         int res = 1;
-        if (arrived != (uint32_t)n) {
+        if (old + 1u != (uint32_t)n) {
             res = 0;
             const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_u32(&rs->bar_gen) == gen) {
+            while ((int32_t)(ld_acquire_u32(&rs->gen) - g) < 0) {
                 if (globaltimer_ns() - t0 > kWaitLimitNs) {
                     record_error(hdr, QSA_ERR_DEVICE_TIMEOUT, kWhereStep, row);
                     res = -1;
                     break;
                 }
-                __nanosleep(100);
+                __nanosleep(32);
             }
         }
-        __threadfence();
         *s_flag = res;
     }
     __syncthreads();
     return *s_flag;
 }
 
-__device__ void row_release(StepRowState *rs) {
+__device__ void bar_release(StepRowState *rs, uint32_t g0, int k) {
+    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        rs->bar_count = 0;
-        __threadfence();
-        atomicAdd(&rs->bar_gen, 1u);
+        const uint32_t g = g0 + (uint32_t)k + 1u;
+        rs->counts[g & 3u] = 0u;
+        st_release_u32(&rs->gen, g);
     }
 }
 
-// Warp 0: in hist[0..nbins) (bins high = better), find the bin where the count from the
-// top first reaches `need`; returns it and the count strictly above it.
-__device__ void warp_find_bin(const uint32_t *hist, int nbins, uint32_t need, int *d_out, uint32_t *above_out) {
-    const int lane = threadIdx.x & 31;
-    const int per = nbins / 32;
-    uint32_t sum = 0;
-    for (int i = 0; i < per; ++i) sum += hist[lane * per + i];
-    uint32_t suf = sum;
+// CTA-wide: in hist[0..nbins) (bins high = better, nbins a power of two >= 256), find the
+// bin where the count from the top first reaches `need` (1 <= need <= total). Writes the
+// bin to *s_d and the count strictly above it to *s_above; all threads return after a sync.
+__device__ void block_find_bin(const uint32_t *hist, int nbins, uint32_t need, int *s_d, uint32_t *s_above,
+                               uint32_t *s_wtot) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = nbins >= kStepThreads ? nbins / kStepThreads : 1;
+    const int nact = nbins / per;
+    uint32_t x = 0;
+    if (tid < nact)
+        for (int i = 0; i < per; ++i) x += hist[tid * per + i];
+    uint32_t s = x;                               // suffix sum within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
-        if (lane + o < 32) suf += v;
+        const uint32_t v = __shfl_down_sync(0xffffffffu, s, o);
+        if (lane + o < 32) s += v;
     }
-    const uint32_t above_lane = suf - sum;
-    const unsigned m = __ballot_sync(0xffffffffu, above_lane < need && suf >= need);
-    const int L = m ? 31 - __clz(m) : 0;
-    if (lane == L) {
-        uint32_t run = above_lane;
-        int d = (L + 1) * per - 1;
-        for (; d > L * per; --d) {
+    if (lane == 0) s_wtot[warp] = s;
+    __syncthreads();
+    uint32_t higher = 0;
+    for (int w = warp + 1; w < kStepWarps; ++w) higher += s_wtot[w];
+    const uint32_t S = s + higher;                // count in this thread's bins and above
+    if (tid < nact && S >= need && S - x < need) {
+        uint32_t run = S - x;
+        int d = tid * per + per - 1;
+        for (; d > tid * per; --d) {
             if (run + hist[d] >= need) break;
             run += hist[d];
         }
-        *d_out = d;
-        *above_out = run;
+        *s_d = d;
+        *s_above = run;
     }
+    __syncthreads();
 }
 
-// CTA-wide: the need-th largest of n 64-bit keys in global memory whose bits above
-// `start` are all equal. 11-bit radix passes, stopping early once the chosen bin holds
-// exactly the keys still needed.
+// CTA-wide: the need-th largest of n 64-bit keys (shared or global memory) whose bits at
+// and above `start` are all equal (start = 64: no shared prefix). 11-bit radix passes,
+// stopping early once the chosen bin holds exactly the keys still needed.
 __device__ unsigned long long select_kth_key64(const unsigned long long *keys, uint32_t n, uint32_t need,
-                                               int start, uint32_t *hist, int *s_d, uint32_t *s_above) {
-    unsigned long long prefix = (__ldcg(&keys[0]) >> start) << start;
+                                               int start, uint32_t *hist, int *s_d, uint32_t *s_above,
+                                               uint32_t *s_wtot) {
+    unsigned long long prefix = start >= 64 ? 0ull : (keys[0] >> start) << start;
     int hi = start;
     while (hi > 0) {
         const int width = hi >= 11 ? 11 : hi;
@@ -199,12 +222,12 @@ __device__ unsigned long long select_kth_key64(const unsigned long long *keys, u
         for (int i = threadIdx.x; i < 2048; i += kStepThreads) hist[i] = 0;
         __syncthreads();
         for (uint32_t i = threadIdx.x; i < n; i += kStepThreads) {
-            const unsigned long long k = __ldcg(&keys[i]);
-            if ((k >> hi) == (prefix >> hi)) atomicAdd(&hist[(uint32_t)(k >> shift) & (nbins - 1)], 1u);
+            const unsigned long long k = keys[i];
+            const bool match = hi >= 64 || (k >> hi) == (prefix >> hi);
+            if (match) atomicAdd(&hist[(uint32_t)(k >> shift) & (nbins - 1)], 1u);
         }
         __syncthreads();
-        if (threadIdx.x < 32) warp_find_bin(hist, nbins < 32 ? 32 : nbins, need, s_d, s_above);
-        __syncthreads();
+        block_find_bin(hist, nbins < 256 ? 256 : nbins, need, s_d, s_above, s_wtot);
         const int d = *s_d;
         const uint32_t in_bin = hist[d];
         prefix |= (unsigned long long)d << shift;
@@ -216,35 +239,70 @@ __device__ unsigned long long select_kth_key64(const unsigned long long *keys, u
     return prefix;
 }
 
+__device__ __forceinline__ unsigned long long key64_of(uint32_t key, int64_t blk) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+}
+
+// Published keys per CTA for a row split over c CTAs: 2 x 512 / c, a power of two in [32, 512].
+__device__ __forceinline__ int pub_count(int c) {
+    int k = 32;
+    while (k < kMaxPub && k * c < 2 * kBlockTopK) k <<= 1;
+    return k;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem + kKeysOff);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kHistOff);
+    uint16_t *q_b = reinterpret_cast<uint16_t *>(smem + kQOff);
     uint16_t *newrow = reinterpret_cast<uint16_t *>(smem + kNewRowOff);
+    unsigned long long *ring64 = reinterpret_cast<unsigned long long *>(smem + kRingOff);
     const uint32_t mbar0 = smem_u32(smem + kMbarOff);
     const uint32_t ring0 = smem_u32(smem + kRingOff);
 
     __shared__ RowPart s_part;
-    __shared__ int s_flag, s_d, s_bad;
-    __shared__ uint32_t s_above;
+    __shared__ int s_flag, s_d, s_overflow;
+    __shared__ uint32_t s_above, s_n;
+    __shared__ unsigned long long s_kmin;
+    __shared__ unsigned long long s_kth[kMaxStepCtas];
     __shared__ int32_t s_sel[kBlockTopK];
-    __shared__ int s_nsel;
     __shared__ uint32_t s_cnt[kMaxStepCtas];
     __shared__ uint32_t s_wsum[kStepWarps];
     __shared__ float s_m[2 * kMaxGroup], s_l[2 * kMaxGroup], s_alpha[2 * kMaxGroup];
+    __shared__ int32_t s_ctx[kMaxStepRows], s_tok_off[kMaxStepRows + 1], s_blk_off[kMaxStepRows + 1];
+    __shared__ int32_t s_debug;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hq = a.n_q_heads, Hkv = a.n_kv_heads;
 
-    if (warp == 0) partition_rows(a.ctx_len, a.B, &s_part);
+    // ---- metadata in one round trip (partition in warp 0, offsets in warps 1-2)
+    if (warp == 0) {
+        partition_rows(a.ctx_len, a.B, &s_part);
+        if (lane < a.B) s_ctx[lane] = a.ctx_len[lane];
+        if (lane + 32 < a.B) s_ctx[lane + 32] = a.ctx_len[lane + 32];
+    } else if (warp == 1) {
+        for (int i = lane; i <= a.B; i += 32) s_tok_off[i] = a.tok_off[i];
+    } else if (warp == 2) {
+        for (int i = lane; i <= a.B; i += 32) s_blk_off[i] = a.blk_off[i];
+    } else if (warp == 3 && lane == 0) {
+        for (int s = 0; s < kRingStages; ++s) mbar_init(mbar0 + 8 * s, 1);
+        fence_mbar_init();
+    } else if (warp == 4 && lane == 0) {
+        s_debug = __ldcg(&a.hdr->debug);
+    }
     __syncthreads();
+    const bool tracing = s_debug == kDebugTrace;
+    unsigned long long *trace = a.trace + (size_t)blockIdx.x * kTraceSlots;
+#define STEP_TRACE(i) \
+    if (tracing && tid == 0) trace[i] = globaltimer_ns()
+    STEP_TRACE(0);
     const int row = s_part.row, jj = s_part.jj, cr = s_part.cr, first = s_part.first;
 
     // ---- row geometry (identical in every CTA of the row)
-    const int p = a.ctx_len[row];
-    const int64_t base = a.tok_off[row], end = a.tok_off[row + 1];
-    const int64_t boff = a.blk_off[row];
+    const int p = s_ctx[row];
+    const int64_t base = s_tok_off[row], end = s_tok_off[row + 1];
+    const int64_t boff = s_blk_off[row];
     const int64_t nb = p >= 0 ? (p >> 2) : 0;
     const int64_t max_range = (nb + cr - 1) / cr;
     const bool ok = p >= 0 && base >= 0 && end <= a.n_tok && base + p + 1 <= end && boff >= 0 &&
@@ -259,9 +317,26 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     const int n_mine = (int)(hi - lo);
     const bool dense = nb <= kBlockTopK;
     const bool owner_new = nb >= 1 && hi == nb && lo < hi;     // owns block nb-1
+    const int n_tma = owner_new ? n_mine - 1 : n_mine;        // block nb-1 is scored from the re-pooled row
+    const int n_chunks = dense ? 0 : (n_tma + kChunkRows - 1) / kChunkRows;
+    const uint16_t *gsrc = a.pooled + (boff + lo) * kIdxDim;
 
+    // ---- 2a. start streaming this CTA's pooled rows (the latency overlaps what follows)
+    uint32_t g0 = 0;                      // barrier generation at launch (thread 0 only)
+    if (tid == 0) {
+        for (int c = 0; c < n_chunks && c < kRingStages; ++c) {
+            const uint32_t bytes = (uint32_t)min(kChunkRows, n_tma - c * kChunkRows) * kIdxDim * 2;
+            mbar_arrive_expect_tx(mbar0 + 8 * c, bytes);
+            bulk_g2s(ring0 + c * kChunkBytes, gsrc + (int64_t)c * kChunkRows * kIdxDim, bytes, mbar0 + 8 * c);
+        }
+        g0 = ld_acquire_u32(&rs->gen);
+    }
+    // the query rows for the attention step, bf16, prefetched now
+    for (int i = tid; i < Hq * kHeadDim / 8; i += kStepThreads)
+        cp_async16(smem_u32(q_b + i * 8), a.q + (int64_t)row * Hq * kHeadDim + i * 8);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     // ---- 1. re-pool block nb-1 (exact mean of its four raw keys)
-    if (owner_new && warp == 0 && lane < 16) {
+    if (owner_new && warp == 1 && lane < 16) {
         const uint16_t *src = a.raw_idx_k + (base + kRatio * (nb - 1)) * kIdxDim + lane * 8;
         float f0[8], f1[8], f2[8], f3[8];
         unpack8(ldg_nc_v4(src), f0);
@@ -280,28 +355,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         *reinterpret_cast<uint4 *>(a.pooled + (boff + nb - 1) * kIdxDim + lane * 8) = v;
         *reinterpret_cast<uint4 *>(newrow + lane * 8) = v;
     }
+    STEP_TRACE(1);
 
+    int bar_k = 0;                        // barriers completed by this row in this launch
+    unsigned long long t64 = 0ull;        // exact threshold key (dense: select all)
+    int out_off = (int)lo;                // this CTA's first output slot (dense: lo)
     if (!dense) {
-        // ---- 2. scan: bulk copies into a 4-stage ring, scores -> keys + histogram
-        const int n_tma = owner_new ? n_mine - 1 : n_mine;
-        const int n_chunks = (n_tma + kChunkRows - 1) / kChunkRows;
+        // ---- 2b. scan: bulk copies into a 4-stage ring, scores -> keys + histogram
         for (int i = tid; i < kHistBins; i += kStepThreads) hist[i] = 0;
-        if (tid == 0) {
-            for (int s = 0; s < kRingStages; ++s) mbar_init(mbar0 + 8 * s, 1);
-            fence_mbar_init();
-        }
-        __syncthreads();
-        const uint16_t *gsrc = a.pooled + (boff + lo) * kIdxDim;
-        if (tid == 0) {
-            for (int c = 0; c < n_chunks && c < kRingStages; ++c) {
-                const uint32_t bytes = (uint32_t)min(kChunkRows, n_tma - c * kChunkRows) * kIdxDim * 2;
-                mbar_arrive_expect_tx(mbar0 + 8 * c, bytes);
-                bulk_g2s(ring0 + c * kChunkBytes, gsrc + (int64_t)c * kChunkRows * kIdxDim, bytes, mbar0 + 8 * c);
-            }
-        }
         float qf[8];
         unpack8(ldg_nc_v4(a.q_idx + (int64_t)row * kIdxDim + (lane & 15) * 8), qf);
         const int half = lane >> 4, c16 = lane & 15;
+        __syncthreads();
         for (int c = 0; c < n_chunks; ++c) {
             const int stage = c % kRingStages;
             if (!mbar_wait_bounded(mbar0 + 8 * stage, (c / kRingStages) & 1, kWaitLimitNs)) {
@@ -359,113 +424,203 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 atomicAdd(&hist[key >> kHistShift], 1u);
             }
         }
-        __syncthreads();
-        uint32_t *ghist = a.hist + (size_t)row * kHistBins;
-        for (int i = tid; i < kHistBins; i += kStepThreads)
-            if (hist[i]) atomicAdd(&ghist[i], hist[i]);
-
-        // ---- 3. threshold bin (last arriver). The test knob adds one arrival that never comes.
-        const int stall = __ldcg(&a.hdr->debug) == kDebugStallBarrier ? 1 : 0;
-        const int r1 = row_arrive(rs, cr + stall, a.hdr, row, &s_flag);
-        if (r1 < 0) return;
-        if (r1 == 1) {
-            for (int i = tid; i < kHistBins; i += kStepThreads) {
-                hist[i] = __ldcg(&ghist[i]);
-                ghist[i] = 0;
-            }
-            __syncthreads();
-            if (warp == 0) warp_find_bin(hist, kHistBins, kBlockTopK, &s_d, &s_above);
-            __syncthreads();
-            if (tid == 0) {
-                rs->t1 = s_d;
-                rs->need = kBlockTopK - (int)s_above;
-            }
-            row_release(rs);
-        }
-        __syncthreads();
-
-        // ---- 4. classify: count blocks above the bin, append the bin's members
-        const uint32_t t1 = (uint32_t)__ldcg(&rs->t1);
-        unsigned long long *cands = a.cands + (size_t)row * a.max_blocks;
-        uint32_t above = 0;
-        for (int base_i = 0; base_i < n_mine; base_i += kStepThreads) {
-            const int i = base_i + tid;
-            const uint32_t key = i < n_mine ? keys[i] : 0u;
-            const uint32_t bin = key >> kHistShift;
-            const bool is_c = i < n_mine && bin == t1;
-            above += (i < n_mine && bin > t1) ? 1u : 0u;
-            const unsigned bal = __ballot_sync(0xffffffffu, is_c);
-            uint32_t slot0 = 0;
-            if (lane == 0 && bal) slot0 = atomicAdd(&rs->cand_count, (uint32_t)__popc(bal));
-            slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-            const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-            if (is_c && slot < (uint32_t)nb) {          // nb <= max_blocks: the row's list capacity
-                const uint32_t blk = (uint32_t)(lo + i);
-                cands[slot] = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - blk);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
-        if (lane == 0) s_wsum[warp] = above;
-        __syncthreads();
         if (tid == 0) {
-            uint32_t t = 0;
-            for (int w = 0; w < kStepWarps; ++w) t += s_wsum[w];
-            rs->definite[jj] = (int32_t)t;
-        }
-
-        // ---- 5. exact threshold and per-CTA offsets (last arriver)
-        const int r2 = row_arrive(rs, cr, a.hdr, row, &s_flag);
-        if (r2 < 0) return;
-        if (r2 == 1) {
-            const uint32_t n_c = min(__ldcg(&rs->cand_count), (uint32_t)nb);
-            const uint32_t need = (uint32_t)__ldcg(&rs->need);
-            const unsigned long long t64 = select_kth_key64(cands, n_c, need, 64 - 12, hist, &s_d, &s_above);
-            for (int i = tid; i < cr; i += kStepThreads) s_cnt[i] = 0;
-            __syncthreads();
-            for (uint32_t i = tid; i < n_c; i += kStepThreads) {
-                const unsigned long long k = __ldcg(&cands[i]);
-                if (k >= t64) {
-                    const int64_t b = (int64_t)(0xFFFFFFFFu - (uint32_t)k);
-                    int j = (int)(b * cr / nb);
-                    while (j + 1 < cr && nb * (j + 1) / cr <= b) ++j;
-                    while (j > 0 && nb * j / cr > b) --j;
-                    atomicAdd(&s_cnt[j], 1u);
-                }
-            }
-            __syncthreads();
-            if (tid == 0) {
-                int32_t run = 0;
-                for (int j = 0; j < cr; ++j) {
-                    rs->offset[j] = run;
-                    run += __ldcg(&rs->definite[j]) + (int32_t)s_cnt[j];
-                }
-                rs->t64 = t64;
-                rs->cand_count = 0;
-                if (run != kBlockTopK) record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereStep, row);
-            }
-            row_release(rs);
+            s_n = 0;
+            s_cnt[0] = 0;
         }
         __syncthreads();
+        STEP_TRACE(2);
+
+        // ---- 3. publish this CTA's exact local top-K. Slot kMaxPub holds 0 when the CTA
+        // published every key it has, else its K-th largest key (the smallest published).
+        const int K = pub_count(cr);
+        unsigned long long *pub = a.pub + (size_t)blockIdx.x * (kMaxPub + 1);
+        if (n_mine <= K) {
+            for (int i = tid; i < K; i += kStepThreads) pub[i] = i < n_mine ? key64_of(keys[i], lo + i) : 0ull;
+            if (tid == 0) pub[kMaxPub] = 0ull;
+        } else {
+            block_find_bin(hist, kHistBins, (uint32_t)K, &s_d, &s_above, s_wsum);
+            const uint32_t lb = (uint32_t)s_d;
+            // members of the bins >= lb: the top K plus the rest of bin lb
+            for (int i = tid; i < n_mine; i += kStepThreads) {
+                const uint32_t key = keys[i];
+                if ((key >> kHistShift) >= lb) {
+                    const uint32_t slot = atomicAdd(&s_n, 1u);
+                    if (slot < (uint32_t)(kRingBytes / 8)) ring64[slot] = key64_of(key, lo + i);
+                }
+            }
+            __syncthreads();
+            const uint32_t nc = min(s_n, (uint32_t)(kRingBytes / 8));
+            if (nc <= (uint32_t)kStepThreads) {
+                // rank by counting: the candidate with rank r goes to slot r
+                if (tid < (int)nc) {
+                    const unsigned long long mine = ring64[tid];
+                    uint32_t rank = 0;
+                    for (uint32_t j = 0; j < nc; ++j) rank += ring64[j] > mine ? 1u : 0u;
+                    if (rank < (uint32_t)K) pub[rank] = mine;
+                    if (rank == (uint32_t)K - 1u) pub[kMaxPub] = mine;
+                }
+            } else {
+                // threshold value with exactly K keys at or above it (need not be a key itself)
+                const unsigned long long tk =
+                    select_kth_key64(ring64, nc, (uint32_t)K, 64, hist, &s_d, &s_above, s_wsum);
+                if (tid == 0) s_kmin = ~0ull;
+                __syncthreads();
+                for (uint32_t i = tid; i < nc; i += kStepThreads) {
+                    const unsigned long long k = ring64[i];
+                    if (k >= tk) {
+                        const uint32_t slot = atomicAdd(&s_cnt[0], 1u);
+                        if (slot < (uint32_t)K) pub[slot] = k;
+                        atomicMin(&s_kmin, k);
+                    }
+                }
+                __syncthreads();
+                if (tid == 0) pub[kMaxPub] = s_kmin;
+            }
+        }
+        STEP_TRACE(3);
+
+        // ---- 4. one barrier; every CTA derives the same threshold and offsets
+        const int stall = s_debug == kDebugStallBarrier ? 1 : 0;
+        const int r1 = bar_arrive(rs, g0, bar_k, cr + stall, a.hdr, row, &s_flag);
+        if (r1 < 0) return;
+        if (r1 == 1) bar_release(rs, g0, bar_k);
+        ++bar_k;
+        STEP_TRACE(4);
+        const unsigned long long *pub_row = a.pub + (size_t)first * (kMaxPub + 1);
+        const int n_slots = cr * K;
+        for (int i = tid; i < n_slots; i += kStepThreads) {
+            const int j = i / K, s = i % K;
+            ring64[i] = __ldcg(&pub_row[(size_t)j * (kMaxPub + 1) + s]);
+        }
+        for (int j = tid; j < cr; j += kStepThreads) s_kth[j] = __ldcg(&pub_row[(size_t)j * (kMaxPub + 1) + kMaxPub]);
+        __syncthreads();
+        // empty slots hold 0, below every real key, so they never reach the threshold;
+        // exactly 512 published keys are >= t64
+        t64 = select_kth_key64(ring64, (uint32_t)n_slots, kBlockTopK, 64, hist, &s_d, &s_above, s_wsum);
+        // a CTA with unpublished keys whose K-th key reaches the threshold might hold more
+        if (tid == 0) s_overflow = 0;
+        __syncthreads();
+        for (int j = tid; j < cr; j += kStepThreads)
+            if (s_kth[j] != 0ull && s_kth[j] >= t64) s_overflow = 1;
+        __syncthreads();
+        if (!s_overflow) {
+            // offsets: selected published keys of every earlier CTA of the row
+            for (int j = tid; j < cr; j += kStepThreads) s_cnt[j] = 0;
+            __syncthreads();
+            for (int i = tid; i < n_slots; i += kStepThreads)
+                if (ring64[i] >= t64) atomicAdd(&s_cnt[i / K], 1u);
+            __syncthreads();
+            if (tid == 0) {
+                int run = 0;
+                for (int j = 0; j < jj; ++j) run += (int)s_cnt[j];
+                s_flag = run;
+            }
+            __syncthreads();
+            out_off = s_flag;
+        } else {
+            // ---- exact fallback: global histogram -> threshold bin -> candidates -> threshold
+            // (the shared histogram was reused as radix scratch: rebuild it from the keys)
+            for (int i = tid; i < kHistBins; i += kStepThreads) hist[i] = 0;
+            __syncthreads();
+            for (int i = tid; i < n_mine; i += kStepThreads) atomicAdd(&hist[keys[i] >> kHistShift], 1u);
+            __syncthreads();
+            uint32_t *ghist = a.hist + (size_t)row * kHistBins;
+            for (int i = tid; i < kHistBins; i += kStepThreads)
+                if (hist[i]) atomicAdd(&ghist[i], hist[i]);
+            const int rb1 = bar_arrive(rs, g0, bar_k, cr, a.hdr, row, &s_flag);
+            if (rb1 < 0) return;
+            if (rb1 == 1) {
+                for (int i = tid; i < kHistBins; i += kStepThreads) {
+                    hist[i] = __ldcg(&ghist[i]);
+                    ghist[i] = 0;
+                }
+                __syncthreads();
+                block_find_bin(hist, kHistBins, kBlockTopK, &s_d, &s_above, s_wsum);
+                if (tid == 0) {
+                    rs->t1 = s_d;
+                    rs->need = kBlockTopK - (int)s_above;
+                }
+                bar_release(rs, g0, bar_k);
+            }
+            ++bar_k;
+            __syncthreads();
+            const uint32_t t1 = (uint32_t)__ldcg(&rs->t1);
+            unsigned long long *cands = a.cands + (size_t)row * a.max_blocks;
+            uint32_t above = 0;
+            for (int base_i = 0; base_i < n_mine; base_i += kStepThreads) {
+                const int i = base_i + tid;
+                const uint32_t key = i < n_mine ? keys[i] : 0u;
+                const uint32_t bin = key >> kHistShift;
+                const bool is_c = i < n_mine && bin == t1;
+                above += (i < n_mine && bin > t1) ? 1u : 0u;
+                const unsigned bal = __ballot_sync(0xffffffffu, is_c);
+                uint32_t slot0 = 0;
+                if (lane == 0 && bal) slot0 = atomicAdd(&rs->cand_count, (uint32_t)__popc(bal));
+                slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+                const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+                if (is_c && slot < (uint32_t)nb) cands[slot] = key64_of(key, lo + i);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+            if (lane == 0) s_wsum[warp] = above;
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t t = 0;
+                for (int w = 0; w < kStepWarps; ++w) t += s_wsum[w];
+                rs->definite[jj] = (int32_t)t;
+            }
+            const int rb2 = bar_arrive(rs, g0, bar_k, cr, a.hdr, row, &s_flag);
+            if (rb2 < 0) return;
+            if (rb2 == 1) {
+                const uint32_t n_c = min(__ldcg(&rs->cand_count), (uint32_t)nb);
+                const uint32_t need = (uint32_t)__ldcg(&rs->need);
+                const bool in_smem = n_c <= (uint32_t)(kRingBytes / 8);
+                if (in_smem)
+                    for (uint32_t i = tid; i < n_c; i += kStepThreads) ring64[i] = __ldcg(&cands[i]);
+                __syncthreads();
+                const unsigned long long *src = in_smem ? ring64 : cands;
+                const unsigned long long tt =
+                    n_c ? select_kth_key64(src, n_c, need, 64 - 12, hist, &s_d, &s_above, s_wsum) : ~0ull;
+                for (int i = tid; i < cr; i += kStepThreads) s_cnt[i] = 0;
+                __syncthreads();
+                for (uint32_t i = tid; i < n_c; i += kStepThreads) {
+                    const unsigned long long k = src[i];
+                    if (k >= tt) {
+                        const int64_t b = (int64_t)(0xFFFFFFFFu - (uint32_t)k);
+                        int j = (int)(b * cr / nb);
+                        while (j + 1 < cr && nb * (j + 1) / cr <= b) ++j;
+                        while (j > 0 && nb * j / cr > b) --j;
+                        atomicAdd(&s_cnt[j], 1u);
+                    }
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    int32_t run = 0;
+                    for (int j = 0; j < cr; ++j) {
+                        rs->offset[j] = run;
+                        run += __ldcg(&rs->definite[j]) + (int32_t)s_cnt[j];
+                    }
+                    rs->t64 = tt;
+                    rs->cand_count = 0;
+                    if (run != kBlockTopK) record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereStep, row);
+                }
+                bar_release(rs, g0, bar_k);
+            }
+            ++bar_k;
+            __syncthreads();
+            t64 = __ldcg(&rs->t64);
+            out_off = __ldcg(&rs->offset[jj]);
+        }
+        STEP_TRACE(5);
     }
 
-    // ---- 6a. this CTA's selected blocks, ascending, and their output slots
-    const unsigned long long t64 = dense ? 0ull : __ldcg(&rs->t64);
-    const int out_off = dense ? (int)lo : __ldcg(&rs->offset[jj]);
+    // ---- 5a. this CTA's selected blocks, ascending, and their output slots
     int32_t *blocks_row = a.blocks + (int64_t)row * kBlockTopK;
     int nsel = 0;
     for (int base_i = 0; base_i < n_mine; base_i += kStepThreads) {
         const int i = base_i + tid;
-        bool take = false;
-        if (i < n_mine) {
-            if (dense) {
-                take = true;
-            } else {
-                const uint32_t blk = (uint32_t)(lo + i);
-                const unsigned long long k = ((unsigned long long)keys[i] << 32) | (0xFFFFFFFFu - blk);
-                take = k >= t64;
-            }
-        }
+        const bool take = i < n_mine && (dense || key64_of(keys[i], lo + i) >= t64);
         const unsigned bal = __ballot_sync(0xffffffffu, take);
         if (lane == 0) s_wsum[warp] = __popc(bal);
         __syncthreads();
@@ -488,17 +643,21 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         for (int i = kk + tid; i < kBlockTopK; i += kStepThreads) blocks_row[i] = -1;
         if (tid == 0) a.count[row] = kk;
     }
+    STEP_TRACE(6);
 
-    // ---- 6b. attention over this CTA's tokens (+ the query's own block in the last CTA)
+    // ---- 5b. attention over this CTA's tokens (+ the query's own block in the last CTA).
+    // Each step gathers up to 32 tokens' K and V rows (all KV heads) into shared memory with
+    // 16-byte async copies issued together, then computes from shared memory.
     const bool last_cta = jj == cr - 1;
     const int n_tail = last_cta ? (int)(p - kRatio * nb + 1) : 0;
     const int n_tok = kRatio * nsel + n_tail;
-    float *q_s = reinterpret_cast<float *>(smem + kRingOff);                 // [Hq][256], ring reused
-    float *pw = q_s + 2 * kMaxGroup * kHeadDim;                              // [Hq][kAttnTok]
-    int64_t *toks = reinterpret_cast<int64_t *>(pw + 2 * kMaxGroup * kAttnTok);
+    const int row_elems = Hkv * kHeadDim;                              // one token's K (or V) row
+    float *q_s = reinterpret_cast<float *>(smem + kRingOff);           // [Hq][256]
+    float *pw = q_s + 2 * kMaxGroup * kHeadDim;                        // [Hq][kAttnTok]
+    uint16_t *kv_s = reinterpret_cast<uint16_t *>(pw + 2 * kMaxGroup * kAttnTok);   // [32][K row | V row]
+    asm volatile("cp.async.wait_group 0;" ::: "memory");            // the prefetched query
     __syncthreads();
-    for (int i = tid; i < Hq * kHeadDim; i += kStepThreads)
-        q_s[i] = bf16_bits_to_float(a.q[(int64_t)row * Hq * kHeadDim + i]) * a.scale_log2;
+    for (int i = tid; i < Hq * kHeadDim; i += kStepThreads) q_s[i] = bf16_bits_to_float(q_b[i]) * a.scale_log2;
     if (tid < Hq) {
         s_m[tid] = -INFINITY;
         s_l[tid] = 0.f;
@@ -507,20 +666,27 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     float acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = 0.f;
-    __syncthreads();
+    const int gran_per_row = row_elems * 2 / 16;                       // 16-byte granules per K row
     for (int t0 = 0; t0 < n_tok; t0 += kAttnTok) {
         const int n = min(kAttnTok, n_tok - t0);
-        if (tid < n) {
-            const int j = t0 + tid;
+        for (int gidx = tid; gidx < n * 2 * gran_per_row; gidx += kStepThreads) {
+            const int i = gidx / (2 * gran_per_row);
+            const int rem = gidx % (2 * gran_per_row);
+            const int is_v = rem >= gran_per_row;
+            const int gpos = rem - is_v * gran_per_row;
+            const int j = t0 + i;
             const int64_t tk = j < kRatio * nsel ? (int64_t)kRatio * s_sel[j >> 2] + (j & 3)
                                                  : kRatio * nb + (j - kRatio * nsel);
-            toks[tid] = base + tk;
+            const uint16_t *src = (is_v ? a.v_cache : a.k_cache) + (base + tk) * row_elems + gpos * 8;
+            cp_async16(smem_u32(kv_s + (size_t)i * 2 * row_elems + is_v * row_elems + gpos * 8), src);
         }
+        cp_async_wait_all();
         __syncthreads();
         for (int i = warp; i < n; i += kStepWarps) {
+            const uint16_t *krow = kv_s + (size_t)i * 2 * row_elems;
             for (int kv = 0; kv < Hkv; ++kv) {
                 float kf[8];
-                unpack8(ldg_nc_v4(a.k_cache + (toks[i] * Hkv + kv) * kHeadDim + lane * 8), kf);
+                unpack8(*reinterpret_cast<const uint4 *>(krow + kv * kHeadDim + lane * 8), kf);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float *qh = q_s + (kv * G + g) * kHeadDim + lane * 8;
@@ -558,7 +724,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
 #pragma unroll
             for (int g = 0; g < G; ++g) acc[g] *= s_alpha[kv_t * G + g];
             for (int i = 0; i < n; ++i) {
-                const float v = bf16_bits_to_float(__ldg(a.v_cache + (toks[i] * Hkv + kv_t) * kHeadDim + d_t));
+                const float v = bf16_bits_to_float(kv_s[(size_t)i * 2 * row_elems + row_elems + kv_t * kHeadDim + d_t]);
 #pragma unroll
                 for (int g = 0; g < G; ++g) acc[g] = fmaf(pw[(kv_t * G + g) * kAttnTok + i], v, acc[g]);
             }
@@ -575,72 +741,88 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
 #pragma unroll
         for (int g = 0; g < G; ++g) mypart[2 * Hq + (kv_t * G + g) * kHeadDim + d_t] = acc[g];
     }
+    STEP_TRACE(7);
 
-    // ---- 7. merge the row's partials; each CTA finishes a slice of the Hq x 256 outputs
-    const int r3 = row_arrive(rs, cr, a.hdr, row, &s_flag);
+    // ---- 6. merge the row's partials; each CTA finishes a slice of the Hq x 256 outputs
+    const int r3 = bar_arrive(rs, g0, bar_k, cr, a.hdr, row, &s_flag);
     if (r3 < 0) return;
-    if (r3 == 1) row_release(rs);
+    if (r3 == 1) bar_release(rs, g0, bar_k);
+    ++bar_k;
     __syncthreads();
+    STEP_TRACE(8);
     const float *parts = a.part + (size_t)first * Hq * (kHeadDim + 2);
     const int stride = Hq * (kHeadDim + 2);
     const int n_out = Hq * kHeadDim;
     const int o_lo = n_out * jj / cr, o_hi = n_out * (jj + 1) / cr;
-    const int h_lo = o_lo / kHeadDim, h_hi = (o_hi - 1) / kHeadDim;
-    // per head in the slice: M = max m_j, weights w_j = 2^(m_j - M), L = sum l_j w_j
-    float *w_s = reinterpret_cast<float *>(smem + kRingOff);              // [heads][cr]
-    for (int h = h_lo; h <= h_hi && o_lo < o_hi; ++h) {
-        float mx = -INFINITY;
-        for (int j = tid; j < cr; j += kStepThreads) mx = fmaxf(mx, __ldcg(&parts[(size_t)j * stride + h]));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) reinterpret_cast<float *>(s_wsum)[warp] = mx;
-        __syncthreads();
-        float M = -INFINITY;
-        for (int w = 0; w < kStepWarps; ++w) M = fmaxf(M, reinterpret_cast<float *>(s_wsum)[w]);
-        __syncthreads();
-        float lsum = 0.f;
-        for (int j = tid; j < cr; j += kStepThreads) {
-            const float mj = __ldcg(&parts[(size_t)j * stride + h]);
-            const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-            w_s[(h - h_lo) * cr + j] = wj;
-            lsum = fmaf(__ldcg(&parts[(size_t)j * stride + Hq + h]), wj, lsum);
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-        if (lane == 0) reinterpret_cast<float *>(s_wsum)[warp] = lsum;
-        __syncthreads();
-        if (tid == 0) {
-            float L = 0.f;
-            for (int w = 0; w < kStepWarps; ++w) L += reinterpret_cast<float *>(s_wsum)[w];
-            s_m[h - h_lo] = M;
-            s_l[h - h_lo] = L;
-        }
-        __syncthreads();
-    }
-    // outputs: `tpo` threads per output, each summing a strided subset of the partials
+    const int h_lo = o_lo / kHeadDim, h_hi = o_hi > o_lo ? (o_hi - 1) / kHeadDim : h_lo - 1;
+    const int nh = h_hi - h_lo + 1;
+    float *w_s = reinterpret_cast<float *>(smem + kRingOff);           // [nh][cr] m, then weights
+    float *l_s = w_s + 2 * kMaxGroup * kMaxStepCtas;                    // [nh][cr] l
     const int n_my = o_hi - o_lo;
-    int tpo = 1;
+    int tpo = 1;                                                        // threads per output
     while (tpo < 32 && (tpo * 2) * n_my <= kStepThreads) tpo *= 2;
     const int sub = tid % tpo;
+    // one round trip: (m, l) of the slice's heads and this thread's acc values
+    for (int idx = tid; idx < nh * cr; idx += kStepThreads) {
+        const int h = h_lo + idx / cr, j = idx % cr;
+        w_s[idx] = __ldcg(&parts[(size_t)j * stride + h]);
+        l_s[idx] = __ldcg(&parts[(size_t)j * stride + Hq + h]);
+    }
     for (int o_base = 0; o_base < n_my; o_base += kStepThreads / tpo) {
         const int oi = o_base + tid / tpo;
-        float s = 0.f;
-        int o = 0, h = 0;
+        float av[kMergeRegs];
+        int o = 0, h = 0, d = 0;
         if (oi < n_my) {
             o = o_lo + oi;
             h = o / kHeadDim;
-            const int d = o % kHeadDim;
+            d = o % kHeadDim;
+        }
+#pragma unroll
+        for (int r = 0; r < kMergeRegs; ++r) {
+            const int j = sub + r * tpo;
+            av[r] = (oi < n_my && j < cr) ? __ldcg(&parts[(size_t)j * stride + 2 * Hq + h * kHeadDim + d]) : 0.f;
+        }
+        __syncthreads();
+        if (o_base == 0) {
+            for (int hh = warp; hh < nh; hh += kStepWarps) {
+                float M = -INFINITY;
+                for (int j = lane; j < cr; j += 32) M = fmaxf(M, w_s[hh * cr + j]);
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                float L = 0.f;
+                for (int j = lane; j < cr; j += 32) {
+                    const float mj = w_s[hh * cr + j];
+                    const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+                    w_s[hh * cr + j] = wj;
+                    L = fmaf(l_s[hh * cr + j], wj, L);
+                }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+                if (lane == 0) {
+                    s_m[hh] = M;
+                    s_l[hh] = L;
+                }
+            }
+            __syncthreads();
+        }
+        float s = 0.f;
+        if (oi < n_my) {
             const float *wv = w_s + (h - h_lo) * cr;
-            for (int j = sub; j < cr; j += tpo) s = fmaf(__ldcg(&parts[(size_t)j * stride + 2 * Hq + h * kHeadDim + d]), wv[j], s);
+#pragma unroll
+            for (int r = 0; r < kMergeRegs; ++r) {
+                const int j = sub + r * tpo;
+                if (j < cr) s = fmaf(av[r], wv[j], s);
+            }
         }
         for (int off = tpo >> 1; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
         if (oi < n_my && sub == 0) {
             const float L = s_l[h - h_lo];
             a.out[(int64_t)row * n_out + o] = float_to_bf16_bits(s / L);
-            if (a.lse != nullptr && (o % kHeadDim) == 0)
-                a.lse[(int64_t)row * Hq + h] = (s_m[h - h_lo] + log2f(L)) * kLn2;
+            if (a.lse != nullptr && d == 0) a.lse[(int64_t)row * Hq + h] = (s_m[h - h_lo] + log2f(L)) * kLn2;
         }
     }
+    STEP_TRACE(9);
+#undef STEP_TRACE
 }
 
 // ------------------------------------------------------------------------------ launcher
@@ -708,6 +890,8 @@ cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st) {
     a.hist = reinterpret_cast<uint32_t *>(w + L.hist);
     a.cands = reinterpret_cast<unsigned long long *>(w + L.cands);
     a.part = reinterpret_cast<float *>(w + L.part);
+    a.pub = reinterpret_cast<unsigned long long *>(w + L.pub);
+    a.trace = reinterpret_cast<unsigned long long *>(w + L.trace);
     const int G = a.n_q_heads / a.n_kv_heads;
     const int ctas = decode_step_grid(G);
     if (ctas < a.B || ctas == 0) return cudaErrorInvalidConfiguration;

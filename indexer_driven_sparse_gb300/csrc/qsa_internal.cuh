@@ -29,6 +29,8 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "status block must be 256 bytes");
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int32_t kDebugStallBarrier = 0x5741171;   // written only by the device-timeout test
+constexpr int32_t kDebugTrace = 0x7ACE;             // record per-CTA phase timestamps (qsa_decode_step)
+constexpr int kTraceSlots = 16;
 constexpr uint64_t kWaitLimitNs = 250ull * 1000 * 1000;   // every device-side wait gives up after 250 ms
 
 enum Where : int32_t {
@@ -162,9 +164,11 @@ struct StepArgs {
     uint32_t *hist;
     unsigned long long *cands;
     float *part;
+    unsigned long long *pub;     // [kMaxStepCtas][513] published local top-K keys + flag
+    unsigned long long *trace;   // [kMaxStepCtas][kTraceSlots] globaltimer stamps
 };
 struct StepLayout {
-    size_t rows, hist, cands, part, total;
+    size_t rows, hist, cands, part, pub, trace, total;
 };
 StepLayout step_layout(int B, int64_t max_blocks, int Hq);
 size_t decode_step_ws_bytes(int B, int64_t max_blocks, int Hq);
