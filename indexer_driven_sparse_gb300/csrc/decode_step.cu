@@ -17,7 +17,7 @@
 //      async copies (TMA engine), keeping the 32-bit order-preserving score keys of its
 //      range on chip and histogramming their top 12 bits.
 //   3. Each CTA publishes its exact local top-K keys (64-bit: score key << 32 | ~block),
-//      K = 2 x 512 / c rounded up to a power of two in [32, 512].
+//      K = 2 x 512 / c rounded up to a power of two in [16, 512].
 //   4. One row barrier. Every CTA then reads all published keys and computes the same
 //      exact 512th key T and every CTA's output offset. If some CTA might hold more than K
 //      selected blocks (its K-th key >= T), all CTAs take the exact fallback instead: a
@@ -53,7 +53,8 @@ constexpr size_t kKeysOff = kRingOff + (size_t)kRingBytes;
 constexpr size_t kHistOff = kKeysOff + (size_t)kMaxKeys * 4;
 constexpr size_t kQOff = kHistOff + (size_t)kHistBins * 4;          // query, bf16 [Hq][256]
 constexpr size_t kNewRowOff = kQOff + (size_t)2 * kMaxGroup * kHeadDim * 2;
-constexpr size_t kMbarOff = kNewRowOff + 256;
+constexpr size_t kRawOff = kNewRowOff + 256;                          // 4 raw key rows, bf16
+constexpr size_t kMbarOff = kRawOff + (size_t)kRatio * kIdxDim * 2;
 constexpr size_t kStepSmem = kMbarOff + 64;
 
 struct StepRowState {
@@ -191,8 +192,14 @@ __device__ void block_find_bin(const uint32_t *hist, int nbins, uint32_t need, i
     }
     if (lane == 0) s_wtot[warp] = s;
     __syncthreads();
-    uint32_t higher = 0;
-    for (int w = warp + 1; w < kStepWarps; ++w) higher += s_wtot[w];
+    // counts of the warps above this one: a suffix scan of the 16 warp totals in registers
+    uint32_t t = lane < kStepWarps ? s_wtot[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < kStepWarps; o <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, t, o);
+        if (lane + o < kStepWarps) t += v;
+    }
+    const uint32_t higher = __shfl_sync(0xffffffffu, t, (warp + 1) & 31) * (warp + 1 < kStepWarps ? 1u : 0u);
     const uint32_t S = s + higher;                // count in this thread's bins and above
     if (tid < nact && S >= need && S - x < need) {
         uint32_t run = S - x;
@@ -207,24 +214,61 @@ __device__ void block_find_bin(const uint32_t *hist, int nbins, uint32_t need, i
     __syncthreads();
 }
 
-// CTA-wide: the need-th largest of n 64-bit keys (shared or global memory) whose bits at
-// and above `start` are all equal (start = 64: no shared prefix). 11-bit radix passes,
-// stopping early once the chosen bin holds exactly the keys still needed.
+// CTA-wide: a threshold T such that exactly `need` of the nonzero 64-bit keys among
+// keys[0..n) (shared or global memory; zero marks an empty slot) are >= T. T is the
+// need-th largest key, or a value just above the next key down. The radix digits start
+// below the prefix that every nonzero key shares (found from their min and max), so the
+// histogram spreads instead of piling into a few hot bins; 11-bit passes stop as soon as
+// the chosen bin holds exactly the keys still needed. With `scratch` (capacity `cap`), the
+// first pass's chosen bin is compacted so later passes touch only its members.
+// Requires need <= number of nonzero keys; returns ~0 when there is none.
 __device__ unsigned long long select_kth_key64(const unsigned long long *keys, uint32_t n, uint32_t need,
-                                               int start, uint32_t *hist, int *s_d, uint32_t *s_above,
-                                               uint32_t *s_wtot) {
-    unsigned long long prefix = start >= 64 ? 0ull : (keys[0] >> start) << start;
-    int hi = start;
+                                               uint32_t *hist, int *s_d, uint32_t *s_above, uint32_t *s_wtot,
+                                               unsigned long long *s_red, unsigned long long *scratch = nullptr,
+                                               uint32_t cap = 0, uint32_t *s_cn = nullptr) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long mn = ~0ull, mx = 0ull;
+    for (uint32_t i = tid; i < n; i += kStepThreads) {
+        const unsigned long long k = keys[i];
+        if (k != 0ull) {
+            mn = k < mn ? k : mn;
+            mx = k > mx ? k : mx;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
+        const unsigned long long b = __shfl_xor_sync(0xffffffffu, mx, o);
+        mn = a < mn ? a : mn;
+        mx = b > mx ? b : mx;
+    }
+    if (lane == 0) {
+        s_red[warp] = mn;
+        s_red[kStepWarps + warp] = mx;
+    }
+    __syncthreads();
+    mn = ~0ull;
+    mx = 0ull;
+    for (int w = 0; w < kStepWarps; ++w) {
+        mn = s_red[w] < mn ? s_red[w] : mn;
+        mx = s_red[kStepWarps + w] > mx ? s_red[kStepWarps + w] : mx;
+    }
+    if (mx == 0ull) return ~0ull;
+    const unsigned long long diff = mn ^ mx;
+    if (diff == 0ull) return mx;                      // a single distinct key
+    int hi = 64 - __clzll((long long)diff);           // bits >= hi are shared by every nonzero key
+    unsigned long long prefix = hi >= 64 ? 0ull : (mx >> hi) << hi;
+    bool compacted = false;
     while (hi > 0) {
         const int width = hi >= 11 ? 11 : hi;
         const int shift = hi - width;
         const int nbins = 1 << width;
-        for (int i = threadIdx.x; i < 2048; i += kStepThreads) hist[i] = 0;
+        for (int i = tid; i < 2048; i += kStepThreads) hist[i] = 0;
         __syncthreads();
-        for (uint32_t i = threadIdx.x; i < n; i += kStepThreads) {
+        for (uint32_t i = tid; i < n; i += kStepThreads) {
             const unsigned long long k = keys[i];
-            const bool match = hi >= 64 || (k >> hi) == (prefix >> hi);
-            if (match) atomicAdd(&hist[(uint32_t)(k >> shift) & (nbins - 1)], 1u);
+            if (k != 0ull && (hi >= 64 || (k >> hi) == (prefix >> hi)))
+                atomicAdd(&hist[(uint32_t)(k >> shift) & (nbins - 1)], 1u);
         }
         __syncthreads();
         block_find_bin(hist, nbins < 256 ? 256 : nbins, need, s_d, s_above, s_wtot);
@@ -234,20 +278,178 @@ __device__ unsigned long long select_kth_key64(const unsigned long long *keys, u
         need -= *s_above;
         __syncthreads();
         if (in_bin == need) return prefix;           // the whole bin is kept
+        if (!compacted && scratch != nullptr && in_bin <= cap) {
+            // later passes see only the members of the chosen bin
+            if (tid == 0) *s_cn = 0;
+            __syncthreads();
+            for (uint32_t i = tid; i < n; i += kStepThreads) {
+                const unsigned long long k = keys[i];
+                if (k != 0ull && (k >> shift) == (prefix >> shift)) scratch[atomicAdd(s_cn, 1u)] = k;
+            }
+            __syncthreads();
+            keys = scratch;
+            n = *s_cn;
+            compacted = true;
+        }
         hi = shift;
     }
     return prefix;
+}
+
+// Register-resident variant of select_kth_key64 for n <= 8 x 512 keys: each thread keeps
+// its (at most 8) keys in registers, so no pass reloads them and every loop unrolls.
+__device__ unsigned long long select_kth_key64_reg(const unsigned long long *keys, uint32_t n, uint32_t need,
+                                                   uint32_t *hist, int *s_d, uint32_t *s_above, uint32_t *s_wtot,
+                                                   unsigned long long *s_red) {
+    constexpr int R = 8;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long kr[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t i = tid + r * kStepThreads;
+        kr[r] = i < n ? keys[i] : 0ull;
+    }
+    unsigned long long mn = ~0ull, mx = 0ull;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (kr[r] != 0ull) mn = kr[r] < mn ? kr[r] : mn;
+        mx = kr[r] > mx ? kr[r] : mx;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
+        const unsigned long long b = __shfl_xor_sync(0xffffffffu, mx, o);
+        mn = a < mn ? a : mn;
+        mx = b > mx ? b : mx;
+    }
+    if (lane == 0) {
+        s_red[warp] = mn;
+        s_red[kStepWarps + warp] = mx;
+    }
+    __syncthreads();
+    {
+        const unsigned long long a = lane < kStepWarps ? s_red[lane] : ~0ull;
+        const unsigned long long b = lane < kStepWarps ? s_red[kStepWarps + lane] : 0ull;
+        mn = a;
+        mx = b;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) {
+            const unsigned long long c = __shfl_xor_sync(0xffffffffu, mn, o);
+            const unsigned long long d = __shfl_xor_sync(0xffffffffu, mx, o);
+            mn = c < mn ? c : mn;
+            mx = d > mx ? d : mx;
+        }
+        mn = __shfl_sync(0xffffffffu, mn, 0);
+        mx = __shfl_sync(0xffffffffu, mx, 0);
+    }
+    if (mx == 0ull) return ~0ull;
+    const unsigned long long diff = mn ^ mx;
+    if (diff == 0ull) return mx;
+    int hi = 64 - __clzll((long long)diff);
+    unsigned long long prefix = hi >= 64 ? 0ull : (mx >> hi) << hi;
+    while (hi > 0) {
+        const int width = hi >= 11 ? 11 : hi;
+        const int shift = hi - width;
+        const int nbins = 1 << width;
+        for (int i = tid; i < 2048; i += kStepThreads) hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const unsigned long long k = kr[r];
+            if (k != 0ull && (hi >= 64 || (k >> hi) == (prefix >> hi)))
+                atomicAdd(&hist[(uint32_t)(k >> shift) & (nbins - 1)], 1u);
+        }
+        __syncthreads();
+        block_find_bin(hist, nbins < 256 ? 256 : nbins, need, s_d, s_above, s_wtot);
+        const int d = *s_d;
+        const uint32_t in_bin = hist[d];
+        prefix |= (unsigned long long)d << shift;
+        need -= *s_above;
+        __syncthreads();
+        if (in_bin == need) return prefix;
+        hi = shift;
+    }
+    return prefix;
+}
+
+// Warp 0: sum of vals[0..count) (shared memory) -> *out. Other warps skip.
+__device__ __forceinline__ void warp_sum_prefix(const uint32_t *vals, int count, int *out) {
+    if (threadIdx.x < 32) {
+        uint32_t sum = 0;
+        for (int j = threadIdx.x; j < count; j += 32) sum += vals[j];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (threadIdx.x == 0) *out = (int)sum;
+    }
+}
+
+// Sum each of NV values over the warp's 32 lanes; afterwards the lane holds the total of
+// value index `idx` (returned). Reduce-scatter: each level halves the values a lane keeps,
+// so the whole reduction takes NV - 1 + log2(32/NV) shuffles instead of 5 NV.
+template <int NV>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane, int *idx) {
+    int base = 0;
+#pragma unroll
+    for (int level = 0; (NV >> level) > 1; ++level) {
+        const int n = NV >> level;          // values still held
+        const int o = 16 >> level;          // exchange distance
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+        if (up) base += n / 2;
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 / NV; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    *idx = base;
+    return r;
 }
 
 __device__ __forceinline__ unsigned long long key64_of(uint32_t key, int64_t blk) {
     return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
 }
 
-// Published keys per CTA for a row split over c CTAs: 2 x 512 / c, a power of two in [32, 512].
+// Published keys per CTA for a row split over c CTAs: 2 x 512 / c, a power of two in [16, 512]
+// (a CTA holds 512 / c selected blocks on average; 16 leaves a wide margin at c = 152).
 __device__ __forceinline__ int pub_count(int c) {
-    int k = 32;
+    int k = 16;
     while (k < kMaxPub && k * c < 2 * kBlockTopK) k <<= 1;
     return k;
+}
+
+// Gather one attention chunk: the K and V rows (all KV heads) of up to kAttnTok tokens of
+// the row's token sequence (list blocks, then the query's own block) into shared memory.
+__device__ void gather_chunk(const StepArgs &a, uint16_t *dst, int j_base, int n, int n_list,
+                                          bool dense, const int32_t *sel, int64_t nb, int64_t base, int p, int row,
+                                          int row_elems) {
+    const int tok_elems = 2 * row_elems;
+    const int gran_per_tok = tok_elems * 2 / 16;                       // 16-byte granules per token
+    for (int gidx = threadIdx.x; gidx < n * gran_per_tok; gidx += kStepThreads) {
+        const int i = gidx / gran_per_tok;
+        const int rem = gidx - i * gran_per_tok;
+        const int is_v = rem >= gran_per_tok / 2;
+        const int gpos = rem - is_v * (gran_per_tok / 2);
+        const int j = j_base + i;
+        int64_t tk;
+        if (j < kRatio * n_list) {
+            const int64_t blk = dense ? (j >> 2) : sel[j >> 2];
+            if (blk < 0 || blk >= nb) {               // never expected: flag it, read a safe row
+                record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereStep, row);
+                tk = p;
+            } else {
+                tk = kRatio * blk + (j & 3);
+            }
+        } else {
+            tk = kRatio * nb + (j - kRatio * n_list);
+        }
+        const uint16_t *src = (is_v ? a.v_cache : a.k_cache) + (base + tk) * row_elems + gpos * 8;
+        cp_async16(smem_u32(dst + (size_t)i * tok_elems + is_v * row_elems + gpos * 8), src);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 template <int G>
@@ -257,6 +459,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kHistOff);
     uint16_t *q_b = reinterpret_cast<uint16_t *>(smem + kQOff);
     uint16_t *newrow = reinterpret_cast<uint16_t *>(smem + kNewRowOff);
+    uint16_t *rawrows = reinterpret_cast<uint16_t *>(smem + kRawOff);
     unsigned long long *ring64 = reinterpret_cast<unsigned long long *>(smem + kRingOff);
     const uint32_t mbar0 = smem_u32(smem + kMbarOff);
     const uint32_t ring0 = smem_u32(smem + kRingOff);
@@ -266,6 +469,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     __shared__ uint32_t s_above, s_n;
     __shared__ unsigned long long s_kmin;
     __shared__ unsigned long long s_kth[kMaxStepCtas];
+    __shared__ unsigned long long s_red[2 * kStepWarps];
     __shared__ int32_t s_sel[kBlockTopK];
     __shared__ uint32_t s_cnt[kMaxStepCtas];
     __shared__ uint32_t s_wsum[kStepWarps];
@@ -335,28 +539,25 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     for (int i = tid; i < Hq * kHeadDim / 8; i += kStepThreads)
         cp_async16(smem_u32(q_b + i * 8), a.q + (int64_t)row * Hq * kHeadDim + i * 8);
     asm volatile("cp.async.commit_group;" ::: "memory");
-    // ---- 1. re-pool block nb-1 (exact mean of its four raw keys)
-    if (owner_new && warp == 1 && lane < 16) {
-        const uint16_t *src = a.raw_idx_k + (base + kRatio * (nb - 1)) * kIdxDim + lane * 8;
-        float f0[8], f1[8], f2[8], f3[8];
-        unpack8(ldg_nc_v4(src), f0);
-        unpack8(ldg_nc_v4(src + kIdxDim), f1);
-        unpack8(ldg_nc_v4(src + 2 * kIdxDim), f2);
-        unpack8(ldg_nc_v4(src + 3 * kIdxDim), f3);
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const double s0 = (((double)f0[2 * i] + (double)f1[2 * i]) + (double)f2[2 * i]) + (double)f3[2 * i];
-            const double s1 = (((double)f0[2 * i + 1] + (double)f1[2 * i + 1]) + (double)f2[2 * i + 1]) +
-                              (double)f3[2 * i + 1];
-            w[i] = (uint32_t)double_to_bf16_rne(s0 * 0.25) | ((uint32_t)double_to_bf16_rne(s1 * 0.25) << 16);
-        }
-        const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4 *>(a.pooled + (boff + nb - 1) * kIdxDim + lane * 8) = v;
-        *reinterpret_cast<uint4 *>(newrow + lane * 8) = v;
-    }
+    // ---- 1a. the four raw key rows of block nb-1 (pooled after the scan, off its critical path)
+    if (owner_new && tid < kRatio * kIdxDim / 8)
+        cp_async16(smem_u32(rawrows + tid * 8), a.raw_idx_k + (base + kRatio * (nb - 1)) * kIdxDim + tid * 8);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     STEP_TRACE(1);
 
+    if (dense) {                          // dense rows re-pool block nb-1 here (no scan)
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        if (owner_new && tid < kIdxDim) {
+            const double s4 = (((double)bf16_bits_to_float(rawrows[tid]) +
+                                (double)bf16_bits_to_float(rawrows[kIdxDim + tid])) +
+                               (double)bf16_bits_to_float(rawrows[2 * kIdxDim + tid])) +
+                              (double)bf16_bits_to_float(rawrows[3 * kIdxDim + tid]);
+            a.pooled[(boff + nb - 1) * kIdxDim + tid] = double_to_bf16_rne(s4 * 0.25);
+        }
+    }
+
+    bool balanced = dense;                // the row's whole selection is known to every CTA
     int bar_k = 0;                        // barriers completed by this row in this launch
     unsigned long long t64 = 0ull;        // exact threshold key (dense: select all)
     int out_off = (int)lo;                // this CTA's first output slot (dense: lo)
@@ -410,6 +611,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                          mbar0 + 8 * stage);
             }
         }
+        // ---- 1b. re-pool block nb-1: exact fp64 mean of its four raw keys, one RNE to bf16
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        if (owner_new && tid < kIdxDim) {
+            const double s4 = (((double)bf16_bits_to_float(rawrows[tid]) +
+                                (double)bf16_bits_to_float(rawrows[kIdxDim + tid])) +
+                               (double)bf16_bits_to_float(rawrows[2 * kIdxDim + tid])) +
+                              (double)bf16_bits_to_float(rawrows[3 * kIdxDim + tid]);
+            const uint16_t v = double_to_bf16_rne(s4 * 0.25);
+            newrow[tid] = v;
+            a.pooled[(boff + nb - 1) * kIdxDim + tid] = v;
+        }
+        __syncthreads();
         if (owner_new && warp == 0) {          // the freshly pooled block, from shared memory
             float f[8];
             unpack8(*reinterpret_cast<const uint4 *>(newrow + c16 * 8), f);
@@ -462,8 +676,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 }
             } else {
                 // threshold value with exactly K keys at or above it (need not be a key itself)
-                const unsigned long long tk =
-                    select_kth_key64(ring64, nc, (uint32_t)K, 64, hist, &s_d, &s_above, s_wsum);
+                const unsigned long long tk = select_kth_key64(ring64, nc, (uint32_t)K, hist, &s_d, &s_above, s_wsum,
+                                                               s_red, ring64 + nc, (uint32_t)(kRingBytes / 8) - nc,
+                                                               &s_cnt[1]);
                 if (tid == 0) s_kmin = ~0ull;
                 __syncthreads();
                 for (uint32_t i = tid; i < nc; i += kStepThreads) {
@@ -489,33 +704,67 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         STEP_TRACE(4);
         const unsigned long long *pub_row = a.pub + (size_t)first * (kMaxPub + 1);
         const int n_slots = cr * K;
-        for (int i = tid; i < n_slots; i += kStepThreads) {
-            const int j = i / K, s = i % K;
-            ring64[i] = __ldcg(&pub_row[(size_t)j * (kMaxPub + 1) + s]);
-        }
+        const int log2k = __ffs(K) - 1;
+        for (int i = tid; i < n_slots; i += kStepThreads)
+            ring64[i] = __ldcg(&pub_row[(size_t)(i >> log2k) * (kMaxPub + 1) + (i & (K - 1))]);
         for (int j = tid; j < cr; j += kStepThreads) s_kth[j] = __ldcg(&pub_row[(size_t)j * (kMaxPub + 1) + kMaxPub]);
         __syncthreads();
+        STEP_TRACE(14);
         // empty slots hold 0, below every real key, so they never reach the threshold;
         // exactly 512 published keys are >= t64
-        t64 = select_kth_key64(ring64, (uint32_t)n_slots, kBlockTopK, 64, hist, &s_d, &s_above, s_wsum);
+        t64 = n_slots <= 8 * kStepThreads
+                  ? select_kth_key64_reg(ring64, (uint32_t)n_slots, kBlockTopK, hist, &s_d, &s_above, s_wsum, s_red)
+                  : select_kth_key64(ring64, (uint32_t)n_slots, kBlockTopK, hist, &s_d, &s_above, s_wsum, s_red,
+                                     ring64 + n_slots, (uint32_t)(kRingBytes / 8 - n_slots), &s_n);
+        STEP_TRACE(15);
         // a CTA with unpublished keys whose K-th key reaches the threshold might hold more
         if (tid == 0) s_overflow = 0;
+        for (int j = tid; j < cr; j += kStepThreads) s_cnt[j] = 0;
         __syncthreads();
         for (int j = tid; j < cr; j += kStepThreads)
             if (s_kth[j] != 0ull && s_kth[j] >= t64) s_overflow = 1;
+        // offsets: selected published keys of every earlier CTA of the row
+        for (int i = tid; i < n_slots; i += kStepThreads)
+            if (ring64[i] >= t64) atomicAdd(&s_cnt[i >> log2k], 1u);
         __syncthreads();
-        if (!s_overflow) {
-            // offsets: selected published keys of every earlier CTA of the row
-            for (int j = tid; j < cr; j += kStepThreads) s_cnt[j] = 0;
-            __syncthreads();
-            for (int i = tid; i < n_slots; i += kStepThreads)
-                if (ring64[i] >= t64) atomicAdd(&s_cnt[i / K], 1u);
-            __syncthreads();
-            if (tid == 0) {
-                int run = 0;
-                for (int j = 0; j < jj; ++j) run += (int)s_cnt[j];
-                s_flag = run;
+        if (!s_overflow && K <= 64) {
+            // Every CTA rebuilds the row's whole ascending selection from the published keys:
+            // exclusive prefix of the per-CTA counts, then each selected key's slot is its
+            // CTA's offset plus the number of selected keys of that CTA with a lower block id.
+            if (warp == 0) {
+                uint32_t run = 0;
+                for (int j0 = 0; j0 < cr; j0 += 32) {
+                    const uint32_t v = j0 + lane < cr ? s_cnt[j0 + lane] : 0u;
+                    uint32_t inc = v;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+                        if (lane >= o) inc += t;
+                    }
+                    if (j0 + lane < cr) s_cnt[j0 + lane] = run + inc - v;
+                    run += __shfl_sync(0xffffffffu, inc, 31);
+                }
             }
+            for (int i = tid; i < kBlockTopK; i += kStepThreads) s_sel[i] = -1;
+            __syncthreads();
+            for (int i = tid; i < n_slots; i += kStepThreads) {
+                const unsigned long long k = ring64[i];
+                if (k >= t64) {
+                    const int j = i >> log2k;
+                    const uint32_t blk = 0xFFFFFFFFu - (uint32_t)k;
+                    uint32_t r = 0;
+                    for (int s2 = 0; s2 < K; ++s2) {
+                        const unsigned long long k2 = ring64[(j << log2k) + s2];
+                        r += (k2 >= t64 && 0xFFFFFFFFu - (uint32_t)k2 < blk) ? 1u : 0u;
+                    }
+                    const uint32_t pos = s_cnt[j] + r;
+                    if (pos < (uint32_t)kBlockTopK) s_sel[pos] = (int32_t)blk;
+                }
+            }
+            __syncthreads();
+            balanced = true;
+        } else if (!s_overflow) {
+            warp_sum_prefix(s_cnt, jj, &s_flag);
             __syncthreads();
             out_off = s_flag;
         } else {
@@ -581,7 +830,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 __syncthreads();
                 const unsigned long long *src = in_smem ? ring64 : cands;
                 const unsigned long long tt =
-                    n_c ? select_kth_key64(src, n_c, need, 64 - 12, hist, &s_d, &s_above, s_wsum) : ~0ull;
+                    n_c ? select_kth_key64(src, n_c, need, hist, &s_d, &s_above, s_wsum, s_red) : ~0ull;
                 for (int i = tid; i < cr; i += kStepThreads) s_cnt[i] = 0;
                 __syncthreads();
                 for (uint32_t i = tid; i < n_c; i += kStepThreads) {
@@ -595,15 +844,26 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                     }
                 }
                 __syncthreads();
-                if (tid == 0) {
-                    int32_t run = 0;
-                    for (int j = 0; j < cr; ++j) {
-                        rs->offset[j] = run;
-                        run += __ldcg(&rs->definite[j]) + (int32_t)s_cnt[j];
+                for (int j = tid; j < cr; j += kStepThreads) s_cnt[j] += (uint32_t)__ldcg(&rs->definite[j]);
+                __syncthreads();
+                if (warp == 0) {            // exclusive prefix over the CTAs of the row
+                    uint32_t run = 0;
+                    for (int j0 = 0; j0 < cr; j0 += 32) {
+                        const uint32_t v = j0 + lane < cr ? s_cnt[j0 + lane] : 0u;
+                        uint32_t inc = v;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+                            if (lane >= o) inc += t;
+                        }
+                        if (j0 + lane < cr) rs->offset[j0 + lane] = (int32_t)(run + inc - v);
+                        run += __shfl_sync(0xffffffffu, inc, 31);
                     }
-                    rs->t64 = tt;
-                    rs->cand_count = 0;
-                    if (run != kBlockTopK) record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereStep, row);
+                    if (lane == 0) {
+                        rs->t64 = tt;
+                        rs->cand_count = 0;
+                        if (run != (uint32_t)kBlockTopK) record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereStep, row);
+                    }
                 }
                 bar_release(rs, g0, bar_k);
             }
@@ -615,20 +875,30 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         STEP_TRACE(5);
     }
 
-    // ---- 5a. this CTA's selected blocks, ascending, and their output slots
+    // ---- 5a. selected blocks, ascending, and their output slots. A balanced sparse row writes
+    // an equal share of the rebuilt list; otherwise each CTA lists its own range's blocks.
     int32_t *blocks_row = a.blocks + (int64_t)row * kBlockTopK;
     int nsel = 0;
-    for (int base_i = 0; base_i < n_mine; base_i += kStepThreads) {
+    if (balanced && !dense) {
+        nsel = kBlockTopK;
+        for (int i = kBlockTopK * jj / cr + tid; i < kBlockTopK * (jj + 1) / cr; i += kStepThreads)
+            blocks_row[i] = s_sel[i];
+    }
+    for (int base_i = 0; base_i < n_mine && !(balanced && !dense); base_i += kStepThreads) {
         const int i = base_i + tid;
         const bool take = i < n_mine && (dense || key64_of(keys[i], lo + i) >= t64);
         const unsigned bal = __ballot_sync(0xffffffffu, take);
         if (lane == 0) s_wsum[warp] = __popc(bal);
         __syncthreads();
-        int before = nsel, total = 0;
-        for (int w = 0; w < kStepWarps; ++w) {
-            if (w < warp) before += s_wsum[w];
-            total += s_wsum[w];
+        const uint32_t wc = lane < kStepWarps ? s_wsum[lane] : 0u;
+        uint32_t inc = wc;
+#pragma unroll
+        for (int o = 1; o < kStepWarps; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
         }
+        const int total = (int)__shfl_sync(0xffffffffu, inc, kStepWarps - 1);
+        int before = nsel + (int)(__shfl_sync(0xffffffffu, inc, warp) - __shfl_sync(0xffffffffu, wc, warp));
         before += __popc(bal & ((1u << lane) - 1u));
         if (take && before < kBlockTopK && out_off + before < kBlockTopK) {
             s_sel[before] = (int32_t)(lo + i);
@@ -646,17 +916,34 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     STEP_TRACE(6);
 
     // ---- 5b. attention over this CTA's tokens (+ the query's own block in the last CTA).
-    // Each step gathers up to 32 tokens' K and V rows (all KV heads) into shared memory with
-    // 16-byte async copies issued together, then computes from shared memory.
-    const bool last_cta = jj == cr - 1;
-    const int n_tail = last_cta ? (int)(p - kRatio * nb + 1) : 0;
-    const int n_tok = kRatio * nsel + n_tail;
+    // Tokens go in chunks of 32: each chunk's K and V rows (all KV heads) are gathered into
+    // one half of the ring with 16-byte async copies, two chunks in flight, and computed from
+    // shared memory. The scores' keys and histogram are dead now: q (fp32) and the chunk's
+    // logits reuse their space.
+    // token sequence: the list's blocks (4 tokens each) then the query's own block; a balanced
+    // row splits it evenly over its CTAs, otherwise each CTA takes its own list (+ the tail in
+    // the row's last CTA)
+    const int n_tail_row = (int)(p - kRatio * nb + 1);
+    const int n_list = dense ? (int)nb : nsel;
+    int t_lo = 0, t_hi = kRatio * nsel + (jj == cr - 1 ? n_tail_row : 0);
+    if (balanced) {
+        const int n_total = kRatio * n_list + n_tail_row;
+        t_lo = n_total * jj / cr;
+        t_hi = n_total * (jj + 1) / cr;
+    }
+    const int n_tok = t_hi - t_lo;
     const int row_elems = Hkv * kHeadDim;                              // one token's K (or V) row
-    float *q_s = reinterpret_cast<float *>(smem + kRingOff);           // [Hq][256]
-    float *pw = q_s + 2 * kMaxGroup * kHeadDim;                        // [Hq][kAttnTok]
-    uint16_t *kv_s = reinterpret_cast<uint16_t *>(pw + 2 * kMaxGroup * kAttnTok);   // [32][K row | V row]
+    const int tok_elems = 2 * row_elems;                               // K row | V row
+    float *q_s = reinterpret_cast<float *>(smem + kKeysOff);           // [Hq][256]
+    float *pw = reinterpret_cast<float *>(smem + kHistOff);            // [Hq][kAttnTok]
+    uint16_t *const kv_ring = reinterpret_cast<uint16_t *>(smem + kRingOff);   // two halves of 64 KiB
+    const int gran_per_tok = tok_elems * 2 / 16;                       // 16-byte granules per token
+    const int n_att_chunks = (n_tok + kAttnTok - 1) / kAttnTok;
     asm volatile("cp.async.wait_group 0;" ::: "memory");            // the prefetched query
-    __syncthreads();
+    __syncthreads();                                                   // ring, keys, hist are free
+    for (int c = 0; c < n_att_chunks && c < 2; ++c)
+        gather_chunk(a, kv_ring + (size_t)(c & 1) * (kRingBytes / 4), t_lo + c * kAttnTok,
+                     min(kAttnTok, n_tok - c * kAttnTok), n_list, dense, s_sel, nb, base, p, row, row_elems);
     for (int i = tid; i < Hq * kHeadDim; i += kStepThreads) q_s[i] = bf16_bits_to_float(q_b[i]) * a.scale_log2;
     if (tid < Hq) {
         s_m[tid] = -INFINITY;
@@ -666,40 +953,46 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     float acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = 0.f;
-    const int gran_per_row = row_elems * 2 / 16;                       // 16-byte granules per K row
-    for (int t0 = 0; t0 < n_tok; t0 += kAttnTok) {
+    for (int c = 0; c < n_att_chunks; ++c) {
+        const int t0 = c * kAttnTok;
         const int n = min(kAttnTok, n_tok - t0);
-        for (int gidx = tid; gidx < n * 2 * gran_per_row; gidx += kStepThreads) {
-            const int i = gidx / (2 * gran_per_row);
-            const int rem = gidx % (2 * gran_per_row);
-            const int is_v = rem >= gran_per_row;
-            const int gpos = rem - is_v * gran_per_row;
-            const int j = t0 + i;
-            const int64_t tk = j < kRatio * nsel ? (int64_t)kRatio * s_sel[j >> 2] + (j & 3)
-                                                 : kRatio * nb + (j - kRatio * nsel);
-            const uint16_t *src = (is_v ? a.v_cache : a.k_cache) + (base + tk) * row_elems + gpos * 8;
-            cp_async16(smem_u32(kv_s + (size_t)i * 2 * row_elems + is_v * row_elems + gpos * 8), src);
-        }
-        cp_async_wait_all();
+        const uint16_t *buf = kv_ring + (size_t)(c & 1) * (kRingBytes / 4);
+        if (c + 1 < n_att_chunks) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
+        if (c == 0) STEP_TRACE(10);
+        // logits: one warp per token, 8 dims per lane per KV head, all heads reduced at once
         for (int i = warp; i < n; i += kStepWarps) {
-            const uint16_t *krow = kv_s + (size_t)i * 2 * row_elems;
-            for (int kv = 0; kv < Hkv; ++kv) {
+            const uint16_t *krow = buf + (size_t)i * tok_elems;
+            float v[2 * G];
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
                 float kf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(krow + kv * kHeadDim + lane * 8), kf);
+                if (kv < Hkv) unpack8(*reinterpret_cast<const uint4 *>(krow + kv * kHeadDim + lane * 8), kf);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float *qh = q_s + (kv * G + g) * kHeadDim + lane * 8;
-                    float s = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) s = fmaf(kf[e], qh[e], s);
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                    if (lane == 0) pw[(kv * G + g) * kAttnTok + i] = s;
+                    float sum = 0.f;
+                    if (kv < Hkv) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(q_s + (kv * G + g) * kHeadDim + lane * 8);
+                        const float4 qb = *reinterpret_cast<const float4 *>(q_s + (kv * G + g) * kHeadDim + lane * 8 + 4);
+                        sum = kf[0] * qa.x;
+                        sum = fmaf(kf[1], qa.y, sum);
+                        sum = fmaf(kf[2], qa.z, sum);
+                        sum = fmaf(kf[3], qa.w, sum);
+                        sum = fmaf(kf[4], qb.x, sum);
+                        sum = fmaf(kf[5], qb.y, sum);
+                        sum = fmaf(kf[6], qb.z, sum);
+                        sum = fmaf(kf[7], qb.w, sum);
+                    }
+                    v[kv * G + g] = sum;
                 }
             }
+            int idx = 0;
+            const float tot = warp_reduce_scatter<2 * G>(v, lane, &idx);
+            if ((lane & (32 / (2 * G) - 1)) == 0 && idx < Hq) pw[idx * kAttnTok + i] = tot;
         }
         __syncthreads();
+        if (c == 0) STEP_TRACE(11);
         for (int h = warp; h < Hq; h += kStepWarps) {
             const float x = lane < n ? pw[h * kAttnTok + lane] : -INFINITY;
             float cm = x;
@@ -723,13 +1016,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         if (kv_t < Hkv) {
 #pragma unroll
             for (int g = 0; g < G; ++g) acc[g] *= s_alpha[kv_t * G + g];
+            const uint16_t *vcol = buf + row_elems + kv_t * kHeadDim + d_t;
+#pragma unroll 4
             for (int i = 0; i < n; ++i) {
-                const float v = bf16_bits_to_float(kv_s[(size_t)i * 2 * row_elems + row_elems + kv_t * kHeadDim + d_t]);
+                const float v = bf16_bits_to_float(vcol[(size_t)i * tok_elems]);
 #pragma unroll
                 for (int g = 0; g < G; ++g) acc[g] = fmaf(pw[(kv_t * G + g) * kAttnTok + i], v, acc[g]);
             }
         }
         __syncthreads();
+        if (c == 0) STEP_TRACE(12);
+        if (c + 2 < n_att_chunks)
+            gather_chunk(a, kv_ring + (size_t)(c & 1) * (kRingBytes / 4), t_lo + (c + 2) * kAttnTok,
+                         min(kAttnTok, n_tok - (c + 2) * kAttnTok), n_list, dense, s_sel, nb, base, p, row,
+                         row_elems);
     }
     // partial of this CTA: m[Hq], l[Hq], acc[Hq][256]
     float *mypart = a.part + (size_t)blockIdx.x * Hq * (kHeadDim + 2);
@@ -783,6 +1083,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
             av[r] = (oi < n_my && j < cr) ? __ldcg(&parts[(size_t)j * stride + 2 * Hq + h * kHeadDim + d]) : 0.f;
         }
         __syncthreads();
+        if (o_base == 0) STEP_TRACE(13);
         if (o_base == 0) {
             for (int hh = warp; hh < nh; hh += kStepWarps) {
                 float M = -INFINITY;

@@ -71,18 +71,28 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
 }
 
 // Round a double to the nearest bf16 (ties to even) in one step. bf16 keeps 8
-// significant bits with fp32's exponent range: near |x| in [2^e, 2^(e+1)) the
-// spacing is 2^(e-7), and 2^-133 below 2^-126. Scaling by a power of two is exact,
-// rint() rounds half to even, and the result converts to fp32 exactly.
+// significant bits with fp32's exponent range: near |x| in [2^e, 2^(e+1)) the spacing is
+// 2^(e-7), and 2^-133 below 2^-126.
+// Normal range: round the 52-bit fp64 fraction at bit 45 with integer arithmetic (add
+// half an ulp minus one plus the kept lsb, clear the dropped bits); the result has 8
+// significant bits and converts to fp32 exactly. Elsewhere (zero, subnormal bf16, inf,
+// NaN): scale by a power of two (exact), rint() (half to even), scale back.
 __device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+    const unsigned e = (unsigned)(b >> 52) & 0x7FFu;
+    const uint16_t sign = (uint16_t)((b >> 48) & 0x8000u);
+    if (e >= 1023u - 126u && e < 1023u + 128u) {
+        const unsigned long long lsb = (b >> 45) & 1ull;
+        unsigned long long r = b + 0x00000FFFFFFFFFFFull + lsb;
+        r &= ~0x00001FFFFFFFFFFFull;
+        if ((((unsigned)(r >> 52)) & 0x7FFu) >= 1023u + 128u) return sign | 0x7F80;
+        return (uint16_t)(__float_as_uint((float)__longlong_as_double((long long)r)) >> 16);
+    }
     if (isnan(x)) return 0x7FC0;
-    const uint16_t sign = signbit(x) ? 0x8000 : 0;
     const double ax = fabs(x);
     if (isinf(ax)) return sign | 0x7F80;
-    int e = (ax == 0.0) ? -126 : ilogb(ax);
-    if (e < -126) e = -126;
-    const double r = ldexp(rint(ldexp(ax, 7 - e)), e - 7);
-    if (r >= 0x1p128) return sign | 0x7F80;
+    if (ax >= 0x1p127) return sign | 0x7F80;    // |x| >= 2^128: overflow
+    const double r = ldexp(rint(ldexp(ax, 133)), -133);
     return sign | (uint16_t)(__float_as_uint((float)r) >> 16);
 }
 
