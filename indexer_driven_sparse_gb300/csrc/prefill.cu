@@ -13,9 +13,12 @@ size_t prefill_scratch_bytes(int Nc, int Hq, int Hkv) {
 
 cudaError_t launch_sparse_prefill(const AttnArgs &a, int interval_tokens, WsHeader *hdr, void *scratch,
                                   size_t scratch_bytes, cudaStream_t st) {
-    (void)interval_tokens;
     (void)scratch;
     (void)scratch_bytes;
+    if (a.rows == 0) return cudaSuccess;
+    // tensor-core interval walk for 8 or 16 query heads per KV head; otherwise one CTA per
+    // (query, KV head) on the CUDA cores
+    if (prefill_tc_supported(a.n_q_heads, a.n_kv_heads)) return launch_prefill_tc(a, interval_tokens, hdr, st);
     return launch_attn_rows(a, hdr, st);
 }
 

@@ -231,6 +231,9 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
              "interval_tokens = %d must be a positive multiple of 128", interval_tokens);
     QSA_TRY(check_ws(QSA_OP_SPARSE_PREFILL_CHUNK, cfg, Nc, 0, ws, ws_bytes));
     if (Nc == 0) return ok();
+    if (prefill_tc_supported(cfg->n_q_heads, cfg->n_kv_heads) && ((int64_t)p0 + Nc) / kRatio + 1 > kPrefillTcMaxBlocks)
+        return fail(QSA_ERR_UNSUPPORTED, "p0 + Nc = %lld exceeds the tensor-core prefill's %lld blocks",
+                    (long long)p0 + Nc, (long long)kPrefillTcMaxBlocks);
     QSA_NEED(q && k_cache && v_cache && blocks && count && out, "NULL tensor pointer");
     QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16),
              "q, k_cache, v_cache and out must be 16-byte aligned");

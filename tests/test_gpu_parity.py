@@ -276,6 +276,34 @@ def test_prefill_interval_invariance(cuda_lib):
         assert (o - outs[0]).abs().max().item() <= 2 ** -7
 
 
+@pytest.mark.parametrize("hq,hkv,p0,nc", [
+    (16, 1, 0, 298),       # 16 heads per KV head; p < 4 .. dense; the last own block runs past the cache
+    (16, 2, 2000, 77),     # 8 per KV head across the dense/sparse threshold, ragged last tile
+    (32, 2, 9000, 40),     # 16 per KV head, sparse, fewer queries than one tile
+    (8, 2, 2040, 50),      # 4 per KV head: the CUDA-core path
+])
+def test_prefill_head_ratios_and_edges(cuda_lib, hq, hkv, p0, nc):
+    w = I.prefill_workload(f"prefill_{hq}_{hkv}", p0, nc, hq, hkv, "planted", seed=11)
+    c, _ = _run_prefill(w, 1024)
+    _check_prefill(w, c, range(nc))
+
+
+def test_prefill_out_of_order_list_is_flagged(cuda_lib):
+    # The tensor-core tiles walk each list interval by interval and need it ascending;
+    # a reversed row is recorded as a bounds error instead of being dropped silently.
+    w = I.prefill_workload("prefill_rev", 20000, 32, 16, 2, "gaussian", seed=12)
+    c, _ = _run_prefill(w, 1024)
+    L = _to(w.layers[0])
+    blocks = c.blocks.clone()
+    blocks[5] = blocks[5].flip(0)
+    c.attend(L.q, L.k_cache, L.v_cache, blocks=blocks)
+    st, det = c.device_status()
+    assert st == qb.QSA_ERR_DEVICE_BOUNDS and det == 5
+    qb.qsa_workspace_init(c.ws)
+    c.attend(L.q, L.k_cache, L.v_cache)
+    _assert_status_ok(c)
+
+
 # ----------------------------------------------------------------------------- full-size workloads, sampled
 
 def test_long_decode_full_size_one_layer(cuda_lib):
