@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-instrument", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--case", choices=sorted(CASES),
+                    help="run one kernel's case a few times and exit (the target of ncu captures)")
     return ap.parse_args(argv)
 
 
@@ -67,6 +69,22 @@ def peaks():
                     bf16_sust=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
     except Exception:
         return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch (read + write) from the committed ncu capture of `kernel`,
+    or None when the kernel's sources changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        m = hashlib.sha256()
+        for name in rec["sources"]:
+            with open(os.path.join(ROOT, "indexer_driven_sparse_gb300", "csrc", name), "rb") as f:
+                m.update(f.read())
+        return float(rec["dram_bytes_per_launch"]) if m.hexdigest() == rec["sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
@@ -399,9 +417,66 @@ def prefill_bench(steps, warmup, pk):
         "attention_only_tok_s": nc / t_att, "ms_attention": t_att * 1e3,
         "attention_gflop_algorithmic": att_flops / 1e9, "scoring_gflop_algorithmic": score_flops / 1e9,
         "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
-                     "frac": ach / pk["bf16"], "traffic": None,
-                     "kernel": "sparse_prefill_chunk (algorithmic FLOPs)"},
+                     "frac": ach / pk["bf16"], "traffic": recorded_traffic("prefill_tc"),
+                     "kernel": "prefill_tc (algorithmic FLOPs)"},
     }
+
+
+# ----------------------------------------------------------------------------- single-kernel cases
+
+def _case_decode_step(reps):
+    """One million-token layer (about 2.2 GB on the device): pool, then `reps` fused
+    decode steps (qsa_decode_step, one launch each)."""
+    import torch
+    from indexer_driven_sparse_gb300 import inputs as I
+    from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+    w = I.million_decode(n_layers=1)
+    L = w.layers[0]
+    b = DecodeBatch(16, 2, w.ctx_len)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    for _ in range(reps):
+        b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+    torch.cuda.synchronize()
+    return b.fused_status()
+
+
+def _case_prefill(reps, attention_only):
+    """The prefill chunk (4096 queries over 262,144 tokens, about 1.1 GB on the device):
+    pool + score + top-k once, then `reps` chunk attentions (or whole chunks)."""
+    import torch
+    from indexer_driven_sparse_gb300 import inputs as I
+    from indexer_driven_sparse_gb300.pipeline import PrefillChunk
+    w = I.prefill_chunk(device="cuda")
+    L = w.layers[0]
+    c = PrefillChunk(16, 2, w.ctx_len[0], w.n_chunk, 8192, device="cuda")
+    pooled = c.new_pooled()
+    c.pool(L.raw_idx_k, pooled)
+    c.run(L.q_idx, L.q, L.k_cache, L.v_cache, pooled)
+    for _ in range(reps):
+        if attention_only:
+            c.attend(L.q, L.k_cache, L.v_cache)
+        else:
+            c.run(L.q_idx, L.q, L.k_cache, L.v_cache, pooled)
+    torch.cuda.synchronize()
+    return c.device_status()
+
+
+CASES = {
+    "decode_step": lambda reps: _case_decode_step(reps),
+    "prefill_attention": lambda reps: _case_prefill(reps, True),
+    "prefill_chunk": lambda reps: _case_prefill(reps, False),
+}
+
+
+def case_main(args):
+    from indexer_driven_sparse_gb300 import binding as qb
+    from indexer_driven_sparse_gb300 import build as qbuild
+    qbuild.build()
+    qb.load()
+    st = CASES[args.case](max(1, args.steps))
+    print(json.dumps({"case": args.case, "reps": max(1, args.steps), "device_status": list(st)}))
+    return 0 if st[0] == 0 else 1
 
 
 # ----------------------------------------------------------------------------- CPU oracle leg
@@ -497,6 +572,8 @@ def main(argv=None):
         return 0
     if args.impl == "reference":
         return reference_main(args)
+    if args.case:
+        return case_main(args)
 
     cpu_base = None
     rank, local, world = dist_setup()
@@ -557,8 +634,8 @@ def main(argv=None):
         if dom in algo:
             ach = algo[dom] / (kt[dom] * 1e-6) / 1e9
             line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
-                                "frac": ach / pk["hbm"], "traffic": None, "kernel": dom,
-                                "peak_src": pk["src"]}
+                                "frac": ach / pk["hbm"], "traffic": recorded_traffic(dom), "kernel": dom,
+                                "algorithmic_bytes": algo[dom], "peak_src": pk["src"]}
         else:
             sc = kt["score"]
             ach = algo["score"] / (sc * 1e-6) / 1e9
