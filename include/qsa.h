@@ -125,6 +125,10 @@ QSA_API qsa_status qsa_pool_keys(const qsa_config *cfg, const qsa_bf16 *raw_idx_
  * fp32 accumulation of exact bf16 products. Entries b >= nb are not written.
  *   q_idx [Nq, idx_dim] bf16; q_seq [Nq], q_pos [Nq] int32; pooled as above;
  *   blk_off [B+1] int32 (per-sequence pooled offsets); scores [Nq, ld] fp32.
+ * q_seq may be NULL: every query then belongs to sequence 0 (a prefill chunk). With
+ * Nq >= 128 and n_pooled_total >= 256 that case runs as one tensor-core GEMM ("GLM-5.3
+ * 最適化 第2部": prefill scoring is quadratic) in tiles of 128 queries x 256 blocks, the
+ * products summed in fp32 in the tensor core's order; otherwise one query at a time.
  * Device checks: nb <= ld, blk_off[s] + nb <= n_pooled_total. */
 QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_seq,
                                    const int32_t *q_pos, int32_t Nq, const qsa_bf16 *pooled,

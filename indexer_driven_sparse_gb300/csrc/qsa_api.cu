@@ -158,11 +158,16 @@ QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx,
     QSA_NEED(ld <= (int64_t)1 << 28, "ld too large");
     QSA_TRY(check_ws(QSA_OP_INDEX_SCORE, cfg, Nq, ld, ws, ws_bytes));
     if (Nq == 0 || ld == 0) return ok();
-    QSA_NEED(q_idx && q_seq && q_pos && pooled && blk_off && scores, "NULL tensor pointer");
+    QSA_NEED(q_idx && q_pos && pooled && blk_off && scores, "NULL tensor pointer");
     QSA_NEED(aligned(q_idx, 16) && aligned(pooled, 16), "q_idx and pooled must be 16-byte aligned");
     QSA_NEED(aligned(scores, 4), "scores must be 4-byte aligned");
-    const cudaError_t e = launch_index_score(q_idx, q_seq, q_pos, Nq, pooled, n_pooled_total, blk_off, scores, ld,
-                                             static_cast<WsHeader *>(ws), static_cast<cudaStream_t>(stream));
+    // one sequence with many queries (a prefill chunk): a tensor-core GEMM
+    const bool gemm = q_seq == nullptr && score_tc_supported(Nq, n_pooled_total);
+    const cudaError_t e =
+        gemm ? launch_score_tc(q_idx, q_pos, Nq, pooled, n_pooled_total, blk_off, scores, ld,
+                               static_cast<WsHeader *>(ws), static_cast<cudaStream_t>(stream))
+             : launch_index_score(q_idx, q_seq, q_pos, Nq, pooled, n_pooled_total, blk_off, scores, ld,
+                                  static_cast<WsHeader *>(ws), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "index_score launch");
     return ok();
 }

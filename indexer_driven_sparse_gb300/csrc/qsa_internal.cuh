@@ -116,6 +116,11 @@ cudaError_t launch_index_score(const uint16_t *q_idx, const int32_t *q_seq, cons
                                int64_t ld, WsHeader *hdr, cudaStream_t st);
 
 size_t topk_scratch_bytes(int Nq, int64_t ld);
+// Tensor-core scoring of many queries of one sequence (score_tc.cu).
+bool score_tc_supported(int Nq, int64_t n_pooled);
+cudaError_t launch_score_tc(const uint16_t *q_idx, const int32_t *q_pos, int Nq, const uint16_t *pooled,
+                            int64_t n_pooled, const int32_t *blk_off, float *scores, int64_t ld, WsHeader *hdr,
+                            cudaStream_t st);
 cudaError_t launch_topk_blocks(const float *scores, int64_t ld, const int32_t *q_pos, int Nq, int32_t *blocks,
                                int32_t *count, WsHeader *hdr, void *scratch, size_t scratch_bytes, cudaStream_t st);
 

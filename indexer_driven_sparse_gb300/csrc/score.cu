@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const uint16
     const int r = blockIdx.y;
     const int p = q_pos[r];
     const int64_t nb = p >= 0 ? (p >> 2) : -1;
-    const int64_t off = blk_off[q_seq[r]];
+    const int64_t off = blk_off[q_seq != nullptr ? q_seq[r] : 0];   // NULL: one sequence
     if (nb < 0 || nb > ld || off < 0 || off + nb > n_pooled) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereScore, r);
         return;

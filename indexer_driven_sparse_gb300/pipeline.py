@@ -130,9 +130,11 @@ class PrefillChunk:
                          torch.tensor([self.n_pooled], **i32), max(0, self.n_pooled - first_block), pooled, self.ws,
                          stream)
 
-    def score(self, q_idx, pooled, stream=None):
-        qb.qsa_index_score(self.cfg, q_idx, self.q_seq, self.q_pos, pooled, self.blk_off, self.scores, self.ws,
-                           stream)
+    def score(self, q_idx, pooled, stream=None, gemm=True):
+        """All chunk queries share one history: with gemm the call passes no per-query
+        sequence ids, which selects the tensor-core GEMM; otherwise one query at a time."""
+        qb.qsa_index_score(self.cfg, q_idx, None if gemm else self.q_seq, self.q_pos, pooled, self.blk_off,
+                           self.scores, self.ws, stream)
 
     def topk(self, stream=None):
         qb.qsa_topk_blocks(self.cfg, self.scores, self.q_pos, self.blocks, self.count, self.ws, stream)

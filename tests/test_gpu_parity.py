@@ -93,6 +93,46 @@ def test_index_score_within_fp32_bound(cuda_lib):
         assert np.all(np.abs(sc[s, :nb] - want) <= bound + 1e-30), s
 
 
+@pytest.mark.parametrize("p0,nc,seq_off", [(20000, 300, 0), (9000, 131, 77), (1000, 128, 5)])
+def test_index_score_gemm_one_sequence(cuda_lib, p0, nc, seq_off):
+    # The queries of a prefill chunk share one history, so their scores run as a
+    # tensor-core GEMM (no per-query sequence ids). Tiles are ragged in both directions,
+    # the sequence starts at an offset inside the pooled array, and entries b >= nb(p)
+    # must stay untouched. The per-query kernel is checked on the same rows.
+    from indexer_driven_sparse_gb300.pipeline import _workspace
+    w = I.prefill_workload("gemm", p0, nc, 16, 2, "planted", seed=13)
+    L = _to(w.layers[0])
+    cfg = qb.make_config(16, 2)
+    n_tok, i32 = p0 + nc, dict(dtype=torch.int32, device=DEV)
+    nbk = n_tok // 4
+    pooled = (torch.randn(seq_off + nbk + 3, 128, generator=torch.Generator().manual_seed(3)) / 8).to(
+        torch.bfloat16).to(DEV)                                    # other sequences' blocks around it
+    tok_off = torch.tensor([0, n_tok], **i32)
+    blk_off = torch.tensor([seq_off, seq_off + nbk], **i32)
+    ld = (n_tok - 1) // 4 + 3
+    ws = _workspace(max(qb.workspace_size(qb.OP_POOL_KEYS, cfg, 1, nbk),
+                        qb.workspace_size(qb.OP_INDEX_SCORE, cfg, nc, ld)), DEV)
+    qb.qsa_pool_keys(cfg, L.raw_idx_k, tok_off, blk_off, torch.tensor([0], **i32), torch.tensor([nbk], **i32), nbk,
+                     pooled, ws)
+    q_pos = torch.arange(p0, p0 + nc, **i32)
+    out = {}
+    for name, q_seq in (("gemm", None), ("rows", torch.zeros(nc, **i32))):
+        sc = torch.full((nc, ld), float("nan"), dtype=torch.float32, device=DEV)
+        qb.qsa_index_score(cfg, L.q_idx, q_seq, q_pos, pooled, blk_off, sc, ws)
+        st, det = qb.qsa_read_device_status(ws)
+        assert st == 0, (name, st, det)
+        out[name] = sc.cpu().numpy().astype(np.float64)
+    pk = O.pool_keys(bits(w.layers[0].raw_idx_k))
+    qib = bits(w.layers[0].q_idx)
+    for i in range(nc):
+        nb = (p0 + i) // 4
+        want = O.score_blocks(qib[i], pk[:nb])
+        bound = O.score_error_bound(qib[i], pk[:nb])
+        for name, sc in out.items():
+            assert np.all(np.abs(sc[i, :nb] - want) <= bound + 1e-30), (name, i)
+            assert np.all(np.isnan(sc[i, nb:])), (name, i)
+
+
 # ----------------------------------------------------------------------------- top-k
 
 def _topk_case_rows():
