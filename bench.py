@@ -396,6 +396,12 @@ def prefill_bench(steps, warmup, pk):
     def attend_only():
         c.attend(L.q, L.k_cache, L.v_cache)
 
+    def score_only():
+        c.score(L.q_idx, pooled)
+
+    def topk_only():
+        c.topk()
+
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         chunk()
@@ -408,6 +414,11 @@ def prefill_bench(steps, warmup, pk):
     t_chunk = time_graph(g_chunk, stream, n, max(1, warmup), 1) / n
     g_att = capture(attend_only, stream)
     t_att = time_graph(g_att, stream, n, max(1, warmup), 1) / n
+    phases = {"attention": t_att * 1e3}
+    for name, fn in (("score", score_only), ("topk", topk_only)):
+        g1 = capture(fn, stream)
+        phases[name] = time_graph(g1, stream, n, max(1, warmup), 1) / n * 1e3
+        del g1
     att_flops = A.prefill_attention_flops(p0, nc)
     score_flops = A.prefill_score_flops(p0, nc)
     ach = att_flops / t_att / 1e12
@@ -415,6 +426,7 @@ def prefill_bench(steps, warmup, pk):
         "workload": f"prefill chunk: {nc} queries at p0={p0}, 16 q / 2 kv heads, intervals 8192",
         "chunk_tok_s": nc / t_chunk, "ms_per_chunk": t_chunk * 1e3,
         "attention_only_tok_s": nc / t_att, "ms_attention": t_att * 1e3,
+        "phases_ms": phases,
         "attention_gflop_algorithmic": att_flops / 1e9, "scoring_gflop_algorithmic": score_flops / 1e9,
         "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": ach / pk["bf16"], "traffic": recorded_traffic("prefill_tc"),

@@ -2,57 +2,214 @@
 // ties to the lower block id, written in ascending id order ("3090x3で 314 万コンテキスト",
 // section "なぜ"; tie rule as in "125B MoE を 3090 3 枚で運用する vLLM 最適化編" section 3.3).
 //
-// One CTA per row: a three-digit (11/11/10-bit) radix select on order-preserving
-// 32-bit score keys finds the exact key T of the k-th best block and how many blocks
-// with key == T to keep; a final pass in index order emits every block with key > T
-// and the first `need` blocks with key == T, so the output is ascending by construction.
+// One CTA per row, three streaming passes over the row (the first from HBM, the others
+// mostly from L2):
+//   1. the row's finite max and min;
+//   2. a histogram over 4096 bins that are linear in the score value (monotone in the
+//      score, so bins above the one holding the k-th best are wholly selected). Linear
+//      bins spread scores evenly, where bins on the float's top bits crowd a few
+//      exponents and serialise the shared-memory atomics;
+//   3. the blocks in higher bins are appended to the selection, the blocks in the k-th
+//      bin become candidates, ranked exactly by their 64-bit keys (score key, then lower
+//      id first) with a bitonic sort in shared memory.
+// The 512 ids are then sorted ascending. Rows the bins cannot split (all scores equal,
+// no finite range, or more than 4096 candidates in one bin) take an exact three-digit
+// radix select on the 32-bit score keys instead.
 #include "qsa_internal.cuh"
+
+#include <float.h>
 
 namespace qsa {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kBins = 2048;
+constexpr int kLinBins = 4096;
+constexpr int kCandCap = 4096;
+static_assert(kCandCap * 2 >= kLinBins, "the histogram lives in the candidate buffer");
 
-// Find the digit d (bins high -> low) where the running count from the top first
-// reaches `need`. Returns d and the count strictly above d. Uses warp 0 only.
-__device__ __forceinline__ void find_digit(const uint32_t *hist, int nbins, uint32_t need, int *d_out,
-                                           uint32_t *above_out) {
-    const int lane = threadIdx.x & 31;
-    const int per = nbins / 32;
-    // lane L owns bins [L*per, (L+1)*per)
-    uint32_t sum = 0;
-    for (int i = 0; i < per; ++i) sum += hist[lane * per + i];
-    // inclusive suffix sum over lanes (from lane 31 down)
-    uint32_t suf = sum;
+// Calls f(i, v, valid) over the row with every thread taking the same number of calls
+// (so f may use warp votes); 16-byte loads for the aligned body.
+template <class F>
+__device__ __forceinline__ void row_scan(const float *__restrict__ s, int64_t nb, F &&f) {
+    const int tid = threadIdx.x;
+    const int64_t mis = (int64_t)(((16 - ((uintptr_t)s & 15)) & 15) >> 2);   // elements before 16-B alignment
+    const int64_t head = mis < nb ? mis : nb;
+    if (head > 0) {
+        const bool ok = tid < head;
+        f((int64_t)tid, ok ? __ldg(s + tid) : 0.f, ok);
+    }
+    const int64_t nvec = (nb - head) >> 2;
+    const float4 *v4 = reinterpret_cast<const float4 *>(s + head);
+#pragma unroll 4
+    for (int64_t j0 = 0; j0 < nvec; j0 += kTopkThreads) {
+        const int64_t j = j0 + tid;
+        const bool ok = j < nvec;
+        const float4 x = ok ? __ldg(v4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int64_t i = head + 4 * j;
+        f(i, x.x, ok);
+        f(i + 1, x.y, ok);
+        f(i + 2, x.z, ok);
+        f(i + 3, x.w, ok);
+    }
+    const int64_t t0 = head + 4 * nvec;
+    if (t0 < nb) {
+        const bool ok = t0 + tid < nb;
+        f(t0 + tid, ok ? __ldg(s + t0 + tid) : 0.f, ok);
+    }
+}
+
+// Bin of a score, non-decreasing in the score: NaN and -inf lowest, +inf highest.
+__device__ __forceinline__ int lin_bin(float v, float vmin, float scale) {
+    if (v != v || v == -INFINITY) return 0;
+    if (v == INFINITY) return kLinBins - 1;
+    const int b = (int)((v - vmin) * scale);
+    return min(b, kLinBins - 2);
+}
+
+// Block-wide: the bin b* (counting from the top) where the running count first reaches
+// `need`, and the count strictly above it. Each thread owns kLinBins / kTopkThreads bins.
+__device__ void find_bin_from_top(const uint32_t *hist, uint32_t need, int *b_out, uint32_t *above_out,
+                                  uint32_t *wtot) {
+    constexpr int per = kLinBins / kTopkThreads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t h[per], sum = 0;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+        h[k] = hist[tid * per + k];
+        sum += h[k];
+    }
+    uint32_t suf = sum;                       // inclusive suffix sum within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
         if (lane + o < 32) suf += v;
     }
-    const uint32_t above_lane = suf - sum;   // count in bins of higher lanes
-    const bool hit = above_lane < need && suf >= need;
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    const int L = 31 - __clz(m);             // exactly one lane hits (counts are monotone)
-    if (lane == L) {
-        uint32_t run = above_lane;
-        int d = (L + 1) * per - 1;
-        for (; d >= L * per; --d) {
-            if (run + hist[d] >= need) break;
-            run += hist[d];
+    if (lane == 0) wtot[warp] = suf;
+    __syncthreads();
+    uint32_t higher = 0;
+    for (int w = warp + 1; w < kTopkWarps; ++w) higher += wtot[w];
+    const uint32_t above = higher + suf - sum;        // count in bins above this thread's
+    if (above < need && above + sum >= need) {
+        uint32_t run = above;
+        int b = per - 1;
+        for (; b > 0; --b) {
+            if (run + h[b] >= need) break;
+            run += h[b];
         }
-        *d_out = d;
+        *b_out = tid * per + b;
         *above_out = run;
+    }
+    __syncthreads();
+}
+
+// Bitonic sort of n (a power of two, <= 4096) 64-bit keys in shared memory.
+__device__ void bitonic_u64(uint64_t *a, int n, bool descending) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const bool up = ((i & k) == 0) != descending;
+                    const uint64_t x = a[i], y = a[l];
+                    if ((x > y) == up) {
+                        a[i] = y;
+                        a[l] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
     }
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float *__restrict__ scores, int64_t ld,
-                                                                 const int32_t *q_pos, int32_t *__restrict__ blocks,
-                                                                 int32_t *__restrict__ count, WsHeader *hdr) {
-    __shared__ uint32_t hist[kBins];
-    __shared__ int s_digit;
-    __shared__ uint32_t s_above;
-    __shared__ uint32_t s_wsum[2][kTopkWarps];
+__device__ void bitonic_i32_asc(int32_t *a, int n) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const bool up = (i & k) == 0;
+                    const int32_t x = a[i], y = a[l];
+                    if ((x > y) == up) {
+                        a[i] = y;
+                        a[l] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Exact fallback: three-digit (11/11/10-bit) radix select on the 32-bit keys, then one
+// pass in index order keeping every key > T and the first `need` keys == T.
+__device__ void radix_select_row(const float *__restrict__ s, int64_t nb, int32_t *out, uint32_t *hist,
+                                 uint32_t *wtot, int *s_b, uint32_t *s_above, uint32_t *written_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t prefix = 0, pmask = 0, need = kBlockTopK;
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+        const int sh = shifts[pass];
+        const uint32_t dmask = (1u << widths[pass]) - 1u;
+        for (int i = tid; i < kLinBins; i += kTopkThreads) hist[i] = 0;
+        __syncthreads();
+        for (int64_t i = tid; i < nb; i += kTopkThreads) {
+            const uint32_t key = score_key(__ldg(s + i));
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & dmask], 1u);
+        }
+        __syncthreads();
+        find_bin_from_top(hist, need, s_b, s_above, wtot);
+        prefix |= (uint32_t)*s_b << sh;
+        pmask |= dmask << sh;
+        need -= *s_above;
+        __syncthreads();
+    }
+    const uint32_t T = prefix, need_eq = need;
+    uint32_t written = 0, eq_seen = 0;
+    for (int64_t base = 0; base < nb; base += kTopkThreads) {
+        const int64_t i = base + tid;
+        const uint32_t key = i < nb ? score_key(__ldg(s + i)) : 0u;
+        const bool gt = i < nb && key > T;
+        const bool eq = i < nb && key == T;
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) wtot[warp] = __popc(beq);
+        __syncthreads();
+        uint32_t eq_before = eq_seen, eq_total = 0;
+        for (int w = 0; w < kTopkWarps; ++w) {
+            if (w < warp) eq_before += wtot[w];
+            eq_total += wtot[w];
+        }
+        eq_before += __popc(beq & ((1u << lane) - 1u));
+        const bool take = gt || (eq && eq_before < need_eq);
+        const unsigned bt = __ballot_sync(0xffffffffu, take);
+        __syncthreads();
+        if (lane == 0) wtot[warp] = __popc(bt);
+        __syncthreads();
+        uint32_t pos = written, t_total = 0;
+        for (int w = 0; w < kTopkWarps; ++w) {
+            if (w < warp) pos += wtot[w];
+            t_total += wtot[w];
+        }
+        pos += __popc(bt & ((1u << lane) - 1u));
+        if (take && pos < kBlockTopK) out[pos] = (int32_t)i;
+        written += t_total;
+        eq_seen += eq_total;
+        __syncthreads();
+    }
+    *written_out = written;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float *__restrict__ scores, int64_t ld,
+                                                                    const int32_t *q_pos, int32_t *__restrict__ blocks,
+                                                                    int32_t *__restrict__ count, WsHeader *hdr) {
+    __shared__ uint64_t cand[kCandCap];        // the histogram shares this space (used before the candidates)
+    uint32_t *hist = reinterpret_cast<uint32_t *>(cand);
+    __shared__ int32_t sel[kBlockTopK];
+    __shared__ uint32_t wtot[kTopkWarps];
+    __shared__ float s_red[2][kTopkWarps];
+    __shared__ int s_b;
+    __shared__ uint32_t s_above, s_nsel, s_ncand, s_written;
 
     const int row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -74,65 +231,100 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float *__
     }
     const float *s = scores + (int64_t)row * ld;
 
-    uint32_t prefix = 0, pmask = 0, need = kBlockTopK;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-        const int sh = shifts[pass];
-        const uint32_t dmask = (1u << widths[pass]) - 1u;
-        const int nbins = 1 << widths[pass];
-        for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
-        __syncthreads();
-        for (int64_t i = tid; i < nb; i += kTopkThreads) {
-            const uint32_t key = score_key(__ldg(s + i));
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & dmask], 1u);
+    // ---- pass 1: finite max and min
+    float vmax = -FLT_MAX, vmin = FLT_MAX;
+    bool any = false;
+    row_scan(s, nb, [&](int64_t, float v, bool ok) {
+        if (ok && fabsf(v) <= FLT_MAX) {
+            vmax = fmaxf(vmax, v);
+            vmin = fminf(vmin, v);
+            any = true;
         }
-        __syncthreads();
-        if (warp == 0) find_digit(hist, nbins, need, &s_digit, &s_above);
-        __syncthreads();
-        prefix |= (uint32_t)s_digit << sh;
-        pmask |= dmask << sh;
-        need -= s_above;
-        __syncthreads();
+    });
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        vmin = fminf(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
     }
-    const uint32_t T = prefix;               // exact key of the k-th best block
-    const uint32_t need_eq = need;           // how many blocks with key == T are kept (>= 1)
+    if (lane == 0) {
+        s_red[0][warp] = vmax;
+        s_red[1][warp] = vmin;
+    }
+    for (int i = tid; i < kLinBins; i += kTopkThreads) hist[i] = 0;
+    if (tid == 0) {
+        s_nsel = 0;
+        s_ncand = 0;
+    }
+    const bool any_finite = __syncthreads_or(any);
+    vmax = s_red[0][0];
+    vmin = s_red[1][0];
+    for (int w = 1; w < kTopkWarps; ++w) {
+        vmax = fmaxf(vmax, s_red[0][w]);
+        vmin = fminf(vmin, s_red[1][w]);
+    }
+    const float scale = (float)(kLinBins - 2) / (vmax - vmin);
+    // rows the linear bins cannot split take the exact radix select (uniform decision)
+    bool linear = any_finite && vmax > vmin && scale > 0.f && scale <= FLT_MAX;
 
-    uint32_t written = 0, eq_seen = 0;
-    for (int64_t base = 0; base < nb; base += kTopkThreads) {
-        const int64_t i = base + tid;
-        const uint32_t key = i < nb ? score_key(__ldg(s + i)) : 0u;
-        const bool gt = i < nb && key > T;
-        const bool eq = i < nb && key == T;
-        const unsigned beq = __ballot_sync(0xffffffffu, eq);
-        if (lane == 0) s_wsum[0][warp] = __popc(beq);
+    if (linear) {
+        // ---- pass 2: histogram of linear bins
+        row_scan(s, nb, [&](int64_t, float v, bool ok) {
+            if (ok) atomicAdd(&hist[lin_bin(v, vmin, scale)], 1u);
+        });
         __syncthreads();
-        uint32_t eq_before = eq_seen, eq_total = 0;
-        for (int w = 0; w < kTopkWarps; ++w) {
-            const uint32_t c = s_wsum[0][w];
-            if (w < warp) eq_before += c;
-            eq_total += c;
-        }
-        eq_before += __popc(beq & ((1u << lane) - 1u));
-        const bool take = gt || (eq && eq_before < need_eq);
-        const unsigned bt = __ballot_sync(0xffffffffu, take);
-        if (lane == 0) s_wsum[1][warp] = __popc(bt);
-        __syncthreads();
-        uint32_t pos = written, t_total = 0;
-        for (int w = 0; w < kTopkWarps; ++w) {
-            const uint32_t c = s_wsum[1][w];
-            if (w < warp) pos += c;
-            t_total += c;
-        }
-        pos += __popc(bt & ((1u << lane) - 1u));
-        if (take && pos < kBlockTopK) out[pos] = (int32_t)i;
-        written += t_total;
-        eq_seen += eq_total;
-        __syncthreads();
+        find_bin_from_top(hist, kBlockTopK, &s_b, &s_above, wtot);
+        if (hist[s_b] > kCandCap) linear = false;
     }
+    const uint32_t n_in_bin = linear ? hist[s_b] : 0u;
+    __syncthreads();                            // the candidates overwrite the histogram
+    if (linear) {
+        const int bstar = s_b;
+        const uint32_t need_eq = kBlockTopK - s_above;
+        // ---- pass 3: append the sure blocks, gather the k-th bin's candidates
+        const unsigned lt = (1u << lane) - 1u;
+        row_scan(s, nb, [&](int64_t i, float v, bool ok) {
+            const int b = ok ? lin_bin(v, vmin, scale) : -1;
+            const bool sure = b > bstar, maybe = b == bstar;
+            const unsigned ms = __ballot_sync(0xffffffffu, sure);
+            const unsigned mc = __ballot_sync(0xffffffffu, maybe);
+            if (ms | mc) {
+                uint32_t bs = 0, bc = 0;
+                if (lane == 0) {
+                    if (ms) bs = atomicAdd(&s_nsel, __popc(ms));
+                    if (mc) bc = atomicAdd(&s_ncand, __popc(mc));
+                }
+                bs = __shfl_sync(0xffffffffu, bs, 0);
+                bc = __shfl_sync(0xffffffffu, bc, 0);
+                if (sure) sel[bs + __popc(ms & lt)] = (int32_t)i;
+                if (maybe)
+                    cand[bc + __popc(mc & lt)] =
+                        ((uint64_t)score_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+            }
+        });
+        __syncthreads();
+        const int nc = (int)s_ncand;
+        int n2 = 2;
+        while (n2 < nc) n2 <<= 1;
+        for (int i = nc + tid; i < n2; i += kTopkThreads) cand[i] = 0ull;   // pads sort last
+        __syncthreads();
+        bitonic_u64(cand, n2, true);
+        const uint32_t base = s_nsel;           // == s_above
+        for (uint32_t k = tid; k < need_eq; k += kTopkThreads)
+            sel[base + k] = (int32_t)(0xFFFFFFFFu - (uint32_t)(cand[k] & 0xFFFFFFFFull));
+        __syncthreads();
+        bitonic_i32_asc(sel, kBlockTopK);
+        for (int i = tid; i < kBlockTopK; i += kTopkThreads) out[i] = sel[i];
+        if (tid == 0) {
+            count[row] = kBlockTopK;
+            if (base != s_above || nc != (int)n_in_bin)
+                record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereTopk, row);
+        }
+        return;
+    }
+    radix_select_row(s, nb, out, hist, wtot, &s_b, &s_above, &s_written);
     if (tid == 0) {
         count[row] = kBlockTopK;
-        if (written != kBlockTopK) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereTopk, row);
+        if (s_written != kBlockTopK) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereTopk, row);
     }
 }
 

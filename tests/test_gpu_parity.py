@@ -153,12 +153,20 @@ def _topk_case_rows():
     y[:600] = -y[:600]
     rows.append(y)
     rows.append(rng.standard_normal(262080).astype(np.float32))                 # million-token row
+    z = (1.0 + 1e-3 * rng.standard_normal(20000)).astype(np.float32)            # one outlier squeezes
+    z[123] = 1e30                                                               # the rest into one bin
+    rows.append(z)
+    t = np.concatenate([np.full(300, 5.0), np.full(4000, 1.0), rng.standard_normal(1000) * 0.1 - 3.0])
+    rows.append(rng.permutation(t).astype(np.float32))                          # 4000 ties at the cut
+    t = np.concatenate([np.full(100, 2.0), np.full(10000, 1.0), rng.standard_normal(500)])
+    rows.append(rng.permutation(t).astype(np.float32))                          # 10000 ties at the cut
+    rows.append((rng.standard_normal(66559) * 2.8).astype(np.float32))          # a prefill row
     return rows
 
 
 def test_topk_exact_on_given_scores(cuda_lib):
     rows = _topk_case_rows()
-    ld = max(len(r) for r in rows)
+    ld = max(len(r) for r in rows) + 1                # odd: most rows start off 16-byte alignment
     sc = np.zeros((len(rows), ld), np.float32)
     for i, r in enumerate(rows):
         sc[i, :len(r)] = r
