@@ -6,21 +6,32 @@
 // merging softmax partials as the walk proceeds.
 //
 // Work unit: a tile of QT consecutive chunk queries x G query heads of one KV head
-// (QT x G = 128 rows, the MMA's M). The tile walks the history interval by interval. In
-// each interval it marks, per pooled block, which of its queries selected the block (and
-// which queries own it as their current, partial block), and compacts the marked blocks
-// into a union. The union's tokens go through the tensor cores 64 at a time:
-//   S = Q K^T         (M=128, N=64,  K=256)   into TMEM columns [0, 64)
-//   softmax rows      one thread per row: each row keeps only the tokens its query may
-//                     see (its own selection, or its own block up to itself), online
-//                     max/sum in base 2 with a lazy rescale of O (only when the running
-//                     max grows by more than 2^8)
-//   O += P V          (M=128, N=256, K=64)   into TMEM columns [256, 512)
-// Operands sit in shared memory in the 128-byte-swizzled layouts the MMA reads directly:
-// Q, K and P K-major, V MN-major. K/V rows are gathered with 16-byte cp.async into two
-// buffers whose completion is tracked by mbarriers; MMAs complete onto mbarriers via
-// tcgen05.commit. Every wait is bounded (250 ms): a timeout records
-// QSA_ERR_DEVICE_TIMEOUT, drains what is in flight (bounded), frees TMEM and returns.
+// (QT x G = 128 rows, the MMA's M). Two kernels:
+//
+// 1. Plan (one CTA per query tile, shared by its KV heads). Walking the history interval
+//    by interval, it marks per pooled block which of the tile's queries selected it (or
+//    own it as their current, partial block), compacts the marked blocks of the interval
+//    into their ascending union, and cuts the union into chunks of 16 blocks (64 tokens;
+//    a chunk never spans two intervals). Each chunk record holds the 16 block ids and,
+//    per query, a 64-bit word of the tokens it may see (its own selection; its own block
+//    only up to itself).
+//
+// 2. Attention (one CTA per SM, persistent over tiles), per chunk g:
+//      S = Q K^T         (M=128, N=64,  K=256)   into TMEM columns [64 (g%2), +64)
+//      softmax rows      one thread per row, online max/sum in base 2 with a lazy rescale
+//                        of O (only when the running max grows by more than 2^8)
+//      O += P V          (M=128, N=256, K=64)    into TMEM columns [256, 512)
+//    Roles:
+//      warps 0-3  softmax: one row per thread; at a tile's end, O / l -> bf16 and the LSE;
+//      warps 4-7  producer: chunk records (cp.async, one ahead), the Q tile, and per chunk
+//                 the K and V rows (16-byte cp.async into 128-byte-swizzled shared
+//                 memory, two stages each, K one chunk ahead of V);
+//      warp 8     one thread issues the MMAs: QK of chunk g+1 before PV of chunk g, so the
+//                 tensor core computes the next scores while the softmax runs.
+//    Hand-offs are mbarriers (cp.async arrivals, tcgen05.commit, thread arrivals).
+// Every wait is bounded (250 ms): a timeout records QSA_ERR_DEVICE_TIMEOUT and raises a CTA
+// flag; each role leaves its loops where all its threads agree, drains what it issued
+// (bounded), and TMEM is freed after a final barrier.
 #include "qsa_internal.cuh"
 #include "qsa_ptx.cuh"
 #include "qsa_tc.cuh"
@@ -29,44 +40,251 @@
 
 namespace qsa {
 
-constexpr int kTcThreads = 128;
 constexpr int kTcRows = 128;                 // MMA M
-constexpr int kTcChunk = 64;                 // tokens per MMA step (N of QK, K of PV)
+constexpr int kTcChunk = 64;                 // tokens per chunk (N of QK, K of PV)
+constexpr int kTcBlocksPerChunk = kTcChunk / kRatio;
 constexpr int kTcMaxBpi = 2048;              // blocks per sub-interval (8192 tokens)
 constexpr int kTcMaxIntervals = 256;
 static_assert((int64_t)kTcMaxBpi * kTcMaxIntervals == kPrefillTcMaxBlocks, "tile table limits");
 constexpr int kTcMaxQt = 16;                 // queries per tile (G = 8)
 
-// shared memory layout (offsets from a 1024-byte aligned base)
-constexpr uint32_t kTcQ = 0;                              // 128 x 256 bf16, K-major   64 KiB
-constexpr uint32_t kTcK0 = 65536;                          // 2 x (64 x 256) K-major    2 x 32 KiB
-constexpr uint32_t kTcV0 = kTcK0 + 2 * 32768;              // 2 x (64 x 256) MN-major   2 x 32 KiB
-constexpr uint32_t kTcP = kTcV0 + 2 * 32768;               // 128 x 64 bf16, K-major     16 KiB
-constexpr uint32_t kTcSel = kTcP + 16384;                  // per-block query bits       4 KiB (uint16 x 2048)
-constexpr uint32_t kTcUnion = kTcSel + 2 * kTcMaxBpi;      // union block offsets        4 KiB (uint16)
-constexpr uint32_t kTcEtab = kTcUnion + 2 * kTcMaxBpi;     // [QT][intervals] list ends  (uint16)
-constexpr uint32_t kTcSmem = kTcEtab + 2 * 16 * kTcMaxIntervals + 1024;   // + alignment slack
+// ----------------------------------------------------------------------------- plan
 
-// OR `bits` into the 16-bit entry i of a shared array (32-bit atomic on the containing word)
+struct ChunkRec {                            // 256 bytes
+    int32_t blk[kTcBlocksPerChunk];          // block ids (-1: padding)
+    uint32_t vis[kTcMaxQt][2];               // per query: tokens it may see (bit j = token j), lo/hi
+    int32_t first, last;                     // first / last chunk of the tile
+    int32_t pad[14];
+};
+static_assert(sizeof(ChunkRec) == 256, "chunk record size");
+constexpr int kRecCopyBytes = 208;           // blk, vis, flags
+// chunks per tile: the union has at most QT * (512 + 1) blocks, plus one partial chunk per interval
+constexpr int kPlanCap = (kTcMaxQt * (kBlockTopK + 1) + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk + kTcMaxIntervals;
+constexpr int kPlanThreads = 256;
+constexpr int kPlanRecsPerInterval = kTcMaxBpi / kTcBlocksPerChunk;
+
+// dynamic shared memory of the plan kernel
+constexpr uint32_t kPlLists = 0;                                           // int32 [QT][512]
+constexpr uint32_t kPlStart = kPlLists + 4 * kTcMaxQt * kBlockTopK;        // uint16 [QT][intervals + 1]
+constexpr uint32_t kPlMasks = kPlStart + 2 * kTcMaxQt * (kTcMaxIntervals + 8);   // uint16 [2048]
+constexpr uint32_t kPlRecs = kPlMasks + 2 * kTcMaxBpi;                     // ChunkRec [128]
+constexpr uint32_t kPlSmem = kPlRecs + sizeof(ChunkRec) * kPlanRecsPerInterval;
+
+size_t prefill_tc_plan_bytes(int Nc, int Hq, int Hkv) {
+    if (!prefill_tc_supported(Hq, Hkv) || Nc <= 0) return 0;
+    const int QT = kTcRows / (Hq / Hkv);
+    const size_t n_qt = (size_t)(Nc + QT - 1) / QT;
+    return ((n_qt * 4 + 255) / 256) * 256 + n_qt * kPlanCap * sizeof(ChunkRec);
+}
+
+struct PlanArgs {
+    const int32_t *blocks;    // [Nc, 512]
+    const int32_t *count;     // [Nc]
+    int32_t p0, Nc, QT, bpi, n_iv;
+    int32_t *n_chunks;        // [n_qt]
+    ChunkRec *recs;           // [n_qt][kPlanCap]
+    WsHeader *hdr;
+};
+
 __device__ __forceinline__ void sel_or(uint16_t *sel, int i, uint32_t bits) {
     uint32_t *w = reinterpret_cast<uint32_t *>(sel) + (i >> 1);
     atomicOr(w, (bits & 0xFFFFu) << ((i & 1) * 16));
 }
 
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) {
+    extern __shared__ __align__(16) uint8_t psm[];
+    int32_t *lists = reinterpret_cast<int32_t *>(psm + kPlLists);
+    uint16_t *start = reinterpret_cast<uint16_t *>(psm + kPlStart);
+    uint16_t *masks = reinterpret_cast<uint16_t *>(psm + kPlMasks);
+    ChunkRec *recs = reinterpret_cast<ChunkRec *>(psm + kPlRecs);
+    __shared__ int32_t s_cnt[kTcMaxQt], s_p[kTcMaxQt];
+    __shared__ int s_wsum[kPlanThreads / 32];
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int qt = blockIdx.x, QT = a.QT;
+    const int i0 = qt * QT, nq = min(QT, a.Nc - i0);
+    const int nb_last = (a.p0 + i0 + nq - 1) >> 2;
+    const int n_iv_tile = min(a.n_iv, nb_last / a.bpi + 1);
+    const int stride_s = kTcMaxIntervals + 8;
+    if (tid < QT) {
+        int c = 0;
+        const int p = a.p0 + i0 + tid;
+        if (tid < nq) {
+            c = a.count[i0 + tid];
+            if (c < 0 || c > kBlockTopK || c > (p >> 2)) {
+                record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0 + tid);
+                c = 0;
+            }
+        }
+        s_cnt[tid] = c;
+        s_p[tid] = tid < nq ? p : -1;
+    }
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    // ---- the tile's lists; each must be strictly ascending below the query's own block
+    for (int e = tid; e < QT * kBlockTopK; e += kPlanThreads) {
+        const int qq = e / kBlockTopK, i = e % kBlockTopK;
+        if (i < s_cnt[qq]) lists[e] = a.blocks[(int64_t)(i0 + qq) * kBlockTopK + i];
+    }
+    __syncthreads();
+    for (int e = tid; e < QT * kBlockTopK; e += kPlanThreads) {
+        const int qq = e / kBlockTopK, i = e % kBlockTopK;
+        const int c = s_cnt[qq];
+        if (i < c) {
+            const int b = lists[e];
+            const int bn = i + 1 < c ? lists[e + 1] : (s_p[qq] >> 2);
+            if (b < 0 || bn <= b) {
+                record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0 + qq);
+                s_bad = 1;
+            }
+        }
+    }
+    __syncthreads();
+    if (s_bad) {                               // nothing is attended for this tile
+        if (tid == 0) a.n_chunks[qt] = 0;
+        return;
+    }
+    // ---- start[q][v]: first list index with block >= v * bpi (binary search)
+    for (int e = tid; e < QT * (n_iv_tile + 1); e += kPlanThreads) {
+        const int qq = e / (n_iv_tile + 1), v = e % (n_iv_tile + 1);
+        const int32_t *l = lists + qq * kBlockTopK;
+        int lo = 0, hi = s_cnt[qq];
+        const int key = v * a.bpi;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (l[mid] < key) lo = mid + 1;
+            else hi = mid;
+        }
+        start[qq * stride_s + v] = (uint16_t)lo;
+    }
+    __syncthreads();
+    ChunkRec *out = a.recs + (size_t)qt * kPlanCap;
+    int base = 0;                              // chunks written for this tile
+    for (int v = 0; v < n_iv_tile; ++v) {
+        const int b_lo = v * a.bpi;
+        const int b_hi = min(b_lo + a.bpi, nb_last + 1);
+        const int span = b_hi - b_lo;
+        for (int i = tid; i < (a.bpi + 1) / 2; i += kPlanThreads) reinterpret_cast<uint32_t *>(masks)[i] = 0u;
+        __syncthreads();
+        for (int qq = 0; qq < nq; ++qq) {
+            const int e0 = start[qq * stride_s + v], e1 = start[qq * stride_s + v + 1];
+            for (int i = e0 + tid; i < e1; i += kPlanThreads) sel_or(masks, lists[qq * kBlockTopK + i] - b_lo, 1u << qq);
+        }
+        if (tid < nq) {
+            const int nbq = s_p[tid] >> 2;
+            if (nbq >= b_lo && nbq < b_hi) sel_or(masks, nbq - b_lo, 1u << tid);   // own block
+        }
+        __syncthreads();
+        // ---- ascending positions of the marked blocks: 8 consecutive blocks per thread
+        constexpr int per = kTcMaxBpi / kPlanThreads;
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < per; ++k) {
+            const int i = tid * per + k;
+            cnt += i < span && masks[i] != 0;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int before = incl - cnt, nu = 0;
+        for (int w = 0; w < kPlanThreads / 32; ++w) {
+            if (w < warp) before += s_wsum[w];
+            nu += s_wsum[w];
+        }
+        const int n_ch = (nu + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
+        if (base + n_ch > kPlanCap) {          // cannot happen for valid lists; stop cleanly
+            if (tid == 0) record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0);
+            break;
+        }
+        // ---- records: zero, then fill
+        for (int i = tid; i < n_ch * (int)(sizeof(ChunkRec) / 4); i += kPlanThreads) {
+            const int r = i / (sizeof(ChunkRec) / 4), w = i % (sizeof(ChunkRec) / 4);
+            reinterpret_cast<int32_t *>(&recs[r])[w] = w < kTcBlocksPerChunk ? -1 : 0;
+        }
+        __syncthreads();
+        int pos = before;
+#pragma unroll 1
+        for (int k = 0; k < per; ++k) {
+            const int i = tid * per + k;
+            if (i >= span) break;
+            const uint32_t m = masks[i];
+            if (m == 0) continue;
+            const int b = b_lo + i;
+            const int c = pos / kTcBlocksPerChunk, slot = pos % kTcBlocksPerChunk;
+            recs[c].blk[slot] = b;
+            for (int qq = 0; qq < nq; ++qq) {
+                if (!((m >> qq) & 1u)) continue;
+                uint32_t bits = 0xFu;
+                const int p = s_p[qq];
+                if ((p >> 2) == b) bits = (1u << ((p & 3) + 1)) - 1u;   // its own block: up to itself
+                atomicOr(&recs[c].vis[qq][slot >> 3], bits << ((slot & 7) * 4));
+            }
+            ++pos;
+        }
+        if (tid < n_ch) {
+            recs[tid].first = base + tid == 0;
+            recs[tid].last = v == n_iv_tile - 1 && tid == n_ch - 1;
+        }
+        __syncthreads();
+        // ---- write the interval's records (16-byte stores)
+        const int n16 = n_ch * (int)(sizeof(ChunkRec) / 16);
+        for (int i = tid; i < n16; i += kPlanThreads)
+            reinterpret_cast<uint4 *>(out + base)[i] = reinterpret_cast<const uint4 *>(recs)[i];
+        base += n_ch;
+        __syncthreads();
+    }
+    if (tid == 0) a.n_chunks[qt] = base;
+}
+
+// ----------------------------------------------------------------------------- attention
+
+constexpr int kTcSoftmaxThreads = 128, kTcProducerThreads = 128;
+constexpr int kTcThreads = kTcSoftmaxThreads + kTcProducerThreads + 32;
+constexpr int kTcRing = 4;                   // chunk records in flight
+constexpr int kBarProducer = 1;              // named barrier of the producer warps
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr uint32_t kTcQ = 0;                              // 128 x 256 bf16, K-major    64 KiB
+constexpr uint32_t kTcK = 65536;                           // 2 x (64 x 256) K-major     2 x 32 KiB
+constexpr uint32_t kTcV = kTcK + 2 * 32768;                // 2 x (64 x 256) MN-major    2 x 32 KiB
+constexpr uint32_t kTcP = kTcV + 2 * 32768;                // 128 x 64 bf16, K-major     16 KiB
+constexpr uint32_t kTcRecs = kTcP + 16384;                 // ChunkRec [ring]
+constexpr uint32_t kTcSmem = kTcRecs + sizeof(ChunkRec) * kTcRing + 1024;   // + alignment slack
+
 struct TcArgs {
     const uint16_t *q;        // [Nc, Hq, 256]
     const uint16_t *k_cache;  // [p0+Nc, Hkv, 256]
     const uint16_t *v_cache;
-    const int32_t *blocks;    // [Nc, 512]
-    const int32_t *count;     // [Nc]
     uint16_t *out;            // [Nc, Hq, 256]
     float *lse;               // [Nc, Hq] or nullptr
+    const int32_t *n_chunks;  // [n_qt] (plan)
+    const ChunkRec *recs;     // [n_qt][kPlanCap] (plan)
     int32_t p0, Nc, Hq, Hkv;
-    int32_t bpi;              // blocks per sub-interval
-    int32_t n_iv;             // sub-intervals
     float scale_log2;
     WsHeader *hdr;
 };
+
+__device__ __forceinline__ void producer_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarProducer), "n"(kTcProducerThreads) : "memory");
+}
+
+// Barrier of the producer warps that also ORs a flag over them.
+__device__ __forceinline__ bool producer_sync_or(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "n"(kBarProducer), "n"(kTcProducerThreads)
+        : "memory");
+    return r != 0;
+}
 
 template <int G>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
@@ -74,238 +292,289 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(sm);
-    uint16_t *sel = reinterpret_cast<uint16_t *>(sm + kTcSel);
-    uint16_t *uni = reinterpret_cast<uint16_t *>(sm + kTcUnion);
-    uint16_t *etab = reinterpret_cast<uint16_t *>(sm + kTcEtab);
+    ChunkRec *ring = reinterpret_cast<ChunkRec *>(sm + kTcRecs);
 
-    __shared__ uint64_t bar_s, bar_o, bar_kv[2];
+    __shared__ uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2];
+    __shared__ uint64_t r_full[kTcRing], r_empty[kTcRing];
+    __shared__ uint64_t q_full, q_free, p_full, pv_done, o_free;
     __shared__ uint32_t tmem_s;
-    __shared__ int s_wc[kTcThreads / 32];
-    __shared__ uint32_t s_allow[kTcChunk];
-    __shared__ int32_t s_cnt[kTcMaxQt];
+    __shared__ volatile int s_abort;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    if (warp == 0) tmem_alloc(&tmem_s, 512);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 8) tmem_alloc(&tmem_s, 512);
     if (tid == 0) {
-        mbar_init(smem_u32(&bar_s), 1);
-        mbar_init(smem_u32(&bar_o), 1);
-        mbar_init(smem_u32(&bar_kv[0]), kTcThreads);
-        mbar_init(smem_u32(&bar_kv[1]), kTcThreads);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&k_full[s]), 2 * kTcProducerThreads);   // cp.async + thread arrivals
+            mbar_init(smem_u32(&v_full[s]), kTcProducerThreads);       // cp.async arrivals
+            mbar_init(smem_u32(&k_empty[s]), 1);
+            mbar_init(smem_u32(&v_empty[s]), 1);
+            mbar_init(smem_u32(&s_full[s]), 1);
+        }
+        for (int s = 0; s < kTcRing; ++s) {
+            mbar_init(smem_u32(&r_full[s]), 1);                        // bulk copy of the record
+            mbar_init(smem_u32(&r_empty[s]), kTcSoftmaxThreads);
+        }
+        mbar_init(smem_u32(&q_full), 2 * kTcProducerThreads);
+        mbar_init(smem_u32(&q_free), 1);
+        mbar_init(smem_u32(&p_full), kTcSoftmaxThreads);
+        mbar_init(smem_u32(&pv_done), 1);
+        mbar_init(smem_u32(&o_free), kTcSoftmaxThreads);
         fence_mbar_init();
+        s_abort = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_s;
-    const uint32_t t_s = tmem + ((uint32_t)(32 * warp) << 16);          // this warp's lanes, S columns
-    const uint32_t t_o = t_s + 256;                                      // O columns
-    uint32_t n_s = 0, n_o = 0, n_kv[2] = {0, 0};                         // completed phases per barrier
-    // A wait that gives up clears `ok` in its thread only; the CTA acts on it at the next
-    // __syncthreads_or, so every thread leaves the loops at the same barrier.
-    bool ok = true;
-
-    auto wait_bar = [&](uint64_t *bar, uint32_t phase) -> bool {
-        if (!mbar_wait_bounded(smem_u32(bar), phase & 1u, kWaitLimitNs)) {
-            record_error(a.hdr, QSA_ERR_DEVICE_TIMEOUT, kWherePrefill, blockIdx.x);
-            return false;
-        }
-        return true;
-    };
-
     const int n_qt = (a.Nc + QT - 1) / QT;
     const int n_tiles = n_qt * a.Hkv;
-    const int row = tid;                         // this thread's MMA row (= TMEM lane)
-    const int q_loc = row / G, h_loc = row % G;
-    const int64_t last_tok = (int64_t)a.p0 + a.Nc - 1;
 
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int qt = tile / a.Hkv, g = tile % a.Hkv;
-        const int i0 = qt * QT;
-        const int nq = min(QT, a.Nc - i0);
-        // ---- tile set-up: query positions, selection counts, Q rows (K-major, swizzled)
-        if (tid < QT) {
-            int c = tid < nq ? a.count[i0 + tid] : 0;
-            const int nbq = tid < nq ? (a.p0 + i0 + tid) >> 2 : 0;
-            if (c < 0 || c > kBlockTopK || c > nbq) {
-                record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0 + tid);
+    auto wait = [&](uint64_t *bar, uint32_t phase) -> bool {
+        if (mbar_wait_bounded(smem_u32(bar), phase & 1u, kWaitLimitNs)) return true;
+        record_error(a.hdr, QSA_ERR_DEVICE_TIMEOUT, kWherePrefill, blockIdx.x);
+        s_abort = 1;
+        return false;
+    };
+
+    if (warp >= 4 && warp < 8) {
+        // ================================================================ producer
+        const int pt = tid - kTcSoftmaxThreads;
+        const int64_t last_tok = (int64_t)a.p0 + a.Nc - 1;
+        bool ok = true;
+        // the CTA's chunk stream: (tile, chunk) in order; a tile has n_chunks[tile / Hkv] chunks
+        int tile = blockIdx.x, c_in = 0, n_ch = tile < n_tiles ? a.n_chunks[tile / a.Hkv] : 0;
+        auto advance = [&](int &t, int &c, int &n) {    // to the next chunk of the stream
+            ++c;
+            while (t < n_tiles && c >= n) {
+                t += gridDim.x;
                 c = 0;
+                n = t < n_tiles ? a.n_chunks[t / a.Hkv] : 0;
             }
-            s_cnt[tid] = c;
+        };
+        if (tile < n_tiles && n_ch == 0) {      // tiles without chunks (invalid lists) are skipped
+            c_in = -1;
+            advance(tile, c_in, n_ch);
         }
-        for (int gi = tid; gi < kTcRows * 32; gi += kTcThreads) {
-            const int r = gi >> 5, gg = gi & 31;
-            const int qq = r / G, hh = r % G;
-            const uint32_t dst = sbase + kTcQ + (gg >> 3) * (kTcRows * 128) + swz(r, gg & 7);
-            if (qq < nq) {
-                cp_async16(dst, a.q + ((int64_t)(i0 + qq) * a.Hq + g * G + hh) * kHeadDim + gg * 8);
-            } else {
-                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0) : "memory");
-            }
-        }
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-        __syncthreads();
-        // ---- list ends per (query, sub-interval): etab[q][v] = first list index in interval > v
-        for (int i = tid; i < QT * a.n_iv; i += kTcThreads) etab[i] = 0xFFFFu;
-        __syncthreads();
-        // (the lists must be strictly ascending below the query's own block: anything else
-        // is recorded as a bounds error, so no entry is dropped silently)
-        for (int qq = 0; qq < nq; ++qq) {
-            const int32_t *lst = a.blocks + (int64_t)(i0 + qq) * kBlockTopK;
-            const int c = s_cnt[qq];
-            const int nbq = (a.p0 + i0 + qq) >> 2;
-            for (int i = tid; i < c; i += kTcThreads) {
-                const int b = lst[i];
-                const int bn = i + 1 < c ? lst[i + 1] : nbq;
-                if (b < 0 || bn <= b || bn > nbq) {
-                    record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0 + qq);
-                    continue;
+        // chunk records arrive through the bulk-copy engine, one chunk ahead of the gathers
+        int pf_tile = tile, pf_c = c_in, pf_n = n_ch, pf_g = 0;
+        auto prefetch = [&]() -> bool {         // record of chunk pf_g into ring slot pf_g % ring
+            if (pf_tile >= n_tiles) return true;
+            const int rs = pf_g % kTcRing;
+            bool w_ok = true;
+            if (pt == 0) {
+                if (pf_g >= kTcRing) w_ok = wait(&r_empty[rs], pf_g / kTcRing - 1);
+                if (w_ok) {
+                    const ChunkRec *src = a.recs + (size_t)(pf_tile / a.Hkv) * kPlanCap + pf_c;
+                    mbar_arrive_expect_tx(smem_u32(&r_full[rs]), kRecCopyBytes);
+                    bulk_g2s(sbase + kTcRecs + rs * (uint32_t)sizeof(ChunkRec), src, kRecCopyBytes,
+                             smem_u32(&r_full[rs]));
                 }
-                const int v = b / a.bpi;
-                if (i + 1 == c || bn / a.bpi != v) etab[qq * a.n_iv + v] = (uint16_t)(i + 1);
             }
-        }
-        __syncthreads();
-        if (tid < QT) {                          // intervals without entries end where the previous one did
-            uint16_t run = 0;
-            for (int v = 0; v < a.n_iv; ++v) {
-                const uint16_t e = etab[tid * a.n_iv + v];
-                if (e != 0xFFFFu) run = e;
-                etab[tid * a.n_iv + v] = run;
+            ++pf_g;
+            advance(pf_tile, pf_c, pf_n);
+            return !producer_sync_or(!w_ok || s_abort);
+        };
+        int g = 0, t_loc = -1, pending = -1, pending_gkv = 0;
+        // V rows of chunk `pending` (token ids from its record, still in the ring)
+        auto flush_v = [&]() {
+            if (pending < 0 || !ok) return;
+            const int s = pending & 1;
+            bool w_ok = true;
+            if (pt == 0 && pending >= 2) w_ok = wait(&v_empty[s], (pending >> 1) - 1);
+            if (producer_sync_or(!w_ok || s_abort)) {
+                ok = false;
+                return;
             }
-        }
-        __syncthreads();
-
-        // per-row softmax state (rows of queries past the chunk end stay fully masked)
-        float m_ref = -INFINITY, l_sum = 0.f;
-        bool o_init = false;
-        const int nb_last = (a.p0 + i0 + nq - 1) >> 2;           // the tile's highest own block
-        const int n_iv_tile = min(a.n_iv, nb_last / a.bpi + 1);
-
-        for (int v = 0; v < n_iv_tile && ok; ++v) {
-            const int b_lo = v * a.bpi;
-            const int b_hi = min(b_lo + a.bpi, nb_last + 1);
-            // ---- mark the blocks of this interval each query selected or owns
-            for (int i = tid; i < a.bpi; i += kTcThreads) sel[i] = 0;
-            __syncthreads();
-            for (int qq = 0; qq < nq; ++qq) {
-                const int32_t *lst = a.blocks + (int64_t)(i0 + qq) * kBlockTopK;
-                const int e0 = v == 0 ? 0 : etab[qq * a.n_iv + v - 1];
-                const int e1 = etab[qq * a.n_iv + v];
-                const int nbq = (a.p0 + i0 + qq) >> 2;
-                for (int i = e0 + tid; i < e1; i += kTcThreads) {
-                    const int b = lst[i];
-                    if (b < 0 || b >= nbq || b < b_lo || b >= b_hi) {
-                        record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0 + qq);
-                        continue;
-                    }
-                    sel_or(sel, b - b_lo, 1u << qq);
-                }
-                if (tid == 0 && nbq >= b_lo && nbq < b_hi) sel_or(sel, nbq - b_lo, 1u << qq);   // own block
+            const ChunkRec &r = ring[pending % kTcRing];
+            for (int gi = pt; gi < kTcChunk * 32; gi += kTcProducerThreads) {
+                const int j = gi >> 5, gg = gi & 31;
+                int b = r.blk[j >> 2];
+                if (b < 0) b = r.blk[0];
+                const int64_t tok = min((int64_t)b * kRatio + (j & 3), last_tok);
+                cp_async16(sbase + kTcV + s * 32768 + (gg >> 3) * (kTcChunk * 128) + swz(j, gg & 7),
+                           a.v_cache + (tok * a.Hkv + pending_gkv) * kHeadDim + gg * 8);
             }
-            __syncthreads();
-            // ---- compact the marked blocks into the union, ascending (ballot + warp-count scan)
-            int nu = 0;
-            for (int base_i = 0; base_i < b_hi - b_lo; base_i += kTcThreads) {
-                const int i = base_i + tid;
-                const bool m = i < b_hi - b_lo && sel[i] != 0;
-                const unsigned bal = __ballot_sync(0xffffffffu, m);
-                if ((tid & 31) == 0) s_wc[warp] = __popc(bal);
-                __syncthreads();
-                int before = nu, total = 0;
-#pragma unroll
-                for (int w = 0; w < kTcThreads / 32; ++w) {
-                    if (w < warp) before += s_wc[w];
-                    total += s_wc[w];
-                }
-                if (m) uni[before + __popc(bal & ((1u << (tid & 31)) - 1u))] = (uint16_t)i;
-                nu += total;
-                __syncthreads();
-            }
-            const int n_ch = (nu + kTcChunk / kRatio - 1) / (kTcChunk / kRatio);
-
-            // ---- gather of chunk c's K and V rows into buffer c & 1 (64 tokens x 256 dims each)
-            auto gather = [&](int c) {
-                const int buf = c & 1;
-                const int ub0 = c * (kTcChunk / kRatio);
-                for (int gi = tid; gi < kTcChunk * 64; gi += kTcThreads) {
-                    const int j = gi >> 6;                 // token within the chunk
-                    const int rem = gi & 63;
-                    const int is_v = rem >> 5, gg = rem & 31;
-                    int ui = ub0 + (j >> 2);
-                    if (ui >= nu) ui = ub0;                // padding column: any valid token (masked)
-                    // the newest block may extend past the last token; its tail is masked
-                    const int64_t tok = min((int64_t)(b_lo + uni[ui]) * kRatio + (j & 3), last_tok);
-                    const uint16_t *src = (is_v ? a.v_cache : a.k_cache) + (tok * a.Hkv + g) * kHeadDim + gg * 8;
-                    const uint32_t dst = sbase + (is_v ? kTcV0 : kTcK0) + buf * 32768 + (gg >> 3) * (kTcChunk * 128) +
-                                         swz(j, gg & 7);
-                    cp_async16(dst, src);
-                }
-                cp_async_arrive(smem_u32(&bar_kv[buf]));
-            };
-            if (n_ch > 0) {
-                // the previous chunk's PV may still read the buffer gather(0) refills
-                if (o_init && !wait_bar(&bar_o, n_o - 1)) ok = false;
-                gather(0);
-            }
-
-            for (int c = 0; c < n_ch; ++c) {
-                const int buf = c & 1;
-                // the other buffer is free once the previous chunk's PV finished
-                if (c + 1 < n_ch) {
-                    if (o_init && !wait_bar(&bar_o, n_o - 1)) ok = false;
-                    gather(c + 1);
-                }
-                // column info: token ids and which queries may see them
-                if (tid < kTcChunk) {
-                    const int j = tid;
-                    const int ui = c * (kTcChunk / kRatio) + (j >> 2);
-                    uint32_t allow = 0u;
-                    if (ui < nu) {
-                        const int blk = b_lo + uni[ui];
-                        const int tok = blk * kRatio + (j & 3);
-                        allow = sel[uni[ui]];
-                        // an owner sees its own block only up to itself
-                        for (int qq = 0; qq < nq; ++qq) {
-                            const int pq = a.p0 + i0 + qq;
-                            if ((pq >> 2) == blk && tok > pq) allow &= ~(1u << qq);
-                        }
-                    }
-                    s_allow[j] = allow;
-                }
-                if (!wait_bar(&bar_kv[buf], n_kv[buf])) ok = false;
-                ++n_kv[buf];
-                fence_proxy_async_smem();
-                tc_fence_before();
-                if (__syncthreads_or(!ok)) {
+            cp_async_arrive(smem_u32(&v_full[s]));
+            pending = -1;
+        };
+        ok = prefetch();
+        int cur_tile = -1;
+        while (ok && tile < n_tiles) {
+            const int gkv = tile % a.Hkv;
+            if (tile != cur_tile) {
+                // ---- a new tile: its Q rows once the previous tile's QK MMAs are done
+                flush_v();
+                if (!ok) break;
+                cur_tile = tile;
+                ++t_loc;
+                const int i0 = (tile / a.Hkv) * QT, nq = min(QT, a.Nc - i0);
+                bool w_ok = true;
+                if (pt == 0 && t_loc > 0) w_ok = wait(&q_free, t_loc - 1);
+                if (producer_sync_or(!w_ok || s_abort)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                if (tid == 0) {               // S = Q K^T
-                    const uint32_t qa = sbase + kTcQ, kb = sbase + kTcK0 + buf * 32768;
-#pragma unroll
-                    for (int s = 0; s < kHeadDim / 16; ++s) {
-                        const uint64_t ad = tc_desc(qa + (s >> 2) * (kTcRows * 128) + (s & 3) * 32, 16, 1024);
-                        const uint64_t bd = tc_desc(kb + (s >> 2) * (kTcChunk * 128) + (s & 3) * 32, 16, 1024);
-                        tc_mma(tmem, ad, bd, tc_idesc(kTcRows, kTcChunk, 0), s > 0);
-                    }
-                    tc_commit(smem_u32(&bar_s));
+                for (int gi = pt; gi < kTcRows * 32; gi += kTcProducerThreads) {
+                    const int r = gi >> 5, gg = gi & 31;
+                    const int qq = r / G, hh = r % G;
+                    const uint32_t dst = sbase + kTcQ + (gg >> 3) * (kTcRows * 128) + swz(r, gg & 7);
+                    if (qq < nq)
+                        cp_async16(dst, a.q + ((int64_t)(i0 + qq) * a.Hq + gkv * G + hh) * kHeadDim + gg * 8);
+                    else
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0) : "memory");
                 }
-                if (!wait_bar(&bar_s, n_s)) ok = false;
-                ++n_s;
-                // the previous PV must be done before P is rewritten or O rescaled
-                if (o_init && !wait_bar(&bar_o, n_o - 1)) ok = false;
+                cp_async_arrive(smem_u32(&q_full));
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&q_full));
+            }
+            // ---- prefetch the next record; wait for this chunk's record and K stage
+            if (!prefetch()) {
+                ok = false;
+                break;
+            }
+            const int s = g & 1, rs = g % kTcRing;
+            bool w2 = true;
+            if (pt == 0) w2 = wait(&r_full[rs], g / kTcRing) && (g < 2 || wait(&k_empty[s], (g >> 1) - 1));
+            if (producer_sync_or(!w2 || s_abort)) {
+                ok = false;
+                break;
+            }
+            const ChunkRec &r = ring[rs];
+            for (int gi = pt; gi < kTcChunk * 32; gi += kTcProducerThreads) {
+                const int j = gi >> 5, gg = gi & 31;
+                int b = r.blk[j >> 2];
+                if (b < 0) b = r.blk[0];               // padding column: any valid token (masked)
+                // the newest block may extend past the last token; its tail is masked
+                const int64_t tok = min((int64_t)b * kRatio + (j & 3), last_tok);
+                cp_async16(sbase + kTcK + s * 32768 + (gg >> 3) * (kTcChunk * 128) + swz(j, gg & 7),
+                           a.k_cache + (tok * a.Hkv + gkv) * kHeadDim + gg * 8);
+            }
+            cp_async_arrive(smem_u32(&k_full[s]));
+            mbar_arrive(smem_u32(&k_full[s]));
+            flush_v();                                 // V of the previous chunk, one behind K
+            if (!ok) break;
+            pending = g;
+            pending_gkv = gkv;
+            ++g;
+            advance(tile, c_in, n_ch);
+        }
+        flush_v();
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 8) {
+        // ================================================================ MMA issue
+        if (lane == 0) {
+            int g = 0, n_q = 0, n_tile = -1;
+            // this CTA's chunk stream: (tile, chunk) in order, tiles without chunks skipped
+            int it_t = blockIdx.x, it_c = -1;
+            int it_n = it_t < n_tiles ? a.n_chunks[it_t / a.Hkv] : 0;
+            auto next_chunk = [&](int &f, int &l) -> bool {
+                ++it_c;
+                while (it_t < n_tiles && it_c >= it_n) {   // each pass moves to the next tile
+                    it_t += gridDim.x;
+                    it_c = 0;
+                    it_n = it_t < n_tiles ? a.n_chunks[it_t / a.Hkv] : 0;
+                }
+                if (it_t >= n_tiles) return false;
+                f = it_c == 0;
+                l = it_c == it_n - 1;
+                return true;
+            };
+            uint64_t *last_bar = nullptr;        // the barrier of the last commit, and its phase
+            uint32_t last_phase = 0;
+            int first = 0, last = 0;
+            bool ok = next_chunk(first, last);
+            auto issue_qk = [&](int gq, int f, int l) -> bool {
+                const int s = gq & 1;
+                if (!wait(&k_full[s], gq >> 1)) return false;
+                if (f) {
+                    if (!wait(&q_full, n_q)) return false;
+                    ++n_q;
+                }
+                fence_proxy_async_smem();
                 tc_fence_after();
-                // ---- softmax of this thread's row
+                const uint32_t qa = sbase + kTcQ, kb = sbase + kTcK + s * 32768;
+#pragma unroll
+                for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+                    const uint64_t ad = tc_desc(qa + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = tc_desc(kb + (ks >> 2) * (kTcChunk * 128) + (ks & 3) * 32, 16, 1024);
+                    tc_mma(tmem + s * kTcChunk, ad, bd, tc_idesc(kTcRows, kTcChunk, 0), ks > 0);
+                }
+                tc_commit(smem_u32(&s_full[s]));
+                tc_commit(smem_u32(&k_empty[s]));
+                last_bar = &k_empty[s];
+                last_phase = (uint32_t)(gq >> 1);
+                if (l) tc_commit(smem_u32(&q_free));
+                return true;
+            };
+            if (ok) ok = issue_qk(0, first, last);
+            while (ok) {
+                int f1 = 0, l1 = 0;
+                const bool more = next_chunk(f1, l1);
+                if (more && !issue_qk(g + 1, f1, l1)) break;
+                // ---- O (+)= P V for chunk g
+                const int s = g & 1;
+                if (!wait(&p_full, g) || !wait(&v_full[s], g >> 1)) break;
+                if (first) {
+                    ++n_tile;
+                    if (n_tile > 0 && !wait(&o_free, n_tile - 1)) break;   // the previous tile's O was read
+                }
+                fence_proxy_async_smem();
+                tc_fence_after();
+                const uint32_t pa = sbase + kTcP, vb = sbase + kTcV + s * 32768;
+#pragma unroll
+                for (int ks = 0; ks < kTcChunk / 16; ++ks) {
+                    const uint64_t ad = tc_desc(pa + ks * 32, 16, 1024);
+                    const uint64_t bd = tc_desc(vb + ks * 2048, kTcChunk * 128, 1024);
+                    tc_mma(tmem + 256, ad, bd, tc_idesc(kTcRows, kHeadDim, 1), !first || ks > 0);
+                }
+                tc_commit(smem_u32(&v_empty[s]));
+                tc_commit(smem_u32(&pv_done));
+                last_bar = &pv_done;
+                last_phase = (uint32_t)g;
+                if (!more) break;
+                ++g;
+                first = f1;
+                last = l1;
+            }
+            // the last commit covers every MMA issued: wait for it before TMEM is freed
+            if (last_bar != nullptr) mbar_wait_bounded(smem_u32(last_bar), last_phase & 1u, kWaitLimitNs);
+        }
+    } else {
+        // ================================================================ softmax
+        const int row = tid;                     // MMA row = TMEM lane
+        const int q_loc = row / G, h_loc = row % G;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+        const uint32_t t_o = t_row + 256;
+        int g = 0;
+        bool ok = true;
+        auto wait_warp = [&](uint64_t *bar, uint32_t phase) -> bool {
+            const bool w = wait(bar, phase);
+            return __all_sync(0xffffffffu, w) && !__any_sync(0xffffffffu, s_abort != 0);
+        };
+        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+            const int n_ch = a.n_chunks[tile / a.Hkv];
+            if (n_ch == 0) continue;                     // invalid lists: nothing attended
+            const int i0 = (tile / a.Hkv) * QT, nq = min(QT, a.Nc - i0), gkv = tile % a.Hkv;
+            float m_ref = -INFINITY, l_sum = 0.f;
+            bool o_init = false;
+            for (int c = 0; c < n_ch; ++c) {
+                const int s = g & 1, rs = g % kTcRing;
+                if (!wait_warp(&r_full[rs], g / kTcRing) || !wait_warp(&s_full[s], g >> 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t vis = ((uint64_t)ring[rs].vis[q_loc][1] << 32) | ring[rs].vis[q_loc][0];
+                mbar_arrive(smem_u32(&r_empty[rs]));
+                tc_fence_after();
                 float x[kTcChunk];
                 {
                     float t0[32], t1[32];
-                    tmem_ld32(t_s, t0);
-                    tmem_ld32(t_s + 32, t1);
+                    tmem_ld32(t_row + s * kTcChunk, t0);
+                    tmem_ld32(t_row + s * kTcChunk + 32, t1);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        x[j] = (s_allow[j] >> q_loc) & 1u ? t0[j] * a.scale_log2 : -INFINITY;
-                        x[j + 32] = (s_allow[j + 32] >> q_loc) & 1u ? t1[j] * a.scale_log2 : -INFINITY;
+                        x[j] = (vis >> j) & 1u ? t0[j] * a.scale_log2 : -INFINITY;
+                        x[j + 32] = (vis >> (j + 32)) & 1u ? t1[j] * a.scale_log2 : -INFINITY;
                     }
                 }
                 float cmax = -INFINITY;
@@ -318,6 +587,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
                     m_ref = cmax;
                 }
                 l_sum *= f;
+                float psum = 0.f;
+                uint32_t pk[kTcChunk / 2];
+#pragma unroll
+                for (int j = 0; j < kTcChunk; j += 2) {
+                    const float e0 = x[j] == -INFINITY ? 0.f : exp2f(x[j] - m_ref);
+                    const float e1 = x[j + 1] == -INFINITY ? 0.f : exp2f(x[j + 1] - m_ref);
+                    psum += e0 + e1;             // fp32 row sum: the LSE stays exact to fp32 rounding
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+                    pk[j / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+                l_sum += psum;
+                // P (shared memory) and O are free once the previous PV is done
+                if (g > 0 && !wait_warp(&pv_done, g - 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 // TMEM loads and stores are warp-collective: the warp rescales together
                 if (o_init && __any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll 1
@@ -329,17 +615,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
                         tmem_st32(t_o + c0, ov);
                     }
                 }
-                float psum = 0.f;
-                uint32_t pk[kTcChunk / 2];
-#pragma unroll
-                for (int j = 0; j < kTcChunk; j += 2) {
-                    const float e0 = x[j] == -INFINITY ? 0.f : exp2f(x[j] - m_ref);
-                    const float e1 = x[j + 1] == -INFINITY ? 0.f : exp2f(x[j + 1] - m_ref);
-                    const uint16_t b0 = float_to_bf16_bits(e0), b1 = float_to_bf16_bits(e1);
-                    psum += e0 + e1;          // fp32 row sum: the LSE stays exact to fp32 rounding
-                    pk[j / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-                }
-                l_sum += psum;
 #pragma unroll
                 for (int gg = 0; gg < 8; ++gg) {
                     const uint32_t dst = sbase + kTcP + swz(row, gg);
@@ -349,46 +624,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                if (__syncthreads_or(!ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (tid == 0) {               // O += P V
-                    const uint32_t pa = sbase + kTcP, vb = sbase + kTcV0 + buf * 32768;
-#pragma unroll
-                    for (int s = 0; s < kTcChunk / 16; ++s) {
-                        const uint64_t ad = tc_desc(pa + s * 32, 16, 1024);
-                        const uint64_t bd = tc_desc(vb + s * 2048, kTcChunk * 128, 1024);
-                        tc_mma(tmem + 256, ad, bd, tc_idesc(kTcRows, kHeadDim, 1), o_init || s > 0);
-                    }
-                    tc_commit(smem_u32(&bar_o));
-                }
-                ++n_o;
+                mbar_arrive(smem_u32(&p_full));
                 o_init = true;
+                ++g;
             }
-        }
-        if (!ok) break;
-        // ---- finish the tile: O / l -> bf16, lse
-        if (o_init && !wait_bar(&bar_o, n_o - 1)) ok = false;
-        if (__syncthreads_or(!ok)) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        if (o_init) {                            // every valid row saw at least its own token
-            const bool store = q_loc < nq && l_sum > 0.f;
+            if (!ok) break;
+            // ---- finish the tile: O / l -> bf16, lse; then O may be overwritten
+            if (!wait_warp(&pv_done, g - 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool store = q_loc < nq && l_sum > 0.f;   // every valid row saw its own token
             const float inv = store ? 1.f / l_sum : 0.f;
-            uint16_t *dst = a.out + ((int64_t)(i0 + q_loc) * a.Hq + g * G + h_loc) * kHeadDim;
+            uint16_t *dst = a.out + ((int64_t)(i0 + q_loc) * a.Hq + gkv * G + h_loc) * kHeadDim;
 #pragma unroll 1
             for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
                 float ov[32];
                 tmem_ld32(t_o + c0, ov);          // warp-collective: every lane loads
                 uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    w[j] = (uint32_t)float_to_bf16_bits(ov[2 * j] * inv) |
-                           ((uint32_t)float_to_bf16_bits(ov[2 * j + 1] * inv) << 16);
+                for (int j = 0; j < 16; ++j) {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[2 * j] * inv, ov[2 * j + 1] * inv);
+                    w[j] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
                 if (store) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
@@ -397,21 +656,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
                 }
             }
             if (store && a.lse != nullptr)
-                a.lse[(int64_t)(i0 + q_loc) * a.Hq + g * G + h_loc] = (m_ref + log2f(l_sum)) * kLn2;
+                a.lse[(int64_t)(i0 + q_loc) * a.Hq + gkv * G + h_loc] = (m_ref + log2f(l_sum)) * kLn2;
+            tc_fence_before();
+            mbar_arrive(smem_u32(&o_free));
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    }
-    if (!ok) {
-        // drain: the last commits may still be in flight (bounded waits), then free TMEM
-        if (n_s > 0) mbar_wait_bounded(smem_u32(&bar_s), (n_s - 1) & 1u, kWaitLimitNs);
-        if (n_o > 0) mbar_wait_bounded(smem_u32(&bar_o), (n_o - 1) & 1u, kWaitLimitNs);
-        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 8) tmem_dealloc(tmem, 512);
 }
 
 bool prefill_tc_supported(int Hq, int Hkv) {
@@ -419,35 +671,60 @@ bool prefill_tc_supported(int Hq, int Hkv) {
     return G == 8 || G == 16;
 }
 
-cudaError_t launch_prefill_tc(const AttnArgs &a, int interval_tokens, WsHeader *hdr, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const AttnArgs &a, int interval_tokens, WsHeader *hdr, void *scratch,
+                              size_t scratch_bytes, cudaStream_t st) {
+    const int G = a.n_q_heads / a.n_kv_heads;
+    const int QT = kTcRows / G;
+    const int n_qt = (a.rows + QT - 1) / QT;
+    if (scratch_bytes < prefill_tc_plan_bytes(a.rows, a.n_q_heads, a.n_kv_heads)) return cudaErrorInvalidValue;
+    char *sp = static_cast<char *>(scratch);
+    int32_t *n_chunks = reinterpret_cast<int32_t *>(sp);
+    ChunkRec *recs = reinterpret_cast<ChunkRec *>(sp + (((size_t)n_qt * 4 + 255) / 256) * 256);
+    if (((uintptr_t)recs & 255) != 0) return cudaErrorInvalidValue;
+
+    const int64_t n_blocks = ((int64_t)a.p0 + a.rows) / kRatio + 1;
+    // the interval sets the evaluation order only; it is clamped to what the on-chip tables hold
+    int64_t bpi = std::min<int64_t>(interval_tokens / kRatio, kTcMaxBpi);
+    bpi = std::max<int64_t>(bpi, (n_blocks + kTcMaxIntervals - 1) / kTcMaxIntervals);
+    if (bpi > kTcMaxBpi) return cudaErrorInvalidValue;
+
+    PlanArgs pa{};
+    pa.blocks = a.blocks;
+    pa.count = a.count;
+    pa.p0 = a.p0;
+    pa.Nc = a.rows;
+    pa.QT = QT;
+    pa.bpi = (int)bpi;
+    pa.n_iv = (int)((n_blocks + bpi - 1) / bpi);
+    pa.n_chunks = n_chunks;
+    pa.recs = recs;
+    pa.hdr = hdr;
+    cudaError_t e = cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPlSmem);
+    if (e != cudaSuccess) return e;
+    prefill_plan_kernel<<<n_qt, kPlanThreads, kPlSmem, st>>>(pa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
     TcArgs t{};
     t.q = a.q;
     t.k_cache = a.k_cache;
     t.v_cache = a.v_cache;
-    t.blocks = a.blocks;
-    t.count = a.count;
     t.out = a.out;
     t.lse = a.lse;
+    t.n_chunks = n_chunks;
+    t.recs = recs;
     t.p0 = a.p0;
     t.Nc = a.rows;
     t.Hq = a.n_q_heads;
     t.Hkv = a.n_kv_heads;
     t.scale_log2 = a.scale_log2;
     t.hdr = hdr;
-    const int64_t n_blocks = ((int64_t)a.p0 + a.rows) / kRatio + 1;
-    // the interval sets the evaluation order only; it is clamped to what the on-chip tables hold
-    int64_t bpi = std::min<int64_t>(interval_tokens / kRatio, kTcMaxBpi);
-    bpi = std::max<int64_t>(bpi, (n_blocks + kTcMaxIntervals - 1) / kTcMaxIntervals);
-    if (bpi > kTcMaxBpi) return cudaErrorInvalidValue;
-    t.bpi = (int)bpi;
-    t.n_iv = (int)((n_blocks + bpi - 1) / bpi);
-    const int G = a.n_q_heads / a.n_kv_heads;
     int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int n_tiles = ((a.rows + kTcRows / G - 1) / (kTcRows / G)) * a.n_kv_heads;
+    const int n_tiles = n_qt * a.n_kv_heads;
     const int grid = std::max(1, std::min(sms, n_tiles));
     switch (G) {
         case 8:

@@ -151,7 +151,9 @@ cudaError_t launch_attn_rows(const AttnArgs &a, WsHeader *hdr, cudaStream_t st);
 size_t prefill_scratch_bytes(int Nc, int Hq, int Hkv);
 bool prefill_tc_supported(int Hq, int Hkv);
 constexpr int64_t kPrefillTcMaxBlocks = 2048 * 256;   // pooled blocks the tile tables cover
-cudaError_t launch_prefill_tc(const AttnArgs &a, int interval_tokens, WsHeader *hdr, cudaStream_t st);
+size_t prefill_tc_plan_bytes(int Nc, int Hq, int Hkv);
+cudaError_t launch_prefill_tc(const AttnArgs &a, int interval_tokens, WsHeader *hdr, void *scratch,
+                              size_t scratch_bytes, cudaStream_t st);
 
 // Fused decode layer-step (decode_step.cu).
 constexpr int kMaxStepCtas = 256;
