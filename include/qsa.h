@@ -171,11 +171,14 @@ QSA_API qsa_status qsa_sparse_decode(const qsa_config *cfg, const qsa_bf16 *q, c
  * p = p_i with its own blocks[i] / count[i]. interval_tokens (a positive multiple of
  * 128) sets the evaluation order only, not the result.
  *   q [Nc, Hq, D] bf16; k_cache, v_cache [p0+Nc, Hkv, D] bf16;
- *   blocks [Nc, k] int32, each row's first count[i] entries strictly ascending (as
- *   qsa_topk_blocks writes them); count [Nc]; out [Nc, Hq, D] bf16; lse [Nc, Hq] fp32 or NULL.
+ *   blocks [Nc, k] int32, 16-byte aligned, each row's first count[i] entries strictly
+ *   ascending (as qsa_topk_blocks writes them); count [Nc]; out [Nc, Hq, D] bf16;
+ *   lse [Nc, Hq] fp32 or NULL. q, k_cache, v_cache and out are 16-byte aligned.
  * With 8 or 16 query heads per KV head the chunk runs on the tensor cores in tiles of
  * 128 (query, head) rows that share each interval's union of selected blocks; a row out
- * of order there is recorded as QSA_ERR_DEVICE_BOUNDS. Other head ratios run one CTA per
+ * of order there is recorded as QSA_ERR_DEVICE_BOUNDS and its tile's outputs are not
+ * written. The workspace (qsa_workspace_size) then holds the tiles' chunk plan, about
+ * 197 KB per 16 queries. Other head ratios run one CTA per
  * (query, KV head) on the CUDA cores. Requires (p0 + Nc) / 4 < 524288 on the tensor-core
  * path (else QSA_ERR_UNSUPPORTED). */
 QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,

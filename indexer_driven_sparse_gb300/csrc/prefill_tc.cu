@@ -60,15 +60,17 @@ static_assert(sizeof(ChunkRec) == 256, "chunk record size");
 constexpr int kRecCopyBytes = 208;           // blk, vis, flags
 // chunks per tile: the union has at most QT * (512 + 1) blocks, plus one partial chunk per interval
 constexpr int kPlanCap = (kTcMaxQt * (kBlockTopK + 1) + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk + kTcMaxIntervals;
-constexpr int kPlanThreads = 256;
-constexpr int kPlanRecsPerInterval = kTcMaxBpi / kTcBlocksPerChunk;
+constexpr int kPlanThreads = 384;                // 12 warps: two CTAs fit an SM
+constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kStartStride = kTcMaxIntervals + 8;
 
 // dynamic shared memory of the plan kernel
 constexpr uint32_t kPlLists = 0;                                           // int32 [QT][512]
 constexpr uint32_t kPlStart = kPlLists + 4 * kTcMaxQt * kBlockTopK;        // uint16 [QT][intervals + 1]
-constexpr uint32_t kPlMasks = kPlStart + 2 * kTcMaxQt * (kTcMaxIntervals + 8);   // uint16 [2048]
-constexpr uint32_t kPlRecs = kPlMasks + 2 * kTcMaxBpi;                     // ChunkRec [128]
-constexpr uint32_t kPlSmem = kPlRecs + sizeof(ChunkRec) * kPlanRecsPerInterval;
+constexpr uint32_t kPlCounts = kPlStart + 2 * kTcMaxQt * kStartStride;     // int32 [intervals + 1]
+constexpr uint32_t kPlMasks = kPlCounts + 4 * (kTcMaxIntervals + 8);       // uint16 [warp][2048]
+constexpr uint32_t kPlStage = kPlMasks + 2 * kTcMaxBpi * kPlanWarps;       // ChunkRec [warp][3]
+constexpr uint32_t kPlSmem = kPlStage + sizeof(ChunkRec) * 3 * kPlanWarps;
 
 size_t prefill_tc_plan_bytes(int Nc, int Hq, int Hkv) {
     if (!prefill_tc_supported(Hq, Hkv) || Nc <= 0) return 0;
@@ -91,22 +93,28 @@ __device__ __forceinline__ void sel_or(uint16_t *sel, int i, uint32_t bits) {
     atomicOr(w, (bits & 0xFFFFu) << ((i & 1) * 16));
 }
 
+__device__ __forceinline__ void stage_clear(ChunkRec *r, int lane) {   // warp: blk = -1, the rest 0
+    int32_t *w = reinterpret_cast<int32_t *>(r);
+    for (int i = lane; i < (int)(sizeof(ChunkRec) / 4); i += 32) w[i] = i < kTcBlocksPerChunk ? -1 : 0;
+}
+
+// One CTA per query tile; warps take intervals v = warp, warp + 8, ... in two passes
+// (chunk counts, then records at the scanned offsets).
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) {
     extern __shared__ __align__(16) uint8_t psm[];
     int32_t *lists = reinterpret_cast<int32_t *>(psm + kPlLists);
     uint16_t *start = reinterpret_cast<uint16_t *>(psm + kPlStart);
-    uint16_t *masks = reinterpret_cast<uint16_t *>(psm + kPlMasks);
-    ChunkRec *recs = reinterpret_cast<ChunkRec *>(psm + kPlRecs);
+    int32_t *counts = reinterpret_cast<int32_t *>(psm + kPlCounts);
     __shared__ int32_t s_cnt[kTcMaxQt], s_p[kTcMaxQt];
-    __shared__ int s_wsum[kPlanThreads / 32];
-    __shared__ int s_bad;
+    __shared__ int s_bad, s_total;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint16_t *m = reinterpret_cast<uint16_t *>(psm + kPlMasks) + warp * kTcMaxBpi;
+    ChunkRec *stage = reinterpret_cast<ChunkRec *>(psm + kPlStage) + warp * 3;
     const int qt = blockIdx.x, QT = a.QT;
     const int i0 = qt * QT, nq = min(QT, a.Nc - i0);
     const int nb_last = (a.p0 + i0 + nq - 1) >> 2;
     const int n_iv_tile = min(a.n_iv, nb_last / a.bpi + 1);
-    const int stride_s = kTcMaxIntervals + 8;
     if (tid < QT) {
         int c = 0;
         const int p = a.p0 + i0 + tid;
@@ -123,10 +131,12 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
     if (tid == 0) s_bad = 0;
     __syncthreads();
     // ---- the tile's lists; each must be strictly ascending below the query's own block
-    for (int e = tid; e < QT * kBlockTopK; e += kPlanThreads) {
-        const int qq = e / kBlockTopK, i = e % kBlockTopK;
-        if (i < s_cnt[qq]) lists[e] = a.blocks[(int64_t)(i0 + qq) * kBlockTopK + i];
+    // (16-byte asynchronous copies, all in flight at once; entries past a count are unused)
+    for (int e = tid; e < QT * kBlockTopK / 4; e += kPlanThreads) {
+        const int qq = (4 * e) / kBlockTopK;
+        if (qq < nq) cp_async16(smem_u32(lists + 4 * e), a.blocks + (int64_t)(i0 + qq) * kBlockTopK + (4 * e) % kBlockTopK);
     }
+    cp_async_wait_all();
     __syncthreads();
     for (int e = tid; e < QT * kBlockTopK; e += kPlanThreads) {
         const int qq = e / kBlockTopK, i = e % kBlockTopK;
@@ -156,90 +166,120 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
             if (l[mid] < key) lo = mid + 1;
             else hi = mid;
         }
-        start[qq * stride_s + v] = (uint16_t)lo;
+        start[qq * kStartStride + v] = (uint16_t)lo;
     }
     __syncthreads();
-    ChunkRec *out = a.recs + (size_t)qt * kPlanCap;
-    int base = 0;                              // chunks written for this tile
-    for (int v = 0; v < n_iv_tile; ++v) {
+
+    // marks of interval v in this warp's mask array; returns how many blocks are marked
+    auto mark = [&](int v) -> int {
         const int b_lo = v * a.bpi;
-        const int b_hi = min(b_lo + a.bpi, nb_last + 1);
-        const int span = b_hi - b_lo;
-        for (int i = tid; i < (a.bpi + 1) / 2; i += kPlanThreads) reinterpret_cast<uint32_t *>(masks)[i] = 0u;
-        __syncthreads();
+        const int span = min(b_lo + a.bpi, nb_last + 1) - b_lo;
+        uint4 *m4 = reinterpret_cast<uint4 *>(m);
+        for (int i = lane; i < kTcMaxBpi / 8; i += 32) m4[i] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
         for (int qq = 0; qq < nq; ++qq) {
-            const int e0 = start[qq * stride_s + v], e1 = start[qq * stride_s + v + 1];
-            for (int i = e0 + tid; i < e1; i += kPlanThreads) sel_or(masks, lists[qq * kBlockTopK + i] - b_lo, 1u << qq);
+            const int e0 = start[qq * kStartStride + v], e1 = start[qq * kStartStride + v + 1];
+            for (int i = e0 + lane; i < e1; i += 32) sel_or(m, lists[qq * kBlockTopK + i] - b_lo, 1u << qq);
         }
-        if (tid < nq) {
-            const int nbq = s_p[tid] >> 2;
-            if (nbq >= b_lo && nbq < b_hi) sel_or(masks, nbq - b_lo, 1u << tid);   // own block
+        if (lane < nq) {
+            const int nbq = s_p[lane] >> 2;
+            if (nbq >= b_lo && nbq - b_lo < span) sel_or(m, nbq - b_lo, 1u << lane);   // own block
         }
-        __syncthreads();
-        // ---- ascending positions of the marked blocks: 8 consecutive blocks per thread
-        constexpr int per = kTcMaxBpi / kPlanThreads;
-        int cnt = 0;
+        __syncwarp();
+        int nu = 0;
+        for (int b0 = 0; b0 < span; b0 += 32) nu += __popc(__ballot_sync(0xffffffffu, b0 + lane < span && m[b0 + lane] != 0));
+        return nu;
+    };
+
+    // ---- pass 1: chunks per interval
+    for (int v = warp; v < n_iv_tile; v += kPlanWarps) {
+        const int nu = mark(v);
+        if (lane == 0) counts[v] = (nu + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
+    }
+    __syncthreads();
+    if (warp == 0) {                           // exclusive scan over the intervals
+        constexpr int per = (kTcMaxIntervals + 31) / 32;
+        int loc[per], sum = 0;
 #pragma unroll
         for (int k = 0; k < per; ++k) {
-            const int i = tid * per + k;
-            cnt += i < span && masks[i] != 0;
+            const int v = lane * per + k;
+            loc[k] = v < n_iv_tile ? counts[v] : 0;
+            sum += loc[k];
         }
-        int incl = cnt;
+        int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        if (lane == 31) s_wsum[warp] = incl;
-        __syncthreads();
-        int before = incl - cnt, nu = 0;
-        for (int w = 0; w < kPlanThreads / 32; ++w) {
-            if (w < warp) before += s_wsum[w];
-            nu += s_wsum[w];
-        }
-        const int n_ch = (nu + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
-        if (base + n_ch > kPlanCap) {          // cannot happen for valid lists; stop cleanly
-            if (tid == 0) record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0);
-            break;
-        }
-        // ---- records: zero, then fill
-        for (int i = tid; i < n_ch * (int)(sizeof(ChunkRec) / 4); i += kPlanThreads) {
-            const int r = i / (sizeof(ChunkRec) / 4), w = i % (sizeof(ChunkRec) / 4);
-            reinterpret_cast<int32_t *>(&recs[r])[w] = w < kTcBlocksPerChunk ? -1 : 0;
-        }
-        __syncthreads();
-        int pos = before;
-#pragma unroll 1
+        __syncwarp();
+        int run = incl - sum;
+#pragma unroll
         for (int k = 0; k < per; ++k) {
-            const int i = tid * per + k;
-            if (i >= span) break;
-            const uint32_t m = masks[i];
-            if (m == 0) continue;
-            const int b = b_lo + i;
-            const int c = pos / kTcBlocksPerChunk, slot = pos % kTcBlocksPerChunk;
-            recs[c].blk[slot] = b;
-            for (int qq = 0; qq < nq; ++qq) {
-                if (!((m >> qq) & 1u)) continue;
-                uint32_t bits = 0xFu;
-                const int p = s_p[qq];
-                if ((p >> 2) == b) bits = (1u << ((p & 3) + 1)) - 1u;   // its own block: up to itself
-                atomicOr(&recs[c].vis[qq][slot >> 3], bits << ((slot & 7) * 4));
-            }
-            ++pos;
+            const int v = lane * per + k;
+            if (v < n_iv_tile) counts[v] = run;
+            run += loc[k];
         }
-        if (tid < n_ch) {
-            recs[tid].first = base + tid == 0;
-            recs[tid].last = v == n_iv_tile - 1 && tid == n_ch - 1;
-        }
-        __syncthreads();
-        // ---- write the interval's records (16-byte stores)
-        const int n16 = n_ch * (int)(sizeof(ChunkRec) / 16);
-        for (int i = tid; i < n16; i += kPlanThreads)
-            reinterpret_cast<uint4 *>(out + base)[i] = reinterpret_cast<const uint4 *>(recs)[i];
-        base += n_ch;
-        __syncthreads();
+        if (lane == 31) s_total = incl;
     }
-    if (tid == 0) a.n_chunks[qt] = base;
+    __syncthreads();
+    const int total = s_total;
+    if (total > kPlanCap) {                    // cannot happen for valid lists; stop cleanly
+        if (tid == 0) {
+            record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0);
+            a.n_chunks[qt] = 0;
+        }
+        return;
+    }
+    // ---- pass 2: records, in ascending block order, through a 3-record staging ring per warp
+    ChunkRec *out = a.recs + (size_t)qt * kPlanCap;
+    for (int v = warp; v < n_iv_tile; v += kPlanWarps) {
+        const int b_lo = v * a.bpi;
+        const int span = min(b_lo + a.bpi, nb_last + 1) - b_lo;
+        const int nu = mark(v);
+        const int n_ch = (nu + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
+        const int off = counts[v];
+        for (int k = 0; k < 3; ++k) stage_clear(&stage[k], lane);
+        __syncwarp();
+        int cur = 0, flushed = 0;
+        auto flush = [&](int c) {              // chunk c of this interval -> global, then clear its slot
+            ChunkRec *r = &stage[c % 3];
+            if (lane == 0) {
+                r->first = off + c == 0;
+                r->last = v == n_iv_tile - 1 && c == n_ch - 1;
+            }
+            __syncwarp();
+            if (lane < (int)(sizeof(ChunkRec) / 16))
+                reinterpret_cast<uint4 *>(out + off + c)[lane] = reinterpret_cast<const uint4 *>(r)[lane];
+            __syncwarp();
+            stage_clear(r, lane);
+            __syncwarp();
+        };
+        for (int b0 = 0; b0 < span; b0 += 32) {
+            const int i = b0 + lane;
+            const uint32_t mk = i < span ? m[i] : 0u;
+            const unsigned bal = __ballot_sync(0xffffffffu, mk != 0);
+            if (bal == 0) continue;
+            if (mk != 0) {
+                const int pos = cur + __popc(bal & ((1u << lane) - 1u));
+                ChunkRec *r = &stage[(pos / kTcBlocksPerChunk) % 3];
+                const int slot = pos % kTcBlocksPerChunk, b = b_lo + i;
+                r->blk[slot] = b;
+                for (uint32_t mm = mk; mm != 0; mm &= mm - 1u) {
+                    const int qq = __ffs(mm) - 1;
+                    uint32_t bits = 0xFu;
+                    const int p = s_p[qq];
+                    if ((p >> 2) == b) bits = (1u << ((p & 3) + 1)) - 1u;   // its own block: up to itself
+                    atomicOr(&r->vis[qq][slot >> 3], bits << ((slot & 7) * 4));
+                }
+            }
+            __syncwarp();
+            cur += __popc(bal);
+            while (flushed < cur / kTcBlocksPerChunk) flush(flushed++);
+        }
+        if (flushed < n_ch) flush(flushed++);  // the interval's last, partial chunk
+    }
+    if (tid == 0) a.n_chunks[qt] = total;
 }
 
 // ----------------------------------------------------------------------------- attention

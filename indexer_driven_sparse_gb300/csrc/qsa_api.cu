@@ -240,8 +240,8 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
         return fail(QSA_ERR_UNSUPPORTED, "p0 + Nc = %lld exceeds the tensor-core prefill's %lld blocks",
                     (long long)p0 + Nc, (long long)kPrefillTcMaxBlocks);
     QSA_NEED(q && k_cache && v_cache && blocks && count && out, "NULL tensor pointer");
-    QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16),
-             "q, k_cache, v_cache and out must be 16-byte aligned");
+    QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16) && aligned(blocks, 16),
+             "q, k_cache, v_cache, out and blocks must be 16-byte aligned");
     char *w = static_cast<char *>(ws);
     AttnArgs a{};
     a.q = q;

@@ -115,6 +115,19 @@ def test_argument_validation(lib):
     assert b"interval" in lib.qsa_last_error()
 
 
+def test_prefill_workspace_and_alignment_checks(lib):
+    # The tensor-core prefill keeps its chunk plan in the workspace; a header-only
+    # workspace is refused before anything launches, and so is a misaligned block list.
+    c = cfg()
+    need = lib.qsa_workspace_size(qb.OP_SPARSE_PREFILL_CHUNK, C.byref(c), 4096, 0)
+    assert need > 4096 // 16 * 150_000
+    assert lib.qsa_sparse_prefill_chunk(C.byref(c), FAKE, 0, 4096, FAKE, FAKE, FAKE, FAKE, 8192, FAKE, 0, FAKE,
+                                        256, 0) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.qsa_sparse_prefill_chunk(C.byref(c), FAKE, 0, 16, FAKE, FAKE, FAKE + 4, FAKE, 8192, FAKE, 0, FAKE,
+                                        need, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"aligned" in lib.qsa_last_error()
+
+
 def test_empty_batches_are_no_ops(lib):
     c = cfg()
     ws = FAKE
