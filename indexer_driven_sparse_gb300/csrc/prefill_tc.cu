@@ -22,12 +22,15 @@
 //                        of O (only when the running max grows by more than 2^8)
 //      O += P V          (M=128, N=256, K=64)    into TMEM columns [256, 512)
 //    Roles:
-//      warps 0-3  softmax: one row per thread; at a tile's end, O / l -> bf16 and the LSE;
-//      warps 4-7  producer: chunk records (cp.async, one ahead), the Q tile, and per chunk
-//                 the K and V rows (16-byte cp.async into 128-byte-swizzled shared
-//                 memory, two stages each, K one chunk ahead of V);
-//      warp 8     one thread issues the MMAs: QK of chunk g+1 before PV of chunk g, so the
-//                 tensor core computes the next scores while the softmax runs.
+//      warps 0-3   softmax: one row per thread; at a tile's end, O / l -> bf16 and the LSE;
+//      warps 4-14  producer: chunk records (bulk copies, one ahead), the Q tile, and per
+//                  chunk the K and V rows (16-byte cp.async into 128-byte-swizzled shared
+//                  memory, two stages each, K one chunk ahead of V). Many warps: a warp's
+//                  cp.async issue stalls on the memory system, so the rows arrive faster
+//                  the more warps issue them (tile::gather4 TMA loads of 128-byte rows
+//                  measured slower still, the engine's cost per operation dominating);
+//      warp 15     one thread issues the MMAs: QK of chunk g+1 before PV of chunk g, so the
+//                  tensor core computes the next scores while the softmax runs.
 //    Hand-offs are mbarriers (cp.async arrivals, tcgen05.commit, thread arrivals).
 // Every wait is bounded (250 ms): a timeout records QSA_ERR_DEVICE_TIMEOUT and raises a CTA
 // flag; each role leaves its loops where all its threads agree, drains what it issued
@@ -284,7 +287,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
 
 // ----------------------------------------------------------------------------- attention
 
-constexpr int kTcSoftmaxThreads = 128, kTcProducerThreads = 128;
+constexpr int kTcSoftmaxThreads = 128, kTcProducerThreads = 352;
+constexpr int kTcMmaWarp = (kTcSoftmaxThreads + kTcProducerThreads) / 32;
 constexpr int kTcThreads = kTcSoftmaxThreads + kTcProducerThreads + 32;
 constexpr int kTcRing = 4;                   // chunk records in flight
 constexpr int kBarProducer = 1;              // named barrier of the producer warps
@@ -326,8 +330,13 @@ __device__ __forceinline__ bool producer_sync_or(bool flag) {
     return r != 0;
 }
 
+// registers per thread: each of the 4 schedulers holds 16K registers for its share of the
+// CTA's warps (one CTA per SM)
+constexpr int kTcMaxRegs = (16384 / (((kTcThreads / 32 + 3) / 4) * 32)) & ~7;
+static_assert(kTcThreads % 128 == 0, "whole warps on every scheduler");
+
 template <int G>
-__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
+__global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
     constexpr int QT = kTcRows / G;                      // queries per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp == 8) tmem_alloc(&tmem_s, 512);
+    if (warp == kTcMmaWarp) tmem_alloc(&tmem_s, 512);
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&k_full[s]), 2 * kTcProducerThreads);   // cp.async + thread arrivals
@@ -376,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
         return false;
     };
 
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 4 && warp < kTcMmaWarp) {
         // ================================================================ producer
         const int pt = tid - kTcSoftmaxThreads;
         const int64_t last_tok = (int64_t)a.p0 + a.Nc - 1;
@@ -500,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
         }
         flush_v();
         asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 8) {
+    } else if (warp == kTcMmaWarp) {
         // ================================================================ MMA issue
         if (lane == 0) {
             int g = 0, n_q = 0, n_tile = -1;
@@ -603,41 +612,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
                     ok = false;
                     break;
                 }
-                const uint64_t vis = ((uint64_t)ring[rs].vis[q_loc][1] << 32) | ring[rs].vis[q_loc][0];
+                const uint32_t vlo = ring[rs].vis[q_loc][0], vhi = ring[rs].vis[q_loc][1];
                 mbar_arrive(smem_u32(&r_empty[rs]));
                 tc_fence_after();
-                float x[kTcChunk];
+                // masked row max over the chunk (raw scores; the scale is positive), 8 partial maxima
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
                 {
-                    float t0[32], t1[32];
-                    tmem_ld32(t_row + s * kTcChunk, t0);
-                    tmem_ld32(t_row + s * kTcChunk + 32, t1);
+                    float s0[32], s1[32];
+                    tmem_ld32_async(t_row + s * kTcChunk, s0);
+                    tmem_ld32_async(t_row + s * kTcChunk + 32, s1);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        x[j] = (vis >> j) & 1u ? t0[j] * a.scale_log2 : -INFINITY;
-                        x[j + 32] = (vis >> (j + 32)) & 1u ? t1[j] * a.scale_log2 : -INFINITY;
+                        mx[j & 7] = fmaxf(mx[j & 7], (vlo >> j) & 1u ? s0[j] : -INFINITY);
+                        mx[j & 7] = fmaxf(mx[j & 7], (vhi >> j) & 1u ? s1[j] : -INFINITY);
                     }
                 }
-                float cmax = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < kTcChunk; ++j) cmax = fmaxf(cmax, x[j]);
+                const float cmax =
+                    fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                    a.scale_log2;
                 // lazy rescale: move the reference only when the row max grew by more than 2^8
                 float f = 1.f;
                 if (cmax > m_ref + 8.f) {
-                    if (m_ref != -INFINITY) f = exp2f(m_ref - cmax);
+                    if (m_ref != -INFINITY) f = ex2_approx(m_ref - cmax);
                     m_ref = cmax;
                 }
                 l_sum *= f;
-                float psum = 0.f;
+                // p = 2^(s * scale - m_ref) on visible columns (m_ref is finite whenever one is);
+                // the scores are read from TMEM again, 32 columns at a time, to keep registers low
+                float ps[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) ps[k] = 0.f;
                 uint32_t pk[kTcChunk / 2];
 #pragma unroll
-                for (int j = 0; j < kTcChunk; j += 2) {
-                    const float e0 = x[j] == -INFINITY ? 0.f : exp2f(x[j] - m_ref);
-                    const float e1 = x[j + 1] == -INFINITY ? 0.f : exp2f(x[j + 1] - m_ref);
-                    psum += e0 + e1;             // fp32 row sum: the LSE stays exact to fp32 rounding
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
-                    pk[j / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                for (int h = 0; h < 2; ++h) {
+                    float sv[32];
+                    tmem_ld32(t_row + s * kTcChunk + h * 32, sv);
+                    const uint32_t vb = h ? vhi : vlo;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float e0 = (vb >> j) & 1u ? ex2_approx(fmaf(sv[j], a.scale_log2, -m_ref)) : 0.f;
+                        const float e1 = (vb >> (j + 1)) & 1u ? ex2_approx(fmaf(sv[j + 1], a.scale_log2, -m_ref)) : 0.f;
+                        ps[(j >> 1) & 7] += e0 + e1;   // fp32 row sum: the LSE stays exact to fp32 rounding
+                        pk[h * 16 + j / 2] = pack_bf16x2(e0, e1);
+                    }
                 }
-                l_sum += psum;
+                l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
                 // P (shared memory) and O are free once the previous PV is done
                 if (g > 0 && !wait_warp(&pv_done, g - 1)) {
                     ok = false;
@@ -703,7 +725,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(TcArgs a) {
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) tmem_dealloc(tmem, 512);
+    if (warp == kTcMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 bool prefill_tc_supported(int Hq, int Hkv) {

@@ -178,13 +178,13 @@ __global__ void __launch_bounds__(kStThreads, 1)
 
 // ----------------------------------------------------------------------------- host side
 
-namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
+// 2-D bf16 tensor maps (rows of `inner` elements, `row_bytes` apart), 128B swizzle
+bool encode_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_rows) {
+    using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                       const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                       CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                       CUtensorMapFloatOOBfill);
     static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q{};
@@ -194,23 +194,15 @@ EncodeTiledFn encode_fn() {
             return nullptr;
         return reinterpret_cast<EncodeTiledFn>(p);
     }();
-    return fn;
-}
-
-// rows x 128 bf16, row stride 256 bytes; boxes of box_rows x 64 columns, 128B swizzle
-bool encode_rows128(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows) {
-    const EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kIdxDim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kIdxDim * 2};
-    const cuuint32_t box[2] = {64, box_rows};
+    if (fn == nullptr || rows == 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool score_tc_supported(int Nq, int64_t n_pooled) {
     return Nq >= kStM && n_pooled >= kStN && n_pooled < ((int64_t)1 << 31) - kStN;
@@ -220,7 +212,8 @@ cudaError_t launch_score_tc(const uint16_t *q_idx, const int32_t *q_pos, int Nq,
                             int64_t n_pooled, const int32_t *blk_off, float *scores, int64_t ld, WsHeader *hdr,
                             cudaStream_t st) {
     CUtensorMap tq, tp;
-    if (!encode_rows128(&tq, q_idx, Nq, kStM) || !encode_rows128(&tp, pooled, n_pooled, kStN))
+    if (!encode_tmap_bf16_2d(&tq, q_idx, kIdxDim, Nq, kIdxDim * 2, 64, kStM) ||
+        !encode_tmap_bf16_2d(&tp, pooled, kIdxDim, n_pooled, kIdxDim * 2, 64, kStN))
         return cudaErrorInvalidValue;
     ScoreTcArgs a{};
     a.q_pos = q_pos;
