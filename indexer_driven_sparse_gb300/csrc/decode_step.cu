@@ -32,6 +32,8 @@
 #include "qsa_internal.cuh"
 #include "qsa_ptx.cuh"
 
+#include <float.h>
+
 namespace qsa {
 
 constexpr int kStepThreads = 512;
@@ -46,7 +48,6 @@ constexpr int kMaxKeys = 12288;                       // score keys per CTA kept
 constexpr int kAttnTok = 32;                          // tokens per attention step
 constexpr int kAttnWeightBlocks = 16384;              // attention cost of a row, in scanned blocks
 constexpr int kMaxPub = 512;                          // published keys per CTA (+1 flag slot)
-constexpr int kMergeRegs = 32;                        // partial values one thread merges
 
 constexpr size_t kRingOff = 0;
 constexpr size_t kKeysOff = kRingOff + (size_t)kRingBytes;
@@ -347,11 +348,13 @@ __device__ unsigned long long select_kth_key64_reg(const unsigned long long *key
     if (diff == 0ull) return mx;
     int hi = 64 - __clzll((long long)diff);
     unsigned long long prefix = hi >= 64 ? 0ull : (mx >> hi) << hi;
+    bool first = true;
     while (hi > 0) {
-        const int width = hi >= 11 ? 11 : hi;
+        // a 12-bit first digit (then 11-bit ones) below the prefix every candidate shares
+        const int width = hi >= (first ? 12 : 11) ? (first ? 12 : 11) : hi;
         const int shift = hi - width;
         const int nbins = 1 << width;
-        for (int i = tid; i < 2048; i += kStepThreads) hist[i] = 0;
+        for (int i = tid; i < 4096; i += kStepThreads) hist[i] = 0;
         __syncthreads();
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -367,9 +370,139 @@ __device__ unsigned long long select_kth_key64_reg(const unsigned long long *key
         need -= *s_above;
         __syncthreads();
         if (in_bin == need) return prefix;
+        if (in_bin <= (uint32_t)kStepThreads) {
+            // the bin's members (distinct keys) -> the need-th largest by counting ranks;
+            // warp-aggregated compaction into the histogram's space
+            unsigned long long *cand = reinterpret_cast<unsigned long long *>(hist);
+            if (tid == 0) *s_above = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const unsigned long long k = kr[r];
+                const bool m = k != 0ull && (k >> shift) == (prefix >> shift);
+                const unsigned bal = __ballot_sync(0xffffffffu, m);
+                if (bal) {
+                    uint32_t base = 0;
+                    if (lane == 0) base = atomicAdd(s_above, (uint32_t)__popc(bal));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    if (m) cand[base + __popc(bal & ((1u << lane) - 1u))] = k;
+                }
+            }
+            __syncthreads();
+            if (tid < (int)in_bin) {
+                const unsigned long long mine = cand[tid];
+                uint32_t rank = 0;
+                for (uint32_t j = 0; j < in_bin; ++j) rank += cand[j] > mine ? 1u : 0u;
+                if (rank == need - 1u) s_red[0] = mine;
+            }
+            __syncthreads();
+            const unsigned long long t = s_red[0];
+            __syncthreads();
+            return t;
+        }
+        first = false;
         hi = shift;
     }
     return prefix;
+}
+
+// The score of a 32-bit order-preserving score key (NaN for the NaN key 0).
+__device__ __forceinline__ float score_of_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// CTA-wide: the need-th largest of the nonzero 64-bit keys in keys[0..n), n <= 8 x 512.
+// The keys' scores (upper halves) fall into 4096 bins linear in the score value, which
+// spreads them where bins on the key's top bits would crowd a few exponents; the threshold
+// bin then holds a few keys, ranked exactly. When the bins cannot split the keys (equal
+// scores, no finite range, more than one CTA's threads of keys in the threshold bin) the
+// radix select takes over.
+__device__ unsigned long long select_kth_key64_lin(const unsigned long long *keys, uint32_t n, uint32_t need,
+                                                   uint32_t *hist, int *s_d, uint32_t *s_above, uint32_t *s_wtot,
+                                                   unsigned long long *s_red, float *s_fred) {
+    constexpr int R = 8;
+    constexpr int kBins = 4096;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t need0 = need;
+    unsigned long long kr[R];
+    float vr[R];
+    float vmin = FLT_MAX, vmax = -FLT_MAX;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t i = tid + r * kStepThreads;
+        kr[r] = i < n ? keys[i] : 0ull;
+        vr[r] = score_of_key((uint32_t)(kr[r] >> 32));
+        if (kr[r] != 0ull && fabsf(vr[r]) <= FLT_MAX) {
+            vmin = fminf(vmin, vr[r]);
+            vmax = fmaxf(vmax, vr[r]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        vmin = fminf(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    }
+    if (lane == 0) {
+        s_fred[warp] = vmin;
+        s_fred[kStepWarps + warp] = vmax;
+    }
+    for (int i = tid; i < kBins; i += kStepThreads) hist[i] = 0;
+    __syncthreads();
+    vmin = lane < kStepWarps ? s_fred[lane] : FLT_MAX;
+    vmax = lane < kStepWarps ? s_fred[kStepWarps + lane] : -FLT_MAX;
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+        vmin = fminf(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    }
+    vmin = __shfl_sync(0xffffffffu, vmin, 0);
+    vmax = __shfl_sync(0xffffffffu, vmax, 0);
+    const float scale = (float)(kBins - 2) / (vmax - vmin);
+    if (!(vmax > vmin && scale > 0.f && scale <= FLT_MAX))
+        return select_kth_key64_reg(keys, n, need, hist, s_d, s_above, s_wtot, s_red);
+    // bins non-decreasing in the key: NaN / -inf lowest, +inf highest
+    auto bin_of = [&](float v) -> int {
+        if (v != v || v == -INFINITY) return 0;
+        if (v == INFINITY) return kBins - 1;
+        return min((int)((v - vmin) * scale), kBins - 2);
+    };
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (kr[r] != 0ull) atomicAdd(&hist[bin_of(vr[r])], 1u);
+    __syncthreads();
+    block_find_bin(hist, kBins, need, s_d, s_above, s_wtot);
+    const int d = *s_d;
+    const uint32_t in_bin = hist[d];
+    need -= *s_above;
+    __syncthreads();
+    if (in_bin > (uint32_t)kStepThreads)
+        return select_kth_key64_reg(keys, n, need0, hist, s_d, s_above, s_wtot, s_red);
+    // the bin's members -> the need-th largest of them by counting ranks (distinct keys)
+    unsigned long long *cand = reinterpret_cast<unsigned long long *>(hist);
+    if (tid == 0) *s_above = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const bool m = kr[r] != 0ull && bin_of(vr[r]) == d;
+        const unsigned bal = __ballot_sync(0xffffffffu, m);
+        if (bal) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(s_above, (uint32_t)__popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (m) cand[base + __popc(bal & ((1u << lane) - 1u))] = kr[r];
+        }
+    }
+    __syncthreads();
+    if (tid < (int)in_bin) {
+        const unsigned long long mine = cand[tid];
+        uint32_t rank = 0;
+        for (uint32_t j = 0; j < in_bin; ++j) rank += cand[j] > mine ? 1u : 0u;
+        if (rank == need - 1u) s_red[0] = mine;
+    }
+    __syncthreads();
+    const unsigned long long t = s_red[0];
+    __syncthreads();
+    return t;
 }
 
 // Warp 0: sum of vals[0..count) (shared memory) -> *out. Other warps skip.
@@ -476,6 +609,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     __shared__ float s_m[2 * kMaxGroup], s_l[2 * kMaxGroup], s_alpha[2 * kMaxGroup];
     __shared__ int32_t s_ctx[kMaxStepRows], s_tok_off[kMaxStepRows + 1], s_blk_off[kMaxStepRows + 1];
     __shared__ int32_t s_debug;
+    __shared__ unsigned long long s_pubk[32];
+    __shared__ float s_fred[2 * kStepWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hq = a.n_q_heads, Hkv = a.n_kv_heads;
@@ -649,8 +784,15 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         // published every key it has, else its K-th largest key (the smallest published).
         const int K = pub_count(cr);
         unsigned long long *pub = a.pub + (size_t)blockIdx.x * (kMaxPub + 1);
+        // with K <= 32 the keys gather in shared memory and are published in block order,
+        // so a reader ranks a CTA's selected keys by block id with one ballot
+        unsigned long long *dst = K <= 32 ? s_pubk : pub;
+        if (K <= 32) {
+            if (tid < 32) s_pubk[tid] = 0ull;
+            __syncthreads();
+        }
         if (n_mine <= K) {
-            for (int i = tid; i < K; i += kStepThreads) pub[i] = i < n_mine ? key64_of(keys[i], lo + i) : 0ull;
+            for (int i = tid; i < K; i += kStepThreads) dst[i] = i < n_mine ? key64_of(keys[i], lo + i) : 0ull;
             if (tid == 0) pub[kMaxPub] = 0ull;
         } else {
             block_find_bin(hist, kHistBins, (uint32_t)K, &s_d, &s_above, s_wsum);
@@ -671,7 +813,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                     const unsigned long long mine = ring64[tid];
                     uint32_t rank = 0;
                     for (uint32_t j = 0; j < nc; ++j) rank += ring64[j] > mine ? 1u : 0u;
-                    if (rank < (uint32_t)K) pub[rank] = mine;
+                    if (rank < (uint32_t)K) dst[rank] = mine;
                     if (rank == (uint32_t)K - 1u) pub[kMaxPub] = mine;
                 }
             } else {
@@ -685,12 +827,26 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                     const unsigned long long k = ring64[i];
                     if (k >= tk) {
                         const uint32_t slot = atomicAdd(&s_cnt[0], 1u);
-                        if (slot < (uint32_t)K) pub[slot] = k;
+                        if (slot < (uint32_t)K) dst[slot] = k;
                         atomicMin(&s_kmin, k);
                     }
                 }
                 __syncthreads();
                 if (tid == 0) pub[kMaxPub] = s_kmin;
+            }
+        }
+        if (K <= 32) {                    // ascending block ids; empty slots (0) last
+            __syncthreads();
+            if (tid < K) {
+                const unsigned long long mine = s_pubk[tid];
+                const uint32_t bm = mine ? 0xFFFFFFFFu - (uint32_t)mine : 0xFFFFFFFFu;
+                uint32_t r = 0;
+                for (int j = 0; j < K; ++j) {
+                    const unsigned long long o = s_pubk[j];
+                    const uint32_t bo = o ? 0xFFFFFFFFu - (uint32_t)o : 0xFFFFFFFFu;
+                    r += (bo < bm || (bo == bm && j < tid)) ? 1u : 0u;
+                }
+                pub[r] = mine;
             }
         }
         STEP_TRACE(3);
@@ -713,19 +869,37 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         // empty slots hold 0, below every real key, so they never reach the threshold;
         // exactly 512 published keys are >= t64
         t64 = n_slots <= 8 * kStepThreads
-                  ? select_kth_key64_reg(ring64, (uint32_t)n_slots, kBlockTopK, hist, &s_d, &s_above, s_wsum, s_red)
+                  ? select_kth_key64_lin(ring64, (uint32_t)n_slots, kBlockTopK, hist, &s_d, &s_above, s_wsum, s_red,
+                                         s_fred)
                   : select_kth_key64(ring64, (uint32_t)n_slots, kBlockTopK, hist, &s_d, &s_above, s_wsum, s_red,
                                      ring64 + n_slots, (uint32_t)(kRingBytes / 8 - n_slots), &s_n);
         STEP_TRACE(15);
         // a CTA with unpublished keys whose K-th key reaches the threshold might hold more
         if (tid == 0) s_overflow = 0;
-        for (int j = tid; j < cr; j += kStepThreads) s_cnt[j] = 0;
-        __syncthreads();
-        for (int j = tid; j < cr; j += kStepThreads)
-            if (s_kth[j] != 0ull && s_kth[j] >= t64) s_overflow = 1;
-        // offsets: selected published keys of every earlier CTA of the row
-        for (int i = tid; i < n_slots; i += kStepThreads)
-            if (ring64[i] >= t64) atomicAdd(&s_cnt[i >> log2k], 1u);
+        for (int i = tid; i < kBlockTopK; i += kStepThreads) s_sel[i] = -1;
+        if (K <= 32) {
+            // one segment of K lanes per publishing CTA: a ballot gives its selected count
+            __syncthreads();
+            const int seg = lane / K, slot = lane % K;
+            const unsigned segmask = K == 32 ? 0xffffffffu : (((1u << K) - 1u) << (seg * K));
+            for (int j0 = warp * (32 / K); j0 < cr; j0 += kStepWarps * (32 / K)) {
+                const int j = j0 + seg;
+                const unsigned long long k = j < cr ? ring64[(j << log2k) + slot] : 0ull;
+                const unsigned bal = __ballot_sync(0xffffffffu, j < cr && k >= t64);
+                if (slot == 0 && j < cr) {
+                    s_cnt[j] = (uint32_t)__popc(bal & segmask);
+                    if (s_kth[j] != 0ull && s_kth[j] >= t64) s_overflow = 1;
+                }
+            }
+        } else {
+            for (int j = tid; j < cr; j += kStepThreads) s_cnt[j] = 0;
+            __syncthreads();
+            for (int j = tid; j < cr; j += kStepThreads)
+                if (s_kth[j] != 0ull && s_kth[j] >= t64) s_overflow = 1;
+            // offsets: selected published keys of every earlier CTA of the row
+            for (int i = tid; i < n_slots; i += kStepThreads)
+                if (ring64[i] >= t64) atomicAdd(&s_cnt[i >> log2k], 1u);
+        }
         __syncthreads();
         if (!s_overflow && K <= 64) {
             // Every CTA rebuilds the row's whole ascending selection from the published keys:
@@ -745,20 +919,36 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                     run += __shfl_sync(0xffffffffu, inc, 31);
                 }
             }
-            for (int i = tid; i < kBlockTopK; i += kStepThreads) s_sel[i] = -1;
             __syncthreads();
-            for (int i = tid; i < n_slots; i += kStepThreads) {
-                const unsigned long long k = ring64[i];
-                if (k >= t64) {
-                    const int j = i >> log2k;
-                    const uint32_t blk = 0xFFFFFFFFu - (uint32_t)k;
-                    uint32_t r = 0;
-                    for (int s2 = 0; s2 < K; ++s2) {
-                        const unsigned long long k2 = ring64[(j << log2k) + s2];
-                        r += (k2 >= t64 && 0xFFFFFFFFu - (uint32_t)k2 < blk) ? 1u : 0u;
+            if (K <= 32) {
+                // a CTA's keys are published in block order: the rank by block id among its
+                // selected keys is the number of selected lanes below in the segment
+                const int seg = lane / K, slot = lane % K;
+                const unsigned segmask = K == 32 ? 0xffffffffu : (((1u << K) - 1u) << (seg * K));
+                for (int j0 = warp * (32 / K); j0 < cr; j0 += kStepWarps * (32 / K)) {
+                    const int j = j0 + seg;
+                    const unsigned long long k = j < cr ? ring64[(j << log2k) + slot] : 0ull;
+                    const bool sel = j < cr && k >= t64;
+                    const unsigned bal = __ballot_sync(0xffffffffu, sel);
+                    if (sel) {
+                        const uint32_t pos = s_cnt[j] + (uint32_t)__popc(bal & segmask & ((1u << lane) - 1u));
+                        if (pos < (uint32_t)kBlockTopK) s_sel[pos] = (int32_t)(0xFFFFFFFFu - (uint32_t)k);
                     }
-                    const uint32_t pos = s_cnt[j] + r;
-                    if (pos < (uint32_t)kBlockTopK) s_sel[pos] = (int32_t)blk;
+                }
+            } else {
+                for (int i = tid; i < n_slots; i += kStepThreads) {
+                    const unsigned long long k = ring64[i];
+                    if (k >= t64) {
+                        const int j = i >> log2k;
+                        const uint32_t blk = 0xFFFFFFFFu - (uint32_t)k;
+                        uint32_t r = 0;
+                        for (int s2 = 0; s2 < K; ++s2) {
+                            const unsigned long long k2 = ring64[(j << log2k) + s2];
+                            r += (k2 >= t64 && 0xFFFFFFFFu - (uint32_t)k2 < blk) ? 1u : 0u;
+                        }
+                        const uint32_t pos = s_cnt[j] + r;
+                        if (pos < (uint32_t)kBlockTopK) s_sel[pos] = (int32_t)blk;
+                    }
                 }
             }
             __syncthreads();
@@ -1031,15 +1221,21 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                          min(kAttnTok, n_tok - (c + 2) * kAttnTok), n_list, dense, s_sel, nb, base, p, row,
                          row_elems);
     }
-    // partial of this CTA: m[Hq], l[Hq], acc[Hq][256]
-    float *mypart = a.part + (size_t)blockIdx.x * Hq * (kHeadDim + 2);
+    // partial of this CTA. The row's region holds (m, l) per CTA, [cr][2 Hq], then the acc
+    // values in blocks of 32 outputs, [Hq x 256 / 32][cr][32]: a warp writes one 128-byte
+    // line per block, and a merging CTA reads each source's line of a block at once.
+    float *rowpart = a.part + (size_t)first * Hq * (kHeadDim + 2);
+    float *ml_r = rowpart, *acc_r = rowpart + (size_t)cr * 2 * Hq;
     if (tid < Hq) {
-        mypart[tid] = s_m[tid];
-        mypart[Hq + tid] = s_l[tid];
+        ml_r[(size_t)jj * 2 * Hq + tid] = s_m[tid];
+        ml_r[(size_t)jj * 2 * Hq + Hq + tid] = s_l[tid];
     }
     if (kv_t < Hkv) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) mypart[2 * Hq + (kv_t * G + g) * kHeadDim + d_t] = acc[g];
+        for (int g = 0; g < G; ++g) {
+            const int o = (kv_t * G + g) * kHeadDim + d_t;
+            acc_r[((size_t)(o >> 5) * cr + jj) * 32 + (o & 31)] = acc[g];
+        }
     }
     STEP_TRACE(7);
 
@@ -1050,77 +1246,77 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     ++bar_k;
     __syncthreads();
     STEP_TRACE(8);
-    const float *parts = a.part + (size_t)first * Hq * (kHeadDim + 2);
-    const int stride = Hq * (kHeadDim + 2);
     const int n_out = Hq * kHeadDim;
     const int o_lo = n_out * jj / cr, o_hi = n_out * (jj + 1) / cr;
     const int h_lo = o_lo / kHeadDim, h_hi = o_hi > o_lo ? (o_hi - 1) / kHeadDim : h_lo - 1;
     const int nh = h_hi - h_lo + 1;
     float *w_s = reinterpret_cast<float *>(smem + kRingOff);           // [nh][cr] m, then weights
     float *l_s = w_s + 2 * kMaxGroup * kMaxStepCtas;                    // [nh][cr] l
-    const int n_my = o_hi - o_lo;
-    int tpo = 1;                                                        // threads per output
-    while (tpo < 32 && (tpo * 2) * n_my <= kStepThreads) tpo *= 2;
-    const int sub = tid % tpo;
-    // one round trip: (m, l) of the slice's heads and this thread's acc values
+    float *red = l_s + 2 * kMaxGroup * kMaxStepCtas;                    // [warps][32]
+    constexpr int kJ = kMaxStepCtas / kStepWarps;                       // sources per warp
+    const int b0 = o_lo >> 5, b1 = o_hi > o_lo ? (o_hi - 1) >> 5 : b0 - 1;
+    // one round trip: (m, l) of the slice's heads and the first block of acc values
     for (int idx = tid; idx < nh * cr; idx += kStepThreads) {
         const int h = h_lo + idx / cr, j = idx % cr;
-        w_s[idx] = __ldcg(&parts[(size_t)j * stride + h]);
-        l_s[idx] = __ldcg(&parts[(size_t)j * stride + Hq + h]);
+        w_s[idx] = __ldcg(&ml_r[(size_t)j * 2 * Hq + h]);
+        l_s[idx] = __ldcg(&ml_r[(size_t)j * 2 * Hq + Hq + h]);
     }
-    for (int o_base = 0; o_base < n_my; o_base += kStepThreads / tpo) {
-        const int oi = o_base + tid / tpo;
-        float av[kMergeRegs];
-        int o = 0, h = 0, d = 0;
-        if (oi < n_my) {
-            o = o_lo + oi;
-            h = o / kHeadDim;
-            d = o % kHeadDim;
+    float v[kJ];
+    auto load_block = [&](int b) {
+#pragma unroll
+        for (int k = 0; k < kJ; ++k) {
+            const int j = warp + k * kStepWarps;
+            v[k] = j < cr ? __ldcg(&acc_r[((size_t)b * cr + j) * 32 + lane]) : 0.f;
+        }
+    };
+    if (b0 <= b1) load_block(b0);
+    __syncthreads();
+    STEP_TRACE(13);
+    for (int hh = warp; hh < nh; hh += kStepWarps) {
+        float M = -INFINITY;
+        for (int j = lane; j < cr; j += 32) M = fmaxf(M, w_s[hh * cr + j]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        for (int j = lane; j < cr; j += 32) {
+            const float mj = w_s[hh * cr + j];
+            const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+            w_s[hh * cr + j] = wj;
+            L = fmaf(l_s[hh * cr + j], wj, L);
         }
 #pragma unroll
-        for (int r = 0; r < kMergeRegs; ++r) {
-            const int j = sub + r * tpo;
-            av[r] = (oi < n_my && j < cr) ? __ldcg(&parts[(size_t)j * stride + 2 * Hq + h * kHeadDim + d]) : 0.f;
+        for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (lane == 0) {
+            s_m[hh] = M;
+            s_l[hh] = L;
+        }
+    }
+    __syncthreads();
+    for (int b = b0; b <= b1; ++b) {
+        if (b > b0) load_block(b);
+        const int h = b >> 3;                                           // 8 blocks of 32 per head
+        const float *wv = w_s + (h - h_lo) * cr;
+        float sacc = 0.f;
+#pragma unroll
+        for (int k = 0; k < kJ; ++k) {
+            const int j = warp + k * kStepWarps;
+            if (j < cr) sacc = fmaf(v[k], wv[j], sacc);
+        }
+        red[warp * 32 + lane] = sacc;
+        __syncthreads();
+        if (warp == 0) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kStepWarps; ++w) tot += red[w * 32 + lane];
+            const int o = b * 32 + lane;
+            if (o >= o_lo && o < o_hi) {
+                const float L = s_l[h - h_lo];
+                a.out[(int64_t)row * n_out + o] = float_to_bf16_bits(tot / L);
+                if (a.lse != nullptr && (o & (kHeadDim - 1)) == 0)
+                    a.lse[(int64_t)row * Hq + h] = (s_m[h - h_lo] + log2f(L)) * kLn2;
+            }
         }
         __syncthreads();
-        if (o_base == 0) STEP_TRACE(13);
-        if (o_base == 0) {
-            for (int hh = warp; hh < nh; hh += kStepWarps) {
-                float M = -INFINITY;
-                for (int j = lane; j < cr; j += 32) M = fmaxf(M, w_s[hh * cr + j]);
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-                float L = 0.f;
-                for (int j = lane; j < cr; j += 32) {
-                    const float mj = w_s[hh * cr + j];
-                    const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-                    w_s[hh * cr + j] = wj;
-                    L = fmaf(l_s[hh * cr + j], wj, L);
-                }
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-                if (lane == 0) {
-                    s_m[hh] = M;
-                    s_l[hh] = L;
-                }
-            }
-            __syncthreads();
-        }
-        float s = 0.f;
-        if (oi < n_my) {
-            const float *wv = w_s + (h - h_lo) * cr;
-#pragma unroll
-            for (int r = 0; r < kMergeRegs; ++r) {
-                const int j = sub + r * tpo;
-                if (j < cr) s = fmaf(av[r], wv[j], s);
-            }
-        }
-        for (int off = tpo >> 1; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (oi < n_my && sub == 0) {
-            const float L = s_l[h - h_lo];
-            a.out[(int64_t)row * n_out + o] = float_to_bf16_bits(s / L);
-            if (a.lse != nullptr && d == 0) a.lse[(int64_t)row * Hq + h] = (s_m[h - h_lo] + log2f(L)) * kLn2;
-        }
     }
     STEP_TRACE(9);
 #undef STEP_TRACE
