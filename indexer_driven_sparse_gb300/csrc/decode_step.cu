@@ -164,12 +164,49 @@ __device__ int bar_arrive(StepRowState *rs, uint32_t g0, int k, int n, WsHeader 
     return *s_flag;
 }
 
-__device__ void bar_release(StepRowState *rs, uint32_t g0, int k) {
+// Plain row barrier (no exclusive work by the last CTA): every CTA polls the arrival
+// counter itself, so no release hop follows the last arrival. Every barrier g leaves the
+// counter of barrier g + 2 cleared: here the last CTA clears it (it was last used by
+// barrier g - 2, which every CTA has passed; no CTA reaches g + 2 before this CTA arrives
+// at g + 1); bar_release clears g + 1 and g + 2 before its release. With publish_gen the
+// last CTA also sets the generation to g (the launch's last barrier; the next launch
+// starts from it). Returns 0, or -1 on a timeout.
+__device__ int bar_sync_fast(StepRowState *rs, uint32_t g0, int k, int n, bool publish_gen, WsHeader *hdr, int row,
+                             int *s_flag) {
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         const uint32_t g = g0 + (uint32_t)k + 1u;
+        uint32_t *cnt = &rs->counts[(g - 1u) & 3u];
+        const uint32_t old = atom_add_acq_rel_u32(cnt, 1u);
+        int res = 0;
+        if (old + 1u == (uint32_t)n) {
+            rs->counts[(g + 1u) & 3u] = 0u;
+            if (publish_gen) st_release_u32(&rs->gen, g);
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_u32(cnt) < (uint32_t)n) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    record_error(hdr, QSA_ERR_DEVICE_TIMEOUT, kWhereStep, row);
+                    res = -1;
+                    break;
+                }
+            }
+        }
+        *s_flag = res;
+    }
+    __syncthreads();
+    return *s_flag;
+}
+
+__device__ void bar_release(StepRowState *rs, uint32_t g0, int k) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // the counters of barriers g + 1 and g + 2: no CTA passes g before this release
+        const uint32_t g = g0 + (uint32_t)k + 1u;
         rs->counts[g & 3u] = 0u;
+        rs->counts[(g + 1u) & 3u] = 0u;
         st_release_u32(&rs->gen, g);
     }
 }
@@ -853,9 +890,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
 
         // ---- 4. one barrier; every CTA derives the same threshold and offsets
         const int stall = s_debug == kDebugStallBarrier ? 1 : 0;
-        const int r1 = bar_arrive(rs, g0, bar_k, cr + stall, a.hdr, row, &s_flag);
-        if (r1 < 0) return;
-        if (r1 == 1) bar_release(rs, g0, bar_k);
+        if (bar_sync_fast(rs, g0, bar_k, cr + stall, false, a.hdr, row, &s_flag) < 0) return;
         ++bar_k;
         STEP_TRACE(4);
         const unsigned long long *pub_row = a.pub + (size_t)first * (kMaxPub + 1);
@@ -1124,7 +1159,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     const int n_tok = t_hi - t_lo;
     const int row_elems = Hkv * kHeadDim;                              // one token's K (or V) row
     const int tok_elems = 2 * row_elems;                               // K row | V row
-    float *q_s = reinterpret_cast<float *>(smem + kKeysOff);           // [Hq][256]
     float *pw = reinterpret_cast<float *>(smem + kHistOff);            // [Hq][kAttnTok]
     uint16_t *const kv_ring = reinterpret_cast<uint16_t *>(smem + kRingOff);   // two halves of 64 KiB
     const int gran_per_tok = tok_elems * 2 / 16;                       // 16-byte granules per token
@@ -1134,12 +1168,23 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     for (int c = 0; c < n_att_chunks && c < 2; ++c)
         gather_chunk(a, kv_ring + (size_t)(c & 1) * (kRingBytes / 4), t_lo + c * kAttnTok,
                      min(kAttnTok, n_tok - c * kAttnTok), n_list, dense, s_sel, nb, base, p, row, row_elems);
-    for (int i = tid; i < Hq * kHeadDim; i += kStepThreads) q_s[i] = bf16_bits_to_float(q_b[i]) * a.scale_log2;
     if (tid < Hq) {
         s_m[tid] = -INFINITY;
         s_l[tid] = 0.f;
     }
     const int kv_t = tid >> 8, d_t = tid & 255;          // PV ownership: (KV head, dim)
+    // logits ownership: a warp takes HW of one KV head's G query heads (their 8 dims per lane
+    // in registers) and every wpg-th token of the chunk, so K is read once per token and group
+    constexpr int HW = G < 8 ? G : 8;
+    constexpr int NH = G / HW;
+    const int n_groups = Hkv * NH, wpg = kStepWarps / n_groups;
+    const int grp = warp / wpg, tsub = warp % wpg;
+    const int kv_l = grp / NH, hs_l = grp % NH;
+    uint4 qr[HW];                                          // bf16 x 8 per head, unpacked in the dot
+#pragma unroll
+    for (int g = 0; g < HW; ++g)
+        qr[g] = grp < n_groups ? *reinterpret_cast<const uint4 *>(q_b + (kv_l * G + hs_l * HW + g) * kHeadDim + lane * 8)
+                               : make_uint4(0, 0, 0, 0);
     float acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = 0.f;
@@ -1151,35 +1196,26 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         else asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
         if (c == 0) STEP_TRACE(10);
-        // logits: one warp per token, 8 dims per lane per KV head, all heads reduced at once
-        for (int i = warp; i < n; i += kStepWarps) {
-            const uint16_t *krow = buf + (size_t)i * tok_elems;
-            float v[2 * G];
-#pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
+        // logits: each warp's HW heads against every wpg-th token (8 dims per lane), the
+        // HW partial dots reduced and scattered over the lanes at once
+        if (grp < n_groups) {
+            for (int i = tsub; i < n; i += wpg) {
                 float kf[8];
-                if (kv < Hkv) unpack8(*reinterpret_cast<const uint4 *>(krow + kv * kHeadDim + lane * 8), kf);
+                unpack8(*reinterpret_cast<const uint4 *>(buf + (size_t)i * tok_elems + kv_l * kHeadDim + lane * 8), kf);
+                float v[HW];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float sum = 0.f;
-                    if (kv < Hkv) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(q_s + (kv * G + g) * kHeadDim + lane * 8);
-                        const float4 qb = *reinterpret_cast<const float4 *>(q_s + (kv * G + g) * kHeadDim + lane * 8 + 4);
-                        sum = kf[0] * qa.x;
-                        sum = fmaf(kf[1], qa.y, sum);
-                        sum = fmaf(kf[2], qa.z, sum);
-                        sum = fmaf(kf[3], qa.w, sum);
-                        sum = fmaf(kf[4], qb.x, sum);
-                        sum = fmaf(kf[5], qb.y, sum);
-                        sum = fmaf(kf[6], qb.z, sum);
-                        sum = fmaf(kf[7], qb.w, sum);
-                    }
-                    v[kv * G + g] = sum;
+                for (int g = 0; g < HW; ++g) {
+                    float qf[8];
+                    unpack8(qr[g], qf);
+                    float sum = kf[0] * qf[0];
+#pragma unroll
+                    for (int e = 1; e < 8; ++e) sum = fmaf(kf[e], qf[e], sum);
+                    v[g] = sum;
                 }
+                int idx = 0;
+                const float tot = warp_reduce_scatter<HW>(v, lane, &idx);
+                if ((lane & (32 / HW - 1)) == 0) pw[(kv_l * G + hs_l * HW + idx) * kAttnTok + i] = tot * a.scale_log2;
             }
-            int idx = 0;
-            const float tot = warp_reduce_scatter<2 * G>(v, lane, &idx);
-            if ((lane & (32 / (2 * G) - 1)) == 0 && idx < Hq) pw[idx * kAttnTok + i] = tot;
         }
         __syncthreads();
         if (c == 0) STEP_TRACE(11);
@@ -1240,9 +1276,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     STEP_TRACE(7);
 
     // ---- 6. merge the row's partials; each CTA finishes a slice of the Hq x 256 outputs
-    const int r3 = bar_arrive(rs, g0, bar_k, cr, a.hdr, row, &s_flag);
-    if (r3 < 0) return;
-    if (r3 == 1) bar_release(rs, g0, bar_k);
+    if (bar_sync_fast(rs, g0, bar_k, cr, true, a.hdr, row, &s_flag) < 0) return;
     ++bar_k;
     __syncthreads();
     STEP_TRACE(8);

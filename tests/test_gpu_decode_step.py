@@ -123,6 +123,29 @@ def test_fused_step_batched_full_size_one_layer(cuda_lib):
     _check(w, b, sep, pooled, rows=[0, 7, 31])
 
 
+def test_fused_step_alternating_paths_share_barrier_state(cuda_lib):
+    # Rows keep barrier counters across launches. Tied scores overflow the published
+    # top-K and take the fallback (four row barriers); spread scores take the common
+    # path (two). Alternating them on one workspace must keep every launch exact.
+    w = I.decode_workload("alt", [200003], 1, 16, 2, "planted", seed=10)
+    L = _to(w.layers[0])
+    b = DecodeBatch(16, 2, w.ctx_len)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    zero_q = torch.zeros_like(L.q_idx)
+    want = {}
+    for name, qi in (("spread", L.q_idx), ("tied", zero_q)):
+        b.step(qi, L.q, L.k_cache, L.v_cache, pooled)
+        want[name] = (b.blocks.clone(), b.out.clone())
+    assert torch.equal(want["tied"][0][0].cpu(), torch.arange(512, dtype=torch.int32))
+    for name in ("tied", "spread", "spread", "tied", "spread", "tied", "tied", "spread"):
+        qi = zero_q if name == "tied" else L.q_idx
+        b.fused_step(L.raw_idx_k, pooled, qi, L.q, L.k_cache, L.v_cache)
+        assert b.fused_status()[0] == 0, name
+        assert torch.equal(b.blocks, want[name][0]), name
+        assert (b.out.float() - want[name][1].float()).abs().max().item() <= 2 ** -6, name
+
+
 def test_fused_step_device_timeout_is_reported(cuda_lib):
     # The header's test knob makes the first row barrier wait for an arrival that never
     # comes; every CTA gives up after its bounded wait and the status says so.
