@@ -30,8 +30,9 @@ constexpr int kStM = 128, kStN = 256;
 constexpr uint32_t kStABytes = kStM * kIdxDim * 2;          // 32 KiB: two 64-column swizzled halves
 constexpr uint32_t kStBBytes = kStN * kIdxDim * 2;          // 64 KiB
 constexpr uint32_t kStStage = kStABytes + kStBBytes;
-constexpr uint32_t kStXpose = 2 * kStStage;                 // per epilogue warp: 32 x 33 floats
-constexpr uint32_t kStSmem = kStXpose + 4 * 32 * 33 * 4 + 1024;
+constexpr int kStXStride = 36;                              // floats per transposed row (16-byte aligned)
+constexpr uint32_t kStXpose = 2 * kStStage;                 // per epilogue warp: 32 x 36 floats
+constexpr uint32_t kStSmem = kStXpose + 4 * 32 * kStXStride * 4 + 1024;
 
 struct ScoreTcArgs {
     const int32_t *q_pos;
@@ -41,6 +42,7 @@ struct ScoreTcArgs {
     float *scores;
     int64_t ld;
     int32_t n_m, n_n;
+    int32_t vec;              // rows 16-byte aligned (scores aligned, ld % 4 == 0): 16-byte stores
     WsHeader *hdr;
 };
 
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
         }
     } else {
         const int q4 = warp & 3;                      // the TMEM lane quarter this warp may access
-        float *xp = reinterpret_cast<float *>(sm + kStXpose) + (warp - 2) * (32 * 33);
+        float *xp = reinterpret_cast<float *>(sm + kStXpose) + (warp - 2) * (32 * kStXStride);
         int i = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
             const int acc = i & 1;
@@ -151,19 +153,33 @@ __global__ void __launch_bounds__(kStThreads, 1)
             const int64_t col0 = (int64_t)n * kStN;
             const int row0 = m * kStM + q4 * 32;
             const int nb_max = __reduce_max_sync(0xffffffffu, (unsigned)nb);
+            // store passes: 4 rows x 32 columns per instruction, lane -> (row, 4 columns)
+            const int sub_r = lane >> 3, sub_c = (lane & 7) * 4;
 #pragma unroll 1
             for (int c = 0; c < kStN / 32; ++c) {
                 float v[32];
                 tmem_ld32(tmem + acc * kStN + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
                 if (col0 + c * 32 >= nb_max) continue;   // warp-uniform: nothing of this slice is kept
 #pragma unroll
-                for (int j = 0; j < 32; ++j) xp[lane * 33 + j] = v[j];
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4 *>(xp + lane * kStXStride + 4 * q) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 __syncwarp();
-                const int64_t col = col0 + c * 32 + lane;
-#pragma unroll 4
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int nb_r = __shfl_sync(0xffffffffu, nb, rr);
-                    if (col < nb_r) a.scores[(int64_t)(row0 + rr) * a.ld + col] = xp[rr * 33 + lane];
+                const int64_t col = col0 + c * 32 + sub_c;
+#pragma unroll
+                for (int pass = 0; pass < 8; ++pass) {
+                    const int rl = pass * 4 + sub_r;
+                    const int nb_r = __shfl_sync(0xffffffffu, nb, rl);
+                    const float4 val = *reinterpret_cast<const float4 *>(xp + rl * kStXStride + sub_c);
+                    float *dst = a.scores + (int64_t)(row0 + rl) * a.ld + col;
+                    if (a.vec && col + 4 <= nb_r) {
+                        *reinterpret_cast<float4 *>(dst) = val;
+                    } else {
+                        if (col < nb_r) dst[0] = val.x;
+                        if (col + 1 < nb_r) dst[1] = val.y;
+                        if (col + 2 < nb_r) dst[2] = val.z;
+                        if (col + 3 < nb_r) dst[3] = val.w;
+                    }
                 }
                 __syncwarp();
             }
@@ -224,6 +240,7 @@ cudaError_t launch_score_tc(const uint16_t *q_idx, const int32_t *q_pos, int Nq,
     a.ld = ld;
     a.n_m = (Nq + kStM - 1) / kStM;
     a.n_n = (int)((ld + kStN - 1) / kStN);
+    a.vec = ((uintptr_t)scores % 16 == 0 && ld % 4 == 0) ? 1 : 0;
     a.hdr = hdr;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -104,7 +104,8 @@ class PrefillChunk:
         i32 = dict(dtype=torch.int32, device=device)
         self.n_tokens = self.p0 + self.Nc
         self.n_pooled = self.n_tokens // RATIO
-        self.ld = max(1, (self.p0 + self.Nc - 1) // RATIO)
+        # score rows padded to 32 floats (128 bytes): aligned line writes and vector reads
+        self.ld = max(1, (self.p0 + self.Nc - 1) // RATIO + 31) // 32 * 32
         self.tok_off = torch.tensor([0, self.n_tokens], **i32)
         self.blk_off = torch.zeros(2, **i32)
         self.q_seq = torch.zeros(self.Nc, **i32)
