@@ -25,6 +25,8 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kLinBins = 4096;
 constexpr int kCandCap = 4096;
+constexpr int kCandBins = 1024;                 // bins over the sampled path's candidates
+constexpr int kScanBatch = 8;                   // 16-byte loads a thread keeps in flight per sweep
 static_assert(kCandCap * 2 >= kLinBins, "the histogram lives in the candidate buffer");
 
 // Calls f(i, v, valid) over the row with every thread taking the same number of calls
@@ -40,16 +42,23 @@ __device__ __forceinline__ void row_scan(const float *__restrict__ s, int64_t nb
     }
     const int64_t nvec = (nb - head) >> 2;
     const float4 *v4 = reinterpret_cast<const float4 *>(s + head);
-#pragma unroll 4
-    for (int64_t j0 = 0; j0 < nvec; j0 += kTopkThreads) {
-        const int64_t j = j0 + tid;
-        const bool ok = j < nvec;
-        const float4 x = ok ? __ldg(v4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const int64_t i = head + 4 * j;
-        f(i, x.x, ok);
-        f(i + 1, x.y, ok);
-        f(i + 2, x.z, ok);
-        f(i + 3, x.w, ok);
+    for (int64_t j0 = 0; j0 < nvec; j0 += kScanBatch * kTopkThreads) {
+        float4 x[kScanBatch];                    // all loads of the batch in flight at once
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+            const int64_t j = j0 + u * kTopkThreads + tid;
+            x[u] = j < nvec ? __ldg(v4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+            const int64_t j = j0 + u * kTopkThreads + tid;
+            const bool ok = j < nvec;
+            const int64_t i = head + 4 * j;
+            f(i, x[u].x, ok);
+            f(i + 1, x[u].y, ok);
+            f(i + 2, x[u].z, ok);
+            f(i + 3, x[u].w, ok);
+        }
     }
     const int64_t t0 = head + 4 * nvec;
     if (t0 < nb) {
@@ -58,19 +67,29 @@ __device__ __forceinline__ void row_scan(const float *__restrict__ s, int64_t nb
     }
 }
 
-// Bin of a score, non-decreasing in the score: NaN and -inf lowest, +inf highest.
+// The score of a 64-bit key (score key << 32 | ~id): NaN for the NaN key.
+__device__ __forceinline__ float key_score(uint64_t key) {
+    const uint32_t k = (uint32_t)(key >> 32);
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Bin of a score, non-decreasing in the score for any vmin and scale > 0 (values outside
+// the range clamp to the end bins): NaN and -inf lowest, +inf highest.
 __device__ __forceinline__ int lin_bin(float v, float vmin, float scale) {
     if (v != v || v == -INFINITY) return 0;
     if (v == INFINITY) return kLinBins - 1;
-    const int b = (int)((v - vmin) * scale);
-    return min(b, kLinBins - 2);
+    const float t = (v - vmin) * scale;
+    if (!(t > 0.f)) return 0;
+    return t >= (float)(kLinBins - 2) ? kLinBins - 2 : (int)t;
 }
 
 // Block-wide: the bin b* (counting from the top) where the running count first reaches
 // `need`, and the count strictly above it. Each thread owns kLinBins / kTopkThreads bins.
+template <int NBINS = kLinBins>
 __device__ void find_bin_from_top(const uint32_t *hist, uint32_t need, int *b_out, uint32_t *above_out,
                                   uint32_t *wtot) {
-    constexpr int per = kLinBins / kTopkThreads;
+    constexpr int per = NBINS / kTopkThreads;
+    static_assert(per >= 1 && NBINS % kTopkThreads == 0, "bins per thread");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t h[per], sum = 0;
 #pragma unroll
@@ -206,6 +225,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float 
     __shared__ uint64_t cand[kCandCap];        // the histogram shares this space (used before the candidates)
     uint32_t *hist = reinterpret_cast<uint32_t *>(cand);
     __shared__ int32_t sel[kBlockTopK];
+    __shared__ uint32_t hist2[kCandBins];
+    __shared__ uint64_t s_eq[kTopkThreads];
+    __shared__ uint32_t s_neq;
     __shared__ uint32_t wtot[kTopkWarps];
     __shared__ float s_red[2][kTopkWarps];
     __shared__ int s_b;
@@ -230,6 +252,215 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float 
         return;
     }
     const float *s = scores + (int64_t)row * ld;
+    const unsigned lt = (1u << lane) - 1u;
+
+    // ---- one pass when a sample places the cut: every 64th score sets value-linear bins
+    // and a bin cut keeping about 3 x 512 of the row; one streaming pass gathers every score
+    // in bins at or above the cut as exact 64-bit keys. Bins are monotone, so when at least
+    // 512 scores clear the cut the row's top 512 are among them. Otherwise (or if they
+    // overflow the candidate buffer) the passes below decide.
+    constexpr int kSampleStride = 64;
+    const int64_t n_s = nb / kSampleStride;
+    if (n_s >= 256) {
+        float smin = FLT_MAX, smax = -FLT_MAX;
+        bool any_s = false;
+        for (int64_t k = tid; k < n_s; k += kTopkThreads) {
+            const float v = __ldg(s + k * kSampleStride);
+            if (fabsf(v) <= FLT_MAX) {
+                smin = fminf(smin, v);
+                smax = fmaxf(smax, v);
+                any_s = true;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+            smin = fminf(smin, __shfl_xor_sync(0xffffffffu, smin, o));
+        }
+        if (lane == 0) {
+            s_red[0][warp] = smax;
+            s_red[1][warp] = smin;
+        }
+        for (int i = tid; i < kLinBins; i += kTopkThreads) hist[i] = 0;
+        if (tid == 0) {
+            s_ncand = 0;
+            s_neq = 0;
+        }
+        const bool any_sample = __syncthreads_or(any_s);
+        smax = s_red[0][0];
+        smin = s_red[1][0];
+        for (int w = 1; w < kTopkWarps; ++w) {
+            smax = fmaxf(smax, s_red[0][w]);
+            smin = fminf(smin, s_red[1][w]);
+        }
+        const float sscale = (float)(kLinBins - 2) / (smax - smin);
+        if (any_sample && smax > smin && sscale > 0.f && sscale <= FLT_MAX) {
+            for (int64_t k = tid; k < n_s; k += kTopkThreads)
+                atomicAdd(&hist[lin_bin(__ldg(s + k * kSampleStride), smin, sscale)], 1u);
+            __syncthreads();
+            const int64_t want = 3 * ((int64_t)kBlockTopK * n_s + nb - 1) / nb + 8;
+            find_bin_from_top(hist, (uint32_t)(want < n_s ? want : n_s), &s_b, &s_above, wtot);
+            const int cut = s_b;
+            __syncthreads();                    // the candidates overwrite the histogram
+            // a cheap floor one bin below the cut filters most scores; the exact bin test and the
+            // warp-aggregated append run only where some lane of the warp has a candidate
+            const float vlow = smin + (float)(cut - 1) / sscale;
+            auto append = [&](int64_t i, float v, bool m) {
+                const unsigned bal = __ballot_sync(0xffffffffu, m);
+                if (bal) {
+                    uint32_t base = 0;
+                    if (lane == 0) base = atomicAdd(&s_ncand, (uint32_t)__popc(bal));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    const uint32_t slot = base + __popc(bal & lt);
+                    if (m && slot < (uint32_t)kCandCap)
+                        cand[slot] = ((uint64_t)score_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+                }
+            };
+            auto is_cand = [&](float v) { return !(v < vlow) && lin_bin(v, smin, sscale) >= cut; };
+            const int64_t mis = (int64_t)(((16 - ((uintptr_t)s & 15)) & 15) >> 2);
+            const int64_t head = mis < nb ? mis : nb;
+            if (head > 0) {
+                const bool okh = tid < head;
+                const float v = okh ? __ldg(s + tid) : 0.f;
+                append(tid, v, okh && is_cand(v));
+            }
+            const int64_t nvec = (nb - head) >> 2;
+            const float4 *v4 = reinterpret_cast<const float4 *>(s + head);
+            for (int64_t j0 = 0; j0 < nvec; j0 += kScanBatch * kTopkThreads) {
+                float4 x[kScanBatch];                // all loads of the batch in flight at once
+#pragma unroll
+                for (int u = 0; u < kScanBatch; ++u) {
+                    const int64_t j = j0 + u * kTopkThreads + tid;
+                    x[u] = j < nvec ? __ldg(v4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+                // this lane's candidates of the batch as a bit mask; one warp scan gives slots
+                uint32_t mk = 0;
+#pragma unroll
+                for (int u = 0; u < kScanBatch; ++u) {
+                    mk |= (is_cand(x[u].x) ? 1u : 0u) << (4 * u);
+                    mk |= (is_cand(x[u].y) ? 1u : 0u) << (4 * u + 1);
+                    mk |= (is_cand(x[u].z) ? 1u : 0u) << (4 * u + 2);
+                    mk |= (is_cand(x[u].w) ? 1u : 0u) << (4 * u + 3);
+                }
+                const uint32_t cnt = __popc(mk);
+                uint32_t incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                uint32_t base = 0;
+                if (lane == 31 && incl) base = atomicAdd(&s_ncand, incl);
+                base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+                if (mk) {
+#pragma unroll
+                    for (int u = 0; u < kScanBatch; ++u) {
+                        const int64_t i = head + 4 * (j0 + u * kTopkThreads + tid);
+                        const float vv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if ((mk >> (4 * u + e)) & 1u) {
+                                if (base < (uint32_t)kCandCap)
+                                    cand[base] = ((uint64_t)score_key(vv[e]) << 32) |
+                                                 (uint64_t)(0xFFFFFFFFu - (uint32_t)(i + e));
+                                ++base;
+                            }
+                        }
+                    }
+                }
+            }
+            const int64_t t0 = head + 4 * nvec;
+            if (t0 < nb) {
+                const bool okt = t0 + tid < nb;
+                const float v = okt ? __ldg(s + t0 + tid) : 0.f;
+                append(t0 + tid, v, okt && is_cand(v));
+            }
+            __syncthreads();
+            const uint32_t nc = s_ncand;
+            if (nc >= (uint32_t)kBlockTopK && nc <= (uint32_t)kCandCap) {
+                // exact top 512 of the candidates: 1024 bins linear in their scores, the
+                // threshold bin's members ranked by key, the sure ones taken directly
+                float cmin = FLT_MAX, cmax = -FLT_MAX;
+                for (uint32_t k = tid; k < nc; k += kTopkThreads) {
+                    const float v = key_score(cand[k]);
+                    if (fabsf(v) <= FLT_MAX) {
+                        cmin = fminf(cmin, v);
+                        cmax = fmaxf(cmax, v);
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+                    cmin = fminf(cmin, __shfl_xor_sync(0xffffffffu, cmin, o));
+                }
+                if (lane == 0) {
+                    s_red[0][warp] = cmax;
+                    s_red[1][warp] = cmin;
+                }
+                for (int i = tid; i < kCandBins; i += kTopkThreads) hist2[i] = 0;
+                if (tid == 0) s_nsel = 0;
+                __syncthreads();
+                cmax = s_red[0][0];
+                cmin = s_red[1][0];
+                for (int w = 1; w < kTopkWarps; ++w) {
+                    cmax = fmaxf(cmax, s_red[0][w]);
+                    cmin = fminf(cmin, s_red[1][w]);
+                }
+                const float cscale = cmax > cmin ? (float)(kCandBins - 2) / (cmax - cmin) : 0.f;
+                if (cscale > 0.f && cscale <= FLT_MAX) {
+                    auto cbin = [&](float v) -> int {
+                        if (v != v || v == -INFINITY) return 0;
+                        if (v == INFINITY) return kCandBins - 1;
+                        const float t = (v - cmin) * cscale;
+                        if (!(t > 0.f)) return 0;
+                        return t >= (float)(kCandBins - 2) ? kCandBins - 2 : (int)t;
+                    };
+                    for (uint32_t k = tid; k < nc; k += kTopkThreads) atomicAdd(&hist2[cbin(key_score(cand[k]))], 1u);
+                    __syncthreads();
+                    find_bin_from_top<kCandBins>(hist2, kBlockTopK, &s_b, &s_above, wtot);
+                    const int bd = s_b;
+                    const uint32_t need_eq = kBlockTopK - s_above;
+                    const uint32_t n_eq = hist2[bd];
+                    if (n_eq <= (uint32_t)kTopkThreads) {
+                        // sure keys -> their ids; the threshold bin's keys -> a small list
+                        for (uint32_t k0 = 0; k0 < nc; k0 += kTopkThreads) {
+                            const uint32_t k = k0 + tid;
+                            const uint64_t key = k < nc ? cand[k] : 0ull;
+                            const int b = k < nc ? cbin(key_score(key)) : -1;
+                            const bool sure = b > bd, eq = b == bd;
+                            const unsigned bs = __ballot_sync(0xffffffffu, sure);
+                            const unsigned be = __ballot_sync(0xffffffffu, eq);
+                            uint32_t o1 = 0, o2 = 0;
+                            if (lane == 0) {
+                                if (bs) o1 = atomicAdd(&s_nsel, (uint32_t)__popc(bs));
+                                if (be) o2 = atomicAdd(&s_neq, (uint32_t)__popc(be));
+                            }
+                            o1 = __shfl_sync(0xffffffffu, o1, 0);
+                            o2 = __shfl_sync(0xffffffffu, o2, 0);
+                            if (sure) sel[o1 + __popc(bs & lt)] = (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+                            if (eq) s_eq[o2 + __popc(be & lt)] = key;
+                        }
+                        __syncthreads();
+                        if (tid < (int)n_eq) {
+                            const uint64_t mine = s_eq[tid];
+                            uint32_t rank = 0;
+                            for (uint32_t j = 0; j < n_eq; ++j) rank += s_eq[j] > mine ? 1u : 0u;
+                            if (rank < need_eq) sel[s_above + rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)mine);
+                        }
+                        __syncthreads();
+                        bitonic_i32_asc(sel, kBlockTopK);
+                        for (int i = tid; i < kBlockTopK; i += kTopkThreads) out[i] = sel[i];
+                        if (tid == 0) {
+                            count[row] = kBlockTopK;
+                            if (s_nsel != s_above || s_neq != n_eq) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereTopk, row);
+                        }
+                        return;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
 
     // ---- pass 1: finite max and min
     float vmax = -FLT_MAX, vmin = FLT_MAX;
@@ -281,7 +512,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float 
         const int bstar = s_b;
         const uint32_t need_eq = kBlockTopK - s_above;
         // ---- pass 3: append the sure blocks, gather the k-th bin's candidates
-        const unsigned lt = (1u << lane) - 1u;
         row_scan(s, nb, [&](int64_t i, float v, bool ok) {
             const int b = ok ? lin_bin(v, vmin, scale) : -1;
             const bool sure = b > bstar, maybe = b == bstar;
