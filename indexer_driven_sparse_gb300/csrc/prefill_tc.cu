@@ -75,11 +75,61 @@ constexpr uint32_t kPlMasks = kPlCounts + 4 * (kTcMaxIntervals + 8);       // ui
 constexpr uint32_t kPlStage = kPlMasks + 2 * kTcMaxBpi * kPlanWarps;       // ChunkRec [warp][3]
 constexpr uint32_t kPlSmem = kPlStage + sizeof(ChunkRec) * 3 * kPlanWarps;
 
+static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// plan layout: chunk counts [n_qt], the dealt tile order [< 2 * n_tiles], chunk records [n_qt][kPlanCap]
 size_t prefill_tc_plan_bytes(int Nc, int Hq, int Hkv) {
     if (!prefill_tc_supported(Hq, Hkv) || Nc <= 0) return 0;
     const int QT = kTcRows / (Hq / Hkv);
     const size_t n_qt = (size_t)(Nc + QT - 1) / QT;
-    return ((n_qt * 4 + 255) / 256) * 256 + n_qt * kPlanCap * sizeof(ChunkRec);
+    return round256(n_qt * 4) + round256(n_qt * Hkv * 2 * 4) + n_qt * kPlanCap * sizeof(ChunkRec);
+}
+
+// One CTA: query tiles sorted by chunk count, largest first (counting sort), and their (tile, KV
+// head) work items dealt to the CTAs in snake order: round r goes left to right when r is even,
+// right to left when odd, so every CTA's summed load stays close to the mean.
+constexpr int kOrderThreads = 1024;
+__global__ void __launch_bounds__(kOrderThreads) prefill_order_kernel(const int32_t *n_chunks, int n_qt, int Hkv,
+                                                                      int grid, int n_rounds, int32_t *order) {
+    __shared__ int base[kPlanCap + 1];
+    for (int i = threadIdx.x; i <= kPlanCap; i += blockDim.x) base[i] = 0;
+    __syncthreads();
+    for (int q = threadIdx.x; q < n_qt; q += blockDim.x) atomicAdd(&base[min(max(n_chunks[q], 0), kPlanCap)], 1);
+    __syncthreads();
+    if (threadIdx.x < 32) {      // base[s] = query tiles with more than s chunks (one warp, sizes descending)
+        const int lane = threadIdx.x;
+        constexpr int kPer = (kPlanCap + 1 + 31) / 32;
+        int v[kPer], sum = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int s = kPlanCap - (lane * kPer + j);
+            v[j] = s >= 0 ? base[s] : 0;
+            sum += v[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int s = kPlanCap - (lane * kPer + j);
+            if (s >= 0) base[s] = run;
+            run += v[j];
+        }
+    }
+    __syncthreads();
+    auto slot = [&](int k) -> int {      // position of sorted work item k in the [round][CTA] table
+        const int r = k / grid, c = k - r * grid;
+        return r * grid + ((r & 1) ? grid - 1 - c : c);
+    };
+    for (int q = threadIdx.x; q < n_qt; q += blockDim.x) {
+        const int rank = atomicAdd(&base[min(max(n_chunks[q], 0), kPlanCap)], 1);
+        for (int h = 0; h < Hkv; ++h) order[slot(rank * Hkv + h)] = q * Hkv + h;
+    }
+    for (int k = n_qt * Hkv + threadIdx.x; k < n_rounds * grid; k += blockDim.x) order[slot(k)] = -1;
 }
 
 struct PlanArgs {
@@ -309,6 +359,7 @@ struct TcArgs {
     float *lse;               // [Nc, Hq] or nullptr
     const int32_t *n_chunks;  // [n_qt] (plan)
     const ChunkRec *recs;     // [n_qt][kPlanCap] (plan)
+    const int32_t *order;     // [rounds][grid] tiles dealt to the CTAs (plan), -1 past the end
     int32_t p0, Nc, Hq, Hkv;
     float scale_log2;
     WsHeader *hdr;
@@ -377,6 +428,10 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
     const uint32_t tmem = tmem_s;
     const int n_qt = (a.Nc + QT - 1) / QT;
     const int n_tiles = n_qt * a.Hkv;
+    // this CTA's tiles: one per round of the dealt order (largest first), -1 past the end
+    const int n_rounds = (n_tiles + (int)gridDim.x - 1) / (int)gridDim.x;
+    auto tile_at = [&](int r) -> int { return r < n_rounds ? a.order[(size_t)r * gridDim.x + blockIdx.x] : -1; };
+    auto size_at = [&](int t) -> int { return t >= 0 ? a.n_chunks[t / a.Hkv] : 0; };
 
     auto wait = [&](uint64_t *bar, uint32_t phase) -> bool {
         if (mbar_wait_bounded(smem_u32(bar), phase & 1u, kWaitLimitNs)) return true;
@@ -390,24 +445,26 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         const int pt = tid - kTcSoftmaxThreads;
         const int64_t last_tok = (int64_t)a.p0 + a.Nc - 1;
         bool ok = true;
-        // the CTA's chunk stream: (tile, chunk) in order; a tile has n_chunks[tile / Hkv] chunks
-        int tile = blockIdx.x, c_in = 0, n_ch = tile < n_tiles ? a.n_chunks[tile / a.Hkv] : 0;
-        auto advance = [&](int &t, int &c, int &n) {    // to the next chunk of the stream
+        // the CTA's chunk stream: its tile list in order, chunk by chunk; tiles without chunks
+        // (invalid lists) are skipped
+        int ri = 0, c_in = 0, tile = tile_at(0), n_ch = size_at(tile);
+        auto advance = [&](int &r, int &t, int &c, int &n) {    // to the next chunk of the stream
             ++c;
-            while (t < n_tiles && c >= n) {
-                t += gridDim.x;
+            while (r < n_rounds && c >= n) {
+                ++r;
+                t = tile_at(r);
                 c = 0;
-                n = t < n_tiles ? a.n_chunks[t / a.Hkv] : 0;
+                n = size_at(t);
             }
         };
-        if (tile < n_tiles && n_ch == 0) {      // tiles without chunks (invalid lists) are skipped
+        if (n_rounds > 0 && n_ch == 0) {
             c_in = -1;
-            advance(tile, c_in, n_ch);
+            advance(ri, tile, c_in, n_ch);
         }
         // chunk records arrive through the bulk-copy engine, one chunk ahead of the gathers
-        int pf_tile = tile, pf_c = c_in, pf_n = n_ch, pf_g = 0;
+        int pf_ri = ri, pf_tile = tile, pf_c = c_in, pf_n = n_ch, pf_g = 0;
         auto prefetch = [&]() -> bool {         // record of chunk pf_g into ring slot pf_g % ring
-            if (pf_tile >= n_tiles) return true;
+            if (pf_ri >= n_rounds) return true;
             const int rs = pf_g % kTcRing;
             bool w_ok = true;
             if (pt == 0) {
@@ -420,7 +477,7 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                 }
             }
             ++pf_g;
-            advance(pf_tile, pf_c, pf_n);
+            advance(pf_ri, pf_tile, pf_c, pf_n);
             return !producer_sync_or(!w_ok || s_abort);
         };
         int g = 0, t_loc = -1, pending = -1, pending_gkv = 0;
@@ -448,7 +505,7 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         };
         ok = prefetch();
         int cur_tile = -1;
-        while (ok && tile < n_tiles) {
+        while (ok && ri < n_rounds) {
             const int gkv = tile % a.Hkv;
             if (tile != cur_tile) {
                 // ---- a new tile: its Q rows once the previous tile's QK MMAs are done
@@ -505,7 +562,7 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
             pending = g;
             pending_gkv = gkv;
             ++g;
-            advance(tile, c_in, n_ch);
+            advance(ri, tile, c_in, n_ch);
         }
         flush_v();
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -514,16 +571,16 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         if (lane == 0) {
             int g = 0, n_q = 0, n_tile = -1;
             // this CTA's chunk stream: (tile, chunk) in order, tiles without chunks skipped
-            int it_t = blockIdx.x, it_c = -1;
-            int it_n = it_t < n_tiles ? a.n_chunks[it_t / a.Hkv] : 0;
+            int it_r = 0, it_c = -1;
+            int it_n = size_at(tile_at(0));
             auto next_chunk = [&](int &f, int &l) -> bool {
                 ++it_c;
-                while (it_t < n_tiles && it_c >= it_n) {   // each pass moves to the next tile
-                    it_t += gridDim.x;
+                while (it_r < n_rounds && it_c >= it_n) {  // each pass moves to the next tile
+                    ++it_r;
                     it_c = 0;
-                    it_n = it_t < n_tiles ? a.n_chunks[it_t / a.Hkv] : 0;
+                    it_n = size_at(tile_at(it_r));
                 }
-                if (it_t >= n_tiles) return false;
+                if (it_r >= n_rounds) return false;
                 f = it_c == 0;
                 l = it_c == it_n - 1;
                 return true;
@@ -600,9 +657,10 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
             const bool w = wait(bar, phase);
             return __all_sync(0xffffffffu, w) && !__any_sync(0xffffffffu, s_abort != 0);
         };
-        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-            const int n_ch = a.n_chunks[tile / a.Hkv];
-            if (n_ch == 0) continue;                     // invalid lists: nothing attended
+        for (int r = 0; r < n_rounds && ok; ++r) {
+            const int tile = tile_at(r);
+            const int n_ch = size_at(tile);
+            if (n_ch == 0) continue;                     // no tile, or invalid lists: nothing attended
             const int i0 = (tile / a.Hkv) * QT, nq = min(QT, a.Nc - i0), gkv = tile % a.Hkv;
             float m_ref = -INFINITY, l_sum = 0.f;
             bool o_init = false;
@@ -739,10 +797,19 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, int interval_tokens, WsHeader *
     const int QT = kTcRows / G;
     const int n_qt = (a.rows + QT - 1) / QT;
     if (scratch_bytes < prefill_tc_plan_bytes(a.rows, a.n_q_heads, a.n_kv_heads)) return cudaErrorInvalidValue;
+    const int n_tiles = n_qt * a.n_kv_heads;
     char *sp = static_cast<char *>(scratch);
     int32_t *n_chunks = reinterpret_cast<int32_t *>(sp);
-    ChunkRec *recs = reinterpret_cast<ChunkRec *>(sp + (((size_t)n_qt * 4 + 255) / 256) * 256);
+    int32_t *order = reinterpret_cast<int32_t *>(sp + round256((size_t)n_qt * 4));
+    ChunkRec *recs = reinterpret_cast<ChunkRec *>(sp + round256((size_t)n_qt * 4) + round256((size_t)n_tiles * 2 * 4));
     if (((uintptr_t)recs & 255) != 0) return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(sms, n_tiles));
+    const int n_rounds = (n_tiles + grid - 1) / grid;    // n_rounds * grid < 2 * n_tiles
 
     const int64_t n_blocks = ((int64_t)a.p0 + a.rows) / kRatio + 1;
     // the interval sets the evaluation order only; it is clamped to what the on-chip tables hold
@@ -761,9 +828,12 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, int interval_tokens, WsHeader *
     pa.n_chunks = n_chunks;
     pa.recs = recs;
     pa.hdr = hdr;
-    cudaError_t e = cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPlSmem);
+    e = cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPlSmem);
     if (e != cudaSuccess) return e;
     prefill_plan_kernel<<<n_qt, kPlanThreads, kPlSmem, st>>>(pa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prefill_order_kernel<<<1, kOrderThreads, 0, st>>>(n_chunks, n_qt, a.n_kv_heads, grid, n_rounds, order);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -775,19 +845,13 @@ cudaError_t launch_prefill_tc(const AttnArgs &a, int interval_tokens, WsHeader *
     t.lse = a.lse;
     t.n_chunks = n_chunks;
     t.recs = recs;
+    t.order = order;
     t.p0 = a.p0;
     t.Nc = a.rows;
     t.Hq = a.n_q_heads;
     t.Hkv = a.n_kv_heads;
     t.scale_log2 = a.scale_log2;
     t.hdr = hdr;
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    const int n_tiles = n_qt * a.n_kv_heads;
-    const int grid = std::max(1, std::min(sms, n_tiles));
     switch (G) {
         case 8:
             e = cudaFuncSetAttribute(prefill_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
