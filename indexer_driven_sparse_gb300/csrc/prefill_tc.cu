@@ -23,12 +23,15 @@
 //      O += P V          (M=128, N=256, K=64)    into TMEM columns [256, 512)
 //    Roles:
 //      warps 0-3   softmax: one row per thread; at a tile's end, O / l -> bf16 and the LSE;
-//      warps 4-14  producer: chunk records (bulk copies, one ahead), the Q tile, and per
-//                  chunk the K and V rows (16-byte cp.async into 128-byte-swizzled shared
-//                  memory, two stages each, K one chunk ahead of V). Many warps: a warp's
-//                  cp.async issue stalls on the memory system, so the rows arrive faster
-//                  the more warps issue them (tile::gather4 TMA loads of 128-byte rows
-//                  measured slower still, the engine's cost per operation dominating);
+//      warps 4-13  V rows: per chunk 64 tokens x 512 bytes as 16-byte cp.async into
+//                  128-byte-swizzled shared memory (two stages). Many warps: a warp's
+//                  cp.async issue stalls on the memory system, so rows arrive faster the
+//                  more warps issue them;
+//      warp 14     one thread drives the tensor-memory-access engine: chunk records (bulk
+//                  copies, one ahead), the Q tile, and the K rows (two stages), one tiled
+//                  load per block and 64-column slice (4 tokens x 128 bytes, swizzled). K
+//                  and V thus travel on two independent paths from L2, the copy engine's
+//                  and the load/store units', which together outrun either alone;
 //      warp 15     one thread issues the MMAs: QK of chunk g+1 before PV of chunk g, so the
 //                  tensor core computes the next scores while the softmax runs.
 //    Hand-offs are mbarriers (cp.async arrivals, tcgen05.commit, thread arrivals).
@@ -337,11 +340,12 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
 
 // ----------------------------------------------------------------------------- attention
 
-constexpr int kTcSoftmaxThreads = 128, kTcProducerThreads = 352;
-constexpr int kTcMmaWarp = (kTcSoftmaxThreads + kTcProducerThreads) / 32;
-constexpr int kTcThreads = kTcSoftmaxThreads + kTcProducerThreads + 32;
+constexpr int kTcSoftmaxThreads = 128;
+constexpr int kTcKWarps = 6, kTcVWarps = 5;  // producer warps for K (and Q, records) and for V
+constexpr int kTcProducerWarps = kTcKWarps + kTcVWarps;
+constexpr int kTcMmaWarp = 4 + kTcProducerWarps;
+constexpr int kTcThreads = kTcSoftmaxThreads + kTcProducerWarps * 32 + 32;
 constexpr int kTcRing = 4;                   // chunk records in flight
-constexpr int kBarProducer = 1;              // named barrier of the producer warps
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kTcQ = 0;                              // 128 x 256 bf16, K-major    64 KiB
@@ -364,22 +368,6 @@ struct TcArgs {
     float scale_log2;
     WsHeader *hdr;
 };
-
-__device__ __forceinline__ void producer_sync() {
-    asm volatile("bar.sync %0, %1;" ::"n"(kBarProducer), "n"(kTcProducerThreads) : "memory");
-}
-
-// Barrier of the producer warps that also ORs a flag over them.
-__device__ __forceinline__ bool producer_sync_or(bool flag) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)flag), "n"(kBarProducer), "n"(kTcProducerThreads)
-        : "memory");
-    return r != 0;
-}
 
 // registers per thread: each of the 4 schedulers holds 16K registers for its share of the
 // CTA's warps (one CTA per SM)
@@ -404,17 +392,17 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
     if (warp == kTcMmaWarp) tmem_alloc(&tmem_s, 512);
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&k_full[s]), 2 * kTcProducerThreads);   // cp.async + thread arrivals
-            mbar_init(smem_u32(&v_full[s]), kTcProducerThreads);       // cp.async arrivals
+            mbar_init(smem_u32(&k_full[s]), kTcKWarps * 32);           // cp.async arrivals
+            mbar_init(smem_u32(&v_full[s]), kTcVWarps * 32);
             mbar_init(smem_u32(&k_empty[s]), 1);
             mbar_init(smem_u32(&v_empty[s]), 1);
             mbar_init(smem_u32(&s_full[s]), 1);
         }
         for (int s = 0; s < kTcRing; ++s) {
             mbar_init(smem_u32(&r_full[s]), 1);                        // bulk copy of the record
-            mbar_init(smem_u32(&r_empty[s]), kTcSoftmaxThreads);
+            mbar_init(smem_u32(&r_empty[s]), kTcSoftmaxThreads + kTcProducerWarps);   // readers
         }
-        mbar_init(smem_u32(&q_full), 2 * kTcProducerThreads);
+        mbar_init(smem_u32(&q_full), 2 * kTcKWarps * 32);          // cp.async + thread arrivals
         mbar_init(smem_u32(&q_free), 1);
         mbar_init(smem_u32(&p_full), kTcSoftmaxThreads);
         mbar_init(smem_u32(&pv_done), 1);
@@ -432,6 +420,16 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
     const int n_rounds = (n_tiles + (int)gridDim.x - 1) / (int)gridDim.x;
     auto tile_at = [&](int r) -> int { return r < n_rounds ? a.order[(size_t)r * gridDim.x + blockIdx.x] : -1; };
     auto size_at = [&](int t) -> int { return t >= 0 ? a.n_chunks[t / a.Hkv] : 0; };
+    // to the next chunk of a stream (round r, tile t, chunk c of n), skipping tiles without chunks
+    auto advance = [&](int &r, int &t, int &c, int &n) {
+        ++c;
+        while (r < n_rounds && c >= n) {
+            ++r;
+            t = tile_at(r);
+            c = 0;
+            n = size_at(t);
+        }
+    };
 
     auto wait = [&](uint64_t *bar, uint32_t phase) -> bool {
         if (mbar_wait_bounded(smem_u32(bar), phase & 1u, kWaitLimitNs)) return true;
@@ -440,87 +438,61 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         return false;
     };
 
+    // a warp's wait: every lane polls; the warp goes on only if all saw the phase and no role
+    // has given up
+    auto wait_warp = [&](uint64_t *bar, uint32_t phase) -> bool {
+        const bool w = wait(bar, phase);
+        return __all_sync(0xffffffffu, w) && !__any_sync(0xffffffffu, s_abort != 0);
+    };
+
     if (warp >= 4 && warp < kTcMmaWarp) {
-        // ================================================================ producer
-        const int pt = tid - kTcSoftmaxThreads;
+        // ================================================================ producers (cp.async)
+        // K warps: records (bulk copies, two ahead), Q tiles, K rows; V warps: V rows. Each
+        // warp follows the mbarriers on its own, so a slow warp holds back no other.
+        const bool is_k = warp < 4 + kTcKWarps;
+        const int nthr = is_k ? kTcKWarps * 32 : kTcVWarps * 32;
+        const int pt = tid - kTcSoftmaxThreads - (is_k ? 0 : kTcKWarps * 32);
+        const bool leader = is_k && pt == 0;
         const int64_t last_tok = (int64_t)a.p0 + a.Nc - 1;
-        bool ok = true;
+        const uint16_t *cache = is_k ? a.k_cache : a.v_cache;
+        const uint32_t stage0 = sbase + (is_k ? kTcK : kTcV);
+        uint64_t *full = is_k ? k_full : v_full;
+        uint64_t *empty = is_k ? k_empty : v_empty;
         // the CTA's chunk stream: its tile list in order, chunk by chunk; tiles without chunks
         // (invalid lists) are skipped
         int ri = 0, c_in = 0, tile = tile_at(0), n_ch = size_at(tile);
-        auto advance = [&](int &r, int &t, int &c, int &n) {    // to the next chunk of the stream
-            ++c;
-            while (r < n_rounds && c >= n) {
-                ++r;
-                t = tile_at(r);
-                c = 0;
-                n = size_at(t);
-            }
-        };
         if (n_rounds > 0 && n_ch == 0) {
             c_in = -1;
             advance(ri, tile, c_in, n_ch);
         }
-        // chunk records arrive through the bulk-copy engine, one chunk ahead of the gathers
         int pf_ri = ri, pf_tile = tile, pf_c = c_in, pf_n = n_ch, pf_g = 0;
-        auto prefetch = [&]() -> bool {         // record of chunk pf_g into ring slot pf_g % ring
+        auto prefetch = [&]() -> bool {         // leader: record of chunk pf_g into ring slot pf_g % ring
             if (pf_ri >= n_rounds) return true;
             const int rs = pf_g % kTcRing;
-            bool w_ok = true;
-            if (pt == 0) {
-                if (pf_g >= kTcRing) w_ok = wait(&r_empty[rs], pf_g / kTcRing - 1);
-                if (w_ok) {
-                    const ChunkRec *src = a.recs + (size_t)(pf_tile / a.Hkv) * kPlanCap + pf_c;
-                    mbar_arrive_expect_tx(smem_u32(&r_full[rs]), kRecCopyBytes);
-                    bulk_g2s(sbase + kTcRecs + rs * (uint32_t)sizeof(ChunkRec), src, kRecCopyBytes,
-                             smem_u32(&r_full[rs]));
-                }
-            }
+            if (pf_g >= kTcRing && !wait(&r_empty[rs], pf_g / kTcRing - 1)) return false;
+            const ChunkRec *src = a.recs + (size_t)(pf_tile / a.Hkv) * kPlanCap + pf_c;
+            mbar_arrive_expect_tx(smem_u32(&r_full[rs]), kRecCopyBytes);
+            bulk_g2s(sbase + kTcRecs + rs * (uint32_t)sizeof(ChunkRec), src, kRecCopyBytes, smem_u32(&r_full[rs]));
             ++pf_g;
             advance(pf_ri, pf_tile, pf_c, pf_n);
-            return !producer_sync_or(!w_ok || s_abort);
+            return true;
         };
-        int g = 0, t_loc = -1, pending = -1, pending_gkv = 0;
-        // V rows of chunk `pending` (token ids from its record, still in the ring)
-        auto flush_v = [&]() {
-            if (pending < 0 || !ok) return;
-            const int s = pending & 1;
-            bool w_ok = true;
-            if (pt == 0 && pending >= 2) w_ok = wait(&v_empty[s], (pending >> 1) - 1);
-            if (producer_sync_or(!w_ok || s_abort)) {
-                ok = false;
-                return;
-            }
-            const ChunkRec &r = ring[pending % kTcRing];
-            for (int gi = pt; gi < kTcChunk * 32; gi += kTcProducerThreads) {
-                const int j = gi >> 5, gg = gi & 31;
-                int b = r.blk[j >> 2];
-                if (b < 0) b = r.blk[0];
-                const int64_t tok = min((int64_t)b * kRatio + (j & 3), last_tok);
-                cp_async16(sbase + kTcV + s * 32768 + (gg >> 3) * (kTcChunk * 128) + swz(j, gg & 7),
-                           a.v_cache + (tok * a.Hkv + pending_gkv) * kHeadDim + gg * 8);
-            }
-            cp_async_arrive(smem_u32(&v_full[s]));
-            pending = -1;
-        };
-        ok = prefetch();
-        int cur_tile = -1;
+        bool ok = true;
+        if (leader) ok = prefetch() && prefetch();
+        ok = __all_sync(0xffffffffu, ok);
+        int g = 0, t_loc = -1, cur_tile = -1;
         while (ok && ri < n_rounds) {
             const int gkv = tile % a.Hkv;
-            if (tile != cur_tile) {
+            if (is_k && tile != cur_tile) {
                 // ---- a new tile: its Q rows once the previous tile's QK MMAs are done
-                flush_v();
-                if (!ok) break;
                 cur_tile = tile;
                 ++t_loc;
-                const int i0 = (tile / a.Hkv) * QT, nq = min(QT, a.Nc - i0);
-                bool w_ok = true;
-                if (pt == 0 && t_loc > 0) w_ok = wait(&q_free, t_loc - 1);
-                if (producer_sync_or(!w_ok || s_abort)) {
+                if (t_loc > 0 && !wait_warp(&q_free, t_loc - 1)) {
                     ok = false;
                     break;
                 }
-                for (int gi = pt; gi < kTcRows * 32; gi += kTcProducerThreads) {
+                const int i0 = (tile / a.Hkv) * QT, nq = min(QT, a.Nc - i0);
+                for (int gi = pt; gi < kTcRows * 32; gi += nthr) {
                     const int r = gi >> 5, gg = gi & 31;
                     const int qq = r / G, hh = r % G;
                     const uint32_t dst = sbase + kTcQ + (gg >> 3) * (kTcRows * 128) + swz(r, gg & 7);
@@ -533,39 +505,34 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&q_full));
             }
-            // ---- prefetch the next record; wait for this chunk's record and K stage
-            if (!prefetch()) {
-                ok = false;
-                break;
-            }
+            if (leader && !prefetch()) ok = false;
             const int s = g & 1, rs = g % kTcRing;
-            bool w2 = true;
-            if (pt == 0) w2 = wait(&r_full[rs], g / kTcRing) && (g < 2 || wait(&k_empty[s], (g >> 1) - 1));
-            if (producer_sync_or(!w2 || s_abort)) {
+            if (!__all_sync(0xffffffffu, ok) || !wait_warp(&r_full[rs], g / kTcRing) ||
+                (g >= 2 && !wait_warp(&empty[s], (g >> 1) - 1))) {
                 ok = false;
                 break;
             }
             const ChunkRec &r = ring[rs];
-            for (int gi = pt; gi < kTcChunk * 32; gi += kTcProducerThreads) {
+            for (int gi = pt; gi < kTcChunk * 32; gi += nthr) {
                 const int j = gi >> 5, gg = gi & 31;
                 int b = r.blk[j >> 2];
                 if (b < 0) b = r.blk[0];               // padding column: any valid token (masked)
                 // the newest block may extend past the last token; its tail is masked
                 const int64_t tok = min((int64_t)b * kRatio + (j & 3), last_tok);
-                cp_async16(sbase + kTcK + s * 32768 + (gg >> 3) * (kTcChunk * 128) + swz(j, gg & 7),
-                           a.k_cache + (tok * a.Hkv + gkv) * kHeadDim + gg * 8);
+                cp_async16(stage0 + s * 32768 + (gg >> 3) * (kTcChunk * 128) + swz(j, gg & 7),
+                           cache + (tok * a.Hkv + gkv) * kHeadDim + gg * 8);
             }
-            cp_async_arrive(smem_u32(&k_full[s]));
-            mbar_arrive(smem_u32(&k_full[s]));
-            flush_v();                                 // V of the previous chunk, one behind K
-            if (!ok) break;
-            pending = g;
-            pending_gkv = gkv;
+            cp_async_arrive(smem_u32(&full[s]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&r_empty[rs]));   // this warp is done with the record
             ++g;
             advance(ri, tile, c_in, n_ch);
         }
-        flush_v();
         asm volatile("cp.async.wait_all;" ::: "memory");
+        // no record copy may still be writing shared memory when the CTA exits (bounded waits)
+        if (leader)
+            for (int j = max(g, pf_g - 2); j < pf_g; ++j)
+                mbar_wait_bounded(smem_u32(&r_full[j % kTcRing]), (uint32_t)(j / kTcRing) & 1u, kWaitLimitNs);
     } else if (warp == kTcMmaWarp) {
         // ================================================================ MMA issue
         if (lane == 0) {
@@ -653,10 +620,6 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         const uint32_t t_o = t_row + 256;
         int g = 0;
         bool ok = true;
-        auto wait_warp = [&](uint64_t *bar, uint32_t phase) -> bool {
-            const bool w = wait(bar, phase);
-            return __all_sync(0xffffffffu, w) && !__any_sync(0xffffffffu, s_abort != 0);
-        };
         for (int r = 0; r < n_rounds && ok; ++r) {
             const int tile = tile_at(r);
             const int n_ch = size_at(tile);
