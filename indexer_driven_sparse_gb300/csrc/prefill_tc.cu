@@ -351,8 +351,9 @@ constexpr int kTcRing = 4;                   // chunk records in flight
 constexpr uint32_t kTcQ = 0;                              // 128 x 256 bf16, K-major    64 KiB
 constexpr uint32_t kTcK = 65536;                           // 2 x (64 x 256) K-major     2 x 32 KiB
 constexpr uint32_t kTcV = kTcK + 2 * 32768;                // 2 x (64 x 256) MN-major    2 x 32 KiB
-constexpr uint32_t kTcP = kTcV + 2 * 32768;                // 128 x 64 bf16, K-major     16 KiB
-constexpr uint32_t kTcRecs = kTcP + 16384;                 // ChunkRec [ring]
+constexpr uint32_t kTcRecs = kTcV + 2 * 32768;             // ChunkRec [ring]
+// tensor memory columns: S (2 x 64 fp32), P (2 x 64 bf16 = 2 x 32), O (256 fp32)
+constexpr uint32_t kTcTmemS = 0, kTcTmemP = 128, kTcTmemO = 256;
 constexpr uint32_t kTcSmem = kTcRecs + sizeof(ChunkRec) * kTcRing + 1024;   // + alignment slack
 
 struct TcArgs {
@@ -384,7 +385,8 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
 
     __shared__ uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2];
     __shared__ uint64_t r_full[kTcRing], r_empty[kTcRing];
-    __shared__ uint64_t q_full, q_free, p_full, pv_done, o_free;
+    __shared__ uint64_t p_full[2], pv_done[2];
+    __shared__ uint64_t q_full, q_free, o_free;
     __shared__ uint32_t tmem_s;
     __shared__ volatile int s_abort;
 
@@ -404,8 +406,10 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         }
         mbar_init(smem_u32(&q_full), 2 * kTcKWarps * 32);          // cp.async + thread arrivals
         mbar_init(smem_u32(&q_free), 1);
-        mbar_init(smem_u32(&p_full), kTcSoftmaxThreads);
-        mbar_init(smem_u32(&pv_done), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&p_full[s]), kTcSoftmaxThreads);
+            mbar_init(smem_u32(&pv_done[s]), 1);
+        }
         mbar_init(smem_u32(&o_free), kTcSoftmaxThreads);
         fence_mbar_init();
         s_abort = 0;
@@ -570,7 +574,7 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                 for (int ks = 0; ks < kHeadDim / 16; ++ks) {
                     const uint64_t ad = tc_desc(qa + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
                     const uint64_t bd = tc_desc(kb + (ks >> 2) * (kTcChunk * 128) + (ks & 3) * 32, 16, 1024);
-                    tc_mma(tmem + s * kTcChunk, ad, bd, tc_idesc(kTcRows, kTcChunk, 0), ks > 0);
+                    tc_mma(tmem + kTcTmemS + s * kTcChunk, ad, bd, tc_idesc(kTcRows, kTcChunk, 0), ks > 0);
                 }
                 tc_commit(smem_u32(&s_full[s]));
                 tc_commit(smem_u32(&k_empty[s]));
@@ -586,24 +590,24 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                 if (more && !issue_qk(g + 1, f1, l1)) break;
                 // ---- O (+)= P V for chunk g
                 const int s = g & 1;
-                if (!wait(&p_full, g) || !wait(&v_full[s], g >> 1)) break;
+                if (!wait(&p_full[s], g >> 1) || !wait(&v_full[s], g >> 1)) break;
                 if (first) {
                     ++n_tile;
                     if (n_tile > 0 && !wait(&o_free, n_tile - 1)) break;   // the previous tile's O was read
                 }
                 fence_proxy_async_smem();
                 tc_fence_after();
-                const uint32_t pa = sbase + kTcP, vb = sbase + kTcV + s * 32768;
+                // P from tensor memory (its 16-token k-steps are 8 columns apart), V from shared memory
+                const uint32_t pa = tmem + kTcTmemP + s * (kTcChunk / 2), vb = sbase + kTcV + s * 32768;
 #pragma unroll
                 for (int ks = 0; ks < kTcChunk / 16; ++ks) {
-                    const uint64_t ad = tc_desc(pa + ks * 32, 16, 1024);
                     const uint64_t bd = tc_desc(vb + ks * 2048, kTcChunk * 128, 1024);
-                    tc_mma(tmem + 256, ad, bd, tc_idesc(kTcRows, kHeadDim, 1), !first || ks > 0);
+                    tc_mma_ta(tmem + kTcTmemO, pa + ks * 8, bd, tc_idesc(kTcRows, kHeadDim, 1), !first || ks > 0);
                 }
                 tc_commit(smem_u32(&v_empty[s]));
-                tc_commit(smem_u32(&pv_done));
-                last_bar = &pv_done;
-                last_phase = (uint32_t)g;
+                tc_commit(smem_u32(&pv_done[s]));
+                last_bar = &pv_done[s];
+                last_phase = (uint32_t)(g >> 1);
                 if (!more) break;
                 ++g;
                 first = f1;
@@ -617,7 +621,7 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         const int row = tid;                     // MMA row = TMEM lane
         const int q_loc = row / G, h_loc = row % G;
         const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
-        const uint32_t t_o = t_row + 256;
+        const uint32_t t_o = t_row + kTcTmemO;
         int g = 0;
         bool ok = true;
         for (int r = 0; r < n_rounds && ok; ++r) {
@@ -681,14 +685,16 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                     }
                 }
                 l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-                // P (shared memory) and O are free once the previous PV is done
-                if (g > 0 && !wait_warp(&pv_done, g - 1)) {
+                // P's buffer is free once the PV two chunks back is done; a rescale of O waits for
+                // the previous PV (TMEM loads and stores are warp-collective: the warp rescales together)
+                const bool rescale = o_init && __any_sync(0xffffffffu, f != 1.f);
+                if ((g >= 2 && !wait_warp(&pv_done[s], (g >> 1) - 1)) ||
+                    (rescale && !wait_warp(&pv_done[s ^ 1], (g - 1) >> 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // TMEM loads and stores are warp-collective: the warp rescales together
-                if (o_init && __any_sync(0xffffffffu, f != 1.f)) {
+                if (rescale) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
                         float ov[32];
@@ -698,22 +704,15 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                         tmem_st32(t_o + c0, ov);
                     }
                 }
-#pragma unroll
-                for (int gg = 0; gg < 8; ++gg) {
-                    const uint32_t dst = sbase + kTcP + swz(row, gg);
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[gg * 4]),
-                                 "r"(pk[gg * 4 + 1]), "r"(pk[gg * 4 + 2]), "r"(pk[gg * 4 + 3])
-                                 : "memory");
-                }
-                fence_proxy_async_smem();
+                tmem_st32(t_row + kTcTmemP + s * (kTcChunk / 2), pk);
                 tc_fence_before();
-                mbar_arrive(smem_u32(&p_full));
+                mbar_arrive(smem_u32(&p_full[s]));
                 o_init = true;
                 ++g;
             }
             if (!ok) break;
             // ---- finish the tile: O / l -> bf16, lse; then O may be overwritten
-            if (!wait_warp(&pv_done, g - 1)) {
+            if (!wait_warp(&pv_done[(g - 1) & 1], (g - 1) >> 1)) {
                 ok = false;
                 break;
             }
