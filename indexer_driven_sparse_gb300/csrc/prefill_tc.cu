@@ -349,12 +349,14 @@ constexpr int kTcRing = 4;                   // chunk records in flight
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kTcQ = 0;                              // 128 x 256 bf16, K-major    64 KiB
-constexpr uint32_t kTcK = 65536;                           // 2 x (64 x 256) K-major     2 x 32 KiB
-constexpr uint32_t kTcV = kTcK + 2 * 32768;                // 2 x (64 x 256) MN-major    2 x 32 KiB
-constexpr uint32_t kTcRecs = kTcV + 2 * 32768;             // ChunkRec [ring]
+constexpr int kTcKStages = 2, kTcVStages = 2;
+constexpr uint32_t kTcK = 65536;                           // stages of 64 x 256, K-major    32 KiB each
+constexpr uint32_t kTcV = kTcK + kTcKStages * 32768;       // stages of 64 x 256, MN-major   32 KiB each
+constexpr uint32_t kTcRecs = kTcV + kTcVStages * 32768;    // ChunkRec [ring]
 // tensor memory columns: S (2 x 64 fp32), P (2 x 64 bf16 = 2 x 32), O (256 fp32)
 constexpr uint32_t kTcTmemS = 0, kTcTmemP = 128, kTcTmemO = 256;
 constexpr uint32_t kTcSmem = kTcRecs + sizeof(ChunkRec) * kTcRing + 1024;   // + alignment slack
+static_assert(kTcSmem + 1024 <= 227 * 1024, "shared memory per CTA (dynamic + static)");
 
 struct TcArgs {
     const uint16_t *q;        // [Nc, Hq, 256]
@@ -383,7 +385,7 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
     const uint32_t sbase = smem_u32(sm);
     ChunkRec *ring = reinterpret_cast<ChunkRec *>(sm + kTcRecs);
 
-    __shared__ uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2];
+    __shared__ uint64_t k_full[kTcKStages], k_empty[kTcKStages], v_full[kTcVStages], v_empty[kTcVStages], s_full[2];
     __shared__ uint64_t r_full[kTcRing], r_empty[kTcRing];
     __shared__ uint64_t p_full[2], pv_done[2];
     __shared__ uint64_t q_full, q_free, o_free;
@@ -394,11 +396,15 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
     if (warp == kTcMmaWarp) tmem_alloc(&tmem_s, 512);
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&k_full[s]), kTcKWarps * 32);           // cp.async arrivals
-            mbar_init(smem_u32(&v_full[s]), kTcVWarps * 32);
-            mbar_init(smem_u32(&k_empty[s]), 1);
-            mbar_init(smem_u32(&v_empty[s]), 1);
             mbar_init(smem_u32(&s_full[s]), 1);
+        }
+        for (int s = 0; s < kTcKStages; ++s) {
+            mbar_init(smem_u32(&k_full[s]), kTcKWarps * 32);           // cp.async arrivals
+            mbar_init(smem_u32(&k_empty[s]), 1);
+        }
+        for (int s = 0; s < kTcVStages; ++s) {
+            mbar_init(smem_u32(&v_full[s]), kTcVWarps * 32);
+            mbar_init(smem_u32(&v_empty[s]), 1);
         }
         for (int s = 0; s < kTcRing; ++s) {
             mbar_init(smem_u32(&r_full[s]), 1);                        // bulk copy of the record
@@ -462,6 +468,7 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         const uint32_t stage0 = sbase + (is_k ? kTcK : kTcV);
         uint64_t *full = is_k ? k_full : v_full;
         uint64_t *empty = is_k ? k_empty : v_empty;
+        const int n_stages = is_k ? kTcKStages : kTcVStages;
         // the CTA's chunk stream: its tile list in order, chunk by chunk; tiles without chunks
         // (invalid lists) are skipped
         int ri = 0, c_in = 0, tile = tile_at(0), n_ch = size_at(tile);
@@ -510,9 +517,9 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                 mbar_arrive(smem_u32(&q_full));
             }
             if (leader && !prefetch()) ok = false;
-            const int s = g & 1, rs = g % kTcRing;
+            const int s = g % n_stages, rs = g % kTcRing;
             if (!__all_sync(0xffffffffu, ok) || !wait_warp(&r_full[rs], g / kTcRing) ||
-                (g >= 2 && !wait_warp(&empty[s], (g >> 1) - 1))) {
+                (g >= n_stages && !wait_warp(&empty[s], g / n_stages - 1))) {
                 ok = false;
                 break;
             }
@@ -561,15 +568,15 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
             int first = 0, last = 0;
             bool ok = next_chunk(first, last);
             auto issue_qk = [&](int gq, int f, int l) -> bool {
-                const int s = gq & 1;
-                if (!wait(&k_full[s], gq >> 1)) return false;
+                const int s = gq & 1, sk = gq % kTcKStages;   // S buffer, K stage
+                if (!wait(&k_full[sk], gq / kTcKStages)) return false;
                 if (f) {
                     if (!wait(&q_full, n_q)) return false;
                     ++n_q;
                 }
                 fence_proxy_async_smem();
                 tc_fence_after();
-                const uint32_t qa = sbase + kTcQ, kb = sbase + kTcK + s * 32768;
+                const uint32_t qa = sbase + kTcQ, kb = sbase + kTcK + sk * 32768;
 #pragma unroll
                 for (int ks = 0; ks < kHeadDim / 16; ++ks) {
                     const uint64_t ad = tc_desc(qa + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
@@ -577,9 +584,9 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                     tc_mma(tmem + kTcTmemS + s * kTcChunk, ad, bd, tc_idesc(kTcRows, kTcChunk, 0), ks > 0);
                 }
                 tc_commit(smem_u32(&s_full[s]));
-                tc_commit(smem_u32(&k_empty[s]));
-                last_bar = &k_empty[s];
-                last_phase = (uint32_t)(gq >> 1);
+                tc_commit(smem_u32(&k_empty[sk]));
+                last_bar = &k_empty[sk];
+                last_phase = (uint32_t)(gq / kTcKStages);
                 if (l) tc_commit(smem_u32(&q_free));
                 return true;
             };
@@ -589,8 +596,8 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                 const bool more = next_chunk(f1, l1);
                 if (more && !issue_qk(g + 1, f1, l1)) break;
                 // ---- O (+)= P V for chunk g
-                const int s = g & 1;
-                if (!wait(&p_full[s], g >> 1) || !wait(&v_full[s], g >> 1)) break;
+                const int s = g & 1, sv = g % kTcVStages;     // P buffer, V stage
+                if (!wait(&p_full[s], g >> 1) || !wait(&v_full[sv], g / kTcVStages)) break;
                 if (first) {
                     ++n_tile;
                     if (n_tile > 0 && !wait(&o_free, n_tile - 1)) break;   // the previous tile's O was read
@@ -598,13 +605,13 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
                 fence_proxy_async_smem();
                 tc_fence_after();
                 // P from tensor memory (its 16-token k-steps are 8 columns apart), V from shared memory
-                const uint32_t pa = tmem + kTcTmemP + s * (kTcChunk / 2), vb = sbase + kTcV + s * 32768;
+                const uint32_t pa = tmem + kTcTmemP + s * (kTcChunk / 2), vb = sbase + kTcV + sv * 32768;
 #pragma unroll
                 for (int ks = 0; ks < kTcChunk / 16; ++ks) {
                     const uint64_t bd = tc_desc(vb + ks * 2048, kTcChunk * 128, 1024);
                     tc_mma_ta(tmem + kTcTmemO, pa + ks * 8, bd, tc_idesc(kTcRows, kHeadDim, 1), !first || ks > 0);
                 }
-                tc_commit(smem_u32(&v_empty[s]));
+                tc_commit(smem_u32(&v_empty[sv]));
                 tc_commit(smem_u32(&pv_done[s]));
                 last_bar = &pv_done[s];
                 last_phase = (uint32_t)(g >> 1);
