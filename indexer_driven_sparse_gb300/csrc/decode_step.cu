@@ -651,6 +651,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hq = a.n_q_heads, Hkv = a.n_kv_heads;
+    // launched as a programmatic dependent of the previous step: its CTAs may be resident
+    // before that step has finished; nothing in global memory is touched before it has
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- metadata in one round trip (partition in warp 0, offsets in warps 1-2)
     if (warp == 0) {
@@ -1280,6 +1283,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     ++bar_k;
     __syncthreads();
     STEP_TRACE(8);
+    // the next launch on the stream may be scheduled now (it waits for this one to finish)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int n_out = Hq * kHeadDim;
     const int o_lo = n_out * jj / cr, o_hi = n_out * (jj + 1) / cr;
     const int h_lo = o_lo / kHeadDim, h_hi = o_hi > o_lo ? (o_hi - 1) / kHeadDim : h_lo - 1;
@@ -1387,11 +1392,13 @@ cudaError_t launch_step_g(const StepArgs &a, int ctas, cudaStream_t st) {
     cfg.blockDim = dim3(kStepThreads);
     cfg.dynamicSmemBytes = kStepSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, decode_step_kernel<G>, a);
 }
 }  // namespace
