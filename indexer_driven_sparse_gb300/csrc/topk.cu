@@ -2,8 +2,12 @@
 // ties to the lower block id, written in ascending id order ("3090x3で 314 万コンテキスト",
 // section "なぜ"; tie rule as in "125B MoE を 3090 3 枚で運用する vLLM 最適化編" section 3.3).
 //
-// One CTA per row, three streaming passes over the row (the first from HBM, the others
-// mostly from L2):
+// One CTA per row. Long rows (at least 16,384 blocks) first try one streaming pass: a
+// sample of every 64th score sets value-linear bins and a cut keeping about 3 x 512 of the
+// row; the pass gathers every score at or above the cut as an exact 64-bit key, and the
+// top 512 of those are resolved by bins and a rank among the boundary bin's members. When
+// fewer than 512 clear the cut (or too many), or for shorter rows, three streaming passes
+// over the row (the first from HBM, the others mostly from L2):
 //   1. the row's finite max and min;
 //   2. a histogram over 4096 bins that are linear in the score value (monotone in the
 //      score, so bins above the one holding the k-th best are wholly selected). Linear
