@@ -260,8 +260,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float 
 
     // ---- one pass when a sample places the cut: every 64th score sets value-linear bins
     // and a bin cut keeping about 3 x 512 of the row; one streaming pass gathers every score
-    // in bins at or above the cut as exact 64-bit keys. Bins are monotone, so when at least
-    // 512 scores clear the cut the row's top 512 are among them. Otherwise (or if they
+    // at or above a floor one bin below the cut as exact 64-bit keys. When at least 512
+    // scores clear the floor the row's top 512 are among them. Otherwise (or if they
     // overflow the candidate buffer) the passes below decide.
     constexpr int kSampleStride = 64;
     const int64_t n_s = nb / kSampleStride;
@@ -306,8 +306,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float 
             find_bin_from_top(hist, (uint32_t)(want < n_s ? want : n_s), &s_b, &s_above, wtot);
             const int cut = s_b;
             __syncthreads();                    // the candidates overwrite the histogram
-            // a cheap floor one bin below the cut filters most scores; the exact bin test and the
-            // warp-aggregated append run only where some lane of the warp has a candidate
+            // the candidates are every score at or above a floor one bin below the cut: a
+            // threshold set, so when it holds at least 512 scores the row's top 512 are in it
+            // (NaN fails the test and ranks below every number anyway)
             const float vlow = smin + (float)(cut - 1) / sscale;
             auto append = [&](int64_t i, float v, bool m) {
                 const unsigned bal = __ballot_sync(0xffffffffu, m);
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float 
                         cand[slot] = ((uint64_t)score_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
                 }
             };
-            auto is_cand = [&](float v) { return !(v < vlow) && lin_bin(v, smin, sscale) >= cut; };
+            auto is_cand = [&](float v) { return v >= vlow; };
             const int64_t mis = (int64_t)(((16 - ((uintptr_t)s & 15)) & 15) >> 2);
             const int64_t head = mis < nb ? mis : nb;
             if (head > 0) {
