@@ -357,21 +357,15 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float 
                 uint32_t base = 0;
                 if (lane == 31 && incl) base = atomicAdd(&s_ncand, incl);
                 base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
-                if (mk) {
-#pragma unroll
-                    for (int u = 0; u < kScanBatch; ++u) {
-                        const int64_t i = head + 4 * (j0 + u * kTopkThreads + tid);
-                        const float vv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if ((mk >> (4 * u + e)) & 1u) {
-                                if (base < (uint32_t)kCandCap)
-                                    cand[base] = ((uint64_t)score_key(vv[e]) << 32) |
-                                                 (uint64_t)(0xFFFFFFFFu - (uint32_t)(i + e));
-                                ++base;
-                            }
-                        }
-                    }
+                // only the set bits: the score is read again (an L1 hit) rather than picked out of
+                // the batch's registers by a runtime index
+                while (mk) {
+                    const int bit = __ffs(mk) - 1;
+                    mk &= mk - 1u;
+                    const int64_t i = head + 4 * (j0 + (bit >> 2) * kTopkThreads + tid) + (bit & 3);
+                    if (base < (uint32_t)kCandCap)
+                        cand[base] = ((uint64_t)score_key(__ldg(s + i)) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+                    ++base;
                 }
             }
             const int64_t t0 = head + 4 * nvec;
