@@ -30,7 +30,7 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kLinBins = 4096;
 constexpr int kCandCap = 4096;
 constexpr int kCandBins = 1024;                 // bins over the sampled path's candidates
-constexpr int kScanBatch = 8;                   // 16-byte loads a thread keeps in flight per sweep
+constexpr int kScanBatch = 4;                   // 16-byte loads a thread keeps in flight per sweep
 static_assert(kCandCap * 2 >= kLinBins, "the histogram lives in the candidate buffer");
 
 // Calls f(i, v, valid) over the row with every thread taking the same number of calls
@@ -223,7 +223,7 @@ __device__ void radix_select_row(const float *__restrict__ s, int64_t nb, int32_
     *written_out = written;
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const float *__restrict__ scores, int64_t ld,
+__global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float *__restrict__ scores, int64_t ld,
                                                                     const int32_t *q_pos, int32_t *__restrict__ blocks,
                                                                     int32_t *__restrict__ count, WsHeader *hdr) {
     __shared__ uint64_t cand[kCandCap];        // the histogram shares this space (used before the candidates)
