@@ -31,8 +31,11 @@ constexpr uint32_t kStABytes = kStM * kIdxDim * 2;          // 32 KiB: two 64-co
 constexpr uint32_t kStBBytes = kStN * kIdxDim * 2;          // 64 KiB
 constexpr uint32_t kStStage = kStABytes + kStBBytes;
 constexpr int kStXStride = 36;                              // floats per transposed row (16-byte aligned)
-constexpr uint32_t kStXpose = 2 * kStStage;                 // per epilogue warp: 32 x 36 floats
-constexpr uint32_t kStSmem = kStXpose + 4 * 32 * kStXStride * 4 + 1024;
+constexpr uint32_t kStXpose = 2 * kStStage;                 // per epilogue warp: two 32 x 32-float boxes
+constexpr uint32_t kStWarpBuf = 2 * 32 * 32 * 4;            // (or one 32 x 36-float transpose)
+static_assert(32 * kStXStride * 4 <= kStWarpBuf, "transpose fits the warp's boxes");
+constexpr uint32_t kStSmem = kStXpose + 4 * kStWarpBuf + 1024;
+static_assert(kStSmem + 1024 <= 227 * 1024, "shared memory per CTA (dynamic + static)");
 
 struct ScoreTcArgs {
     const int32_t *q_pos;
@@ -43,12 +46,13 @@ struct ScoreTcArgs {
     int64_t ld;
     int32_t n_m, n_n;
     int32_t vec;              // rows 16-byte aligned (scores aligned, ld % 4 == 0): 16-byte stores
+    int32_t tma_store;        // whole 32 x 32 slices leave through the tensor map of the scores
     WsHeader *hdr;
 };
 
 __global__ void __launch_bounds__(kStThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_p,
-                    ScoreTcArgs a) {
+                    const __grid_constant__ CUtensorMap tm_s, ScoreTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(sm);
@@ -128,7 +132,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
         }
     } else {
         const int q4 = warp & 3;                      // the TMEM lane quarter this warp may access
-        float *xp = reinterpret_cast<float *>(sm + kStXpose) + (warp - 2) * (32 * kStXStride);
+        float *xp = reinterpret_cast<float *>(sm + kStXpose + (warp - 2) * kStWarpBuf);
+        const uint32_t box0 = sbase + kStXpose + (warp - 2) * kStWarpBuf;   // two 4 KiB boxes
+        int nbox = 0;                                 // boxes stored by this warp so far
         int i = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
             const int acc = i & 1;
@@ -153,6 +159,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
             const int64_t col0 = (int64_t)n * kStN;
             const int row0 = m * kStM + q4 * 32;
             const int nb_max = __reduce_max_sync(0xffffffffu, (unsigned)nb);
+            // rows past the queries are clipped by the tensor map; they do not limit the slices
+            const int nb_min = __reduce_min_sync(0xffffffffu, row < a.Nq ? (unsigned)nb : 0x7fffffffu);
             // store passes: 4 rows x 32 columns per instruction, lane -> (row, 4 columns)
             const int sub_r = lane >> 3, sub_c = (lane & 7) * 4;
 #pragma unroll 1
@@ -160,6 +168,29 @@ __global__ void __launch_bounds__(kStThreads, 1)
                 float v[32];
                 tmem_ld32(tmem + acc * kStN + ((uint32_t)(q4 * 32) << 16) + c * 32, v);
                 if (col0 + c * 32 >= nb_max) continue;   // warp-uniform: nothing of this slice is kept
+                if (a.tma_store && col0 + c * 32 + 32 <= nb_min) {
+                    // the whole slice is kept: a 128B-swizzled 32 x 32 box, stored by the TMA engine
+                    const uint32_t box = box0 + (uint32_t)(nbox & 1) * 4096u;
+                    if (lane == 0 && nbox >= 2) bulk_wait_read<1>();   // this box's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(box + lane * 128 + ((q ^ (lane & 7)) << 4)),
+                                     "f"(v[4 * q]), "f"(v[4 * q + 1]), "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                                     : "memory");
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_s, (int32_t)(col0 + c * 32), row0, box);
+                        bulk_commit_group();
+                    }
+                    ++nbox;
+                    continue;
+                }
+                if (nbox > 0) {                          // the transpose overwrites both boxes
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     *reinterpret_cast<float4 *>(xp + lane * kStXStride + 4 * q) =
@@ -186,6 +217,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));
         }
+        if (lane == 0 && nbox > 0) bulk_wait_all();   // no store may still read shared memory at exit
     }
     tc_fence_before();
     __syncthreads();
@@ -194,9 +226,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
 
 // ----------------------------------------------------------------------------- host side
 
-// 2-D bf16 tensor maps (rows of `inner` elements, `row_bytes` apart), 128B swizzle
-bool encode_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
-                         uint32_t box_inner, uint32_t box_rows) {
+// 2-D tensor maps (rows of `inner` elements, `row_bytes` apart), 128B swizzle
+static bool encode_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                           uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
     using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                        const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                        CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -215,9 +247,19 @@ bool encode_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint6
     const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_rows) {
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, rows, row_bytes, box_inner, box_rows);
+}
+
+bool encode_tmap_f32_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_rows) {
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, inner, rows, row_bytes, box_inner, box_rows);
 }
 
 bool score_tc_supported(int Nq, int64_t n_pooled) {
@@ -241,6 +283,10 @@ cudaError_t launch_score_tc(const uint16_t *q_idx, const int32_t *q_pos, int Nq,
     a.n_m = (Nq + kStM - 1) / kStM;
     a.n_n = (int)((ld + kStN - 1) / kStN);
     a.vec = ((uintptr_t)scores % 16 == 0 && ld % 4 == 0) ? 1 : 0;
+    // the scores as [Nq rows of ld floats] in 32 x 32 boxes (needs 16-byte rows)
+    CUtensorMap ts;
+    memset(&ts, 0, sizeof(ts));
+    a.tma_store = a.vec && encode_tmap_f32_2d(&ts, scores, (uint64_t)ld, (uint64_t)Nq, (uint64_t)ld * 4, 32, 32) ? 1 : 0;
     a.hdr = hdr;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -252,7 +298,7 @@ cudaError_t launch_score_tc(const uint16_t *q_idx, const int32_t *q_pos, int Nq,
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, n_tiles));
     e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStSmem);
     if (e != cudaSuccess) return e;
-    score_tc_kernel<<<grid, kStThreads, kStSmem, st>>>(tq, tp, a);
+    score_tc_kernel<<<grid, kStThreads, kStSmem, st>>>(tq, tp, ts, a);
     return cudaGetLastError();
 }
 
