@@ -242,9 +242,14 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
             if (nbq >= b_lo && nbq - b_lo < span) sel_or(m, nbq - b_lo, 1u << lane);   // own block
         }
         __syncwarp();
+        // marked blocks: 8 masks per 16-byte load (entries past the span are never marked)
         int nu = 0;
-        for (int b0 = 0; b0 < span; b0 += 32) nu += __popc(__ballot_sync(0xffffffffu, b0 + lane < span && m[b0 + lane] != 0));
-        return nu;
+        for (int i = lane; i < (span + 7) / 8; i += 32) {
+            const uint4 w = m4[i];
+            nu += ((w.x & 0xFFFFu) != 0) + ((w.x >> 16) != 0) + ((w.y & 0xFFFFu) != 0) + ((w.y >> 16) != 0) +
+                  ((w.z & 0xFFFFu) != 0) + ((w.z >> 16) != 0) + ((w.w & 0xFFFFu) != 0) + ((w.w >> 16) != 0);
+        }
+        return (int)__reduce_add_sync(0xffffffffu, (unsigned)nu);
     };
 
     // ---- pass 1: chunks per interval
