@@ -75,8 +75,7 @@ constexpr uint32_t kPlLists = 0;                                           // in
 constexpr uint32_t kPlStart = kPlLists + 4 * kTcMaxQt * kBlockTopK;        // uint16 [QT][intervals + 1]
 constexpr uint32_t kPlCounts = kPlStart + 2 * kTcMaxQt * kStartStride;     // int32 [intervals + 1]
 constexpr uint32_t kPlMasks = kPlCounts + 4 * (kTcMaxIntervals + 8);       // uint16 [warp][2048]
-constexpr uint32_t kPlStage = kPlMasks + 2 * kTcMaxBpi * kPlanWarps;       // ChunkRec [warp][3]
-constexpr uint32_t kPlSmem = kPlStage + sizeof(ChunkRec) * 3 * kPlanWarps;
+constexpr uint32_t kPlSmem = kPlMasks + 2 * kTcMaxBpi * kPlanWarps;
 
 static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
@@ -149,11 +148,6 @@ __device__ __forceinline__ void sel_or(uint16_t *sel, int i, uint32_t bits) {
     atomicOr(w, (bits & 0xFFFFu) << ((i & 1) * 16));
 }
 
-__device__ __forceinline__ void stage_clear(ChunkRec *r, int lane) {   // warp: blk = -1, the rest 0
-    int32_t *w = reinterpret_cast<int32_t *>(r);
-    for (int i = lane; i < (int)(sizeof(ChunkRec) / 4); i += 32) w[i] = i < kTcBlocksPerChunk ? -1 : 0;
-}
-
 // One CTA per query tile; warps take intervals v = warp, warp + 8, ... in two passes
 // (chunk counts, then records at the scanned offsets).
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) {
@@ -166,7 +160,6 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint16_t *m = reinterpret_cast<uint16_t *>(psm + kPlMasks) + warp * kTcMaxBpi;
-    ChunkRec *stage = reinterpret_cast<ChunkRec *>(psm + kPlStage) + warp * 3;
     const int qt = blockIdx.x, QT = a.QT;
     const int i0 = qt * QT, nq = min(QT, a.Nc - i0);
     const int nb_last = (a.p0 + i0 + nq - 1) >> 2;
@@ -292,7 +285,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
         }
         return;
     }
-    // ---- pass 2: records, in ascending block order, through a 3-record staging ring per warp
+    // ---- pass 2: records, in ascending block order, written in place
     ChunkRec *out = a.recs + (size_t)qt * kPlanCap;
     for (int v = warp; v < n_iv_tile; v += kPlanWarps) {
         const int b_lo = v * a.bpi;
@@ -300,45 +293,57 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
         const int nu = mark(v);
         const int n_ch = (nu + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
         const int off = counts[v];
-        for (int k = 0; k < 3; ++k) stage_clear(&stage[k], lane);
+        // the interval's records in place: blk = -1, visibility 0, the tile's first / last flags
+        for (int e = lane; e < n_ch * (int)(sizeof(ChunkRec) / 16); e += 32) {
+            const int c = e / (int)(sizeof(ChunkRec) / 16), w = e % (int)(sizeof(ChunkRec) / 16);
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (w < kTcBlocksPerChunk / 4) val = make_uint4(~0u, ~0u, ~0u, ~0u);
+            if (w == (int)(offsetof(ChunkRec, first) / 16))
+                reinterpret_cast<int32_t *>(&val)[(offsetof(ChunkRec, first) % 16) / 4] = off + c == 0;
+            if (w == (int)(offsetof(ChunkRec, last) / 16))
+                reinterpret_cast<int32_t *>(&val)[(offsetof(ChunkRec, last) % 16) / 4] = v == n_iv_tile - 1 && c == n_ch - 1;
+            reinterpret_cast<uint4 *>(out + off + c)[w] = val;
+        }
         __syncwarp();
-        int cur = 0, flushed = 0;
-        auto flush = [&](int c) {              // chunk c of this interval -> global, then clear its slot
-            ChunkRec *r = &stage[c % 3];
-            if (lane == 0) {
-                r->first = off + c == 0;
-                r->last = v == n_iv_tile - 1 && c == n_ch - 1;
+        // the marked blocks in ascending order, 8 masks per lane and 256 per sweep: a warp scan
+        // of the lanes' counts places each block in its chunk and slot
+        const int n4 = (span + 7) / 8;
+        int cur = 0;
+        for (int i0 = 0; i0 < n4; i0 += 32) {
+            const int i4 = i0 + lane;
+            uint32_t mw[8];
+            {
+                const uint4 w = i4 < n4 ? reinterpret_cast<const uint4 *>(m)[i4] : make_uint4(0, 0, 0, 0);
+                mw[0] = w.x & 0xFFFFu; mw[1] = w.x >> 16; mw[2] = w.y & 0xFFFFu; mw[3] = w.y >> 16;
+                mw[4] = w.z & 0xFFFFu; mw[5] = w.z >> 16; mw[6] = w.w & 0xFFFFu; mw[7] = w.w >> 16;
             }
-            __syncwarp();
-            if (lane < (int)(sizeof(ChunkRec) / 16))
-                reinterpret_cast<uint4 *>(out + off + c)[lane] = reinterpret_cast<const uint4 *>(r)[lane];
-            __syncwarp();
-            stage_clear(r, lane);
-            __syncwarp();
-        };
-        for (int b0 = 0; b0 < span; b0 += 32) {
-            const int i = b0 + lane;
-            const uint32_t mk = i < span ? m[i] : 0u;
-            const unsigned bal = __ballot_sync(0xffffffffu, mk != 0);
-            if (bal == 0) continue;
-            if (mk != 0) {
-                const int pos = cur + __popc(bal & ((1u << lane) - 1u));
-                ChunkRec *r = &stage[(pos / kTcBlocksPerChunk) % 3];
-                const int slot = pos % kTcBlocksPerChunk, b = b_lo + i;
+            int cnt = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) cnt += mw[k] != 0;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int pos = cur + incl - cnt;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (mw[k] == 0) continue;
+                ChunkRec *r = out + off + pos / kTcBlocksPerChunk;
+                const int slot = pos % kTcBlocksPerChunk, b = b_lo + 8 * i4 + k;
                 r->blk[slot] = b;
-                for (uint32_t mm = mk; mm != 0; mm &= mm - 1u) {
+                for (uint32_t mm = mw[k]; mm != 0; mm &= mm - 1u) {
                     const int qq = __ffs(mm) - 1;
                     uint32_t bits = 0xFu;
                     const int p = s_p[qq];
                     if ((p >> 2) == b) bits = (1u << ((p & 3) + 1)) - 1u;   // its own block: up to itself
                     atomicOr(&r->vis[qq][slot >> 3], bits << ((slot & 7) * 4));
                 }
+                ++pos;
             }
-            __syncwarp();
-            cur += __popc(bal);
-            while (flushed < cur / kTcBlocksPerChunk) flush(flushed++);
+            cur += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (flushed < n_ch) flush(flushed++);  // the interval's last, partial chunk
     }
     if (tid == 0) a.n_chunks[qt] = total;
 }
