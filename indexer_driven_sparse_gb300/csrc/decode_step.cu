@@ -56,7 +56,7 @@ constexpr size_t kQOff = kHistOff + (size_t)kHistBins * 4;          // query, bf
 constexpr size_t kNewRowOff = kQOff + (size_t)2 * kMaxGroup * kHeadDim * 2;
 constexpr size_t kRawOff = kNewRowOff + 256;                          // 4 raw key rows, bf16
 constexpr size_t kMbarOff = kRawOff + (size_t)kRatio * kIdxDim * 2;
-constexpr size_t kStepSmem = kMbarOff + 64;
+constexpr size_t kStepSmem = kMbarOff + 16 * kRingStages;      // ring full / empty mbarriers
 
 struct StepRowState {
     uint32_t gen;               // barrier generation, advanced once per completed barrier
@@ -665,7 +665,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     } else if (warp == 2) {
         for (int i = lane; i <= a.B; i += 32) s_blk_off[i] = a.blk_off[i];
     } else if (warp == 3 && lane == 0) {
-        for (int s = 0; s < kRingStages; ++s) mbar_init(mbar0 + 8 * s, 1);
+        for (int s = 0; s < kRingStages; ++s) {
+            mbar_init(mbar0 + 8 * s, 1);                              // full: the stage's bytes
+            mbar_init(mbar0 + 8 * (kRingStages + s), kStepWarps);     // empty: every warp read it
+        }
         fence_mbar_init();
     } else if (warp == 4 && lane == 0) {
         s_debug = __ldcg(&a.hdr->debug);
@@ -776,14 +779,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                     atomicAdd(&hist[key >> kHistShift], 1u);
                 }
             }
-            __syncthreads();
+            // the stage is refilled once every warp has read it; no block-wide barrier per chunk
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mbar0 + 8 * (kRingStages + stage));
             if (tid == 0 && c + kRingStages < n_chunks) {
-                const int cn = c + kRingStages;
-                const uint32_t bytes = (uint32_t)min(kChunkRows, n_tma - cn * kChunkRows) * kIdxDim * 2;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(mbar0 + 8 * stage, bytes);
-                bulk_g2s(ring0 + stage * kChunkBytes, gsrc + (int64_t)cn * kChunkRows * kIdxDim, bytes,
-                         mbar0 + 8 * stage);
+                if (!mbar_wait_bounded(mbar0 + 8 * (kRingStages + stage), (c / kRingStages) & 1, kWaitLimitNs)) {
+                    record_error(a.hdr, QSA_ERR_DEVICE_TIMEOUT, kWhereStep, row);   // the others time out too
+                } else {
+                    const int cn = c + kRingStages;
+                    const uint32_t bytes = (uint32_t)min(kChunkRows, n_tma - cn * kChunkRows) * kIdxDim * 2;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(mbar0 + 8 * stage, bytes);
+                    bulk_g2s(ring0 + stage * kChunkBytes, gsrc + (int64_t)cn * kChunkRows * kIdxDim, bytes,
+                             mbar0 + 8 * stage);
+                }
             }
         }
         // ---- 1b. re-pool block nb-1: exact fp64 mean of its four raw keys, one RNE to bf16
