@@ -325,45 +325,70 @@ def instrumented_kernel_times(dl, stream, steps):
 
 def e2e_decode(dl, stream, steps, warmup):
     """Same step with the new token's inputs copied host->device from pinned memory
-    and the last layer's output read back, every step."""
+    and the last layer's output read back, every step. The layers' q and q_idx live in
+    one staging buffer (one copy for all layers); the new token's K, V and raw indexer-key
+    rows are appended to caches stacked with a fixed layer stride (one strided copy each,
+    qsa_copy_rows)."""
     import torch
+    from indexer_driven_sparse_gb300 import binding as qb
     b, layers = dl.b, dl.w.layers
+    n_l = len(layers)
     p = dl.w.ctx_len[0]
     # per layer: q [16,256] + q_idx [128] + new token k,v [2,256] each + raw idx key [128] (bf16)
-    per_layer = 16 * 256 + 128 + 2 * 2 * 256 + 128
-    host_in = torch.empty(len(layers) * per_layer, dtype=torch.bfloat16).pin_memory()
+    qq = 16 * 256 + 128
+    per_layer = qq + 2 * 2 * 256 + 128
+    # restack the caches (same values) and re-home q / q_idx into the staging buffer
+    stacked = {}
+    for name in ("k_cache", "v_cache", "raw_idx_k"):
+        t0 = getattr(layers[0], name)
+        allt = torch.empty((n_l,) + tuple(t0.shape), dtype=t0.dtype, device=t0.device)
+        for l, L in enumerate(layers):
+            allt[l].copy_(getattr(L, name))
+            setattr(L, name, allt[l])
+        stacked[name] = allt
+    dev_q = torch.empty(n_l * qq, dtype=torch.bfloat16, device="cuda")
+    for l, L in enumerate(layers):
+        dev_q[l * qq:l * qq + 4096].copy_(L.q.view(-1))
+        dev_q[l * qq + 4096:(l + 1) * qq].copy_(L.q_idx.view(-1))
+        L.q = dev_q[l * qq:l * qq + 4096].view(L.q.shape)
+        L.q_idx = dev_q[l * qq + 4096:(l + 1) * qq].view(L.q_idx.shape)
+    torch.cuda.synchronize()
+    host_in = torch.empty(n_l * per_layer, dtype=torch.bfloat16).pin_memory()
     host_in.copy_(torch.randn(host_in.shape, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16) / 16)
-    dev_in = torch.empty_like(host_in, device="cuda")
+    h_q = host_in[:n_l * qq]
+    h_k = host_in[n_l * qq:n_l * (qq + 512)]
+    h_v = host_in[n_l * (qq + 512):n_l * (qq + 1024)]
+    h_r = host_in[n_l * (qq + 1024):]
+    rows = []                               # (dst, dst pitch, src, row bytes) of the appended rows
+    for name, src, row in (("k_cache", h_k, 1024), ("v_cache", h_v, 1024), ("raw_idx_k", h_r, 256)):
+        allt = stacked[name]
+        rows.append((allt[0, p].data_ptr(), allt.stride(0) * 2, src.data_ptr(), row))
     host_out = torch.empty(16 * 256 + 32, dtype=torch.bfloat16).pin_memory()
     out_view = b.out.view(-1)
     lse_view = b.lse.view(torch.bfloat16).view(-1)
 
     def body():
-        for l, L in enumerate(layers):
-            o = l * per_layer
-            L.q.view(-1).copy_(dev_in[o:o + 4096])
-            L.q_idx.view(-1).copy_(dev_in[o + 4096:o + 4224])
-            L.k_cache[p].view(-1).copy_(dev_in[o + 4224:o + 4736])
-            L.v_cache[p].view(-1).copy_(dev_in[o + 4736:o + 5248])
-            L.raw_idx_k[p].copy_(dev_in[o + 5248:o + 5376])
+        for l in range(n_l):
             dl.layer_step(l)
 
     g = capture(body, stream)
+
+    def one_step():
+        dev_q.copy_(h_q, non_blocking=True)
+        for dst, pitch, src, row in rows:
+            qb.qsa_copy_rows(dst, pitch, src, row, row, n_l, stream)
+        g.replay()
+        host_out[:4096].copy_(out_view, non_blocking=True)
+        host_out[4096:].copy_(lse_view, non_blocking=True)
+        stream.synchronize()
+
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            dev_in.copy_(host_in, non_blocking=True)
-            g.replay()
-            host_out[:4096].copy_(out_view, non_blocking=True)
-            host_out[4096:].copy_(lse_view, non_blocking=True)
-            stream.synchronize()
+            one_step()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(steps):
-            dev_in.copy_(host_in, non_blocking=True)
-            g.replay()
-            host_out[:4096].copy_(out_view, non_blocking=True)
-            host_out[4096:].copy_(lse_view, non_blocking=True)
-            stream.synchronize()
+            one_step()
         dt = time.perf_counter() - t0
     h2d = host_in.numel() * 2
     d2h = host_out.numel() * 2

@@ -101,6 +101,16 @@ QSA_API qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stre
  * kernel-specific detail (e.g. the offending row) to *detail (may be NULL). */
 QSA_API qsa_status qsa_read_device_status(const void *ws, qsa_stream stream, qsa_status *out, int32_t *detail);
 
+/* Input staging helper (not a step of the method): copies n_rows rows of row_bytes bytes
+ * from src (rows src_pitch bytes apart) to dst (rows dst_pitch bytes apart), host or device
+ * memory on either side, asynchronously on `stream` (one strided copy, no kernel). Used
+ * to append a new token's rows to per-layer caches stacked with a fixed layer stride.
+ * Host memory should be pinned for the copy to be asynchronous. Errors: NULL pointers,
+ * row_bytes larger than either pitch -> QSA_ERR_INVALID_ARGUMENT; n_rows == 0 copies
+ * nothing. */
+QSA_API qsa_status qsa_copy_rows(void *dst, size_t dst_pitch, const void *src, size_t src_pitch, size_t row_bytes,
+                                 size_t n_rows, qsa_stream stream);
+
 /* a1 — Pool indexer keys ("VRAM に残す必要があるもの": one pooled 128 x bf16 key per
  * 4-token block). For each sequence s < B and each block b in [blk_begin[s], blk_end[s]):
  *   pooled[blk_off[s] + b][d] = bf16_rne( (raw[t0][d] + raw[t0+1][d] + raw[t0+2][d] + raw[t0+3][d]) / 4 ),

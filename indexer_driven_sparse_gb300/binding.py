@@ -62,6 +62,7 @@ _SIGNATURES = {
     "qsa_decode_step": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _P,
                                 _P, _SZ, _P]),
     "qsa_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P]),
+    "qsa_copy_rows": (_I32, [_P, _SZ, _P, _SZ, _SZ, _SZ, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
     "qsa_last_error": (C.c_char_p, []),
     "qsa_version": (C.c_char_p, []),
@@ -138,6 +139,13 @@ def qsa_read_device_status(ws, stream=None):
     _check(load().qsa_read_device_status(_ptr(ws), _stream(stream), C.byref(st), C.byref(det)),
            "qsa_read_device_status")
     return st.value, det.value
+
+
+def qsa_copy_rows(dst, dst_pitch, src, src_pitch, row_bytes, n_rows, stream=None):
+    """Strided row copy between any two memories (pointers or tensors' data pointers)."""
+    d = dst if isinstance(dst, int) else dst.data_ptr()
+    s = src if isinstance(src, int) else src.data_ptr()
+    _check(load().qsa_copy_rows(d, dst_pitch, s, src_pitch, row_bytes, n_rows, _stream(stream)), "qsa_copy_rows")
 
 
 def _ws_args(ws):

@@ -116,6 +116,17 @@ QSA_API qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stre
     return ok();
 }
 
+QSA_API qsa_status qsa_copy_rows(void *dst, size_t dst_pitch, const void *src, size_t src_pitch, size_t row_bytes,
+                                 size_t n_rows, qsa_stream stream) {
+    if (n_rows == 0 || row_bytes == 0) return ok();
+    QSA_NEED(dst != nullptr && src != nullptr, "dst and src must be non-NULL");
+    QSA_NEED(row_bytes <= dst_pitch && row_bytes <= src_pitch, "row_bytes exceeds a pitch");
+    const cudaError_t e = cudaMemcpy2DAsync(dst, dst_pitch, src, src_pitch, row_bytes, n_rows, cudaMemcpyDefault,
+                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync");
+    return ok();
+}
+
 QSA_API qsa_status qsa_read_device_status(const void *ws, qsa_stream stream, qsa_status *out, int32_t *detail) {
     QSA_NEED(ws != nullptr && out != nullptr, "workspace and out must be non-NULL");
     int32_t h[3] = {0, 0, 0};

@@ -136,3 +136,30 @@ def test_empty_batches_are_no_ops(lib):
     assert lib.qsa_topk_blocks(C.byref(c), 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
     assert lib.qsa_sparse_decode(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
     assert lib.qsa_sparse_prefill_chunk(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 8192, 0, 0, ws, 256, 0) == qb.QSA_OK
+
+
+def test_copy_rows_argument_checks(lib):
+    """Host-side validation of the strided row copy; an empty copy is a no-op."""
+    buf = (C.c_uint8 * 64)()
+    p = C.addressof(buf)
+    assert lib.qsa_copy_rows(p, 16, p, 16, 16, 0, None) == qb.QSA_OK
+    assert lib.qsa_copy_rows(None, 16, p, 16, 16, 1, None) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_copy_rows(p, 8, p, 16, 16, 1, None) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_copy_rows(p, 16, p, 8, 16, 1, None) == qb.QSA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.gpu
+def test_copy_rows_strided_host_to_device_and_back(lib):
+    """Rows land at the destination pitch, untouched bytes between them stay as they were."""
+    import torch
+    rows, row_bytes, pitch = 5, 48, 80
+    src = torch.arange(rows * row_bytes, dtype=torch.uint8).pin_memory()
+    dst = torch.full((rows * pitch,), 255, dtype=torch.uint8, device="cuda")
+    qb.qsa_copy_rows(dst, pitch, src, row_bytes, row_bytes, rows)
+    back = torch.empty(rows * row_bytes, dtype=torch.uint8).pin_memory()
+    qb.qsa_copy_rows(back, row_bytes, dst, pitch, row_bytes, rows)
+    torch.cuda.synchronize()
+    d = dst.cpu().view(rows, pitch)
+    assert torch.equal(d[:, :row_bytes].reshape(-1), src)
+    assert bool((d[:, row_bytes:] == 255).all())
+    assert torch.equal(back, src)
