@@ -21,6 +21,12 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller. The library
  *    never allocates, never frees, never keeps a pointer after returning and never
  *    synchronises, except qsa_read_device_status, which synchronises the stream it is given.
+ *  - The K/V cache (k_cache, v_cache) of the attention calls, and raw_idx_k of
+ *    qsa_decode_step, may instead live in pinned host memory mapped into the device's
+ *    address space (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped): the
+ *    kernels then gather the selected rows over the host link ("3090x3で 314 万コンテキスト",
+ *    section "VRAM に残す必要があるもの": only the pooled keys must stay on the GPU). A pointer
+ *    the device cannot read at the same address returns QSA_ERR_INVALID_ARGUMENT.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
  *    stream). Nothing else is launched, so the calls can be captured in a CUDA graph.
  *  - Row-major layouts; bf16 values are passed as raw 16-bit patterns (qsa_bf16).

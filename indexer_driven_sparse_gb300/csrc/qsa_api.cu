@@ -108,6 +108,23 @@ QSA_API size_t qsa_workspace_size(int32_t op, const qsa_config *cfg, int32_t n_r
     return ws_size(op, cfg, n_rows, max_blocks);
 }
 
+// The GPU reads p at the same address: device or managed memory, or pinned host memory mapped
+// into the device's address space (cudaHostAlloc; cudaHostRegister with the mapped flag) -
+// the K/V cache may live in host memory and be gathered over the host link.
+static bool device_accessible(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged: return true;
+        case cudaMemoryTypeHost: return at.devicePointer == p;
+        default: return false;
+    }
+}
+
 QSA_API qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream) {
     QSA_NEED(ws != nullptr, "workspace is NULL");
     QSA_NEED(ws_bytes >= kWsHeaderBytes, "workspace smaller than its 256-byte status block");
@@ -212,6 +229,8 @@ QSA_API qsa_status qsa_sparse_decode(const qsa_config *cfg, const qsa_bf16 *q, c
     QSA_NEED(q && k_cache && v_cache && tok_off && ctx_len && blocks && count && out, "NULL tensor pointer");
     QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16),
              "q, k_cache, v_cache and out must be 16-byte aligned");
+    QSA_NEED(device_accessible(k_cache) && device_accessible(v_cache),
+             "k_cache and v_cache must be device memory or mapped pinned host memory");
     char *w = static_cast<char *>(ws);
     AttnArgs a{};
     a.q = q;
@@ -253,6 +272,8 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
     QSA_NEED(q && k_cache && v_cache && blocks && count && out, "NULL tensor pointer");
     QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16) && aligned(blocks, 16),
              "q, k_cache, v_cache, out and blocks must be 16-byte aligned");
+    QSA_NEED(device_accessible(k_cache) && device_accessible(v_cache),
+             "k_cache and v_cache must be device memory or mapped pinned host memory");
     char *w = static_cast<char *>(ws);
     AttnArgs a{};
     a.q = q;
@@ -297,6 +318,8 @@ QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_id
     QSA_NEED(aligned(raw_idx_k, 16) && aligned(pooled, 16) && aligned(q_idx, 16) && aligned(k_cache, 16) &&
                  aligned(v_cache, 16) && aligned(q, 16),
              "bf16 tensors must be 16-byte aligned");
+    QSA_NEED(device_accessible(raw_idx_k) && device_accessible(k_cache) && device_accessible(v_cache),
+             "raw_idx_k, k_cache and v_cache must be device memory or mapped pinned host memory");
     const int G = cfg->n_q_heads / cfg->n_kv_heads;
     const int ctas = decode_step_grid(G);
     if (ctas == 0) return fail(QSA_ERR_CUDA, "decode step: cannot size the cooperative grid on this device");

@@ -171,3 +171,34 @@ def test_fused_step_rejects_unsupported(cuda_lib):
     st = lib.qsa_decode_step(C.byref(cfg), fake, fake, 10, fake, fake, fake, fake, fake, 100, fake, fake, 1, 10,
                              fake, fake, fake, None, fake, 1 << 30, None)
     assert st == qb.QSA_ERR_UNSUPPORTED
+
+
+def test_cache_in_pinned_host_memory(cuda_lib):
+    """K/V (and the raw indexer keys) in pinned host memory, gathered over the host link: the
+    fused step and the separate decode give the same selection and bit-identical outputs as
+    with the cache in device memory. Unregistered host memory is refused on the host."""
+    w = I.decode_workload("host_kv", [70001, 5000, 2051], 1, 16, 2, "planted", seed=9)
+    L = _to(w.layers[0])
+    b = DecodeBatch(w.n_q_heads, w.n_kv_heads, w.ctx_len)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+    assert b.fused_status()[0] == 0
+    want = (b.blocks.clone(), b.count.clone(), b.out.clone(), b.lse.clone())
+    hk, hv, hr = (t.cpu().pin_memory() for t in (L.k_cache, L.v_cache, L.raw_idx_k))
+    b.blocks.fill_(-7)
+    b.out.zero_()
+    b.fused_step(hr, pooled, L.q_idx, L.q, hk, hv)
+    assert b.fused_status()[0] == 0
+    got = (b.blocks, b.count, b.out, b.lse)
+    assert all(torch.equal(x, y) for x, y in zip(got, want))
+    # the separate attention call on the same selection
+    b.attend(L.q, L.k_cache, L.v_cache, want[0], want[1])
+    dev_out = b.out.clone()
+    b.out.zero_()
+    b.attend(L.q, hk, hv, want[0], want[1])
+    assert b.device_status()[0] == 0
+    assert torch.equal(b.out, dev_out)
+    with pytest.raises(qb.QsaError) as e:
+        b.fused_step(hr, pooled, L.q_idx, L.q, L.k_cache.cpu(), hv)   # pageable host memory
+    assert e.value.status == qb.QSA_ERR_INVALID_ARGUMENT

@@ -352,6 +352,21 @@ def test_prefill_out_of_order_list_is_flagged(cuda_lib):
     _assert_status_ok(c)
 
 
+def test_prefill_cache_in_pinned_host_memory(cuda_lib):
+    # K/V gathered from pinned host memory over the host link: the same outputs, bit for bit,
+    # on the tensor-core path (16 q / 2 KV heads) and the CUDA-core path (8 q / 2 KV heads)
+    for hq in (16, 8):
+        w = I.prefill_workload(f"prefill_host_{hq}", 9000, 40, hq, 2, "planted", seed=13)
+        c, _ = _run_prefill(w, 1024)
+        L = _to(w.layers[0])
+        dev_out, dev_lse = c.out.clone(), c.lse.clone()
+        hk, hv = L.k_cache.cpu().pin_memory(), L.v_cache.cpu().pin_memory()
+        c.out.zero_()
+        c.attend(L.q, hk, hv)
+        _assert_status_ok(c)
+        assert torch.equal(c.out, dev_out) and torch.equal(c.lse, dev_lse)
+
+
 # ----------------------------------------------------------------------------- full-size workloads, sampled
 
 def test_long_decode_full_size_one_layer(cuda_lib):
