@@ -50,6 +50,7 @@ def parse_args(argv=None):
                     help="fused: qsa_decode_step (one launch per layer-step); separate: the five calls")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kv-host", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-instrument", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -395,6 +396,42 @@ def e2e_decode(dl, stream, steps, warmup):
     return dt, h2d, d2h
 
 
+def kv_host_bench(dl, stream, steps, warmup, n_layers=2):
+    """The fused step with each layer's K/V cache and raw indexer keys in pinned host memory
+    (the pooled keys stay in HBM): the selected rows are gathered over the host link."""
+    import torch
+    b, layers = dl.b, dl.w.layers[:n_layers]
+    host = []
+    for L in layers:
+        hk, hv, hr = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.k_cache, L.v_cache, L.raw_idx_k))
+        hk.copy_(L.k_cache)
+        hv.copy_(L.v_cache)
+        hr.copy_(L.raw_idx_k)
+        host.append((hk, hv, hr))
+    torch.cuda.synchronize()
+
+    def body():
+        for l, L in enumerate(layers):
+            hk, hv, hr = host[l]
+            b.fused_step(hr, dl.pooled[l], L.q_idx, L.q, hk, hv)
+
+    with torch.cuda.stream(stream):
+        body()
+    torch.cuda.synchronize()
+    st = b.fused_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status with host K/V: {st}")
+    g = capture(body, stream)
+    t = time_graph(g, stream, steps, warmup, 1)
+    del g
+    n = steps * len(layers)
+    p = dl.w.ctx_len[0]
+    kv_bytes = (2048 + (p % 4) + 1) * 2 * 2 * 256 * 2      # selected tokens + tail, K and V, both heads
+    return {"layers": len(layers), "layer_steps_per_s": n / t, "us_per_layer_step": 1e6 * t / n,
+            "kv_bytes_per_layer_step": kv_bytes, "host_gather_gbs": kv_bytes * n / t / 1e9,
+            "note": "K/V and raw indexer keys in pinned host memory; pooled keys in HBM"}
+
+
 # ----------------------------------------------------------------------------- prefill
 
 def prefill_bench(steps, warmup, pk):
@@ -686,6 +723,9 @@ def main(argv=None):
         n = max(10, args.steps // 4)
         line["e2e"] = {"value": n * n_layers / dt * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h}
+
+    if not args.no_kv_host:
+        line["decode_kv_in_host_memory"] = kv_host_bench(dl, stream, max(20, args.steps // 4), max(3, args.warmup))
 
     if not args.no_prefill:
         del g
