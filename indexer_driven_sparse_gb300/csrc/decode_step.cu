@@ -1309,15 +1309,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         w_s[idx] = __ldcg(&ml_r[(size_t)j * 2 * Hq + h]);
         l_s[idx] = __ldcg(&ml_r[(size_t)j * 2 * Hq + Hq + h]);
     }
-    float v[kJ];
-    auto load_block = [&](int b) {
+    // a slice spans at most two blocks of 32 outputs when the row has 128 CTAs or more: both
+    // are loaded in the same round trip (further blocks, for fewer CTAs, one trip each)
+    float v[kJ], v2[kJ];
+    auto load_block = [&](int b, float (&dst)[kJ]) {
 #pragma unroll
         for (int k = 0; k < kJ; ++k) {
             const int j = warp + k * kStepWarps;
-            v[k] = j < cr ? __ldcg(&acc_r[((size_t)b * cr + j) * 32 + lane]) : 0.f;
+            dst[k] = j < cr ? __ldcg(&acc_r[((size_t)b * cr + j) * 32 + lane]) : 0.f;
         }
     };
-    if (b0 <= b1) load_block(b0);
+    if (b0 <= b1) load_block(b0, v);
+    if (b0 + 1 <= b1) load_block(b0 + 1, v2);
     __syncthreads();
     STEP_TRACE(13);
     for (int hh = warp; hh < nh; hh += kStepWarps) {
@@ -1341,7 +1344,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     }
     __syncthreads();
     for (int b = b0; b <= b1; ++b) {
-        if (b > b0) load_block(b);
+        if (b == b0 + 1) {
+#pragma unroll
+            for (int k = 0; k < kJ; ++k) v[k] = v2[k];
+        } else if (b > b0 + 1) {
+            load_block(b, v);
+        }
         const int h = b >> 3;                                           // 8 blocks of 32 per head
         const float *wv = w_s + (h - h_lo) * cr;
         float sacc = 0.f;
