@@ -430,6 +430,11 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
         fence_mbar_init();
         s_abort = 0;
     }
+    // the K and V stages start as zeros: a chunk's padding columns are not loaded, so they
+    // hold zeros or an earlier chunk's rows, finite either way (masked in S, P = 0 against V)
+    for (uint32_t i = tid; i < (kTcKStages + kTcVStages) * 32768u / 16u; i += kTcThreads)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + kTcK + 16u * i), "r"(0) : "memory");
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -536,8 +541,8 @@ __global__ void __maxnreg__(kTcMaxRegs) prefill_tc_kernel(TcArgs a) {
             const ChunkRec &r = ring[rs];
             for (int gi = pt; gi < kTcChunk * 32; gi += nthr) {
                 const int j = gi >> 5, gg = gi & 31;
-                int b = r.blk[j >> 2];
-                if (b < 0) b = r.blk[0];               // padding column: any valid token (masked)
+                const int b = r.blk[j >> 2];
+                if (b < 0) continue;                   // padding column: not loaded (masked)
                 // the newest block may extend past the last token; its tail is masked
                 const int64_t tok = min((int64_t)b * kRatio + (j & 3), last_tok);
                 cp_async16(stage0 + s * 32768 + (gg >> 3) * (kTcChunk * 128) + swz(j, gg & 7),
