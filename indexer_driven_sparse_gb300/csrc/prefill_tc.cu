@@ -10,9 +10,10 @@
 //
 // 1. Plan (one CTA per query tile, shared by its KV heads). Walking the history interval
 //    by interval, it marks per pooled block which of the tile's queries selected it (or
-//    own it as their current, partial block), compacts the marked blocks of the interval
-//    into their ascending union, and cuts the union into chunks of 16 blocks (64 tokens;
-//    a chunk never spans two intervals). Each chunk record holds the 16 block ids and,
+//    own it as their current, partial block), and places the marked blocks of every interval
+//    in the tile's ascending union, cut into chunks of 16 blocks (64 tokens; a chunk may
+//    straddle two intervals, so only the tile's last chunk is partial). Each chunk record
+//    holds the 16 block ids and,
 //    per query, a 64-bit word of the tokens it may see (its own selection; its own block
 //    only up to itself).
 //
@@ -64,7 +65,7 @@ struct ChunkRec {                            // 256 bytes
 };
 static_assert(sizeof(ChunkRec) == 256, "chunk record size");
 constexpr int kRecCopyBytes = 208;           // blk, vis, flags
-// chunks per tile: the union has at most QT * (512 + 1) blocks, plus one partial chunk per interval
+// chunks per tile: the union has at most QT * (512 + 1) blocks (the bound keeps a chunk of slack per interval)
 constexpr int kPlanCap = (kTcMaxQt * (kBlockTopK + 1) + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk + kTcMaxIntervals;
 constexpr int kPlanThreads = 384;                // 12 warps: two CTAs fit an SM
 constexpr int kPlanWarps = kPlanThreads / 32;
@@ -245,10 +246,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
         return (int)__reduce_add_sync(0xffffffffu, (unsigned)nu);
     };
 
-    // ---- pass 1: chunks per interval
+    // ---- pass 1: union blocks per interval
     for (int v = warp; v < n_iv_tile; v += kPlanWarps) {
         const int nu = mark(v);
-        if (lane == 0) counts[v] = (nu + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
+        if (lane == 0) counts[v] = nu;
     }
     __syncthreads();
     if (warp == 0) {                           // exclusive scan over the intervals
@@ -277,7 +278,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
         if (lane == 31) s_total = incl;
     }
     __syncthreads();
-    const int total = s_total;
+    // the tile's union in ascending block order, cut into chunks of 16 blocks: a chunk may
+    // straddle two intervals (the intervals set the walk's order, not the chunking)
+    const int total = (s_total + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
     if (total > kPlanCap) {                    // cannot happen for valid lists; stop cleanly
         if (tid == 0) {
             record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWherePrefill, i0);
@@ -285,26 +288,25 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
         }
         return;
     }
-    // ---- pass 2: records, in ascending block order, written in place
+    // ---- the records start as blk = -1, visibility 0, with the tile's first / last flags
     ChunkRec *out = a.recs + (size_t)qt * kPlanCap;
+    for (int e = tid; e < total * (int)(sizeof(ChunkRec) / 16); e += kPlanThreads) {
+        const int c = e / (int)(sizeof(ChunkRec) / 16), w = e % (int)(sizeof(ChunkRec) / 16);
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (w < kTcBlocksPerChunk / 4) val = make_uint4(~0u, ~0u, ~0u, ~0u);
+        if (w == (int)(offsetof(ChunkRec, first) / 16))
+            reinterpret_cast<int32_t *>(&val)[(offsetof(ChunkRec, first) % 16) / 4] = c == 0;
+        if (w == (int)(offsetof(ChunkRec, last) / 16))
+            reinterpret_cast<int32_t *>(&val)[(offsetof(ChunkRec, last) % 16) / 4] = c == total - 1;
+        reinterpret_cast<uint4 *>(out + c)[w] = val;
+    }
+    __syncthreads();
+    // ---- pass 2: every marked block at its position in the tile's union
     for (int v = warp; v < n_iv_tile; v += kPlanWarps) {
         const int b_lo = v * a.bpi;
         const int span = min(b_lo + a.bpi, nb_last + 1) - b_lo;
-        const int nu = mark(v);
-        const int n_ch = (nu + kTcBlocksPerChunk - 1) / kTcBlocksPerChunk;
-        const int off = counts[v];
-        // the interval's records in place: blk = -1, visibility 0, the tile's first / last flags
-        for (int e = lane; e < n_ch * (int)(sizeof(ChunkRec) / 16); e += 32) {
-            const int c = e / (int)(sizeof(ChunkRec) / 16), w = e % (int)(sizeof(ChunkRec) / 16);
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (w < kTcBlocksPerChunk / 4) val = make_uint4(~0u, ~0u, ~0u, ~0u);
-            if (w == (int)(offsetof(ChunkRec, first) / 16))
-                reinterpret_cast<int32_t *>(&val)[(offsetof(ChunkRec, first) % 16) / 4] = off + c == 0;
-            if (w == (int)(offsetof(ChunkRec, last) / 16))
-                reinterpret_cast<int32_t *>(&val)[(offsetof(ChunkRec, last) % 16) / 4] = v == n_iv_tile - 1 && c == n_ch - 1;
-            reinterpret_cast<uint4 *>(out + off + c)[w] = val;
-        }
-        __syncwarp();
+        mark(v);
+        const int off = counts[v];             // union blocks of the earlier intervals
         // the marked blocks in ascending order, 8 masks per lane and 256 per sweep: a warp scan
         // of the lanes' counts places each block in its chunk and slot
         const int n4 = (span + 7) / 8;
@@ -330,8 +332,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 if (mw[k] == 0) continue;
-                ChunkRec *r = out + off + pos / kTcBlocksPerChunk;
-                const int slot = pos % kTcBlocksPerChunk, b = b_lo + 8 * i4 + k;
+                ChunkRec *r = out + (off + pos) / kTcBlocksPerChunk;
+                const int slot = (off + pos) % kTcBlocksPerChunk, b = b_lo + 8 * i4 + k;
                 r->blk[slot] = b;
                 for (uint32_t mm = mw[k]; mm != 0; mm &= mm - 1u) {
                     const int qq = __ffs(mm) - 1;
