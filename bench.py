@@ -464,6 +464,9 @@ def prefill_bench(steps, warmup, pk):
     def topk_only():
         c.topk()
 
+    def select_only():
+        c.select(L.q_idx, pooled)
+
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         chunk()
@@ -477,7 +480,7 @@ def prefill_bench(steps, warmup, pk):
     g_att = capture(attend_only, stream)
     t_att = time_graph(g_att, stream, n, max(1, warmup), 1) / n
     phases = {"attention": t_att * 1e3}
-    for name, fn in (("score", score_only), ("topk", topk_only)):
+    for name, fn in (("select", select_only), ("score", score_only), ("topk", topk_only)):
         g1 = capture(fn, stream)
         phases[name] = time_graph(g1, stream, n, max(1, warmup), 1) / n * 1e3
         del g1

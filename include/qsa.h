@@ -73,7 +73,8 @@ typedef enum {
     QSA_OP_TOPK_BLOCKS = 2,
     QSA_OP_SPARSE_DECODE = 3,
     QSA_OP_SPARSE_PREFILL_CHUNK = 4,
-    QSA_OP_DECODE_STEP = 5
+    QSA_OP_DECODE_STEP = 5,
+    QSA_OP_PREFILL_SELECT = 6
 } qsa_op;
 
 /* Geometry. Field names follow the model config the page quotes
@@ -150,6 +151,25 @@ QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx,
                                    const int32_t *q_pos, int32_t Nq, const qsa_bf16 *pooled,
                                    int64_t n_pooled_total, const int32_t *blk_off, float *scores, int64_t ld,
                                    void *ws, size_t ws_bytes, qsa_stream stream);
+
+/* a2 + a3 fused for a prefill chunk (one sequence, q_seq NULL): the same blocks and counts
+ * as qsa_index_score followed by qsa_topk_blocks, without writing the score matrix
+ * ("GLM-5.3 最適化 第2部": prefill scoring is quadratic; "なぜ": top-512 per query). The
+ * scoring GEMM runs twice: first it keeps each row's maximum over every 64 consecutive
+ * visible blocks, whose 512th largest is a floor that at least 512 scores reach; then its
+ * epilogue keeps every visible score at or above the floor (exact fp32 scores, as
+ * qsa_index_score computes them) and the top-k takes each row's top 512 from those. A row
+ * whose candidates overflow (more than 32 in a tile of 256 blocks, e.g. many equal scores)
+ * or fall short is finished on the exact path: the full scores are then written to
+ * `scores` [Nq, ld] and that row streamed as by qsa_topk_blocks; otherwise `scores` is
+ * not touched. Arguments as for those two calls; workspace
+ * qsa_workspace_size(QSA_OP_PREFILL_SELECT, cfg, Nq, ld) (about 300 MB for 4096 queries
+ * over 66,560 blocks). Needs Nq >= 128, n_pooled_total >= 256, ld <= 524288, else
+ * QSA_ERR_UNSUPPORTED. */
+QSA_API qsa_status qsa_prefill_select(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_pos, int32_t Nq,
+                                      const qsa_bf16 *pooled, int64_t n_pooled_total, const int32_t *blk_off,
+                                      float *scores, int64_t ld, int32_t *blocks, int32_t *count, void *ws,
+                                      size_t ws_bytes, qsa_stream stream);
 
 /* a3 — Fixed-budget block selection ("なぜ": exactly 2048 tokens = 512 blocks beyond 2051
  * tokens of context; all blocks below). For row r with nb = q_pos[r] / 4, k = budget/ratio:

@@ -23,7 +23,8 @@ QSA_ERR_CUDA = 4
 QSA_ERR_DEVICE_TIMEOUT = 5
 QSA_ERR_DEVICE_BOUNDS = 6
 
-OP_POOL_KEYS, OP_INDEX_SCORE, OP_TOPK_BLOCKS, OP_SPARSE_DECODE, OP_SPARSE_PREFILL_CHUNK, OP_DECODE_STEP = range(6)
+(OP_POOL_KEYS, OP_INDEX_SCORE, OP_TOPK_BLOCKS, OP_SPARSE_DECODE, OP_SPARSE_PREFILL_CHUNK, OP_DECODE_STEP,
+ OP_PREFILL_SELECT) = range(7)
 BLOCK_TOPK = 512
 
 
@@ -63,6 +64,7 @@ _SIGNATURES = {
                                 _P, _SZ, _P]),
     "qsa_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "qsa_copy_rows": (_I32, [_P, _SZ, _P, _SZ, _SZ, _SZ, _P]),
+    "qsa_prefill_select": (_I32, [_CFG, _P, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
     "qsa_last_error": (C.c_char_p, []),
     "qsa_version": (C.c_char_p, []),
@@ -166,6 +168,15 @@ def qsa_index_score(cfg, q_idx, q_seq, q_pos, pooled, blk_off, scores, ws, strea
                                   _ptr(q_pos, torch.int32), q_idx.shape[0], _ptr(pooled, torch.bfloat16, "pooled"),
                                   pooled.shape[0], _ptr(blk_off, torch.int32), _ptr(scores, torch.float32, "scores"),
                                   scores.shape[1], *_ws_args(ws), _stream(stream)), "qsa_index_score")
+
+
+def qsa_prefill_select(cfg, q_idx, q_pos, pooled, blk_off, scores, blocks, count, ws, stream=None):
+    _check(load().qsa_prefill_select(C.byref(cfg), _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(q_pos, torch.int32),
+                                     q_idx.shape[0], _ptr(pooled, torch.bfloat16, "pooled"), pooled.shape[0],
+                                     _ptr(blk_off, torch.int32), _ptr(scores, torch.float32, "scores"),
+                                     scores.shape[1], _ptr(blocks, torch.int32, "blocks"),
+                                     _ptr(count, torch.int32, "count"), *_ws_args(ws), _stream(stream)),
+           "qsa_prefill_select")
 
 
 def qsa_topk_blocks(cfg, scores, q_pos, blocks, count, ws, stream=None):

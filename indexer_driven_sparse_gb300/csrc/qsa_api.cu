@@ -70,6 +70,7 @@ size_t ws_size(int32_t op, const qsa_config *c, int32_t n_rows, int64_t max_bloc
         case QSA_OP_SPARSE_PREFILL_CHUNK:
             return kWsHeaderBytes + prefill_scratch_bytes(n_rows, c->n_q_heads, c->n_kv_heads);
         case QSA_OP_DECODE_STEP: return decode_step_ws_bytes(n_rows, max_blocks, c->n_q_heads);
+        case QSA_OP_PREFILL_SELECT: return kWsHeaderBytes + prefill_select_scratch_bytes(n_rows, max_blocks);
         default: return 0;
     }
 }
@@ -197,6 +198,29 @@ QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx,
              : launch_index_score(q_idx, q_seq, q_pos, Nq, pooled, n_pooled_total, blk_off, scores, ld,
                                   static_cast<WsHeader *>(ws), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "index_score launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_prefill_select(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_pos, int32_t Nq,
+                                      const qsa_bf16 *pooled, int64_t n_pooled_total, const int32_t *blk_off,
+                                      float *scores, int64_t ld, int32_t *blocks, int32_t *count, void *ws,
+                                      size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(Nq >= 0 && Nq <= kMaxGridYZ, "Nq = %d out of range [0, 65535]", Nq);
+    QSA_NEED(ld >= 0 && n_pooled_total >= 0, "negative size");
+    QSA_NEED(ld <= (int64_t)1 << 28, "ld too large");
+    QSA_TRY(check_ws(QSA_OP_PREFILL_SELECT, cfg, Nq, ld, ws, ws_bytes));
+    if (Nq == 0) return ok();
+    if (!prefill_select_supported(Nq, n_pooled_total, ld))
+        return fail(QSA_ERR_UNSUPPORTED, "prefill select needs Nq >= 128, n_pooled >= 256 and ld <= 524288");
+    QSA_NEED(q_idx && q_pos && pooled && blk_off && scores && blocks && count, "NULL tensor pointer");
+    QSA_NEED(aligned(q_idx, 16) && aligned(pooled, 16), "q_idx and pooled must be 16-byte aligned");
+    QSA_NEED(aligned(scores, 4), "scores must be 4-byte aligned");
+    char *w = static_cast<char *>(ws);
+    const cudaError_t e = launch_prefill_select(q_idx, q_pos, Nq, pooled, n_pooled_total, blk_off, scores, ld, blocks,
+                                                count, reinterpret_cast<WsHeader *>(w), w + kWsHeaderBytes,
+                                                ws_bytes - kWsHeaderBytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prefill_select launch");
     return ok();
 }
 

@@ -124,6 +124,38 @@ cudaError_t launch_score_tc(const uint16_t *q_idx, const int32_t *q_pos, int Nq,
 cudaError_t launch_topk_blocks(const float *scores, int64_t ld, const int32_t *q_pos, int Nq, int32_t *blocks,
                                int32_t *count, WsHeader *hdr, void *scratch, size_t scratch_bytes, cudaStream_t st);
 
+// ---------------------------------------------------------------------------- fused prefill selection
+// Scoring and top-k of a prefill chunk without materialising the score matrix:
+//   1. the scoring GEMM keeps, per row, the max of every 64 consecutive visible blocks;
+//   2. each row's floor T = the 512th largest of those maxima (at least 512 scores reach it);
+//   3. the GEMM runs again and its epilogue keeps every visible score >= T as a 64-bit key in
+//      per-(row, 256-block tile) slots;
+//   4. the top-k kernel takes each row's exact top 512 from its candidates;
+//   5. rows whose candidates overflowed a tile's slots (or fell short) are left to the exact
+//      path: the GEMM stores the full scores and the top-k kernel streams those rows only
+//      (both launches return at once when no row needs them).
+constexpr int kSelGroup = 64;                 // blocks per maximum
+constexpr int kSelSlots = 16;                 // candidate slots per (row, half a tile: 128 blocks)
+constexpr int kSelSegsPerThread = 8;          // top-k: half-tile segments of a row per thread
+constexpr int kSelMaxTiles = 512 * kSelSegsPerThread / 2;   // 2048 tiles of 256 blocks
+
+struct TopkCandidates {
+    const uint64_t *slots = nullptr;   // [Nq][n_segs][kSelSlots] candidate keys (nullptr: stream the scores)
+    const uint8_t *scnt = nullptr;     // [Nq][n_segs] candidates per segment (> kSelSlots: overflowed)
+    int32_t n_segs = 0;                // segments of a row: two per tile of 256 blocks
+    int32_t *fb_rows = nullptr;        // [Nq] rows left to the exact path
+    int32_t *fb_any = nullptr;         // set when some row is
+    int32_t fallback_only = 0;         // run only the rows of fb_rows (on the stored scores)
+};
+
+cudaError_t launch_topk_with(const float *scores, int64_t ld, const int32_t *q_pos, int Nq, int32_t *blocks,
+                             int32_t *count, WsHeader *hdr, const TopkCandidates &tc, cudaStream_t st);
+size_t prefill_select_scratch_bytes(int Nq, int64_t ld);
+bool prefill_select_supported(int Nq, int64_t n_pooled, int64_t ld);
+cudaError_t launch_prefill_select(const uint16_t *q_idx, const int32_t *q_pos, int Nq, const uint16_t *pooled,
+                                  int64_t n_pooled, const int32_t *blk_off, float *scores, int64_t ld, int32_t *blocks,
+                                  int32_t *count, WsHeader *hdr, void *scratch, size_t scratch_bytes, cudaStream_t st);
+
 struct AttnArgs {
     const uint16_t *q;        // [rows, Hq, D]
     const uint16_t *k_cache;  // [T, Hkv, D]

@@ -96,6 +96,18 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, float (&v)[32]) 
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The wait, with v passed through it: no use of v can be scheduled before the loads land.
+__device__ __forceinline__ void tmem_wait_ld(float (&v)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]), "+f"(v[8]),
+          "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]),
+          "+f"(v[17]), "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]),
+          "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
+        :
+        : "memory");
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; flushes subnormals)
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

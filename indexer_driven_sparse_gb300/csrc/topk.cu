@@ -225,7 +225,8 @@ __device__ void radix_select_row(const float *__restrict__ s, int64_t nb, int32_
 
 __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float *__restrict__ scores, int64_t ld,
                                                                     const int32_t *q_pos, int32_t *__restrict__ blocks,
-                                                                    int32_t *__restrict__ count, WsHeader *hdr) {
+                                                                    int32_t *__restrict__ count, WsHeader *hdr,
+                                                                    TopkCandidates tc) {
     __shared__ uint64_t cand[kCandCap];        // the histogram shares this space (used before the candidates)
     uint32_t *hist = reinterpret_cast<uint32_t *>(cand);
     __shared__ int32_t sel[kBlockTopK];
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
 
     const int row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tc.fallback_only && tc.fb_rows[row] == 0) return;   // this row was settled from its candidates
     const int p = q_pos[row];
     const int64_t nb = p >= 0 ? (p >> 2) : -1;
     int32_t *out = blocks + (int64_t)row * kBlockTopK;
@@ -257,6 +259,142 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
     }
     const float *s = scores + (int64_t)row * ld;
     const unsigned lt = (1u << lane) - 1u;
+
+    // Exact top 512 of nc candidate keys in cand[] (512 <= nc <= kCandCap): 1024 bins linear in
+    // their scores, the threshold bin's members ranked by key, the sure ones taken directly;
+    // the ids are written ascending. Returns false (nothing written) when the bins cannot
+    // split the candidates. Called by every thread of the CTA.
+    auto finish_candidates = [&](uint32_t nc) -> bool {
+        // exact top 512 of the candidates: 1024 bins linear in their scores, the
+        // threshold bin's members ranked by key, the sure ones taken directly
+        float cmin = FLT_MAX, cmax = -FLT_MAX;
+        for (uint32_t k = tid; k < nc; k += kTopkThreads) {
+            const float v = key_score(cand[k]);
+            if (fabsf(v) <= FLT_MAX) {
+                cmin = fminf(cmin, v);
+                cmax = fmaxf(cmax, v);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+            cmin = fminf(cmin, __shfl_xor_sync(0xffffffffu, cmin, o));
+        }
+        if (lane == 0) {
+            s_red[0][warp] = cmax;
+            s_red[1][warp] = cmin;
+        }
+        for (int i = tid; i < kCandBins; i += kTopkThreads) hist2[i] = 0;
+        if (tid == 0) {
+            s_nsel = 0;
+            s_neq = 0;
+        }
+        __syncthreads();
+        cmax = s_red[0][0];
+        cmin = s_red[1][0];
+        for (int w = 1; w < kTopkWarps; ++w) {
+            cmax = fmaxf(cmax, s_red[0][w]);
+            cmin = fminf(cmin, s_red[1][w]);
+        }
+        const float cscale = cmax > cmin ? (float)(kCandBins - 2) / (cmax - cmin) : 0.f;
+        if (cscale > 0.f && cscale <= FLT_MAX) {
+            auto cbin = [&](float v) -> int {
+                if (v != v || v == -INFINITY) return 0;
+                if (v == INFINITY) return kCandBins - 1;
+                const float t = (v - cmin) * cscale;
+                if (!(t > 0.f)) return 0;
+                return t >= (float)(kCandBins - 2) ? kCandBins - 2 : (int)t;
+            };
+            for (uint32_t k = tid; k < nc; k += kTopkThreads) atomicAdd(&hist2[cbin(key_score(cand[k]))], 1u);
+            __syncthreads();
+            find_bin_from_top<kCandBins>(hist2, kBlockTopK, &s_b, &s_above, wtot);
+            const int bd = s_b;
+            const uint32_t need_eq = kBlockTopK - s_above;
+            const uint32_t n_eq = hist2[bd];
+            if (n_eq <= (uint32_t)kTopkThreads) {
+                // sure keys -> their ids; the threshold bin's keys -> a small list
+                for (uint32_t k0 = 0; k0 < nc; k0 += kTopkThreads) {
+                    const uint32_t k = k0 + tid;
+                    const uint64_t key = k < nc ? cand[k] : 0ull;
+                    const int b = k < nc ? cbin(key_score(key)) : -1;
+                    const bool sure = b > bd, eq = b == bd;
+                    const unsigned bs = __ballot_sync(0xffffffffu, sure);
+                    const unsigned be = __ballot_sync(0xffffffffu, eq);
+                    uint32_t o1 = 0, o2 = 0;
+                    if (lane == 0) {
+                        if (bs) o1 = atomicAdd(&s_nsel, (uint32_t)__popc(bs));
+                        if (be) o2 = atomicAdd(&s_neq, (uint32_t)__popc(be));
+                    }
+                    o1 = __shfl_sync(0xffffffffu, o1, 0);
+                    o2 = __shfl_sync(0xffffffffu, o2, 0);
+                    if (sure) sel[o1 + __popc(bs & lt)] = (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+                    if (eq) s_eq[o2 + __popc(be & lt)] = key;
+                }
+                __syncthreads();
+                if (tid < (int)n_eq) {
+                    const uint64_t mine = s_eq[tid];
+                    uint32_t rank = 0;
+                    for (uint32_t j = 0; j < n_eq; ++j) rank += s_eq[j] > mine ? 1u : 0u;
+                    if (rank < need_eq) sel[s_above + rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)mine);
+                }
+                __syncthreads();
+                bitonic_i32_asc(sel, kBlockTopK);
+                for (int i = tid; i < kBlockTopK; i += kTopkThreads) out[i] = sel[i];
+                if (tid == 0) {
+                    count[row] = kBlockTopK;
+                    if (s_nsel != s_above || s_neq != n_eq) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereTopk, row);
+                }
+                return true;
+            }
+        }
+        return false;
+    };
+
+
+    // ---- candidate mode: the row's candidates were gathered by the scoring epilogue (every
+    // score at or above a floor that at least 512 scores reach), 64-bit keys in per-segment slots
+    if (tc.slots != nullptr) {
+        const uint8_t *cn = tc.scnt + (size_t)row * tc.n_segs;
+        const uint64_t *sl = tc.slots + (size_t)row * tc.n_segs * kSelSlots;
+        uint32_t c[kSelSegsPerThread], mine = 0;
+        bool over = false;
+#pragma unroll
+        for (int k = 0; k < kSelSegsPerThread; ++k) {
+            const int t = tid * kSelSegsPerThread + k;
+            c[k] = t < tc.n_segs ? cn[t] : 0u;
+            over |= c[k] > (uint32_t)kSelSlots;
+            mine += c[k];
+        }
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) wtot[warp] = incl;
+        const bool any_over = __syncthreads_or(over);
+        uint32_t base = incl - mine, total = 0;
+        for (int w = 0; w < kTopkWarps; ++w) {
+            total += wtot[w];
+            if (w < warp) base += wtot[w];
+        }
+        const bool ok = !any_over && total >= (uint32_t)kBlockTopK && total <= (uint32_t)kCandCap;
+        if (ok) {
+#pragma unroll
+            for (int k = 0; k < kSelSegsPerThread; ++k) {
+                const int t = tid * kSelSegsPerThread + k;
+                for (uint32_t e = 0; e < c[k]; ++e) cand[base + e] = sl[(size_t)t * kSelSlots + e];
+                base += c[k];
+            }
+        }
+        __syncthreads();
+        if (ok && finish_candidates(total)) return;
+        if (tid == 0) {                        // left to the exact path over the stored scores
+            tc.fb_rows[row] = 1;
+            atomicExch(tc.fb_any, 1);
+        }
+        return;
+    }
 
     // ---- one pass when a sample places the cut: every 64th score sets value-linear bins
     // and a bin cut keeping about 3 x 512 of the row; one streaming pass gathers every score
@@ -376,87 +514,7 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
             }
             __syncthreads();
             const uint32_t nc = s_ncand;
-            if (nc >= (uint32_t)kBlockTopK && nc <= (uint32_t)kCandCap) {
-                // exact top 512 of the candidates: 1024 bins linear in their scores, the
-                // threshold bin's members ranked by key, the sure ones taken directly
-                float cmin = FLT_MAX, cmax = -FLT_MAX;
-                for (uint32_t k = tid; k < nc; k += kTopkThreads) {
-                    const float v = key_score(cand[k]);
-                    if (fabsf(v) <= FLT_MAX) {
-                        cmin = fminf(cmin, v);
-                        cmax = fmaxf(cmax, v);
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) {
-                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-                    cmin = fminf(cmin, __shfl_xor_sync(0xffffffffu, cmin, o));
-                }
-                if (lane == 0) {
-                    s_red[0][warp] = cmax;
-                    s_red[1][warp] = cmin;
-                }
-                for (int i = tid; i < kCandBins; i += kTopkThreads) hist2[i] = 0;
-                if (tid == 0) s_nsel = 0;
-                __syncthreads();
-                cmax = s_red[0][0];
-                cmin = s_red[1][0];
-                for (int w = 1; w < kTopkWarps; ++w) {
-                    cmax = fmaxf(cmax, s_red[0][w]);
-                    cmin = fminf(cmin, s_red[1][w]);
-                }
-                const float cscale = cmax > cmin ? (float)(kCandBins - 2) / (cmax - cmin) : 0.f;
-                if (cscale > 0.f && cscale <= FLT_MAX) {
-                    auto cbin = [&](float v) -> int {
-                        if (v != v || v == -INFINITY) return 0;
-                        if (v == INFINITY) return kCandBins - 1;
-                        const float t = (v - cmin) * cscale;
-                        if (!(t > 0.f)) return 0;
-                        return t >= (float)(kCandBins - 2) ? kCandBins - 2 : (int)t;
-                    };
-                    for (uint32_t k = tid; k < nc; k += kTopkThreads) atomicAdd(&hist2[cbin(key_score(cand[k]))], 1u);
-                    __syncthreads();
-                    find_bin_from_top<kCandBins>(hist2, kBlockTopK, &s_b, &s_above, wtot);
-                    const int bd = s_b;
-                    const uint32_t need_eq = kBlockTopK - s_above;
-                    const uint32_t n_eq = hist2[bd];
-                    if (n_eq <= (uint32_t)kTopkThreads) {
-                        // sure keys -> their ids; the threshold bin's keys -> a small list
-                        for (uint32_t k0 = 0; k0 < nc; k0 += kTopkThreads) {
-                            const uint32_t k = k0 + tid;
-                            const uint64_t key = k < nc ? cand[k] : 0ull;
-                            const int b = k < nc ? cbin(key_score(key)) : -1;
-                            const bool sure = b > bd, eq = b == bd;
-                            const unsigned bs = __ballot_sync(0xffffffffu, sure);
-                            const unsigned be = __ballot_sync(0xffffffffu, eq);
-                            uint32_t o1 = 0, o2 = 0;
-                            if (lane == 0) {
-                                if (bs) o1 = atomicAdd(&s_nsel, (uint32_t)__popc(bs));
-                                if (be) o2 = atomicAdd(&s_neq, (uint32_t)__popc(be));
-                            }
-                            o1 = __shfl_sync(0xffffffffu, o1, 0);
-                            o2 = __shfl_sync(0xffffffffu, o2, 0);
-                            if (sure) sel[o1 + __popc(bs & lt)] = (int32_t)(0xFFFFFFFFu - (uint32_t)key);
-                            if (eq) s_eq[o2 + __popc(be & lt)] = key;
-                        }
-                        __syncthreads();
-                        if (tid < (int)n_eq) {
-                            const uint64_t mine = s_eq[tid];
-                            uint32_t rank = 0;
-                            for (uint32_t j = 0; j < n_eq; ++j) rank += s_eq[j] > mine ? 1u : 0u;
-                            if (rank < need_eq) sel[s_above + rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)mine);
-                        }
-                        __syncthreads();
-                        bitonic_i32_asc(sel, kBlockTopK);
-                        for (int i = tid; i < kBlockTopK; i += kTopkThreads) out[i] = sel[i];
-                        if (tid == 0) {
-                            count[row] = kBlockTopK;
-                            if (s_nsel != s_above || s_neq != n_eq) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereTopk, row);
-                        }
-                        return;
-                    }
-                }
-            }
+            if (nc >= (uint32_t)kBlockTopK && nc <= (uint32_t)kCandCap && finish_candidates(nc)) return;
         }
         __syncthreads();
     }
@@ -563,12 +621,19 @@ size_t topk_scratch_bytes(int Nq, int64_t ld) {
     return 0;
 }
 
+cudaError_t launch_topk_with(const float *scores, int64_t ld, const int32_t *q_pos, int Nq, int32_t *blocks,
+                             int32_t *count, WsHeader *hdr, const TopkCandidates &tc, cudaStream_t st) {
+    if (Nq == 0) return cudaSuccess;
+    topk_rows_kernel<<<Nq, kTopkThreads, 0, st>>>(scores, ld, q_pos, blocks, count, hdr, tc);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_topk_blocks(const float *scores, int64_t ld, const int32_t *q_pos, int Nq, int32_t *blocks,
                                int32_t *count, WsHeader *hdr, void *scratch, size_t scratch_bytes, cudaStream_t st) {
     (void)scratch;
     (void)scratch_bytes;
     if (Nq == 0) return cudaSuccess;
-    topk_rows_kernel<<<Nq, kTopkThreads, 0, st>>>(scores, ld, q_pos, blocks, count, hdr);
+    topk_rows_kernel<<<Nq, kTopkThreads, 0, st>>>(scores, ld, q_pos, blocks, count, hdr, TopkCandidates{});
     return cudaGetLastError();
 }
 

@@ -119,6 +119,10 @@ class PrefillChunk:
                  qb.workspace_size(qb.OP_INDEX_SCORE, self.cfg, self.Nc, self.ld),
                  qb.workspace_size(qb.OP_TOPK_BLOCKS, self.cfg, self.Nc, self.ld),
                  qb.workspace_size(qb.OP_SPARSE_PREFILL_CHUNK, self.cfg, self.Nc, self.ld)]
+        # scoring and top-k fused (no score matrix) for chunks of at least one 128-query tile
+        self.fused_select = self.Nc >= 128 and self.n_pooled >= 256
+        if self.fused_select:
+            sizes.append(qb.workspace_size(qb.OP_PREFILL_SELECT, self.cfg, self.Nc, self.ld))
         self.ws = _workspace(max(sizes), device)
 
     def new_pooled(self):
@@ -140,6 +144,11 @@ class PrefillChunk:
     def topk(self, stream=None):
         qb.qsa_topk_blocks(self.cfg, self.scores, self.q_pos, self.blocks, self.count, self.ws, stream)
 
+    def select(self, q_idx, pooled, stream=None):
+        """Scores and top-k in one call without the score matrix (qsa_prefill_select)."""
+        qb.qsa_prefill_select(self.cfg, q_idx, self.q_pos, pooled, self.blk_off, self.scores, self.blocks, self.count,
+                              self.ws, stream)
+
     def attend(self, q, k_cache, v_cache, blocks=None, count=None, stream=None):
         qb.qsa_sparse_prefill_chunk(self.cfg, q, self.p0, k_cache, v_cache,
                                     self.blocks if blocks is None else blocks,
@@ -147,9 +156,13 @@ class PrefillChunk:
                                     self.ws, stream)
 
     def run(self, q_idx, q, k_cache, v_cache, pooled, stream=None):
-        """The chunk's path after pooling: score -> top-k -> interval-walk attention."""
-        self.score(q_idx, pooled, stream)
-        self.topk(stream)
+        """The chunk's path after pooling: score -> top-k (fused when the chunk has a full
+        query tile) -> interval-walk attention."""
+        if self.fused_select:
+            self.select(q_idx, pooled, stream)
+        else:
+            self.score(q_idx, pooled, stream)
+            self.topk(stream)
         self.attend(q, k_cache, v_cache, stream=stream)
 
     def device_status(self, stream=None):

@@ -352,6 +352,38 @@ def test_prefill_out_of_order_list_is_flagged(cuda_lib):
     _assert_status_ok(c)
 
 
+@pytest.mark.parametrize("case", ["chunk_full", "short_history", "all_equal", "sharp"])
+def test_prefill_select_equals_score_then_topk(cuda_lib, case):
+    # the fused selection (no score matrix) returns exactly the blocks of qsa_index_score +
+    # qsa_topk_blocks: the same fp32 scores, the same keys; the equal-score and short-history
+    # rows overflow their candidate slots and take the exact path
+    if case == "chunk_full":
+        w = I.prefill_chunk(device="cuda")
+    elif case == "short_history":
+        w = I.prefill_workload("sel_short", 3000, 300, 16, 2, "planted", seed=21)
+    elif case == "all_equal":
+        w = I.prefill_workload("sel_ties", 150000, 256, 16, 2, "gaussian", seed=22)
+        w.layers[0].q_idx.zero_()
+    else:
+        w = I.prefill_workload("sel_sharp", 140000, 640, 16, 2, "sharp", seed=23)
+    L = _to(w.layers[0])
+    c = PrefillChunk(w.n_q_heads, w.n_kv_heads, w.ctx_len[0], w.n_chunk, 8192)
+    assert c.fused_select
+    pooled = c.new_pooled()
+    c.pool(L.raw_idx_k, pooled)
+    c.score(L.q_idx, pooled)
+    c.topk()
+    _assert_status_ok(c)
+    want_b, want_c = c.blocks.clone(), c.count.clone()
+    c.blocks.fill_(-9)
+    c.count.fill_(-9)
+    c.scores.fill_(float("nan"))
+    c.select(L.q_idx, pooled)
+    _assert_status_ok(c)
+    assert torch.equal(c.count, want_c)
+    assert torch.equal(c.blocks, want_b)
+
+
 def test_prefill_cache_in_pinned_host_memory(cuda_lib):
     # K/V gathered from pinned host memory over the host link: the same outputs, bit for bit,
     # on the tensor-core path (16 q / 2 KV heads) and the CUDA-core path (8 q / 2 KV heads)
