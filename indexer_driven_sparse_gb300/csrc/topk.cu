@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
     __shared__ float s_red[2][kTopkWarps];
     __shared__ int s_b;
     __shared__ uint32_t s_above, s_nsel, s_ncand, s_written;
+    __shared__ uint64_t s_thr64;
 
     const int row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -351,6 +352,94 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
     };
 
 
+    // Exact top 512 of nc candidate keys already in ascending block order in cand[]: the
+    // 512th largest key by bins over their scores and a rank among the boundary bin's members,
+    // then an order-preserving compaction of the keys at or above it (no sort). Returns false
+    // (nothing written) when the bins cannot split the candidates.
+    auto finish_ordered = [&](uint32_t nc) -> bool {
+        float cmin = FLT_MAX, cmax = -FLT_MAX;
+        for (uint32_t k = tid; k < nc; k += kTopkThreads) {
+            const float v = key_score(cand[k]);
+            if (fabsf(v) <= FLT_MAX) {
+                cmin = fminf(cmin, v);
+                cmax = fmaxf(cmax, v);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+            cmin = fminf(cmin, __shfl_xor_sync(0xffffffffu, cmin, o));
+        }
+        if (lane == 0) {
+            s_red[0][warp] = cmax;
+            s_red[1][warp] = cmin;
+        }
+        for (int i = tid; i < kCandBins; i += kTopkThreads) hist2[i] = 0;
+        if (tid == 0) s_neq = 0;
+        __syncthreads();
+        cmax = s_red[0][0];
+        cmin = s_red[1][0];
+        for (int w = 1; w < kTopkWarps; ++w) {
+            cmax = fmaxf(cmax, s_red[0][w]);
+            cmin = fminf(cmin, s_red[1][w]);
+        }
+        const float cscale = cmax > cmin ? (float)(kCandBins - 2) / (cmax - cmin) : 0.f;
+        if (!(cscale > 0.f && cscale <= FLT_MAX)) return false;
+        auto cbin = [&](float v) -> int {
+            if (v != v || v == -INFINITY) return 0;
+            if (v == INFINITY) return kCandBins - 1;
+            const float t = (v - cmin) * cscale;
+            if (!(t > 0.f)) return 0;
+            return t >= (float)(kCandBins - 2) ? kCandBins - 2 : (int)t;
+        };
+        for (uint32_t k = tid; k < nc; k += kTopkThreads) atomicAdd(&hist2[cbin(key_score(cand[k]))], 1u);
+        __syncthreads();
+        find_bin_from_top<kCandBins>(hist2, kBlockTopK, &s_b, &s_above, wtot);
+        const int bd = s_b;
+        const uint32_t need_eq = kBlockTopK - s_above, n_eq = hist2[bd];
+        if (n_eq > (uint32_t)kTopkThreads) return false;
+        for (uint32_t k = tid; k < nc; k += kTopkThreads) {
+            const uint64_t key = cand[k];
+            if (cbin(key_score(key)) == bd) s_eq[atomicAdd(&s_neq, 1u)] = key;
+        }
+        __syncthreads();
+        if (tid < (int)n_eq) {                  // the boundary bin's need_eq-th largest key
+            const uint64_t mine = s_eq[tid];
+            uint32_t rank = 0;
+            for (uint32_t j = 0; j < n_eq; ++j) rank += s_eq[j] > mine ? 1u : 0u;
+            if (rank == need_eq - 1u) s_thr64 = mine;
+        }
+        __syncthreads();
+        const uint64_t t64 = s_thr64;
+        // contiguous candidates per thread keep the order; a block scan places them
+        const uint32_t per = (nc + kTopkThreads - 1) / kTopkThreads;
+        const uint32_t i0 = min(nc, tid * per), i1 = min(nc, i0 + per);
+        uint32_t cnt = 0;
+        for (uint32_t k = i0; k < i1; ++k) cnt += cand[k] >= t64 ? 1u : 0u;
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) wtot[warp] = incl;
+        __syncthreads();
+        uint32_t pos = incl - cnt;
+        for (int w = 0; w < warp; ++w) pos += wtot[w];
+        for (uint32_t k = i0; k < i1; ++k) {
+            const uint64_t key = cand[k];
+            if (key >= t64) {
+                if (pos < (uint32_t)kBlockTopK) out[pos] = (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+                ++pos;
+            }
+        }
+        if (tid == 0) {
+            count[row] = kBlockTopK;
+            if (s_neq != n_eq) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereTopk, row);
+        }
+        return true;
+    };
+
     // ---- candidate mode: the row's candidates were gathered by the scoring epilogue (every
     // score at or above a floor that at least 512 scores reach), 64-bit keys in per-segment slots
     if (tc.slots != nullptr) {
@@ -388,7 +477,7 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
             }
         }
         __syncthreads();
-        if (ok && finish_candidates(total)) return;
+        if (ok && finish_ordered(total)) return;
         if (tid == 0) {                        // left to the exact path over the stored scores
             tc.fb_rows[row] = 1;
             atomicExch(tc.fb_any, 1);
