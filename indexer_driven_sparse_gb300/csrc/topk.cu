@@ -445,12 +445,14 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
     if (tc.slots != nullptr) {
         const uint8_t *cn = tc.scnt + (size_t)row * tc.n_segs;
         const uint64_t *sl = tc.slots + (size_t)row * tc.n_segs * kSelSlots;
+        // ceil(n_segs / threads) consecutive segments per thread, so their loads spread widely
+        const int per = (tc.n_segs + kTopkThreads - 1) / kTopkThreads;
         uint32_t c[kSelSegsPerThread], mine = 0;
         bool over = false;
 #pragma unroll
         for (int k = 0; k < kSelSegsPerThread; ++k) {
-            const int t = tid * kSelSegsPerThread + k;
-            c[k] = t < tc.n_segs ? cn[t] : 0u;
+            const int t = tid * per + k;
+            c[k] = k < per && t < tc.n_segs ? cn[t] : 0u;
             over |= c[k] > (uint32_t)kSelSlots;
             mine += c[k];
         }
@@ -469,10 +471,16 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
         }
         const bool ok = !any_over && total >= (uint32_t)kBlockTopK && total <= (uint32_t)kCandCap;
         if (ok) {
+#pragma unroll 1
+            for (int k = 0; k < per; ++k) {
+                if (c[k] == 0u) continue;
+                const uint64_t *src = sl + (size_t)(tid * per + k) * kSelSlots;
+                uint64_t x[kSelSlots];              // the segment's loads all in flight at once
 #pragma unroll
-            for (int k = 0; k < kSelSegsPerThread; ++k) {
-                const int t = tid * kSelSegsPerThread + k;
-                for (uint32_t e = 0; e < c[k]; ++e) cand[base + e] = sl[(size_t)t * kSelSlots + e];
+                for (int e = 0; e < kSelSlots; ++e) x[e] = (uint32_t)e < c[k] ? __ldcg(src + e) : 0ull;
+#pragma unroll
+                for (int e = 0; e < kSelSlots; ++e)
+                    if ((uint32_t)e < c[k]) cand[base + e] = x[e];
                 base += c[k];
             }
         }
