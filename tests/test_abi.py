@@ -163,3 +163,21 @@ def test_copy_rows_strided_host_to_device_and_back(lib):
     assert torch.equal(d[:, :row_bytes].reshape(-1), src)
     assert bool((d[:, row_bytes:] == 255).all())
     assert torch.equal(back, src)
+
+
+def test_prefill_select_host_checks(lib):
+    # the fused selection: workspace sized for the chunk, refused when too small, too few
+    # queries for a tensor-core tile, or NULL tensors; nothing launches on a refusal
+    c = cfg()
+    need = lib.qsa_workspace_size(qb.OP_PREFILL_SELECT, C.byref(c), 4096, 66560)
+    assert need > 4096 * 260 * 2 * 16 * 8          # the candidate slots dominate
+    assert lib.qsa_prefill_select(C.byref(c), FAKE, FAKE, 4096, FAKE, 66560, FAKE, FAKE, 66560, FAKE, FAKE, FAKE,
+                                  256, 0) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    need_small = lib.qsa_workspace_size(qb.OP_PREFILL_SELECT, C.byref(c), 64, 66560)
+    assert lib.qsa_prefill_select(C.byref(c), FAKE, FAKE, 64, FAKE, 66560, FAKE, FAKE, 66560, FAKE, FAKE, FAKE,
+                                  need_small, 0) == qb.QSA_ERR_UNSUPPORTED
+    assert lib.qsa_prefill_select(C.byref(c), FAKE, FAKE, 4096, FAKE, 66560, FAKE, 0, 66560, FAKE, FAKE, FAKE,
+                                  need, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    need0 = lib.qsa_workspace_size(qb.OP_PREFILL_SELECT, C.byref(c), 0, 66560)
+    assert lib.qsa_prefill_select(C.byref(c), FAKE, FAKE, 0, FAKE, 66560, FAKE, FAKE, 66560, FAKE, FAKE, FAKE,
+                                  need0, 0) == qb.QSA_OK
