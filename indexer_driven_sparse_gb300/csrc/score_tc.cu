@@ -12,6 +12,11 @@
 //   warp 1: one thread issues the 8 MMAs (K = 16 each) of a tile and commits them;
 //   warps 2-5: read the accumulator (one row per thread), transpose 32x32 through shared
 //   memory, and store rows with coalesced 128-byte writes, only columns b < nb(p_row).
+// For the fused prefill selection the same GEMM runs with two other epilogues: per row the
+// maximum of every 64 visible blocks, or every visible score at or above the row's floor as
+// a 64-bit key in per-(row, half tile) slots (8 epilogue warps then, two per lane quarter).
+// Each CTA takes a contiguous run of tiles, queries fastest, so a stage keeps its pooled-key
+// tile while the query tiles change.
 // Products of bf16 values are exact in fp32; the tensor core sums them in fp32 in its own
 // order. Every wait is bounded; a timeout records QSA_ERR_DEVICE_TIMEOUT and the roles
 // drain what they issued before TMEM is freed.

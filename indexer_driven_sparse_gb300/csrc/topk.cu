@@ -19,6 +19,13 @@
 // The 512 ids are then sorted ascending. Rows the bins cannot split (all scores equal,
 // no finite range, or more than 4096 candidates in one bin) take an exact three-digit
 // radix select on the 32-bit score keys instead.
+//
+// Two more modes serve the fused prefill selection (qsa_prefill_select): in candidate mode
+// a row's candidates come from the scoring epilogue (every score at or above a floor that
+// at least 512 scores reach, already in ascending block order), so the top 512 are the
+// keys at or above the 512th largest, compacted in order with no sort; rows whose
+// candidates overflowed are flagged. In fallback mode only the flagged rows run, streaming
+// the full scores as above.
 #include "qsa_internal.cuh"
 
 #include <float.h>
