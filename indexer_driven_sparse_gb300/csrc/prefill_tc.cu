@@ -76,7 +76,8 @@ constexpr uint32_t kPlLists = 0;                                           // in
 constexpr uint32_t kPlStart = kPlLists + 4 * kTcMaxQt * kBlockTopK;        // uint16 [QT][intervals + 1]
 constexpr uint32_t kPlCounts = kPlStart + 2 * kTcMaxQt * kStartStride;     // int32 [intervals + 1]
 constexpr uint32_t kPlMasks = kPlCounts + 4 * (kTcMaxIntervals + 8);       // uint16 [warp][2048]
-constexpr uint32_t kPlSmem = kPlMasks + 2 * kTcMaxBpi * kPlanWarps;
+constexpr uint32_t kPlBits = kPlMasks + 2 * kTcMaxBpi * kPlanWarps;         // uint32 [warp][64]: marked blocks
+constexpr uint32_t kPlSmem = kPlBits + 4 * (kTcMaxBpi / 32) * kPlanWarps;
 
 static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint16_t *m = reinterpret_cast<uint16_t *>(psm + kPlMasks) + warp * kTcMaxBpi;
+    uint32_t *bits = reinterpret_cast<uint32_t *>(psm + kPlBits) + warp * (kTcMaxBpi / 32);
     const int qt = blockIdx.x, QT = a.QT;
     const int i0 = qt * QT, nq = min(QT, a.Nc - i0);
     const int nb_last = (a.p0 + i0 + nq - 1) >> 2;
@@ -226,24 +228,24 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
         const int span = min(b_lo + a.bpi, nb_last + 1) - b_lo;
         uint4 *m4 = reinterpret_cast<uint4 *>(m);
         for (int i = lane; i < kTcMaxBpi / 8; i += 32) m4[i] = make_uint4(0, 0, 0, 0);
+        bits[lane] = 0u;
+        bits[lane + 32] = 0u;
         __syncwarp();
+        // per block: which of the tile's queries take it (mask), and that it is marked (bit)
+        auto mark_one = [&](int i, uint32_t q_bit) {
+            sel_or(m, i, q_bit);
+            atomicOr(&bits[i >> 5], 1u << (i & 31));
+        };
         for (int qq = 0; qq < nq; ++qq) {
             const int e0 = start[qq * kStartStride + v], e1 = start[qq * kStartStride + v + 1];
-            for (int i = e0 + lane; i < e1; i += 32) sel_or(m, lists[qq * kBlockTopK + i] - b_lo, 1u << qq);
+            for (int i = e0 + lane; i < e1; i += 32) mark_one(lists[qq * kBlockTopK + i] - b_lo, 1u << qq);
         }
         if (lane < nq) {
             const int nbq = s_p[lane] >> 2;
-            if (nbq >= b_lo && nbq - b_lo < span) sel_or(m, nbq - b_lo, 1u << lane);   // own block
+            if (nbq >= b_lo && nbq - b_lo < span) mark_one(nbq - b_lo, 1u << lane);   // own block
         }
         __syncwarp();
-        // marked blocks: 8 masks per 16-byte load (entries past the span are never marked)
-        int nu = 0;
-        for (int i = lane; i < (span + 7) / 8; i += 32) {
-            const uint4 w = m4[i];
-            nu += ((w.x & 0xFFFFu) != 0) + ((w.x >> 16) != 0) + ((w.y & 0xFFFFu) != 0) + ((w.y >> 16) != 0) +
-                  ((w.z & 0xFFFFu) != 0) + ((w.z >> 16) != 0) + ((w.w & 0xFFFFu) != 0) + ((w.w >> 16) != 0);
-        }
-        return (int)__reduce_add_sync(0xffffffffu, (unsigned)nu);
+        return (int)__reduce_add_sync(0xffffffffu, (unsigned)(__popc(bits[lane]) + __popc(bits[lane + 32])));
     };
 
     // ---- pass 1: union blocks per interval
@@ -304,47 +306,36 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PlanArgs a) 
     // ---- pass 2: every marked block at its position in the tile's union
     for (int v = warp; v < n_iv_tile; v += kPlanWarps) {
         const int b_lo = v * a.bpi;
-        const int span = min(b_lo + a.bpi, nb_last + 1) - b_lo;
         mark(v);
         const int off = counts[v];             // union blocks of the earlier intervals
-        // the marked blocks in ascending order, 8 masks per lane and 256 per sweep: a warp scan
-        // of the lanes' counts places each block in its chunk and slot
-        const int n4 = (span + 7) / 8;
-        int cur = 0;
-        for (int i0 = 0; i0 < n4; i0 += 32) {
-            const int i4 = i0 + lane;
-            uint32_t mw[8];
-            {
-                const uint4 w = i4 < n4 ? reinterpret_cast<const uint4 *>(m)[i4] : make_uint4(0, 0, 0, 0);
-                mw[0] = w.x & 0xFFFFu; mw[1] = w.x >> 16; mw[2] = w.y & 0xFFFFu; mw[3] = w.y >> 16;
-                mw[4] = w.z & 0xFFFFu; mw[5] = w.z >> 16; mw[6] = w.w & 0xFFFFu; mw[7] = w.w >> 16;
-            }
-            int cnt = 0;
+        // the marked blocks in ascending order: lane l takes the bit words 2 l and 2 l + 1
+        // (blocks [64 l, 64 l + 64) of the interval); a warp scan of their counts places each
+        const uint32_t w0 = bits[2 * lane], w1 = bits[2 * lane + 1];
+        const int cnt = __popc(w0) + __popc(w1);
+        int incl = cnt;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) cnt += mw[k] != 0;
-            int incl = cnt;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int pos = off + incl - cnt;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            int pos = cur + incl - cnt;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (mw[k] == 0) continue;
-                ChunkRec *r = out + (off + pos) / kTcBlocksPerChunk;
-                const int slot = (off + pos) % kTcBlocksPerChunk, b = b_lo + 8 * i4 + k;
+        for (int h = 0; h < 2; ++h) {
+            for (uint32_t bb = h ? w1 : w0; bb != 0u; bb &= bb - 1u) {
+                const int i = 64 * lane + 32 * h + __ffs(bb) - 1;
+                const uint32_t mk = m[i];
+                ChunkRec *r = out + pos / kTcBlocksPerChunk;
+                const int slot = pos % kTcBlocksPerChunk, b = b_lo + i;
                 r->blk[slot] = b;
-                for (uint32_t mm = mw[k]; mm != 0; mm &= mm - 1u) {
+                for (uint32_t mm = mk; mm != 0; mm &= mm - 1u) {
                     const int qq = __ffs(mm) - 1;
-                    uint32_t bits = 0xFu;
+                    uint32_t vbits = 0xFu;
                     const int p = s_p[qq];
-                    if ((p >> 2) == b) bits = (1u << ((p & 3) + 1)) - 1u;   // its own block: up to itself
-                    atomicOr(&r->vis[qq][slot >> 3], bits << ((slot & 7) * 4));
+                    if ((p >> 2) == b) vbits = (1u << ((p & 3) + 1)) - 1u;   // its own block: up to itself
+                    atomicOr(&r->vis[qq][slot >> 3], vbits << ((slot & 7) * 4));
                 }
                 ++pos;
             }
-            cur += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
     if (tid == 0) a.n_chunks[qt] = total;
