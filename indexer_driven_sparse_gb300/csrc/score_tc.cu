@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
                 // selection passes: the row's 64-block maxima, or its scores at or above the floor
                 // as 64-bit keys (score key, then the lower block id first) in the tile's slots
                 const float T = T_row;
-                uint64_t *slot = a.slots + (((size_t)row * a.n_n + n) * 2 + half) * kSelSlots;
+                uint64_t *slot = a.mode == 2 ? a.slots + (((size_t)row * a.n_n + n) * 2 + half) * kSelSlots : nullptr;
                 float gm = -INFINITY;
                 uint32_t k = 0;
                 auto process = [&](const float (&v)[32], int c) {

@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kTopkThreads, 3) topk_rows_kernel(const float 
         if (tid == 0) count[row] = (int32_t)nb;
         return;
     }
-    const float *s = scores + (int64_t)row * ld;
+    const float *s = scores != nullptr ? scores + (int64_t)row * ld : nullptr;   // none in candidate mode
     const unsigned lt = (1u << lane) - 1u;
 
     // Exact top 512 of nc candidate keys in cand[] (512 <= nc <= kCandCap): 1024 bins linear in
