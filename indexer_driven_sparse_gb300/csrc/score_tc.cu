@@ -230,14 +230,13 @@ __global__ void __launch_bounds__(kStThreads, 1)
                         for (int j = 0; j < 32; ++j) msk |= v[j] >= T ? (1u << j) : 0u;
                         if (lim < 32) msk &= (1u << lim) - 1u;   // lim < 32 here: the visible columns only
                     }
-                    if (__any_sync(0xffffffffu, msk != 0)) {
-                        // the slice's values through shared memory (16-byte granules XOR-swizzled by
-                        // row), so the set bits pick them by index
+                    if (msk != 0u) {
+                        // this row's values through its own row of shared memory (16-byte granules
+                        // XOR-swizzled by row), so the set bits pick them by index
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             *reinterpret_cast<float4 *>(xs + lane * 32 + 4 * (q ^ (lane & 7))) =
                                 make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                        __syncwarp();
                         for (; msk != 0u; msk &= msk - 1u) {
                             const int jj = __ffs(msk) - 1;
                             if (k < (uint32_t)kSelSlots)
@@ -246,7 +245,6 @@ __global__ void __launch_bounds__(kStThreads, 1)
                                           (uint64_t)(0xFFFFFFFFu - (uint32_t)(cb + jj));
                             ++k;
                         }
-                        __syncwarp();
                     }
                 };
                 // slices two at a time: the next slice's TMEM load is in flight while one is processed
