@@ -38,6 +38,7 @@ __all__ = [
     "score_blocks", "kth_score", "select_blocks", "attended_tokens",
     "attend_partial", "lse_merge", "attend", "decode_query",
     "interval_walk_query", "score_error_bound",
+    "E4M3_MAX", "e4m3_round", "quantize_pooled_fp8", "score_blocks_fp8", "decode_query_fp8",
 ]
 
 # indexer_compress_ratio and indexer_budget from the model's text_config
@@ -116,6 +117,58 @@ def visible_blocks(p: int) -> int:
     if p < 0:
         raise ValueError("p must be >= 0")
     return p // COMPRESS_RATIO
+
+
+# --------------------------------------------------------------------------- FP8 indexer keys
+
+# FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; the all-ones exponent with
+# mantissa 7 is NaN, so the largest finite value is 1.75 * 2^8): the "128 FP8 + 4 B scale"
+# indexer key of the page "GLM-5.3 最適化 第2部" (footnote on the indexer cache).
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Nearest E4M3 value of each input (ties to the even mantissa), saturating at +-448.
+
+    In the binade [2^k, 2^(k+1)) the E4M3 values are 2^(k-3) apart (3 mantissa bits); below
+    the smallest normal 2^-6 the subnormals are 2^-9 apart. The quotient by the spacing is
+    exact in float64, so rint (half to even) gives the round-to-nearest-even value.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))           # a = m 2^e, m in [0.5, 1): binade k = e - 1
+    k = np.maximum(e - 1, -6)
+    q = np.ldexp(1.0, k - 3)
+    r = np.minimum(np.rint(a / q) * q, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def quantize_pooled_fp8(pooled_bits):
+    """Per pooled block: scale = max |key| / 448 and codes = E4M3(key / scale).
+
+    Reading (the pages give the format, not the arithmetic): the scale and the quotient are
+    single float32 operations (an IEEE division rounded to nearest), the code is the
+    nearest E4M3 value of the float32 quotient; an all-zero key has scale 0 and zero codes.
+    Returns (values [nb, idx_dim] float64 of the codes, scales [nb] float32).
+    """
+    pk = bf16_bits_to_f64(pooled_bits)
+    if pk.ndim == 1:
+        pk = pk[None, :]
+    amax = np.abs(pk).max(axis=1) if pk.shape[0] else np.zeros(0)
+    scale = (amax.astype(np.float32) / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    quot = (pk.astype(np.float32) / safe[:, None]).astype(np.float32)
+    vals = e4m3_round(quot)
+    vals[scale == 0] = 0.0
+    return vals, scale
+
+
+def score_blocks_fp8(q_idx_bits: np.ndarray, vals: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Indexer score against FP8 keys: s_b = scale_b * (q_idx . codes_b), in float64."""
+    q = bf16_bits_to_f64(q_idx_bits)
+    if vals.shape[0] == 0:
+        return np.zeros(0, dtype=np.float64)
+    return (vals @ q) * scales.astype(np.float64)
 
 
 # --------------------------------------------------------------------------- scoring
@@ -288,6 +341,19 @@ def decode_query(p: int, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_kv_h
     # attend over the compacted rows (row j of kk is token tokens[j])
     out, lse = attend(q, kk, vv, np.arange(tokens.size), n_kv_heads, scale)
     return dict(scores=scores, sel=np.asarray(sel, dtype=np.int64), tokens=tokens, out=out, lse=lse)
+
+
+def decode_query_fp8(p: int, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_kv_heads: int,
+                     scale: float | None = None, k_blocks: int = BLOCK_TOPK, sel=None):
+    """decode_query with the selection scored against FP8 copies of the pooled keys."""
+    nb = visible_blocks(p)
+    vals, scl = quantize_pooled_fp8(np.asarray(pooled_bits)[:nb])
+    scores = score_blocks_fp8(q_idx_bits, vals, scl)
+    if sel is None:
+        sel = select_blocks(scores, k_blocks)
+    r = decode_query(p, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_kv_heads, scale, k_blocks, sel=sel)
+    r["scores"] = scores
+    return r
 
 
 def interval_walk_query(p: int, sel, q_bits, k_bits, v_bits, n_kv_heads: int,

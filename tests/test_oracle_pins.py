@@ -349,3 +349,80 @@ def test_tiny_worked_example():
     want_lse = np.array([_closed_form(x) for x in g["expect_lse"]])
     np.testing.assert_allclose(r["out"], want_out, rtol=1e-14, atol=1e-14)
     np.testing.assert_allclose(r["lse"], want_lse, rtol=1e-14)
+
+
+# --------------------------------------------------------------------------- FP8 indexer keys
+
+def _e4m3_table():
+    """Every finite non-negative E4M3 value with its mantissa field, from the bit layout:
+    exponent field e (bias 7) and mantissa m; e = 0 subnormal (m/8) 2^-6; e = 15, m = 7 NaN."""
+    out = {}
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue
+            v = (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+            out[v] = m
+    vals = sorted(out)
+    return np.array(vals), np.array([out[v] for v in vals])
+
+
+def test_e4m3_table_constants():
+    vals, _ = _e4m3_table()
+    assert vals.max() == O.E4M3_MAX == 448.0
+    assert vals[1] == 2.0 ** -9                     # smallest subnormal
+    assert 2.0 ** -6 in vals and vals.size == 127   # 126 non-zero values and zero
+
+
+def test_e4m3_round_fixed_points_midpoints_and_saturation():
+    vals, mant = _e4m3_table()
+    for sign in (1.0, -1.0):
+        np.testing.assert_array_equal(O.e4m3_round(sign * vals), sign * vals)
+    mid = (vals[:-1] + vals[1:]) / 2                # ties: to the even mantissa
+    want = np.where(mant[:-1] % 2 == 0, vals[:-1], vals[1:])
+    np.testing.assert_array_equal(O.e4m3_round(mid), want)
+    eps = np.minimum(np.diff(vals) / 8, 1.0)
+    np.testing.assert_array_equal(O.e4m3_round(mid - eps), vals[:-1])
+    np.testing.assert_array_equal(O.e4m3_round(mid + eps), vals[1:])
+    np.testing.assert_array_equal(O.e4m3_round([449.0, 464.0, 1e9, -1e9]), [448.0, 448.0, 448.0, -448.0])
+
+
+def test_e4m3_round_is_the_nearest_table_value():
+    vals, mant = _e4m3_table()
+    rng = np.random.default_rng(41)
+    x = np.exp(rng.uniform(np.log(2.0 ** -12), np.log(440.0), 5000)) * rng.choice([-1.0, 1.0], 5000)
+    full = np.concatenate([-vals[::-1], vals[1:]])
+    for xi, r in zip(x, O.e4m3_round(x)):
+        d = np.abs(full - xi)
+        assert r == full[np.argmin(d)] or np.isclose(d.min(), np.sort(d)[1])   # ties are pinned above
+
+
+def test_quantize_pooled_fp8_cases():
+    # the largest magnitude maps to 448, an all-zero key to scale 0, every value within half a
+    # mantissa step (2^-4 relative) of the key where it is a normal E4M3 value
+    rng = np.random.default_rng(43)
+    keys = torch.from_numpy(rng.standard_normal((64, 128)).astype(np.float32) / 8).bfloat16().float().numpy()
+    keys[5] = 0.0
+    bits = to_bits(keys)
+    vals, scales = O.quantize_pooled_fp8(bits)
+    exact = O.bf16_bits_to_f64(bits)
+    assert scales.dtype == np.float32 and scales[5] == 0 and not vals[5].any()
+    rows = [r for r in range(64) if r != 5]
+    np.testing.assert_array_equal(np.abs(vals[rows]).max(axis=1), 448.0)
+    deq = vals[rows] * scales[rows, None].astype(np.float64)
+    big = np.abs(exact[rows]) >= 2.0 ** -6 * scales[rows, None] * 1.01
+    rel = np.abs(deq - exact[rows])[big] / np.abs(exact[rows])[big]
+    assert rel.max() <= 2.0 ** -4 * (1 + 1e-6)
+
+
+def test_score_blocks_fp8_one_hot_and_linearity():
+    q = np.zeros(128, np.float32)
+    q[7] = 3.0
+    key = np.zeros((2, 128), np.float32)
+    key[0, 7] = -0.5
+    key[1, 7] = 2.0
+    key[1, 9] = 1.0
+    vals, scl = O.quantize_pooled_fp8(to_bits(key))
+    s = O.score_blocks_fp8(to_bits(q), vals, scl)
+    assert s[0] == 3.0 * -448.0 * float(np.float32(0.5) / np.float32(448.0))
+    assert s[1] == 3.0 * 448.0 * float(np.float32(2.0) / np.float32(448.0))
