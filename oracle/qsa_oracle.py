@@ -39,6 +39,7 @@ __all__ = [
     "attend_partial", "lse_merge", "attend", "decode_query",
     "interval_walk_query", "score_error_bound",
     "E4M3_MAX", "e4m3_round", "quantize_pooled_fp8", "score_blocks_fp8", "decode_query_fp8",
+    "score_error_bound_fp8",
 ]
 
 # indexer_compress_ratio and indexer_budget from the model's text_config
@@ -169,6 +170,25 @@ def score_blocks_fp8(q_idx_bits: np.ndarray, vals: np.ndarray, scales: np.ndarra
     if vals.shape[0] == 0:
         return np.zeros(0, dtype=np.float64)
     return (vals @ q) * scales.astype(np.float64)
+
+
+def score_error_bound_fp8(q_idx_bits: np.ndarray, vals: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Worst-case error of an FP8-key score computed as fl(scale * fl(sum_d q_d c_d)) in fp32.
+
+    A bf16 value times an E4M3 value is exact in fp32 (8 + 4 significant bits), so the sum
+    errs by at most gamma_n * sum_d |q_d c_d| (Higham ch. 3), and the final product by one
+    rounding of the result, u |scale * s~|. Used only to grade GPU scores and label swaps.
+    """
+    q = np.abs(bf16_bits_to_f64(q_idx_bits))
+    if vals.shape[0] == 0:
+        return np.zeros(0, dtype=np.float64)
+    n = q.shape[0]
+    u = 2.0 ** -24
+    gamma = n * u / (1.0 - n * u)
+    a = np.abs(vals) @ q
+    d = np.abs(vals @ bf16_bits_to_f64(q_idx_bits))
+    sc = scales.astype(np.float64)
+    return sc * (gamma * a + u * (d + gamma * a))
 
 
 # --------------------------------------------------------------------------- scoring

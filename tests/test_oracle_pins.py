@@ -426,3 +426,28 @@ def test_score_blocks_fp8_one_hot_and_linearity():
     s = O.score_blocks_fp8(to_bits(q), vals, scl)
     assert s[0] == 3.0 * -448.0 * float(np.float32(0.5) / np.float32(448.0))
     assert s[1] == 3.0 * 448.0 * float(np.float32(2.0) / np.float32(448.0))
+
+
+def test_score_error_bound_fp8_covers_an_fp32_evaluation():
+    # the bound must cover a float32 evaluation of the same score in any summation order:
+    # sequential, pairwise and reversed sums of the exact products, then the scale product
+    rng = np.random.default_rng(47)
+    keys = torch.from_numpy(rng.standard_normal((200, 128)).astype(np.float32) / 8).bfloat16().float().numpy()
+    q = torch.from_numpy(rng.standard_normal(128).astype(np.float32)).bfloat16().float().numpy()
+    vals, scl = O.quantize_pooled_fp8(to_bits(keys))
+    exact = O.score_blocks_fp8(to_bits(q), vals, scl)
+    bound = O.score_error_bound_fp8(to_bits(q), vals, scl)
+    prods = (vals.astype(np.float32) * q[None, :]).astype(np.float32)     # exact in float32
+    assert np.array_equal(prods.astype(np.float64), vals * q[None, :].astype(np.float64))
+    for order in (slice(None), slice(None, None, -1)):
+        acc = np.zeros(200, np.float32)
+        for d in range(128)[order]:
+            acc = (acc + prods[:, d]).astype(np.float32)
+        got = (acc * scl).astype(np.float32).astype(np.float64)
+        assert np.all(np.abs(got - exact) <= bound)
+    pw = prods.copy()
+    while pw.shape[1] > 1:
+        pw = (pw[:, 0::2] + pw[:, 1::2]).astype(np.float32)
+    got = (pw[:, 0] * scl).astype(np.float32).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= bound)
+    assert np.all(bound > 0) and np.all(bound <= 1e-5 * (np.abs(vals) @ np.abs(q)) * scl + 1e-30)
