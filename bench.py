@@ -51,6 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kv-host", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-instrument", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -433,6 +434,60 @@ def kv_host_bench(dl, stream, steps, warmup, n_layers=2):
             "note": "K/V and raw indexer keys in pinned host memory; pooled keys in HBM"}
 
 
+def fp8_keys_bench(dl, stream, steps, warmup, pk):
+    """Decode with FP8 indexer keys (128 E4M3 codes + one fp32 scale per pooled block): per
+    layer, re-pool the newest block into codes, then score -> top-k -> attention as separate
+    calls; and each scan alone (FP8 and bf16 keys) over the same 12 layers."""
+    import torch
+    from indexer_driven_sparse_gb300 import accounting as A
+    from indexer_driven_sparse_gb300 import binding as qb
+    b, layers = dl.b, dl.w.layers
+    keys = []
+    for L in layers:
+        codes, scales = b.new_fp8_keys()
+        b.pool_fp8(L.raw_idx_k, codes, scales)
+        keys.append((codes, scales))
+    torch.cuda.synchronize()
+
+    def step():
+        for l, L in enumerate(layers):
+            codes, scales = keys[l]
+            qb.qsa_pool_keys_fp8(b.cfg, L.raw_idx_k, b.tok_off, b.blk_off, dl.inc_begin, dl.inc_end, 1, codes,
+                                 scales, b.ws)
+            b.step_fp8(L.q_idx, L.q, L.k_cache, L.v_cache, codes, scales)
+
+    def scan_fp8():
+        for l, L in enumerate(layers):
+            b.score_fp8(L.q_idx, *keys[l])
+
+    def scan_bf16():
+        for l, L in enumerate(layers):
+            b.score(L.q_idx, dl.pooled[l])
+
+    us = {}
+    for name, fn in (("step", step), ("scan_fp8", scan_fp8), ("scan_bf16", scan_bf16)):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        st = b.device_status()
+        if st[0] != 0:
+            raise RuntimeError(f"device status in the FP8 leg ({name}): {st}")
+        g = capture(fn, stream)
+        t = time_graph(g, stream, steps, warmup, 1)
+        del g
+        us[name] = 1e6 * t / (steps * len(layers))
+    ctx = dl.w.ctx_len
+    b8, b16 = A.score_scan_bytes_fp8(ctx), A.score_scan_bytes(ctx)
+    g8 = b8 / (us["scan_fp8"] * 1e-6) / 1e9
+    g16 = b16 / (us["scan_bf16"] * 1e-6) / 1e9
+    return {"path": "separate calls: pool_fp8 (newest block), score_fp8, topk, attention + merge",
+            "layer_steps_per_s": 1e6 / us["step"], "us_per_layer_step": us["step"],
+            "scan_fp8_us": us["scan_fp8"], "scan_fp8_bytes": b8, "scan_fp8_gbs": g8,
+            "scan_fp8_frac": g8 / pk["hbm"], "scan_bf16_us": us["scan_bf16"], "scan_bf16_bytes": b16,
+            "scan_bf16_gbs": g16, "scan_bf16_frac": g16 / pk["hbm"], "peak_src": pk["src"],
+            "gpu_launches_per_layer_step": 5}
+
+
 # ----------------------------------------------------------------------------- prefill
 
 def prefill_bench(steps, warmup, pk):
@@ -730,6 +785,10 @@ def main(argv=None):
 
     if not args.no_kv_host:
         line["decode_kv_in_host_memory"] = kv_host_bench(dl, stream, max(20, args.steps // 4), max(3, args.warmup))
+
+    if not args.no_fp8:
+        line["decode_fp8_indexer_keys"] = fp8_keys_bench(dl, stream, max(20, args.steps // 4), max(3, args.warmup),
+                                                         pk)
 
     if not args.no_prefill:
         del g

@@ -152,6 +152,36 @@ QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx,
                                    int64_t n_pooled_total, const int32_t *blk_off, float *scores, int64_t ld,
                                    void *ws, size_t ws_bytes, qsa_stream stream);
 
+/* a1 with FP8 keys — pooled indexer keys stored as 128 FP8 (E4M3) codes plus one fp32 scale
+ * per block ("GLM-5.3 最適化 第2部：16基のH200上でのPCP、DCP、およびHybrid HiSparse", footnote on
+ * the indexer cache: 128 FP8 values and a 4-byte scale per key), so the scan of every pooled
+ * block reads 132 bytes instead of 256. For each block the call first forms the bf16 pooled
+ * key exactly as qsa_pool_keys does (key[d]), then
+ *   scales[i] = amax / 448 (fp32 IEEE division, amax = max_d |key[d]|),
+ *   codes[i][d] = E4M3(key[d] / scales[i]) (fp32 IEEE division; nearest, ties to even;
+ *                 saturating at +-448),
+ * with i = blk_off[s] + b; a block whose key is all zero (scale 0) gets zero codes.
+ *   codes [n_pooled_total, idx_dim] uint8 (written), 16-byte aligned;
+ *   scales [n_pooled_total] fp32 (written), 4-byte aligned.
+ * Other arguments, the workspace (QSA_OP_POOL_KEYS) and the device checks as qsa_pool_keys. */
+QSA_API qsa_status qsa_pool_keys_fp8(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, int64_t n_tokens_total,
+                                     const int32_t *tok_off, const int32_t *blk_off, const int32_t *blk_begin,
+                                     const int32_t *blk_end, int32_t B, int64_t max_blocks_per_seq, uint8_t *codes,
+                                     float *scales, int64_t n_pooled_total, void *ws, size_t ws_bytes,
+                                     qsa_stream stream);
+
+/* a2 with FP8 keys — indexer scores against the keys qsa_pool_keys_fp8 writes. For query r
+ * with nb = q_pos[r] / 4 and i = blk_off[q_seq[r]] + b:
+ *   scores[r * ld + b] = scales[i] * sum_d q_idx[r][d] * codes[i][d],  b < nb,
+ * with exact products and an fp32 sum, then one fp32 multiply by the scale. Entries b >= nb
+ * are not written. q_seq may be NULL (every query in sequence 0). One query at a time (an
+ * HBM stream; no tensor-core path). Workspace QSA_OP_INDEX_SCORE. Device checks: nb <= ld,
+ * blk_off[s] + nb <= n_pooled_total. The scores feed qsa_topk_blocks unchanged. */
+QSA_API qsa_status qsa_index_score_fp8(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_seq,
+                                       const int32_t *q_pos, int32_t Nq, const uint8_t *codes, const float *scales,
+                                       int64_t n_pooled_total, const int32_t *blk_off, float *scores, int64_t ld,
+                                       void *ws, size_t ws_bytes, qsa_stream stream);
+
 /* a2 + a3 fused for a prefill chunk (one sequence, q_seq NULL): the same blocks and counts
  * as qsa_index_score followed by qsa_topk_blocks, without writing the score matrix
  * ("GLM-5.3 最適化 第2部": prefill scoring is quadratic; "なぜ": top-512 per query). The

@@ -57,6 +57,13 @@ def score_scan_bytes(ctx_lens, idx_dim: int = 128) -> int:
     return sum(pooled_scan_bytes(visible_blocks(p), idx_dim) + idx_dim * BF16 for p in ctx_lens)
 
 
+def score_scan_bytes_fp8(ctx_lens, idx_dim: int = 128) -> int:
+    """Bytes the scan over FP8 indexer keys must read: per visible block 128 one-byte codes
+    and a 4-byte scale (the "128 FP8 + 4 B scale" key of "GLM-5.3 最適化 第2部", footnote on
+    the indexer cache), plus the bf16 indexer query."""
+    return sum(visible_blocks(p) * (idx_dim + 4) + idx_dim * BF16 for p in ctx_lens)
+
+
 def prefill_attention_flops(p0: int, n_chunk: int, n_q_heads: int = 16, head_dim: int = 256) -> int:
     """QK^T + PV FLOPs over each chunk query's own selection (2 per multiply-add)."""
     return sum(attended(p0 + i) for i in range(n_chunk)) * n_q_heads * head_dim * 2 * 2

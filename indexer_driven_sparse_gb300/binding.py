@@ -65,6 +65,8 @@ _SIGNATURES = {
     "qsa_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "qsa_copy_rows": (_I32, [_P, _SZ, _P, _SZ, _SZ, _SZ, _P]),
     "qsa_prefill_select": (_I32, [_CFG, _P, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
+    "qsa_pool_keys_fp8": (_I32, [_CFG, _P, _I64, _P, _P, _P, _P, _I32, _I64, _P, _P, _I64, _P, _SZ, _P]),
+    "qsa_index_score_fp8": (_I32, [_CFG, _P, _P, _P, _I32, _P, _P, _I64, _P, _P, _I64, _P, _SZ, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
     "qsa_last_error": (C.c_char_p, []),
     "qsa_version": (C.c_char_p, []),
@@ -168,6 +170,29 @@ def qsa_index_score(cfg, q_idx, q_seq, q_pos, pooled, blk_off, scores, ws, strea
                                   _ptr(q_pos, torch.int32), q_idx.shape[0], _ptr(pooled, torch.bfloat16, "pooled"),
                                   pooled.shape[0], _ptr(blk_off, torch.int32), _ptr(scores, torch.float32, "scores"),
                                   scores.shape[1], *_ws_args(ws), _stream(stream)), "qsa_index_score")
+
+
+def qsa_pool_keys_fp8(cfg, raw_idx_k, tok_off, blk_off, blk_begin, blk_end, max_blocks_per_seq, codes, scales, ws,
+                      stream=None):
+    B = tok_off.numel() - 1
+    if codes.shape[0] != scales.shape[0]:
+        raise ValueError("codes and scales must have one row per pooled block")
+    _check(load().qsa_pool_keys_fp8(C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"), raw_idx_k.shape[0],
+                                    _ptr(tok_off, torch.int32), _ptr(blk_off, torch.int32),
+                                    _ptr(blk_begin, torch.int32), _ptr(blk_end, torch.int32), B,
+                                    int(max_blocks_per_seq), _ptr(codes, torch.uint8, "codes"),
+                                    _ptr(scales, torch.float32, "scales"), codes.shape[0], *_ws_args(ws),
+                                    _stream(stream)), "qsa_pool_keys_fp8")
+
+
+def qsa_index_score_fp8(cfg, q_idx, q_seq, q_pos, codes, scales, blk_off, scores, ws, stream=None):
+    if codes.shape[0] != scales.shape[0]:
+        raise ValueError("codes and scales must have one row per pooled block")
+    _check(load().qsa_index_score_fp8(C.byref(cfg), _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(q_seq, torch.int32),
+                                      _ptr(q_pos, torch.int32), q_idx.shape[0], _ptr(codes, torch.uint8, "codes"),
+                                      _ptr(scales, torch.float32, "scales"), codes.shape[0],
+                                      _ptr(blk_off, torch.int32), _ptr(scores, torch.float32, "scores"),
+                                      scores.shape[1], *_ws_args(ws), _stream(stream)), "qsa_index_score_fp8")
 
 
 def qsa_prefill_select(cfg, q_idx, q_pos, pooled, blk_off, scores, blocks, count, ws, stream=None):

@@ -201,6 +201,47 @@ QSA_API qsa_status qsa_index_score(const qsa_config *cfg, const qsa_bf16 *q_idx,
     return ok();
 }
 
+QSA_API qsa_status qsa_pool_keys_fp8(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, int64_t n_tokens_total,
+                                     const int32_t *tok_off, const int32_t *blk_off, const int32_t *blk_begin,
+                                     const int32_t *blk_end, int32_t B, int64_t max_blocks_per_seq, uint8_t *codes,
+                                     float *scales, int64_t n_pooled_total, void *ws, size_t ws_bytes,
+                                     qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(B >= 0 && B <= kMaxGridYZ, "B = %d out of range [0, 65535]", B);
+    QSA_NEED(n_tokens_total >= 0 && n_pooled_total >= 0 && max_blocks_per_seq >= 0, "negative size");
+    QSA_NEED(max_blocks_per_seq <= (int64_t)1 << 28, "max_blocks_per_seq too large");
+    QSA_TRY(check_ws(QSA_OP_POOL_KEYS, cfg, B, max_blocks_per_seq, ws, ws_bytes));
+    if (B == 0 || max_blocks_per_seq == 0) return ok();
+    QSA_NEED(raw_idx_k && codes && scales && tok_off && blk_off && blk_begin && blk_end, "NULL tensor pointer");
+    QSA_NEED(aligned(raw_idx_k, 16) && aligned(codes, 16), "raw_idx_k and codes must be 16-byte aligned");
+    QSA_NEED(aligned(scales, 4), "scales must be 4-byte aligned");
+    const cudaError_t e = launch_pool_keys_fp8(raw_idx_k, n_tokens_total, tok_off, blk_off, blk_begin, blk_end, B,
+                                               max_blocks_per_seq, codes, scales, n_pooled_total,
+                                               static_cast<WsHeader *>(ws), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pool_keys_fp8 launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_index_score_fp8(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_seq,
+                                       const int32_t *q_pos, int32_t Nq, const uint8_t *codes, const float *scales,
+                                       int64_t n_pooled_total, const int32_t *blk_off, float *scores, int64_t ld,
+                                       void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(Nq >= 0 && Nq <= kMaxGridYZ, "Nq = %d out of range [0, 65535]", Nq);
+    QSA_NEED(ld >= 0 && n_pooled_total >= 0, "negative size");
+    QSA_NEED(ld <= (int64_t)1 << 28, "ld too large");
+    QSA_TRY(check_ws(QSA_OP_INDEX_SCORE, cfg, Nq, ld, ws, ws_bytes));
+    if (Nq == 0 || ld == 0) return ok();
+    QSA_NEED(q_idx && q_pos && codes && scales && blk_off && scores, "NULL tensor pointer");
+    QSA_NEED(aligned(q_idx, 16) && aligned(codes, 16), "q_idx and codes must be 16-byte aligned");
+    QSA_NEED(aligned(scales, 4) && aligned(scores, 4), "scales and scores must be 4-byte aligned");
+    const cudaError_t e = launch_index_score_fp8(q_idx, q_seq, q_pos, Nq, codes, scales, n_pooled_total, blk_off,
+                                                 scores, ld, static_cast<WsHeader *>(ws),
+                                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "index_score_fp8 launch");
+    return ok();
+}
+
 QSA_API qsa_status qsa_prefill_select(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_pos, int32_t Nq,
                                       const qsa_bf16 *pooled, int64_t n_pooled_total, const int32_t *blk_off,
                                       float *scores, int64_t ld, int32_t *blocks, int32_t *count, void *ws,

@@ -115,6 +115,15 @@ cudaError_t launch_index_score(const uint16_t *q_idx, const int32_t *q_seq, cons
                                const uint16_t *pooled, int64_t n_pooled, const int32_t *blk_off, float *scores,
                                int64_t ld, WsHeader *hdr, cudaStream_t st);
 
+// FP8 (E4M3) indexer keys with a per-block fp32 scale (fp8_keys.cu).
+cudaError_t launch_pool_keys_fp8(const uint16_t *raw, int64_t n_tok, const int32_t *tok_off, const int32_t *blk_off,
+                                 const int32_t *blk_begin, const int32_t *blk_end, int B, int64_t max_blocks,
+                                 uint8_t *codes, float *scales, int64_t n_pooled, WsHeader *hdr, cudaStream_t st);
+cudaError_t launch_index_score_fp8(const uint16_t *q_idx, const int32_t *q_seq, const int32_t *q_pos, int Nq,
+                                   const uint8_t *codes, const float *scales, int64_t n_pooled,
+                                   const int32_t *blk_off, float *scores, int64_t ld, WsHeader *hdr,
+                                   cudaStream_t st);
+
 size_t topk_scratch_bytes(int Nq, int64_t ld);
 // Tensor-core scoring of many queries of one sequence (score_tc.cu).
 bool score_tc_supported(int Nq, int64_t n_pooled);

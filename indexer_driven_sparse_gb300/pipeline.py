@@ -88,6 +88,26 @@ class DecodeBatch:
         self.topk(stream)
         self.attend(q, k_cache, v_cache, stream=stream)
 
+    def new_fp8_keys(self):
+        """Buffers of the FP8 indexer keys: codes [n_pooled, 128] uint8 and scales [n_pooled] fp32."""
+        n = max(self.n_pooled, 1)
+        return (torch.empty(n, 128, dtype=torch.uint8, device=self.device),
+                torch.empty(n, dtype=torch.float32, device=self.device))
+
+    def pool_fp8(self, raw_idx_k, codes, scales, stream=None):
+        qb.qsa_pool_keys_fp8(self.cfg, raw_idx_k, self.tok_off, self.blk_off, self.blk_begin, self.blk_end,
+                             self.max_blocks, codes, scales, self.ws, stream)
+
+    def score_fp8(self, q_idx, codes, scales, stream=None):
+        qb.qsa_index_score_fp8(self.cfg, q_idx, self.q_seq, self.ctx_len, codes, scales, self.blk_off, self.scores,
+                               self.ws, stream)
+
+    def step_fp8(self, q_idx, q, k_cache, v_cache, codes, scales, stream=None):
+        """One decode layer-step with FP8 indexer keys: score -> top-k -> sparse attention."""
+        self.score_fp8(q_idx, codes, scales, stream)
+        self.topk(stream)
+        self.attend(q, k_cache, v_cache, stream=stream)
+
     def device_status(self, stream=None):
         return qb.qsa_read_device_status(self.ws, stream)
 

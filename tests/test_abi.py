@@ -181,3 +181,29 @@ def test_prefill_select_host_checks(lib):
     need0 = lib.qsa_workspace_size(qb.OP_PREFILL_SELECT, C.byref(c), 0, 66560)
     assert lib.qsa_prefill_select(C.byref(c), FAKE, FAKE, 0, FAKE, 66560, FAKE, FAKE, 66560, FAKE, FAKE, FAKE,
                                   need0, 0) == qb.QSA_OK
+
+
+def test_fp8_key_calls_host_checks(lib):
+    # FP8 indexer keys: same validation as the bf16 calls, plus the code and scale buffers
+    c = cfg()
+    ws = FAKE
+    assert lib.qsa_pool_keys_fp8(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
+    assert lib.qsa_index_score_fp8(C.byref(c), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, ws, 256, 0) == qb.QSA_OK
+    # NULL scales, misaligned codes, misaligned scales
+    assert lib.qsa_pool_keys_fp8(C.byref(c), FAKE, 100, FAKE, FAKE, FAKE, FAKE, 1, 4, FAKE, 0, 25, ws, 256,
+                                 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_pool_keys_fp8(C.byref(c), FAKE, 100, FAKE, FAKE, FAKE, FAKE, 1, 4, FAKE + 8, FAKE, 25, ws, 256,
+                                 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"aligned" in lib.qsa_last_error()
+    assert lib.qsa_index_score_fp8(C.byref(c), FAKE, 0, FAKE, 1, FAKE, FAKE + 2, 10, FAKE, FAKE, 10, ws, 256,
+                                   0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"aligned" in lib.qsa_last_error()
+    # sizes and workspace
+    assert lib.qsa_index_score_fp8(C.byref(c), FAKE, 0, FAKE, -1, FAKE, FAKE, 10, FAKE, FAKE, 10, ws, 256, 0) == \
+        qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_pool_keys_fp8(C.byref(c), FAKE, 100, FAKE, FAKE, FAKE, FAKE, 70000, 4, FAKE, FAKE, 25, ws, 256,
+                                 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_index_score_fp8(C.byref(c), FAKE, 0, FAKE, 1, FAKE, FAKE, 10, FAKE, FAKE, 10, ws, 128, 0) == \
+        qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.qsa_index_score_fp8(C.byref(cfg(idx_dim=64)), FAKE, 0, FAKE, 1, FAKE, FAKE, 10, FAKE, FAKE, 10, ws,
+                                   256, 0) == qb.QSA_ERR_UNSUPPORTED

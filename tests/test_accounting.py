@@ -60,3 +60,11 @@ def test_workload_totals():
     assert A.prefill_score_flops(262144, 4096) == 256 * 270_530_560
     assert A.prefill_attention_flops(262144, 4096) / 1e9 == pytest.approx(137.6, abs=0.05)
     assert A.prefill_score_flops(262144, 4096) / 1e9 == pytest.approx(69.26, abs=0.01)
+
+
+def test_fp8_scan_bytes():
+    # 128 one-byte codes + a 4-byte scale per block: 132 of the bf16 key's 256 bytes
+    assert A.score_scan_bytes_fp8([1048320]) == 262080 * 132 + 256
+    assert A.score_scan_bytes_fp8([3]) == 256
+    bf16 = A.score_scan_bytes([1048320]) - 256
+    assert (A.score_scan_bytes_fp8([1048320]) - 256) / bf16 == 132 / 256
