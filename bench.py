@@ -464,12 +464,17 @@ def fp8_keys_bench(dl, stream, steps, warmup, pk):
         for l, L in enumerate(layers):
             b.score(L.q_idx, dl.pooled[l])
 
+    def fused():
+        for l, L in enumerate(layers):
+            codes, scales = keys[l]
+            b.fused_step_fp8(L.raw_idx_k, codes, scales, L.q_idx, L.q, L.k_cache, L.v_cache)
+
     us = {}
-    for name, fn in (("step", step), ("scan_fp8", scan_fp8), ("scan_bf16", scan_bf16)):
+    for name, fn in (("fused", fused), ("step", step), ("scan_fp8", scan_fp8), ("scan_bf16", scan_bf16)):
         with torch.cuda.stream(stream):
             fn()
         torch.cuda.synchronize()
-        st = b.device_status()
+        st = b.fused_status() if name == "fused" else b.device_status()
         if st[0] != 0:
             raise RuntimeError(f"device status in the FP8 leg ({name}): {st}")
         g = capture(fn, stream)
@@ -480,7 +485,12 @@ def fp8_keys_bench(dl, stream, steps, warmup, pk):
     b8, b16 = A.score_scan_bytes_fp8(ctx), A.score_scan_bytes(ctx)
     g8 = b8 / (us["scan_fp8"] * 1e-6) / 1e9
     g16 = b16 / (us["scan_bf16"] * 1e-6) / 1e9
-    return {"path": "separate calls: pool_fp8 (newest block), score_fp8, topk, attention + merge",
+    fb = A.decode_layer_step_bytes_fp8(ctx, 16)
+    fg = fb / (us["fused"] * 1e-6) / 1e9
+    return {"fused_layer_steps_per_s": 1e6 / us["fused"], "fused_us_per_layer_step": us["fused"],
+            "fused_algorithmic_bytes": fb, "fused_hbm_gbs_algorithmic": fg, "fused_frac": fg / pk["hbm"],
+            "path": "fused: qsa_decode_step_fp8 (one launch per layer-step); separate: pool_fp8 (newest block), "
+                    "score_fp8, topk, attention + merge",
             "layer_steps_per_s": 1e6 / us["step"], "us_per_layer_step": us["step"],
             "scan_fp8_us": us["scan_fp8"], "scan_fp8_bytes": b8, "scan_fp8_gbs": g8,
             "scan_fp8_frac": g8 / pk["hbm"], "scan_bf16_us": us["scan_bf16"], "scan_bf16_bytes": b16,

@@ -277,6 +277,27 @@ QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_id
                                    int64_t max_blocks, int32_t *blocks, int32_t *count, qsa_bf16 *out, float *lse,
                                    void *ws, size_t ws_bytes, qsa_stream stream);
 
+/* a1-a5 fused with FP8 keys — qsa_decode_step over the keys qsa_pool_keys_fp8 writes
+ * (128 E4M3 codes + an fp32 scale per block; "GLM-5.3 最適化 第2部：16基のH200上でのPCP、DCP、
+ * およびHybrid HiSparse", footnote on the indexer cache), so the scan reads 132 bytes per block
+ * instead of 256. For sequence s with p = ctx_len[s], nb = p / 4:
+ *   1. block blk_off[s] + nb - 1 is (re)pooled from raw_idx_k and quantised as by
+ *      qsa_pool_keys_fp8 (codes and scale written);
+ *   2. every block b < nb is scored as by qsa_index_score_fp8 (same products, fp32 sum order
+ *      and scale multiply, hence the same fp32 scores);
+ *   3.-4. selection and attention as in qsa_decode_step.
+ *   codes [n_pooled_total, idx_dim] uint8, 16-byte aligned; scales [n_pooled_total] fp32,
+ *   16-byte aligned. n_pooled_total must be a multiple of 4 (the scan copies whole
+ *   16-byte groups of scales): pad both arrays to it. Else QSA_ERR_INVALID_ARGUMENT.
+ * Other arguments, the workspace (QSA_OP_DECODE_STEP), limits and errors as qsa_decode_step. */
+QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, uint8_t *codes,
+                                       float *scales, int64_t n_pooled_total, const int32_t *blk_off,
+                                       const qsa_bf16 *q_idx, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                       const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
+                                       const int32_t *ctx_len, int32_t B, int64_t max_blocks, int32_t *blocks,
+                                       int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                       qsa_stream stream);
+
 /* Allocation-free variant of qsa_sparse_decode (the pages have no counterpart; this
  * is a library convenience). Same arguments and result, but no workspace: the split
  * partials live in a 16 MiB static device array inside the library, for callers that

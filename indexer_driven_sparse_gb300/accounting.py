@@ -64,6 +64,17 @@ def score_scan_bytes_fp8(ctx_lens, idx_dim: int = 128) -> int:
     return sum(visible_blocks(p) * (idx_dim + 4) + idx_dim * BF16 for p in ctx_lens)
 
 
+def decode_layer_step_bytes_fp8(ctx_lens, n_q_heads: int, n_kv_heads: int = 2, head_dim: int = 256,
+                                idx_dim: int = 128) -> int:
+    """decode_layer_step_bytes with the scan over FP8 indexer keys (idx_dim + 4 bytes per block)."""
+    total = 0
+    for p in ctx_lens:
+        total += visible_blocks(p) * (idx_dim + 4)
+        total += kv_read_bytes(attended(p), n_kv_heads, head_dim)
+        total += 2 * n_q_heads * head_dim * BF16 + idx_dim * BF16
+    return total
+
+
 def prefill_attention_flops(p0: int, n_chunk: int, n_q_heads: int = 16, head_dim: int = 256) -> int:
     """QK^T + PV FLOPs over each chunk query's own selection (2 per multiply-add)."""
     return sum(attended(p0 + i) for i in range(n_chunk)) * n_q_heads * head_dim * 2 * 2

@@ -67,6 +67,8 @@ _SIGNATURES = {
     "qsa_prefill_select": (_I32, [_CFG, _P, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
     "qsa_pool_keys_fp8": (_I32, [_CFG, _P, _I64, _P, _P, _P, _P, _I32, _I64, _P, _P, _I64, _P, _SZ, _P]),
     "qsa_index_score_fp8": (_I32, [_CFG, _P, _P, _P, _I32, _P, _P, _I64, _P, _P, _I64, _P, _SZ, _P]),
+    "qsa_decode_step_fp8": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P,
+                                    _P, _P, _P, _SZ, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
     "qsa_last_error": (C.c_char_p, []),
     "qsa_version": (C.c_char_p, []),
@@ -230,6 +232,21 @@ def qsa_decode_step(cfg, raw_idx_k, pooled, blk_off, q_idx, q, k_cache, v_cache,
                                   ctx_len.numel(), int(max_blocks), _ptr(blocks, torch.int32),
                                   _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
                                   _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _stream(stream)), "qsa_decode_step")
+
+
+def qsa_decode_step_fp8(cfg, raw_idx_k, codes, scales, blk_off, q_idx, q, k_cache, v_cache, tok_off, ctx_len,
+                        max_blocks, blocks, count, out, lse, ws, stream=None):
+    if codes.shape[0] != scales.shape[0]:
+        raise ValueError("codes and scales must have one row per pooled block")
+    _check(load().qsa_decode_step_fp8(C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"),
+                                      _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                                      codes.shape[0], _ptr(blk_off, torch.int32), _ptr(q_idx, torch.bfloat16, "q_idx"),
+                                      _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k"),
+                                      _ptr(v_cache, torch.bfloat16, "v"), k_cache.shape[0], _ptr(tok_off, torch.int32),
+                                      _ptr(ctx_len, torch.int32), ctx_len.numel(), int(max_blocks),
+                                      _ptr(blocks, torch.int32), _ptr(count, torch.int32),
+                                      _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                                      *_ws_args(ws), _stream(stream)), "qsa_decode_step_fp8")
 
 
 def qsa_sparse_decode_noalloc(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out, lse, stream=None):

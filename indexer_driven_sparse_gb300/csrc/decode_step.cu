@@ -57,6 +57,53 @@ constexpr size_t kNewRowOff = kQOff + (size_t)2 * kMaxGroup * kHeadDim * 2;
 constexpr size_t kRawOff = kNewRowOff + 256;                          // 4 raw key rows, bf16
 constexpr size_t kMbarOff = kRawOff + (size_t)kRatio * kIdxDim * 2;
 constexpr size_t kStepSmem = kMbarOff + 16 * kRingStages;      // ring full / empty mbarriers
+// FP8 keys (128 one-byte codes + an fp32 scale per block): a stage holds 256 code rows, and
+// its scales arrive on the same mbarrier as the 16-byte-aligned run of whole 4-scale groups
+// that covers them (at most 260 floats), in a ring of their own after the mbarriers.
+constexpr int kChunkRows8 = kChunkBytes / kIdxDim;
+constexpr int kScaleStageBytes = (kChunkRows8 + 8) * 4;
+constexpr size_t kScaleOff = kStepSmem;
+constexpr size_t kStepSmem8 = kScaleOff + (size_t)kRingStages * kScaleStageBytes;
+static_assert(kScaleOff % 16 == 0, "bulk copies need 16-byte aligned destinations");
+
+template <bool F8>
+constexpr size_t step_smem() { return F8 ? kStepSmem8 : kStepSmem; }
+
+// First scale and byte count of the aligned run of 4-scale groups covering rows
+// [first, first + rows) (the scale array is padded to a multiple of 4 entries).
+__device__ __forceinline__ void scale_run(int64_t first, int rows, int64_t *s0, uint32_t *bytes) {
+    const int64_t a = first & ~(int64_t)3;
+    const int64_t e = (first + rows + 3) & ~(int64_t)3;
+    *s0 = a;
+    *bytes = (uint32_t)((e - a) * 4);
+}
+
+// FP8: quantise the newest pooled block exactly as pool_keys_fp8_kernel does. Threads
+// 0..127 hold one bf16 dim each in v (when `active`); every thread of the CTA calls this.
+// Writes the codes and the scale to global memory, the codes to row8 (shared) and the scale
+// to s_amax[4].
+__device__ void quantize_newest(const StepArgs &a, int64_t dst, bool active, uint16_t v, uint8_t *row8,
+                                float *s_amax) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool mine = active && tid < kIdxDim;
+    const float x = mine ? bf16_bits_to_float(v) : 0.f;
+    float m = fabsf(x);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0 && warp < kIdxDim / 32) s_amax[warp] = m;
+    __syncthreads();
+    const float amax = fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
+    const float scale = __fdiv_rn(amax, kE4m3Max);
+    if (mine) {
+        const uint8_t code = scale > 0.f ? (uint8_t)(e4m3x2_of(__fdiv_rn(x, scale), 0.f) & 0xFFu) : (uint8_t)0;
+        row8[tid] = code;
+        a.codes[dst * kIdxDim + tid] = code;
+        if (tid == 0) a.scales[dst] = scale;
+    }
+    __syncthreads();
+    if (tid == 0) s_amax[4] = scale;
+    __syncthreads();
+}
 
 struct StepRowState {
     uint32_t gen;               // barrier generation, advanced once per completed barrier
@@ -622,13 +669,17 @@ __device__ void gather_chunk(const StepArgs &a, uint16_t *dst, int j_base, int n
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-template <int G>
+template <int G, bool F8>
 __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a) {
+    constexpr int kRows = F8 ? kChunkRows8 : kChunkRows;      // key rows per ring stage
+    constexpr int kRowBytes = F8 ? kIdxDim : kIdxDim * 2;
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem + kKeysOff);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kHistOff);
     uint16_t *q_b = reinterpret_cast<uint16_t *>(smem + kQOff);
     uint16_t *newrow = reinterpret_cast<uint16_t *>(smem + kNewRowOff);
+    uint8_t *newrow8 = reinterpret_cast<uint8_t *>(smem + kNewRowOff);
+    const uint32_t scale0 = smem_u32(smem + kScaleOff);                 // FP8 only
     uint16_t *rawrows = reinterpret_cast<uint16_t *>(smem + kRawOff);
     unsigned long long *ring64 = reinterpret_cast<unsigned long long *>(smem + kRingOff);
     const uint32_t mbar0 = smem_u32(smem + kMbarOff);
@@ -648,6 +699,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     __shared__ int32_t s_debug;
     __shared__ unsigned long long s_pubk[32];
     __shared__ float s_fred[2 * kStepWarps];
+    __shared__ float s_amax[5];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hq = a.n_q_heads, Hkv = a.n_kv_heads;
@@ -700,17 +752,25 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     const bool dense = nb <= kBlockTopK;
     const bool owner_new = nb >= 1 && hi == nb && lo < hi;     // owns block nb-1
     const int n_tma = owner_new ? n_mine - 1 : n_mine;        // block nb-1 is scored from the re-pooled row
-    const int n_chunks = dense ? 0 : (n_tma + kChunkRows - 1) / kChunkRows;
-    const uint16_t *gsrc = a.pooled + (boff + lo) * kIdxDim;
+    const int n_chunks = dense ? 0 : (n_tma + kRows - 1) / kRows;
+    const unsigned char *gsrc = F8 ? a.codes + (boff + lo) * kIdxDim
+                                   : reinterpret_cast<const unsigned char *>(a.pooled + (boff + lo) * kIdxDim);
+    // stage c of the ring: its key rows (and, FP8, their scales) on full mbarrier c
+    auto issue_stage = [&](int c, int stage) {
+        const int rows = min(kRows, n_tma - c * kRows);
+        const uint32_t bytes = (uint32_t)rows * kRowBytes;
+        int64_t s0 = 0;
+        uint32_t sbytes = 0;
+        if (F8) scale_run(boff + lo + (int64_t)c * kRows, rows, &s0, &sbytes);
+        mbar_arrive_expect_tx(mbar0 + 8 * stage, bytes + sbytes);
+        bulk_g2s(ring0 + stage * kChunkBytes, gsrc + (int64_t)c * kChunkBytes, bytes, mbar0 + 8 * stage);
+        if (F8) bulk_g2s(scale0 + stage * kScaleStageBytes, a.scales + s0, sbytes, mbar0 + 8 * stage);
+    };
 
     // ---- 2a. start streaming this CTA's pooled rows (the latency overlaps what follows)
     uint32_t g0 = 0;                      // barrier generation at launch (thread 0 only)
     if (tid == 0) {
-        for (int c = 0; c < n_chunks && c < kRingStages; ++c) {
-            const uint32_t bytes = (uint32_t)min(kChunkRows, n_tma - c * kChunkRows) * kIdxDim * 2;
-            mbar_arrive_expect_tx(mbar0 + 8 * c, bytes);
-            bulk_g2s(ring0 + c * kChunkBytes, gsrc + (int64_t)c * kChunkRows * kIdxDim, bytes, mbar0 + 8 * c);
-        }
+        for (int c = 0; c < n_chunks && c < kRingStages; ++c) issue_stage(c, c);
         g0 = ld_acquire_u32(&rs->gen);
     }
     // the query rows for the attention step, bf16, prefetched now
@@ -726,13 +786,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     if (dense) {                          // dense rows re-pool block nb-1 here (no scan)
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
+        uint16_t v = 0;
         if (owner_new && tid < kIdxDim) {
             const double s4 = (((double)bf16_bits_to_float(rawrows[tid]) +
                                 (double)bf16_bits_to_float(rawrows[kIdxDim + tid])) +
                                (double)bf16_bits_to_float(rawrows[2 * kIdxDim + tid])) +
                               (double)bf16_bits_to_float(rawrows[3 * kIdxDim + tid]);
-            a.pooled[(boff + nb - 1) * kIdxDim + tid] = double_to_bf16_rne(s4 * 0.25);
+            v = double_to_bf16_rne(s4 * 0.25);
+            if (!F8) a.pooled[(boff + nb - 1) * kIdxDim + tid] = v;
         }
+        if (F8 && owner_new) quantize_newest(a, boff + nb - 1, true, v, newrow8, s_amax);   // CTA-uniform
     }
 
     bool balanced = dense;                // the row's whole selection is known to every CTA
@@ -742,9 +805,22 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     if (!dense) {
         // ---- 2b. scan: bulk copies into a 4-stage ring, scores -> keys + histogram
         for (int i = tid; i < kHistBins; i += kStepThreads) hist[i] = 0;
-        float qf[8];
-        unpack8(ldg_nc_v4(a.q_idx + (int64_t)row * kIdxDim + (lane & 15) * 8), qf);
+        // bf16: a half-warp per row, 8 dims per lane; FP8: 8 lanes per row, 16 dims per lane
+        float qf[F8 ? 16 : 8];
+        if constexpr (F8) {
+            float qa[8], qb[8];
+            unpack8(ldg_nc_v4(a.q_idx + (int64_t)row * kIdxDim + (lane & 7) * 16), qa);
+            unpack8(ldg_nc_v4(a.q_idx + (int64_t)row * kIdxDim + (lane & 7) * 16 + 8), qb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                qf[e] = qa[e];
+                qf[8 + e] = qb[e];
+            }
+        } else {
+            unpack8(ldg_nc_v4(a.q_idx + (int64_t)row * kIdxDim + (lane & 15) * 8), qf);
+        }
         const int half = lane >> 4, c16 = lane & 15;
+        const int g8 = lane >> 3, c8 = lane & 7;
         __syncthreads();
         for (int c = 0; c < n_chunks; ++c) {
             const int stage = c % kRingStages;
@@ -758,25 +834,52 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 __syncthreads();
                 return;
             }
-            const int rows_c = min(kChunkRows, n_tma - c * kChunkRows);
-            const uint16_t *buf = reinterpret_cast<const uint16_t *>(smem + kRingOff + (size_t)stage * kChunkBytes);
-            // 16 warps x 8 rows: each half-warp takes one row per step
+            const int rows_c = min(kRows, n_tma - c * kRows);
+            if constexpr (F8) {
+                // 16 warps x 16 rows: each 8-lane group takes one row per step; the score is
+                // formed as in index_score_fp8_kernel (same products, order and scale multiply)
+                const uint8_t *buf8 = smem + kRingOff + (size_t)stage * kChunkBytes;
+                const float *sbuf = reinterpret_cast<const float *>(smem + kScaleOff + (size_t)stage * kScaleStageBytes) +
+                                    ((boff + lo + (int64_t)c * kRows) & 3);
 #pragma unroll
-            for (int it = 0; it < kChunkRows / (2 * kStepWarps); ++it) {
-                const int r = (warp * (kChunkRows / kStepWarps)) + it * 2 + half;
-                float s = 0.f;
-                if (r < rows_c) {
-                    float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(buf + r * kIdxDim + c16 * 8), f);
+                for (int it = 0; it < kRows / (4 * kStepWarps); ++it) {
+                    const int r = (warp * (kRows / kStepWarps)) + it * 4 + g8;
+                    float s = 0.f;
+                    if (r < rows_c) {
+                        float f[16];
+                        e4m3x16_to_f32(*reinterpret_cast<const uint4 *>(buf8 + r * kIdxDim + c8 * 16), f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) s = fmaf(f[e], qf[e], s);
+                        for (int e = 0; e < 16; ++e) s = fmaf(f[e], qf[e], s);
+                    }
+#pragma unroll
+                    for (int o = 4; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                    if (c8 == 0 && r < rows_c) {
+                        const uint32_t key = score_key(s * sbuf[r]);
+                        keys[c * kRows + r] = key;
+                        atomicAdd(&hist[key >> kHistShift], 1u);
+                    }
                 }
+            } else {
+                const uint16_t *buf =
+                    reinterpret_cast<const uint16_t *>(smem + kRingOff + (size_t)stage * kChunkBytes);
+                // 16 warps x 8 rows: each half-warp takes one row per step
 #pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (c16 == 0 && r < rows_c) {
-                    const uint32_t key = score_key(s);
-                    keys[c * kChunkRows + r] = key;
-                    atomicAdd(&hist[key >> kHistShift], 1u);
+                for (int it = 0; it < kRows / (2 * kStepWarps); ++it) {
+                    const int r = (warp * (kRows / kStepWarps)) + it * 2 + half;
+                    float s = 0.f;
+                    if (r < rows_c) {
+                        float f[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(buf + r * kIdxDim + c16 * 8), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) s = fmaf(f[e], qf[e], s);
+                    }
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                    if (c16 == 0 && r < rows_c) {
+                        const uint32_t key = score_key(s);
+                        keys[c * kRows + r] = key;
+                        atomicAdd(&hist[key >> kHistShift], 1u);
+                    }
                 }
             }
             // the stage is refilled once every warp has read it; no block-wide barrier per chunk
@@ -786,36 +889,50 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 if (!mbar_wait_bounded(mbar0 + 8 * (kRingStages + stage), (c / kRingStages) & 1, kWaitLimitNs)) {
                     record_error(a.hdr, QSA_ERR_DEVICE_TIMEOUT, kWhereStep, row);   // the others time out too
                 } else {
-                    const int cn = c + kRingStages;
-                    const uint32_t bytes = (uint32_t)min(kChunkRows, n_tma - cn * kChunkRows) * kIdxDim * 2;
                     fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(mbar0 + 8 * stage, bytes);
-                    bulk_g2s(ring0 + stage * kChunkBytes, gsrc + (int64_t)cn * kChunkRows * kIdxDim, bytes,
-                             mbar0 + 8 * stage);
+                    issue_stage(c + kRingStages, stage);
                 }
             }
         }
         // ---- 1b. re-pool block nb-1: exact fp64 mean of its four raw keys, one RNE to bf16
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
+        uint16_t v = 0;
         if (owner_new && tid < kIdxDim) {
             const double s4 = (((double)bf16_bits_to_float(rawrows[tid]) +
                                 (double)bf16_bits_to_float(rawrows[kIdxDim + tid])) +
                                (double)bf16_bits_to_float(rawrows[2 * kIdxDim + tid])) +
                               (double)bf16_bits_to_float(rawrows[3 * kIdxDim + tid]);
-            const uint16_t v = double_to_bf16_rne(s4 * 0.25);
-            newrow[tid] = v;
-            a.pooled[(boff + nb - 1) * kIdxDim + tid] = v;
+            v = double_to_bf16_rne(s4 * 0.25);
+            if (!F8) {
+                newrow[tid] = v;
+                a.pooled[(boff + nb - 1) * kIdxDim + tid] = v;
+            }
+        }
+        if constexpr (F8) {
+            if (owner_new) quantize_newest(a, boff + nb - 1, true, v, newrow8, s_amax);   // CTA-uniform
         }
         __syncthreads();
         if (owner_new && warp == 0) {          // the freshly pooled block, from shared memory
-            float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(newrow + c16 * 8), f);
             float s = 0.f;
+            if constexpr (F8) {
+                if (lane < 8) {
+                    float f[16];
+                    e4m3x16_to_f32(*reinterpret_cast<const uint4 *>(newrow8 + c8 * 16), f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s = fmaf(f[e], qf[e], s);
+                    for (int e = 0; e < 16; ++e) s = fmaf(f[e], qf[e], s);
+                }
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                for (int o = 4; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                s *= s_amax[4];
+            } else {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(newrow + c16 * 8), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s = fmaf(f[e], qf[e], s);
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            }
             if (lane == 0) {
                 const uint32_t key = score_key(s);
                 keys[n_mine - 1] = key;
@@ -1381,20 +1498,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
 // ------------------------------------------------------------------------------ launcher
 
 namespace {
-int g_step_ctas[64][5];     // per device and per G (1,2,4,8,16): co-resident CTAs, 0 = unknown
+int g_step_ctas[64][5][2];  // per device, per G (1,2,4,8,16) and key format: co-resident CTAs, 0 = unknown
 
 int g_index(int G) { return G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : 4; }
 
-template <int G>
+template <int G, bool F8>
 int step_ctas_g(int dev) {
-    int &slot = g_step_ctas[dev][g_index(G)];
+    int &slot = g_step_ctas[dev][g_index(G)][F8 ? 1 : 0];
     if (slot == 0) {
-        auto kern = decode_step_kernel<G>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStepSmem) != cudaSuccess)
-            return 0;
+        auto kern = decode_step_kernel<G, F8>;
+        const int smem = (int)step_smem<F8>();
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
         int sms = 0, per_sm = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStepThreads, kStepSmem) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStepThreads, smem) != cudaSuccess)
             return 0;
         if (per_sm < 1) return 0;
         slot = min(sms * per_sm, kMaxStepCtas);
@@ -1402,12 +1519,12 @@ int step_ctas_g(int dev) {
     return slot;
 }
 
-template <int G>
+template <int G, bool F8>
 cudaError_t launch_step_g(const StepArgs &a, int ctas, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kStepThreads);
-    cfg.dynamicSmemBytes = kStepSmem;
+    cfg.dynamicSmemBytes = step_smem<F8>();
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -1416,7 +1533,31 @@ cudaError_t launch_step_g(const StepArgs &a, int ctas, cudaStream_t st) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_step_kernel<G>, a);
+    return cudaLaunchKernelEx(&cfg, decode_step_kernel<G, F8>, a);
+}
+
+template <bool F8>
+int grid_for(int G, int dev) {
+    switch (G) {
+        case 1: return step_ctas_g<1, F8>(dev);
+        case 2: return step_ctas_g<2, F8>(dev);
+        case 4: return step_ctas_g<4, F8>(dev);
+        case 8: return step_ctas_g<8, F8>(dev);
+        case 16: return step_ctas_g<16, F8>(dev);
+        default: return 0;
+    }
+}
+
+template <bool F8>
+cudaError_t launch_for(const StepArgs &a, int G, int ctas, cudaStream_t st) {
+    switch (G) {
+        case 1: return launch_step_g<1, F8>(a, ctas, st);
+        case 2: return launch_step_g<2, F8>(a, ctas, st);
+        case 4: return launch_step_g<4, F8>(a, ctas, st);
+        case 8: return launch_step_g<8, F8>(a, ctas, st);
+        case 16: return launch_step_g<16, F8>(a, ctas, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 }  // namespace
 
@@ -1424,17 +1565,10 @@ size_t decode_step_ws_bytes(int B, int64_t max_blocks, int Hq) { return step_lay
 
 int decode_step_max_keys() { return kMaxKeys; }
 
-int decode_step_grid(int G) {
+int decode_step_grid(int G, bool fp8) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    switch (G) {
-        case 1: return step_ctas_g<1>(dev);
-        case 2: return step_ctas_g<2>(dev);
-        case 4: return step_ctas_g<4>(dev);
-        case 8: return step_ctas_g<8>(dev);
-        case 16: return step_ctas_g<16>(dev);
-        default: return 0;
-    }
+    return fp8 ? grid_for<true>(G, dev) : grid_for<false>(G, dev);
 }
 
 cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st) {
@@ -1448,16 +1582,10 @@ cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st) {
     a.pub = reinterpret_cast<unsigned long long *>(w + L.pub);
     a.trace = reinterpret_cast<unsigned long long *>(w + L.trace);
     const int G = a.n_q_heads / a.n_kv_heads;
-    const int ctas = decode_step_grid(G);
+    const bool fp8 = a.codes != nullptr;
+    const int ctas = decode_step_grid(G, fp8);
     if (ctas < a.B || ctas == 0) return cudaErrorInvalidConfiguration;
-    switch (G) {
-        case 1: return launch_step_g<1>(a, ctas, st);
-        case 2: return launch_step_g<2>(a, ctas, st);
-        case 4: return launch_step_g<4>(a, ctas, st);
-        case 8: return launch_step_g<8>(a, ctas, st);
-        case 16: return launch_step_g<16>(a, ctas, st);
-        default: return cudaErrorInvalidValue;
-    }
+    return fp8 ? launch_for<true>(a, G, ctas, st) : launch_for<false>(a, G, ctas, st);
 }
 
 }  // namespace qsa

@@ -10,36 +10,9 @@
 //                          an all-zero key has scale 0 and zero codes.
 //   index_score_fp8_kernel: s_b = scale_b * sum_d q_idx[d] * code_b[d]; every product of a
 //                          bf16 and an E4M3 value is exact in fp32, summed in fp32.
-#include <cuda_fp16.h>
-
 #include "qsa_internal.cuh"
 
 namespace qsa {
-
-constexpr float kE4m3Max = 448.f;   // largest finite E4M3 value: 1.75 * 2^8
-
-// Two fp32 values -> two E4M3 codes (nearest even, saturating at +-448); `lo` lands in
-// bits 0-7, `hi` in bits 8-15 (the instruction puts its first source in the upper byte).
-__device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Sixteen E4M3 codes (byte k = dim k) -> fp32, exactly: E4M3 -> f16 is exact, f16 -> f32 too.
-__device__ __forceinline__ void e4m3x16_to_f32(const uint4 &v, float (&f)[16]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t h0, h1;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)(w[i] & 0xFFFFu)));
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)(w[i] >> 16)));
-        f[4 * i + 0] = __half2float(__ushort_as_half((unsigned short)(h0 & 0xFFFFu)));
-        f[4 * i + 1] = __half2float(__ushort_as_half((unsigned short)(h0 >> 16)));
-        f[4 * i + 2] = __half2float(__ushort_as_half((unsigned short)(h1 & 0xFFFFu)));
-        f[4 * i + 3] = __half2float(__ushort_as_half((unsigned short)(h1 >> 16)));
-    }
-}
 
 // 16 threads per pooled block, each owning 8 of the 128 dims; the block's |max| is reduced
 // over its 16 threads (one half-warp).

@@ -364,40 +364,52 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
     return ok();
 }
 
-QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
-                                   int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
-                                   const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
-                                   int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len, int32_t B,
-                                   int64_t max_blocks, int32_t *blocks, int32_t *count, qsa_bf16 *out, float *lse,
-                                   void *ws, size_t ws_bytes, qsa_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// The fused step with bf16 keys (pooled) or FP8 keys (codes + scales).
+qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                              uint8_t *codes, float *scales, int64_t n_pooled_total, const int32_t *blk_off,
+                              const qsa_bf16 *q_idx, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                              const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
+                              const int32_t *ctx_len, int32_t B, int64_t max_blocks, int32_t *blocks,
+                              int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                              qsa_stream stream) {
+    const bool fp8 = pooled == nullptr;
     QSA_TRY(check_config(cfg));
     QSA_NEED(B >= 0 && B <= kMaxStepRows, "B = %d out of range [0, 64]", B);
     QSA_NEED(max_blocks >= 0 && max_blocks <= (int64_t)1 << 28, "max_blocks out of range");
     QSA_NEED(n_tokens_total >= 0 && n_pooled_total >= 0, "negative size");
-    if (cfg->n_kv_heads > 2) return fail(QSA_ERR_UNSUPPORTED, "qsa_decode_step supports n_kv_heads <= 2");
+    if (cfg->n_kv_heads > 2) return fail(QSA_ERR_UNSUPPORTED, "%s supports n_kv_heads <= 2", name);
     QSA_TRY(check_ws(QSA_OP_DECODE_STEP, cfg, B, max_blocks, ws, ws_bytes));
     if (B == 0) return ok();
-    QSA_NEED(raw_idx_k && pooled && blk_off && q_idx && q && k_cache && v_cache && tok_off && ctx_len && blocks &&
-                 count && out,
+    QSA_NEED(raw_idx_k && (fp8 ? codes && scales : pooled != nullptr) && blk_off && q_idx && q && k_cache &&
+                 v_cache && tok_off && ctx_len && blocks && count && out,
              "NULL tensor pointer");
-    QSA_NEED(aligned(raw_idx_k, 16) && aligned(pooled, 16) && aligned(q_idx, 16) && aligned(k_cache, 16) &&
-                 aligned(v_cache, 16) && aligned(q, 16),
-             "bf16 tensors must be 16-byte aligned");
+    QSA_NEED(aligned(raw_idx_k, 16) && aligned(q_idx, 16) && aligned(k_cache, 16) && aligned(v_cache, 16) &&
+                 aligned(q, 16) && (fp8 ? aligned(codes, 16) && aligned(scales, 16) : aligned(pooled, 16)),
+             "bf16 tensors, codes and scales must be 16-byte aligned");
+    if (fp8)
+        QSA_NEED(n_pooled_total % 4 == 0, "n_pooled_total = %lld must be a multiple of 4 with FP8 keys",
+                 (long long)n_pooled_total);
     QSA_NEED(device_accessible(raw_idx_k) && device_accessible(k_cache) && device_accessible(v_cache),
              "raw_idx_k, k_cache and v_cache must be device memory or mapped pinned host memory");
     const int G = cfg->n_q_heads / cfg->n_kv_heads;
-    const int ctas = decode_step_grid(G);
-    if (ctas == 0) return fail(QSA_ERR_CUDA, "decode step: cannot size the cooperative grid on this device");
-    if (B > ctas) return fail(QSA_ERR_UNSUPPORTED, "decode step: B = %d exceeds %d co-resident CTAs", B, ctas);
+    const int ctas = decode_step_grid(G, fp8);
+    if (ctas == 0) return fail(QSA_ERR_CUDA, "%s: cannot size the cooperative grid on this device", name);
+    if (B > ctas) return fail(QSA_ERR_UNSUPPORTED, "%s: B = %d exceeds %d co-resident CTAs", name, B, ctas);
     // every CTA keeps at most decode_step_max_keys() scores on chip; bound the worst row
     const int64_t K = 16384;
     const int64_t worst = ctas > B ? (int64_t)B * (max_blocks + K) / (ctas - B) + 1 : max_blocks;
     if (std::min<int64_t>(worst, max_blocks) > decode_step_max_keys())
-        return fail(QSA_ERR_UNSUPPORTED, "decode step: %lld blocks per CTA exceed the on-chip limit %d",
+        return fail(QSA_ERR_UNSUPPORTED, "%s: %lld blocks per CTA exceed the on-chip limit %d", name,
                     (long long)std::min<int64_t>(worst, max_blocks), decode_step_max_keys());
     StepArgs a{};
     a.raw_idx_k = raw_idx_k;
     a.pooled = pooled;
+    a.codes = fp8 ? codes : nullptr;
+    a.scales = fp8 ? scales : nullptr;
     a.n_pooled = n_pooled_total;
     a.blk_off = blk_off;
     a.q_idx = q_idx;
@@ -419,6 +431,36 @@ QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_id
     const cudaError_t e = launch_decode_step(a, ws, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                   int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
+                                   const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                   int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len, int32_t B,
+                                   int64_t max_blocks, int32_t *blocks, int32_t *count, qsa_bf16 *out, float *lse,
+                                   void *ws, size_t ws_bytes, qsa_stream stream) {
+    if (pooled == nullptr && B > 0) return fail(QSA_ERR_INVALID_ARGUMENT, "pooled is NULL");
+    return decode_step_common("qsa_decode_step", cfg, raw_idx_k, pooled, nullptr, nullptr, n_pooled_total, blk_off,
+                              q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, max_blocks, blocks,
+                              count, out, lse, ws, ws_bytes, stream);
+}
+
+QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, uint8_t *codes,
+                                       float *scales, int64_t n_pooled_total, const int32_t *blk_off,
+                                       const qsa_bf16 *q_idx, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                       const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
+                                       const int32_t *ctx_len, int32_t B, int64_t max_blocks, int32_t *blocks,
+                                       int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                       qsa_stream stream) {
+    if ((codes == nullptr || scales == nullptr) && B > 0)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "codes and scales must be non-NULL");
+    return decode_step_common("qsa_decode_step_fp8", cfg, raw_idx_k, nullptr, codes, scales, n_pooled_total,
+                              blk_off, q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, max_blocks,
+                              blocks, count, out, lse, ws, ws_bytes, stream);
 }
 
 QSA_API const char *qsa_status_string(qsa_status s) {

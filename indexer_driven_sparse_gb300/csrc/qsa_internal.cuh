@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "qsa.h"
@@ -94,6 +95,32 @@ __device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
     if (ax >= 0x1p127) return sign | 0x7F80;    // |x| >= 2^128: overflow
     const double r = ldexp(rint(ldexp(ax, 133)), -133);
     return sign | (uint16_t)(__float_as_uint((float)r) >> 16);
+}
+
+// ---------------------------------------------------------------------------- FP8 (E4M3) keys
+constexpr float kE4m3Max = 448.f;   // largest finite E4M3 value: 1.75 * 2^8
+
+// Two fp32 values -> two E4M3 codes (nearest even, saturating at +-448); `lo` lands in
+// bits 0-7, `hi` in bits 8-15 (the instruction puts its first source in the upper byte).
+__device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Sixteen E4M3 codes (byte k = dim k) -> fp32, exactly: E4M3 -> f16 is exact, f16 -> f32 too.
+__device__ __forceinline__ void e4m3x16_to_f32(const uint4 &v, float (&f)[16]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h0, h1;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)(w[i] & 0xFFFFu)));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)(w[i] >> 16)));
+        f[4 * i + 0] = __half2float(__ushort_as_half((unsigned short)(h0 & 0xFFFFu)));
+        f[4 * i + 1] = __half2float(__ushort_as_half((unsigned short)(h0 >> 16)));
+        f[4 * i + 2] = __half2float(__ushort_as_half((unsigned short)(h1 & 0xFFFFu)));
+        f[4 * i + 3] = __half2float(__ushort_as_half((unsigned short)(h1 >> 16)));
+    }
 }
 
 // Order-preserving map of an fp32 score to uint32: larger score -> larger key.
@@ -201,7 +228,9 @@ constexpr int kMaxStepCtas = 256;
 constexpr int kMaxStepRows = 64;
 struct StepArgs {
     const uint16_t *raw_idx_k;
-    uint16_t *pooled;
+    uint16_t *pooled;           // bf16 keys [n_pooled][128] (nullptr with FP8 keys)
+    uint8_t *codes;             // FP8 keys: codes [n_pooled][128] and scales [n_pooled] (else nullptr)
+    float *scales;
     int64_t n_pooled;
     const int32_t *blk_off;
     const uint16_t *q_idx;
@@ -235,7 +264,7 @@ StepLayout step_layout(int B, int64_t max_blocks, int Hq);
 size_t decode_step_ws_bytes(int B, int64_t max_blocks, int Hq);
 int decode_step_max_keys();
 // Number of CTAs the cooperative step kernel runs with on the current device (0 on error).
-int decode_step_grid(int G);
+int decode_step_grid(int G, bool fp8);
 cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st);
 
 // Set the calling thread's qsa_last_error() text to "<what>: <detail>" and return s.

@@ -63,6 +63,12 @@ class DecodeBatch:
         qb.qsa_decode_step(self.cfg, raw_idx_k, pooled, self.blk_off, q_idx, q, k_cache, v_cache, self.tok_off,
                            self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse, self.step_ws, stream)
 
+    def fused_step_fp8(self, raw_idx_k, codes, scales, q_idx, q, k_cache, v_cache, stream=None):
+        """qsa_decode_step over FP8 indexer keys (qsa_decode_step_fp8)."""
+        qb.qsa_decode_step_fp8(self.cfg, raw_idx_k, codes, scales, self.blk_off, q_idx, q, k_cache, v_cache,
+                               self.tok_off, self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse,
+                               self.step_ws, stream)
+
     def fused_status(self, stream=None):
         return qb.qsa_read_device_status(self.step_ws, stream)
 
@@ -89,8 +95,9 @@ class DecodeBatch:
         self.attend(q, k_cache, v_cache, stream=stream)
 
     def new_fp8_keys(self):
-        """Buffers of the FP8 indexer keys: codes [n_pooled, 128] uint8 and scales [n_pooled] fp32."""
-        n = max(self.n_pooled, 1)
+        """Buffers of the FP8 indexer keys: codes [n, 128] uint8 and scales [n] fp32, n = the
+        pooled block count padded to a multiple of 4 (the fused step copies whole groups of 4 scales)."""
+        n = max((self.n_pooled + 3) // 4 * 4, 4)
         return (torch.empty(n, 128, dtype=torch.uint8, device=self.device),
                 torch.empty(n, dtype=torch.float32, device=self.device))
 

@@ -207,3 +207,18 @@ def test_fp8_key_calls_host_checks(lib):
         qb.QSA_ERR_WORKSPACE_TOO_SMALL
     assert lib.qsa_index_score_fp8(C.byref(cfg(idx_dim=64)), FAKE, 0, FAKE, 1, FAKE, FAKE, 10, FAKE, FAKE, 10, ws,
                                    256, 0) == qb.QSA_ERR_UNSUPPORTED
+
+
+def test_decode_step_fp8_host_checks(lib):
+    c = cfg()
+    need = lib.qsa_workspace_size(qb.OP_DECODE_STEP, C.byref(c), 1, 1000)
+    args = lambda codes, scales, n_pooled, B: (C.byref(c), FAKE, codes, scales, n_pooled, FAKE, FAKE, FAKE, FAKE,
+                                                FAKE, 4001, FAKE, FAKE, B, 1000, FAKE, FAKE, FAKE, 0, FAKE, need, 0)
+    assert lib.qsa_decode_step_fp8(*args(0, 0, 0, 0)) == qb.QSA_OK                      # empty batch
+    assert lib.qsa_decode_step_fp8(*args(0, FAKE, 1000, 1)) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_decode_step_fp8(*args(FAKE, FAKE + 4, 1000, 1)) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"aligned" in lib.qsa_last_error()
+    assert lib.qsa_decode_step_fp8(*args(FAKE, FAKE, 1001, 1)) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"multiple of 4" in lib.qsa_last_error()
+    assert lib.qsa_decode_step(C.byref(c), FAKE, 0, 1000, FAKE, FAKE, FAKE, FAKE, FAKE, 4001, FAKE, FAKE, 1, 1000,
+                               FAKE, FAKE, FAKE, 0, FAKE, need, 0) == qb.QSA_ERR_INVALID_ARGUMENT

@@ -68,3 +68,11 @@ def test_fp8_scan_bytes():
     assert A.score_scan_bytes_fp8([3]) == 256
     bf16 = A.score_scan_bytes([1048320]) - 256
     assert (A.score_scan_bytes_fp8([1048320]) - 256) / bf16 == 132 / 256
+
+
+def test_fp8_layer_step_bytes():
+    # the million-token step: the scan shrinks from 256 to 132 bytes per block, the rest is unchanged
+    bf16 = A.decode_layer_step_bytes([1048320], 16)
+    fp8 = A.decode_layer_step_bytes_fp8([1048320], 16)
+    assert bf16 == 71_305_472
+    assert bf16 - fp8 == 262080 * (256 - 132)

@@ -145,7 +145,7 @@ def _run_fp8_decode(w):
     return b, codes, scales
 
 
-def _check_fp8_decode(w, b, codes, scales, rows=None):
+def _check_fp8_decode(w, b, codes, scales, rows=None, check_scores=True):
     Lh = w.layers[0]
     qib, qbits, kb, vb = bits(Lh.q_idx), bits(Lh.q), bits(Lh.k_cache), bits(Lh.v_cache)
     blocks, count = b.blocks.cpu().numpy(), b.count.cpu().numpy()
@@ -161,7 +161,8 @@ def _check_fp8_decode(w, b, codes, scales, rows=None):
         vals, scl = _check_keys(codes[lo:hi], scales[lo:hi], pk)
         want = O.score_blocks_fp8(qib[s], vals[:nb], scl[:nb])
         bound = O.score_error_bound_fp8(qib[s], vals[:nb], scl[:nb])
-        assert np.all(np.abs(sc[s, :nb] - want) <= bound + 1e-30), s
+        if check_scores:
+            assert np.all(np.abs(sc[s, :nb] - want) <= bound + 1e-30), s
         n_band, n_fp32 = check_selection_fp8(blocks[s], count[s], qib[s], vals, scl, nb)
         stats["band"] += n_band
         stats["fp32"] += n_fp32
@@ -206,3 +207,65 @@ def test_million_decode_fp8_full_size_one_layer(cuda_lib):
     b, codes, scales = _run_fp8_decode(w)
     w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
     _check_fp8_decode(w, b, codes, scales)
+
+
+# ----------------------------------------------------------------------------- fused step, FP8 keys
+
+def _run_fused_fp8(w, corrupt_newest=True):
+    """Separate FP8 calls, then qsa_decode_step_fp8 on keys whose newest block was corrupted:
+    the step must re-pool it, reproduce the separate path's selection exactly and attend."""
+    L = _to(w.layers[0])
+    b = DecodeBatch(w.n_q_heads, w.n_kv_heads, w.ctx_len)
+    codes, scales = b.new_fp8_keys()
+    b.pool_fp8(L.raw_idx_k, codes, scales)
+    b.step_fp8(L.q_idx, L.q, L.k_cache, L.v_cache, codes, scales)
+    assert b.device_status()[0] == 0
+    sep = (b.blocks.clone(), b.count.clone(), b.out.clone())
+    want_codes, want_scales = codes.clone(), scales.clone()
+    if corrupt_newest:
+        for s, p in enumerate(w.ctx_len):
+            if p >= 4:
+                r = b.blk_off[s].item() + p // 4 - 1
+                codes[r] = 0x38       # 1.0
+                scales[r] = 3.0
+    b.blocks.fill_(-7)
+    b.out.zero_()
+    b.fused_step_fp8(L.raw_idx_k, codes, scales, L.q_idx, L.q, L.k_cache, L.v_cache)
+    st = b.fused_status()
+    assert st[0] == 0, st
+    assert torch.equal(codes, want_codes)
+    assert torch.equal(scales.view(torch.int32), want_scales.view(torch.int32))
+    assert torch.equal(b.count, sep[1])
+    assert torch.equal(b.blocks, sep[0]), "fused FP8 selection differs from the separate FP8 calls"
+    assert (b.out.float() - sep[2].float()).abs().max().item() <= 2 ** -6
+    return b, codes, scales
+
+
+@pytest.mark.parametrize("case", ["planted_ragged", "tiny_sharp", "batched_short"])
+def test_fused_step_fp8_small(cuda_lib, case):
+    if case == "planted_ragged":
+        w = I.decode_workload("fp8_fused_ragged", [5000, 2052, 70001, 4, 12345, 0, 3, 2051], 1, 16, 2, "planted",
+                              seed=31)
+    elif case == "tiny_sharp":
+        w = I.tiny_decode(kind="sharp", seed=32)
+    else:
+        w = I.decode_workload("fp8_fused_short", I.batched_ctx_lens(short_draw=True), 1, 8, 2, "gaussian", seed=33)
+    b, codes, scales = _run_fused_fp8(w)
+    _check_fp8_decode(w, b, codes, scales)
+
+
+def test_fused_step_fp8_million_full_size(cuda_lib):
+    w = I.million_decode(n_layers=1)
+    b, codes, scales = _run_fused_fp8(w)
+    w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
+    _check_fp8_decode(w, b, codes, scales)
+
+
+def test_fused_step_fp8_rejects_unpadded_keys(cuda_lib):
+    w = I.tiny_decode(seed=4)
+    L = _to(w.layers[0])
+    b = DecodeBatch(8, 2, w.ctx_len)
+    codes, scales = b.new_fp8_keys()
+    with pytest.raises(qb.QsaError) as e:
+        b.fused_step_fp8(L.raw_idx_k, codes[:-1], scales[:-1], L.q_idx, L.q, L.k_cache, L.v_cache)
+    assert e.value.status == qb.QSA_ERR_INVALID_ARGUMENT
