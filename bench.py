@@ -584,6 +584,25 @@ def _case_decode_step(reps):
     return b.fused_status()
 
 
+def _case_decode_fp8(reps):
+    """One million-token layer with FP8 indexer keys: pool into codes + scales, then `reps`
+    times the standalone FP8 scan (qsa_index_score_fp8) and the fused FP8 step."""
+    import torch
+    from indexer_driven_sparse_gb300 import inputs as I
+    from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+    w = I.million_decode(n_layers=1)
+    L = w.layers[0]
+    b = DecodeBatch(16, 2, w.ctx_len)
+    codes, scales = b.new_fp8_keys()
+    b.pool_fp8(L.raw_idx_k, codes, scales)
+    for _ in range(reps):
+        b.score_fp8(L.q_idx, codes, scales)
+        b.fused_step_fp8(L.raw_idx_k, codes, scales, L.q_idx, L.q, L.k_cache, L.v_cache)
+    torch.cuda.synchronize()
+    st = b.device_status()
+    return st if st[0] != 0 else b.fused_status()
+
+
 def _case_prefill(reps, attention_only):
     """The prefill chunk (4096 queries over 262,144 tokens, about 1.1 GB on the device):
     pool + score + top-k once, then `reps` chunk attentions (or whole chunks)."""
@@ -607,6 +626,7 @@ def _case_prefill(reps, attention_only):
 
 CASES = {
     "decode_step": lambda reps: _case_decode_step(reps),
+    "decode_fp8": lambda reps: _case_decode_fp8(reps),
     "prefill_attention": lambda reps: _case_prefill(reps, True),
     "prefill_chunk": lambda reps: _case_prefill(reps, False),
 }

@@ -11,6 +11,9 @@
 //   index_score_fp8_kernel: s_b = scale_b * sum_d q_idx[d] * code_b[d]; every product of a
 //                          bf16 and an E4M3 value is exact in fp32, summed in fp32.
 #include "qsa_internal.cuh"
+#include "qsa_ptx.cuh"
+
+#include <algorithm>
 
 namespace qsa {
 
@@ -67,12 +70,16 @@ __global__ void __launch_bounds__(256) pool_keys_fp8_kernel(const uint16_t *__re
 }
 
 constexpr int kF8Threads = 256;
-constexpr int kF8RowsPerWarp = 32;
-constexpr int kF8RowsPerCta = kF8RowsPerWarp * (kF8Threads / 32);   // 256 rows = 32 KiB of codes
+constexpr int kF8TileRows = 128;                                     // 16 KiB of codes per stage
+constexpr int kF8Stages = 4;
+constexpr int kF8TileBytes = kF8TileRows * kIdxDim;
+constexpr int kF8Smem = kF8Stages * kF8TileBytes + 8 * kF8Stages;   // ring + full mbarriers
 
-// Each warp covers 32 consecutive 128-byte code rows: a row is 8 lanes x 16 bytes (16 dims
-// per lane), so one 16-byte load instruction of the warp covers 4 rows; all 8 loads of a
-// lane are issued before use. The 32 scales of the warp's rows are one coalesced load.
+// The CTAs of a query row (gridDim.x of them) split its visible blocks into equal contiguous
+// ranges. A CTA streams its range through a 4-stage shared-memory ring of 128-row tiles
+// filled by bulk async copies (TMA engine), so every stage's bytes are requested without
+// holding registers; a tile is scored from shared memory (8 lanes per row, 16 dims per lane)
+// while later tiles are in flight. Each lane loads its rows' scales one tile ahead.
 __global__ void __launch_bounds__(kF8Threads) index_score_fp8_kernel(const uint16_t *__restrict__ q_idx,
                                                                      const int32_t *q_seq, const int32_t *q_pos,
                                                                      const uint8_t *__restrict__ codes,
@@ -80,6 +87,7 @@ __global__ void __launch_bounds__(kF8Threads) index_score_fp8_kernel(const uint1
                                                                      int64_t n_pooled, const int32_t *blk_off,
                                                                      float *__restrict__ scores, int64_t ld,
                                                                      WsHeader *hdr) {
+    extern __shared__ __align__(128) unsigned char smem[];
     const int r = blockIdx.y;
     const int p = q_pos[r];
     const int64_t nb = p >= 0 ? (p >> 2) : -1;
@@ -88,10 +96,23 @@ __global__ void __launch_bounds__(kF8Threads) index_score_fp8_kernel(const uint1
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(hdr, QSA_ERR_DEVICE_BOUNDS, kWhereScore, r);
         return;
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row0 = (int64_t)blockIdx.x * kF8RowsPerCta + warp * kF8RowsPerWarp;
-    if (row0 >= nb) return;   // whole warps leave
-    const int g = lane >> 3, c = lane & 7;
+    const int64_t lo = nb * blockIdx.x / gridDim.x, hi = nb * (blockIdx.x + 1) / gridDim.x;
+    if (lo >= hi) return;   // the whole CTA leaves
+    const int n_tiles = (int)((hi - lo + kF8TileRows - 1) / kF8TileRows);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 3, c = lane & 7;
+    const uint32_t ring = smem_u32(smem), bar = smem_u32(smem + kF8Stages * kF8TileBytes);
+    const uint8_t *src = codes + (off + lo) * kIdxDim;
+    auto issue = [&](int t) {                      // thread 0: tile t into stage t % kF8Stages
+        const int st = t % kF8Stages;
+        const uint32_t bytes = (uint32_t)(hi - lo - (int64_t)t * kF8TileRows < kF8TileRows ? hi - lo - (int64_t)t * kF8TileRows : (int64_t)kF8TileRows) * kIdxDim;
+        mbar_arrive_expect_tx(bar + 8 * st, bytes);
+        bulk_g2s(ring + st * kF8TileBytes, src + (int64_t)t * kF8TileBytes, bytes, bar + 8 * st);
+    };
+    if (tid == 0) {
+        for (int i = 0; i < kF8Stages; ++i) mbar_init(bar + 8 * i, 1);
+        fence_mbar_init();
+        for (int t = 0; t < n_tiles && t < kF8Stages; ++t) issue(t);
+    }
     float qf[16];
     {
         float a[8], b[8];
@@ -103,38 +124,59 @@ __global__ void __launch_bounds__(kF8Threads) index_score_fp8_kernel(const uint1
             qf[8 + e] = b[e];
         }
     }
-    const uint8_t *base = codes + (off + row0) * kIdxDim + c * 16;
-    uint4 v[kF8RowsPerWarp / 4];
+    // warp w scores rows 16w .. 16w+15 of a tile; lane L < 16 holds the scale of row 16w + L
+    auto scale_at = [&](int t) {
+        const int64_t row = lo + (int64_t)t * kF8TileRows + warp * 16 + (lane & 15);
+        return row < hi ? __ldg(scales + off + row) : 0.f;
+    };
+    float sc_next = scale_at(0);
+    __syncthreads();                               // mbarriers initialised
+    for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % kF8Stages;
+        const float sc = sc_next;
+        if (t + 1 < n_tiles) sc_next = scale_at(t + 1);
+        const bool late = !mbar_wait_bounded(bar + 8 * st, (t / kF8Stages) & 1, kWaitLimitNs);
+        if (__syncthreads_or(late)) {              // every thread leaves together
+            if (tid == 0) {
+                record_error(hdr, QSA_ERR_DEVICE_TIMEOUT, kWhereScore, r);
+                for (int t2 = t; t2 < n_tiles && t2 < t + kF8Stages; ++t2)   // copies still in flight
+                    mbar_wait_bounded(bar + 8 * (t2 % kF8Stages), (t2 / kF8Stages) & 1, kWaitLimitNs);
+            }
+            return;
+        }
+        const int64_t row0 = lo + (int64_t)t * kF8TileRows;
+        const int rows = (int)(hi - row0 < kF8TileRows ? hi - row0 : (int64_t)kF8TileRows);
+        const uint8_t *buf = smem + st * kF8TileBytes;
+        float part[4];
 #pragma unroll
-    for (int j = 0; j < kF8RowsPerWarp / 4; ++j) {
-        const int64_t row = row0 + 4 * j + g;
-        v[j] = row < nb ? ldg_nc_v4(base + (int64_t)(4 * j + g) * kIdxDim) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 4; ++j) {
+            const int rr = warp * 16 + 4 * j + g;
+            float s = 0.f;
+            if (rr < rows) {
+                float f[16];
+                e4m3x16_to_f32(*reinterpret_cast<const uint4 *>(buf + rr * kIdxDim + c * 16), f);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) s = fmaf(f[e], qf[e], s);
+            }
+#pragma unroll
+            for (int o = 4; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            part[j] = s;
+        }
+        // row 16w + 4j + g sits in every lane of group g: lane L < 16 takes row 16w + L
+        float mine = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float v = __shfl_sync(0xffffffffu, part[j], (lane & 3) * 8);
+            if (j == ((lane & 15) >> 2)) mine = v;
+        }
+        const int my = warp * 16 + lane;
+        if (lane < 16 && my < rows) scores[(int64_t)r * ld + row0 + my] = mine * sc;
+        __syncthreads();                           // the stage has been read
+        if (tid == 0 && t + kF8Stages < n_tiles) {
+            fence_proxy_async_smem();
+            issue(t + kF8Stages);
+        }
     }
-    const int64_t my_row = row0 + lane;
-    const float sc = my_row < nb ? __ldg(scales + off + my_row) : 0.f;
-    float part[kF8RowsPerWarp / 4];
-#pragma unroll
-    for (int j = 0; j < kF8RowsPerWarp / 4; ++j) {
-        float f[16];
-        e4m3x16_to_f32(v[j], f);
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) s = fmaf(f[e], qf[e], s);
-        part[j] = s;
-    }
-#pragma unroll
-    for (int j = 0; j < kF8RowsPerWarp / 4; ++j) {
-#pragma unroll
-        for (int o = 4; o >= 1; o >>= 1) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
-    }
-    // row 4j + g sits in every lane of group g: lane L takes row L = 4 (L >> 2) + (L & 3)
-    float mine = 0.f;
-#pragma unroll
-    for (int j = 0; j < kF8RowsPerWarp / 4; ++j) {
-        const float a = __shfl_sync(0xffffffffu, part[j], (lane & 3) * 8);
-        if (j == (lane >> 2)) mine = a;
-    }
-    if (my_row < nb) scores[(int64_t)r * ld + my_row] = mine * sc;
 }
 
 cudaError_t launch_pool_keys_fp8(const uint16_t *raw, int64_t n_tok, const int32_t *tok_off, const int32_t *blk_off,
@@ -148,14 +190,42 @@ cudaError_t launch_pool_keys_fp8(const uint16_t *raw, int64_t n_tok, const int32
     return cudaGetLastError();
 }
 
+namespace {
+int g_f8_resident[64];   // per device: co-resident scan CTAs, 0 = unknown
+
+int f8_resident() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int &slot = g_f8_resident[dev];
+    if (slot == 0) {
+        if (cudaFuncSetAttribute(index_score_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem) !=
+            cudaSuccess)
+            return 0;
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_score_fp8_kernel, kF8Threads, kF8Smem) !=
+                cudaSuccess ||
+            per_sm < 1)
+            return 0;
+        slot = sms * per_sm;
+    }
+    return slot;
+}
+}  // namespace
+
 cudaError_t launch_index_score_fp8(const uint16_t *q_idx, const int32_t *q_seq, const int32_t *q_pos, int Nq,
                                    const uint8_t *codes, const float *scales, int64_t n_pooled,
                                    const int32_t *blk_off, float *scores, int64_t ld, WsHeader *hdr,
                                    cudaStream_t st) {
     if (Nq == 0 || ld == 0) return cudaSuccess;
-    dim3 grid((unsigned)((ld + kF8RowsPerCta - 1) / kF8RowsPerCta), (unsigned)Nq);
-    index_score_fp8_kernel<<<grid, kF8Threads, 0, st>>>(q_idx, q_seq, q_pos, codes, scales, n_pooled, blk_off,
-                                                        scores, ld, hdr);
+    const int resident = f8_resident();
+    if (resident == 0) return cudaErrorInvalidConfiguration;
+    // one wave: the resident CTAs shared over the rows, at most one per 128-row tile of the longest
+    const int64_t tiles = (ld + kF8TileRows - 1) / kF8TileRows;
+    const int64_t per_row = std::max<int64_t>(1, std::min<int64_t>(tiles, resident / Nq));
+    dim3 grid((unsigned)per_row, (unsigned)Nq);
+    index_score_fp8_kernel<<<grid, kF8Threads, kF8Smem, st>>>(q_idx, q_seq, q_pos, codes, scales, n_pooled, blk_off,
+                                                             scores, ld, hdr);
     return cudaGetLastError();
 }
 
