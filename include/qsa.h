@@ -174,9 +174,11 @@ QSA_API qsa_status qsa_pool_keys_fp8(const qsa_config *cfg, const qsa_bf16 *raw_
  * with nb = q_pos[r] / 4 and i = blk_off[q_seq[r]] + b:
  *   scores[r * ld + b] = scales[i] * sum_d q_idx[r][d] * codes[i][d],  b < nb,
  * with exact products and an fp32 sum, then one fp32 multiply by the scale. Entries b >= nb
- * are not written. q_seq may be NULL (every query in sequence 0). One query at a time (an
- * HBM stream; no tensor-core path). Workspace QSA_OP_INDEX_SCORE. Device checks: nb <= ld,
- * blk_off[s] + nb <= n_pooled_total. The scores feed qsa_topk_blocks unchanged. */
+ * are not written. q_seq may be NULL (every query in sequence 0). An HBM stream (no
+ * tensor-core path): the CTAs resident in one wave are shared over the queries, each
+ * streaming an equal range of its query's blocks. The first call on a device queries that
+ * occupancy and should precede stream capture. Workspace QSA_OP_INDEX_SCORE. Device checks:
+ * nb <= ld, blk_off[s] + nb <= n_pooled_total. The scores feed qsa_topk_blocks unchanged. */
 QSA_API qsa_status qsa_index_score_fp8(const qsa_config *cfg, const qsa_bf16 *q_idx, const int32_t *q_seq,
                                        const int32_t *q_pos, int32_t Nq, const uint8_t *codes, const float *scales,
                                        int64_t n_pooled_total, const int32_t *blk_off, float *scores, int64_t ld,
