@@ -7,7 +7,10 @@ figures printed in "3090x3で 314 万コンテキスト; KVキャッシュをホ
 token at K_pad ~ 2048, 48 MiB per 12-layer step), section "VRAM に残す必要があるもの"
 (250,000 blocks x 128 x 2 B = 64 MB per layer, 732 MiB per 12-layer step; 0.75
 KiB/token in VRAM, 27.00 KiB/token in RAM) and section "ちなみにこの欠点" (204 GiB
-per naive 4096-token prefill chunk).
+per naive 4096-token prefill chunk). The FP8 indexer key and the sparse-MLA row sizes are
+checked against the footnotes of "GLM-5.3 最適化 第2部：16基のH200上でのPCP、DCP、および
+Hybrid HiSparse" (132-byte indexer keys; 656-byte FP8 MLA rows with a 4-byte index; per-head
+query/output bytes and FLOPs per row).
 """
 
 from __future__ import annotations
@@ -15,6 +18,11 @@ from __future__ import annotations
 BF16 = 2
 RATIO = 4
 BLOCK_TOPK = 512
+FP8_KEY_SCALE_BYTES = 4          # one fp32 scale per FP8 indexer key
+MLA_LATENT = 512                 # sparse MLA: latent (value) width shared by all heads
+MLA_ROPE = 64                    # rotary part of the key; QK runs over 512 + 64 = 576 dims
+MLA_ROW_BYTES = MLA_LATENT + 4 * 4 + MLA_ROPE * BF16   # FP8 latent, 4 fp32 scales, bf16 rope = 656
+MLA_INDEX_BYTES = 4              # int32 id of a selected row
 
 
 def visible_blocks(p: int) -> int:
@@ -57,11 +65,16 @@ def score_scan_bytes(ctx_lens, idx_dim: int = 128) -> int:
     return sum(pooled_scan_bytes(visible_blocks(p), idx_dim) + idx_dim * BF16 for p in ctx_lens)
 
 
+def fp8_key_bytes(idx_dim: int = 128) -> int:
+    """Bytes of one FP8 indexer key: idx_dim one-byte codes and an fp32 scale."""
+    return idx_dim + FP8_KEY_SCALE_BYTES
+
+
 def score_scan_bytes_fp8(ctx_lens, idx_dim: int = 128) -> int:
     """Bytes the scan over FP8 indexer keys must read: per visible block 128 one-byte codes
     and a 4-byte scale (the "128 FP8 + 4 B scale" key of "GLM-5.3 最適化 第2部", footnote on
     the indexer cache), plus the bf16 indexer query."""
-    return sum(visible_blocks(p) * (idx_dim + 4) + idx_dim * BF16 for p in ctx_lens)
+    return sum(visible_blocks(p) * fp8_key_bytes(idx_dim) + idx_dim * BF16 for p in ctx_lens)
 
 
 def decode_layer_step_bytes_fp8(ctx_lens, n_q_heads: int, n_kv_heads: int = 2, head_dim: int = 256,
@@ -69,7 +82,7 @@ def decode_layer_step_bytes_fp8(ctx_lens, n_q_heads: int, n_kv_heads: int = 2, h
     """decode_layer_step_bytes with the scan over FP8 indexer keys (idx_dim + 4 bytes per block)."""
     total = 0
     for p in ctx_lens:
-        total += visible_blocks(p) * (idx_dim + 4)
+        total += visible_blocks(p) * fp8_key_bytes(idx_dim)
         total += kv_read_bytes(attended(p), n_kv_heads, head_dim)
         total += 2 * n_q_heads * head_dim * BF16 + idx_dim * BF16
     return total
@@ -101,3 +114,14 @@ def per_token_memory(n_layers: int, n_kv_heads: int = 2, head_dim: int = 256, id
     pooled = n_layers * idx_dim * BF16 // RATIO
     host = n_layers * (kv_read_bytes(1, n_kv_heads, head_dim) + idx_dim * BF16)
     return pooled, host
+
+
+def sparse_mla_query_bytes(n_heads: int, rows: int = 2048) -> int:
+    """Bytes one sparse-MLA decode query moves: its selected FP8 rows with their int32 ids,
+    plus each head's bf16 query (576 dims) and output (512 dims)."""
+    return rows * (MLA_ROW_BYTES + MLA_INDEX_BYTES) + n_heads * (MLA_LATENT + MLA_ROPE + MLA_LATENT) * BF16
+
+
+def sparse_mla_query_flops(n_heads: int, rows: int = 2048) -> int:
+    """FLOPs of one sparse-MLA decode query: QK over 576 dims and PV over 512 dims per row and head."""
+    return rows * n_heads * 2 * ((MLA_LATENT + MLA_ROPE) + MLA_LATENT)

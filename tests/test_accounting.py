@@ -7,14 +7,15 @@ import pytest
 from indexer_driven_sparse_gb300 import accounting as A
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_figures.txt")
+GOLDEN_GLM = os.path.join(os.path.dirname(__file__), "golden", "glm_page_figures.txt")
 MiB = 1 << 20
 GiB = 1 << 30
 KiB = 1 << 10
 
 
-def figs():
+def figs(path=GOLDEN):
     vals = {}
-    with open(GOLDEN, encoding="utf-8") as f:
+    with open(path, encoding="utf-8") as f:
         for line in f:
             line = line.split("#", 1)[0].strip()
             if line:
@@ -76,3 +77,23 @@ def test_fp8_layer_step_bytes():
     fp8 = A.decode_layer_step_bytes_fp8([1048320], 16)
     assert bf16 == 71_305_472
     assert bf16 - fp8 == 262080 * (256 - 132)
+
+
+def test_glm_page_byte_figures():
+    # the FP8 indexer key and the sparse-MLA row sizes against the footnotes that print them
+    g = figs(GOLDEN_GLM)
+    assert A.fp8_key_bytes() == g["indexer_key_bytes"]
+    assert A.MLA_ROW_BYTES == g["mla_row_bytes"] and A.MLA_INDEX_BYTES == g["mla_row_index_bytes"]
+    rows = int(g["mla_rows_per_query"])
+    assert round(rows * (A.MLA_ROW_BYTES + A.MLA_INDEX_BYTES) / 1e6, 2) == g["mla_rows_mb"]
+    assert A.sparse_mla_query_bytes(1, rows) - A.sparse_mla_query_bytes(0, rows) == g["mla_head_bytes"]
+    assert A.sparse_mla_query_flops(1, 1) == g["mla_flops_per_row_head"]
+    for h in (8, 64):
+        b, f = A.sparse_mla_query_bytes(h, rows), A.sparse_mla_query_flops(h, rows)
+        assert round(b / 1e6, 2) == g[f"mla_{h}_heads_mb"]
+        assert round(f / 1e6, 1 if h == 8 else 0) == g[f"mla_{h}_heads_mflops"]
+        assert round(f / b) == g[f"mla_{h}_heads_intensity"]
+    per_token = 78 * A.MLA_ROW_BYTES + 21 * A.fp8_key_bytes() + 788
+    assert per_token == g["token_bytes_total"]
+    assert round(per_token * (1 << 20) / (1 << 30), 1) == g["million_token_gib"]
+    assert round(989e12 / 4.8e12) == g["h200_ridge_flops_per_byte"]
