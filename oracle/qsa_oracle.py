@@ -39,7 +39,8 @@ __all__ = [
     "attend_partial", "lse_merge", "attend", "decode_query",
     "interval_walk_query", "score_error_bound",
     "E4M3_MAX", "e4m3_round", "quantize_pooled_fp8", "score_blocks_fp8", "decode_query_fp8",
-    "score_error_bound_fp8",
+    "score_error_bound_fp8", "MLA_LATENT", "MLA_ROPE", "MLA_GROUP", "quantize_mla_rows_fp8",
+    "sparse_mla_attend",
 ]
 
 # indexer_compress_ratio and indexer_budget from the model's text_config
@@ -374,6 +375,52 @@ def decode_query_fp8(p: int, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_
     r = decode_query(p, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_kv_heads, scale, k_blocks, sel=sel)
     r["scores"] = scores
     return r
+
+
+# --------------------------------------------------------------------------- sparse MLA (MQA form)
+
+# "GLM-5.3 最適化 第2部" (footnote 1): a sparse-MLA query reads 2,048 selected rows of an FP8
+# KV cache; QK runs over 576 dims and PV over 512, and one row serves all 64 heads. Readings
+# (the page gives sizes only): the row is a 512-wide latent that is also the value, plus 64
+# rotary dims that only enter the key; the latent is stored as E4M3 codes in 4 groups of 128
+# with one fp32 scale each (512 + 16 bytes) and the rotary part as bf16 (128 bytes): 656 B.
+MLA_LATENT = 512
+MLA_ROPE = 64
+MLA_GROUP = 128
+
+
+def quantize_mla_rows_fp8(latent_bits, rope_bits):
+    """FP8 rows of the sparse-MLA cache: each 128-dim group of the bf16 latent quantised as an
+    FP8 indexer key is (scale = group max|x| / 448, codes = E4M3(x / scale), fp32 divisions);
+    the rotary dims kept in bf16. Returns (latent [n, 512] float64 as the codes and scales
+    represent it, rope [n, 64] float64, scales [n, 4] float32)."""
+    lat = np.asarray(latent_bits)
+    n = lat.shape[0]
+    vals, scl = quantize_pooled_fp8(lat.reshape(n * (MLA_LATENT // MLA_GROUP), MLA_GROUP))
+    deq = vals * scl.astype(np.float64)[:, None]
+    return (deq.reshape(n, MLA_LATENT), bf16_bits_to_f64(np.asarray(rope_bits)).reshape(n, MLA_ROPE),
+            scl.reshape(n, MLA_LATENT // MLA_GROUP))
+
+
+def sparse_mla_attend(q_bits, latent: np.ndarray, rope: np.ndarray, rows, scale: float | None = None):
+    """One decode query of sparse MLA in its MQA form: head h attends the selected rows j with
+    logit scale * (q_h[:512] . latent_j + q_h[512:] . rope_j) and output sum_j softmax_j latent_j.
+    q_bits [H, 576] (bf16 bits or float); latent [n, 512], rope [n, 64] float64. The scale
+    defaults to 1/sqrt(576) (the pages do not give it). Returns (out [H, 512], lse [H]);
+    no rows give zeros and -inf."""
+    q = _as_f64(q_bits)
+    rows = np.asarray(rows, dtype=np.int64)
+    if scale is None:
+        scale = 1.0 / np.sqrt(MLA_LATENT + MLA_ROPE)
+    if rows.size == 0:
+        return np.zeros((q.shape[0], MLA_LATENT)), np.full(q.shape[0], -np.inf)
+    k = np.concatenate([latent[rows], rope[rows]], axis=1)
+    v = latent[rows]
+    logits = (q @ k.T) * scale
+    m = logits.max(axis=1)
+    w = np.exp(logits - m[:, None])
+    l = w.sum(axis=1)
+    return (w @ v) / l[:, None], m + np.log(l)
 
 
 def interval_walk_query(p: int, sel, q_bits, k_bits, v_bits, n_kv_heads: int,

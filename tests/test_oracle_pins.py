@@ -451,3 +451,70 @@ def test_score_error_bound_fp8_covers_an_fp32_evaluation():
     got = (pw[:, 0] * scl).astype(np.float32).astype(np.float64)
     assert np.all(np.abs(got - exact) <= bound)
     assert np.all(bound > 0) and np.all(bound <= 1e-5 * (np.abs(vals) @ np.abs(q)) * scl + 1e-30)
+
+
+# --------------------------------------------------------------------------- sparse MLA (MQA form)
+
+def _mla_case(n=40, h=8, seed=51):
+    rng = np.random.default_rng(seed)
+    lat = torch.from_numpy(rng.standard_normal((n, 512)).astype(np.float32) / 8).bfloat16().float().numpy()
+    rope = torch.from_numpy(rng.standard_normal((n, 64)).astype(np.float32) / 8).bfloat16().float().numpy()
+    q = torch.from_numpy(rng.standard_normal((h, 576)).astype(np.float32)).bfloat16().float().numpy()
+    return to_bits(lat), to_bits(rope), to_bits(q)
+
+
+def test_mla_row_quantisation_groups():
+    # each 128-dim group has its own scale: scaling one group by 2^k scales only its scale by
+    # 2^k (codes unchanged); every group's largest code is 448; rope passes through exactly
+    lat, rope, _ = _mla_case(n=6)
+    deq, rp, scl = O.quantize_mla_rows_fp8(lat, rope)
+    assert deq.shape == (6, 512) and scl.shape == (6, 4)
+    np.testing.assert_array_equal(rp, O.bf16_bits_to_f64(rope))
+    lat2 = O.bf16_bits_to_f64(lat).copy()
+    lat2[:, 128:256] *= 2.0 ** -5
+    deq2, _, scl2 = O.quantize_mla_rows_fp8(to_bits(lat2), rope)
+    np.testing.assert_array_equal(scl2[:, 1], scl[:, 1] * np.float32(2.0 ** -5))
+    np.testing.assert_array_equal(deq2[:, 128:256], deq[:, 128:256] * 2.0 ** -5)
+    np.testing.assert_array_equal(np.delete(deq2, np.s_[128:256], axis=1), np.delete(deq, np.s_[128:256], axis=1))
+    codes = deq.reshape(6, 4, 128) / scl.astype(np.float64)[:, :, None]
+    np.testing.assert_allclose(np.abs(codes).max(axis=2), 448.0, rtol=0, atol=0)
+    exact = O.bf16_bits_to_f64(lat)
+    rel = np.abs(deq - exact)[np.abs(exact) > 1e-3] / np.abs(exact)[np.abs(exact) > 1e-3]
+    assert rel.max() <= 2.0 ** -4 * (1 + 1e-6)
+
+
+def test_sparse_mla_attend_vs_sdpa():
+    # every head attends the same selected rows (MQA); the value is the latent, the key adds
+    # the rotary dims: torch's scaled_dot_product_attention in fp64 on the expanded heads
+    lat, rope, qb_ = _mla_case(n=50, h=16)
+    latent, rp, _ = O.quantize_mla_rows_fp8(lat, rope)
+    rows = np.array([3, 7, 8, 20, 31, 32, 49])
+    out, lse = O.sparse_mla_attend(qb_, latent, rp, rows)
+    q = torch.from_numpy(O.bf16_bits_to_f64(qb_))[None, :, None, :]
+    k = torch.from_numpy(np.concatenate([latent[rows], rp[rows]], axis=1))[None, None].expand(1, 16, -1, -1)
+    v = torch.from_numpy(latent[rows])[None, None].expand(1, 16, -1, -1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=1.0 / 24.0)[0, :, 0].numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-14)
+    logits = O.bf16_bits_to_f64(qb_) @ np.concatenate([latent[rows], rp[rows]], axis=1).T / 24.0
+    from scipy.special import logsumexp
+    np.testing.assert_allclose(lse, logsumexp(logits, axis=1), rtol=1e-13)
+
+
+def test_sparse_mla_attend_closed_forms_and_merge():
+    lat, rope, qb_ = _mla_case(n=30, h=4)
+    latent, rp, _ = O.quantize_mla_rows_fp8(lat, rope)
+    # one row: every head outputs that row's latent
+    out, lse = O.sparse_mla_attend(qb_, latent, rp, [11])
+    np.testing.assert_array_equal(out, np.repeat(latent[11][None], 4, axis=0))
+    # no rows
+    out0, lse0 = O.sparse_mla_attend(qb_, latent, rp, [])
+    assert not out0.any() and np.all(np.isneginf(lse0))
+    # log-sum-exp merge of two disjoint halves equals the whole
+    rows = np.arange(30)
+    o1, l1 = O.sparse_mla_attend(qb_, latent, rp, rows[:13])
+    o2, l2 = O.sparse_mla_attend(qb_, latent, rp, rows[13:])
+    ow, lw = O.sparse_mla_attend(qb_, latent, rp, rows)
+    lm = np.logaddexp(l1, l2)
+    np.testing.assert_allclose(lm, lw, rtol=1e-14)
+    np.testing.assert_allclose(np.exp(l1 - lm)[:, None] * o1 + np.exp(l2 - lm)[:, None] * o2, ow, rtol=1e-12,
+                               atol=1e-15)
