@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kF8Threads) index_score_fp8_kernel(const uint1
     const uint8_t *src = codes + (off + lo) * kIdxDim;
     auto issue = [&](int t) {                      // thread 0: tile t into stage t % kF8Stages
         const int st = t % kF8Stages;
-        const uint32_t bytes = (uint32_t)(hi - lo - (int64_t)t * kF8TileRows < kF8TileRows ? hi - lo - (int64_t)t * kF8TileRows : (int64_t)kF8TileRows) * kIdxDim;
+        const int64_t left = hi - lo - (int64_t)t * kF8TileRows;
+        const uint32_t bytes = (uint32_t)(left < kF8TileRows ? left : (int64_t)kF8TileRows) * kIdxDim;
         mbar_arrive_expect_tx(bar + 8 * st, bytes);
         bulk_g2s(ring + st * kF8TileBytes, src + (int64_t)t * kF8TileBytes, bytes, bar + 8 * st);
     };
