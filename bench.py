@@ -52,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kv-host", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-mla", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-instrument", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -498,6 +499,45 @@ def fp8_keys_bench(dl, stream, steps, warmup, pk):
             "gpu_launches_per_layer_step": 5}
 
 
+def mla_bench(steps, warmup, pk, batch=64):
+    """Sparse MLA decode (MQA form, tensor cores): `batch` queries of 64 heads, each over its
+    own 2048 rows of a million-token FP8 cache (656 B per row)."""
+    import torch
+    from indexer_driven_sparse_gb300 import accounting as A
+    from indexer_driven_sparse_gb300 import binding as qb
+    from indexer_driven_sparse_gb300 import inputs as I
+    H, rows = 64, 2048
+    w = I.mla_workload(1 << 20, [rows] * batch, H, seed=0, device="cuda")
+    ws = qb.sparse_mla_workspace(H, batch, rows)
+    out = torch.empty(batch, H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(batch, H, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def call():
+        qb.qsa_sparse_mla_decode(w.q, w.kv, w.rows, w.n_rows, out, lse, ws)
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    st = qb.qsa_read_device_status(ws)
+    if st[0] != 0:
+        raise RuntimeError(f"sparse MLA device status {st}")
+    g = capture(call, stream)
+    n = max(20, steps // 4)
+    t = time_graph(g, stream, n, max(3, warmup), 1) / n
+    del g
+    flops = batch * A.sparse_mla_query_flops(H, rows)
+    nbytes = batch * A.sparse_mla_query_bytes(H, rows)
+    ach = flops / t / 1e12
+    return {"workload": f"sparse MLA decode: {batch} queries x 64 heads, 2048 FP8 rows each (656 B), "
+                        "million-token cache",
+            "queries_per_s": batch / t, "us_per_call": t * 1e6,
+            "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6, "hbm_gbs": nbytes / t / 1e9,
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": ach / pk["bf16"], "traffic": None, "kernel": "mla_tile + mla_merge"},
+            "gpu_launches_per_call": 2}
+
+
 # ----------------------------------------------------------------------------- prefill
 
 def prefill_bench(steps, warmup, pk):
@@ -819,6 +859,9 @@ def main(argv=None):
     if not args.no_fp8:
         line["decode_fp8_indexer_keys"] = fp8_keys_bench(dl, stream, max(20, args.steps // 4), max(3, args.warmup),
                                                          pk)
+
+    if not args.no_mla:
+        line["sparse_mla_decode"] = mla_bench(args.steps, args.warmup, pk)
 
     if not args.no_prefill:
         del g

@@ -321,6 +321,30 @@ QSA_API qsa_status qsa_sparse_decode_noalloc(const qsa_config *cfg, const qsa_bf
                                              const int32_t *blocks, const int32_t *count, qsa_bf16 *out,
                                              float *lse, qsa_stream stream);
 
+/* f3 — Sparse MLA decode in its MQA form ("GLM-5.3 最適化 第2部：16基のH200上でのPCP、DCP、
+ * およびHybrid HiSparse", footnote 1: each query reads 2,048 selected FP8 rows of 656 bytes;
+ * QK runs over 576 dims, PV over 512; every row serves all heads). Row layout, 656 bytes:
+ *   bytes 0..511   the 512-dim latent as E4M3 codes (dim d at byte d),
+ *   bytes 512..527 four fp32 scales (scale g applies to latent dims 128g .. 128g+127),
+ *   bytes 528..655 the 64 rotary dims as bf16.
+ * With latent_j = code x scale and k_j = [latent_j, rope_j], query b's head h gives
+ *   out[b][h] = sum_j softmax_j(scale_qk * q[b][h] . k_j) latent_j,  lse[b][h] = ln sum_j e^(...)
+ * over j in rows[b][0 .. n_rows[b]) (token ids, any order, no repeats).
+ *   q [B, n_heads, 576] bf16, 16-byte aligned; kv_rows [n_tokens, 656] uint8, 16-byte aligned;
+ *   rows [B, max_rows] int32; n_rows [B] int32 (<= max_rows); out [B, n_heads, 512] bf16;
+ *   lse [B, n_heads] fp32 or NULL; softmax_scale <= 0 selects 1/sqrt(576).
+ * Tensor cores: tiles of 64 selected rows; latent values rounded once to bf16 for the MMA
+ * (code x scale in fp32, then bf16), P rounded to bf16; fp32 accumulation; the tiles'
+ * partials merged by log-sum-exp. n_heads 1..128 (MMA rows; else QSA_ERR_UNSUPPORTED).
+ * Workspace: qsa_sparse_mla_workspace_size(n_heads, B, max_rows) bytes (status block + the
+ * tiles' partials); device checks: 0 <= row id < n_tokens, n_rows <= max_rows (a bad row is
+ * skipped and QSA_ERR_DEVICE_BOUNDS recorded). */
+QSA_API size_t qsa_sparse_mla_workspace_size(int32_t n_heads, int32_t B, int32_t max_rows);
+QSA_API qsa_status qsa_sparse_mla_decode(const qsa_bf16 *q, int32_t n_heads, const uint8_t *kv_rows,
+                                         int64_t n_tokens, const int32_t *rows, const int32_t *n_rows,
+                                         int32_t max_rows, int32_t B, float softmax_scale, qsa_bf16 *out, float *lse,
+                                         void *ws, size_t ws_bytes, qsa_stream stream);
+
 /* Static description of a status code. */
 QSA_API const char *qsa_status_string(qsa_status s);
 

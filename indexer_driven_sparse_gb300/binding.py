@@ -69,6 +69,8 @@ _SIGNATURES = {
     "qsa_index_score_fp8": (_I32, [_CFG, _P, _P, _P, _I32, _P, _P, _I64, _P, _P, _I64, _P, _SZ, _P]),
     "qsa_decode_step_fp8": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P,
                                     _P, _P, _P, _SZ, _P]),
+    "qsa_sparse_mla_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "qsa_sparse_mla_decode": (_I32, [_P, _I32, _P, _I64, _P, _P, _I32, _I32, C.c_float, _P, _P, _P, _SZ, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
     "qsa_last_error": (C.c_char_p, []),
     "qsa_version": (C.c_char_p, []),
@@ -265,6 +267,29 @@ def qsa_sparse_prefill_chunk(cfg, q, p0, k_cache, v_cache, blocks, count, interv
                                            _ptr(blocks, torch.int32), _ptr(count, torch.int32), int(interval_tokens),
                                            _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
                                            *_ws_args(ws), _stream(stream)), "qsa_sparse_prefill_chunk")
+
+
+def sparse_mla_workspace(n_heads: int, B: int, max_rows: int, device="cuda", stream=None):
+    """A zero-initialised workspace for qsa_sparse_mla_decode (allocated by torch)."""
+    n = int(load().qsa_sparse_mla_workspace_size(n_heads, B, max_rows))
+    if n == 0:
+        raise QsaError(QSA_ERR_UNSUPPORTED, "unsupported sparse-MLA geometry")
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    qsa_workspace_init(ws, stream)
+    return ws
+
+
+def qsa_sparse_mla_decode(q, kv_rows, rows, n_rows, out, lse, ws, softmax_scale: float = 0.0, stream=None):
+    """q [B, H, 576] bf16; kv_rows [T, 656] uint8; rows [B, max_rows] int32; n_rows [B] int32;
+    out [B, H, 512] bf16; lse [B, H] fp32 or None."""
+    B, H = q.shape[0], q.shape[1]
+    _check(load().qsa_sparse_mla_decode(_ptr(q, torch.bfloat16, "q"), H, _ptr(kv_rows, torch.uint8, "kv_rows"),
+                                        kv_rows.shape[0], _ptr(rows, torch.int32, "rows"),
+                                        _ptr(n_rows, torch.int32, "n_rows"), rows.shape[1], B, float(softmax_scale),
+                                        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                                        *_ws_args(ws), _stream(stream)), "qsa_sparse_mla_decode")
 
 
 def version() -> str:

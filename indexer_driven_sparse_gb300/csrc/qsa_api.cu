@@ -463,6 +463,36 @@ QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *ra
                               blocks, count, out, lse, ws, ws_bytes, stream);
 }
 
+QSA_API size_t qsa_sparse_mla_workspace_size(int32_t n_heads, int32_t B, int32_t max_rows) {
+    if (n_heads < 1 || n_heads > 128 || B < 0 || B > kMaxGridYZ || max_rows < 0 || max_rows > 65536) return 0;
+    return kWsHeaderBytes + mla_scratch_bytes(n_heads, B, max_rows);
+}
+
+QSA_API qsa_status qsa_sparse_mla_decode(const qsa_bf16 *q, int32_t n_heads, const uint8_t *kv_rows,
+                                         int64_t n_tokens, const int32_t *rows, const int32_t *n_rows,
+                                         int32_t max_rows, int32_t B, float softmax_scale, qsa_bf16 *out, float *lse,
+                                         void *ws, size_t ws_bytes, qsa_stream stream) {
+    if (n_heads < 1 || n_heads > 128) return fail(QSA_ERR_UNSUPPORTED, "n_heads = %d (1 .. 128)", n_heads);
+    QSA_NEED(B >= 0 && B <= kMaxGridYZ, "B = %d out of range [0, 65535]", B);
+    QSA_NEED(max_rows >= 0 && max_rows <= 65536, "max_rows = %d out of range [0, 65536]", max_rows);
+    QSA_NEED(n_tokens >= 0, "negative size");
+    QSA_NEED(!(softmax_scale > 0.f) || isfinite(softmax_scale), "softmax_scale must be finite");
+    QSA_NEED(ws != nullptr && aligned(ws, 256), "workspace must be non-NULL and 256-byte aligned");
+    const size_t need = qsa_sparse_mla_workspace_size(n_heads, B, max_rows);
+    if (ws_bytes < need) return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, need);
+    if (B == 0) return ok();
+    QSA_NEED(q && kv_rows && rows && n_rows && out, "NULL tensor pointer");
+    QSA_NEED(aligned(q, 16) && aligned(kv_rows, 16), "q and kv_rows must be 16-byte aligned");
+    QSA_NEED(aligned(out, 2) && aligned(rows, 4) && aligned(n_rows, 4) && aligned(lse, 4), "misaligned output");
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(576.0f);
+    char *w = static_cast<char *>(ws);
+    const cudaError_t e = launch_sparse_mla(q, n_heads, kv_rows, n_tokens, rows, n_rows, max_rows, B, scale, out, lse,
+                                            reinterpret_cast<WsHeader *>(w), w + kWsHeaderBytes,
+                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_decode launch");
+    return ok();
+}
+
 QSA_API const char *qsa_status_string(qsa_status s) {
     switch (s) {
         case QSA_OK: return "ok";

@@ -195,3 +195,43 @@ def million_decode(seed=0, device="cuda", n_layers=12):
 def prefill_chunk(seed=0, device="cuda", kind="planted", rho=PREFILL_RHO, p0=262144, n_chunk=4096):
     """4096 chunk queries over a 262,144-token history, 16 query / 2 KV heads."""
     return prefill_workload(f"prefill_chunk_p{p0}_n{n_chunk}", p0, n_chunk, 16, 2, kind, rho, seed, device)
+
+
+# ----------------------------------------------------------------------------- sparse MLA (FP8 rows)
+
+MLA_ROW_BYTES = 656        # 512 E4M3 latent codes, 4 fp32 group scales, 64 bf16 rotary dims
+MLA_QK_DIM = 576
+
+
+@dataclass
+class MlaWorkload:
+    kv: torch.Tensor           # [n_tokens, 656] uint8 rows
+    q: torch.Tensor            # [B, H, 576] bf16
+    rows: torch.Tensor         # [B, max_rows] int32 selected token ids (ascending, -1 padded)
+    n_rows: torch.Tensor       # [B] int32
+
+
+def mla_workload(n_tokens: int, n_rows, n_heads: int = 64, seed: int = 0, device="cpu") -> MlaWorkload:
+    """A synthetic FP8 sparse-MLA cache and a batch of decode queries, each with its own
+    selected rows. Row bytes: random E4M3 codes (sign and a magnitude byte drawn from
+    0x08..0x77, normal values 2^-6 .. 240), four fp32 scales 2^-9 * U(0.5, 1) and 64 bf16
+    rotary values N(0,1)/8. Queries are bf16 16 N(0,1) (logits of std about 1 under the
+    1/sqrt(576) scale, so the softmax is far from uniform). Each query's rows are a uniform random
+    subset of the tokens, ascending. Creation order: codes, scales, rope, queries, subsets."""
+    g = _gen(seed, device)
+    n_rows = [int(n) for n in n_rows]
+    B, mr = len(n_rows), max(max(n_rows, default=1), 1)
+    sign = torch.randint(0, 2, (n_tokens, 512), generator=g, device=device, dtype=torch.int32)
+    mag = torch.randint(0x08, 0x78, (n_tokens, 512), generator=g, device=device, dtype=torch.int32)
+    codes = (sign * 128 + mag).to(torch.uint8)
+    scales = torch.rand((n_tokens, 4), generator=g, device=device, dtype=torch.float32).mul_(0.5).add_(0.5)
+    scales.mul_(2.0 ** -9)
+    rope = _randn((n_tokens, 64), g, device, 1.0 / 8.0).to(torch.bfloat16)
+    kv = torch.cat([codes, scales.view(torch.uint8), rope.view(torch.uint8)], dim=1).contiguous()
+    q = _randn((B, n_heads, MLA_QK_DIM), g, device, 16.0).to(torch.bfloat16)
+    rows = torch.full((B, mr), -1, dtype=torch.int32, device=device)
+    for b, n in enumerate(n_rows):
+        if n:
+            sel = torch.randperm(n_tokens, generator=g, device=device)[:n].sort().values
+            rows[b, :n] = sel.to(torch.int32)
+    return MlaWorkload(kv, q, rows, torch.tensor(n_rows, dtype=torch.int32, device=device))

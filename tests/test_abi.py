@@ -222,3 +222,19 @@ def test_decode_step_fp8_host_checks(lib):
     assert b"multiple of 4" in lib.qsa_last_error()
     assert lib.qsa_decode_step(C.byref(c), FAKE, 0, 1000, FAKE, FAKE, FAKE, FAKE, FAKE, 4001, FAKE, FAKE, 1, 1000,
                                FAKE, FAKE, FAKE, 0, FAKE, need, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+
+
+def test_sparse_mla_host_checks(lib):
+    need = lib.qsa_sparse_mla_workspace_size(64, 4, 2048)
+    assert need == 256 + 4 * 32 * 2 * 64 * 256 * 4 + 4 * 32 * 64 * 2 * 4 + 256
+    assert lib.qsa_sparse_mla_workspace_size(0, 4, 2048) == 0
+    assert lib.qsa_sparse_mla_workspace_size(129, 4, 2048) == 0
+    assert lib.qsa_sparse_mla_workspace_size(64, 4, 70000) == 0
+    args = lambda q, heads, B, ws_bytes: (q, heads, FAKE, 1000, FAKE, FAKE, 2048, B, C.c_float(0.0), FAKE, 0, FAKE,
+                                          ws_bytes, 0)
+    assert lib.qsa_sparse_mla_decode(*args(FAKE, 64, 0, need)) == qb.QSA_OK                # empty batch
+    assert lib.qsa_sparse_mla_decode(*args(FAKE, 200, 4, need)) == qb.QSA_ERR_UNSUPPORTED
+    assert lib.qsa_sparse_mla_decode(*args(FAKE, 64, 4, need - 1)) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.qsa_sparse_mla_decode(*args(FAKE + 8, 64, 4, need)) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"aligned" in lib.qsa_last_error()
+    assert lib.qsa_sparse_mla_decode(*args(0, 64, 4, need)) == qb.QSA_ERR_INVALID_ARGUMENT

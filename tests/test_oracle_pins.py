@@ -518,3 +518,23 @@ def test_sparse_mla_attend_closed_forms_and_merge():
     np.testing.assert_allclose(lm, lw, rtol=1e-14)
     np.testing.assert_allclose(np.exp(l1 - lm)[:, None] * o1 + np.exp(l2 - lm)[:, None] * o2, ow, rtol=1e-12,
                                atol=1e-15)
+
+
+def test_mla_row_bytes_decode_by_hand():
+    # one 656-byte row built by hand: codes 0x38 (1.0), 0x01 (2^-9), 0xFE (-448), 0x00, 0x80
+    # (zero), the four group scales 0.5, 2, 0.25, 8, and rope = bf16 1.5 and -3 alternating
+    row = np.zeros(656, np.uint8)
+    row[0], row[1], row[2], row[3], row[4] = 0x38, 0x01, 0xFE, 0x00, 0x80
+    row[128], row[300], row[511] = 0x38, 0x39, 0x40       # 1.0 in group 1, 1.125 in group 2, 2.0 in group 3
+    row[512:528] = np.array([0.5, 2.0, 0.25, 8.0], dtype="<f4").view(np.uint8)
+    rope = np.array([1.5, -3.0] * 32, dtype=np.float32)
+    row[528:] = to_bits(rope).astype("<u2").view(np.uint8)
+    lat, rp = O.mla_rows_from_bytes(row[None])
+    assert O.MLA_ROW_BYTES == 656 and lat.shape == (1, 512) and rp.shape == (1, 64)
+    assert lat[0, 0] == 0.5 and lat[0, 1] == 2.0 ** -10 and lat[0, 2] == -224.0 and lat[0, 3] == 0.0
+    assert lat[0, 4] == 0.0 and lat[0, 128] == 2.0 and lat[0, 300] == 1.125 * 0.25 and lat[0, 511] == 16.0
+    assert np.count_nonzero(lat) == 6
+    np.testing.assert_array_equal(rp[0], rope)
+    assert np.isnan(O.e4m3_value(0x7F)) and np.isnan(O.e4m3_value(0xFF))
+    vals, _ = _e4m3_table()
+    np.testing.assert_array_equal(np.sort(O.e4m3_value(np.arange(0x7F))), vals)      # every finite code
