@@ -40,7 +40,7 @@ __all__ = [
     "interval_walk_query", "score_error_bound",
     "E4M3_MAX", "e4m3_round", "quantize_pooled_fp8", "score_blocks_fp8", "decode_query_fp8",
     "score_error_bound_fp8", "MLA_LATENT", "MLA_ROPE", "MLA_GROUP", "quantize_mla_rows_fp8",
-    "sparse_mla_attend",
+    "sparse_mla_attend", "MLA_ROW_BYTES", "e4m3_value", "mla_rows_from_bytes",
 ]
 
 # indexer_compress_ratio and indexer_budget from the model's text_config
@@ -400,6 +400,33 @@ def quantize_mla_rows_fp8(latent_bits, rope_bits):
     deq = vals * scl.astype(np.float64)[:, None]
     return (deq.reshape(n, MLA_LATENT), bf16_bits_to_f64(np.asarray(rope_bits)).reshape(n, MLA_ROPE),
             scl.reshape(n, MLA_LATENT // MLA_GROUP))
+
+
+MLA_ROW_BYTES = MLA_LATENT + 4 * (MLA_LATENT // MLA_GROUP) + 2 * MLA_ROPE   # 656
+
+
+def e4m3_value(code) -> np.ndarray:
+    """Value of E4M3 byte codes from the bit layout: sign, 4 exponent bits (bias 7), 3
+    mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); 0x7F and 0xFF are NaN."""
+    c = np.asarray(code, dtype=np.int64)
+    s, e, m = c >> 7, (c >> 3) & 15, c & 7
+    v = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return np.where(s == 1, -v, v)
+
+
+def mla_rows_from_bytes(row_bytes) -> tuple:
+    """Decode FP8 MLA rows as stored (reading of the 656-byte row): bytes 0..511 the latent's
+    E4M3 codes, 512..527 four little-endian fp32 scales (one per 128 latent dims), 528..655
+    the 64 rotary dims as bf16. Returns (latent [n, 512], rope [n, 64]) in float64, the
+    latent exactly code x scale."""
+    r = np.ascontiguousarray(np.asarray(row_bytes, dtype=np.uint8)).reshape(-1, MLA_ROW_BYTES)
+    n = r.shape[0]
+    codes = e4m3_value(r[:, :MLA_LATENT])
+    scales = r[:, MLA_LATENT:MLA_LATENT + 16].copy().view("<f4").astype(np.float64)
+    latent = (codes.reshape(n, 4, MLA_GROUP) * scales[:, :, None]).reshape(n, MLA_LATENT)
+    rope = bf16_bits_to_f64(r[:, MLA_LATENT + 16:].copy().view("<u2"))
+    return latent, rope
 
 
 def sparse_mla_attend(q_bits, latent: np.ndarray, rope: np.ndarray, rows, scale: float | None = None):
