@@ -529,12 +529,16 @@ def mla_bench(steps, warmup, pk, batch=64):
     flops = batch * A.sparse_mla_query_flops(H, rows)
     nbytes = batch * A.sparse_mla_query_bytes(H, rows)
     ach = flops / t / 1e12
+    # DRAM bytes of the tile kernel from its capture on 16 queries, scaled by the query count
+    # (each query's tiles read and write the same amounts)
+    cap = recorded_traffic("mla_tile")
+    traffic = cap * batch / 16 if cap is not None else None
     return {"workload": f"sparse MLA decode: {batch} queries x 64 heads, 2048 FP8 rows each (656 B), "
                         "million-token cache",
             "queries_per_s": batch / t, "us_per_call": t * 1e6,
             "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6, "hbm_gbs": nbytes / t / 1e9,
             "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
-                         "frac": ach / pk["bf16"], "traffic": None, "kernel": "mla_tile + mla_merge"},
+                         "frac": ach / pk["bf16"], "traffic": traffic, "kernel": "mla_tile + mla_merge"},
             "gpu_launches_per_call": 2}
 
 
@@ -643,6 +647,22 @@ def _case_decode_fp8(reps):
     return st if st[0] != 0 else b.fused_status()
 
 
+def _case_mla(reps):
+    """Sparse MLA decode: 16 queries x 64 heads over 2048 rows each of a million-token FP8
+    cache (about 0.7 GB on the device), `reps` calls."""
+    import torch
+    from indexer_driven_sparse_gb300 import binding as qb
+    from indexer_driven_sparse_gb300 import inputs as I
+    w = I.mla_workload(1 << 20, [2048] * 16, 64, seed=0, device="cuda")
+    ws = qb.sparse_mla_workspace(64, 16, 2048)
+    out = torch.empty(16, 64, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(16, 64, dtype=torch.float32, device="cuda")
+    for _ in range(reps):
+        qb.qsa_sparse_mla_decode(w.q, w.kv, w.rows, w.n_rows, out, lse, ws)
+    torch.cuda.synchronize()
+    return qb.qsa_read_device_status(ws)
+
+
 def _case_prefill(reps, attention_only):
     """The prefill chunk (4096 queries over 262,144 tokens, about 1.1 GB on the device):
     pool + score + top-k once, then `reps` chunk attentions (or whole chunks)."""
@@ -667,6 +687,7 @@ def _case_prefill(reps, attention_only):
 CASES = {
     "decode_step": lambda reps: _case_decode_step(reps),
     "decode_fp8": lambda reps: _case_decode_fp8(reps),
+    "mla": lambda reps: _case_mla(reps),
     "prefill_attention": lambda reps: _case_prefill(reps, True),
     "prefill_chunk": lambda reps: _case_prefill(reps, False),
 }
