@@ -12,6 +12,14 @@
 
 using namespace qsa;
 
+namespace qsa {
+// Sparse MLA decode, MQA form, on the tensor cores (mla.cu).
+size_t mla_scratch_bytes(int H, int B, int max_rows);
+cudaError_t launch_sparse_mla(const uint16_t *q, int H, const uint8_t *kv, int64_t n_tok, const int32_t *rows,
+                              const int32_t *n_rows, int max_rows, int B, float scale, uint16_t *out, float *lse,
+                              WsHeader *hdr, void *scratch, cudaStream_t st);
+}  // namespace qsa
+
 namespace {
 
 thread_local char g_last_error[512] = "";

@@ -267,12 +267,6 @@ int decode_step_max_keys();
 int decode_step_grid(int G, bool fp8);
 cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st);
 
-// Sparse MLA decode, MQA form, on the tensor cores (mla.cu).
-size_t mla_scratch_bytes(int H, int B, int max_rows);
-cudaError_t launch_sparse_mla(const uint16_t *q, int H, const uint8_t *kv, int64_t n_tok, const int32_t *rows,
-                              const int32_t *n_rows, int max_rows, int B, float scale, uint16_t *out, float *lse,
-                              WsHeader *hdr, void *scratch, cudaStream_t st);
-
 // Set the calling thread's qsa_last_error() text to "<what>: <detail>" and return s.
 qsa_status host_fail(qsa_status s, const char *what, const char *detail);
 cudaError_t launch_sparse_prefill(const AttnArgs &a, int interval_tokens, WsHeader *hdr, void *scratch,
