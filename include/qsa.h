@@ -337,8 +337,10 @@ QSA_API qsa_status qsa_sparse_decode_noalloc(const qsa_config *cfg, const qsa_bf
  * (code x scale in fp32, then bf16), P rounded to bf16; fp32 accumulation; the tiles'
  * partials merged by log-sum-exp. n_heads 1..128 (MMA rows; else QSA_ERR_UNSUPPORTED).
  * Workspace: qsa_sparse_mla_workspace_size(n_heads, B, max_rows) bytes (status block + the
- * tiles' partials); device checks: 0 <= row id < n_tokens, n_rows <= max_rows (a bad row is
- * skipped and QSA_ERR_DEVICE_BOUNDS recorded). */
+ * tiles' partials); device checks: 0 <= row id < n_tokens (a bad row is skipped and
+ * QSA_ERR_DEVICE_BOUNDS recorded); n_rows[b] is clamped to [0, max_rows], a value above
+ * max_rows also recording QSA_ERR_DEVICE_BOUNDS. A query with no rows gets out = 0 and
+ * lse = -inf. */
 QSA_API size_t qsa_sparse_mla_workspace_size(int32_t n_heads, int32_t B, int32_t max_rows);
 QSA_API qsa_status qsa_sparse_mla_decode(const qsa_bf16 *q, int32_t n_heads, const uint8_t *kv_rows,
                                          int64_t n_tokens, const int32_t *rows, const int32_t *n_rows,
