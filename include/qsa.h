@@ -303,12 +303,15 @@ QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *ra
 /* Allocation-free variant of qsa_sparse_decode (the pages have no counterpart; this
  * is a library convenience). Same arguments and result, but no workspace: the split
  * partials live in a 16 MiB static device array inside the library, for callers that
- * cannot allocate device memory at all (code running under global-mode stream
- * capture, plug-in hosts that own all device memory, loops that must not risk an
- * allocation's implicit synchronisation).
+ * cannot allocate device memory at all (a plug-in inside a host application that owns
+ * the whole device memory pool, a process whose device memory another allocator has
+ * fully reserved, loops that must not risk an allocation's implicit synchronisation).
  *  - Limit: qsa_workspace_size(QSA_OP_SPARSE_DECODE, cfg, B, 0) must not exceed 16 MiB
  *    (B <= 30 at 16 query / 2 KV heads, B <= 61 at 8 / 2); larger batches return
- *    QSA_ERR_WORKSPACE_TOO_SMALL with nothing enqueued.
+ *    QSA_ERR_WORKSPACE_TOO_SMALL. Every host check (configuration, sizes, pointers, the
+ *    stream's device) runs before anything is enqueued.
+ *  - `stream` must belong to the current device (else QSA_ERR_INVALID_ARGUMENT): the
+ *    array has one address per device.
  *  - The first call on a device resolves the array's device address
  *    (cudaGetSymbolAddress, with that device current); make it before any stream capture.
  *  - The array stays resident on every GPU that loads the library until exit.

@@ -22,17 +22,16 @@
 //      softmax rows      one thread per row, online max/sum in base 2 with a lazy rescale
 //                        of O (only when the running max grows by more than 2^8)
 //      O += P V          (M=128, N=256, K=64)    into TMEM columns [256, 512)
-//    Roles:
+//    Roles (512 threads):
 //      warps 0-3   softmax: one row per thread; at a tile's end, O / l -> bf16 and the LSE;
-//      warps 4-13  V rows: per chunk 64 tokens x 512 bytes as 16-byte cp.async into
-//                  128-byte-swizzled shared memory (two stages). Many warps: a warp's
-//                  cp.async issue stalls on the memory system, so rows arrive faster the
-//                  more warps issue them;
-//      warp 14     one thread drives the tensor-memory-access engine: chunk records (bulk
-//                  copies, one ahead), the Q tile, and the K rows (two stages), one tiled
-//                  load per block and 64-column slice (4 tokens x 128 bytes, swizzled). K
-//                  and V thus travel on two independent paths from L2, the copy engine's
-//                  and the load/store units', which together outrun either alone;
+//      warps 4-9   K producers: the leading thread bulk-copies chunk records two ahead; the
+//                  six warps load each new tile's Q rows and every chunk's K rows (64 tokens
+//                  x 512 bytes) as 16-byte cp.async into 128-byte-swizzled shared memory,
+//                  two stages;
+//      warps 10-14 V producers: the V rows the same way into their own two stages. Each
+//                  producer warp follows the mbarriers on its own, so a slow warp holds back
+//                  no other; many issuing warps make rows arrive faster, since one warp's
+//                  cp.async issue stalls on the memory system;
 //      warp 15     one thread issues the MMAs: QK of chunk g+1 before PV of chunk g, so the
 //                  tensor core computes the next scores while the softmax runs.
 //    Hand-offs are mbarriers (cp.async arrivals, tcgen05.commit, thread arrivals).

@@ -290,20 +290,36 @@ QSA_API qsa_status qsa_topk_blocks(const qsa_config *cfg, const float *scores, i
     return ok();
 }
 
-QSA_API qsa_status qsa_sparse_decode(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *k_cache,
-                                     const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
-                                     const int32_t *ctx_len, int32_t B, const int32_t *blocks, const int32_t *count,
-                                     qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, qsa_stream stream) {
+}  // extern "C"
+
+qsa_status qsa::sparse_decode_shape_check(const qsa_config *cfg, int32_t B, int64_t n_tokens_total) {
     QSA_TRY(check_config(cfg));
     QSA_NEED(B >= 0 && B <= kMaxGridYZ, "B = %d out of range [0, 65535]", B);
     QSA_NEED(n_tokens_total >= 0, "negative size");
-    QSA_TRY(check_ws(QSA_OP_SPARSE_DECODE, cfg, B, 0, ws, ws_bytes));
-    if (B == 0) return ok();
+    return QSA_OK;
+}
+
+qsa_status qsa::sparse_decode_pointer_check(const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                            const int32_t *tok_off, const int32_t *ctx_len, const int32_t *blocks,
+                                            const int32_t *count, const qsa_bf16 *out) {
     QSA_NEED(q && k_cache && v_cache && tok_off && ctx_len && blocks && count && out, "NULL tensor pointer");
     QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16),
              "q, k_cache, v_cache and out must be 16-byte aligned");
     QSA_NEED(device_accessible(k_cache) && device_accessible(v_cache),
              "k_cache and v_cache must be device memory or mapped pinned host memory");
+    return QSA_OK;
+}
+
+extern "C" {
+
+QSA_API qsa_status qsa_sparse_decode(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                     const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
+                                     const int32_t *ctx_len, int32_t B, const int32_t *blocks, const int32_t *count,
+                                     qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(sparse_decode_shape_check(cfg, B, n_tokens_total));
+    QSA_TRY(check_ws(QSA_OP_SPARSE_DECODE, cfg, B, 0, ws, ws_bytes));
+    if (B == 0) return ok();
+    QSA_TRY(sparse_decode_pointer_check(q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out));
     char *w = static_cast<char *>(ws);
     AttnArgs a{};
     a.q = q;

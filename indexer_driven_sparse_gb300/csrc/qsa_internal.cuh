@@ -269,6 +269,13 @@ cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st);
 
 // Set the calling thread's qsa_last_error() text to "<what>: <detail>" and return s.
 qsa_status host_fail(qsa_status s, const char *what, const char *detail);
+// The host checks of qsa_sparse_decode, in its order: the configuration, B and the token
+// count first; the tensor pointers (non-NULL, 16-byte alignment, readable by the device) once
+// the workspace has been checked and B > 0. Each records its message as qsa_last_error.
+qsa_status sparse_decode_shape_check(const qsa_config *cfg, int32_t B, int64_t n_tokens_total);
+qsa_status sparse_decode_pointer_check(const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                       const int32_t *tok_off, const int32_t *ctx_len, const int32_t *blocks,
+                                       const int32_t *count, const qsa_bf16 *out);
 cudaError_t launch_sparse_prefill(const AttnArgs &a, int interval_tokens, WsHeader *hdr, void *scratch,
                                   size_t scratch_bytes, cudaStream_t st);
 

@@ -13,6 +13,8 @@ Distributions (no page measures this path on a dataset; all inputs are synthetic
   128x8 basis; block b draws z_b ~ N(0, I8) and its tokens' raw keys are
   U z_b + eps/sqrt(128); a query draws a ~ N(0, I8) and q_idx = U a + eta/sqrt(128).
 * "sharp": Q/K/V ~ N(0,1) (logit std about 1) instead of N(0,1)/sqrt(256).
+* "planted_sharp": the planted indexer tensors with sharp Q/K/V (the prefill chunk's
+  selection structure with outputs large enough to grade by relative error).
 * Prefill queries can be temporally correlated: a_i = rho a_(i-1) + sqrt(1-rho^2) xi_i,
   which makes consecutive queries' selections overlap (rho is chosen so that
   the mean overlap of consecutive top-512 selections is about 0.72, the value
@@ -100,8 +102,8 @@ def _planted_basis(g, device):
 def _layer(n_tok: int, n_q: int, hq: int, hkv: int, kind: str, g, device,
            block_of_token=None, rho: float = 0.0) -> Layer:
     s_idx = 1.0 / math.sqrt(IDX_DIM)
-    s_head = 1.0 if kind == "sharp" else 1.0 / math.sqrt(HEAD_DIM)
-    if kind == "planted":
+    s_head = 1.0 if kind in ("sharp", "planted_sharp") else 1.0 / math.sqrt(HEAD_DIM)
+    if kind in ("planted", "planted_sharp"):
         u = _planted_basis(g, device)
         if block_of_token is None:
             block_of_token = torch.arange(n_tok, device=device) // RATIO
@@ -133,7 +135,7 @@ def decode_workload(name: str, ctx_len, n_layers: int, n_q_heads: int, n_kv_head
     w = Workload(name, n_q_heads, n_kv_heads, [int(p) for p in ctx_len])
     g = _gen(seed, device)
     blocks = None
-    if kind == "planted":
+    if kind in ("planted", "planted_sharp"):
         # block index of every flat token, so that blocks never straddle sequences
         parts, base = [], 0
         for p in w.ctx_len:
@@ -175,21 +177,21 @@ def tiny_decode(seed=0, device="cpu", kind="gaussian"):
     return decode_workload("tiny_decode_ctx4096", [4096], 1, 8, 2, kind, seed, device)
 
 
-def long_decode(seed=0, device="cuda", n_layers=12):
+def long_decode(seed=0, device="cuda", n_layers=12, kind="planted"):
     """Batch 1 at context 131072, 12 layers, 16 query / 2 KV heads, planted indexer."""
-    return decode_workload("long_decode_ctx131072", [131072], n_layers, 16, 2, "planted", seed, device)
+    return decode_workload("long_decode_ctx131072", [131072], n_layers, 16, 2, kind, seed, device)
 
 
-def batched_decode(seed=0, device="cuda", n_layers=12, short_draw=False):
+def batched_decode(seed=0, device="cuda", n_layers=12, short_draw=False, kind="gaussian"):
     """Batch 32, contexts uniform in [4096, 65536], 12 layers, 8 query / 2 KV heads."""
     lens = batched_ctx_lens(short_draw=short_draw, seed=seed)
     name = "batched_decode_b32" + ("_short" if short_draw else "")
-    return decode_workload(name, lens, n_layers, 8, 2, "gaussian", seed, device)
+    return decode_workload(name, lens, n_layers, 8, 2, kind, seed, device)
 
 
-def million_decode(seed=0, device="cuda", n_layers=12):
+def million_decode(seed=0, device="cuda", n_layers=12, kind="planted"):
     """Batch 1 at context 1,048,320 (262,080 blocks), 12 layers, 16 query / 2 KV heads."""
-    return decode_workload("million_decode_ctx1048320", [1048320], n_layers, 16, 2, "planted", seed, device)
+    return decode_workload("million_decode_ctx1048320", [1048320], n_layers, 16, 2, kind, seed, device)
 
 
 def prefill_chunk(seed=0, device="cuda", kind="planted", rho=PREFILL_RHO, p0=262144, n_chunk=4096):

@@ -38,7 +38,7 @@ __all__ = [
     "score_blocks", "kth_score", "select_blocks", "attended_tokens",
     "attend_partial", "lse_merge", "attend", "decode_query",
     "interval_walk_query", "score_error_bound",
-    "E4M3_MAX", "e4m3_round", "quantize_pooled_fp8", "score_blocks_fp8", "decode_query_fp8",
+    "E4M3_MAX", "e4m3_round", "quantize_pooled_fp8", "score_blocks_fp8",
     "score_error_bound_fp8", "MLA_LATENT", "MLA_ROPE", "MLA_GROUP", "quantize_mla_rows_fp8",
     "sparse_mla_attend", "MLA_ROW_BYTES", "e4m3_value", "mla_rows_from_bytes",
 ]
@@ -362,19 +362,6 @@ def decode_query(p: int, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_kv_h
     # attend over the compacted rows (row j of kk is token tokens[j])
     out, lse = attend(q, kk, vv, np.arange(tokens.size), n_kv_heads, scale)
     return dict(scores=scores, sel=np.asarray(sel, dtype=np.int64), tokens=tokens, out=out, lse=lse)
-
-
-def decode_query_fp8(p: int, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_kv_heads: int,
-                     scale: float | None = None, k_blocks: int = BLOCK_TOPK, sel=None):
-    """decode_query with the selection scored against FP8 copies of the pooled keys."""
-    nb = visible_blocks(p)
-    vals, scl = quantize_pooled_fp8(np.asarray(pooled_bits)[:nb])
-    scores = score_blocks_fp8(q_idx_bits, vals, scl)
-    if sel is None:
-        sel = select_blocks(scores, k_blocks)
-    r = decode_query(p, q_idx_bits, pooled_bits, q_bits, k_bits, v_bits, n_kv_heads, scale, k_blocks, sel=sel)
-    r["scores"] = scores
-    return r
 
 
 # --------------------------------------------------------------------------- sparse MLA (MQA form)

@@ -160,6 +160,82 @@ def test_scores_basis_vectors():
     assert np.array_equal(O.score_blocks(q, eye), np.arange(128) - 64.0)
 
 
+def _fp32_sums(prods):
+    """float32 sums of each row of exact float32 products in three orders: sequential,
+    reversed and pairwise (tree)."""
+    out = []
+    for order in (slice(None), slice(None, None, -1)):
+        acc = np.zeros(prods.shape[0], np.float32)
+        for d in range(prods.shape[1])[order]:
+            acc = (acc + prods[:, d]).astype(np.float32)
+        out.append(acc.astype(np.float64))
+    pw = prods.copy()
+    while pw.shape[1] > 1:
+        pw = (pw[:, 0::2] + pw[:, 1::2]).astype(np.float32)
+    out.append(pw[:, 0].astype(np.float64))
+    return out
+
+
+def test_score_error_bound_covers_fp32_evaluations():
+    # random rows, rows with heavy cancellation and rows of mixed magnitudes: a float32
+    # evaluation of q . p (exact bf16 x bf16 products, float32 additions) in each of three
+    # orders stays within the bound of the exact score
+    rng = np.random.default_rng(61)
+    keys = rng.standard_normal((300, 128)).astype(np.float32) / 8
+    keys[100:200] *= np.exp2(rng.integers(-20, 20, (100, 128))).astype(np.float32)
+    q = rng.standard_normal(128).astype(np.float32)
+    kb, qb_ = to_bits(torch.from_numpy(keys).bfloat16().float().numpy()), None
+    qv = torch.from_numpy(q).bfloat16().float().numpy()
+    keys_v = O.bf16_bits_to_f64(kb)
+    # rows 200..299: p_d = +-q_d-ish so the sum nearly cancels
+    sign = np.where(rng.random((100, 128)) < 0.5, -1.0, 1.0)
+    keys_v[200:] = torch.from_numpy((sign * qv[None, :] * (1 + rng.random((100, 128)) / 64)).astype(np.float32)
+                                    ).bfloat16().double().numpy()
+    kb = to_bits(keys_v)
+    qb_ = to_bits(qv)
+    exact = O.score_blocks(qb_, kb)
+    bound = O.score_error_bound(qb_, kb)
+    prods = (keys_v.astype(np.float32) * qv[None, :]).astype(np.float32)
+    assert np.array_equal(prods.astype(np.float64), keys_v * qv[None, :].astype(np.float64))   # exact
+    worst = 0.0
+    for got in _fp32_sums(prods):
+        err = np.abs(got - exact)
+        assert np.all(err <= bound)
+        worst = max(worst, float(np.max(err / bound)))
+    assert worst > 0.0
+
+
+def test_score_error_bound_is_attained_by_sequential_fp32():
+    # One product of 1 followed by 127 products just below half an ulp of 1: a sequential
+    # float32 sum rounds every small term away, so its error is 127 x (255/256) 2^-24, within
+    # 1.2 % of any bound of the form gamma_128 sum|q p|. The oracle's bound must cover it and
+    # may not exceed it by more than 2 %: a bound inflated by a stray factor (u = 2^-23, a
+    # wrong n) fails one side or the other.
+    q = np.full(128, 2.0 ** -12)
+    p = np.full(128, (1 + 127 / 128) * 2.0 ** -13)              # q p = (255/256) 2^-24
+    q[0], p[0] = 1.0, 1.0
+    qb_, pb = to_bits(q), to_bits(p[None, :])
+    exact = O.score_blocks(qb_, pb)
+    bound = O.score_error_bound(qb_, pb)
+    prods = (p.astype(np.float32) * q.astype(np.float32))[None, :].astype(np.float32)
+    seq, rev, tree = _fp32_sums(prods)
+    assert seq[0] == 1.0                                          # every small term rounded away
+    err = abs(seq[0] - exact[0])
+    assert err == 127 * 255 * 2.0 ** -32
+    assert err <= bound[0] <= 1.02 * err
+    assert abs(rev[0] - exact[0]) <= bound[0] and abs(tree[0] - exact[0]) <= bound[0]
+    # the same with a last product of -1: the float32 sum cancels to 0 while the exact score
+    # is the 126 lost terms, so only a bound on sum |q p| (not |sum q p|) covers it
+    q[127], p[127] = -1.0, 1.0
+    qb_, pb = to_bits(q), to_bits(p[None, :])
+    exact = O.score_blocks(qb_, pb)
+    bound = O.score_error_bound(qb_, pb)
+    prods = (p.astype(np.float32) * q.astype(np.float32))[None, :].astype(np.float32)
+    seq = _fp32_sums(prods)[0]
+    assert seq[0] == 0.0 and exact[0] == 126 * 255 * 2.0 ** -32
+    assert abs(seq[0] - exact[0]) <= bound[0]
+
+
 # ----------------------------------------------------------------------------- top-k
 
 def _brute_force_topk(s, k):
