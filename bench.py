@@ -53,6 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-kv-host", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-mla", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the tiny / long / batched decode legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-instrument", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -287,6 +288,95 @@ def time_graph(g, stream, steps, warmup, world):
     torch.cuda.synchronize()
     barrier(world)
     return t0.elapsed_time(t1) / 1000.0
+
+
+def time_graph_per_replay(g, stream, steps, warmup, flush=None):
+    """Each replay timed alone with CUDA events on the launching stream; with `flush` (a
+    tensor larger than L2) the buffer is rewritten between replays, outside the timed
+    events, so every replay starts with a cold L2. Returns the per-replay seconds."""
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            if flush is not None:
+                flush.add_(1)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) / 1000.0 for a, b in ev]
+
+
+def decode_config_leg(name, w, pk, steps, warmup, cold=False):
+    """A decode workload's layers resident in HBM, one CUDA graph of its fused layer-steps
+    (layers in stream order). Warm: replays back to back; cold (optional): L2 flushed by
+    writing a 512 MiB buffer between replays. Reports layer-steps/s (mean and median over
+    replays), the algorithmic bytes per layer-step and the HBM roofline fraction."""
+    import torch
+    from indexer_driven_sparse_gb300 import accounting as A
+    from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+    b = DecodeBatch(w.n_q_heads, w.n_kv_heads, w.ctx_len, device="cuda")
+    pooled = []
+    for L in w.layers:
+        pk_l = b.new_pooled()
+        b.pool(L.raw_idx_k, pk_l)
+        pooled.append(pk_l)
+    stream = torch.cuda.Stream()
+
+    def body():
+        for l, L in enumerate(w.layers):
+            b.fused_step(L.raw_idx_k, pooled[l], L.q_idx, L.q, L.k_cache, L.v_cache)
+
+    with torch.cuda.stream(stream):
+        body()
+    torch.cuda.synchronize()
+    st = b.fused_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status in the {name} leg: {st}")
+    g = capture(body, stream)
+    n_l = len(w.layers)
+    t_all = time_graph(g, stream, steps, warmup, 1)
+    per = time_graph_per_replay(g, stream, steps, 0)
+    nbytes = A.decode_layer_step_bytes(w.ctx_len, w.n_q_heads, w.n_kv_heads)
+    us_mean = 1e6 * t_all / (steps * n_l)
+    us_med = 1e6 * statistics.median(per) / n_l
+    gbs = nbytes / (us_mean * 1e-6) / 1e9
+    out = {"workload": name, "batch": w.batch, "layers": n_l, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+           "layer_steps_per_s": 1e6 / us_mean, "us_per_layer_step_mean": us_mean,
+           "us_per_layer_step_median": us_med, "algorithmic_bytes_per_layer_step": nbytes,
+           "hbm_gbs_algorithmic": gbs, "roofline_frac": gbs / pk["hbm"], "peak_gbs": pk["hbm"],
+           "gpu_launches_per_layer_step": 1}
+    if cold:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        per_c = time_graph_per_replay(g, stream, steps, 0, flush=flush.view(torch.int32))
+        us_c = 1e6 * statistics.mean(per_c) / n_l
+        out.update({"cold_l2_us_per_layer_step_mean": us_c,
+                    "cold_l2_us_per_layer_step_median": 1e6 * statistics.median(per_c) / n_l,
+                    "cold_l2_layer_steps_per_s": 1e6 / us_c,
+                    "cold_l2_hbm_gbs_algorithmic": nbytes / (us_c * 1e-6) / 1e9,
+                    "cold_l2_roofline_frac": nbytes / (us_c * 1e-6) / 1e9 / pk["hbm"]})
+        del flush
+    del g
+    return out
+
+
+def config_legs(pk, steps, warmup):
+    """Throughput of the tiny (1 layer), long (12 layers) and batched (B = 32, 12 layers)
+    decode workloads, each through the fused step; the tiny and long ones also cold-L2."""
+    import torch
+    from indexer_driven_sparse_gb300 import inputs as I
+    legs = {}
+    for name, make, cold in (("tiny_decode_ctx4096", lambda: I.tiny_decode(device="cuda"), True),
+                             ("long_decode_ctx131072", lambda: I.long_decode(device="cuda"), True),
+                             ("batched_decode_b32", lambda: I.batched_decode(device="cuda"), False)):
+        w = make()
+        legs[name] = decode_config_leg(name, w, pk, steps, warmup, cold)
+        del w
+        torch.cuda.empty_cache()
+    return legs
 
 
 def instrumented_kernel_times(dl, stream, steps):
@@ -533,12 +623,17 @@ def mla_bench(steps, warmup, pk, batch=64):
     # (each query's tiles read and write the same amounts)
     cap = recorded_traffic("mla_tile")
     traffic = cap * batch / 16 if cap is not None else None
+    # 191 FLOP/B is below GB300's ridge (measured bf16 / measured HBM, about 283 FLOP/B), so
+    # the binding roofline is HBM; the tensor fraction is reported beside it
+    gbs = nbytes / t / 1e9
     return {"workload": f"sparse MLA decode: {batch} queries x 64 heads, 2048 FP8 rows each (656 B), "
                         "million-token cache",
             "queries_per_s": batch / t, "us_per_call": t * 1e6,
-            "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6, "hbm_gbs": nbytes / t / 1e9,
-            "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s",
-                         "frac": ach / pk["bf16"], "traffic": traffic, "kernel": "mla_tile + mla_merge"},
+            "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6, "hbm_gbs": gbs,
+            "intensity_flop_per_byte": flops / nbytes, "ridge_flop_per_byte": pk["bf16"] * 1e12 / (pk["hbm"] * 1e9),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm"], "traffic": traffic, "kernel": "mla_tile + mla_merge"},
+            "tensor_frac": ach / pk["bf16"], "tensor_tflops": ach,
             "gpu_launches_per_call": 2}
 
 
@@ -705,9 +800,42 @@ def case_main(args):
 
 # ----------------------------------------------------------------------------- CPU oracle leg
 
+_ORACLE_CASE = {}
+
+
+def _oracle_layer_steps(seconds: float) -> int:
+    """Layer-steps of the fp64 oracle (pool the newest block, then the whole decode query)
+    completed in `seconds` on the drawn million-token layer."""
+    import oracle as O
+    c = _ORACLE_CASE
+    p, raw = c["p"], c["raw"]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        O.pool_keys(raw[4 * (p // 4 - 1):4 * (p // 4)])
+        O.decode_query(p, c["qi"][0], c["pooled"], c["q"][0], c["k"], c["v"], 2)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            return n
+
+
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def cpu_baseline_child(seconds: float):
     """Time the fp64 oracle on one layer of the million-token decode workload (CPU draw
-    of the same recipe), single-threaded BLAS; prints one JSON object."""
+    of the same recipe): one process with single-threaded BLAS, then one worker per host
+    core (forked after the draw, so they share it; no CUDA in this process). Prints one
+    JSON object."""
+    import multiprocessing as mp
+
     import numpy as np
     import torch
     import oracle as O
@@ -717,19 +845,23 @@ def cpu_baseline_child(seconds: float):
     w = I.million_decode(seed=0, device="cpu", n_layers=1)
     L = w.layers[0]
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    raw, qi, q, k, v = bits(L.raw_idx_k), bits(L.q_idx), bits(L.q), bits(L.k_cache), bits(L.v_cache)
-    p = w.ctx_len[0]
-    pooled = O.pool_keys(raw)                 # setup (steady state pools one block per 4 steps)
+    raw = bits(L.raw_idx_k)
+    _ORACLE_CASE.update(p=w.ctx_len[0], raw=raw, qi=bits(L.q_idx), q=bits(L.q), k=bits(L.k_cache),
+                        v=bits(L.v_cache), pooled=O.pool_keys(raw))   # setup: pooled once
+    del w, L
     setup = time.perf_counter() - t_setup
-    n, t0 = 0, time.perf_counter()
-    while True:
-        O.pool_keys(raw[4 * (p // 4 - 1):4 * (p // 4)])
-        O.decode_query(p, qi[0], pooled, q[0], k, v, 2)
-        n += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    print(json.dumps({"value": n / dt, "n": n, "seconds": dt, "setup_s": setup}))
+    t0 = time.perf_counter()
+    n1 = _oracle_layer_steps(seconds)
+    dt1 = time.perf_counter() - t0
+    cores = os.cpu_count() or 1
+    all_s = max(seconds * 2.0 / 3.0, 1.0)
+    with mp.get_context("fork").Pool(cores) as pool:
+        t0 = time.perf_counter()
+        counts = pool.map(_oracle_layer_steps, [all_s] * cores)
+        dt_all = time.perf_counter() - t0
+    print(json.dumps({"value": n1 / dt1, "n": n1, "seconds": dt1, "setup_s": setup,
+                      "all_value": sum(counts) / dt_all, "all_n": sum(counts), "all_seconds": dt_all,
+                      "cores": cores, "model": _cpu_model()}))
 
 
 def run_cpu_baseline(seconds: float):
@@ -740,9 +872,12 @@ def run_cpu_baseline(seconds: float):
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{d['n']} layer-steps of one million-token layer (CPU draw of the same recipe), "
-                      f"fp64 numpy, single-threaded BLAS, {d['seconds']:.1f} s"}
+    return {"value": d["all_value"], "unit": UNIT, "cores": d["cores"], "kind": "oracle",
+            "cpu_model": d["model"], "nproc": d["cores"],
+            "sample": f"one million-token layer (CPU draw of the same recipe), fp64 numpy, single-threaded BLAS "
+                      f"per worker: {d['all_n']} layer-steps in {d['all_seconds']:.1f} s over {d['cores']} "
+                      f"forked workers (one per core)",
+            "single_core": {"value": d["value"], "cores": 1, "layer_steps": d["n"], "seconds": d["seconds"]}}
 
 
 def reference_main(args):
@@ -825,6 +960,7 @@ def main(argv=None):
 
     with ClockSampler(local) as clk:
         t = time_graph(g, stream, args.steps, args.warmup, world)
+        per_step = time_graph_per_replay(g, stream, args.steps, 0)
     clocks = clk.summary()
     t = max_over_ranks(t, world)
     n_layers = len(dl.w.layers)
@@ -842,31 +978,36 @@ def main(argv=None):
                    "l2": "inputs larger than L2 (12 x 64 MiB pooled keys + 12 x 2 GiB K/V), no flush"},
         "hbm_gbs_algorithmic": bytes_ls * value / world / 1e9,
         "us_per_layer_step": 1e6 * t / (args.steps * n_layers),
+        "us_per_layer_step_median": 1e6 * statistics.median(per_step) / n_layers,
+        "us_per_layer_step_mean": 1e6 * statistics.mean(per_step) / n_layers,
         "clocks": clocks,
         "gpu_launches": None,
     }
     launches_per_layer = 1 if dl.fused else 5    # fused step | pool, score, topk, attention, merge
     line["gpu_launches"] = launches_per_layer * n_layers * args.steps
 
+    if dl.fused:
+        # The step graph holds only the 12 fused launches, back to back (each a programmatic
+        # dependent of the previous one), so a launch's share of the step time is its duration
+        # as it runs in the step: step time / layers.
+        us_k = 1e6 * t / (args.steps * n_layers)
+        ach = bytes_ls / (us_k * 1e-6) / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
+                            "frac": ach / pk["hbm"], "traffic": recorded_traffic("decode_step"),
+                            "kernel": "decode_step", "algorithmic_bytes": bytes_ls, "us_per_launch": us_k,
+                            "timing": "graph of 12 fused launches; step time / 12 (CUDA events on the stream)",
+                            "peak_src": pk["src"]}
     if not args.no_instrument:
+        # event nodes between the launches serialise them (no programmatic dependent launch
+        # overlap), so these per-launch times are upper bounds, reported for the phase split only
         kt = instrumented_kernel_times(dl, stream, max(5, min(50, args.steps)))
-        line["kernel_us"] = kt
-        algo = {"score": A.score_scan_bytes(dl.w.ctx_len),
-                "attend": A.kv_read_bytes(A.attended(CTX_1M)) + 2 * 16 * 256 * 2,
-                "decode_step": bytes_ls}
-        dom = max(kt, key=kt.get)
-        if dom in algo:
-            ach = algo[dom] / (kt[dom] * 1e-6) / 1e9
-            line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
-                                "frac": ach / pk["hbm"], "traffic": recorded_traffic(dom), "kernel": dom,
-                                "algorithmic_bytes": algo[dom], "peak_src": pk["src"]}
-        else:
-            sc = kt["score"]
-            ach = algo["score"] / (sc * 1e-6) / 1e9
+        line["kernel_us_event_nodes"] = kt
+        if not dl.fused:
+            algo = {"score": A.score_scan_bytes(dl.w.ctx_len)}
+            ach = algo["score"] / (kt["score"] * 1e-6) / 1e9
             line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
                                 "frac": ach / pk["hbm"], "traffic": None, "kernel": "score",
-                                "note": f"dominant kernel is {dom} (latency-bound); score scan reported",
-                                "peak_src": pk["src"]}
+                                "note": "separate calls: the score scan", "peak_src": pk["src"]}
 
     if not args.no_e2e:
         dt, h2d, d2h = e2e_decode(dl, stream, max(10, args.steps // 4), max(3, args.warmup))
@@ -887,6 +1028,11 @@ def main(argv=None):
     if not args.no_prefill:
         del g
         line["prefill"] = prefill_bench(args.steps, args.warmup, pk)
+
+    if not args.no_configs:
+        del dl
+        torch.cuda.empty_cache()
+        line["decode_configs"] = config_legs(pk, max(20, args.steps // 4), max(3, args.warmup))
 
     if cpu_base is not None:
         line["cpu_baseline"] = cpu_base
