@@ -300,6 +300,33 @@ QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *ra
                                        int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
                                        qsa_stream stream);
 
+/* a1-a5 fused, with an L2 prefetch hint — qsa_decode_step (and qsa_decode_step_fp8) plus
+ * the memory the caller's next call will read, typically the next layer's pooled keys (or
+ * FP8 codes). Each CTA, once its own pooled-key stream is done, issues L2 prefetch hints for
+ * its slice of [next_read, next_read + next_read_bytes), so the bytes the next layer-step
+ * scans arrive in L2 while this step exchanges keys and partials (those phases leave HBM
+ * idle). The next layer's keys do not depend on this step's output; nothing of the next
+ * step is computed here. A hint only: results are bit-identical to qsa_decode_step's.
+ *   next_read: 16-byte aligned, device memory or mapped pinned host memory, or NULL (no
+ *   hint); next_read_bytes is rounded down to a multiple of 16 (below 16: no hint).
+ * Everything else as qsa_decode_step / qsa_decode_step_fp8. A misaligned or unreadable
+ * next_read is QSA_ERR_INVALID_ARGUMENT. */
+QSA_API qsa_status qsa_decode_step_prefetch(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                            int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
+                                            const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                            int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len,
+                                            int32_t B, int64_t max_blocks, int32_t *blocks, int32_t *count,
+                                            qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                            const void *next_read, size_t next_read_bytes, qsa_stream stream);
+QSA_API qsa_status qsa_decode_step_fp8_prefetch(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, uint8_t *codes,
+                                                float *scales, int64_t n_pooled_total, const int32_t *blk_off,
+                                                const qsa_bf16 *q_idx, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                                const qsa_bf16 *v_cache, int64_t n_tokens_total,
+                                                const int32_t *tok_off, const int32_t *ctx_len, int32_t B,
+                                                int64_t max_blocks, int32_t *blocks, int32_t *count, qsa_bf16 *out,
+                                                float *lse, void *ws, size_t ws_bytes, const void *next_read,
+                                                size_t next_read_bytes, qsa_stream stream);
+
 /* Allocation-free variant of qsa_sparse_decode (the pages have no counterpart; this
  * is a library convenience). Same arguments and result, but no workspace: the split
  * partials live in a 16 MiB static device array inside the library, for callers that

@@ -62,6 +62,10 @@ _SIGNATURES = {
     "qsa_sparse_prefill_chunk": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "qsa_decode_step": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _P,
                                 _P, _SZ, _P]),
+    "qsa_decode_step_prefetch": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P,
+                                         _P, _P, _P, _SZ, _P, _SZ, _P]),
+    "qsa_decode_step_fp8_prefetch": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64,
+                                             _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P]),
     "qsa_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "qsa_copy_rows": (_I32, [_P, _SZ, _P, _SZ, _SZ, _SZ, _P]),
     "qsa_prefill_select": (_I32, [_CFG, _P, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P, _P, _SZ, _P]),
@@ -224,31 +228,48 @@ def qsa_sparse_decode(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count,
            "qsa_sparse_decode")
 
 
+def _next_read(t):
+    """(pointer, bytes) of an optional L2 prefetch hint tensor (contiguous, any dtype)."""
+    if t is None:
+        return None, 0
+    if not t.is_contiguous():
+        raise ValueError("next_read must be contiguous")
+    return t.data_ptr(), t.numel() * t.element_size()
+
+
 def qsa_decode_step(cfg, raw_idx_k, pooled, blk_off, q_idx, q, k_cache, v_cache, tok_off, ctx_len, max_blocks,
-                    blocks, count, out, lse, ws, stream=None):
-    _check(load().qsa_decode_step(C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"),
-                                  _ptr(pooled, torch.bfloat16, "pooled"), pooled.shape[0], _ptr(blk_off, torch.int32),
-                                  _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(q, torch.bfloat16, "q"),
-                                  _ptr(k_cache, torch.bfloat16, "k"), _ptr(v_cache, torch.bfloat16, "v"),
-                                  k_cache.shape[0], _ptr(tok_off, torch.int32), _ptr(ctx_len, torch.int32),
-                                  ctx_len.numel(), int(max_blocks), _ptr(blocks, torch.int32),
-                                  _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
-                                  _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _stream(stream)), "qsa_decode_step")
+                    blocks, count, out, lse, ws, stream=None, next_read=None):
+    """One fused decode layer-step; with `next_read` (the tensor the next call will scan, e.g.
+    the next layer's pooled keys) the step also prefetches it into L2 (qsa_decode_step_prefetch)."""
+    args = [C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"), _ptr(pooled, torch.bfloat16, "pooled"),
+            pooled.shape[0], _ptr(blk_off, torch.int32), _ptr(q_idx, torch.bfloat16, "q_idx"),
+            _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k"), _ptr(v_cache, torch.bfloat16, "v"),
+            k_cache.shape[0], _ptr(tok_off, torch.int32), _ptr(ctx_len, torch.int32), ctx_len.numel(),
+            int(max_blocks), _ptr(blocks, torch.int32), _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
+            _ptr(lse, torch.float32, "lse"), *_ws_args(ws)]
+    if next_read is None:
+        _check(load().qsa_decode_step(*args, _stream(stream)), "qsa_decode_step")
+    else:
+        _check(load().qsa_decode_step_prefetch(*args, *_next_read(next_read), _stream(stream)),
+               "qsa_decode_step_prefetch")
 
 
 def qsa_decode_step_fp8(cfg, raw_idx_k, codes, scales, blk_off, q_idx, q, k_cache, v_cache, tok_off, ctx_len,
-                        max_blocks, blocks, count, out, lse, ws, stream=None):
+                        max_blocks, blocks, count, out, lse, ws, stream=None, next_read=None):
     if codes.shape[0] != scales.shape[0]:
         raise ValueError("codes and scales must have one row per pooled block")
-    _check(load().qsa_decode_step_fp8(C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"),
-                                      _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
-                                      codes.shape[0], _ptr(blk_off, torch.int32), _ptr(q_idx, torch.bfloat16, "q_idx"),
-                                      _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k"),
-                                      _ptr(v_cache, torch.bfloat16, "v"), k_cache.shape[0], _ptr(tok_off, torch.int32),
-                                      _ptr(ctx_len, torch.int32), ctx_len.numel(), int(max_blocks),
-                                      _ptr(blocks, torch.int32), _ptr(count, torch.int32),
-                                      _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
-                                      *_ws_args(ws), _stream(stream)), "qsa_decode_step_fp8")
+    args = [C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"), _ptr(codes, torch.uint8, "codes"),
+            _ptr(scales, torch.float32, "scales"), codes.shape[0], _ptr(blk_off, torch.int32),
+            _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k"),
+            _ptr(v_cache, torch.bfloat16, "v"), k_cache.shape[0], _ptr(tok_off, torch.int32),
+            _ptr(ctx_len, torch.int32), ctx_len.numel(), int(max_blocks), _ptr(blocks, torch.int32),
+            _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+            *_ws_args(ws)]
+    if next_read is None:
+        _check(load().qsa_decode_step_fp8(*args, _stream(stream)), "qsa_decode_step_fp8")
+    else:
+        _check(load().qsa_decode_step_fp8_prefetch(*args, *_next_read(next_read), _stream(stream)),
+               "qsa_decode_step_fp8_prefetch")
 
 
 def qsa_sparse_decode_noalloc(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out, lse, stream=None):

@@ -669,6 +669,18 @@ __device__ void gather_chunk(const StepArgs &a, uint16_t *dst, int j_base, int n
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// This CTA's share of the caller's next read (its grid slice, in 16-byte units), issued as
+// L2 prefetch hints of up to 64 KiB by a few threads. Called once, when the CTA's own
+// pooled-key stream is done, so the prefetch uses HBM time the exchanges below leave idle.
+__device__ __forceinline__ void prefetch_next_read(const StepArgs &a) {
+    if (a.next_read == nullptr || a.next_read_bytes < 16) return;
+    const int64_t units = a.next_read_bytes >> 4;
+    const int64_t u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+    constexpr int64_t kPiece = 4096;                       // 64 KiB
+    for (int64_t u = u0 + (int64_t)threadIdx.x * kPiece; u < u1; u += (int64_t)kStepThreads * kPiece)
+        bulk_prefetch_l2(a.next_read + u * 16, (uint32_t)(min(kPiece, u1 - u) * 16));
+}
+
 template <int G, bool F8>
 __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a) {
     constexpr int kRows = F8 ? kChunkRows8 : kChunkRows;      // key rows per ring stage
@@ -796,6 +808,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
             if (!F8) a.pooled[(boff + nb - 1) * kIdxDim + tid] = v;
         }
         if (F8 && owner_new) quantize_newest(a, boff + nb - 1, true, v, newrow8, s_amax);   // CTA-uniform
+        prefetch_next_read(a);
     }
 
     bool balanced = dense;                // the row's whole selection is known to every CTA
@@ -805,8 +818,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     if (!dense) {
         // ---- 2b. scan: bulk copies into a 4-stage ring, scores -> keys + histogram
         for (int i = tid; i < kHistBins; i += kStepThreads) hist[i] = 0;
-        // bf16: a half-warp per row, 8 dims per lane; FP8: 8 lanes per row, 16 dims per lane
-        float qf[F8 ? 16 : 8];
+        // bf16: lane l holds dims 4l .. 4l+3 of 8 rows at a time (dot4_bf16 order); FP8: 8 lanes
+        // per row, 16 dims per lane
+        float qf[F8 ? 16 : 4];
         if constexpr (F8) {
             float qa[8], qb[8];
             unpack8(ldg_nc_v4(a.q_idx + (int64_t)row * kIdxDim + (lane & 7) * 16), qa);
@@ -817,9 +831,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 qf[8 + e] = qb[e];
             }
         } else {
-            unpack8(ldg_nc_v4(a.q_idx + (int64_t)row * kIdxDim + (lane & 15) * 8), qf);
+            load_q4(a.q_idx + (int64_t)row * kIdxDim, lane, qf);
         }
-        const int half = lane >> 4, c16 = lane & 15;
         const int g8 = lane >> 3, c8 = lane & 7;
         __syncthreads();
         for (int c = 0; c < n_chunks; ++c) {
@@ -862,24 +875,23 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
             } else {
                 const uint16_t *buf =
                     reinterpret_cast<const uint16_t *>(smem + kRingOff + (size_t)stage * kChunkBytes);
-                // 16 warps x 8 rows: each half-warp takes one row per step
+                // 16 warps x 8 rows: 8-byte loads (one row per warp instruction, no bank
+                // conflicts), one reduce-scatter for the 8 rows; lanes 4i hold row i's score
+                constexpr int kR = kRows / kStepWarps;
+                float part[kR];
 #pragma unroll
-                for (int it = 0; it < kRows / (2 * kStepWarps); ++it) {
-                    const int r = (warp * (kRows / kStepWarps)) + it * 2 + half;
-                    float s = 0.f;
-                    if (r < rows_c) {
-                        float f[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(buf + r * kIdxDim + c16 * 8), f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) s = fmaf(f[e], qf[e], s);
-                    }
-#pragma unroll
-                    for (int o = 8; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                    if (c16 == 0 && r < rows_c) {
-                        const uint32_t key = score_key(s);
-                        keys[c * kRows + r] = key;
-                        atomicAdd(&hist[key >> kHistShift], 1u);
-                    }
+                for (int i = 0; i < kR; ++i) {
+                    const int r = warp * kR + i;
+                    const uint2 x = r < rows_c ? *reinterpret_cast<const uint2 *>(buf + r * kIdxDim + 4 * lane)
+                                               : make_uint2(0u, 0u);
+                    part[i] = dot4_bf16(x, qf);
+                }
+                const float s = reduce_rows<kR>(part, lane);
+                const int r = warp * kR + row_of_lane<kR>(lane);
+                if ((lane & (32 / kR - 1)) == 0 && r < rows_c) {
+                    const uint32_t key = score_key(s);
+                    keys[c * kRows + r] = key;
+                    atomicAdd(&hist[key >> kHistShift], 1u);
                 }
             }
             // the stage is refilled once every warp has read it; no block-wide barrier per chunk
@@ -894,6 +906,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 }
             }
         }
+        prefetch_next_read(a);
         // ---- 1b. re-pool block nb-1: exact fp64 mean of its four raw keys, one RNE to bf16
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
@@ -926,12 +939,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
                 for (int o = 4; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 s *= s_amax[4];
             } else {
-                float f[8];
-                unpack8(*reinterpret_cast<const uint4 *>(newrow + c16 * 8), f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s = fmaf(f[e], qf[e], s);
-#pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                float p1[1] = {dot4_bf16(*reinterpret_cast<const uint2 *>(newrow + 4 * lane), qf)};
+                s = reduce_rows<1>(p1, lane);
             }
             if (lane == 0) {
                 const uint32_t key = score_key(s);

@@ -399,7 +399,7 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
                               const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
                               const int32_t *ctx_len, int32_t B, int64_t max_blocks, int32_t *blocks,
                               int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
-                              qsa_stream stream) {
+                              qsa_stream stream, const void *next_read = nullptr, size_t next_read_bytes = 0) {
     const bool fp8 = pooled == nullptr;
     QSA_TRY(check_config(cfg));
     QSA_NEED(B >= 0 && B <= kMaxStepRows, "B = %d out of range [0, 64]", B);
@@ -419,6 +419,10 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
                  (long long)n_pooled_total);
     QSA_NEED(device_accessible(raw_idx_k) && device_accessible(k_cache) && device_accessible(v_cache),
              "raw_idx_k, k_cache and v_cache must be device memory or mapped pinned host memory");
+    if (next_read != nullptr && next_read_bytes >= 16) {
+        QSA_NEED(aligned(next_read, 16), "next_read must be 16-byte aligned");
+        QSA_NEED(device_accessible(next_read), "next_read must be device memory or mapped pinned host memory");
+    }
     const int G = cfg->n_q_heads / cfg->n_kv_heads;
     const int ctas = decode_step_grid(G, fp8);
     if (ctas == 0) return fail(QSA_ERR_CUDA, "%s: cannot size the cooperative grid on this device", name);
@@ -452,6 +456,8 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
     a.n_q_heads = cfg->n_q_heads;
     a.n_kv_heads = cfg->n_kv_heads;
     a.scale_log2 = scale_of(cfg) * kLog2e;
+    a.next_read = next_read_bytes >= 16 ? static_cast<const unsigned char *>(next_read) : nullptr;
+    a.next_read_bytes = a.next_read ? (int64_t)(next_read_bytes & ~(size_t)15) : 0;
     const cudaError_t e = launch_decode_step(a, ws, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
     return ok();
@@ -485,6 +491,35 @@ QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *ra
     return decode_step_common("qsa_decode_step_fp8", cfg, raw_idx_k, nullptr, codes, scales, n_pooled_total,
                               blk_off, q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, max_blocks,
                               blocks, count, out, lse, ws, ws_bytes, stream);
+}
+
+QSA_API qsa_status qsa_decode_step_prefetch(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                            int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
+                                            const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                            int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len,
+                                            int32_t B, int64_t max_blocks, int32_t *blocks, int32_t *count,
+                                            qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                            const void *next_read, size_t next_read_bytes, qsa_stream stream) {
+    if (pooled == nullptr && B > 0) return fail(QSA_ERR_INVALID_ARGUMENT, "pooled is NULL");
+    return decode_step_common("qsa_decode_step_prefetch", cfg, raw_idx_k, pooled, nullptr, nullptr, n_pooled_total,
+                              blk_off, q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, max_blocks,
+                              blocks, count, out, lse, ws, ws_bytes, stream, next_read, next_read_bytes);
+}
+
+QSA_API qsa_status qsa_decode_step_fp8_prefetch(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, uint8_t *codes,
+                                                float *scales, int64_t n_pooled_total, const int32_t *blk_off,
+                                                const qsa_bf16 *q_idx, const qsa_bf16 *q, const qsa_bf16 *k_cache,
+                                                const qsa_bf16 *v_cache, int64_t n_tokens_total,
+                                                const int32_t *tok_off, const int32_t *ctx_len, int32_t B,
+                                                int64_t max_blocks, int32_t *blocks, int32_t *count, qsa_bf16 *out,
+                                                float *lse, void *ws, size_t ws_bytes, const void *next_read,
+                                                size_t next_read_bytes, qsa_stream stream) {
+    if ((codes == nullptr || scales == nullptr) && B > 0)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "codes and scales must be non-NULL");
+    return decode_step_common("qsa_decode_step_fp8_prefetch", cfg, raw_idx_k, nullptr, codes, scales,
+                              n_pooled_total, blk_off, q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len,
+                              B, max_blocks, blocks, count, out, lse, ws, ws_bytes, stream, next_read,
+                              next_read_bytes);
 }
 
 QSA_API size_t qsa_sparse_mla_workspace_size(int32_t n_heads, int32_t B, int32_t max_rows) {

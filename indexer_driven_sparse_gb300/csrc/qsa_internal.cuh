@@ -123,6 +123,56 @@ __device__ __forceinline__ void e4m3x16_to_f32(const uint4 &v, float (&f)[16]) {
     }
 }
 
+// The indexer score's evaluation order, shared by every bf16 scan (index_score_kernel and
+// the fused step) so that their scores agree bit for bit: lane l of a warp holds dims
+// 4l .. 4l+3 of the 128-dim row and of the query; its partial is x0 q0 + x1 q1 + x2 q2 + x3 q3
+// as one product and three fused multiply-adds (bf16 x bf16 products are exact in fp32);
+// the row's score is the butterfly sum of the 32 partials over lane distances 16, 8, 4, 2, 1.
+__device__ __forceinline__ float dot4_bf16(uint2 x, const float (&q)[4]) {
+    float t = __uint_as_float(x.x << 16) * q[0];
+    t = fmaf(__uint_as_float(x.x & 0xFFFF0000u), q[1], t);
+    t = fmaf(__uint_as_float(x.y << 16), q[2], t);
+    return fmaf(__uint_as_float(x.y & 0xFFFF0000u), q[3], t);
+}
+
+__device__ __forceinline__ void load_q4(const uint16_t *q_row, int lane, float (&q)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(q_row + 4 * lane);
+    q[0] = __uint_as_float(v.x << 16);
+    q[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    q[2] = __uint_as_float(v.y << 16);
+    q[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+
+// Reduce-scatter of NV rows' partials (NV a power of two <= 32) over the warp in the
+// butterfly order above: afterwards every lane holds the full score of row
+// row_of_lane<NV>(lane) (the rows' sums are identical to a per-row butterfly).
+template <int NV>
+__device__ __forceinline__ float reduce_rows(float (&v)[NV], int lane) {
+#pragma unroll
+    for (int level = 0; (NV >> level) > 1; ++level) {
+        const int n = NV >> level, o = 16 >> level;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 / NV; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
+// Row index whose total lane `lane` holds after reduce_rows<NV>: the top log2(NV) lane bits.
+constexpr int ilog2(int n) { return n <= 1 ? 0 : 1 + ilog2(n >> 1); }
+
+template <int NV>
+__device__ __forceinline__ int row_of_lane(int lane) {
+    return (lane >> (5 - ilog2(NV))) & (NV - 1);
+}
+
 // Order-preserving map of an fp32 score to uint32: larger score -> larger key.
 // -0 is folded onto +0 and NaN onto the smallest key.
 __device__ __forceinline__ uint32_t score_key(float s) {
@@ -248,6 +298,8 @@ struct StepArgs {
     float *lse;
     int32_t n_q_heads, n_kv_heads;
     float scale_log2;
+    const unsigned char *next_read;   // optional L2 prefetch hint (16-byte aligned) or nullptr
+    int64_t next_read_bytes;
     // workspace views (set by launch_decode_step)
     WsHeader *hdr;
     void *rows;

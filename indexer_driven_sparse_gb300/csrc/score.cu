@@ -1,8 +1,9 @@
 // a2 — indexer scores of every visible pooled block ("3090x3で 314 万コンテキスト",
 // sections "なぜ" and "VRAM に残す必要があるもの": the scan over all pooled keys is the
 // one read that grows with context). HBM-bound streaming dot products: each warp
-// covers 32 consecutive 256-byte rows with 128-bit coalesced non-allocating loads
-// (a half-warp per row, 8 dims per lane), all 16 loads of a lane issued before use.
+// covers 32 consecutive 256-byte rows; lane l loads dims 4l .. 4l+3 of every row (8-byte
+// coalesced non-allocating loads, all 32 issued before use) and a reduce-scatter over the
+// 32 rows leaves row l's score in lane l, in the evaluation order of dot4_bf16.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -28,41 +29,25 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const uint16
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row0 = (int64_t)blockIdx.x * kRowsPerCta + warp * kRowsPerWarp;
     if (row0 >= nb) return;
-    const int half = lane >> 4, c = lane & 15;
-    float qf[8];
-    unpack8(ldg_nc_v4(q_idx + (int64_t)r * kIdxDim + c * 8), qf);
-    const uint16_t *base = pooled + (off + row0) * kIdxDim + c * 8;
-    uint4 v[kRowsPerWarp / 2];
+    float q4[4];
+    load_q4(q_idx + (int64_t)r * kIdxDim, lane, q4);
+    const uint16_t *base = pooled + (off + row0) * kIdxDim + 4 * lane;
+    uint2 x[kRowsPerWarp];
 #pragma unroll
-    for (int j = 0; j < kRowsPerWarp / 2; ++j) {
-        const int64_t row = row0 + 2 * j + half;
-        v[j] = row < nb ? ldg_nc_v4(base + (int64_t)(2 * j + half) * kIdxDim) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < kRowsPerWarp; ++j) {
+        const int64_t row = row0 + j;
+        if (row < nb) {
+            asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                         : "=r"(x[j].x), "=r"(x[j].y) : "l"(base + (int64_t)j * kIdxDim));
+        } else {
+            x[j] = make_uint2(0, 0);
+        }
     }
-    float part[kRowsPerWarp / 2];
+    float part[kRowsPerWarp];
 #pragma unroll
-    for (int j = 0; j < kRowsPerWarp / 2; ++j) {
-        float f[8];
-        unpack8(v[j], f);
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s = fmaf(f[e], qf[e], s);
-        part[j] = s;
-    }
-#pragma unroll
-    for (int j = 0; j < kRowsPerWarp / 2; ++j) {
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
-    }
-    // lane 0 holds rows 2j, lane 16 rows 2j+1: let lane 2j+half write row 2j+half.
-    float mine = 0.f;
-#pragma unroll
-    for (int j = 0; j < kRowsPerWarp / 2; ++j) {
-        const float a = __shfl_sync(0xffffffffu, part[j], 0);
-        const float b = __shfl_sync(0xffffffffu, part[j], 16);
-        if (lane == 2 * j) mine = a;
-        if (lane == 2 * j + 1) mine = b;
-    }
-    const int64_t my_row = row0 + lane;
+    for (int j = 0; j < kRowsPerWarp; ++j) part[j] = dot4_bf16(x[j], q4);
+    const float mine = reduce_rows<kRowsPerWarp>(part, lane);      // row row_of_lane<32>(lane) = lane
+    const int64_t my_row = row0 + row_of_lane<kRowsPerWarp>(lane);
     if (my_row < nb) scores[(int64_t)r * ld + my_row] = mine;
 }
 

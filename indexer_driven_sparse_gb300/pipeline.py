@@ -57,17 +57,19 @@ class DecodeBatch:
     def new_pooled(self):
         return torch.empty(max(self.n_pooled, 1), 128, dtype=torch.bfloat16, device=self.device)
 
-    def fused_step(self, raw_idx_k, pooled, q_idx, q, k_cache, v_cache, stream=None):
+    def fused_step(self, raw_idx_k, pooled, q_idx, q, k_cache, v_cache, stream=None, next_read=None):
         """One decode layer-step in one launch (qsa_decode_step): re-pool the newest
-        block, score, select, attend, merge."""
+        block, score, select, attend, merge. `next_read` (e.g. the next layer's pooled
+        keys) is prefetched into L2 while the step exchanges keys and partials."""
         qb.qsa_decode_step(self.cfg, raw_idx_k, pooled, self.blk_off, q_idx, q, k_cache, v_cache, self.tok_off,
-                           self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse, self.step_ws, stream)
+                           self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse, self.step_ws, stream,
+                           next_read)
 
-    def fused_step_fp8(self, raw_idx_k, codes, scales, q_idx, q, k_cache, v_cache, stream=None):
+    def fused_step_fp8(self, raw_idx_k, codes, scales, q_idx, q, k_cache, v_cache, stream=None, next_read=None):
         """qsa_decode_step over FP8 indexer keys (qsa_decode_step_fp8)."""
         qb.qsa_decode_step_fp8(self.cfg, raw_idx_k, codes, scales, self.blk_off, q_idx, q, k_cache, v_cache,
                                self.tok_off, self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse,
-                               self.step_ws, stream)
+                               self.step_ws, stream, next_read)
 
     def fused_status(self, stream=None):
         return qb.qsa_read_device_status(self.step_ws, stream)

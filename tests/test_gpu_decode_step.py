@@ -144,6 +144,29 @@ def test_fused_step_batched_full_size_one_layer(cuda_lib, kind):
     assert st["rows"] == 32
 
 
+def test_fused_step_prefetch_hint_changes_nothing(cuda_lib):
+    # qsa_decode_step_prefetch: the L2 prefetch of another buffer (here a second layer's
+    # pooled keys, and a misaligned-length view) leaves selection, out and lse bit-identical
+    w = I.decode_workload("pf", [200003, 9001, 2051], 2, 16, 2, "planted", seed=12)
+    L0, L1 = _to(w.layers[0]), _to(w.layers[1])
+    b = DecodeBatch(16, 2, w.ctx_len)
+    p0, p1 = b.new_pooled(), b.new_pooled()
+    b.pool(L0.raw_idx_k, p0)
+    b.pool(L1.raw_idx_k, p1)
+    b.fused_step(L0.raw_idx_k, p0, L0.q_idx, L0.q, L0.k_cache, L0.v_cache)
+    assert b.fused_status()[0] == 0
+    want = (b.blocks.clone(), b.count.clone(), b.out.clone(), b.lse.clone())
+    for nxt in (p1, p1.view(-1)[:1001], L1.k_cache):
+        b.blocks.fill_(-7)
+        b.out.zero_()
+        b.fused_step(L0.raw_idx_k, p0, L0.q_idx, L0.q, L0.k_cache, L0.v_cache, next_read=nxt)
+        assert b.fused_status()[0] == 0
+        assert all(torch.equal(x, y) for x, y in zip((b.blocks, b.count, b.out, b.lse), want))
+    with pytest.raises(qb.QsaError) as e:
+        b.fused_step(L0.raw_idx_k, p0, L0.q_idx, L0.q, L0.k_cache, L0.v_cache, next_read=p1.view(-1)[1:])
+    assert e.value.status == qb.QSA_ERR_INVALID_ARGUMENT
+
+
 def test_fused_step_alternating_paths_share_barrier_state(cuda_lib):
     # Rows keep barrier counters across launches. Tied scores overflow the published
     # top-K and take the fallback (four row barriers); spread scores take the common
