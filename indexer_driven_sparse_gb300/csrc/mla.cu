@@ -92,12 +92,18 @@ __device__ __forceinline__ int64_t mla_range_lo(const MlaArgs &a, int c) {
     return (int64_t)a.B * 2 * a.n_tiles * c / a.grid;
 }
 
-// The row id of tile row j of item (b, t), or -1 (past the query's rows, or out of the cache:
-// then the error is recorded and the row is skipped).
-__device__ __forceinline__ int mla_row_id(const MlaArgs &a, int b, int t, int j, int nr) {
+constexpr int kMlaNoRow = INT32_MIN;                 // tile row past the query's rows
+
+// The raw row id of tile row j of item (b, t) (no check yet), or kMlaNoRow past the query's rows.
+__device__ __forceinline__ int mla_raw_id(const MlaArgs &a, int b, int t, int j, int nr) {
     const int r = t * kMlaTok + j;
-    if (r >= nr) return -1;
-    const int id = a.rows[(int64_t)b * a.max_rows + r];
+    return r < nr ? __ldg(a.rows + (int64_t)b * a.max_rows + r) : kMlaNoRow;
+}
+
+// The id a tile row reads, or -1: past the query's rows, or an id outside the cache (then the
+// error is recorded and the row is skipped).
+__device__ __forceinline__ int mla_checked_id(const MlaArgs &a, int id, int b) {
+    if (id == kMlaNoRow) return -1;
     if (id < 0 || id >= a.n_tok) {
         record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereMla, b);
         return -1;
@@ -142,31 +148,36 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_tile_kernel(MlaArgs a) {
     tc_fence_after();
     const uint32_t tmem = tmem_s;
 
-    // registers of the next tile: its row ids (one tile ahead) and its row data (loaded early)
-    int id_lat[kMlaLatItems], id_rope[kMlaRopeItems], id_sc = -1;
+    // registers of the next tile: its raw row ids (one tile further ahead, loaded without a
+    // check so that the loads overlap) and its row data (loaded while the previous tile computes)
+    int id_lat[kMlaLatItems], id_rope[kMlaRopeItems], id_sc = kMlaNoRow, id_b = 0;
     uint4 d_lat[kMlaLatItems], d_rope[kMlaRopeItems], d_sc = make_uint4(0, 0, 0, 0);
     bool d_valid = false;                            // the data's row (threads < 64) is attended
     auto load_ids = [&](int64_t w) {
         const int64_t P = w / a.n_tiles;
         const int b = (int)(P >> 1), t = (int)(w - P * a.n_tiles), nr = mla_rows_of(a, b);
+        id_b = b;
 #pragma unroll
-        for (int k = 0; k < kMlaLatItems; ++k) id_lat[k] = mla_row_id(a, b, t, warp + kMlaWarps * k, nr);
+        for (int k = 0; k < kMlaLatItems; ++k) id_lat[k] = mla_raw_id(a, b, t, warp + kMlaWarps * k, nr);
 #pragma unroll
-        for (int k = 0; k < kMlaRopeItems; ++k) id_rope[k] = mla_row_id(a, b, t, (tid + kMlaThreads * k) >> 3, nr);
-        id_sc = tid < kMlaTok ? mla_row_id(a, b, t, tid, nr) : -1;
+        for (int k = 0; k < kMlaRopeItems; ++k) id_rope[k] = mla_raw_id(a, b, t, (tid + kMlaThreads * k) >> 3, nr);
+        id_sc = tid < kMlaTok ? mla_raw_id(a, b, t, tid, nr) : kMlaNoRow;
     };
     auto load_data = [&]() {
 #pragma unroll
-        for (int k = 0; k < kMlaLatItems; ++k)
-            d_lat[k] = id_lat[k] >= 0 ? ldg_nc_v4(a.kv + (int64_t)id_lat[k] * kMlaRowBytes + lane * 16)
-                                      : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < kMlaLatItems; ++k) {
+            const int id = mla_checked_id(a, id_lat[k], id_b);
+            d_lat[k] = id >= 0 ? ldg_nc_v4(a.kv + (int64_t)id * kMlaRowBytes + lane * 16) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int k = 0; k < kMlaRopeItems; ++k)
-            d_rope[k] = id_rope[k] >= 0 ? ldg_nc_v4(a.kv + (int64_t)id_rope[k] * kMlaRowBytes + kMlaRopeOff +
-                                                    (tid & 7) * 16)
-                                        : make_uint4(0, 0, 0, 0);
-        d_sc = id_sc >= 0 ? ldg_nc_v4(a.kv + (int64_t)id_sc * kMlaRowBytes + kMlaScaleOff) : make_uint4(0, 0, 0, 0);
-        d_valid = id_sc >= 0;
+        for (int k = 0; k < kMlaRopeItems; ++k) {
+            const int id = mla_checked_id(a, id_rope[k], id_b);
+            d_rope[k] = id >= 0 ? ldg_nc_v4(a.kv + (int64_t)id * kMlaRowBytes + kMlaRopeOff + (tid & 7) * 16)
+                                : make_uint4(0, 0, 0, 0);
+        }
+        const int id = mla_checked_id(a, id_sc, id_b);
+        d_sc = id >= 0 ? ldg_nc_v4(a.kv + (int64_t)id * kMlaRowBytes + kMlaScaleOff) : make_uint4(0, 0, 0, 0);
+        d_valid = id >= 0;
     };
 
     int64_t w = mla_next_item(a, w_lo, w_hi);
@@ -240,6 +251,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_tile_kernel(MlaArgs a) {
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        const uint32_t qa = sbase + kMlaQ, kb = sbase + kMlaK;
+        if (warp == 4 && lane == 0) {                // S = Q K^T runs while the warps issue loads
+#pragma unroll 1
+            for (int ks = 0; ks < kMlaDim / 16; ++ks) {
+                const uint64_t ad = tc_desc(qa + (ks >> 2) * (kMlaRows * 128) + (ks & 3) * 32, 16, 1024);
+                const uint64_t bd = tc_desc(kb + (ks >> 2) * (kMlaTok * 128) + (ks & 3) * 32, 16, 1024);
+                tc_mma(tmem + kMlaTmS, ad, bd, tc_idesc(kMlaRows, kMlaTok, 0), ks > 0);
+            }
+            tc_commit(smem_u32(&s_full));
+        }
         // ---- (c) the next tile's rows in flight while this one is computed (ids one further)
         const int64_t w2 = w_next;
         if (w2 < w_hi) {
@@ -252,14 +273,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_tile_kernel(MlaArgs a) {
         // ---- (d) roles
         if (warp == 4) {
             if (lane == 0) {
-                const uint32_t qa = sbase + kMlaQ, kb = sbase + kMlaK;
-#pragma unroll 1
-                for (int ks = 0; ks < kMlaDim / 16; ++ks) {
-                    const uint64_t ad = tc_desc(qa + (ks >> 2) * (kMlaRows * 128) + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = tc_desc(kb + (ks >> 2) * (kMlaTok * 128) + (ks & 3) * 32, 16, 1024);
-                    tc_mma(tmem + kMlaTmS, ad, bd, tc_idesc(kMlaRows, kMlaTok, 0), ks > 0);
-                }
-                tc_commit(smem_u32(&s_full));
                 if (mbar_wait_bounded(smem_u32(&p_full), ph, kWaitLimitNs)) {
                     tc_fence_after();
                     // V: this half's four column blocks of the latent, read MN-major (16 rows per k-step)
