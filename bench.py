@@ -54,8 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-mla", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the tiny / long / batched decode legs")
-    ap.add_argument("--no-prefetch", action="store_true",
-                    help="fused steps without the next layer's L2 prefetch hint")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="headline graph with each layer-step's L2 prefetch hint of the next layer's keys")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-instrument", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -217,7 +217,7 @@ def max_over_ranks(x: float, world: int) -> float:
 class DecodeLayers:
     """12 layers of the million-token decode workload resident in HBM."""
 
-    def __init__(self, n_layers, device, fused=True, prefetch=True):
+    def __init__(self, n_layers, device, fused=True, prefetch=False):
         import torch
         from indexer_driven_sparse_gb300 import inputs as I
         from indexer_driven_sparse_gb300.pipeline import DecodeBatch
@@ -336,8 +336,7 @@ def decode_config_leg(name, w, pk, steps, warmup, cold=False):
 
     def body():
         for l, L in enumerate(w.layers):
-            nxt = pooled[(l + 1) % n_l] if n_l > 1 else None      # next layer's keys into L2
-            b.fused_step(L.raw_idx_k, pooled[l], L.q_idx, L.q, L.k_cache, L.v_cache, next_read=nxt)
+            b.fused_step(L.raw_idx_k, pooled[l], L.q_idx, L.q, L.k_cache, L.v_cache)
 
     with torch.cuda.stream(stream):
         body()
@@ -956,7 +955,7 @@ def main(argv=None):
     torch.cuda.set_device(local)
     pk = peaks()
 
-    dl = DecodeLayers(args.layers, "cuda", fused=args.path == "fused", prefetch=not args.no_prefetch)
+    dl = DecodeLayers(args.layers, "cuda", fused=args.path == "fused", prefetch=args.prefetch)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         dl.step()                               # eager warm-up, checks status below
@@ -983,8 +982,8 @@ def main(argv=None):
                    "layers": n_layers,
                    "n_q_heads": 16, "n_kv_heads": 2, "head_dim": 256, "idx_dim": 128, "ratio": 4,
                    "budget": 2048, "parallelism": f"replicas{world}",
-                   "l2_prefetch": "none" if args.no_prefetch else "each layer-step prefetches the next layer's "
-                                                                  "pooled keys into L2 (qsa_decode_step_prefetch)",
+                   "l2_prefetch": "each layer-step prefetches the next layer's pooled keys into L2 "
+                                  "(qsa_decode_step_prefetch)" if args.prefetch else "none",
                    "l2": "inputs larger than L2 (12 x 64 MiB pooled keys + 12 x 2 GiB K/V), no flush"},
         "hbm_gbs_algorithmic": bytes_ls * value / world / 1e9,
         "us_per_layer_step": 1e6 * t / (args.steps * n_layers),
@@ -996,17 +995,19 @@ def main(argv=None):
     launches_per_layer = 1 if dl.fused else 5    # fused step | pool, score, topk, attention, merge
     line["gpu_launches"] = launches_per_layer * n_layers * args.steps
 
-    if dl.fused and not args.no_prefetch:
-        # the same graph without the L2 prefetch hint
-        dl.prefetch = False
-        g_np = capture(dl.step, stream)
-        t_np = time_graph(g_np, stream, args.steps, args.warmup, world)
-        dl.prefetch = True
-        del g_np
-        us_np = 1e6 * t_np / (args.steps * n_layers)
-        line["without_l2_prefetch"] = {"layer_steps_per_s": 1e6 / us_np, "us_per_layer_step": us_np,
-                                       "hbm_gbs_algorithmic": bytes_ls / (us_np * 1e-6) / 1e9,
-                                       "frac": bytes_ls / (us_np * 1e-6) / 1e9 / pk["hbm"]}
+    if dl.fused:
+        # the same graph with the other setting of the L2 prefetch hint (qsa_decode_step_prefetch)
+        dl.prefetch = not args.prefetch
+        g_alt = capture(dl.step, stream)
+        t_alt = time_graph(g_alt, stream, args.steps, args.warmup, world)
+        dl.prefetch = args.prefetch
+        del g_alt
+        us_alt = 1e6 * t_alt / (args.steps * n_layers)
+        line["with_l2_prefetch" if not args.prefetch else "without_l2_prefetch"] = {
+            "layer_steps_per_s": 1e6 / us_alt, "us_per_layer_step": us_alt,
+            "hbm_gbs_algorithmic": bytes_ls / (us_alt * 1e-6) / 1e9,
+            "frac": bytes_ls / (us_alt * 1e-6) / 1e9 / pk["hbm"],
+            "note": "each layer-step prefetches the next layer's pooled keys into L2 during its exchanges"}
     if dl.fused:
         # The step graph holds only the 12 fused launches, back to back (each a programmatic
         # dependent of the previous one), so a launch's share of the step time is its duration
