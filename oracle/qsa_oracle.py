@@ -41,6 +41,7 @@ __all__ = [
     "E4M3_MAX", "e4m3_round", "quantize_pooled_fp8", "score_blocks_fp8",
     "score_error_bound_fp8", "MLA_LATENT", "MLA_ROPE", "MLA_GROUP", "quantize_mla_rows_fp8",
     "sparse_mla_attend", "MLA_ROW_BYTES", "e4m3_value", "mla_rows_from_bytes",
+    "KV_GROUP", "e4m3_code", "quantize_kv_fp8", "dequantize_kv_fp8",
 ]
 
 # indexer_compress_ratio and indexer_budget from the model's text_config
@@ -414,6 +415,61 @@ def mla_rows_from_bytes(row_bytes) -> tuple:
     latent = (codes.reshape(n, 4, MLA_GROUP) * scales[:, :, None]).reshape(n, MLA_LATENT)
     rope = bf16_bits_to_f64(r[:, MLA_LATENT + 16:].copy().view("<u2"))
     return latent, rope
+
+
+# --------------------------------------------------------------------------- FP8 K/V rows
+
+# "GLM-5.3 最適化 第2部" (footnote 1) stores the attended KV rows as FP8: E4M3 codes in groups
+# of 128 dims, one fp32 scale per group (the 656-byte MLA row above; the indexer key of
+# footnote 3 is the same 128 codes + 4 B scale). Reading for the GQA cache of the QSA path
+# (the pages give no separate format for it): each token's K row and V row of each KV head
+# (head_dim 256) is quantised the same way, two groups of 128 dims, and stored as a plane of
+# codes [T, Hkv, 256] (uint8) beside a plane of scales [T, Hkv, 2] (fp32). Attention then
+# reads the value code x scale of every element in place of the bf16 value.
+KV_GROUP = 128
+
+
+def e4m3_code(values) -> np.ndarray:
+    """Byte code of E4M3 values (each exactly representable, |v| <= 448): bit 7 the sign,
+    bits 6..3 the exponent field (bias 7; 0 for zero and subnormals), bits 2..0 the mantissa.
+    A normal value v = (1 + m/8) 2^(e-7); a subnormal v = (m/8) 2^-6. Negative zero is 0x80.
+    Raises ValueError for a value the format cannot hold exactly."""
+    v = np.asarray(values, dtype=np.float64)
+    a = np.abs(v)
+    if np.any(~np.isfinite(a)) or np.any(a > E4M3_MAX):
+        raise ValueError("value outside the E4M3 range")
+    _, e = np.frexp(np.where(a > 0, a, 1.0))           # a = f 2^e, f in [0.5, 1): a in [2^(e-1), 2^e)
+    normal = a >= 2.0 ** -6
+    field = np.where(normal, e - 1 + 7, 0)
+    mant = np.where(normal, (a / np.ldexp(1.0, e - 1) - 1.0) * 8.0, a / 2.0 ** -9)
+    if np.any(mant != np.rint(mant)) or np.any(mant > 7):
+        raise ValueError("value not exactly representable in E4M3")
+    code = (np.signbit(v).astype(np.int64) << 7) | (field.astype(np.int64) << 3) | mant.astype(np.int64)
+    return code.astype(np.uint8)
+
+
+def quantize_kv_fp8(kv_bits):
+    """FP8 K (or V) cache rows from bf16 rows [..., D] (D a multiple of 128): every 128-dim
+    group quantised as an FP8 indexer key is (scale = group max|x| / 448 and codes =
+    E4M3(x / scale), fp32 divisions, nearest-even codes; an all-zero group has scale 0 and
+    zero codes). Returns (codes uint8 [..., D] as stored, scales float32 [..., D / 128])."""
+    x = np.asarray(kv_bits)
+    d = x.shape[-1]
+    if d % KV_GROUP:
+        raise ValueError("row length must be a multiple of 128")
+    groups = x.reshape(-1, KV_GROUP)
+    vals, scl = quantize_pooled_fp8(groups) if groups.shape[0] else (np.zeros((0, KV_GROUP)), np.zeros(0, np.float32))
+    return e4m3_code(vals).reshape(x.shape), scl.reshape(x.shape[:-1] + (d // KV_GROUP,))
+
+
+def dequantize_kv_fp8(codes, scales) -> np.ndarray:
+    """Values of FP8 K/V rows: element d of a row is e4m3_value(code_d) x scale[d // 128],
+    exact in float64. codes [..., D] uint8, scales [..., D / 128]; returns float64 [..., D]."""
+    c = np.asarray(codes, dtype=np.uint8)
+    s = np.asarray(scales, dtype=np.float64)
+    d = c.shape[-1]
+    v = e4m3_value(c).reshape(c.shape[:-1] + (d // KV_GROUP, KV_GROUP))
+    return (v * s[..., None]).reshape(c.shape)
 
 
 def sparse_mla_attend(q_bits, latent: np.ndarray, rope: np.ndarray, rows, scale: float | None = None):

@@ -614,3 +614,115 @@ def test_mla_row_bytes_decode_by_hand():
     assert np.isnan(O.e4m3_value(0x7F)) and np.isnan(O.e4m3_value(0xFF))
     vals, _ = _e4m3_table()
     np.testing.assert_array_equal(np.sort(O.e4m3_value(np.arange(0x7F))), vals)      # every finite code
+
+
+# --------------------------------------------------------------------------- FP8 K/V rows
+
+def test_e4m3_code_by_hand_and_round_trip():
+    # codes from the bit layout (sign | exponent field, bias 7 | 3 mantissa bits)
+    vals = [1.0, 448.0, -448.0, 2.0 ** -9, 0.0, -0.0, 1.125, 0.5, 2.0 ** -6, 3.5, -0.875 * 2.0 ** -6, 240.0]
+    want = [0x38, 0x7E, 0xFE, 0x01, 0x00, 0x80, 0x39, 0x30, 0x08, 0x46, 0x87, 0x77]
+    np.testing.assert_array_equal(O.e4m3_code(vals), want)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    np.testing.assert_array_equal(O.e4m3_code(O.e4m3_value(finite)), finite)
+    for bad in (1.0625, 449.0, 2.0 ** -10, float("nan"), float("inf")):
+        with pytest.raises(ValueError):
+            O.e4m3_code([bad])
+
+
+def _kv_case(t=9, hkv=2, seed=61):
+    rng = np.random.default_rng(seed)
+    x = torch.from_numpy(rng.standard_normal((t, hkv, 256)).astype(np.float32)).bfloat16().float().numpy()
+    x[2, hkv - 1] = 0.0                # an all-zero row: both groups scale 0
+    x[1, 0, 128:] = 0.0                # one zero group beside a live one
+    x[0, hkv - 1, :128] *= 2.0 ** -20  # a group whose quotients are all tiny before scaling
+    return x, to_bits(x)
+
+
+def test_quantize_kv_fp8_scales_are_group_maxima():
+    x, bits = _kv_case()
+    codes, scales = O.quantize_kv_fp8(bits)
+    assert codes.dtype == np.uint8 and codes.shape == (9, 2, 256)
+    assert scales.dtype == np.float32 and scales.shape == (9, 2, 2)
+    g = x.reshape(9, 2, 2, 128)
+    want = (np.abs(g).max(axis=3).astype(np.float32) / np.float32(448.0)).astype(np.float32)
+    np.testing.assert_array_equal(scales, want)
+    assert scales[2, 1, 0] == scales[2, 1, 1] == 0 and not codes[2, 1].any()
+    assert scales[1, 0, 1] == 0 and not codes[1, 0, 128:].any() and scales[1, 0, 0] > 0
+    # the largest magnitude of every live group is coded as +-448
+    live = scales > 0
+    mags = np.abs(O.e4m3_value(codes)).reshape(9, 2, 2, 128).max(axis=3)
+    np.testing.assert_array_equal(mags[live], 448.0)
+
+
+def test_quantize_kv_fp8_codes_are_nearest_table_values():
+    # brute force: each code is the table value nearest to the fp32 quotient x / scale
+    x, bits = _kv_case(t=3, hkv=1, seed=62)
+    codes, scales = O.quantize_kv_fp8(bits)
+    vals, _ = _e4m3_table()
+    full = np.concatenate([-vals[::-1], vals[1:]])
+    g = x.reshape(-1, 128)
+    s = scales.reshape(-1)
+    got = O.e4m3_value(codes).reshape(-1, 128)
+    assert (s == 0).sum() == 3 and not got[s == 0].any()      # token 2 (both groups), token 1 group 1
+    for r in np.flatnonzero(s > 0):
+        quot = (g[r].astype(np.float32) / s[r]).astype(np.float64)
+        for qv, gv in zip(quot, got[r]):
+            d = np.abs(full - qv)
+            assert gv == full[np.argmin(d)] or np.isclose(d.min(), np.sort(d)[1])
+
+
+def test_quantize_kv_fp8_groups_are_independent():
+    # the groups are dims [0, 128) and [128, 256) of each (token, head) row: scaling one group
+    # by 2^-5 scales only its scale, codes unchanged
+    x, bits = _kv_case(seed=63)
+    codes, scales = O.quantize_kv_fp8(bits)
+    y = x.copy()
+    y[:, 1, 128:] *= 2.0 ** -5
+    codes2, scales2 = O.quantize_kv_fp8(to_bits(y))
+    np.testing.assert_array_equal(codes2, codes)
+    np.testing.assert_array_equal(scales2[:, 1, 1], scales[:, 1, 1] * np.float32(2.0 ** -5))
+    np.testing.assert_array_equal(np.delete(scales2.reshape(9, 4), 3, axis=1), np.delete(scales.reshape(9, 4), 3, axis=1))
+
+
+def test_dequantize_kv_fp8_by_hand_and_error_bound():
+    codes = np.zeros((1, 2, 256), np.uint8)
+    codes[0, 0, 0], codes[0, 0, 127], codes[0, 0, 128], codes[0, 1, 255] = 0x38, 0xFE, 0x39, 0x01
+    scales = np.array([[[0.5, 4.0], [1.0, 2.0]]], np.float32)
+    v = O.dequantize_kv_fp8(codes, scales)
+    assert v[0, 0, 0] == 0.5 and v[0, 0, 127] == -224.0 and v[0, 0, 128] == 4.5 and v[0, 1, 255] == 2.0 ** -8
+    assert np.count_nonzero(v) == 4
+    # half a mantissa step: |deq - x| <= 2^-4 |x| where x / scale is a normal E4M3 value, and
+    # the bound is nearly reached somewhere
+    x, bits = _kv_case(seed=64)
+    c, s = O.quantize_kv_fp8(bits)
+    deq = O.dequantize_kv_fp8(c, s)
+    sc = np.repeat(s.astype(np.float64), 128, axis=-1)
+    big = (np.abs(x) >= 2.0 ** -6 * sc * 1.01) & (x != 0)
+    rel = np.abs(deq - x)[big] / np.abs(x)[big]
+    assert rel.max() <= 2.0 ** -4 * (1 + 1e-6) and rel.max() > 2.0 ** -4 * 0.9
+
+
+def test_decode_query_on_fp8_kv_closed_forms():
+    # identical K rows: every attended token gets the same weight, so each head outputs the mean
+    # of the dequantised V rows of its KV head over the attended tokens, and lse = logit + ln n
+    rng = np.random.default_rng(65)
+    p, hkv, hq = 30, 2, 8
+    krow = torch.from_numpy(rng.standard_normal((hkv, 256)).astype(np.float32)).bfloat16().float().numpy()
+    k = np.broadcast_to(krow, (p + 1, hkv, 256)).copy()
+    vv = torch.from_numpy(rng.standard_normal((p + 1, hkv, 256)).astype(np.float32)).bfloat16().float().numpy()
+    kc, ks = O.quantize_kv_fp8(to_bits(k))
+    vc, vs = O.quantize_kv_fp8(to_bits(vv))
+    kd, vd = O.dequantize_kv_fp8(kc, ks), O.dequantize_kv_fp8(vc, vs)
+    q = to_bits(torch.from_numpy(rng.standard_normal((hq, 256)).astype(np.float32)).bfloat16().float().numpy())
+    raw = to_bits(torch.from_numpy(rng.standard_normal((p + 1, 128)).astype(np.float32)).bfloat16().float().numpy())
+    qi = to_bits(torch.from_numpy(rng.standard_normal(128).astype(np.float32)).bfloat16().float().numpy())
+    r = O.decode_query(p, qi, O.pool_keys(raw), q, kd, vd, hkv)
+    n = r["tokens"].size
+    assert n == p + 1                                # dense: every token up to p
+    qf = O.bf16_bits_to_f64(q)
+    for h in range(hq):
+        kv = h // (hq // hkv)
+        np.testing.assert_allclose(r["out"][h], vd[r["tokens"], kv].mean(axis=0), rtol=1e-12, atol=1e-14)
+        logit = (kd[0, kv] @ qf[h]) / 16.0
+        np.testing.assert_allclose(r["lse"][h], logit + np.log(n), rtol=1e-12)
