@@ -300,6 +300,42 @@ QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *ra
                                        int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
                                        qsa_stream stream);
 
+/* FP8 K/V rows — the KV-row format of "GLM-5.3 最適化 第2部：16基のH200上でのPCP、DCP、および
+ * Hybrid HiSparse" (footnote 1: E4M3 codes in groups of 128 dims, one fp32 scale per group)
+ * applied to the GQA cache of this library. Each 256-dim row (one token's K, or V, of one KV
+ * head) is two groups; for group g of row r:
+ *   scales[r][g] = max_d |x[r][128 g + d]| / 448 (an fp32 IEEE division);
+ *   codes[r][128 g + d] = E4M3(x[r][128 g + d] / scales[r][g]) (fp32 IEEE division, nearest
+ *   even, saturated at +-448); a group of zeros has scale 0 and zero codes.
+ *   x [n_rows][256] bf16, 16-byte aligned (a cache [T][Hkv][256] is n_rows = T x Hkv);
+ *   codes [n_rows][256] uint8 (written), 16-byte aligned; scales [n_rows][2] fp32 (written),
+ *   8-byte aligned. Device memory or mapped pinned host memory.
+ * No workspace, no device-side errors (inputs are not indexed). n_rows = 0 is a no-op;
+ * n_rows < 0 or above 2^34, NULL or misaligned pointers: QSA_ERR_INVALID_ARGUMENT. Non-finite
+ * inputs are outside the contract. Use it to append the new token's rows to an FP8 cache. */
+QSA_API qsa_status qsa_quantize_kv_fp8(const qsa_bf16 *x, int64_t n_rows, uint8_t *codes, float *scales,
+                                       qsa_stream stream);
+
+/* a1-a5 fused over FP8 K/V rows — qsa_decode_step (bf16 indexer keys: `pooled`) or
+ * qsa_decode_step_fp8 (FP8 indexer keys: `codes`, `scales`), with the selected tokens' K and
+ * V read from FP8 rows as qsa_quantize_kv_fp8 writes them instead of bf16 rows. Give exactly
+ * one key format (the other pointer(s) NULL), else QSA_ERR_INVALID_ARGUMENT.
+ *   k_codes, v_codes [n_tokens_total][n_kv_heads][256] uint8, 16-byte aligned;
+ *   k_scales, v_scales [n_tokens_total][n_kv_heads][2] fp32, 16-byte aligned.
+ * Element d of a row has the value code_d x scale[d / 128]. The logit of query head h and
+ * token t is scale_softmax x sum over the two groups of (scale_g x the fp32 sum of the
+ * group's exact bf16 x E4M3 products); the output is sum_t softmax_t x (code x scale) in
+ * fp32, rounded once to bf16. Selection, outputs, workspace (QSA_OP_DECODE_STEP), limits and
+ * errors as qsa_decode_step; the rows (and scales) may live in mapped pinned host memory. */
+QSA_API qsa_status qsa_decode_step_fp8kv(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                         uint8_t *codes, float *scales, int64_t n_pooled_total,
+                                         const int32_t *blk_off, const qsa_bf16 *q_idx, const qsa_bf16 *q,
+                                         const uint8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                                         const float *v_scales, int64_t n_tokens_total, const int32_t *tok_off,
+                                         const int32_t *ctx_len, int32_t B, int64_t max_blocks, int32_t *blocks,
+                                         int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                         qsa_stream stream);
+
 /* a1-a5 fused, with an L2 prefetch hint — qsa_decode_step (and qsa_decode_step_fp8) plus
  * the memory the caller's next call will read, typically the next layer's pooled keys (or
  * FP8 codes). Each CTA, once its own pooled-key stream is done, issues L2 prefetch hints for

@@ -73,6 +73,9 @@ _SIGNATURES = {
     "qsa_index_score_fp8": (_I32, [_CFG, _P, _P, _P, _I32, _P, _P, _I64, _P, _P, _I64, _P, _SZ, _P]),
     "qsa_decode_step_fp8": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P,
                                     _P, _P, _P, _SZ, _P]),
+    "qsa_decode_step_fp8kv": (_I32, [_CFG, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32,
+                                      _I64, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qsa_quantize_kv_fp8": (_I32, [_P, _I64, _P, _P, _P]),
     "qsa_sparse_mla_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "qsa_sparse_mla_decode": (_I32, [_P, _I32, _P, _I64, _P, _P, _I32, _I32, C.c_float, _P, _P, _P, _SZ, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
@@ -270,6 +273,34 @@ def qsa_decode_step_fp8(cfg, raw_idx_k, codes, scales, blk_off, q_idx, q, k_cach
     else:
         _check(load().qsa_decode_step_fp8_prefetch(*args, *_next_read(next_read), _stream(stream)),
                "qsa_decode_step_fp8_prefetch")
+
+
+def qsa_quantize_kv_fp8(x, codes, scales, stream=None):
+    """FP8 K/V rows: x [..., 256] bf16 -> codes [..., 256] uint8 and scales [..., 2] fp32."""
+    if x.shape[-1] != 256 or codes.shape != x.shape or scales.shape != x.shape[:-1] + (2,):
+        raise ValueError("x [..., 256], codes [..., 256], scales [..., 2]")
+    n_rows = x.numel() // 256
+    _check(load().qsa_quantize_kv_fp8(_ptr(x, torch.bfloat16, "x"), n_rows, _ptr(codes, torch.uint8, "codes"),
+                                      _ptr(scales, torch.float32, "scales"), _stream(stream)),
+           "qsa_quantize_kv_fp8")
+
+
+def qsa_decode_step_fp8kv(cfg, raw_idx_k, pooled, codes, scales, blk_off, q_idx, q, k_codes, k_scales, v_codes,
+                          v_scales, tok_off, ctx_len, max_blocks, blocks, count, out, lse, ws, stream=None):
+    """One fused decode layer-step over FP8 K/V rows (codes [T, Hkv, 256] uint8 + scales [T, Hkv, 2]
+    fp32); the indexer keys are bf16 (`pooled`) or FP8 (`codes`, `scales`), the other pair None."""
+    n_pooled = pooled.shape[0] if pooled is not None else codes.shape[0]
+    if pooled is None and codes.shape[0] != scales.shape[0]:
+        raise ValueError("codes and scales must have one row per pooled block")
+    args = [C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"), _ptr(pooled, torch.bfloat16, "pooled"),
+            _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"), n_pooled,
+            _ptr(blk_off, torch.int32), _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(q, torch.bfloat16, "q"),
+            _ptr(k_codes, torch.uint8, "k_codes"), _ptr(k_scales, torch.float32, "k_scales"),
+            _ptr(v_codes, torch.uint8, "v_codes"), _ptr(v_scales, torch.float32, "v_scales"), k_codes.shape[0],
+            _ptr(tok_off, torch.int32), _ptr(ctx_len, torch.int32), ctx_len.numel(), int(max_blocks),
+            _ptr(blocks, torch.int32), _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
+            _ptr(lse, torch.float32, "lse"), *_ws_args(ws)]
+    _check(load().qsa_decode_step_fp8kv(*args, _stream(stream)), "qsa_decode_step_fp8kv")
 
 
 def qsa_sparse_decode_noalloc(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out, lse, stream=None):

@@ -10,6 +10,10 @@
 //                          an all-zero key has scale 0 and zero codes.
 //   index_score_fp8_kernel: s_b = scale_b * sum_d q_idx[d] * code_b[d]; every product of a
 //                          bf16 and an E4M3 value is exact in fp32, summed in fp32.
+//   quantize_kv_fp8_kernel: FP8 K/V rows for the fused decode step ("GLM-5.3 最適化 第2部",
+//                          footnote 1: KV rows as E4M3 codes in 128-dim groups with an fp32
+//                          scale each): every 128-dim group of a 256-dim K or V row is
+//                          quantised exactly as a pooled key above.
 #include "qsa_internal.cuh"
 #include "qsa_ptx.cuh"
 
@@ -178,6 +182,43 @@ __global__ void __launch_bounds__(kF8Threads) index_score_fp8_kernel(const uint1
             issue(t + kF8Stages);
         }
     }
+}
+
+// 16 threads per 128-dim group (8 dims each; a warp is one 256-dim row), grid-stride.
+__global__ void __launch_bounds__(256) quantize_kv_fp8_kernel(const uint16_t *__restrict__ x, int64_t n_groups,
+                                                              uint8_t *__restrict__ codes,
+                                                              float *__restrict__ scales) {
+    const int c = threadIdx.x & 15;
+    const unsigned grp = 0xFFFFu << (threadIdx.x & 16);
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 4);
+    for (int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4; g < n_groups; g += stride) {
+        float v[8];
+        unpack8(ldg_nc_v4(x + g * 128 + c * 8), v);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(grp, amax, o, 16));
+        const float scale = __fdiv_rn(amax, kE4m3Max);
+        uint32_t w0 = 0u, w1 = 0u;
+        if (scale > 0.f) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(v[i], scale);
+            w0 = e4m3x2_of(y[0], y[1]) | (e4m3x2_of(y[2], y[3]) << 16);
+            w1 = e4m3x2_of(y[4], y[5]) | (e4m3x2_of(y[6], y[7]) << 16);
+        }
+        *reinterpret_cast<uint2 *>(codes + g * 128 + c * 8) = make_uint2(w0, w1);
+        if (c == 0) scales[g] = scale;
+    }
+}
+
+cudaError_t launch_quantize_kv_fp8(const uint16_t *x, int64_t n_rows, uint8_t *codes, float *scales,
+                                   cudaStream_t st) {
+    const int64_t n_groups = 2 * n_rows;                      // two 128-dim groups per 256-dim row
+    const int64_t blocks = std::min<int64_t>((n_groups * 16 + 255) / 256, (int64_t)1 << 20);
+    quantize_kv_fp8_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, n_groups, codes, scales);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_pool_keys_fp8(const uint16_t *raw, int64_t n_tok, const int32_t *tok_off, const int32_t *blk_off,

@@ -393,14 +393,23 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
 namespace {
 
 // The fused step with bf16 keys (pooled) or FP8 keys (codes + scales).
+// K/V rows of the fused step: bf16 rows, or FP8 codes + scales planes.
+struct StepKv {
+    const qsa_bf16 *k_cache = nullptr, *v_cache = nullptr;
+    const uint8_t *k_codes = nullptr, *v_codes = nullptr;
+    const float *k_scales = nullptr, *v_scales = nullptr;
+    bool is_fp8 = false;
+    bool fp8() const { return is_fp8; }
+};
+
 qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
                               uint8_t *codes, float *scales, int64_t n_pooled_total, const int32_t *blk_off,
-                              const qsa_bf16 *q_idx, const qsa_bf16 *q, const qsa_bf16 *k_cache,
-                              const qsa_bf16 *v_cache, int64_t n_tokens_total, const int32_t *tok_off,
-                              const int32_t *ctx_len, int32_t B, int64_t max_blocks, int32_t *blocks,
-                              int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                              const qsa_bf16 *q_idx, const qsa_bf16 *q, const StepKv &kv, int64_t n_tokens_total,
+                              const int32_t *tok_off, const int32_t *ctx_len, int32_t B, int64_t max_blocks,
+                              int32_t *blocks, int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
                               qsa_stream stream, const void *next_read = nullptr, size_t next_read_bytes = 0) {
     const bool fp8 = pooled == nullptr;
+    const bool kv8 = kv.fp8();
     QSA_TRY(check_config(cfg));
     QSA_NEED(B >= 0 && B <= kMaxStepRows, "B = %d out of range [0, 64]", B);
     QSA_NEED(max_blocks >= 0 && max_blocks <= (int64_t)1 << 28, "max_blocks out of range");
@@ -408,23 +417,28 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
     if (cfg->n_kv_heads > 2) return fail(QSA_ERR_UNSUPPORTED, "%s supports n_kv_heads <= 2", name);
     QSA_TRY(check_ws(QSA_OP_DECODE_STEP, cfg, B, max_blocks, ws, ws_bytes));
     if (B == 0) return ok();
-    QSA_NEED(raw_idx_k && (fp8 ? codes && scales : pooled != nullptr) && blk_off && q_idx && q && k_cache &&
-                 v_cache && tok_off && ctx_len && blocks && count && out,
+    QSA_NEED(raw_idx_k && (fp8 ? codes && scales : pooled != nullptr) && blk_off && q_idx && q &&
+                 (kv8 ? kv.k_codes && kv.k_scales && kv.v_codes && kv.v_scales : kv.k_cache && kv.v_cache) &&
+                 tok_off && ctx_len && blocks && count && out,
              "NULL tensor pointer");
-    QSA_NEED(aligned(raw_idx_k, 16) && aligned(q_idx, 16) && aligned(k_cache, 16) && aligned(v_cache, 16) &&
-                 aligned(q, 16) && (fp8 ? aligned(codes, 16) && aligned(scales, 16) : aligned(pooled, 16)),
+    const void *k_rows = kv8 ? static_cast<const void *>(kv.k_codes) : kv.k_cache;
+    const void *v_rows = kv8 ? static_cast<const void *>(kv.v_codes) : kv.v_cache;
+    QSA_NEED(aligned(raw_idx_k, 16) && aligned(q_idx, 16) && aligned(k_rows, 16) && aligned(v_rows, 16) &&
+                 aligned(q, 16) && (fp8 ? aligned(codes, 16) && aligned(scales, 16) : aligned(pooled, 16)) &&
+                 (!kv8 || (aligned(kv.k_scales, 16) && aligned(kv.v_scales, 16))),
              "bf16 tensors, codes and scales must be 16-byte aligned");
     if (fp8)
         QSA_NEED(n_pooled_total % 4 == 0, "n_pooled_total = %lld must be a multiple of 4 with FP8 keys",
                  (long long)n_pooled_total);
-    QSA_NEED(device_accessible(raw_idx_k) && device_accessible(k_cache) && device_accessible(v_cache),
-             "raw_idx_k, k_cache and v_cache must be device memory or mapped pinned host memory");
+    QSA_NEED(device_accessible(raw_idx_k) && device_accessible(k_rows) && device_accessible(v_rows) &&
+                 (!kv8 || (device_accessible(kv.k_scales) && device_accessible(kv.v_scales))),
+             "raw_idx_k and the K/V rows (and their scales) must be device memory or mapped pinned host memory");
     if (next_read != nullptr && next_read_bytes >= 16) {
         QSA_NEED(aligned(next_read, 16), "next_read must be 16-byte aligned");
         QSA_NEED(device_accessible(next_read), "next_read must be device memory or mapped pinned host memory");
     }
     const int G = cfg->n_q_heads / cfg->n_kv_heads;
-    const int ctas = decode_step_grid(G, fp8);
+    const int ctas = decode_step_grid(G, fp8, kv8);
     if (ctas == 0) return fail(QSA_ERR_CUDA, "%s: cannot size the cooperative grid on this device", name);
     if (B > ctas) return fail(QSA_ERR_UNSUPPORTED, "%s: B = %d exceeds %d co-resident CTAs", name, B, ctas);
     // every CTA keeps at most decode_step_max_keys() scores on chip; bound the worst row
@@ -442,8 +456,12 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
     a.blk_off = blk_off;
     a.q_idx = q_idx;
     a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
+    a.k_cache = kv8 ? nullptr : kv.k_cache;
+    a.v_cache = kv8 ? nullptr : kv.v_cache;
+    a.k_codes = kv8 ? kv.k_codes : nullptr;
+    a.k_scales = kv8 ? kv.k_scales : nullptr;
+    a.v_codes = kv8 ? kv.v_codes : nullptr;
+    a.v_scales = kv8 ? kv.v_scales : nullptr;
     a.n_tok = n_tokens_total;
     a.tok_off = tok_off;
     a.ctx_len = ctx_len;
@@ -463,6 +481,13 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
     return ok();
 }
 
+StepKv bf16_kv(const qsa_bf16 *k_cache, const qsa_bf16 *v_cache) {
+    StepKv kv;
+    kv.k_cache = k_cache;
+    kv.v_cache = v_cache;
+    return kv;
+}
+
 }  // namespace
 
 extern "C" {
@@ -475,7 +500,7 @@ QSA_API qsa_status qsa_decode_step(const qsa_config *cfg, const qsa_bf16 *raw_id
                                    void *ws, size_t ws_bytes, qsa_stream stream) {
     if (pooled == nullptr && B > 0) return fail(QSA_ERR_INVALID_ARGUMENT, "pooled is NULL");
     return decode_step_common("qsa_decode_step", cfg, raw_idx_k, pooled, nullptr, nullptr, n_pooled_total, blk_off,
-                              q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, max_blocks, blocks,
+                              q_idx, q, bf16_kv(k_cache, v_cache), n_tokens_total, tok_off, ctx_len, B, max_blocks, blocks,
                               count, out, lse, ws, ws_bytes, stream);
 }
 
@@ -489,7 +514,7 @@ QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *ra
     if ((codes == nullptr || scales == nullptr) && B > 0)
         return fail(QSA_ERR_INVALID_ARGUMENT, "codes and scales must be non-NULL");
     return decode_step_common("qsa_decode_step_fp8", cfg, raw_idx_k, nullptr, codes, scales, n_pooled_total,
-                              blk_off, q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, max_blocks,
+                              blk_off, q_idx, q, bf16_kv(k_cache, v_cache), n_tokens_total, tok_off, ctx_len, B, max_blocks,
                               blocks, count, out, lse, ws, ws_bytes, stream);
 }
 
@@ -502,7 +527,7 @@ QSA_API qsa_status qsa_decode_step_prefetch(const qsa_config *cfg, const qsa_bf1
                                             const void *next_read, size_t next_read_bytes, qsa_stream stream) {
     if (pooled == nullptr && B > 0) return fail(QSA_ERR_INVALID_ARGUMENT, "pooled is NULL");
     return decode_step_common("qsa_decode_step_prefetch", cfg, raw_idx_k, pooled, nullptr, nullptr, n_pooled_total,
-                              blk_off, q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len, B, max_blocks,
+                              blk_off, q_idx, q, bf16_kv(k_cache, v_cache), n_tokens_total, tok_off, ctx_len, B, max_blocks,
                               blocks, count, out, lse, ws, ws_bytes, stream, next_read, next_read_bytes);
 }
 
@@ -517,9 +542,44 @@ QSA_API qsa_status qsa_decode_step_fp8_prefetch(const qsa_config *cfg, const qsa
     if ((codes == nullptr || scales == nullptr) && B > 0)
         return fail(QSA_ERR_INVALID_ARGUMENT, "codes and scales must be non-NULL");
     return decode_step_common("qsa_decode_step_fp8_prefetch", cfg, raw_idx_k, nullptr, codes, scales,
-                              n_pooled_total, blk_off, q_idx, q, k_cache, v_cache, n_tokens_total, tok_off, ctx_len,
+                              n_pooled_total, blk_off, q_idx, q, bf16_kv(k_cache, v_cache), n_tokens_total, tok_off, ctx_len,
                               B, max_blocks, blocks, count, out, lse, ws, ws_bytes, stream, next_read,
                               next_read_bytes);
+}
+
+QSA_API qsa_status qsa_decode_step_fp8kv(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                         uint8_t *codes, float *scales, int64_t n_pooled_total,
+                                         const int32_t *blk_off, const qsa_bf16 *q_idx, const qsa_bf16 *q,
+                                         const uint8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                                         const float *v_scales, int64_t n_tokens_total, const int32_t *tok_off,
+                                         const int32_t *ctx_len, int32_t B, int64_t max_blocks, int32_t *blocks,
+                                         int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                                         qsa_stream stream) {
+    if (B > 0 && (pooled == nullptr) == (codes == nullptr || scales == nullptr))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "give either pooled or codes and scales");
+    StepKv kv;
+    kv.is_fp8 = true;
+    kv.k_codes = k_codes;
+    kv.k_scales = k_scales;
+    kv.v_codes = v_codes;
+    kv.v_scales = v_scales;
+    return decode_step_common("qsa_decode_step_fp8kv", cfg, raw_idx_k, pooled, pooled ? nullptr : codes,
+                              pooled ? nullptr : scales, n_pooled_total, blk_off, q_idx, q, kv, n_tokens_total,
+                              tok_off, ctx_len, B, max_blocks, blocks, count, out, lse, ws, ws_bytes, stream);
+}
+
+QSA_API qsa_status qsa_quantize_kv_fp8(const qsa_bf16 *x, int64_t n_rows, uint8_t *codes, float *scales,
+                                       qsa_stream stream) {
+    QSA_NEED(n_rows >= 0 && n_rows <= ((int64_t)1 << 34), "n_rows = %lld out of range", (long long)n_rows);
+    if (n_rows == 0) return ok();
+    QSA_NEED(x && codes && scales, "NULL tensor pointer");
+    QSA_NEED(aligned(x, 16) && aligned(codes, 16) && aligned(scales, 8), "x and codes must be 16-byte aligned, "
+             "scales 8-byte aligned");
+    QSA_NEED(device_accessible(x) && device_accessible(codes) && device_accessible(scales),
+             "x, codes and scales must be device memory or mapped pinned host memory");
+    const cudaError_t e = launch_quantize_kv_fp8(x, n_rows, codes, scales, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize_kv_fp8 launch");
+    return ok();
 }
 
 QSA_API size_t qsa_sparse_mla_workspace_size(int32_t n_heads, int32_t B, int32_t max_rows) {

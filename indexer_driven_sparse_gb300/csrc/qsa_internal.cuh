@@ -285,8 +285,12 @@ struct StepArgs {
     const int32_t *blk_off;
     const uint16_t *q_idx;
     const uint16_t *q;
-    const uint16_t *k_cache;
+    const uint16_t *k_cache;    // bf16 K/V rows [n_tok][Hkv][256] (nullptr with FP8 K/V)
     const uint16_t *v_cache;
+    const uint8_t *k_codes;     // FP8 K/V: codes [n_tok][Hkv][256], scales [n_tok][Hkv][2] (else nullptr)
+    const float *k_scales;
+    const uint8_t *v_codes;
+    const float *v_scales;
     int64_t n_tok;
     const int32_t *tok_off;
     const int32_t *ctx_len;
@@ -315,9 +319,14 @@ struct StepLayout {
 StepLayout step_layout(int B, int64_t max_blocks, int Hq);
 size_t decode_step_ws_bytes(int B, int64_t max_blocks, int Hq);
 int decode_step_max_keys();
-// Number of CTAs the cooperative step kernel runs with on the current device (0 on error).
-int decode_step_grid(int G, bool fp8);
+// Number of CTAs the cooperative step kernel runs with on the current device (0 on error),
+// for FP8 or bf16 indexer keys and FP8 or bf16 K/V rows.
+int decode_step_grid(int G, bool fp8_keys, bool fp8_kv);
 cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st);
+
+// FP8 K/V rows: x [n_rows][256] bf16 -> codes [n_rows][256] E4M3, scales [n_rows][2] fp32.
+cudaError_t launch_quantize_kv_fp8(const uint16_t *x, int64_t n_rows, uint8_t *codes, float *scales,
+                                   cudaStream_t st);
 
 // Set the calling thread's qsa_last_error() text to "<what>: <detail>" and return s.
 qsa_status host_fail(qsa_status s, const char *what, const char *detail);

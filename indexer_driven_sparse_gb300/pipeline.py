@@ -71,6 +71,15 @@ class DecodeBatch:
                                self.tok_off, self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse,
                                self.step_ws, stream, next_read)
 
+    def fused_step_fp8kv(self, raw_idx_k, keys, q_idx, q, kv8, stream=None):
+        """The fused step over FP8 K/V rows (qsa_decode_step_fp8kv). `keys` is the bf16 pooled-key
+        tensor or a (codes, scales) pair of FP8 keys; `kv8` is (k_codes, k_scales, v_codes,
+        v_scales) as qsa_quantize_kv_fp8 writes them."""
+        pooled, codes, scales = (keys, None, None) if torch.is_tensor(keys) else (None, *keys)
+        qb.qsa_decode_step_fp8kv(self.cfg, raw_idx_k, pooled, codes, scales, self.blk_off, q_idx, q, *kv8,
+                                 self.tok_off, self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse,
+                                 self.step_ws, stream)
+
     def fused_status(self, stream=None):
         return qb.qsa_read_device_status(self.step_ws, stream)
 

@@ -224,6 +224,36 @@ def test_decode_step_fp8_host_checks(lib):
                                FAKE, FAKE, FAKE, 0, FAKE, need, 0) == qb.QSA_ERR_INVALID_ARGUMENT
 
 
+def test_fp8_kv_calls_host_checks(lib):
+    # the quantiser: empty is a no-op; NULL, misaligned and out-of-range arguments are refused
+    assert lib.qsa_quantize_kv_fp8(0, 0, 0, 0, 0) == qb.QSA_OK
+    assert lib.qsa_quantize_kv_fp8(FAKE, -1, FAKE, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_quantize_kv_fp8(FAKE, (1 << 34) + 1, FAKE, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_quantize_kv_fp8(FAKE, 4, FAKE, 0, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_quantize_kv_fp8(FAKE, 4, FAKE + 8, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"aligned" in lib.qsa_last_error()
+    assert lib.qsa_quantize_kv_fp8(FAKE, 4, FAKE, FAKE + 4, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    # the fused step over FP8 K/V: exactly one key format, all four K/V planes, 16-byte alignment
+    c = cfg()
+    need = lib.qsa_workspace_size(qb.OP_DECODE_STEP, C.byref(c), 1, 1000)
+
+    def call(pooled, codes, scales, kc, ks, vc, vs, B=1):
+        return lib.qsa_decode_step_fp8kv(C.byref(c), FAKE, pooled, codes, scales, 1000, FAKE, FAKE, FAKE, kc, ks, vc,
+                                         vs, 4001, FAKE, FAKE, B, 1000, FAKE, FAKE, FAKE, 0, FAKE, need, 0)
+    assert call(0, 0, 0, 0, 0, 0, 0, B=0) == qb.QSA_OK                                   # empty batch
+    assert call(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE) == qb.QSA_ERR_INVALID_ARGUMENT  # both key formats
+    assert b"either" in lib.qsa_last_error()
+    assert call(0, 0, 0, FAKE, FAKE, FAKE, FAKE) == qb.QSA_ERR_INVALID_ARGUMENT          # neither
+    assert call(FAKE, 0, 0, FAKE, 0, FAKE, FAKE) == qb.QSA_ERR_INVALID_ARGUMENT          # NULL k_scales
+    assert b"NULL" in lib.qsa_last_error()
+    assert call(FAKE, 0, 0, FAKE, FAKE + 8, FAKE, FAKE) == qb.QSA_ERR_INVALID_ARGUMENT   # misaligned scales
+    assert b"aligned" in lib.qsa_last_error()
+    assert call(0, FAKE, FAKE, FAKE + 4, FAKE, FAKE, FAKE) == qb.QSA_ERR_INVALID_ARGUMENT  # misaligned codes
+    assert lib.qsa_decode_step_fp8kv(C.byref(cfg(n_kv_heads=4)), FAKE, FAKE, 0, 0, 1000, FAKE, FAKE, FAKE, FAKE,
+                                     FAKE, FAKE, FAKE, 4001, FAKE, FAKE, 1, 1000, FAKE, FAKE, FAKE, 0, FAKE,
+                                     need, 0) == qb.QSA_ERR_UNSUPPORTED
+
+
 def test_sparse_mla_host_checks(lib):
     need = lib.qsa_sparse_mla_workspace_size(64, 4, 2048)
     # status block + one segment partial (64 heads x 256 fp32, and a (max, sum) pair per head)

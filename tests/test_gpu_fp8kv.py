@@ -1,0 +1,168 @@
+"""FP8 K/V rows (E4M3 codes per 128-dim group with an fp32 scale): the GPU quantiser against
+the oracle's bit for bit, and the fused decode step over FP8 K/V (qsa_decode_step_fp8kv)
+against the oracle's attention on the dequantised rows, with bf16 and with FP8 indexer keys.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from indexer_driven_sparse_gb300 import binding as qb
+from indexer_driven_sparse_gb300 import inputs as I
+from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+from parity import bits, check_attention, check_lse, check_selection
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _quantize_gpu(x):
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(x.shape[:-1] + (2,), dtype=torch.float32, device=x.device)
+    qb.qsa_quantize_kv_fp8(x, codes, scales)
+    return codes, scales
+
+
+def _special_rows(n, seed):
+    """bf16 rows [n, 2, 256] with the quantiser's edge cases: zero rows and groups, one
+    non-zero element, the bf16 extremes, subnormal bf16 values, exact E4M3 multiples."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((n, 2, 256), generator=g)
+    x[0] = 0.0
+    x[1, 0, 128:] = 0.0
+    x[2, 1] = 0.0
+    x[2, 1, 77] = -3.0
+    x[3, 0] = 3.3895e38                            # largest finite bf16
+    x[3, 0, 5] = -3.3895e38
+    x[4, 1, :128] = torch.randn(128, generator=g) * 1e-39     # bf16 subnormals
+    x[5, 0] = torch.arange(256) % 15 - 7           # small integers: exact codes
+    x[6] *= 1e-30
+    x[7] *= 1e30
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("n", [8, 9, 1000, 4097])
+def test_quantize_kv_fp8_bit_exact(cuda_lib, n):
+    x = _special_rows(n, seed=n)
+    codes, scales = _quantize_gpu(x.to(DEV))
+    want_c, want_s = O.quantize_kv_fp8(bits(x))
+    assert np.array_equal(codes.cpu().numpy(), want_c)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), want_s.view(np.uint32))
+
+
+def _kv8(L):
+    kc, ks = _quantize_gpu(L.k_cache)
+    vc, vs = _quantize_gpu(L.v_cache)
+    return kc, ks, vc, vs
+
+
+def _grade(w, b, blocks_ref, kv8, fp8_keys=None, max_fp32_swaps=0):
+    """Selection: equal to the bf16-K/V step's on the same keys, and graded against the oracle
+    by the band rule. Attention: the oracle on the oracle's FP8 rows of the attended tokens."""
+    assert torch.equal(b.blocks, blocks_ref), "FP8-K/V step selected other blocks than the bf16-K/V step"
+    Lh = w.layers[0]
+    rb, qib, qbits = bits(Lh.raw_idx_k), bits(Lh.q_idx), bits(Lh.q)
+    kb, vb = bits(Lh.k_cache), bits(Lh.v_cache)
+    blocks, count, out, lse = b.blocks.cpu().numpy(), b.count.cpu().numpy(), b.out.cpu(), b.lse.cpu().numpy()
+    off = w.tok_off
+    stats = dict(band=0, fp32=0, rel=0.0, lse=0.0, rows=0)
+    for s in range(w.batch):
+        p = w.ctx_len[s]
+        nb = p // 4
+        pk = O.pool_keys(rb[off[s]:off[s + 1]])
+        if fp8_keys is None:
+            n_band, n_fp32 = check_selection(blocks[s], count[s], qib[s], pk, nb)
+        else:
+            vals, scl = O.quantize_pooled_fp8(pk)
+            n_band, n_fp32 = check_selection(blocks[s], count[s], qib[s], None, nb,
+                                             scores=O.score_blocks_fp8(qib[s], vals[:nb], scl[:nb]),
+                                             bound=O.score_error_bound_fp8(qib[s], vals[:nb], scl[:nb]))
+        stats["band"] += n_band
+        stats["fp32"] += n_fp32
+        tokens = O.attended_tokens(p, blocks[s, :count[s]])
+        kd = O.dequantize_kv_fp8(*O.quantize_kv_fp8(kb[off[s] + tokens]))
+        vd = O.dequantize_kv_fp8(*O.quantize_kv_fp8(vb[off[s] + tokens]))
+        ref_out, ref_lse = O.attend(O.bf16_bits_to_f64(qbits[s]), kd, vd, np.arange(tokens.size), w.n_kv_heads,
+                                    1.0 / 16.0)
+        stats["rel"] = max(stats["rel"], check_attention(out[s], ref_out)[2])
+        stats["lse"] = max(stats["lse"], check_lse(lse[s], ref_lse))
+        stats["rows"] += 1
+    print(f"{w.name} fp8 kv: {stats}")
+    assert stats["fp32"] <= max_fp32_swaps, stats
+    return stats
+
+
+def _run(w, fp8_keys=False):
+    L = w.layers[0]
+    L = I.Layer(*(getattr(L, f).to(DEV) for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))
+    b = DecodeBatch(w.n_q_heads, w.n_kv_heads, w.ctx_len)
+    if fp8_keys:
+        keys = b.new_fp8_keys()
+        b.pool_fp8(L.raw_idx_k, *keys)
+        b.fused_step_fp8(L.raw_idx_k, *keys, L.q_idx, L.q, L.k_cache, L.v_cache)
+    else:
+        keys = b.new_pooled()
+        b.pool(L.raw_idx_k, keys)
+        b.fused_step(L.raw_idx_k, keys, L.q_idx, L.q, L.k_cache, L.v_cache)
+    assert b.fused_status()[0] == 0
+    blocks_ref = b.blocks.clone()
+    kv8 = _kv8(L)
+    want = O.quantize_kv_fp8(bits(w.layers[0].k_cache))
+    assert np.array_equal(kv8[0].cpu().numpy(), want[0])
+    b.blocks.fill_(-7)
+    b.out.zero_()
+    b.fused_step_fp8kv(L.raw_idx_k, keys, L.q_idx, L.q, kv8)
+    st = b.fused_status()
+    assert st[0] == 0, st
+    return b, blocks_ref, kv8, (keys if fp8_keys else None)
+
+
+@pytest.mark.parametrize("case", ["sharp16_2052", "sharp16_9001", "sharp16_131072", "sharp_ragged", "dense",
+                                  "tiny_sharp", "g1", "one_kv_head", "fp8_keys_ragged"])
+def test_fused_step_fp8kv(cuda_lib, case):
+    fp8_keys = False
+    if case.startswith("sharp16_"):
+        p = int(case.split("_")[1])
+        w = I.decode_workload(case, [p], 1, 16, 2, "sharp", seed=70 + p % 13)
+    elif case == "sharp_ragged":
+        w = I.decode_workload(case, [2052, 70001, 9001, 4, 2051, 33333], 1, 16, 2, "planted_sharp", seed=71)
+    elif case == "dense":
+        w = I.decode_workload(case, [0, 1, 7, 2047, 2051], 1, 16, 2, "sharp", seed=72)
+    elif case == "tiny_sharp":
+        w = I.tiny_decode(kind="sharp", seed=73)
+    elif case == "g1":                              # one query head per KV head
+        w = I.decode_workload(case, [5000, 3001], 1, 2, 2, "sharp", seed=74)
+    elif case == "one_kv_head":                     # Hkv = 1: 8-byte scale pairs per token
+        w = I.decode_workload(case, [9000, 2051, 40000], 1, 8, 1, "planted_sharp", seed=75)
+    else:
+        fp8_keys = True
+        w = I.decode_workload(case, [5000, 2052, 70001, 4, 12345, 0, 3, 2051], 1, 16, 2, "planted_sharp", seed=76)
+    b, blocks_ref, kv8, keys = _run(w, fp8_keys)
+    _grade(w, b, blocks_ref, kv8, keys)
+
+
+@pytest.mark.parametrize("fp8_keys", [False, True])
+def test_fused_step_fp8kv_million_full_size(cuda_lib, fp8_keys):
+    # the headline geometry (16 / 2 heads, 1,048,320 tokens) with N(0,1) Q/K/V
+    w = I.million_decode(n_layers=1, kind="planted_sharp")
+    b, blocks_ref, kv8, keys = _run(w, fp8_keys)
+    w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
+    _grade(w, b, blocks_ref, kv8, keys)
+
+
+def test_fused_step_fp8kv_host_memory_rows_match(cuda_lib):
+    # FP8 K/V (codes and scales) in mapped pinned host memory: the same results bit for bit
+    w = I.decode_workload("fp8kv_host", [70001, 2052], 1, 16, 2, "planted_sharp", seed=77)
+    b, blocks_ref, kv8, _ = _run(w)
+    want = (b.blocks.clone(), b.out.clone(), b.lse.clone())
+    host = [t.cpu().pin_memory() for t in kv8]
+    L = w.layers[0]
+    L = I.Layer(*(getattr(L, f).to(DEV) for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    b.out.zero_()
+    b.fused_step_fp8kv(L.raw_idx_k, pooled, L.q_idx, L.q, host)
+    torch.cuda.synchronize()
+    assert b.fused_status()[0] == 0
+    assert torch.equal(b.blocks, want[0]) and torch.equal(b.out, want[1]) and torch.equal(b.lse, want[2])
