@@ -596,6 +596,54 @@ def fp8_keys_bench(dl, stream, steps, warmup, pk):
             "gpu_launches_per_layer_step": 5}
 
 
+def fp8_kv_bench(dl, stream, steps, warmup, pk):
+    """Decode with FP8 K/V rows (codes + one fp32 scale per 128 dims, qsa_quantize_kv_fp8) on the
+    same 12 million-token layers: the fused step (qsa_decode_step_fp8kv) in a 12-layer graph over
+    bf16 indexer keys and over FP8 indexer keys, each against its algorithmic bytes."""
+    import torch
+    from indexer_driven_sparse_gb300 import accounting as A
+    from indexer_driven_sparse_gb300 import binding as qb
+    b, layers = dl.b, dl.w.layers
+    kv8, keys8 = [], []
+    for L in layers:
+        planes = []
+        for x in (L.k_cache, L.v_cache):
+            c = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+            sc = torch.empty(x.shape[:-1] + (2,), dtype=torch.float32, device=x.device)
+            qb.qsa_quantize_kv_fp8(x, c, sc)
+            planes += [c, sc]
+        kv8.append(tuple(planes))
+        codes, scales = b.new_fp8_keys()
+        b.pool_fp8(L.raw_idx_k, codes, scales)
+        keys8.append((codes, scales))
+    torch.cuda.synchronize()
+    out = {"format": "K and V rows as 256 E4M3 codes + 2 fp32 scales per token and KV head (264 B of 512)",
+           "kv_bytes_per_layer_step": A.kv_read_bytes_fp8(A.attended(dl.w.ctx_len[0])), "peak_src": pk["src"],
+           "gpu_launches_per_layer_step": 1}
+    for name, fp8_keys in (("bf16_keys", False), ("fp8_keys", True)):
+        def fn():
+            for l, L in enumerate(layers):
+                keys = keys8[l] if fp8_keys else dl.pooled[l]
+                b.fused_step_fp8kv(L.raw_idx_k, keys, L.q_idx, L.q, kv8[l])
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        st = b.fused_status()
+        if st[0] != 0:
+            raise RuntimeError(f"device status in the FP8 K/V leg ({name}): {st}")
+        g = capture(fn, stream)
+        t = time_graph(g, stream, steps, warmup, 1)
+        del g
+        us = 1e6 * t / (steps * len(layers))
+        nbytes = A.decode_layer_step_bytes_fp8kv(dl.w.ctx_len, 16, fp8_keys)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"layer_steps_per_s": 1e6 / us, "us_per_layer_step": us, "algorithmic_bytes": nbytes,
+                     "hbm_gbs_algorithmic": gbs, "frac": gbs / pk["hbm"]}
+    del kv8, keys8
+    torch.cuda.empty_cache()
+    return out
+
+
 def mla_bench(steps, warmup, pk, batch=64):
     """Sparse MLA decode (MQA form, tensor cores): `batch` queries of 64 heads, each over its
     own 2048 rows of a million-token FP8 cache (656 B per row)."""
@@ -749,6 +797,30 @@ def _case_decode_fp8(reps):
     return st if st[0] != 0 else b.fused_status()
 
 
+def _case_decode_fp8kv(reps):
+    """One million-token layer with FP8 K/V rows (bf16 indexer keys): quantise K and V, pool,
+    then `reps` fused steps over the FP8 rows (qsa_decode_step_fp8kv)."""
+    import torch
+    from indexer_driven_sparse_gb300 import binding as qb
+    from indexer_driven_sparse_gb300 import inputs as I
+    from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+    w = I.million_decode(n_layers=1)
+    L = w.layers[0]
+    b = DecodeBatch(16, 2, w.ctx_len)
+    planes = []
+    for x in (L.k_cache, L.v_cache):
+        c = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        sc = torch.empty(x.shape[:-1] + (2,), dtype=torch.float32, device=x.device)
+        qb.qsa_quantize_kv_fp8(x, c, sc)
+        planes += [c, sc]
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    for _ in range(reps):
+        b.fused_step_fp8kv(L.raw_idx_k, pooled, L.q_idx, L.q, planes)
+    torch.cuda.synchronize()
+    return b.fused_status()
+
+
 def _case_mla(reps):
     """Sparse MLA decode: 16 queries x 64 heads over 2048 rows each of a million-token FP8
     cache (about 0.7 GB on the device), `reps` calls."""
@@ -789,6 +861,7 @@ def _case_prefill(reps, attention_only):
 CASES = {
     "decode_step": lambda reps: _case_decode_step(reps),
     "decode_fp8": lambda reps: _case_decode_fp8(reps),
+    "decode_fp8kv": lambda reps: _case_decode_fp8kv(reps),
     "mla": lambda reps: _case_mla(reps),
     "prefill_attention": lambda reps: _case_prefill(reps, True),
     "prefill_chunk": lambda reps: _case_prefill(reps, False),
@@ -1043,6 +1116,9 @@ def main(argv=None):
     if not args.no_fp8:
         line["decode_fp8_indexer_keys"] = fp8_keys_bench(dl, stream, max(20, args.steps // 4), max(3, args.warmup),
                                                          pk)
+
+    if not args.no_fp8:
+        line["decode_fp8_kv"] = fp8_kv_bench(dl, stream, max(20, args.steps // 4), max(3, args.warmup), pk)
 
     if not args.no_mla:
         line["sparse_mla_decode"] = mla_bench(args.steps, args.warmup, pk)

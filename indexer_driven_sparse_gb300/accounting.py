@@ -88,6 +88,24 @@ def decode_layer_step_bytes_fp8(ctx_lens, n_q_heads: int, n_kv_heads: int = 2, h
     return total
 
 
+def kv_read_bytes_fp8(n_tokens: int, n_kv_heads: int = 2, head_dim: int = 256, group: int = 128) -> int:
+    """K and V bytes of n_tokens tokens over all KV heads as FP8 rows: one code byte per dim and
+    one fp32 scale per 128-dim group (the KV-row format of "GLM-5.3 最適化 第2部", footnote 1)."""
+    return n_tokens * (head_dim + 4 * (head_dim // group)) * 2 * n_kv_heads
+
+
+def decode_layer_step_bytes_fp8kv(ctx_lens, n_q_heads: int, fp8_keys: bool, n_kv_heads: int = 2,
+                                  head_dim: int = 256, idx_dim: int = 128) -> int:
+    """decode_layer_step_bytes with FP8 K/V rows, over bf16 or FP8 indexer keys."""
+    total = 0
+    for p in ctx_lens:
+        nb = visible_blocks(p)
+        total += nb * fp8_key_bytes(idx_dim) if fp8_keys else pooled_scan_bytes(nb, idx_dim)
+        total += kv_read_bytes_fp8(attended(p), n_kv_heads, head_dim)
+        total += 2 * n_q_heads * head_dim * BF16 + idx_dim * BF16
+    return total
+
+
 def prefill_attention_flops(p0: int, n_chunk: int, n_q_heads: int = 16, head_dim: int = 256) -> int:
     """QK^T + PV FLOPs over each chunk query's own selection (2 per multiply-add)."""
     return sum(attended(p0 + i) for i in range(n_chunk)) * n_q_heads * head_dim * 2 * 2

@@ -256,10 +256,10 @@ def test_fp8_kv_calls_host_checks(lib):
 
 def test_sparse_mla_host_checks(lib):
     need = lib.qsa_sparse_mla_workspace_size(64, 4, 2048)
-    # status block + one segment partial (64 heads x 256 fp32, and a (max, sum) pair per head)
-    # per (query, half) and per persistent CTA (up to 256), + slack
-    n_part = 256 + 2 * 4
-    assert need == 256 + n_part * 64 * 256 * 4 + n_part * 64 * 2 * 4 + 256
+    # status block + the partials: up to 256 persistent CTAs + one per query of 64 heads x 512
+    # fp32 (two latent halves of 256 per (query, half) above 64 heads fit the same bytes), and a
+    # (max, sum) pair per head for up to 256 + 2 per query segments, + slack
+    assert need == 256 + (256 + 4) * 64 * 512 * 4 + (256 + 2 * 4) * 64 * 2 * 4 + 256
     assert lib.qsa_sparse_mla_workspace_size(0, 4, 2048) == 0
     assert lib.qsa_sparse_mla_workspace_size(129, 4, 2048) == 0
     assert lib.qsa_sparse_mla_workspace_size(64, 4, 70000) == 0

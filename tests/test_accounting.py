@@ -79,6 +79,20 @@ def test_fp8_layer_step_bytes():
     assert bf16 - fp8 == 262080 * (256 - 132)
 
 
+def test_fp8_kv_bytes():
+    # an FP8 K or V row of one head: 256 code bytes + two fp32 scales = 264 of the bf16 row's 512
+    assert A.kv_read_bytes_fp8(1, 1) == 2 * 264
+    assert A.kv_read_bytes_fp8(2048) == 2048 * 2 * 2 * 264
+    assert A.kv_read_bytes_fp8(2048) / A.kv_read_bytes(2048) == 264 / 512
+    # the million-token step with FP8 K/V: only the gathered rows shrink
+    bf16 = A.decode_layer_step_bytes([1048320], 16)
+    assert bf16 - A.decode_layer_step_bytes_fp8kv([1048320], 16, False) == 2049 * 2 * 2 * (512 - 264)   # 2048 + own token
+    assert A.decode_layer_step_bytes_fp8kv([1048320], 16, True) == \
+        A.decode_layer_step_bytes_fp8([1048320], 16) - 2049 * 2 * 2 * (512 - 264)
+    # a dense row (p = 10) attends p + 1 tokens
+    assert A.decode_layer_step_bytes_fp8kv([10], 8, False) == 2 * 256 + 11 * 2 * 2 * 264 + 2 * 8 * 512 + 256
+
+
 def test_glm_page_byte_figures():
     # the FP8 indexer key and the sparse-MLA row sizes against the footnotes that print them
     g = figs(GOLDEN_GLM)

@@ -65,9 +65,23 @@ def test_mla_ragged_batch(cuda_lib):
     _check(w, out, lse)
 
 
-@pytest.mark.parametrize("heads", [1, 16, 128])
+@pytest.mark.parametrize("heads", [1, 16, 33, 64, 65, 128])
 def test_mla_head_counts(cuda_lib, heads):
     w = I.mla_workload(3000, [300, 64, 7], heads, seed=4 + heads)
+    out, lse, st = _run(w)
+    assert st[0] == 0, st
+    _check(w, out, lse)
+
+
+def test_mla_many_short_queries(cuda_lib):
+    # 300 queries of 0-200 rows at 64 heads: a CTA's run crosses many (query, half) segments
+    # and query changes, with single-tile segments and empty queries among them
+    g = torch.Generator().manual_seed(21)
+    counts = torch.randint(0, 201, (300,), generator=g).tolist()
+    counts[7] = 0
+    counts[8] = 64
+    counts[9] = 1
+    w = I.mla_workload(20000, counts, 64, seed=21)
     out, lse, st = _run(w)
     assert st[0] == 0, st
     _check(w, out, lse)
