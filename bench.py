@@ -527,9 +527,43 @@ def kv_host_bench(dl, stream, steps, warmup, n_layers=2):
     n = steps * len(layers)
     p = dl.w.ctx_len[0]
     kv_bytes = (2048 + (p % 4) + 1) * 2 * 2 * 256 * 2      # selected tokens + tail, K and V, both heads
-    return {"layers": len(layers), "layer_steps_per_s": n / t, "us_per_layer_step": 1e6 * t / n,
-            "kv_bytes_per_layer_step": kv_bytes, "host_gather_gbs": kv_bytes * n / t / 1e9,
-            "note": "K/V and raw indexer keys in pinned host memory; pooled keys in HBM"}
+    out = {"layers": len(layers), "layer_steps_per_s": n / t, "us_per_layer_step": 1e6 * t / n,
+           "kv_bytes_per_layer_step": kv_bytes, "host_gather_gbs": kv_bytes * n / t / 1e9,
+           "note": "K/V and raw indexer keys in pinned host memory; pooled keys in HBM"}
+    out["host_link"] = host_link_bench(host[0][0], stream)
+    return out
+
+
+def host_link_bench(hk, stream, nbytes=1 << 29, reps=5):
+    """The host link's bandwidth, through this library's calls: bulk copies of 512 MiB between
+    pinned host memory and HBM (qsa_copy_rows), and a kernel streaming 512 MiB of bf16 K rows out
+    of mapped pinned host memory (qsa_quantize_kv_fp8 reads each row once and writes its FP8
+    codes and scales to HBM)."""
+    import torch
+    from indexer_driven_sparse_gb300 import binding as qb
+    src = hk.view(-1)[: nbytes // 2]                          # pinned, bf16
+    dev = torch.empty(nbytes // 2, dtype=torch.bfloat16, device="cuda")
+    rows = nbytes // 512
+    codes = torch.empty(rows, 256, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows, 2, dtype=torch.float32, device="cuda")
+    res = {}
+    for name, fn in (("h2d_copy_gbs", lambda: qb.qsa_copy_rows(dev, nbytes, src, nbytes, nbytes, 1, stream)),
+                     ("d2h_copy_gbs", lambda: qb.qsa_copy_rows(src, nbytes, dev, nbytes, nbytes, 1, stream)),
+                     ("zero_copy_read_gbs", lambda: qb.qsa_quantize_kv_fp8(src.view(rows, 256), codes, scales, stream))):
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    res["bytes"] = nbytes
+    res["note"] = "copies: one cudaMemcpy2DAsync of 512 MiB; zero-copy: 16-byte loads of mapped pinned memory"
+    del dev, codes, scales
+    return res
 
 
 def fp8_keys_bench(dl, stream, steps, warmup, pk):

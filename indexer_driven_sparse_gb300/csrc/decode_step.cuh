@@ -685,15 +685,44 @@ __device__ __forceinline__ int chunk_tok_bytes(int Hkv) {
 
 // Gather one attention chunk: the K and V rows (all KV heads) of up to kAttnTok tokens of
 // the row's token sequence (list blocks, then the query's own block) into shared memory,
-// as 16-byte async copies (bf16 rows, FP8 codes) and 8-byte ones (FP8 scale pairs).
-template <bool KV8>
-__device__ void gather_chunk(const StepArgs &a, unsigned char *dst, int j_base, int n, int n_list, bool dense,
-                             const int32_t *sel, int64_t nb, int64_t base, int p, int row) {
+// bf16 rows, as 16-byte async copies.
+__device__ void gather_chunk_bf16(const StepArgs &a, uint16_t *dst, int j_base, int n, int n_list, bool dense,
+                                  const int32_t *sel, int64_t nb, int64_t base, int p, int row, int row_elems) {
+    const int tok_elems = 2 * row_elems;
+    const int gran_per_tok = tok_elems * 2 / 16;                       // 16-byte granules per token
+    for (int gidx = threadIdx.x; gidx < n * gran_per_tok; gidx += kStepThreads) {
+        const int i = gidx / gran_per_tok;
+        const int rem = gidx - i * gran_per_tok;
+        const int is_v = rem >= gran_per_tok / 2;
+        const int gpos = rem - is_v * (gran_per_tok / 2);
+        const int j = j_base + i;
+        int64_t tk;
+        if (j < kRatio * n_list) {
+            const int64_t blk = dense ? (j >> 2) : sel[j >> 2];
+            if (blk < 0 || blk >= nb) {               // never expected: flag it, read a safe row
+                record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereStep, row);
+                tk = p;
+            } else {
+                tk = kRatio * blk + (j & 3);
+            }
+        } else {
+            tk = kRatio * nb + (j - kRatio * n_list);
+        }
+        const uint16_t *src = (is_v ? a.v_cache : a.k_cache) + (base + tk) * row_elems + gpos * 8;
+        cp_async16(smem_u32(dst + (size_t)i * tok_elems + is_v * row_elems + gpos * 8), src);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// The same chunk with FP8 K/V: per token, the K codes and V codes of every KV head, then their
+// scale pairs, as 16-byte (codes) and 8-byte (scale pairs) async copies.
+__device__ void gather_chunk_fp8kv(const StepArgs &a, unsigned char *dst, int j_base, int n, int n_list, bool dense,
+                                   const int32_t *sel, int64_t nb, int64_t base, int p, int row) {
     const int Hkv = a.n_kv_heads;
-    const int tok_bytes = chunk_tok_bytes<KV8>(Hkv);
-    const int row_bytes = KV8 ? Hkv * kHeadDim : Hkv * kHeadDim * 2;   // one token's K (or V) row
+    const int tok_bytes = chunk_tok_bytes<true>(Hkv);
+    const int row_bytes = Hkv * kHeadDim;                              // one token's K (or V) codes
     const int n_gran = row_bytes / 8;                                  // 16-byte pieces of K and V
-    const int units = n_gran + (KV8 ? 2 * Hkv : 0);                    // + 8-byte scale pairs
+    const int units = n_gran + 2 * Hkv;                                // + 8-byte scale pairs
     for (int gidx = threadIdx.x; gidx < n * units; gidx += kStepThreads) {
         const int i = gidx / units;
         const int rem = gidx - i * units;
@@ -714,22 +743,29 @@ __device__ void gather_chunk(const StepArgs &a, unsigned char *dst, int j_base, 
         if (rem < n_gran) {
             const int is_v = rem >= n_gran / 2;
             const int gpos = rem - is_v * (n_gran / 2);
-            const unsigned char *src;
-            if constexpr (KV8)
-                src = (is_v ? a.v_codes : a.k_codes) + (base + tk) * row_bytes + gpos * 16;
-            else
-                src = reinterpret_cast<const unsigned char *>(is_v ? a.v_cache : a.k_cache) + (base + tk) * row_bytes +
-                      gpos * 16;
-            cp_async16(smem_u32(tdst + is_v * row_bytes + gpos * 16), src);
-        } else if constexpr (KV8) {
+            cp_async16(smem_u32(tdst + is_v * row_bytes + gpos * 16),
+                       (is_v ? a.v_codes : a.k_codes) + (base + tk) * row_bytes + gpos * 16);
+        } else {
             const int su = rem - n_gran;                                   // 0 .. 2 Hkv - 1
             const int is_v = su >= Hkv;
             const int h = su - is_v * Hkv;
-            const float *src = (is_v ? a.v_scales : a.k_scales) + ((base + tk) * Hkv + h) * 2;
-            cp_async8(smem_u32(tdst + 2 * row_bytes + (is_v * Hkv + h) * 8), src);
+            cp_async8(smem_u32(tdst + 2 * row_bytes + (is_v * Hkv + h) * 8),
+                      (is_v ? a.v_scales : a.k_scales) + ((base + tk) * Hkv + h) * 2);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// One chunk of either format into ring half `half` (64 KiB).
+template <bool KV8>
+__device__ __forceinline__ void gather_chunk(const StepArgs &a, unsigned char *ring, int j_base, int n, int n_list,
+                                             bool dense, const int32_t *sel, int64_t nb, int64_t base, int p,
+                                             int row) {
+    if constexpr (KV8)
+        gather_chunk_fp8kv(a, ring, j_base, n, n_list, dense, sel, nb, base, p, row);
+    else
+        gather_chunk_bf16(a, reinterpret_cast<uint16_t *>(ring), j_base, n, n_list, dense, sel, nb, base, p, row,
+                          a.n_kv_heads * kHeadDim);
 }
 
 // This CTA's share of the caller's next read (its grid slice, in 16-byte units), issued as
@@ -1449,17 +1485,25 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         if (kv_t < Hkv) {
 #pragma unroll
             for (int g = 0; g < G; ++g) acc[g] *= s_alpha[kv_t * G + g];
-            const unsigned char *vcol = buf + row_bytes + (KV8 ? kv_t * kHeadDim + d_t : (kv_t * kHeadDim + d_t) * 2);
-            const unsigned char *vscl = buf + 2 * row_bytes + (Hkv + kv_t) * 8 + (d_t >> 7) * 4;   // FP8 V only
+            if constexpr (KV8) {
+                const unsigned char *vcol = buf + row_bytes + kv_t * kHeadDim + d_t;
+                const unsigned char *vscl = buf + 2 * row_bytes + (Hkv + kv_t) * 8 + (d_t >> 7) * 4;
 #pragma unroll 4
-            for (int i = 0; i < n; ++i) {
-                float v;
-                if constexpr (KV8)
-                    v = e4m3_to_f32(vcol[(size_t)i * tok_bytes]) * *reinterpret_cast<const float *>(vscl + (size_t)i * tok_bytes);
-                else
-                    v = bf16_bits_to_float(*reinterpret_cast<const uint16_t *>(vcol + (size_t)i * tok_bytes));
+                for (int i = 0; i < n; ++i) {
+                    const float v = e4m3_to_f32(vcol[(size_t)i * tok_bytes]) *
+                                    *reinterpret_cast<const float *>(vscl + (size_t)i * tok_bytes);
 #pragma unroll
-                for (int g = 0; g < G; ++g) acc[g] = fmaf(pw[(kv_t * G + g) * kAttnTok + i], v, acc[g]);
+                    for (int g = 0; g < G; ++g) acc[g] = fmaf(pw[(kv_t * G + g) * kAttnTok + i], v, acc[g]);
+                }
+            } else {
+                const int tok_elems = tok_bytes / 2;
+                const uint16_t *vcol = reinterpret_cast<const uint16_t *>(buf) + tok_elems / 2 + kv_t * kHeadDim + d_t;
+#pragma unroll 4
+                for (int i = 0; i < n; ++i) {
+                    const float v = bf16_bits_to_float(vcol[(size_t)i * tok_elems]);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) acc[g] = fmaf(pw[(kv_t * G + g) * kAttnTok + i], v, acc[g]);
+                }
             }
         }
         __syncthreads();
