@@ -530,8 +530,51 @@ def kv_host_bench(dl, stream, steps, warmup, n_layers=2):
     out = {"layers": len(layers), "layer_steps_per_s": n / t, "us_per_layer_step": 1e6 * t / n,
            "kv_bytes_per_layer_step": kv_bytes, "host_gather_gbs": kv_bytes * n / t / 1e9,
            "note": "K/V and raw indexer keys in pinned host memory; pooled keys in HBM"}
+    out["with_row_cache"] = rowcache_bench(b, dl, layers, host, stream, steps)
     out["host_link"] = host_link_bench(host[0][0], stream)
     return out
+
+
+def rowcache_bench(b, dl, layers, host, stream, steps, n_slots=16384):
+    """The same host-memory layers through qsa_decode_step_rowcache, eager (every call takes a
+    new epoch, so a captured graph cannot replay it): the first step of each layer misses
+    everywhere and fills the cache; the steps after it repeat the same selection and hit
+    everywhere (the pages measured 60-85 % overlap between consecutive steps)."""
+    import torch
+    from indexer_driven_sparse_gb300 import binding as qb
+    caches = [qb.rowcache_new(b.cfg, n_slots) for _ in layers]
+    epoch = [0]
+
+    def body():
+        epoch[0] += 1
+        for l, L in enumerate(layers):
+            hk, hv, hr = host[l]
+            b.fused_step_rowcache(hr, dl.pooled[l], L.q_idx, L.q, hk, hv, caches[l], n_slots, epoch[0])
+
+    res = {}
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        body()                                        # cold: every row missed and cached
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["cold_us_per_layer_step"] = e0.elapsed_time(e1) * 1e3 / len(layers)
+        for _ in range(3):
+            body()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            body()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = b.fused_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status with the row cache: {st}")
+    us = e0.elapsed_time(e1) * 1e3 / (steps * len(layers))
+    res.update({"hot_us_per_layer_step": us, "hot_layer_steps_per_s": 1e6 / us, "n_slots": n_slots,
+                "timing": "eager launches (one epoch per call), CUDA events on the stream"})
+    del caches
+    return res
 
 
 def host_link_bench(hk, stream, nbytes=1 << 29, reps=5):

@@ -336,6 +336,47 @@ QSA_API qsa_status qsa_decode_step_fp8kv(const qsa_config *cfg, const qsa_bf16 *
                                          int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
                                          qsa_stream stream);
 
+/* f1: a VRAM row cache in front of K/V that live in host memory ("125B MoE を 3090 3 枚で運用
+ * する vLLM 最適化編", section 5: consecutive decode steps select largely the same rows, so rows
+ * read over the host link are kept in unused device memory). A direct-mapped cache of n_slots
+ * token rows; a slot holds one token's K and V rows of every KV head (n_kv_heads x 2 x 512 B)
+ * with a tag (the token's index in the flat K/V arrays), the epoch of its last hit and the
+ * epoch's winning claim. Layout inside the caller's buffer: rows, then int64 tags, uint32 hit
+ * epochs, uint64 claims; its size is qsa_rowcache_bytes (0 for a bad configuration, more than
+ * 2 KV heads, or n_slots outside [1, 2^31]). The caller owns the buffer (device memory,
+ * 16-byte aligned) and keeps one per layer. */
+QSA_API size_t qsa_rowcache_bytes(const qsa_config *cfg, int64_t n_slots);
+
+/* Empty every slot of a row cache (tags -1, hit epochs and claims 0). Call it once before the
+ * first step, and again whenever rows the cache may hold change in host memory other than by
+ * appending new tokens (a sequence's cache reused for another request, blocks reassigned). */
+QSA_API qsa_status qsa_rowcache_init(const qsa_config *cfg, void *cache, size_t cache_bytes, int64_t n_slots,
+                                     qsa_stream stream);
+
+/* a1-a5 fused with the row cache — qsa_decode_step, for K/V (and raw indexer keys) in mapped
+ * pinned host memory (or device memory), with every selected row looked up in `cache` first.
+ * Sequence s owns slots [s n_slots / B, (s + 1) n_slots / B); token t of it maps to slot
+ * lo_s + t mod (its slot count). Per step (`epoch`: at least 1, larger than at every earlier
+ * call with this cache):
+ *   - a selected token whose slot's tag is the token's flat index is read from the cache and
+ *     the slot is marked as hit in this epoch; any other selected token is read from k_cache /
+ *     v_cache and claims its slot with an atomic max of (epoch << 32 | flat index);
+ *   - after every CTA of the sequence has read its rows, a claim's winner writes the row and
+ *     the tag, unless some token hit the slot in this epoch (the rows of each CTA's last two
+ *     chunks of at most 32 tokens each are written, any earlier ones stay uncached this step).
+ * The query's own (incomplete) block is always read from k_cache / v_cache and never cached:
+ * the caller may still be writing it. Hits return exactly the bytes in host memory, so the
+ * outputs equal qsa_decode_step's bit for bit. Cache errors: NULL or misaligned cache,
+ * n_slots < B or above 2^31, epoch 0 -> QSA_ERR_INVALID_ARGUMENT; cache_bytes short ->
+ * QSA_ERR_WORKSPACE_TOO_SMALL. Everything else (bf16 keys and K/V only) as qsa_decode_step. */
+QSA_API qsa_status qsa_decode_step_rowcache(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                            int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
+                                            const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                            int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len,
+                                            int32_t B, int64_t max_blocks, int32_t *blocks, int32_t *count,
+                                            qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *cache,
+                                            size_t cache_bytes, int64_t n_slots, uint32_t epoch, qsa_stream stream);
+
 /* a1-a5 fused, with an L2 prefetch hint — qsa_decode_step (and qsa_decode_step_fp8) plus
  * the memory the caller's next call will read, typically the next layer's pooled keys (or
  * FP8 codes). Each CTA, once its own pooled-key stream is done, issues L2 prefetch hints for

@@ -76,6 +76,10 @@ _SIGNATURES = {
     "qsa_decode_step_fp8kv": (_I32, [_CFG, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32,
                                       _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "qsa_quantize_kv_fp8": (_I32, [_P, _I64, _P, _P, _P]),
+    "qsa_rowcache_bytes": (_SZ, [_CFG, _I64]),
+    "qsa_rowcache_init": (_I32, [_CFG, _P, _SZ, _I64, _P]),
+    "qsa_decode_step_rowcache": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P,
+                                        _P, _P, _P, _SZ, _P, _SZ, _I64, C.c_uint32, _P]),
     "qsa_sparse_mla_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "qsa_sparse_mla_decode": (_I32, [_P, _I32, _P, _I64, _P, _P, _I32, _I32, C.c_float, _P, _P, _P, _SZ, _P]),
     "qsa_status_string": (C.c_char_p, [_I32]),
@@ -301,6 +305,32 @@ def qsa_decode_step_fp8kv(cfg, raw_idx_k, pooled, codes, scales, blk_off, q_idx,
             _ptr(blocks, torch.int32), _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
             _ptr(lse, torch.float32, "lse"), *_ws_args(ws)]
     _check(load().qsa_decode_step_fp8kv(*args, _stream(stream)), "qsa_decode_step_fp8kv")
+
+
+def rowcache_new(cfg, n_slots, device="cuda"):
+    """A row cache of n_slots token rows (uint8 device tensor), emptied."""
+    nbytes = load().qsa_rowcache_bytes(C.byref(cfg), int(n_slots))
+    if nbytes == 0:
+        raise ValueError("bad row-cache configuration")
+    cache = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    qsa_rowcache_init(cfg, cache, n_slots)
+    return cache
+
+
+def qsa_rowcache_init(cfg, cache, n_slots, stream=None):
+    _check(load().qsa_rowcache_init(C.byref(cfg), _ptr(cache), cache.numel(), int(n_slots), _stream(stream)),
+           "qsa_rowcache_init")
+
+
+def qsa_decode_step_rowcache(cfg, raw_idx_k, pooled, blk_off, q_idx, q, k_cache, v_cache, tok_off, ctx_len,
+                             max_blocks, blocks, count, out, lse, ws, cache, n_slots, epoch, stream=None):
+    args = [C.byref(cfg), _ptr(raw_idx_k, torch.bfloat16, "raw_idx_k"), _ptr(pooled, torch.bfloat16, "pooled"),
+            pooled.shape[0], _ptr(blk_off, torch.int32), _ptr(q_idx, torch.bfloat16, "q_idx"),
+            _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k"), _ptr(v_cache, torch.bfloat16, "v"),
+            k_cache.shape[0], _ptr(tok_off, torch.int32), _ptr(ctx_len, torch.int32), ctx_len.numel(),
+            int(max_blocks), _ptr(blocks, torch.int32), _ptr(count, torch.int32), _ptr(out, torch.bfloat16, "out"),
+            _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _ptr(cache), cache.numel(), int(n_slots), int(epoch)]
+    _check(load().qsa_decode_step_rowcache(*args, _stream(stream)), "qsa_decode_step_rowcache")
 
 
 def qsa_sparse_decode_noalloc(cfg, q, k_cache, v_cache, tok_off, ctx_len, blocks, count, out, lse, stream=None):

@@ -11,9 +11,20 @@ size_t decode_step_ws_bytes(int B, int64_t max_blocks, int Hq) { return step_lay
 
 int decode_step_max_keys() { return kMaxKeys; }
 
-int decode_step_grid(int G, bool fp8_keys, bool fp8_kv) {
+RowCacheLayout row_cache_layout(int n_kv_heads, int64_t n_slots) {
+    RowCacheLayout L;
+    L.rows = 0;
+    L.tag = (size_t)n_slots * 2 * n_kv_heads * kHeadDim * 2;
+    L.hit = L.tag + (size_t)n_slots * 8;
+    L.claim = L.hit + ((size_t)n_slots * 4 + 7) / 8 * 8;
+    L.total = L.claim + (size_t)n_slots * 8;
+    return L;
+}
+
+int decode_step_grid(int G, bool fp8_keys, bool fp8_kv, bool row_cache) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (row_cache) return fp8_keys || fp8_kv ? 0 : step_grid_rc(G, dev);
     if (fp8_kv) return step_grid_kv8(G, fp8_keys, dev);
     return fp8_keys ? step_grid_for<true, false>(G, dev) : step_grid_for<false, false>(G, dev);
 }
@@ -31,8 +42,10 @@ cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st) {
     const int G = a.n_q_heads / a.n_kv_heads;
     const bool fp8_keys = a.codes != nullptr;
     const bool fp8_kv = a.k_codes != nullptr;
-    const int ctas = decode_step_grid(G, fp8_keys, fp8_kv);
+    const bool rc = a.rc_rows != nullptr;
+    const int ctas = decode_step_grid(G, fp8_keys, fp8_kv, rc);
     if (ctas < a.B || ctas == 0) return cudaErrorInvalidConfiguration;
+    if (rc) return step_launch_rc(a, G, ctas, st);
     if (fp8_kv) return step_launch_kv8(a, G, fp8_keys, ctas, st);
     return fp8_keys ? step_launch_for<true, false>(a, G, ctas, st) : step_launch_for<false, false>(a, G, ctas, st);
 }

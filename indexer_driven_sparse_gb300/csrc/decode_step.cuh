@@ -33,7 +33,15 @@
 // Template parameters: G query heads per KV head; F8, FP8 indexer keys (128 E4M3 codes +
 // an fp32 scale per block) instead of bf16; KV8, FP8 K/V rows (per token and KV head, 256
 // E4M3 codes in a codes plane and one fp32 scale per 128 dims in a scales plane) instead
-// of bf16 rows. The kernel template lives in this header; decode_step.cu instantiates the
+// of bf16 rows; RC, a VRAM row cache in front of bf16 K/V rows that live in host memory
+// ("125B MoE を 3090 3 枚で運用する vLLM 最適化編", section 5): a direct-mapped cache of whole
+// token rows (K and V of every KV head), each sequence owning an equal share of the slots.
+// A selected token whose slot holds it is read from the cache (its slot is marked as hit in
+// this step's epoch), any other from host memory; a missed token claims its slot with an
+// atomic max of (epoch << 32 | token). After the row's second barrier, when no CTA of the row
+// reads the cache any more, the claim's winner writes the row and the tag, unless the slot
+// was hit in this step. Only tokens of complete blocks are cached (the query's own block may
+// still be written by the caller). The kernel template lives in this header; decode_step.cu instantiates the
 // bf16-K/V kernels and decode_step_kv8.cu the FP8-K/V ones, so the two compile in parallel.
 #pragma once
 #include "qsa_internal.cuh"
@@ -756,6 +764,94 @@ __device__ void gather_chunk_fp8kv(const StepArgs &a, unsigned char *dst, int j_
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// Per-token bookkeeping of the row cache for the two chunks in flight, in the score-key area
+// (dead during attention): source rows, and the slot and claim of a token that may fill.
+struct RcChunk {
+    const uint16_t *k_src[kAttnTok], *v_src[kAttnTok];
+    int64_t slot[kAttnTok];                  // -1: nothing to fill
+    unsigned long long claim[kAttnTok];
+    int64_t flat[kAttnTok];
+};
+
+// The bf16 chunk with the row cache: one thread per token decides hit or miss (marking the
+// slot, or claiming it), then the granules are copied from the cache or from host memory.
+__device__ void gather_chunk_rc(const StepArgs &a, uint16_t *dst, RcChunk *rc, int j_base, int n, int n_list,
+                                bool dense, const int32_t *sel, int64_t nb, int64_t base, int p, int row,
+                                int row_elems, int64_t slot_lo, int64_t slot_n) {
+    const int tok_elems = 2 * row_elems;
+    const int gran_per_tok = tok_elems * 2 / 16;
+    for (int i = threadIdx.x; i < n; i += kStepThreads) {
+        const int j = j_base + i;
+        int64_t tk;
+        bool cacheable = false;
+        if (j < kRatio * n_list) {
+            const int64_t blk = dense ? (j >> 2) : sel[j >> 2];
+            if (blk < 0 || blk >= nb) {
+                record_error(a.hdr, QSA_ERR_DEVICE_BOUNDS, kWhereStep, row);
+                tk = p;
+            } else {
+                tk = kRatio * blk + (j & 3);
+                cacheable = true;
+            }
+        } else {
+            tk = kRatio * nb + (j - kRatio * n_list);
+        }
+        const int64_t flat = base + tk;
+        const uint16_t *k_src = a.k_cache + flat * row_elems, *v_src = a.v_cache + flat * row_elems;
+        int64_t fill = -1;
+        unsigned long long claim = 0ull;
+        if (cacheable) {
+            const int64_t slot = slot_lo + tk % slot_n;
+            if (__ldcg(a.rc_tag + slot) == flat) {            // hit: read the cached row
+                a.rc_hit[slot] = a.rc_epoch;
+                k_src = a.rc_rows + slot * tok_elems;
+                v_src = k_src + row_elems;
+            } else {                                          // miss: claim the slot
+                claim = ((unsigned long long)a.rc_epoch << 32) | (uint32_t)flat;
+                atomicMax(a.rc_claim + slot, claim);
+                fill = slot;
+            }
+        }
+        rc->k_src[i] = k_src;
+        rc->v_src[i] = v_src;
+        rc->slot[i] = fill;
+        rc->claim[i] = claim;
+        rc->flat[i] = flat;
+    }
+    __syncthreads();
+    for (int gidx = threadIdx.x; gidx < n * gran_per_tok; gidx += kStepThreads) {
+        const int i = gidx / gran_per_tok;
+        const int rem = gidx - i * gran_per_tok;
+        const int is_v = rem >= gran_per_tok / 2;
+        const int gpos = rem - is_v * (gran_per_tok / 2);
+        cp_async16(smem_u32(dst + (size_t)i * tok_elems + is_v * row_elems + gpos * 8),
+                   (is_v ? rc->v_src[i] : rc->k_src[i]) + gpos * 8);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// After the row's last cache read: the claims this CTA won (and whose slot no token hit in this
+// step) write a chunk's rows, still in shared memory, and their tags.
+__device__ void fill_rc(const StepArgs &a, const uint16_t *rows, const RcChunk *rc, int n, int row_elems,
+                        int *s_ok) {
+    const int tok_elems = 2 * row_elems;
+    const int gran_per_tok = tok_elems * 2 / 16;
+    for (int i = threadIdx.x; i < n; i += kStepThreads) {
+        const int64_t slot = rc->slot[i];
+        s_ok[i] = slot >= 0 && __ldcg(a.rc_claim + slot) == rc->claim[i] && __ldcg(a.rc_hit + slot) != a.rc_epoch;
+    }
+    __syncthreads();
+    for (int gidx = threadIdx.x; gidx < n * gran_per_tok; gidx += kStepThreads) {
+        const int i = gidx / gran_per_tok;
+        if (!s_ok[i]) continue;
+        const int rem = gidx - i * gran_per_tok;
+        *reinterpret_cast<uint4 *>(a.rc_rows + rc->slot[i] * tok_elems + rem * 8) =
+            *reinterpret_cast<const uint4 *>(rows + (size_t)i * tok_elems + rem * 8);
+    }
+    for (int i = threadIdx.x; i < n; i += kStepThreads)
+        if (s_ok[i]) a.rc_tag[rc->slot[i]] = rc->flat[i];
+}
+
 // One chunk of either format into ring half `half` (64 KiB).
 template <bool KV8>
 __device__ __forceinline__ void gather_chunk(const StepArgs &a, unsigned char *ring, int j_base, int n, int n_list,
@@ -780,7 +876,7 @@ __device__ __forceinline__ void prefetch_next_read(const StepArgs &a) {
         bulk_prefetch_l2(a.next_read + u * 16, (uint32_t)(min(kPiece, u1 - u) * 16));
 }
 
-template <int G, bool F8, bool KV8>
+template <int G, bool F8, bool KV8, bool RC = false>
 __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a) {
     constexpr int kRows = F8 ? kChunkRows8 : kChunkRows;      // key rows per ring stage
     constexpr int kRowBytes = F8 ? kIdxDim : kIdxDim * 2;
@@ -1401,9 +1497,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     const int n_att_chunks = (n_tok + kAttnTok - 1) / kAttnTok;
     asm volatile("cp.async.wait_group 0;" ::: "memory");            // the prefetched query
     __syncthreads();                                                   // ring, keys, hist are free
-    for (int c = 0; c < n_att_chunks && c < 2; ++c)
-        gather_chunk<KV8>(a, kv_ring + (size_t)(c & 1) * (kRingBytes / 2), t_lo + c * kAttnTok,
-                          min(kAttnTok, n_tok - c * kAttnTok), n_list, dense, s_sel, nb, base, p, row);
+    RcChunk *const rcc = reinterpret_cast<RcChunk *>(smem + kKeysOff);   // RC: [2], chunks in flight
+    const int64_t rc_lo = RC ? (int64_t)row * a.rc_slots / a.B : 0;
+    const int64_t rc_n = RC ? (int64_t)(row + 1) * a.rc_slots / a.B - rc_lo : 1;
+    auto gather = [&](int c) {
+        const int n = min(kAttnTok, n_tok - c * kAttnTok);
+        if constexpr (RC)
+            gather_chunk_rc(a, reinterpret_cast<uint16_t *>(kv_ring + (size_t)(c & 1) * (kRingBytes / 2)), rcc + (c & 1),
+                            t_lo + c * kAttnTok, n, n_list, dense, s_sel, nb, base, p, row, Hkv * kHeadDim, rc_lo,
+                            rc_n);
+        else
+            gather_chunk<KV8>(a, kv_ring + (size_t)(c & 1) * (kRingBytes / 2), t_lo + c * kAttnTok, n, n_list, dense,
+                              s_sel, nb, base, p, row);
+    };
+    for (int c = 0; c < n_att_chunks && c < 2; ++c) gather(c);
     if (tid < Hq) {
         s_m[tid] = -INFINITY;
         s_l[tid] = 0.f;
@@ -1508,9 +1615,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         }
         __syncthreads();
         if (c == 0) STEP_TRACE(12);
-        if (c + 2 < n_att_chunks)
-            gather_chunk<KV8>(a, kv_ring + (size_t)(c & 1) * (kRingBytes / 2), t_lo + (c + 2) * kAttnTok,
-                              min(kAttnTok, n_tok - (c + 2) * kAttnTok), n_list, dense, s_sel, nb, base, p, row);
+        if (c + 2 < n_att_chunks) gather(c + 2);
     }
     // partial of this CTA. The row's region holds (m, l) per CTA, [cr][2 Hq], then the acc
     // values in blocks of 32 outputs, [Hq x 256 / 32][cr][32]: a warp writes one 128-byte
@@ -1534,6 +1639,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
     if (bar_sync_fast(rs, g0, bar_k, cr, true, a.hdr, row, &s_flag) < 0) return;
     ++bar_k;
     __syncthreads();
+    if constexpr (RC) {                              // no CTA of the row reads the cache any more
+        // the last two chunks are still in the ring's two halves
+        for (int cl = max(n_att_chunks - 2, 0); cl < n_att_chunks; ++cl) {
+            fill_rc(a, reinterpret_cast<const uint16_t *>(kv_ring + (size_t)(cl & 1) * (kRingBytes / 2)), rcc + (cl & 1),
+                    min(kAttnTok, n_tok - cl * kAttnTok), Hkv * kHeadDim, reinterpret_cast<int *>(smem + kHistOff));
+            __syncthreads();
+        }
+    }
     STEP_TRACE(8);
     // the next launch on the stream may be scheduled now (it waits for this one to finish)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1625,12 +1738,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
 // Each translation unit that includes this header instantiates the kernels of one K/V format.
 
 // Co-resident CTAs of decode_step_kernel<G, F8, KV8> on device `dev` (cached; 0 on error).
-template <int G, bool F8, bool KV8>
+template <int G, bool F8, bool KV8, bool RC = false>
 int step_ctas_g(int dev) {
     static int cache[64];   // per device, 0 = unknown
     int &slot = cache[dev];
     if (slot == 0) {
-        auto kern = decode_step_kernel<G, F8, KV8>;
+        auto kern = decode_step_kernel<G, F8, KV8, RC>;
         const int smem = (int)step_smem<F8>();
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
         int sms = 0, per_sm = 0;
@@ -1645,7 +1758,7 @@ int step_ctas_g(int dev) {
 
 // Cooperative launch (every CTA co-resident: the row barriers need it) as a programmatic
 // dependent of the previous kernel on the stream.
-template <int G, bool F8, bool KV8>
+template <int G, bool F8, bool KV8, bool RC = false>
 cudaError_t launch_step_g(const StepArgs &a, int ctas, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
@@ -1659,37 +1772,40 @@ cudaError_t launch_step_g(const StepArgs &a, int ctas, cudaStream_t st) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_step_kernel<G, F8, KV8>, a);
+    return cudaLaunchKernelEx(&cfg, decode_step_kernel<G, F8, KV8, RC>, a);
 }
 
-template <bool F8, bool KV8>
+template <bool F8, bool KV8, bool RC = false>
 int step_grid_for(int G, int dev) {
     switch (G) {
-        case 1: return step_ctas_g<1, F8, KV8>(dev);
-        case 2: return step_ctas_g<2, F8, KV8>(dev);
-        case 4: return step_ctas_g<4, F8, KV8>(dev);
-        case 8: return step_ctas_g<8, F8, KV8>(dev);
-        case 16: return step_ctas_g<16, F8, KV8>(dev);
+        case 1: return step_ctas_g<1, F8, KV8, RC>(dev);
+        case 2: return step_ctas_g<2, F8, KV8, RC>(dev);
+        case 4: return step_ctas_g<4, F8, KV8, RC>(dev);
+        case 8: return step_ctas_g<8, F8, KV8, RC>(dev);
+        case 16: return step_ctas_g<16, F8, KV8, RC>(dev);
         default: return 0;
     }
 }
 
-template <bool F8, bool KV8>
+template <bool F8, bool KV8, bool RC = false>
 cudaError_t step_launch_for(const StepArgs &a, int G, int ctas, cudaStream_t st) {
     switch (G) {
-        case 1: return launch_step_g<1, F8, KV8>(a, ctas, st);
-        case 2: return launch_step_g<2, F8, KV8>(a, ctas, st);
-        case 4: return launch_step_g<4, F8, KV8>(a, ctas, st);
-        case 8: return launch_step_g<8, F8, KV8>(a, ctas, st);
-        case 16: return launch_step_g<16, F8, KV8>(a, ctas, st);
+        case 1: return launch_step_g<1, F8, KV8, RC>(a, ctas, st);
+        case 2: return launch_step_g<2, F8, KV8, RC>(a, ctas, st);
+        case 4: return launch_step_g<4, F8, KV8, RC>(a, ctas, st);
+        case 8: return launch_step_g<8, F8, KV8, RC>(a, ctas, st);
+        case 16: return launch_step_g<16, F8, KV8, RC>(a, ctas, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-// Grid size and launch of the FP8-K/V kernels (decode_step_kv8.cu).
+// Grid size and launch of the FP8-K/V kernels (decode_step_kv8.cu) and of the row-cache kernels
+// (bf16 keys and K/V, decode_step_rc.cu).
 int step_grid_kv8(int G, bool fp8_keys, int dev);
 cudaError_t step_launch_kv8(const StepArgs &a, int G, bool fp8_keys, int ctas, cudaStream_t st);
+int step_grid_rc(int G, int dev);
+cudaError_t step_launch_rc(const StepArgs &a, int G, int ctas, cudaStream_t st);
 
 }  // namespace qsa

@@ -402,12 +402,21 @@ struct StepKv {
     bool fp8() const { return is_fp8; }
 };
 
+// The VRAM row cache of qsa_decode_step_rowcache (cache == nullptr: none).
+struct StepRc {
+    void *cache = nullptr;
+    size_t bytes = 0;
+    int64_t slots = 0;
+    uint32_t epoch = 0;
+};
+
 qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
                               uint8_t *codes, float *scales, int64_t n_pooled_total, const int32_t *blk_off,
                               const qsa_bf16 *q_idx, const qsa_bf16 *q, const StepKv &kv, int64_t n_tokens_total,
                               const int32_t *tok_off, const int32_t *ctx_len, int32_t B, int64_t max_blocks,
                               int32_t *blocks, int32_t *count, qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
-                              qsa_stream stream, const void *next_read = nullptr, size_t next_read_bytes = 0) {
+                              qsa_stream stream, const void *next_read = nullptr, size_t next_read_bytes = 0,
+                              const StepRc &rc = StepRc()) {
     const bool fp8 = pooled == nullptr;
     const bool kv8 = kv.fp8();
     QSA_TRY(check_config(cfg));
@@ -433,12 +442,23 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
     QSA_NEED(device_accessible(raw_idx_k) && device_accessible(k_rows) && device_accessible(v_rows) &&
                  (!kv8 || (device_accessible(kv.k_scales) && device_accessible(kv.v_scales))),
              "raw_idx_k and the K/V rows (and their scales) must be device memory or mapped pinned host memory");
+    const bool use_rc = rc.cache != nullptr;
+    if (use_rc) {
+        QSA_NEED(aligned(rc.cache, 16), "the row cache must be 16-byte aligned");
+        QSA_NEED(rc.slots >= B && rc.slots <= ((int64_t)1 << 31), "n_slots = %lld must be in [B, 2^31]",
+                 (long long)rc.slots);
+        QSA_NEED(rc.epoch >= 1, "epoch must be at least 1");
+        const RowCacheLayout L = row_cache_layout(cfg->n_kv_heads, rc.slots);
+        if (rc.bytes < L.total)
+            return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "row cache %zu bytes < %zu needed", rc.bytes, L.total);
+        QSA_NEED(device_accessible(rc.cache), "the row cache must be device memory");
+    }
     if (next_read != nullptr && next_read_bytes >= 16) {
         QSA_NEED(aligned(next_read, 16), "next_read must be 16-byte aligned");
         QSA_NEED(device_accessible(next_read), "next_read must be device memory or mapped pinned host memory");
     }
     const int G = cfg->n_q_heads / cfg->n_kv_heads;
-    const int ctas = decode_step_grid(G, fp8, kv8);
+    const int ctas = decode_step_grid(G, fp8, kv8, use_rc);
     if (ctas == 0) return fail(QSA_ERR_CUDA, "%s: cannot size the cooperative grid on this device", name);
     if (B > ctas) return fail(QSA_ERR_UNSUPPORTED, "%s: B = %d exceeds %d co-resident CTAs", name, B, ctas);
     // every CTA keeps at most decode_step_max_keys() scores on chip; bound the worst row
@@ -474,6 +494,16 @@ qsa_status decode_step_common(const char *name, const qsa_config *cfg, const qsa
     a.n_q_heads = cfg->n_q_heads;
     a.n_kv_heads = cfg->n_kv_heads;
     a.scale_log2 = scale_of(cfg) * kLog2e;
+    if (use_rc) {
+        const RowCacheLayout L = row_cache_layout(cfg->n_kv_heads, rc.slots);
+        char *c = static_cast<char *>(rc.cache);
+        a.rc_rows = reinterpret_cast<uint16_t *>(c + L.rows);
+        a.rc_tag = reinterpret_cast<int64_t *>(c + L.tag);
+        a.rc_hit = reinterpret_cast<uint32_t *>(c + L.hit);
+        a.rc_claim = reinterpret_cast<unsigned long long *>(c + L.claim);
+        a.rc_slots = rc.slots;
+        a.rc_epoch = rc.epoch;
+    }
     a.next_read = next_read_bytes >= 16 ? static_cast<const unsigned char *>(next_read) : nullptr;
     a.next_read_bytes = a.next_read ? (int64_t)(next_read_bytes & ~(size_t)15) : 0;
     const cudaError_t e = launch_decode_step(a, ws, static_cast<cudaStream_t>(stream));
@@ -566,6 +596,45 @@ QSA_API qsa_status qsa_decode_step_fp8kv(const qsa_config *cfg, const qsa_bf16 *
     return decode_step_common("qsa_decode_step_fp8kv", cfg, raw_idx_k, pooled, pooled ? nullptr : codes,
                               pooled ? nullptr : scales, n_pooled_total, blk_off, q_idx, q, kv, n_tokens_total,
                               tok_off, ctx_len, B, max_blocks, blocks, count, out, lse, ws, ws_bytes, stream);
+}
+
+QSA_API size_t qsa_rowcache_bytes(const qsa_config *cfg, int64_t n_slots) {
+    if (check_config(cfg) != QSA_OK || cfg->n_kv_heads > 2 || n_slots < 1 || n_slots > ((int64_t)1 << 31)) return 0;
+    return row_cache_layout(cfg->n_kv_heads, n_slots).total;
+}
+
+QSA_API qsa_status qsa_rowcache_init(const qsa_config *cfg, void *cache, size_t cache_bytes, int64_t n_slots,
+                                     qsa_stream stream) {
+    const size_t need = qsa_rowcache_bytes(cfg, n_slots);
+    QSA_NEED(need > 0, "bad configuration or n_slots = %lld", (long long)n_slots);
+    QSA_NEED(cache != nullptr && aligned(cache, 16), "the row cache must be non-NULL and 16-byte aligned");
+    if (cache_bytes < need) return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "row cache %zu bytes < %zu needed", cache_bytes, need);
+    const RowCacheLayout L = row_cache_layout(cfg->n_kv_heads, n_slots);
+    char *c = static_cast<char *>(cache);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(c + L.tag, 0xFF, L.hit - L.tag, st);        // every tag -1: empty
+    if (e == cudaSuccess) e = cudaMemsetAsync(c + L.hit, 0, L.total - L.hit, st);  // marks and claims 0
+    if (e != cudaSuccess) return cuda_fail(e, "rowcache_init");
+    return ok();
+}
+
+QSA_API qsa_status qsa_decode_step_rowcache(const qsa_config *cfg, const qsa_bf16 *raw_idx_k, qsa_bf16 *pooled,
+                                            int64_t n_pooled_total, const int32_t *blk_off, const qsa_bf16 *q_idx,
+                                            const qsa_bf16 *q, const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                            int64_t n_tokens_total, const int32_t *tok_off, const int32_t *ctx_len,
+                                            int32_t B, int64_t max_blocks, int32_t *blocks, int32_t *count,
+                                            qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *cache,
+                                            size_t cache_bytes, int64_t n_slots, uint32_t epoch, qsa_stream stream) {
+    if (B > 0 && (pooled == nullptr || cache == nullptr))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "pooled and the row cache must be non-NULL");
+    StepRc rc;
+    rc.cache = cache;
+    rc.bytes = cache_bytes;
+    rc.slots = n_slots;
+    rc.epoch = epoch;
+    return decode_step_common("qsa_decode_step_rowcache", cfg, raw_idx_k, pooled, nullptr, nullptr, n_pooled_total,
+                              blk_off, q_idx, q, bf16_kv(k_cache, v_cache), n_tokens_total, tok_off, ctx_len, B,
+                              max_blocks, blocks, count, out, lse, ws, ws_bytes, stream, nullptr, 0, rc);
 }
 
 QSA_API qsa_status qsa_quantize_kv_fp8(const qsa_bf16 *x, int64_t n_rows, uint8_t *codes, float *scales,

@@ -304,6 +304,13 @@ struct StepArgs {
     float scale_log2;
     const unsigned char *next_read;   // optional L2 prefetch hint (16-byte aligned) or nullptr
     int64_t next_read_bytes;
+    // VRAM row cache (nullptr: none): rows [rc_slots][2][Hkv][256] bf16, tags, hit marks, claims
+    uint16_t *rc_rows;
+    int64_t *rc_tag;
+    uint32_t *rc_hit;
+    unsigned long long *rc_claim;
+    int64_t rc_slots;
+    uint32_t rc_epoch;
     // workspace views (set by launch_decode_step)
     WsHeader *hdr;
     void *rows;
@@ -320,8 +327,13 @@ StepLayout step_layout(int B, int64_t max_blocks, int Hq);
 size_t decode_step_ws_bytes(int B, int64_t max_blocks, int Hq);
 int decode_step_max_keys();
 // Number of CTAs the cooperative step kernel runs with on the current device (0 on error),
-// for FP8 or bf16 indexer keys and FP8 or bf16 K/V rows.
-int decode_step_grid(int G, bool fp8_keys, bool fp8_kv);
+// for FP8 or bf16 indexer keys, FP8 or bf16 K/V rows, with or without the row cache.
+int decode_step_grid(int G, bool fp8_keys, bool fp8_kv, bool row_cache = false);
+// Bytes of a row cache of n_slots token rows for n_kv_heads, and its parts' offsets.
+struct RowCacheLayout {
+    size_t rows, tag, hit, claim, total;
+};
+RowCacheLayout row_cache_layout(int n_kv_heads, int64_t n_slots);
 cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st);
 
 // FP8 K/V rows: x [n_rows][256] bf16 -> codes [n_rows][256] E4M3, scales [n_rows][2] fp32.

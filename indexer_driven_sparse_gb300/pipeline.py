@@ -80,6 +80,13 @@ class DecodeBatch:
                                  self.tok_off, self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse,
                                  self.step_ws, stream)
 
+    def fused_step_rowcache(self, raw_idx_k, pooled, q_idx, q, k_cache, v_cache, cache, n_slots, epoch, stream=None):
+        """qsa_decode_step with the VRAM row cache `cache` (binding.rowcache_new) in front of
+        K/V in host memory; `epoch` grows by at least one per call with the same cache."""
+        qb.qsa_decode_step_rowcache(self.cfg, raw_idx_k, pooled, self.blk_off, q_idx, q, k_cache, v_cache,
+                                    self.tok_off, self.ctx_len, self.ld, self.blocks, self.count, self.out, self.lse,
+                                    self.step_ws, cache, n_slots, epoch, stream)
+
     def fused_status(self, stream=None):
         return qb.qsa_read_device_status(self.step_ws, stream)
 

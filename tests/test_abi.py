@@ -254,6 +254,32 @@ def test_fp8_kv_calls_host_checks(lib):
                                      need, 0) == qb.QSA_ERR_UNSUPPORTED
 
 
+def test_rowcache_host_checks(lib):
+    # one slot: the token's K and V rows of every KV head, an int64 tag, a uint32 hit epoch
+    # (the array rounded up to 8 bytes) and a uint64 claim
+    c = cfg()
+    assert lib.qsa_rowcache_bytes(C.byref(c), 1000) == 1000 * (2 * 2 * 512 + 8) + 4000 + 1000 * 8
+    assert lib.qsa_rowcache_bytes(C.byref(c), 3) == 3 * (2048 + 8) + 16 + 24
+    assert lib.qsa_rowcache_bytes(C.byref(cfg(n_q_heads=8, n_kv_heads=1)), 4) == 4 * (1024 + 8) + 16 + 32
+    assert lib.qsa_rowcache_bytes(C.byref(c), 0) == 0
+    assert lib.qsa_rowcache_bytes(C.byref(cfg(n_kv_heads=4)), 10) == 0
+    assert lib.qsa_rowcache_bytes(C.byref(cfg(head_dim=128)), 10) == 0
+    need = lib.qsa_rowcache_bytes(C.byref(c), 64)
+    assert lib.qsa_rowcache_init(C.byref(c), 0, need, 64, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_rowcache_init(C.byref(c), FAKE + 8, need, 64, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_rowcache_init(C.byref(c), FAKE, need - 1, 64, 0) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.qsa_rowcache_init(C.byref(c), FAKE, need, 0, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    # the fused step with the cache: an empty batch is a no-op; a NULL cache is refused
+    ws_need = lib.qsa_workspace_size(qb.OP_DECODE_STEP, C.byref(c), 1, 1000)
+
+    def step(cache, n_slots, epoch, B=1):
+        return lib.qsa_decode_step_rowcache(C.byref(c), FAKE, FAKE, 1000, FAKE, FAKE, FAKE, FAKE, FAKE, 4001, FAKE,
+                                            FAKE, B, 1000, FAKE, FAKE, FAKE, 0, FAKE, ws_need, cache, need, n_slots,
+                                            epoch, 0)
+    assert step(0, 64, 1, B=0) == qb.QSA_OK
+    assert step(0, 64, 1) == qb.QSA_ERR_INVALID_ARGUMENT
+
+
 def test_sparse_mla_host_checks(lib):
     need = lib.qsa_sparse_mla_workspace_size(64, 4, 2048)
     # status block + the partials: up to 256 persistent CTAs + one per query of 64 heads x 512
