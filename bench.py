@@ -753,7 +753,7 @@ def mla_bench(steps, warmup, pk, batch=64):
     ach = flops / t / 1e12
     # DRAM bytes of the tile kernel from its capture on 16 queries, scaled by the query count
     # (each query's tiles read and write the same amounts)
-    cap = recorded_traffic("mla_tile")
+    cap = recorded_traffic("mla_tr")
     traffic = cap * batch / 16 if cap is not None else None
     # 191 FLOP/B is below GB300's ridge (measured bf16 / measured HBM, about 283 FLOP/B), so
     # the binding roofline is HBM; the tensor fraction is reported beside it
@@ -764,7 +764,7 @@ def mla_bench(steps, warmup, pk, batch=64):
             "algorithmic_gflop": flops / 1e9, "algorithmic_mb": nbytes / 1e6, "hbm_gbs": gbs,
             "intensity_flop_per_byte": flops / nbytes, "ridge_flop_per_byte": pk["bf16"] * 1e12 / (pk["hbm"] * 1e9),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm"], "traffic": traffic, "kernel": "mla_tile + mla_merge"},
+                         "frac": gbs / pk["hbm"], "traffic": traffic, "kernel": "mla_tr + mla_merge_tr"},
             "tensor_frac": ach / pk["bf16"], "tensor_tflops": ach,
             "gpu_launches_per_call": 2}
 
@@ -821,10 +821,25 @@ def prefill_bench(steps, warmup, pk):
         g1 = capture(fn, stream)
         phases[name] = time_graph(g1, stream, n, max(1, warmup), 1) / n * 1e3
         del g1
+    # the same attention with K/V in pinned host memory: gathered over the link, or staged into
+    # a device arena first (one bulk copy of the rows per call)
+    hk, hv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.k_cache, L.v_cache))
+    hk.copy_(L.k_cache)
+    hv.copy_(L.v_cache)
+    stage = torch.empty(2 * hk.numel() * 2, dtype=torch.uint8, device="cuda")
+    host = {}
+    for name, fn in (("zero_copy_ms", lambda: c.attend(L.q, hk, hv)),
+                     ("staged_ms", lambda: c.attend_staged(L.q, hk, hv, stage))):
+        g1 = capture(fn, stream)
+        host[name] = time_graph(g1, stream, n, max(1, warmup), 1) / n * 1e3
+        del g1
+    host["staged_bytes"] = stage.numel()
+    del hk, hv, stage
     att_flops = A.prefill_attention_flops(p0, nc)
     score_flops = A.prefill_score_flops(p0, nc)
     ach = att_flops / t_att / 1e12
     return {
+        "attention_kv_in_host_memory": host,
         "workload": f"prefill chunk: {nc} queries at p0={p0}, 16 q / 2 kv heads, intervals 8192",
         "chunk_tok_s": nc / t_chunk, "ms_per_chunk": t_chunk * 1e3,
         "attention_only_tok_s": nc / t_att, "ms_attention": t_att * 1e3,

@@ -255,6 +255,22 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
                                             qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes,
                                             qsa_stream stream);
 
+/* a6 staged, for K/V in host memory ("3090x3で 314 万コンテキスト", section "ちなみにこの欠点":
+ * the prefill copies the history over the link into a device staging arena and computes
+ * from there, so each row crosses the link once instead of once per tile that gathers it).
+ * Rows [0, p0 + Nc) of k_cache and v_cache (any memory the copy engine reaches, pinned host
+ * memory for an asynchronous copy) are copied into `stage` (K rows, then V rows:
+ * 2 (p0 + Nc) n_kv_heads head_dim x 2 bytes, device memory, 16-byte aligned), then
+ * qsa_sparse_prefill_chunk runs on the staged rows: the results are bit-identical to running
+ * it on device-resident K/V. A stage shorter than needed -> QSA_ERR_WORKSPACE_TOO_SMALL;
+ * a NULL or misaligned stage -> QSA_ERR_INVALID_ARGUMENT. Other arguments and errors as
+ * qsa_sparse_prefill_chunk. The caller keeps the stage (an arena it may reuse for every layer). */
+QSA_API qsa_status qsa_sparse_prefill_chunk_staged(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
+                                                   const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                                   const int32_t *blocks, const int32_t *count, int32_t interval_tokens,
+                                                   qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *stage,
+                                                   size_t stage_bytes, qsa_stream stream);
+
 /* a1-a5 fused — one decode layer-step for a batch of B <= 64 sequences in a single
  * cooperative launch ("なぜ", "VRAM に残す必要があるもの", "カーネルを書き換えずに済む";
  * LSE merge from "GLM-5.3 最適化 第2部" section DCP). For sequence s with p = ctx_len[s],

@@ -60,6 +60,8 @@ _SIGNATURES = {
     "qsa_topk_blocks": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "qsa_sparse_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "qsa_sparse_prefill_chunk": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "qsa_sparse_prefill_chunk_staged": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P, _SZ,
+                                               _P]),
     "qsa_decode_step": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _P,
                                 _P, _SZ, _P]),
     "qsa_decode_step_prefetch": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P,
@@ -349,6 +351,19 @@ def qsa_sparse_prefill_chunk(cfg, q, p0, k_cache, v_cache, blocks, count, interv
                                            _ptr(blocks, torch.int32), _ptr(count, torch.int32), int(interval_tokens),
                                            _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
                                            *_ws_args(ws), _stream(stream)), "qsa_sparse_prefill_chunk")
+
+
+def qsa_sparse_prefill_chunk_staged(cfg, q, p0, k_cache, v_cache, blocks, count, interval_tokens, out, lse, ws,
+                                    stage, stream=None):
+    """qsa_sparse_prefill_chunk with K/V (e.g. in pinned host memory) first copied into `stage`
+    (a device uint8 tensor of at least 2 x rows x n_kv_heads x head_dim x 2 bytes)."""
+    _check(load().qsa_sparse_prefill_chunk_staged(C.byref(cfg), _ptr(q, torch.bfloat16, "q"), int(p0), q.shape[0],
+                                                  _ptr(k_cache, torch.bfloat16, "k"), _ptr(v_cache, torch.bfloat16, "v"),
+                                                  _ptr(blocks, torch.int32), _ptr(count, torch.int32),
+                                                  int(interval_tokens), _ptr(out, torch.bfloat16, "out"),
+                                                  _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _ptr(stage),
+                                                  stage.numel() * stage.element_size(), _stream(stream)),
+           "qsa_sparse_prefill_chunk_staged")
 
 
 def sparse_mla_workspace(n_heads: int, B: int, max_rows: int, device="cuda", stream=None):

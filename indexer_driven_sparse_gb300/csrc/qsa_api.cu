@@ -598,6 +598,32 @@ QSA_API qsa_status qsa_decode_step_fp8kv(const qsa_config *cfg, const qsa_bf16 *
                               tok_off, ctx_len, B, max_blocks, blocks, count, out, lse, ws, ws_bytes, stream);
 }
 
+QSA_API qsa_status qsa_sparse_prefill_chunk_staged(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
+                                                   const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                                   const int32_t *blocks, const int32_t *count, int32_t interval_tokens,
+                                                   qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *stage,
+                                                   size_t stage_bytes, qsa_stream stream) {
+    QSA_TRY(check_config(cfg));
+    QSA_NEED(p0 >= 0 && Nc >= 0 && (int64_t)p0 + Nc <= INT32_MAX, "p0 = %d / Nc = %d out of range", p0, Nc);
+    if (Nc == 0) return qsa_sparse_prefill_chunk(cfg, q, p0, Nc, k_cache, v_cache, blocks, count, interval_tokens,
+                                                 out, lse, ws, ws_bytes, stream);
+    const size_t rows_bytes = ((size_t)p0 + Nc) * cfg->n_kv_heads * cfg->head_dim * 2;
+    QSA_NEED(stage != nullptr && aligned(stage, 16), "the stage must be non-NULL and 16-byte aligned");
+    if (stage_bytes < 2 * rows_bytes)
+        return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "stage %zu bytes < %zu needed", stage_bytes, 2 * rows_bytes);
+    QSA_NEED(k_cache && v_cache, "NULL tensor pointer");
+    QSA_NEED(device_accessible(stage), "the stage must be device memory");
+    // the history and the chunk cross the link once, as two bulk copies, before the chunk runs
+    char *sk = static_cast<char *>(stage), *sv = sk + rows_bytes;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(sk, k_cache, rows_bytes, cudaMemcpyDefault, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sv, v_cache, rows_bytes, cudaMemcpyDefault, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill staging copy");
+    return qsa_sparse_prefill_chunk(cfg, q, p0, Nc, reinterpret_cast<const qsa_bf16 *>(sk),
+                                    reinterpret_cast<const qsa_bf16 *>(sv), blocks, count, interval_tokens, out, lse,
+                                    ws, ws_bytes, stream);
+}
+
 QSA_API size_t qsa_rowcache_bytes(const qsa_config *cfg, int64_t n_slots) {
     if (check_config(cfg) != QSA_OK || cfg->n_kv_heads > 2 || n_slots < 1 || n_slots > ((int64_t)1 << 31)) return 0;
     return row_cache_layout(cfg->n_kv_heads, n_slots).total;

@@ -200,6 +200,12 @@ class PrefillChunk:
                                     self.count if count is None else count, self.interval, self.out, self.lse,
                                     self.ws, stream)
 
+    def attend_staged(self, q, k_cache, v_cache, stage, stream=None):
+        """attend() with K/V (e.g. in pinned host memory) copied into the device arena `stage`
+        first (qsa_sparse_prefill_chunk_staged)."""
+        qb.qsa_sparse_prefill_chunk_staged(self.cfg, q, self.p0, k_cache, v_cache, self.blocks, self.count,
+                                           self.interval, self.out, self.lse, self.ws, stage, stream)
+
     def run(self, q_idx, q, k_cache, v_cache, pooled, stream=None):
         """The chunk's path after pooling: score -> top-k (fused when the chunk has a full
         query tile) -> interval-walk attention."""

@@ -280,6 +280,22 @@ def test_rowcache_host_checks(lib):
     assert step(0, 64, 1) == qb.QSA_ERR_INVALID_ARGUMENT
 
 
+def test_prefill_staged_host_checks(lib):
+    c = cfg()
+    ws_need = lib.qsa_workspace_size(qb.OP_SPARSE_PREFILL_CHUNK, C.byref(c), 40, 0)
+    rows = 1000 + 40
+    need = 2 * rows * 2 * 256 * 2
+
+    def call(stage, stage_bytes, nc=40):
+        return lib.qsa_sparse_prefill_chunk_staged(C.byref(c), FAKE, 1000, nc, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 0,
+                                                   FAKE, ws_need, stage, stage_bytes, 0)
+    assert call(0, 0, nc=0) == qb.QSA_OK                               # empty chunk
+    assert call(0, need) == qb.QSA_ERR_INVALID_ARGUMENT                # no stage
+    assert call(FAKE + 8, need) == qb.QSA_ERR_INVALID_ARGUMENT         # misaligned
+    assert call(FAKE, need - 1) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    assert b"stage" in lib.qsa_last_error()
+
+
 def test_sparse_mla_host_checks(lib):
     need = lib.qsa_sparse_mla_workspace_size(64, 4, 2048)
     # status block + the partials: up to 256 persistent CTAs + one per query of 64 heads x 512

@@ -430,6 +430,17 @@ def test_prefill_cache_in_pinned_host_memory(cuda_lib):
         c.attend(L.q, hk, hv)
         _assert_status_ok(c)
         assert torch.equal(c.out, dev_out) and torch.equal(c.lse, dev_lse)
+        # staged: the rows copied into a device arena first (one pass over the link), then the
+        # same kernel; a stage one byte short is refused
+        need = 2 * hk.numel() * 2
+        stage = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+        c.out.zero_()
+        c.attend_staged(L.q, hk, hv, stage)
+        _assert_status_ok(c)
+        assert torch.equal(c.out, dev_out) and torch.equal(c.lse, dev_lse)
+        with pytest.raises(qb.QsaError) as e:
+            c.attend_staged(L.q, hk, hv, stage[: need - 1])
+        assert e.value.status == qb.QSA_ERR_WORKSPACE_TOO_SMALL
 
 
 # ----------------------------------------------------------------------------- full-size workloads, sampled
