@@ -544,6 +544,11 @@ def rowcache_bench(b, dl, layers, host, stream, steps, n_slots=16384):
     from indexer_driven_sparse_gb300 import binding as qb
     caches = [qb.rowcache_new(b.cfg, n_slots) for _ in layers]
     epoch = [0]
+    # the first call of the row-cache kernel sizes its grid on the host: make it before timing
+    L0, h0 = layers[0], host[0]
+    b.fused_step_rowcache(h0[2], dl.pooled[0], L0.q_idx, L0.q, h0[0], h0[1], qb.rowcache_new(b.cfg, n_slots),
+                          n_slots, 1)
+    torch.cuda.synchronize()
 
     def body():
         epoch[0] += 1
