@@ -151,6 +151,15 @@ def test_fused_step_fp8kv_million_full_size(cuda_lib, fp8_keys):
     _grade(w, b, blocks_ref, kv8, keys)
 
 
+@pytest.mark.parametrize("kind", ["gaussian", "sharp"])
+def test_fused_step_fp8kv_batched_full_size(cuda_lib, kind):
+    # the batched workload (32 ragged sequences, 8 query / 2 KV heads): every row graded
+    w = I.batched_decode(n_layers=1, kind=kind)
+    b, blocks_ref, kv8, keys = _run(w)
+    w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
+    _grade(w, b, blocks_ref, kv8, keys)
+
+
 def test_fused_step_fp8kv_host_memory_rows_match(cuda_lib):
     # FP8 K/V (codes and scales) in mapped pinned host memory: the same results bit for bit
     w = I.decode_workload("fp8kv_host", [70001, 2052], 1, 16, 2, "planted_sharp", seed=77)

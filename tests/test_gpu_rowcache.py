@@ -133,3 +133,18 @@ def test_rowcache_rejects_bad_arguments(cuda_lib):
         with pytest.raises(qb.QsaError) as e:
             b.fused_step_rowcache(host[0], pooled, q_idx, q, host[1], host[2], cache, n_slots, epoch)
         assert e.value.status == code
+
+
+def test_rowcache_batched_sequences(cuda_lib):
+    # 32 ragged sequences share the cache (each its own share of the slots); two steps
+    w, b, pooled, host, q_idx, q = _setup(I.batched_ctx_lens(seed=3), seed=85, hq=8)
+    n_slots = 32 * 1024
+    cache = qb.rowcache_new(b.cfg, n_slots)
+    want = _reference(b, pooled, host, q_idx, q)
+    for epoch in (1, 2):
+        _check_equal(_cached(b, pooled, host, q_idx, q, cache, n_slots, epoch), want)
+    # a CTA caches the rows of its last two 32-token chunks (here a CTA attends several hundred
+    # tokens), and the second step hits every slot the first filled
+    _, tag, hit = _cache_view(cache, n_slots)
+    assert (hit == 2).sum() == (tag >= 0).sum() > 32 * 40
+    _check_consistent(cache, n_slots, host, w)
