@@ -474,8 +474,8 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
 // ------------------------------------------------------------------ transposed kernel, H <= 64
 // mla_tr_kernel computes each 64-row tile once for all 512 latent dims, with the roles of the
 // operands exchanged so that the 64 heads are the N dimension of every MMA:
-//   S^T(t) = K(t) Q^T        M 128 (the tile's rows; rows 64-127 read the 8 KB after each
-//                            column block and are never used), N 64 heads, K 576;
+//   S^T(t) = K(t) Q^T        M 64 (the tile's rows), N 64 heads, K 576; an M = 64 result
+//                            holds row 16 q + l in lane l < 16 of tensor-memory lane quarter q;
 //   O^T   += V(t)^T P(t)^T   per 128 latent dims: M 128 dims (V read MN-major from the same
 //                            K tile), N 64 heads, K 64 rows; P^T (bf16, one 128-byte row of 64
 //                            heads per tile row) is written to shared memory by the softmax.
@@ -485,8 +485,8 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
 //     ahead), stored as bf16 into one of two K tiles; the query's heads reloaded when it changes;
 //   - warp 8 (one thread): S^T(t) as soon as K(t) is stored, then O^T += V(t-1)^T P(t-1)^T once
 //     the softmax of the previous tile is done;
-//   - warps 0-7 (softmax group): warps 0, 1, 4, 5 hold one tile row each (warps 0/4 rows 0-31,
-//     1/5 rows 32-63) for heads 0-31 (warps 0-1) or 32-63 (4-5); per head, the tile maximum and
+//   - warps 0-7 (softmax group): lanes 0-15 of warp w hold tile row 16 (w mod 4) + lane for
+//     heads 0-31 (warps 0-3) or 32-63 (4-7); per head, the tile maximum and
 //     sum are reduced over the rows by warp reduce-scatter and shared memory, the running maximum
 //     (raised, with O rescaled, only past 2^8 growth) kept by one lane per head. All eight warps
 //     rescale O^T and write the segment's partial (each warp one lane quarter, 32 heads).
@@ -510,8 +510,8 @@ struct TrMisc {
     uint64_t kfull[2], kfree[2], sfull[2], pfull, ofull, ofree, done;
     uint32_t tmem, abort, resc, pad;
     uint32_t valid[2][2];
-    float red[2][kMlaTok];        // per-warp head maxima, then sums
-    float sum[2][kMlaTok];
+    float red[4][kMlaTok];        // per lane quarter: head maxima
+    float sum[4][kMlaTok];        // per lane quarter: head sums
     float mref[kMlaTok], alpha[kMlaTok];
     int count[kTrCount];
 };
@@ -782,7 +782,7 @@ __global__ void __launch_bounds__(kTrThreads, 1) mla_tr_kernel(MlaArgs a) {
                     for (int ks = 0; ks < kMlaDim / 16; ++ks) {
                         const uint64_t ad = tc_desc(kb + (ks >> 2) * kTrBlk + (ks & 3) * 32, 16, 1024);
                         const uint64_t bd = tc_desc(qa + (ks >> 2) * kTrBlk + (ks & 3) * 32, 16, 1024);
-                        tc_mma(tmem + kTrTmS + buf * 64, ad, bd, tr_idesc(128, kMlaTok, 0, 0), ks > 0);
+                        tc_mma(tmem + kTrTmS + buf * 64, ad, bd, tr_idesc(kMlaTok, kMlaTok, 0, 0), ks > 0);
                     }
                 } else {
                     record_error(a.hdr, QSA_ERR_DEVICE_TIMEOUT, kWhereMla, wk.b);
@@ -801,10 +801,10 @@ __global__ void __launch_bounds__(kTrThreads, 1) mla_tr_kernel(MlaArgs a) {
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax group, epilogue
-        const bool math = (warp & 2) == 0;            // warps 0, 1, 4, 5
+        // S^T is an M = 64 MMA: tile row 16 q + l sits in lane l < 16 of TMEM lane quarter q
         const int quad = warp & 3, hg = warp >> 2;    // TMEM lane quarter; head group (32 heads)
-        const int row = 32 * (warp & 1) + lane;       // math warps: the tile row (TMEM lane)
-        const bool owner = math && (warp & 1) == 0;   // lane l of warps 0 / 4 keeps head 32 hg + l
+        const int row = 16 * quad + (lane & 15);      // the tile row of lanes 0-15
+        const bool owner = quad == 0;                 // lane l of warps 0 / 4 keeps head 32 hg + l
         const int oh = 32 * hg + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(32 * quad) << 16);
         float m_run = -INFINITY, l_run = 0.f;         // owners: the head's running max and sum
@@ -814,20 +814,17 @@ __global__ void __launch_bounds__(kTrThreads, 1) mla_tr_kernel(MlaArgs a) {
             ok = tr_wait(smem_u32(&m.sfull[buf]), (t >> 1) & 1, abort) && ok;
             tc_fence_after();
             float s[32], v[32];
-            bool valid = false;
-            if (math) {
-                tmem_ld32_async(t_lane + kTrTmS + buf * 64 + 32 * hg, s);
-                tmem_wait_ld(s);
-                valid = (m.valid[buf][warp & 1] >> lane) & 1u;
+            tmem_ld32_async(t_lane + kTrTmS + buf * 64 + 32 * hg, s);
+            tmem_wait_ld(s);
+            const bool valid = lane < 16 && ((m.valid[buf][row >> 5] >> (row & 31)) & 1u);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = valid ? s[j] : -INFINITY;
-                m.red[warp & 1][oh] = tr_reduce_scatter<true>(v, lane);
-            }
+            for (int j = 0; j < 32; ++j) v[j] = valid ? s[j] : -INFINITY;
+            m.red[quad][oh] = tr_reduce_scatter<true>(v, lane);
             named_bar(kTrBarSoft, kTrSoft);
             if (owner) {
                 // the previous tile's sums, then this tile's maximum against the running one
-                if (!wk.first) l_run += m.sum[0][oh] + m.sum[1][oh];
-                const float m_t = fmaxf(m.red[0][oh], m.red[1][oh]) * a.scale_log2;
+                if (!wk.first) l_run += (m.sum[0][oh] + m.sum[1][oh]) + (m.sum[2][oh] + m.sum[3][oh]);
+                const float m_t = fmaxf(fmaxf(m.red[0][oh], m.red[1][oh]), fmaxf(m.red[2][oh], m.red[3][oh])) * a.scale_log2;
                 if (wk.first) {
                     m_run = -INFINITY;
                     l_run = 0.f;
@@ -846,7 +843,7 @@ __global__ void __launch_bounds__(kTrThreads, 1) mla_tr_kernel(MlaArgs a) {
             if (t > 0) ok = tr_wait(smem_u32(&m.ofull), (t - 1) & 1, abort) && ok;
             named_bar(kTrBarSoft, kTrSoft);
             tc_fence_after();
-            if (math) {
+            {
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
@@ -856,10 +853,13 @@ __global__ void __launch_bounds__(kTrThreads, 1) mla_tr_kernel(MlaArgs a) {
                     v[j + 1] = e1;
                     pk[j >> 1] = pack_bf16x2(e0, e1);
                 }
+                if (lane < 16) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    st_shared_v4(pt + swz(row, 4 * hg + g), make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
-                m.sum[warp & 1][oh] = tr_reduce_scatter<false>(v, lane);
+                    for (int g = 0; g < 4; ++g)
+                        st_shared_v4(pt + swz(row, 4 * hg + g),
+                                     make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+                }
+                m.sum[quad][oh] = tr_reduce_scatter<false>(v, lane);
             }
             if (m.resc) {                            // warp-uniform: every lane reads the flag
 #pragma unroll 1
@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(kTrThreads, 1) mla_tr_kernel(MlaArgs a) {
                 if (owner && oh < H) {
                     float *ml = a.part_ml + ((size_t)(c + b) * H + oh) * 2;
                     ml[0] = m_run;
-                    ml[1] = l_run + m.sum[0][oh] + m.sum[1][oh];
+                    ml[1] = l_run + ((m.sum[0][oh] + m.sum[1][oh]) + (m.sum[2][oh] + m.sum[3][oh]));
                 }
 #pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
