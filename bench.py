@@ -839,12 +839,50 @@ def prefill_bench(steps, warmup, pk):
         host[name] = time_graph(g1, stream, n, max(1, warmup), 1) / n * 1e3
         del g1
     host["staged_bytes"] = stage.numel()
-    del hk, hv, stage
+    del hk, hv
+    # the same attention over FP8 K/V rows (qsa_sparse_prefill_chunk_fp8kv: the rows dequantised
+    # into the bf16 stage by one launch, then the same kernel); the dequantiser alone (two calls,
+    # K then V) against the HBM roofline
+    kv8 = []
+    for t in (L.k_cache, L.v_cache):
+        codes = torch.empty(t.shape, dtype=torch.uint8, device="cuda")
+        scales = torch.empty(t.shape[:-1] + (2,), dtype=torch.float32, device="cuda")
+        qb.qsa_quantize_kv_fp8(t, codes, scales)
+        kv8 += [codes, scales]
+    half = L.k_cache.numel() * 2
+    kx = stage[:half].view(torch.bfloat16).view(L.k_cache.shape)
+    vx = stage[half:].view(torch.bfloat16).view(L.v_cache.shape)
+
+    def dequant():
+        qb.qsa_dequantize_kv_fp8(kv8[0], kv8[1], kx)
+        qb.qsa_dequantize_kv_fp8(kv8[2], kv8[3], vx)
+
+    fp8kv = {}
+    for name, fn in (("attention_ms", lambda: c.attend_fp8kv(L.q, kv8, stage)), ("dequant_ms", dequant)):
+        g1 = capture(fn, stream)
+        fp8kv[name] = time_graph(g1, stream, n, max(1, warmup), 1) / n * 1e3
+        del g1
+    st = c.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"prefill device status after the FP8 K/V leg {st}")
+    dq_bytes = A.kv_dequant_bytes_fp8(p0 + nc)
+    dq_gbs = dq_bytes / (fp8kv["dequant_ms"] * 1e-3) / 1e9
+    # DRAM bytes of one launch over K (its capture), twice for the K and V launches
+    dq_cap = recorded_traffic("dequantize_kv_fp8")
+    fp8kv.update({"format": "K and V rows as 256 E4M3 codes + 2 fp32 scales per token and KV head",
+                  "fp8_kv_bytes": A.kv_read_bytes_fp8(p0 + nc), "bf16_stage_bytes": stage.numel(),
+                  "dequant_roofline": {"bound": "hbm", "achieved": dq_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                                       "frac": dq_gbs / pk["hbm"], "algorithmic_bytes": dq_bytes,
+                                       "traffic": 2 * dq_cap if dq_cap is not None else None,
+                                       "kernel": "dequantize_kv_fp8 (two launches: K, V)"},
+                  "gpu_launches_per_call": 4})
+    del kv8, stage, kx, vx
     att_flops = A.prefill_attention_flops(p0, nc)
     score_flops = A.prefill_score_flops(p0, nc)
     ach = att_flops / t_att / 1e12
     return {
         "attention_kv_in_host_memory": host,
+        "attention_fp8_kv": fp8kv,
         "workload": f"prefill chunk: {nc} queries at p0={p0}, 16 q / 2 kv heads, intervals 8192",
         "chunk_tok_s": nc / t_chunk, "ms_per_chunk": t_chunk * 1e3,
         "attention_only_tok_s": nc / t_att, "ms_attention": t_att * 1e3,
@@ -934,6 +972,29 @@ def _case_mla(reps):
     return qb.qsa_read_device_status(ws)
 
 
+def _case_dequant_kv_fp8(reps):
+    """The prefill chunk's history and chunk (266,240 tokens x 2 KV heads) as FP8 K/V rows,
+    dequantised `reps` times into a bf16 stage (qsa_sparse_prefill_chunk_fp8kv's first launch;
+    about 1.1 GB on the device)."""
+    import torch
+    from indexer_driven_sparse_gb300 import binding as qb
+    from indexer_driven_sparse_gb300 import inputs as I
+    w = I.prefill_chunk(device="cuda")
+    L = w.layers[0]
+    kv8 = []
+    for t in (L.k_cache, L.v_cache):
+        codes = torch.empty(t.shape, dtype=torch.uint8, device="cuda")
+        scales = torch.empty(t.shape[:-1] + (2,), dtype=torch.float32, device="cuda")
+        qb.qsa_quantize_kv_fp8(t, codes, scales)
+        kv8 += [codes, scales]
+    del w, L
+    kx = torch.empty(kv8[0].shape, dtype=torch.bfloat16, device="cuda")
+    for _ in range(reps):
+        qb.qsa_dequantize_kv_fp8(kv8[0], kv8[1], kx)
+    torch.cuda.synchronize()
+    return (0, 0)
+
+
 def _case_prefill(reps, attention_only):
     """The prefill chunk (4096 queries over 262,144 tokens, about 1.1 GB on the device):
     pool + score + top-k once, then `reps` chunk attentions (or whole chunks)."""
@@ -960,6 +1021,7 @@ CASES = {
     "decode_fp8": lambda reps: _case_decode_fp8(reps),
     "decode_fp8kv": lambda reps: _case_decode_fp8kv(reps),
     "mla": lambda reps: _case_mla(reps),
+    "dequant_kv_fp8": lambda reps: _case_dequant_kv_fp8(reps),
     "prefill_attention": lambda reps: _case_prefill(reps, True),
     "prefill_chunk": lambda reps: _case_prefill(reps, False),
 }

@@ -271,6 +271,25 @@ QSA_API qsa_status qsa_sparse_prefill_chunk_staged(const qsa_config *cfg, const 
                                                    qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *stage,
                                                    size_t stage_bytes, qsa_stream stream);
 
+/* a6 over FP8 K/V rows (the row format of qsa_quantize_kv_fp8; "GLM-5.3 最適化 第2部", footnote 1).
+ * The prefill multiplies bf16 tiles on the tensor cores, so rows [0, p0 + Nc) of the K and V
+ * caches are first dequantised into `stage` as qsa_dequantize_kv_fp8 does (K rows, then V
+ * rows: 2 (p0 + Nc) n_kv_heads x 512 bytes of device memory, 16-byte aligned), then
+ * qsa_sparse_prefill_chunk runs on the staged rows: the results are bit-identical to running it
+ * on the dequantised bf16 caches. Each element is thus code x scale rounded once to bf16 (at
+ * most 2^-9 of its magnitude off the exact value) before the attention.
+ *   k_codes, v_codes [p0 + Nc][n_kv_heads][256] uint8, 16-byte aligned; k_scales, v_scales
+ *   [p0 + Nc][n_kv_heads][2] fp32, 8-byte aligned (device memory or mapped pinned host memory).
+ * A stage shorter than needed -> QSA_ERR_WORKSPACE_TOO_SMALL; a NULL or misaligned stage or
+ * row pointer -> QSA_ERR_INVALID_ARGUMENT. Other arguments and errors as
+ * qsa_sparse_prefill_chunk. The caller keeps the stage (an arena it may reuse for every layer). */
+QSA_API qsa_status qsa_sparse_prefill_chunk_fp8kv(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
+                                                  const uint8_t *k_codes, const float *k_scales,
+                                                  const uint8_t *v_codes, const float *v_scales,
+                                                  const int32_t *blocks, const int32_t *count, int32_t interval_tokens,
+                                                  qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *stage,
+                                                  size_t stage_bytes, qsa_stream stream);
+
 /* a1-a5 fused — one decode layer-step for a batch of B <= 64 sequences in a single
  * cooperative launch ("なぜ", "VRAM に残す必要があるもの", "カーネルを書き換えずに済む";
  * LSE merge from "GLM-5.3 最適化 第2部" section DCP). For sequence s with p = ctx_len[s],
@@ -331,6 +350,16 @@ QSA_API qsa_status qsa_decode_step_fp8(const qsa_config *cfg, const qsa_bf16 *ra
  * inputs are outside the contract. Use it to append the new token's rows to an FP8 cache. */
 QSA_API qsa_status qsa_quantize_kv_fp8(const qsa_bf16 *x, int64_t n_rows, uint8_t *codes, float *scales,
                                        qsa_stream stream);
+
+/* The inverse of qsa_quantize_kv_fp8 for computing on bf16 tiles: x[r][d] = the value
+ * code_d x scales[r][d / 128] rounded once to bf16 (nearest, ties to even; magnitudes that
+ * round past the largest bf16 become infinity; an E4M3 NaN code gives a NaN).
+ *   codes [n_rows][256] uint8, 16-byte aligned; scales [n_rows][2] fp32, 8-byte aligned;
+ *   x [n_rows][256] bf16 (written), 16-byte aligned. Device memory or mapped pinned host memory.
+ * No workspace, no device-side errors. n_rows = 0 is a no-op; n_rows < 0 or above 2^34, NULL
+ * or misaligned pointers: QSA_ERR_INVALID_ARGUMENT. */
+QSA_API qsa_status qsa_dequantize_kv_fp8(const uint8_t *codes, const float *scales, int64_t n_rows, qsa_bf16 *x,
+                                         qsa_stream stream);
 
 /* a1-a5 fused over FP8 K/V rows — qsa_decode_step (bf16 indexer keys: `pooled`) or
  * qsa_decode_step_fp8 (FP8 indexer keys: `codes`, `scales`), with the selected tokens' K and

@@ -106,6 +106,12 @@ def decode_layer_step_bytes_fp8kv(ctx_lens, n_q_heads: int, fp8_keys: bool, n_kv
     return total
 
 
+def kv_dequant_bytes_fp8(n_tokens: int, n_kv_heads: int = 2, head_dim: int = 256) -> int:
+    """HBM bytes of dequantising n_tokens tokens of FP8 K and V rows into bf16 rows: the FP8
+    rows read once (kv_read_bytes_fp8) and the bf16 rows written once."""
+    return kv_read_bytes_fp8(n_tokens, n_kv_heads, head_dim) + n_tokens * n_kv_heads * 2 * head_dim * BF16
+
+
 def prefill_attention_flops(p0: int, n_chunk: int, n_q_heads: int = 16, head_dim: int = 256) -> int:
     """QK^T + PV FLOPs over each chunk query's own selection (2 per multiply-add)."""
     return sum(attended(p0 + i) for i in range(n_chunk)) * n_q_heads * head_dim * 2 * 2

@@ -78,6 +78,9 @@ _SIGNATURES = {
     "qsa_decode_step_fp8kv": (_I32, [_CFG, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32,
                                       _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "qsa_quantize_kv_fp8": (_I32, [_P, _I64, _P, _P, _P]),
+    "qsa_dequantize_kv_fp8": (_I32, [_P, _P, _I64, _P, _P]),
+    "qsa_sparse_prefill_chunk_fp8kv": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ,
+                                              _P, _SZ, _P]),
     "qsa_rowcache_bytes": (_SZ, [_CFG, _I64]),
     "qsa_rowcache_init": (_I32, [_CFG, _P, _SZ, _I64, _P]),
     "qsa_decode_step_rowcache": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _P, _P,
@@ -291,6 +294,16 @@ def qsa_quantize_kv_fp8(x, codes, scales, stream=None):
            "qsa_quantize_kv_fp8")
 
 
+def qsa_dequantize_kv_fp8(codes, scales, x, stream=None):
+    """codes [..., 256] uint8 and scales [..., 2] fp32 -> x [..., 256] bf16 (code x scale rounded once)."""
+    if codes.shape[-1] != 256 or x.shape != codes.shape or scales.shape != codes.shape[:-1] + (2,):
+        raise ValueError("codes [..., 256], scales [..., 2], x [..., 256]")
+    n_rows = codes.numel() // 256
+    _check(load().qsa_dequantize_kv_fp8(_ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.float32, "scales"),
+                                        n_rows, _ptr(x, torch.bfloat16, "x"), _stream(stream)),
+           "qsa_dequantize_kv_fp8")
+
+
 def qsa_decode_step_fp8kv(cfg, raw_idx_k, pooled, codes, scales, blk_off, q_idx, q, k_codes, k_scales, v_codes,
                           v_scales, tok_off, ctx_len, max_blocks, blocks, count, out, lse, ws, stream=None):
     """One fused decode layer-step over FP8 K/V rows (codes [T, Hkv, 256] uint8 + scales [T, Hkv, 2]
@@ -364,6 +377,24 @@ def qsa_sparse_prefill_chunk_staged(cfg, q, p0, k_cache, v_cache, blocks, count,
                                                   _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _ptr(stage),
                                                   stage.numel() * stage.element_size(), _stream(stream)),
            "qsa_sparse_prefill_chunk_staged")
+
+
+def qsa_sparse_prefill_chunk_fp8kv(cfg, q, p0, kv8, blocks, count, interval_tokens, out, lse, ws, stage,
+                                   stream=None):
+    """qsa_sparse_prefill_chunk over FP8 K/V rows: kv8 = (k_codes, k_scales, v_codes, v_scales) as
+    qsa_quantize_kv_fp8 writes them; `stage` a device uint8 tensor of at least
+    2 x rows x n_kv_heads x 512 bytes that receives the dequantised bf16 rows."""
+    k_codes, k_scales, v_codes, v_scales = kv8
+    _check(load().qsa_sparse_prefill_chunk_fp8kv(C.byref(cfg), _ptr(q, torch.bfloat16, "q"), int(p0), q.shape[0],
+                                                 _ptr(k_codes, torch.uint8, "k_codes"),
+                                                 _ptr(k_scales, torch.float32, "k_scales"),
+                                                 _ptr(v_codes, torch.uint8, "v_codes"),
+                                                 _ptr(v_scales, torch.float32, "v_scales"),
+                                                 _ptr(blocks, torch.int32), _ptr(count, torch.int32),
+                                                 int(interval_tokens), _ptr(out, torch.bfloat16, "out"),
+                                                 _ptr(lse, torch.float32, "lse"), *_ws_args(ws), _ptr(stage),
+                                                 stage.numel() * stage.element_size(), _stream(stream)),
+           "qsa_sparse_prefill_chunk_fp8kv")
 
 
 def sparse_mla_workspace(n_heads: int, B: int, max_rows: int, device="cuda", stream=None):

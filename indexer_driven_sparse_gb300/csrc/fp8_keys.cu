@@ -14,6 +14,9 @@
 //                          footnote 1: KV rows as E4M3 codes in 128-dim groups with an fp32
 //                          scale each): every 128-dim group of a 256-dim K or V row is
 //                          quantised exactly as a pooled key above.
+//   dequantize_kv_fp8_kernel: the inverse for the tensor-core prefill, which multiplies bf16
+//                          tiles: element d of a row becomes code_d x scale[d / 128] rounded
+//                          once to bf16 (nearest, ties to even).
 #include "qsa_internal.cuh"
 #include "qsa_ptx.cuh"
 
@@ -218,6 +221,147 @@ cudaError_t launch_quantize_kv_fp8(const uint16_t *x, int64_t n_rows, uint8_t *c
     const int64_t n_groups = 2 * n_rows;                      // two 128-dim groups per 256-dim row
     const int64_t blocks = std::min<int64_t>((n_groups * 16 + 255) / 256, (int64_t)1 << 20);
     quantize_kv_fp8_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, n_groups, codes, scales);
+    return cudaGetLastError();
+}
+
+// bf16 bits of a x s rounded once (nearest, ties to even), for an E4M3 value a and an fp32 s.
+// The fp32 product is rounded, but every point where bf16 rounding changes direction (a
+// midpoint between two bf16 values) is itself an fp32 value, and rounding to fp32 is monotone:
+// the fp32 product and the exact one lie on the same side of every midpoint unless the fp32
+// product is a midpoint. So the fp32 product rounds to the right bf16 except when it is a
+// midpoint, zero, below the normal range (where a flush to zero may have lost it), infinite
+// or NaN; those take the exact product in fp64 (a 4-bit by 24-bit product fits its 53 bits).
+// Not inlined: the caller branches to it only for those rare elements, where an inlined copy
+// was if-converted and ran its fp64 arithmetic for every element.
+__device__ __noinline__ uint32_t bf16_of_product(float a, float s) {
+    const float p = a * s;
+    const uint32_t u = __float_as_uint(p), mag = u & 0x7FFFFFFFu;
+    if ((u & 0xFFFFu) != 0x8000u && mag >= 0x00800000u && mag < 0x7F800000u) return float_to_bf16_bits(p);
+    return double_to_bf16_rne((double)a * (double)s);
+}
+
+// True when a byte of w is an E4M3 NaN code (0x7F or 0xFF).
+__device__ __forceinline__ bool has_e4m3_nan(uint32_t w) {
+    const uint32_t v = (w & 0x7F7F7F7Fu) ^ 0x7F7F7F7Fu;   // a zero byte where the code is NaN
+    return ((v - 0x01010101u) & ~v & 0x80808080u) != 0u;
+}
+
+// Eight E4M3 codes (byte k = element k) -> fp32, exactly (E4M3 -> f16 -> f32).
+__device__ __forceinline__ void e4m3x8_to_f32(uint2 c, float (&a)[8]) {
+    const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            uint32_t h;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)(w[i] >> (16 * j))));
+            const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+            a[4 * i + 2 * j] = x.x;
+            a[4 * i + 2 * j + 1] = x.y;
+        }
+    }
+}
+
+// Eight codes by the exact route of bf16_of_product (see dequant8 for when). Not inlined, for
+// the same reason as bf16_of_product.
+__device__ __noinline__ uint4 dequant8_exact(uint2 c, float s) {
+    float a[8];
+    e4m3x8_to_f32(c, a);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = bf16_of_product(a[2 * i], s) | (bf16_of_product(a[2 * i + 1], s) << 16);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Eight codes (byte k = element k) times s, each rounded once to bf16. The fp32 product p is
+// converted by the packed round-to-nearest-even instruction, which is right unless p lies
+// exactly on a bf16 midpoint while the exact product does not (see bf16_of_product); the
+// residual a s - p of one fused multiply-add, exact while p is a normal number, tells the two
+// apart. Exact midpoints are common (when a group's scale has few significant bits many
+// products are exact and sit on midpoints) and are right as converted; only a granule with an
+// inexact one, a NaN code, or a scale below 2^-117 (where a nonzero product, at least 2^-9 s,
+// may be subnormal) takes the exact route.
+__device__ __forceinline__ uint4 dequant8(uint2 c, float s) {
+    float a[8];
+    e4m3x8_to_f32(c, a);
+    uint32_t o[4];
+    bool slow = has_e4m3_nan(c.x) | has_e4m3_nan(c.y) | !(fabsf(s) >= 0x1p-117f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float p0 = a[2 * i] * s, p1 = a[2 * i + 1] * s;
+        const float r0 = fmaf(a[2 * i], s, -p0), r1 = fmaf(a[2 * i + 1], s, -p1);
+        slow |= (((__float_as_uint(p0) & 0xFFFFu) == 0x8000u) & (r0 != 0.f)) |
+                (((__float_as_uint(p1) & 0xFFFFu) == 0x8000u) & (r1 != 0.f));
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    if (slow) return dequant8_exact(c, s);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// A thread takes 8 codes (an 8-byte load; 16 bytes of bf16 written, so a warp's stores cover 512
+// contiguous bytes) of kDqUnroll granules a block-width apart, all loaded before any is
+// converted; a 128-dim group is 16 granules sharing one scale. The grid is one wave of
+// resident CTAs striding over the rows. blockIdx.y selects K (0) or V (1).
+constexpr int kDqUnroll = 4, kDqThreads = 256;
+struct DequantKvArgs {
+    const uint8_t *codes[2];
+    const float *scales[2];
+    uint16_t *out[2];
+    int64_t n_gran;                                  // 8-code granules per tensor
+};
+
+__global__ void __launch_bounds__(kDqThreads) dequantize_kv_fp8_kernel(DequantKvArgs a) {
+    const bool v = blockIdx.y != 0;                  // selects, not indexes, the parameters
+    const uint8_t *__restrict__ codes = v ? a.codes[1] : a.codes[0];
+    const float *__restrict__ scales = v ? a.scales[1] : a.scales[0];
+    uint16_t *__restrict__ out = v ? a.out[1] : a.out[0];
+    const int64_t step = (int64_t)gridDim.x * kDqThreads * kDqUnroll;
+    for (int64_t g0 = (int64_t)blockIdx.x * kDqThreads * kDqUnroll + threadIdx.x; g0 < a.n_gran; g0 += step) {
+        uint2 c[kDqUnroll];
+        float sc[kDqUnroll];
+#pragma unroll
+        for (int k = 0; k < kDqUnroll; ++k) {
+            const int64_t g = g0 + (int64_t)k * kDqThreads;
+            c[k] = g < a.n_gran ? __ldg(reinterpret_cast<const uint2 *>(codes + g * 8)) : make_uint2(0u, 0u);
+            sc[k] = g < a.n_gran ? __ldg(scales + (g >> 4)) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kDqUnroll; ++k) {
+            const int64_t g = g0 + (int64_t)k * kDqThreads;
+            if (g < a.n_gran) *reinterpret_cast<uint4 *>(out + g * 8) = dequant8(c[k], sc[k]);
+        }
+    }
+}
+
+int g_dq_resident[64];   // per device: co-resident dequantiser CTAs, 0 = unknown
+
+int dq_resident() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int &slot = g_dq_resident[dev];
+    if (slot == 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dequantize_kv_fp8_kernel, kDqThreads, 0) !=
+                cudaSuccess ||
+            per_sm < 1)
+            return 0;
+        slot = sms * per_sm;
+    }
+    return slot;
+}
+
+cudaError_t launch_dequantize_kv_fp8(const uint8_t *k_codes, const float *k_scales, uint16_t *k_out,
+                                     const uint8_t *v_codes, const float *v_scales, uint16_t *v_out, int64_t n_rows,
+                                     cudaStream_t st) {
+    DequantKvArgs a{{k_codes, v_codes}, {k_scales, v_scales}, {k_out, v_out}, n_rows * 32};
+    const int resident = dq_resident();
+    if (resident == 0) return cudaErrorInvalidConfiguration;
+    const unsigned ny = v_codes ? 2u : 1u;
+    const int64_t need = (a.n_gran + kDqThreads * kDqUnroll - 1) / (kDqThreads * kDqUnroll);
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(need, resident / ny));
+    dequantize_kv_fp8_kernel<<<dim3((unsigned)blocks, ny), kDqThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -344,10 +344,10 @@ QSA_API qsa_status qsa_sparse_decode(const qsa_config *cfg, const qsa_bf16 *q, c
     return ok();
 }
 
-QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
-                                            const qsa_bf16 *k_cache, const qsa_bf16 *v_cache, const int32_t *blocks,
-                                            const int32_t *count, int32_t interval_tokens, qsa_bf16 *out, float *lse,
-                                            void *ws, size_t ws_bytes, qsa_stream stream) {
+// The prefill's checks that do not look at the K/V pointers, shared by the staged entry points
+// so that nothing is copied or dequantised for a call that would be refused.
+static qsa_status check_prefill_args(const qsa_config *cfg, int32_t p0, int32_t Nc, int32_t interval_tokens,
+                                     void *ws, size_t ws_bytes) {
     QSA_TRY(check_config(cfg));
     QSA_NEED(p0 >= 0 && Nc >= 0 && Nc <= kMaxGridYZ, "p0 = %d / Nc = %d out of range", p0, Nc);
     QSA_NEED((int64_t)p0 + Nc <= INT32_MAX, "p0 + Nc overflows int32");
@@ -358,6 +358,15 @@ QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf1
     if (prefill_tc_supported(cfg->n_q_heads, cfg->n_kv_heads) && ((int64_t)p0 + Nc) / kRatio + 1 > kPrefillTcMaxBlocks)
         return fail(QSA_ERR_UNSUPPORTED, "p0 + Nc = %lld exceeds the tensor-core prefill's %lld blocks",
                     (long long)p0 + Nc, (long long)kPrefillTcMaxBlocks);
+    return ok();
+}
+
+QSA_API qsa_status qsa_sparse_prefill_chunk(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
+                                            const qsa_bf16 *k_cache, const qsa_bf16 *v_cache, const int32_t *blocks,
+                                            const int32_t *count, int32_t interval_tokens, qsa_bf16 *out, float *lse,
+                                            void *ws, size_t ws_bytes, qsa_stream stream) {
+    QSA_TRY(check_prefill_args(cfg, p0, Nc, interval_tokens, ws, ws_bytes));
+    if (Nc == 0) return ok();
     QSA_NEED(q && k_cache && v_cache && blocks && count && out, "NULL tensor pointer");
     QSA_NEED(aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 16) && aligned(out, 16) && aligned(blocks, 16),
              "q, k_cache, v_cache, out and blocks must be 16-byte aligned");
@@ -603,10 +612,8 @@ QSA_API qsa_status qsa_sparse_prefill_chunk_staged(const qsa_config *cfg, const 
                                                    const int32_t *blocks, const int32_t *count, int32_t interval_tokens,
                                                    qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *stage,
                                                    size_t stage_bytes, qsa_stream stream) {
-    QSA_TRY(check_config(cfg));
-    QSA_NEED(p0 >= 0 && Nc >= 0 && (int64_t)p0 + Nc <= INT32_MAX, "p0 = %d / Nc = %d out of range", p0, Nc);
-    if (Nc == 0) return qsa_sparse_prefill_chunk(cfg, q, p0, Nc, k_cache, v_cache, blocks, count, interval_tokens,
-                                                 out, lse, ws, ws_bytes, stream);
+    QSA_TRY(check_prefill_args(cfg, p0, Nc, interval_tokens, ws, ws_bytes));
+    if (Nc == 0) return ok();
     const size_t rows_bytes = ((size_t)p0 + Nc) * cfg->n_kv_heads * cfg->head_dim * 2;
     QSA_NEED(stage != nullptr && aligned(stage, 16), "the stage must be non-NULL and 16-byte aligned");
     if (stage_bytes < 2 * rows_bytes)
@@ -675,6 +682,50 @@ QSA_API qsa_status qsa_quantize_kv_fp8(const qsa_bf16 *x, int64_t n_rows, uint8_
     const cudaError_t e = launch_quantize_kv_fp8(x, n_rows, codes, scales, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "quantize_kv_fp8 launch");
     return ok();
+}
+
+QSA_API qsa_status qsa_dequantize_kv_fp8(const uint8_t *codes, const float *scales, int64_t n_rows, qsa_bf16 *x,
+                                         qsa_stream stream) {
+    QSA_NEED(n_rows >= 0 && n_rows <= ((int64_t)1 << 34), "n_rows = %lld out of range", (long long)n_rows);
+    if (n_rows == 0) return ok();
+    QSA_NEED(x && codes && scales, "NULL tensor pointer");
+    QSA_NEED(aligned(x, 16) && aligned(codes, 16) && aligned(scales, 8), "codes and x must be 16-byte aligned, "
+             "scales 8-byte aligned");
+    QSA_NEED(device_accessible(x) && device_accessible(codes) && device_accessible(scales),
+             "codes, scales and x must be device memory or mapped pinned host memory");
+    const cudaError_t e = launch_dequantize_kv_fp8(codes, scales, x, nullptr, nullptr, nullptr, n_rows,
+                                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dequantize_kv_fp8 launch");
+    return ok();
+}
+
+QSA_API qsa_status qsa_sparse_prefill_chunk_fp8kv(const qsa_config *cfg, const qsa_bf16 *q, int32_t p0, int32_t Nc,
+                                                  const uint8_t *k_codes, const float *k_scales,
+                                                  const uint8_t *v_codes, const float *v_scales,
+                                                  const int32_t *blocks, const int32_t *count, int32_t interval_tokens,
+                                                  qsa_bf16 *out, float *lse, void *ws, size_t ws_bytes, void *stage,
+                                                  size_t stage_bytes, qsa_stream stream) {
+    QSA_TRY(check_prefill_args(cfg, p0, Nc, interval_tokens, ws, ws_bytes));
+    if (Nc == 0) return ok();
+    const int64_t n_rows = ((int64_t)p0 + Nc) * cfg->n_kv_heads;          // 256-dim rows of K (and of V)
+    const size_t rows_bytes = (size_t)n_rows * cfg->head_dim * 2;
+    QSA_NEED(stage != nullptr && aligned(stage, 16), "the stage must be non-NULL and 16-byte aligned");
+    if (stage_bytes < 2 * rows_bytes)
+        return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "stage %zu bytes < %zu needed", stage_bytes, 2 * rows_bytes);
+    QSA_NEED(k_codes && k_scales && v_codes && v_scales, "NULL tensor pointer");
+    QSA_NEED(aligned(k_codes, 16) && aligned(v_codes, 16) && aligned(k_scales, 8) && aligned(v_scales, 8),
+             "codes must be 16-byte aligned, scales 8-byte aligned");
+    QSA_NEED(device_accessible(stage), "the stage must be device memory");
+    QSA_NEED(device_accessible(k_codes) && device_accessible(k_scales) && device_accessible(v_codes) &&
+             device_accessible(v_scales), "codes and scales must be device memory or mapped pinned host memory");
+    // the history and the chunk dequantised once into the stage, then the bf16 prefill on it
+    uint16_t *sk = static_cast<uint16_t *>(stage), *sv = sk + (size_t)n_rows * cfg->head_dim;
+    const cudaError_t e = launch_dequantize_kv_fp8(k_codes, k_scales, sk, v_codes, v_scales, sv, n_rows,
+                                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dequantize_kv_fp8 launch");
+    return qsa_sparse_prefill_chunk(cfg, q, p0, Nc, reinterpret_cast<const qsa_bf16 *>(sk),
+                                    reinterpret_cast<const qsa_bf16 *>(sv), blocks, count, interval_tokens, out, lse,
+                                    ws, ws_bytes, stream);
 }
 
 QSA_API size_t qsa_sparse_mla_workspace_size(int32_t n_heads, int32_t B, int32_t max_rows) {

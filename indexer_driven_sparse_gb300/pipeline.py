@@ -206,6 +206,12 @@ class PrefillChunk:
         qb.qsa_sparse_prefill_chunk_staged(self.cfg, q, self.p0, k_cache, v_cache, self.blocks, self.count,
                                            self.interval, self.out, self.lse, self.ws, stage, stream)
 
+    def attend_fp8kv(self, q, kv8, stage, stream=None):
+        """attend() over FP8 K/V rows kv8 = (k_codes, k_scales, v_codes, v_scales), dequantised
+        into the device arena `stage` first (qsa_sparse_prefill_chunk_fp8kv)."""
+        qb.qsa_sparse_prefill_chunk_fp8kv(self.cfg, q, self.p0, kv8, self.blocks, self.count, self.interval,
+                                          self.out, self.lse, self.ws, stage, stream)
+
     def run(self, q_idx, q, k_cache, v_cache, pooled, stream=None):
         """The chunk's path after pooling: score -> top-k (fused when the chunk has a full
         query tile) -> interval-walk attention."""

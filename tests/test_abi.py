@@ -296,6 +296,37 @@ def test_prefill_staged_host_checks(lib):
     assert b"stage" in lib.qsa_last_error()
 
 
+def test_fp8_kv_prefill_and_dequantiser_host_checks(lib):
+    # the dequantiser: empty is a no-op; NULL, misaligned and out-of-range arguments are refused
+    assert lib.qsa_dequantize_kv_fp8(0, 0, 0, 0, 0) == qb.QSA_OK
+    assert lib.qsa_dequantize_kv_fp8(FAKE, FAKE, -1, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_dequantize_kv_fp8(FAKE, FAKE, (1 << 34) + 1, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_dequantize_kv_fp8(FAKE, 0, 4, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_dequantize_kv_fp8(FAKE + 8, FAKE, 4, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert b"aligned" in lib.qsa_last_error()
+    assert lib.qsa_dequantize_kv_fp8(FAKE, FAKE + 4, 4, FAKE, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert lib.qsa_dequantize_kv_fp8(FAKE, FAKE, 4, FAKE + 8, 0) == qb.QSA_ERR_INVALID_ARGUMENT
+    # the FP8 K/V prefill: the stage and the four row planes are checked before anything runs
+    c = cfg()
+    ws_need = lib.qsa_workspace_size(qb.OP_SPARSE_PREFILL_CHUNK, C.byref(c), 40, 0)
+    need = 2 * (1000 + 40) * 2 * 256 * 2
+
+    def call(stage, stage_bytes, nc=40, kc=FAKE, ks=FAKE, vc=FAKE, vs=FAKE, interval=1024, ws_bytes=ws_need):
+        return lib.qsa_sparse_prefill_chunk_fp8kv(C.byref(c), FAKE, 1000, nc, kc, ks, vc, vs, FAKE, FAKE, interval,
+                                                  FAKE, 0, FAKE, ws_bytes, stage, stage_bytes, 0)
+    assert call(0, 0, nc=0) == qb.QSA_OK                               # empty chunk
+    assert call(FAKE, need, interval=1000) == qb.QSA_ERR_INVALID_ARGUMENT       # refused before staging
+    assert b"interval" in lib.qsa_last_error()
+    assert call(FAKE, need, ws_bytes=ws_need - 1) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    assert call(0, need) == qb.QSA_ERR_INVALID_ARGUMENT                # no stage
+    assert call(FAKE + 8, need) == qb.QSA_ERR_INVALID_ARGUMENT         # misaligned stage
+    assert call(FAKE, need - 1) == qb.QSA_ERR_WORKSPACE_TOO_SMALL
+    assert b"stage" in lib.qsa_last_error()
+    assert call(FAKE, need, vs=0) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert call(FAKE, need, kc=FAKE + 8) == qb.QSA_ERR_INVALID_ARGUMENT
+    assert call(FAKE, need, ks=FAKE + 4) == qb.QSA_ERR_INVALID_ARGUMENT
+
+
 def test_sparse_mla_host_checks(lib):
     need = lib.qsa_sparse_mla_workspace_size(64, 4, 2048)
     # status block + the partials: up to 256 persistent CTAs + one per query of 64 heads x 512

@@ -93,6 +93,13 @@ def test_fp8_kv_bytes():
     assert A.decode_layer_step_bytes_fp8kv([10], 8, False) == 2 * 256 + 11 * 2 * 2 * 264 + 2 * 8 * 512 + 256
 
 
+def test_fp8_kv_dequant_bytes():
+    # one token of one head: K and V rows of 264 B read, of 512 B written
+    assert A.kv_dequant_bytes_fp8(1, 1) == 2 * (264 + 512)
+    # the prefill chunk's history and chunk (266,240 tokens, 2 KV heads)
+    assert A.kv_dequant_bytes_fp8(262144 + 4096) == 266240 * 2 * 2 * 776
+
+
 def test_glm_page_byte_figures():
     # the FP8 indexer key and the sparse-MLA row sizes against the footnotes that print them
     g = figs(GOLDEN_GLM)
