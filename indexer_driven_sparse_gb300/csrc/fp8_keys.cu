@@ -18,6 +18,7 @@
 //                          tiles: element d of a row becomes code_d x scale[d / 128] rounded
 //                          once to bf16 (nearest, ties to even).
 #include "qsa_internal.cuh"
+#include "kv_fp8.cuh"
 #include "qsa_ptx.cuh"
 
 #include <algorithm>

@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "qsa_internal.cuh"
+#include "kv_fp8.cuh"
 
 using namespace qsa;
 

@@ -339,11 +339,6 @@ cudaError_t launch_decode_step(StepArgs a, void *ws, cudaStream_t st);
 // FP8 K/V rows: x [n_rows][256] bf16 -> codes [n_rows][256] E4M3, scales [n_rows][2] fp32.
 cudaError_t launch_quantize_kv_fp8(const uint16_t *x, int64_t n_rows, uint8_t *codes, float *scales,
                                    cudaStream_t st);
-// The inverse, rounded once to bf16: K rows into k_out and, when v_codes is not NULL, V rows
-// into v_out in the same launch (n_rows 256-dim rows each).
-cudaError_t launch_dequantize_kv_fp8(const uint8_t *k_codes, const float *k_scales, uint16_t *k_out,
-                                     const uint8_t *v_codes, const float *v_scales, uint16_t *v_out, int64_t n_rows,
-                                     cudaStream_t st);
 
 // Set the calling thread's qsa_last_error() text to "<what>: <detail>" and return s.
 qsa_status host_fail(qsa_status s, const char *what, const char *detail);
