@@ -462,7 +462,7 @@ QSA_API qsa_status qsa_decode_step_fp8_prefetch(const qsa_config *cfg, const qsa
  *  - `stream` must belong to the current device (else QSA_ERR_INVALID_ARGUMENT): the
  *    array has one address per device.
  *  - The first call on a device resolves the array's device address
- *    (cudaGetSymbolAddress, with that device current); make it before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and caches it.
  *  - The array stays resident on every GPU that loads the library until exit.
  *  - Every call reuses the same array: calls that overlap on the GPU race. Each call
  *    clears the array's status block on `stream`; device-side bounds errors are not

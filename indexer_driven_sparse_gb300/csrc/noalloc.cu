@@ -10,7 +10,7 @@
 // The array is kNoAllocScratchBytes (16 MiB) and stays resident on every GPU that
 // loads the library until the process exits. The first call on a device looks up
 // the array's device address with cudaGetSymbolAddress (with that device current)
-// and caches it; make that first call before any stream capture. Calls share the
+// and caches it. Calls share the
 // array and each call overwrites it, so calls that overlap on the GPU (different
 // streams, or concurrent graphs) race; serialise them.
 #include <atomic>
