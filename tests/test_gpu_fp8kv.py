@@ -248,9 +248,10 @@ def _prefill_fp8kv(w, interval=8192, host_rows=False):
     c.run(L.q_idx, L.q, L.k_cache, L.v_cache, pooled)
     assert c.device_status()[0] == 0
     kv8 = _kv8(L)
-    want = O.quantize_kv_fp8(bits(w.layers[0].v_cache))
-    assert np.array_equal(kv8[2].cpu().numpy(), want[0])
-    assert np.array_equal(kv8[3].cpu().numpy().view(np.uint32), want[1].view(np.uint32))
+    n_chk = min(L.v_cache.shape[0], 8192)            # the quantiser against the oracle's on these rows
+    want = O.quantize_kv_fp8(bits(L.v_cache[-n_chk:]))
+    assert np.array_equal(kv8[2][-n_chk:].cpu().numpy(), want[0])
+    assert np.array_equal(kv8[3][-n_chk:].cpu().numpy().view(np.uint32), want[1].view(np.uint32))
     stage = torch.empty(2 * L.k_cache.numel() * 2, dtype=torch.uint8, device=DEV)
     c.out.zero_()
     c.attend_fp8kv(L.q, [t.cpu().pin_memory() for t in kv8] if host_rows else kv8, stage)
@@ -266,21 +267,24 @@ def _grade_prefill_fp8kv(w, c, rows):
     Lh = w.layers[0]
     qbits = bits(Lh.q)
     kb, vb = bits(Lh.k_cache), bits(Lh.v_cache)
-    kd = O.dequantize_kv_fp8(*O.quantize_kv_fp8(kb))
-    vd = O.dequantize_kv_fp8(*O.quantize_kv_fp8(vb))
-    kr, vr = O.f64_to_bf16_bits(kd), O.f64_to_bf16_bits(vd)
     blocks, count = c.blocks.cpu().numpy(), c.count.cpu().numpy()
     out, lse = c.out.cpu(), c.lse.cpu().numpy()
     qf = O.bf16_bits_to_f64(qbits)
+    # the oracle's FP8 rows of every token the graded rows attend, quantised once
+    toks = {i: O.attended_tokens(c.p0 + i, blocks[i, :count[i]]) for i in rows}
+    union = np.unique(np.concatenate([toks[i] for i in rows])) if toks else np.zeros(0, np.int64)
+    kd_u = O.dequantize_kv_fp8(*O.quantize_kv_fp8(kb[union]))
+    vd_u = O.dequantize_kv_fp8(*O.quantize_kv_fp8(vb[union]))
     stats = dict(rel=0.0, rel_exact=0.0, lse=0.0, rows=0)
     for i in rows:
-        p = c.p0 + i
-        tokens = O.attended_tokens(p, blocks[i, :count[i]])
-        ref_out, ref_lse = O.attend(qf[i], O.bf16_bits_to_f64(kr[tokens]), O.bf16_bits_to_f64(vr[tokens]),
-                                    np.arange(tokens.size), w.n_kv_heads, 1.0 / 16.0)
+        tokens = toks[i]
+        at = np.searchsorted(union, tokens)
+        kd, vd = kd_u[at], vd_u[at]
+        kr, vr = O.bf16_bits_to_f64(O.f64_to_bf16_bits(kd)), O.bf16_bits_to_f64(O.f64_to_bf16_bits(vd))
+        ref_out, ref_lse = O.attend(qf[i], kr, vr, np.arange(tokens.size), w.n_kv_heads, 1.0 / 16.0)
         stats["rel"] = max(stats["rel"], check_attention(out[i], ref_out)[2])
         stats["lse"] = max(stats["lse"], check_lse(lse[i], ref_lse))
-        ex_out, _ = O.attend(qf[i], kd[tokens], vd[tokens], np.arange(tokens.size), w.n_kv_heads, 1.0 / 16.0)
+        ex_out, _ = O.attend(qf[i], kd, vd, np.arange(tokens.size), w.n_kv_heads, 1.0 / 16.0)
         stats["rel_exact"] = max(stats["rel_exact"], check_attention(out[i], ex_out)[2])
         stats["rows"] += 1
     print(f"{w.name} fp8 kv prefill: {stats}")
@@ -293,6 +297,17 @@ def test_prefill_fp8kv_sharp_multi_tile_all_rows(cuda_lib):
     c, _, _, _ = _prefill_fp8kv(w)
     st = _grade_prefill_fp8kv(w, c, range(300))
     assert st["rows"] == 300 and st["rel"] < 8e-3
+
+
+def test_prefill_fp8kv_full_size_sampled(cuda_lib):
+    # the bench's chunk (4096 queries at p0 = 262,144, 16 / 2 heads) over FP8 K/V with Q/K/V ~
+    # N(0,1): the first and the last query of every 16-query tile (512 rows)
+    w = I.prefill_chunk(kind="planted_sharp")
+    c, _, _, _ = _prefill_fp8kv(w)
+    w.layers = [I.Layer(*(getattr(w.layers[0], f).cpu() for f in ("raw_idx_k", "q_idx", "q", "k_cache", "v_cache")))]
+    rows = sorted({r for t in range(0, 4096, 16) for r in (t, t + 15)})
+    st = _grade_prefill_fp8kv(w, c, rows)
+    assert st["rows"] == 512 and st["rel"] < 8e-3
 
 
 @pytest.mark.parametrize("hq,hkv,p0,nc", [
