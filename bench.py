@@ -429,7 +429,8 @@ def e2e_decode(dl, stream, steps, warmup):
     and the last layer's output read back, every step. The layers' q and q_idx live in
     one staging buffer (one copy for all layers); the new token's K, V and raw indexer-key
     rows are appended to caches stacked with a fixed layer stride (one strided copy each,
-    qsa_copy_rows)."""
+    qsa_copy_rows). The copies and the layer-steps are one CUDA graph, replayed and waited
+    for on the host once per step."""
     import torch
     from indexer_driven_sparse_gb300 import binding as qb
     b, layers = dl.b, dl.w.layers
@@ -469,18 +470,19 @@ def e2e_decode(dl, stream, steps, warmup):
     lse_view = b.lse.view(torch.bfloat16).view(-1)
 
     def body():
+        # the step's copies in, the 12 layer-steps, the result out: one graph per step
+        dev_q.copy_(h_q, non_blocking=True)
+        for dst, pitch, src, row in rows:
+            qb.qsa_copy_rows(dst, pitch, src, row, row, n_l, stream)
         for l in range(n_l):
             dl.layer_step(l)
+        host_out[:4096].copy_(out_view, non_blocking=True)
+        host_out[4096:].copy_(lse_view, non_blocking=True)
 
     g = capture(body, stream)
 
     def one_step():
-        dev_q.copy_(h_q, non_blocking=True)
-        for dst, pitch, src, row in rows:
-            qb.qsa_copy_rows(dst, pitch, src, row, row, n_l, stream)
         g.replay()
-        host_out[:4096].copy_(out_view, non_blocking=True)
-        host_out[4096:].copy_(lse_view, non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
