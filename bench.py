@@ -915,6 +915,42 @@ def _case_decode_step(reps):
     return b.fused_status()
 
 
+def _case_decode_trace(reps):
+    """Phase trace of the fused decode step on one million-token layer: the workspace's debug
+    word asks every CTA's thread 0 to stamp %globaltimer at 16 points of the launch; prints the
+    median over the CTAs of each stamp, in us from the earliest first stamp, for `reps` eager
+    launches (the last one's table)."""
+    import numpy as np
+    import torch
+    from indexer_driven_sparse_gb300 import inputs as I
+    from indexer_driven_sparse_gb300.pipeline import DecodeBatch
+    w = I.million_decode(n_layers=1)
+    L = w.layers[0]
+    b = DecodeBatch(16, 2, w.ctx_len)
+    pooled = b.new_pooled()
+    b.pool(L.raw_idx_k, pooled)
+    for _ in range(3):
+        b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+    torch.cuda.synchronize()
+    n_slots, max_ctas = 16, 256                       # the kernel's trace slots per CTA and CTA bound
+    ws = b.step_ws
+    tr = ws[ws.numel() - max_ctas * n_slots * 8:].view(torch.int64).view(max_ctas, n_slots)
+    table = None
+    for _ in range(reps):
+        ws.view(torch.int32)[3] = 0x7ACE              # the header's debug word: trace this launch
+        tr.zero_()
+        b.fused_step(L.raw_idx_k, pooled, L.q_idx, L.q, L.k_cache, L.v_cache)
+        torch.cuda.synchronize()
+        ws.view(torch.int32)[3] = 0
+        t = tr.cpu().numpy().astype(np.int64)
+        t = t[t[:, 0] > 0]
+        rel = np.where(t > 0, (t - t[:, 0].min()) / 1000.0, np.nan)
+        table = {f"slot{i}": [round(float(np.nanmedian(rel[:, i])), 2), round(float(np.nanmin(rel[:, i])), 2),
+                              round(float(np.nanmax(rel[:, i])), 2)] for i in range(n_slots)}
+    print(json.dumps({"decode_trace_us_median_min_max": table, "ctas": int(t.shape[0])}))
+    return b.fused_status()
+
+
 def _case_decode_fp8(reps):
     """One million-token layer with FP8 indexer keys: pool into codes + scales, then `reps`
     times the standalone FP8 scan (qsa_index_score_fp8) and the fused FP8 step."""
@@ -1022,6 +1058,7 @@ CASES = {
     "decode_step": lambda reps: _case_decode_step(reps),
     "decode_fp8": lambda reps: _case_decode_fp8(reps),
     "decode_fp8kv": lambda reps: _case_decode_fp8kv(reps),
+    "decode_trace": lambda reps: _case_decode_trace(reps),
     "mla": lambda reps: _case_mla(reps),
     "dequant_kv_fp8": lambda reps: _case_dequant_kv_fp8(reps),
     "prefill_attention": lambda reps: _case_prefill(reps, True),
