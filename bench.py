@@ -778,6 +778,28 @@ def mla_bench(steps, warmup, pk, batch=64):
 
 # ----------------------------------------------------------------------------- prefill
 
+def union_stats(c, nc, p0, att_flops):
+    """Selection structure of a prefill chunk (reporting only, from the blocks the chunk
+    selected): the mean overlap of consecutive queries' top-512 sets, and the union of the
+    selected blocks (and own blocks) per 16-query tile, which the tensor-core kernel packs
+    into 64-token chunks of 128 (query, head) rows; executed FLOPs are estimated as
+    chunks x 64 tokens x 128 rows x 256 dims x 2 (QK and PV) x 2 FLOP for each of 2 KV heads."""
+    import torch
+    blocks = c.blocks[:nc].long()
+    prev, cur = blocks[:-1].contiguous(), blocks[1:].contiguous()
+    idx = torch.searchsorted(prev, cur).clamp(max=prev.shape[1] - 1)
+    overlap = (torch.gather(prev, 1, idx) == cur).float().mean(dim=1).mean().item()
+    own = ((p0 + torch.arange(nc, device=blocks.device)) // 4).unsqueeze(1)
+    tiles = torch.cat([blocks, own], dim=1).view(nc // 16, -1)
+    srt = torch.sort(tiles, dim=1).values
+    union = 1 + (srt[:, 1:] != srt[:, :-1]).sum(dim=1)
+    chunks = torch.div(4 * union + 63, 64, rounding_mode="floor")
+    executed = float(chunks.sum().item()) * 2 * 64 * 128 * 256 * 2 * 2
+    return {"mean_consecutive_overlap": overlap, "union_blocks_per_16_query_tile": float(union.float().mean().item()),
+            "chunks_estimate": int(2 * chunks.sum().item()), "executed_gflop_estimate": executed / 1e9,
+            "executed_over_algorithmic": executed / att_flops}
+
+
 def prefill_bench(steps, warmup, pk):
     import torch
     from indexer_driven_sparse_gb300 import accounting as A
@@ -882,7 +904,28 @@ def prefill_bench(steps, warmup, pk):
     att_flops = A.prefill_attention_flops(p0, nc)
     score_flops = A.prefill_score_flops(p0, nc)
     ach = att_flops / t_att / 1e12
+    unions = {"correlated_rho_0.985": dict(union_stats(c, nc, p0, att_flops), attention_ms=t_att * 1e3)}
+    # the stress datum: independent queries (rho = 0), the worst case for union tiles
+    w0 = I.prefill_chunk(device="cuda", rho=0.0)
+    L0 = w0.layers[0]
+    c0 = PrefillChunk(16, 2, p0, nc, 8192, device="cuda")
+    pooled0 = c0.new_pooled()
+    c0.pool(L0.raw_idx_k, pooled0)
+    with torch.cuda.stream(stream):
+        c0.run(L0.q_idx, L0.q, L0.k_cache, L0.v_cache, pooled0)
+    torch.cuda.synchronize()
+    st = c0.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"prefill device status (independent queries) {st}")
+    g1 = capture(lambda: c0.attend(L0.q, L0.k_cache, L0.v_cache), stream)
+    t_att0 = time_graph(g1, stream, n, max(1, warmup), 1) / n
+    del g1
+    unions["independent_rho_0"] = dict(union_stats(c0, nc, p0, att_flops), attention_ms=t_att0 * 1e3,
+                                       attention_tflops=att_flops / t_att0 / 1e12)
+    del w0, L0, c0, pooled0
+    torch.cuda.empty_cache()
     return {
+        "selection_overlap_and_union_tiles": unions,
         "attention_kv_in_host_memory": host,
         "attention_fp8_kv": fp8kv,
         "workload": f"prefill chunk: {nc} queries at p0={p0}, 16 q / 2 kv heads, intervals 8192",
