@@ -521,11 +521,13 @@ __device__ __forceinline__ float score_of_key(uint32_t k) {
 // radix select takes over.
 __device__ unsigned long long select_kth_key64_lin(const unsigned long long *keys, uint32_t n, uint32_t need,
                                                    uint32_t *hist, int *s_d, uint32_t *s_above, uint32_t *s_wtot,
-                                                   unsigned long long *s_red, float *s_fred) {
+                                                   unsigned long long *s_red, float *s_fred,
+                                                   unsigned long long *cand, uint32_t *s_ncand) {
     constexpr int R = 8;
     constexpr int kBins = 4096;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t need0 = need;
+    if (tid == 0) *s_ncand = 0u;                  // the bin's candidates, counted below
     unsigned long long kr[R];
     float vr[R];
     float vmin = FLT_MAX, vmax = -FLT_MAX;
@@ -573,23 +575,24 @@ __device__ unsigned long long select_kth_key64_lin(const unsigned long long *key
         if (kr[r] != 0ull) atomicAdd(&hist[bin_of(vr[r])], 1u);
     __syncthreads();
     block_find_bin(hist, kBins, need, s_d, s_above, s_wtot);
+    // hist, s_d and s_above are not written again on this path, so they are read without a
+    // further barrier; every thread reads the same values and takes the same branch
     const int d = *s_d;
     const uint32_t in_bin = hist[d];
     need -= *s_above;
-    __syncthreads();
-    if (in_bin > (uint32_t)kStepThreads)
+    if (in_bin > (uint32_t)kStepThreads) {
+        __syncthreads();                            // every thread has read them: the fallback rewrites them
         return select_kth_key64_reg(keys, n, need0, hist, s_d, s_above, s_wtot, s_red);
-    // the bin's members -> the need-th largest of them by counting ranks (distinct keys)
-    unsigned long long *cand = reinterpret_cast<unsigned long long *>(hist);
-    if (tid == 0) *s_above = 0u;
-    __syncthreads();
+    }
+    // the bin's members (into `cand`, beside the keys) -> the need-th largest of them by
+    // counting ranks (distinct keys)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const bool m = kr[r] != 0ull && bin_of(vr[r]) == d;
         const unsigned bal = __ballot_sync(0xffffffffu, m);
         if (bal) {
             uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(s_above, (uint32_t)__popc(bal));
+            if (lane == 0) base = atomicAdd(s_ncand, (uint32_t)__popc(bal));
             base = __shfl_sync(0xffffffffu, base, 0);
             if (m) cand[base + __popc(bal & ((1u << lane) - 1u))] = kr[r];
         }
@@ -602,9 +605,8 @@ __device__ unsigned long long select_kth_key64_lin(const unsigned long long *key
         if (rank == need - 1u) s_red[0] = mine;
     }
     __syncthreads();
-    const unsigned long long t = s_red[0];
-    __syncthreads();
-    return t;
+    // s_red[0] holds the result until the caller's next barrier (the caller writes it no earlier)
+    return s_red[0];
 }
 
 // Warp 0: sum of vals[0..count) (shared memory) -> *out. Other warps skip.
@@ -1238,7 +1240,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(StepArgs a
         // exactly 512 published keys are >= t64
         t64 = n_slots <= 8 * kStepThreads
                   ? select_kth_key64_lin(ring64, (uint32_t)n_slots, kBlockTopK, hist, &s_d, &s_above, s_wsum, s_red,
-                                         s_fred)
+                                         s_fred, ring64 + n_slots, &s_n)
                   : select_kth_key64(ring64, (uint32_t)n_slots, kBlockTopK, hist, &s_d, &s_above, s_wsum, s_red,
                                      ring64 + n_slots, (uint32_t)(kRingBytes / 8 - n_slots), &s_n);
         STEP_TRACE(15);
