@@ -277,7 +277,7 @@ QSA_API qsa_status qsa_sparse_prefill_chunk_staged(const qsa_config *cfg, const 
  * rows: 2 (p0 + Nc) n_kv_heads x 512 bytes of device memory, 16-byte aligned), then
  * qsa_sparse_prefill_chunk runs on the staged rows: the results are bit-identical to running it
  * on the dequantised bf16 caches. Each element is thus code x scale rounded once to bf16 (at
- * most 2^-9 of its magnitude off the exact value) before the attention.
+ * most 2^-8 of its magnitude off the exact value) before the attention.
  *   k_codes, v_codes [p0 + Nc][n_kv_heads][256] uint8, 16-byte aligned; k_scales, v_scales
  *   [p0 + Nc][n_kv_heads][2] fp32, 8-byte aligned (device memory or mapped pinned host memory).
  * A stage shorter than needed -> QSA_ERR_WORKSPACE_TOO_SMALL; a NULL or misaligned stage or

@@ -703,6 +703,26 @@ def test_dequantize_kv_fp8_by_hand_and_error_bound():
     assert rel.max() <= 2.0 ** -4 * (1 + 1e-6) and rel.max() > 2.0 ** -4 * 0.9
 
 
+def test_fp8_kv_rows_rounded_to_bf16_for_the_prefill():
+    # the FP8 K/V prefill computes on code x scale rounded once to bf16 (the grader composes
+    # dequantize_kv_fp8 with f64_to_bf16_bits). With scale 1 (or any power of two) every E4M3
+    # value, at most 4 significant bits, is a bf16 value: the rounding is the identity
+    rng = np.random.default_rng(66)
+    codes = rng.integers(0, 256, (64, 256)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x00
+    for sc in (1.0, 2.0 ** -20, 2.0 ** 30):
+        x = O.dequantize_kv_fp8(codes, np.full((64, 2), sc, np.float32))
+        assert np.array_equal(O.bf16_bits_to_f64(O.f64_to_bf16_bits(x)), x)
+    # other scales: half a bf16 step at most, 2^-8 of the magnitude, reached within a few percent
+    scales = (2.0 ** rng.uniform(-20, 20, (64, 2))).astype(np.float32)
+    x = O.dequantize_kv_fp8(codes, scales)
+    r = O.bf16_bits_to_f64(O.f64_to_bf16_bits(x))
+    nz = x != 0
+    rel = np.abs(r - x)[nz] / np.abs(x)[nz]
+    assert rel.max() <= 2.0 ** -8 and rel.max() > 2.0 ** -8 * 0.9
+    assert np.array_equal(r == 0, x == 0)
+
+
 def test_decode_query_on_fp8_kv_closed_forms():
     # identical K rows: every attended token gets the same weight, so each head outputs the mean
     # of the dequantised V rows of its KV head over the attended tokens, and lse = logit + ln n
