@@ -704,7 +704,7 @@ def test_dequantize_kv_fp8_by_hand_and_error_bound():
 
 
 def test_fp8_kv_rows_rounded_to_bf16_for_the_prefill():
-    # the FP8 K/V prefill computes on code x scale rounded once to bf16 (the grader composes
+    # the FP8 K/V prefill computes on code x scale rounded once to bf16 (its parity tests compose
     # dequantize_kv_fp8 with f64_to_bf16_bits). With scale 1 (or any power of two) every E4M3
     # value, at most 4 significant bits, is a bf16 value: the rounding is the identity
     rng = np.random.default_rng(66)
